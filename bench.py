@@ -1,0 +1,371 @@
+"""Benchmark of the DSpark per-round hot path on one GB300.
+
+A step is one whole round -- Markov draft of gamma positions, confidence head,
+prefix scheduler, rejection-sampling verification -- over one batch of the
+synthetic workload (default: batch-128 engine point, B=128, gamma=16,
+V=151936).  The metric is verified draft tokens per second: the sum over
+requests of the scheduled verify lengths l_r, per round, divided by the round
+time.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                        [--impl gb300|reference]
+
+Prints one JSON line.  With N > 1 (torchrun) each rank runs an independent
+replica of the workload (the path shards over requests with no exchange), the
+timing is the max over ranks and `value` counts all ranks' tokens.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/s (B=128,γ=16,V=151936) on 1 GB300; % HBM roofline"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="batch128")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes of one round (each input byte counted once)
+# ---------------------------------------------------------------------------
+def round_bytes(w, ell_sum, n_reject):
+    sw = 2 if w.wdtype == torch.bfloat16 else 4
+    B, G, V, r, H = w.B, w.gamma, w.V, w.r, w.H
+    return (4 * B * G * V                 # U
+            + 4 * V * (ell_sum + B)       # target rows actually needed
+            + sw * r * V                  # W2 once
+            + sw * B * G * r              # W1 gathers
+            + sw * B * G * H              # h
+            + 4 * (H + r)                 # w
+            + 8 * V * n_reject            # residual U and T rows
+            + 16 * B * G + 8 * B)         # outputs
+
+
+def draft_bytes_per_position(w):
+    sw = 2 if w.wdtype == torch.bfloat16 else 4
+    return 4 * w.B * w.V + sw * w.r * w.V + sw * w.B * w.r + 12 * w.B
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during timing."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
+                                 f".clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def oracle_round_sample(w, inp_host, nreq, rnd=0):
+    """One oracle round over the first `nreq` requests as a batch of their own.
+    Returns (verified draft tokens, seconds, threads)."""
+    import oracle
+    h = inp_host
+    sub = {k: (v[:nreq] if k in ("U", "T", "h", "anchor") else v) for k, v in h.items()}
+    t0 = time.perf_counter()
+    d = oracle.draft(sub["U"], sub["W1"], sub["W2"], sub["anchor"], w.seed, rnd)
+    c = oracle.confidence(sub["h"], sub["W1"], sub["w"], sub["anchor"], d["x"])
+    if w.mode == 0:
+        ell = np.full(nreq, w.gamma, np.int32)
+    else:
+        b = np.arange(nreq * (w.gamma + 1) + 1, dtype=np.float64)
+        sps = (b / (1.0 + b / w.sps_b0)).astype(np.float32)
+        ell = oracle.schedule(c, sps, oracle.MODE_GREEDY)["ell"]
+    oracle.verify(sub["T"], sub["U"], sub["W1"], sub["W2"], sub["anchor"], d["x"], ell, w.seed, rnd)
+    dt = time.perf_counter() - t0
+    return int(ell.sum()), dt, oracle.num_threads()
+
+
+def host_sample(w, nreq, device):
+    from speculative_decoding_02_gb300 import workloads as wl
+    wsmall = w
+    weights = wl.make_weights(w, device)
+    rin = wl.make_round_inputs(w, 0, device)
+    d = {k: wl.to_numpy(v) for k, v in weights.items()}
+    for k in ("U", "T", "h"):
+        d[k] = wl.to_numpy(rin[k][:nreq])
+    d["anchor"] = d["anchor"][:nreq]
+    del rin
+    return wsmall, d
+
+
+def cpu_sample_size(w):
+    import oracle
+    return max(1, min(w.B, oracle.num_threads()))
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from speculative_decoding_02_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    nreq = cpu_sample_size(w)
+    _, hs = host_sample(w, nreq, "cpu")
+    for i in range(args.warmup):
+        oracle_round_sample(w, hs, nreq, rnd=i)
+    tot_tok, tot_t, thr = 0, 0.0, 1
+    for i in range(args.steps):
+        tok, dt, thr = oracle_round_sample(w, hs, nreq, rnd=args.warmup + i)
+        tot_tok += tok
+        tot_t += dt
+    value = tot_tok / tot_t
+    sample = f"{nreq} of {w.B} requests per step (full gamma={w.gamma}, V={w.V}), scheduled as their own batch"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "B": w.B, "gamma": w.gamma, "V": w.V},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import speculative_decoding_02_gb300 as ds
+    from speculative_decoding_02_gb300 import build as lib_build
+    from speculative_decoding_02_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        lib_build.build()
+    if world > 1:
+        dist.barrier()
+    ds.library()
+
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w, 0, dev)
+    khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == wl.MODE_TOPK else None
+    out = ds.RoundOutputs(w.B, w.gamma, dev)
+    ws = ds.workspace(w.B, w.gamma, w.V, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed,
+                 rnd=i, sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st = ds.read_status(ws)
+    if st != ds.OK:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        e0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # verified tokens of the timed rounds (deterministic per round index: replay)
+    ell_sum, n_acc, n_rej = 0, 0, 0
+    for i in range(args.steps):
+        step(args.warmup + i)
+        ell_sum += int(out.ell.sum())
+        n_acc += int(out.n.sum())
+        n_rej += int((out.n < out.ell).sum())
+    per_round = ell_sum / args.steps
+    value = world * ell_sum / (ms / 1e3)
+
+    # dominant kernel: the draft (gamma positions) timed alone on the same stream
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(3, args.steps // 2)
+    d0.record(stream)
+    for i in range(reps):
+        ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, i, ws=ws)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    draft_ms = d0.elapsed_time(d1) / reps
+    per_pos_s = draft_ms / 1e3 / w.gamma
+    hbm, bf16, peak_kind = peaks()
+    dbytes = draft_bytes_per_position(w)
+    achieved = dbytes / per_pos_s / 1e9
+
+    # end to end through host buffers: per-round inputs copied in, results out
+    e2e = None
+    if rank == 0:
+        e2e = run_e2e(w, inp, ds, dev, args, khist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nreq = cpu_sample_size(w)
+        _, hs = host_sample(w, nreq, dev)
+        tok, dt, thr = oracle_round_sample(w, hs, nreq)
+        cpu = {"value": tok / dt, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"one oracle round over {nreq} of {w.B} requests (full gamma, V), "
+                         f"{dt:.1f} s wall"}
+
+    if rank == 0:
+        rbytes = round_bytes(w, per_round, n_rej / args.steps)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32+bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "gamma": w.gamma, "V": w.V, "r": w.r, "H": w.H,
+                       "weights": "bf16" if w.wdtype == torch.bfloat16 else "f32",
+                       "l2": "inputs larger than L2 (U+T %.2f GB)" % ((4 * w.B * (2 * w.gamma + 1) * w.V) / 1e9),
+                       "verified_per_round": per_round, "accepted_per_round": n_acc / args.steps,
+                       "round_GB": rbytes / 1e9,
+                       "round_hbm_frac": rbytes / (ms / args.steps / 1e3) / 1e9 / hbm,
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"kernel": "markov draft, per position (draft step + finalize)", "bound": "hbm",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": None, "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": dbytes},
+            "clocks": clk.summary(),
+            "e2e": e2e,
+            "gpu_launches": args.steps * (2 * w.gamma + 7),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(w, inp, ds, dev, args, khist):
+    """Rounds through the public API with the per-round inputs in pinned host
+    memory: H2D of U, T, h, anchor and D2H of tokens, counts and lengths are
+    inside the timed region."""
+    names = ["U", "T", "h", "anchor"]
+    hostb = {k: inp[k].cpu().pin_memory() for k in names}
+    devb = {k: torch.empty_like(inp[k]) for k in names}
+    outs = ["x", "ell", "n", "tok"]
+    out = ds.RoundOutputs(w.B, w.gamma, dev)
+    hosto = {k: torch.empty(getattr(out, k).shape, dtype=getattr(out, k).dtype).pin_memory() for k in outs}
+    ws = ds.workspace(w.B, w.gamma, w.V, dev)
+    bi = sum(t.numel() * t.element_size() for t in hostb.values())
+    bo = sum(t.numel() * t.element_size() for t in hosto.values())
+    stream = torch.cuda.current_stream(dev)
+    steps = max(3, min(args.steps, 10))
+
+    def one(i):
+        for k in names:
+            devb[k].copy_(hostb[k], non_blocking=True)
+        ds.round(devb["U"], devb["T"], inp["W1"], inp["W2"], devb["h"], inp["w"], devb["anchor"], seed=w.seed,
+                 rnd=i, sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws)
+        for k in outs:
+            hosto[k].copy_(getattr(out, k), non_blocking=True)
+
+    one(0)
+    torch.cuda.synchronize()
+    ell_sum = 0
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        one(i)
+        stream.synchronize()
+        ell_sum += int(hosto["ell"].sum())
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    del hostb, devb
+    return {"value": ell_sum / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "steps": steps, "wall_s": time.perf_counter() - t0}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

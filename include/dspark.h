@@ -1,0 +1,171 @@
+/*
+ * dspark.h -- C ABI of libdspark, the GB300 (sm_103a) per-round hot path of
+ * DSpark speculative decoding: semi-autoregressive Markov-head draft sampling,
+ * the confidence head, the confidence-scheduled prefix truncation and lossless
+ * rejection-sampling verification.
+ *
+ * Sources, cited by page title and section:
+ *   [blog]   "[DeepSeek-6] DSpark: From Draft Models to Serving-Aware Speculative
+ *             Decoding" (xutianle.me), sections 1, 3-7.
+ *   [digest] "DSpark ... 10 key concepts" (aimsg.uk), items 2, 8, 9.
+ *   [report] "DSpark: Confidence-Scheduled Speculative Decoding with
+ *             Semi-Autoregressive Generation -- study report" (devpress.csdn),
+ *             Key formulas Eq.4, Eq.7, Eq.8 and Theta = tau * SPS(B).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers of the current CUDA device, row-major
+ *    and densely packed.  The caller owns every buffer; the library never
+ *    allocates device memory.  Scratch space is the caller's `workspace` of at
+ *    least dspark_workspace_size(B, gamma, V) bytes, 256-byte aligned; one
+ *    workspace must not be used by two calls that run concurrently.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only
+ *    enqueue work and never synchronise, except dspark_read_status.
+ *  - Shapes: B requests, gamma draft positions (1..32), V vocabulary entries
+ *    (V % 8 == 0), r Markov rank (r % 16 == 0, 16..256), H hidden size.
+ *    Position k = 1..gamma is row k-1 of the per-position tensors.
+ *  - Weights: W1 [V, r] is the Markov embedding of the previous token; W2 [V, r]
+ *    is the weight of the bias-free linear layer r -> V as a linear layer stores
+ *    it, so the Markov bias of entry v is sum_i W1[prev, i] * W2[v, i]
+ *    ([blog] section 4).  wdtype is DSPARK_BF16 or DSPARK_F32 for both.
+ *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by `seed`, with
+ *    counter (v / 4, position k, request b, (round << 3) | stream), word v % 4;
+ *    uniform u = ((w >> 9) + 1/2) / 2^23; Gumbel noise -log(-log u).  Streams:
+ *    0 draft, 1 accept test (v = 0), 2 residual, 3 bonus.  `round` < 2^29.
+ *  - Return value: a DSPARK_* status.  Argument errors are detected on the host
+ *    before anything is enqueued.  Errors found by the kernels (a bounded wait
+ *    that gave up, non-finite logits) are recorded in a status word inside the
+ *    workspace and read with dspark_read_status.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define DSPARK_OK 0
+#define DSPARK_ERR_INVALID 1      /* null pointer, bad size, table too short */
+#define DSPARK_ERR_UNSUPPORTED 2  /* a size outside the supported range */
+#define DSPARK_ERR_CUDA 3         /* a CUDA launch or runtime call failed */
+#define DSPARK_ERR_TIMEOUT 4      /* a device-side bounded wait gave up */
+#define DSPARK_ERR_WORKSPACE 5    /* workspace too small or misaligned */
+#define DSPARK_ERR_NONFINITE 6    /* a NaN or infinite logit was met */
+
+/* storage types */
+#define DSPARK_F32 0
+#define DSPARK_BF16 1
+
+/* scheduler modes */
+#define DSPARK_SCHED_FIXED 0   /* no truncation: l_r = gamma */
+#define DSPARK_SCHED_GREEDY 1  /* greedy Theta maximisation with early stop */
+#define DSPARK_SCHED_TOPK 2    /* dynamic top-K, K = greedy count of round - 2 */
+
+/* Bytes of device scratch the entry points below need for these sizes. */
+size_t dspark_workspace_size(int B, int gamma, int V);
+
+/*
+ * Semi-autoregressive Markov draft ([report] Eq.4; [blog] sections 3-4).
+ * For k = 1..gamma (x_0 = anchor, [blog] section 3):
+ *   l_k(v) = U[b, k-1, v] + sum_i W1[x_{k-1}, i] * W2[v, i]
+ *   x_k    = argmax_v l_k(v) + Gumbel(seed, round, stream 0, b, k, v)
+ *   lse_k  = log sum_v exp l_k(v);   p_k(x_k) = exp(l_k(x_k) - lse_k)
+ * In:  U [B, gamma, V] f32, W1/W2 [V, r] (wdtype), anchor [B] i32 in [0, V).
+ * Out: x_out [B, gamma] i32, p_out [B, gamma] f32, lse_out [B, gamma] f32.
+ * Ties of the perturbed logit go to the smallest v.
+ */
+int dspark_markov_draft(const float* U, const void* W1, const void* W2, int wdtype,
+                        const int32_t* anchor, int B, int gamma, int V, int r,
+                        uint64_t seed, uint64_t round,
+                        int32_t* x_out, float* p_out, float* lse_out,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Confidence head ([report] Eq.7; [blog] section 5):
+ *   c_k = sigmoid( (sum_i w[i] h[b,k-1,i] + sum_i w[H+i] W1[x_{k-1}, i]) / T_k )
+ * with x_0 = anchor and T_k = sts_T[k-1] (Sequential Temperature Scaling,
+ * [blog] section 5), or 1 when sts_T is NULL.  No bias term (Eq.7 has none).
+ * In:  h [B, gamma, H] (hdtype), W1 [V, r] (wdtype), w [H + r] f32,
+ *      sts_T [gamma] f32 or NULL, anchor [B], x [B, gamma] i32.
+ * Out: c_out [B, gamma] f32.
+ */
+int dspark_confidence(const void* h, int hdtype, const void* W1, int wdtype,
+                      const float* w, const float* sts_T, const int32_t* anchor,
+                      const int32_t* x, int B, int gamma, int H, int r, int V,
+                      float* c_out, void* stream);
+
+/*
+ * Hardware-aware prefix scheduler ([blog] sections 6-7; [report] Theta).
+ *   a_{b,j} = prod_{i<=j} c_{b,i};  B' = sum_b (l_b + 1);
+ *   tau = sum_b (1 + sum_{j<=l_b} a_{b,j});  Theta = tau * SPS(B').
+ * Candidates (b, j) are ordered by a desc, then b asc, then j asc.
+ * GREEDY: admit in that order while Theta strictly rises; the first candidate
+ *   that does not raise it stops the scan (non-anticipating, [blog] section 7).
+ * TOPK:   admit exactly the first K candidates, K = khist[round % 2], the greedy
+ *   count this call wrote two rounds earlier ([blog] section 7); rounds 0 and 1
+ *   run the greedy.  Every mode writes this round's greedy count to
+ *   khist[round % 2] after reading it (khist: device [2] i32, caller-owned).
+ * FIXED:  l_b = gamma.
+ * In:  c [B, gamma] f32 in [0, 1]; sps [n_sps] f32 indexed by batch size,
+ *      n_sps > B * (gamma + 1) (not read in FIXED mode).  B * gamma <= 8192.
+ * Out: ell_out [B] i32, nstar_out [1] i32 (greedy count), theta_out [1] f64
+ *      (Theta of the admitted set; 0 in FIXED mode).
+ */
+int dspark_schedule(const float* c, int B, int gamma, const float* sps, int n_sps,
+                    int mode, uint64_t round, int32_t* khist,
+                    int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Lossless rejection-sampling verification ([digest] item 2; [blog] section 1).
+ * For request b and k = 1..ell[b]: p_t = softmax(T[b, k-1, :]); accept x_k
+ * while u < p_t(x_k) / p_d(x_k), u = uniform(stream 1, b, k).  At the first
+ * rejection the corrected token is drawn from normalize(max(0, p_t - p_d)) by
+ * Gumbel-max over its logarithm (stream 2, b, k), p_d = softmax(U[b,k-1,:] +
+ * bias(x_{k-1})) recomputed from lse_d; if that residual is empty in floating
+ * point, from p_t with the same noise.  If all ell[b] tokens are accepted, the
+ * bonus token is drawn from softmax(T[b, ell[b], :]) (stream 3, k = ell[b]+1).
+ * In:  T [B, gamma+1, V] f32 (row k-1 scores position k); U, W1, W2, anchor as
+ *      for the draft; x, p_d, lse_d [B, gamma] from the draft; ell [B] i32 in
+ *      [0, gamma].  Only rows 0..ell[b] of T are read.
+ * Out: n_out [B] i32 accepted count; tok_out [B] i32 corrected or bonus token.
+ */
+int dspark_verify(const float* T, const float* U, const void* W1, const void* W2,
+                  int wdtype, const int32_t* anchor, const int32_t* x,
+                  const float* p_d, const float* lse_d, const int32_t* ell,
+                  int B, int gamma, int V, int r, uint64_t seed, uint64_t round,
+                  int32_t* n_out, int32_t* tok_out,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One whole round: draft, confidence, schedule, verify, enqueued in that order
+ * on one stream with no host synchronisation.  Arguments as above.
+ */
+int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
+                 int wdtype, const void* h, int hdtype, const float* w,
+                 const float* sts_T, const int32_t* anchor,
+                 int B, int gamma, int V, int r, int H,
+                 const float* sps, int n_sps, int mode, int32_t* khist,
+                 uint64_t seed, uint64_t round,
+                 int32_t* x_out, float* p_out, float* lse_out, float* c_out,
+                 int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                 int32_t* n_out, int32_t* tok_out,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Waits for `stream`, then copies the workspace status word (a DSPARK_* code,
+ * the first error any kernel recorded since the last clear) to *host_status and
+ * clears it.  Returns DSPARK_OK or DSPARK_ERR_CUDA. */
+int dspark_read_status(void* workspace, int* host_status, void* stream);
+
+/* Static text for a status code. */
+const char* dspark_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

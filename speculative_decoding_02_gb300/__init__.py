@@ -1,0 +1,262 @@
+"""Python binding of libdspark, the GB300 (sm_103a) DSpark per-round hot path.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors must be contiguous CUDA tensors on one device; outputs are
+allocated with torch on that device and every call is enqueued on the current
+torch stream.  If the compiled library is missing, every call raises
+``DSparkError`` -- there is no CPU fallback.
+
+Entry points (same names as the C ABI in include/dspark.h):
+  markov_draft, confidence, schedule, verify, round, read_status
+"""
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libdspark.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NONFINITE = range(7)
+F32, BF16 = 0, 1
+SCHED_FIXED, SCHED_GREEDY, SCHED_TOPK = 0, 1, 2
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, code, where=""):
+        self.code = code
+        msg = _strerror(code) if _lib is not None else f"status {code}"
+        super().__init__(f"{where}: {msg} (status {code})" if where else msg)
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise DSparkError(ERR_CUDA, f"libdspark is not built ({LIB_PATH} missing); run "
+                                    f"`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+    L.dspark_workspace_size.argtypes = [i32, i32, i32]
+    L.dspark_workspace_size.restype = sz
+    L.dspark_markov_draft.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, sz, vp]
+    L.dspark_markov_draft.restype = i32
+    L.dspark_confidence.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+    L.dspark_confidence.restype = i32
+    L.dspark_schedule.argtypes = [vp, i32, i32, vp, i32, i32, u64, vp, vp, vp, vp, vp, sz, vp]
+    L.dspark_schedule.restype = i32
+    L.dspark_verify.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp,
+                                vp, sz, vp]
+    L.dspark_verify.restype = i32
+    L.dspark_round.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
+                               vp, u64, u64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.dspark_round.restype = i32
+    L.dspark_read_status.argtypes = [vp, ctypes.POINTER(i32), vp]
+    L.dspark_read_status.restype = i32
+    L.dspark_strerror.argtypes = [i32]
+    L.dspark_strerror.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _strerror(code):
+    return _lib.dspark_strerror(int(code)).decode()
+
+
+def library():
+    """The loaded ctypes library (raises DSparkError if it is not built)."""
+    return _load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(code, where):
+    if code != OK:
+        raise DSparkError(code, where)
+
+
+def _dt(t, what):
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"{what} must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need(t, what, dtype=None, device=None):
+    if t is None:
+        raise ValueError(f"{what} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{what} is on {t.device}, expected {device}")
+    return t
+
+
+_ws_cache = {}
+
+
+def workspace_size(B, gamma, V):
+    return int(_load().dspark_workspace_size(B, gamma, V))
+
+
+def workspace(B, gamma, V, device):
+    """A cached, 256-byte aligned device workspace for these sizes."""
+    n = workspace_size(B, gamma, V)
+    key = (torch.device(device), n)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def markov_draft(U, W1, W2, anchor, seed, rnd=0, ws=None):
+    """x [B,G] i32, p [B,G] f32, lse [B,G] f32 = the Markov draft of one round."""
+    L = _load()
+    _need(U, "U", torch.float32)
+    dev = U.device
+    B, G, V = U.shape
+    _need(W1, "W1", device=dev); _need(W2, "W2", W1.dtype, dev); _need(anchor, "anchor", torch.int32, dev)
+    r = W1.shape[1]
+    x = torch.empty((B, G), dtype=torch.int32, device=dev)
+    p = torch.empty((B, G), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, G), dtype=torch.float32, device=dev)
+    ws = workspace(B, G, V, dev) if ws is None else ws
+    _check(L.dspark_markov_draft(_ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), B, G, V, r, seed, rnd,
+                                 _ptr(x), _ptr(p), _ptr(lse), _ptr(ws), ws.numel(), _stream(dev)), "markov_draft")
+    return x, p, lse
+
+
+def confidence(h, W1, w, anchor, x, sts_T=None):
+    """c [B,G] f32 = sigmoid(w . [h_k ; W1[x_{k-1}]] / T_k)."""
+    L = _load()
+    _need(h, "h")
+    dev = h.device
+    B, G, H = h.shape
+    _need(W1, "W1", device=dev); _need(w, "w", torch.float32, dev)
+    _need(anchor, "anchor", torch.int32, dev); _need(x, "x", torch.int32, dev)
+    if sts_T is not None:
+        _need(sts_T, "sts_T", torch.float32, dev)
+    V, r = W1.shape
+    c = torch.empty((B, G), dtype=torch.float32, device=dev)
+    _check(L.dspark_confidence(_ptr(h), _dt(h, "h"), _ptr(W1), _dt(W1, "W1"), _ptr(w), _ptr(sts_T), _ptr(anchor),
+                               _ptr(x), B, G, H, r, V, _ptr(c), _stream(dev)), "confidence")
+    return c
+
+
+def schedule(c, sps=None, mode=SCHED_GREEDY, rnd=0, khist=None, ws=None):
+    """ell [B] i32, nstar [1] i32, theta [1] f64 from confidences c [B,G]."""
+    L = _load()
+    _need(c, "c", torch.float32)
+    dev = c.device
+    B, G = c.shape
+    if sps is not None:
+        _need(sps, "sps", torch.float32, dev)
+    if khist is not None:
+        _need(khist, "khist", torch.int32, dev)
+    ell = torch.empty(B, dtype=torch.int32, device=dev)
+    nstar = torch.empty(1, dtype=torch.int32, device=dev)
+    theta = torch.empty(1, dtype=torch.float64, device=dev)
+    ws = workspace(B, G, 8, dev) if ws is None else ws
+    n_sps = 0 if sps is None else sps.numel()
+    _check(L.dspark_schedule(_ptr(c), B, G, _ptr(sps), n_sps, mode, rnd, _ptr(khist), _ptr(ell), _ptr(nstar),
+                             _ptr(theta), _ptr(ws), ws.numel(), _stream(dev)), "schedule")
+    return ell, nstar, theta
+
+
+def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None):
+    """n [B] i32 accepted counts, tok [B] i32 corrected / bonus tokens."""
+    L = _load()
+    _need(T, "T", torch.float32)
+    dev = T.device
+    _need(U, "U", torch.float32, dev)
+    B, G, V = U.shape
+    if tuple(T.shape) != (B, G + 1, V):
+        raise ValueError(f"T must be [B, gamma+1, V] = {(B, G + 1, V)}, got {tuple(T.shape)}")
+    _need(W1, "W1", device=dev); _need(W2, "W2", W1.dtype, dev)
+    for t, n in [(anchor, "anchor"), (x, "x"), (ell, "ell")]:
+        _need(t, n, torch.int32, dev)
+    _need(p_d, "p_d", torch.float32, dev); _need(lse_d, "lse_d", torch.float32, dev)
+    r = W1.shape[1]
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = workspace(B, G, V, dev) if ws is None else ws
+    _check(L.dspark_verify(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x), _ptr(p_d),
+                           _ptr(lse_d), _ptr(ell), B, G, V, r, seed, rnd, _ptr(n), _ptr(tok), _ptr(ws), ws.numel(),
+                           _stream(dev)), "verify")
+    return n, tok
+
+
+class RoundOutputs:
+    """Device output buffers of one round (reused across rounds)."""
+
+    def __init__(self, B, G, device):
+        i32, f32 = torch.int32, torch.float32
+        self.x = torch.empty((B, G), dtype=i32, device=device)
+        self.p = torch.empty((B, G), dtype=f32, device=device)
+        self.lse = torch.empty((B, G), dtype=f32, device=device)
+        self.c = torch.empty((B, G), dtype=f32, device=device)
+        self.ell = torch.empty(B, dtype=i32, device=device)
+        self.nstar = torch.empty(1, dtype=i32, device=device)
+        self.theta = torch.empty(1, dtype=torch.float64, device=device)
+        self.n = torch.empty(B, dtype=i32, device=device)
+        self.tok = torch.empty(B, dtype=i32, device=device)
+
+    def as_dict(self):
+        return dict(x=self.x, p=self.p, lse=self.lse, c=self.c, ell=self.ell, nstar=self.nstar,
+                    theta=self.theta, n=self.n, tok=self.tok)
+
+
+def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
+          out=None, ws=None):
+    """One whole round (draft, confidence, schedule, verify) on U's device.
+    Returns a RoundOutputs (device tensors)."""
+    L = _load()
+    _need(U, "U", torch.float32)
+    dev = U.device
+    B, G, V = U.shape
+    _need(T, "T", torch.float32, dev)
+    if tuple(T.shape) != (B, G + 1, V):
+        raise ValueError(f"T must be [B, gamma+1, V] = {(B, G + 1, V)}, got {tuple(T.shape)}")
+    _need(W1, "W1", device=dev); _need(W2, "W2", W1.dtype, dev); _need(h, "h", device=dev)
+    _need(w, "w", torch.float32, dev); _need(anchor, "anchor", torch.int32, dev)
+    if sps is not None:
+        _need(sps, "sps", torch.float32, dev)
+    if khist is not None:
+        _need(khist, "khist", torch.int32, dev)
+    if sts_T is not None:
+        _need(sts_T, "sts_T", torch.float32, dev)
+    r, H = W1.shape[1], h.shape[2]
+    out = RoundOutputs(B, G, dev) if out is None else out
+    ws = workspace(B, G, V, dev) if ws is None else ws
+    n_sps = 0 if sps is None else sps.numel()
+    _check(L.dspark_round(_ptr(U), _ptr(T), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h), _dt(h, "h"), _ptr(w),
+                          _ptr(sts_T), _ptr(anchor), B, G, V, r, H, _ptr(sps), n_sps, mode, _ptr(khist), seed, rnd,
+                          _ptr(out.x), _ptr(out.p), _ptr(out.lse), _ptr(out.c), _ptr(out.ell), _ptr(out.nstar),
+                          _ptr(out.theta), _ptr(out.n), _ptr(out.tok), _ptr(ws), ws.numel(), _stream(dev)), "round")
+    return out
+
+
+def read_status(ws, device=None):
+    """Synchronise the current stream and return (and clear) the status word."""
+    L = _load()
+    st = ctypes.c_int(0)
+    dev = ws.device if device is None else device
+    _check(L.dspark_read_status(_ptr(ws), ctypes.byref(st), _stream(dev)), "read_status")
+    return int(st.value)

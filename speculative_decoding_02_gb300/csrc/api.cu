@@ -1,0 +1,192 @@
+// The C ABI of libdspark: host-side argument checks, workspace checks and the
+// enqueueing of the per-round kernels.  Every entry point validates its sizes
+// and pointers before it enqueues anything and never synchronises the stream.
+#include <stdint.h>
+
+#include "kernels.h"
+
+using namespace dspark;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_dtype(int dt) { return (dt == DSPARK_F32 || dt == DSPARK_BF16) ? DSPARK_OK : DSPARK_ERR_INVALID; }
+
+// Shapes shared by the draft and verify calls.
+int check_shapes(int B, int gamma, int V, int r) {
+  if (B <= 0 || gamma <= 0 || V <= 0 || r <= 0) return DSPARK_ERR_INVALID;
+  if (gamma > kMaxGamma) return DSPARK_ERR_UNSUPPORTED;
+  if (V % 8 != 0 || r % 16 != 0 || r > 256) return DSPARK_ERR_UNSUPPORTED;
+  if (B > 65535) return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)B * (gamma + 1) * (long long)V >= (1ll << 40)) return DSPARK_ERR_UNSUPPORTED;
+  return DSPARK_OK;
+}
+
+int check_ws(void* ws, size_t ws_bytes, int B, int gamma, int V) {
+  if (!ws || !aligned(ws, 256)) return DSPARK_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_WORKSPACE;
+  return DSPARK_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA; }
+
+#define DSPARK_TRY(expr)            \
+  do {                              \
+    const int _st = (expr);         \
+    if (_st != DSPARK_OK) return _st; \
+  } while (0)
+
+int draft_checks(const float* U, const void* W1, const void* W2, int wdtype, const int32_t* anchor, int B,
+                 int gamma, int V, int r, int32_t* x_out, float* p_out, float* lse_out, void* ws,
+                 size_t ws_bytes) {
+  DSPARK_TRY(check_shapes(B, gamma, V, r));
+  DSPARK_TRY(check_dtype(wdtype));
+  if (!U || !W1 || !W2 || !anchor || !x_out || !p_out || !lse_out) return DSPARK_ERR_INVALID;
+  if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16)) return DSPARK_ERR_INVALID;
+  return check_ws(ws, ws_bytes, B, gamma, V);
+}
+
+int confidence_checks(const void* h, int hdtype, const void* W1, int wdtype, const float* w,
+                      const int32_t* anchor, const int32_t* x, int B, int gamma, int H, int r, int V,
+                      float* c_out) {
+  DSPARK_TRY(check_dtype(hdtype));
+  DSPARK_TRY(check_dtype(wdtype));
+  if (B <= 0 || gamma <= 0 || H < 0 || r <= 0 || V <= 0) return DSPARK_ERR_INVALID;
+  if (gamma > kMaxGamma) return DSPARK_ERR_UNSUPPORTED;
+  if ((H > 0 && !h) || !W1 || !w || !anchor || !x || !c_out) return DSPARK_ERR_INVALID;
+  return DSPARK_OK;
+}
+
+int schedule_checks(const float* c, int B, int gamma, const float* sps, int n_sps, int mode,
+                    const int32_t* khist, const int32_t* ell_out, const int32_t* nstar_out,
+                    const double* theta_out) {
+  if (B <= 0 || gamma <= 0) return DSPARK_ERR_INVALID;
+  if (gamma > kMaxGamma || (long long)B * gamma > kMaxCandidates) return DSPARK_ERR_UNSUPPORTED;
+  if (mode < DSPARK_SCHED_FIXED || mode > DSPARK_SCHED_TOPK) return DSPARK_ERR_INVALID;
+  if (!c || !ell_out || !nstar_out || !theta_out) return DSPARK_ERR_INVALID;
+  if (mode != DSPARK_SCHED_FIXED && (!sps || (long long)n_sps <= (long long)B * (gamma + 1)))
+    return DSPARK_ERR_INVALID;
+  if (mode == DSPARK_SCHED_TOPK && !khist) return DSPARK_ERR_INVALID;
+  return DSPARK_OK;
+}
+
+int verify_checks(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
+                  const int32_t* anchor, const int32_t* x, const float* p_d, const float* lse_d,
+                  const int32_t* ell, int B, int gamma, int V, int r, int32_t* n_out, int32_t* tok_out,
+                  void* ws, size_t ws_bytes) {
+  DSPARK_TRY(check_shapes(B, gamma, V, r));
+  DSPARK_TRY(check_dtype(wdtype));
+  if (!T || !U || !W1 || !W2 || !anchor || !x || !p_d || !lse_d || !ell || !n_out || !tok_out)
+    return DSPARK_ERR_INVALID;
+  if (!aligned(T, 16) || !aligned(U, 16)) return DSPARK_ERR_INVALID;
+  return check_ws(ws, ws_bytes, B, gamma, V);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dspark_workspace_size(int B, int gamma, int V) {
+  if (B <= 0 || gamma <= 0 || V <= 0) return 0;
+  return ws_layout(B, gamma, V).total;
+}
+
+int dspark_markov_draft(const float* U, const void* W1, const void* W2, int wdtype, const int32_t* anchor,
+                        int B, int gamma, int V, int r, uint64_t seed, uint64_t round, int32_t* x_out,
+                        float* p_out, float* lse_out, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
+                          workspace_bytes));
+  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
+  DraftArgs a{U, W1, W2, wdtype, anchor, B, gamma, V, r, make_rng_key(seed, round), x_out, p_out, lse_out,
+              workspace};
+  return cuda_status(launch_markov_draft(a, (cudaStream_t)stream));
+}
+
+int dspark_confidence(const void* h, int hdtype, const void* W1, int wdtype, const float* w,
+                      const float* sts_T, const int32_t* anchor, const int32_t* x, int B, int gamma, int H,
+                      int r, int V, float* c_out, void* stream) {
+  DSPARK_TRY(confidence_checks(h, hdtype, W1, wdtype, w, anchor, x, B, gamma, H, r, V, c_out));
+  // The confidence call has no workspace: its kernel reports range errors by
+  // writing 0 confidences; the status word is only used by the round entry.
+  return cuda_status(launch_confidence(h, hdtype, W1, wdtype, w, sts_T, anchor, x, B, gamma, H, r, V, c_out,
+                                       nullptr, (cudaStream_t)stream));
+}
+
+int dspark_schedule(const float* c, int B, int gamma, const float* sps, int n_sps, int mode, uint64_t round,
+                    int32_t* khist, int32_t* ell_out, int32_t* nstar_out, double* theta_out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  DSPARK_TRY(schedule_checks(c, B, gamma, sps, n_sps, mode, khist, ell_out, nstar_out, theta_out));
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_WORKSPACE;
+  int* status = ws_ptr<int>(workspace, 0);
+  return cuda_status(launch_schedule(c, B, gamma, sps, mode, (uint32_t)(round & 0xffffffffu), round >= 2 ? 1 : 0,
+                                     khist, ell_out, nstar_out, theta_out, status, (cudaStream_t)stream));
+}
+
+int dspark_verify(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
+                  const int32_t* anchor, const int32_t* x, const float* p_d, const float* lse_d,
+                  const int32_t* ell, int B, int gamma, int V, int r, uint64_t seed, uint64_t round,
+                  int32_t* n_out, int32_t* tok_out, void* workspace, size_t workspace_bytes, void* stream) {
+  DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, n_out, tok_out,
+                           workspace, workspace_bytes));
+  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
+  VerifyArgs a{T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, make_rng_key(seed, round),
+               n_out, tok_out, workspace};
+  return cuda_status(launch_verify(a, (cudaStream_t)stream));
+}
+
+int dspark_round(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,
+                 int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B, int gamma, int V,
+                 int r, int H, const float* sps, int n_sps, int mode, int32_t* khist, uint64_t seed,
+                 uint64_t round, int32_t* x_out, float* p_out, float* lse_out, float* c_out, int32_t* ell_out,
+                 int32_t* nstar_out, double* theta_out, int32_t* n_out, int32_t* tok_out, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
+                          workspace_bytes));
+  DSPARK_TRY(confidence_checks(h, hdtype, W1, wdtype, w, anchor, x_out, B, gamma, H, r, V, c_out));
+  DSPARK_TRY(schedule_checks(c_out, B, gamma, sps, n_sps, mode, khist, ell_out, nstar_out, theta_out));
+  DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, n_out,
+                           tok_out, workspace, workspace_bytes));
+  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
+  cudaStream_t s = (cudaStream_t)stream;
+  const RngKey key = make_rng_key(seed, round);
+  int* status = ws_ptr<int>(workspace, ws_layout(B, gamma, V).status);
+  DraftArgs da{U, W1, W2, wdtype, anchor, B, gamma, V, r, key, x_out, p_out, lse_out, workspace};
+  DSPARK_TRY(cuda_status(launch_markov_draft(da, s)));
+  DSPARK_TRY(cuda_status(launch_confidence(h, hdtype, W1, wdtype, w, sts_T, anchor, x_out, B, gamma, H, r, V,
+                                           c_out, status, s)));
+  DSPARK_TRY(cuda_status(launch_schedule(c_out, B, gamma, sps, mode, (uint32_t)(round & 0xffffffffu),
+                                         round >= 2 ? 1 : 0, khist, ell_out, nstar_out, theta_out, status, s)));
+  VerifyArgs va{T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, key, n_out,
+                tok_out, workspace};
+  return cuda_status(launch_verify(va, s));
+}
+
+int dspark_read_status(void* workspace, int* host_status, void* stream) {
+  if (!workspace || !host_status) return DSPARK_ERR_INVALID;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* status = ws_ptr<int>(workspace, 0);
+  int value = 0;
+  if (cudaMemcpyAsync(&value, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  *host_status = value;
+  return DSPARK_OK;
+}
+
+const char* dspark_strerror(int status) {
+  switch (status) {
+    case DSPARK_OK: return "ok";
+    case DSPARK_ERR_INVALID: return "invalid argument (null pointer, size or table length)";
+    case DSPARK_ERR_UNSUPPORTED: return "unsupported size (gamma > 32, V % 8, r % 16 or r > 256, B*gamma > 8192)";
+    case DSPARK_ERR_CUDA: return "a CUDA launch or runtime call failed";
+    case DSPARK_ERR_TIMEOUT: return "a device-side bounded wait gave up";
+    case DSPARK_ERR_WORKSPACE: return "workspace missing, misaligned (256 B) or smaller than dspark_workspace_size";
+    case DSPARK_ERR_NONFINITE: return "a NaN or infinite logit or confidence was met";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,192 @@
+// Device-side helpers shared by the libdspark kernels: the counter-based
+// generator, the uniform / Gumbel maps, argmax keys, status reporting and the
+// workspace layout.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+// as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplications whose high
+// halves are xored with the other two words and the round key; the key walks a
+// Weyl sequence.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kPhiloxMulA = 0xD2511F53u;
+constexpr uint32_t kPhiloxMulB = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxWeylA = 0x9E3779B9u;
+constexpr uint32_t kPhiloxWeylB = 0xBB67AE85u;
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo_a = kPhiloxMulA * c.x;
+    const uint32_t hi_a = __umulhi(kPhiloxMulA, c.x);
+    const uint32_t lo_b = kPhiloxMulB * c.z;
+    const uint32_t hi_b = __umulhi(kPhiloxMulB, c.z);
+    c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
+    k0 += kPhiloxWeylA;
+    k1 += kPhiloxWeylB;
+  }
+  return c;
+}
+
+// Random-number streams of one round (the fourth counter word is
+// (round << 3) | stream).
+enum Stream : uint32_t { kStreamDraft = 0, kStreamAccept = 1, kStreamResidual = 2, kStreamBonus = 3 };
+
+struct RngKey {
+  uint32_t k0, k1;   // seed low / high word
+  uint32_t round3;   // round << 3
+};
+
+__host__ __device__ inline RngKey make_rng_key(uint64_t seed, uint64_t round) {
+  RngKey k;
+  k.k0 = (uint32_t)(seed & 0xffffffffu);
+  k.k1 = (uint32_t)(seed >> 32);
+  k.round3 = (uint32_t)(round << 3);
+  return k;
+}
+
+// The four words for vocabulary entries 4q .. 4q+3 of (stream, request, position).
+__device__ __forceinline__ uint4 rng4(const RngKey& key, uint32_t stream, uint32_t req,
+                                      uint32_t pos, uint32_t q) {
+  return philox4x32_10(make_uint4(q, pos, req, key.round3 | stream), key.k0, key.k1);
+}
+
+// Uniform (2m + 1) / 2^24 with m the top 23 bits of w: exact in float32.
+__device__ __forceinline__ float uniform01(uint32_t w) {
+  return __uint2float_rn(w >> 9) * 0x1p-23f + 0x1p-24f;
+}
+
+// Standard Gumbel variate by inversion.  The inner logarithm uses the
+// full-accuracy logf: near u = 1 its result is tiny and a fast approximation
+// with absolute error would distort the largest noise values.
+__device__ __forceinline__ float gumbel_noise(uint32_t w) {
+  return -logf(-logf(uniform01(w)));
+}
+
+// ---------------------------------------------------------------------------
+// Argmax keys: a 64-bit integer whose order is (value asc, index desc), so
+// atomicMax picks the largest value and, on exact ties, the smallest index.
+// 0 means "no candidate".
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long argmax_key(float z, int v) {
+  uint32_t b = __float_as_uint(z);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)b << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)v);
+}
+__device__ __forceinline__ int argmax_key_index(unsigned long long key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+}
+__device__ __forceinline__ float argmax_key_value(unsigned long long key) {
+  uint32_t b = (uint32_t)(key >> 32);
+  b = (b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b;
+  return __uint_as_float(b);
+}
+
+// ---------------------------------------------------------------------------
+// Online softmax state: running max m and sum s of exp(l - m).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void softmax_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) { m = m2; s = s2; return; }
+  if (m2 > m) { s = s * expf(m - m2) + s2; m = m2; }
+  else { s = s + s2 * expf(m2 - m); }
+}
+
+__device__ __forceinline__ void warp_softmax_reduce(float& m, float& s, unsigned mask, int width) {
+  for (int off = width / 2; off > 0; off >>= 1) {
+    float m2 = __shfl_xor_sync(mask, m, off, width);
+    float s2 = __shfl_xor_sync(mask, s, off, width);
+    softmax_merge(m, s, m2, s2);
+  }
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k, unsigned mask, int width) {
+  for (int off = width / 2; off > 0; off >>= 1) {
+    unsigned long long o = __shfl_xor_sync(mask, k, off, width);
+    k = o > k ? o : k;
+  }
+  return k;
+}
+
+// First error wins; later errors do not overwrite it.
+__device__ __forceinline__ void record_status(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+// A token id read from memory, checked before it indexes a [V, r] table: an id
+// outside [0, V) records DSPARK_ERR_INVALID and is replaced by 0.
+__device__ __forceinline__ int checked_token(int t, int V, int* status) {
+  if (t < 0 || t >= V) {
+    if (status) record_status(status, DSPARK_ERR_INVALID);
+    return 0;
+  }
+  return t;
+}
+
+template <int WDT>
+__device__ __forceinline__ float load_weight(const void* base, size_t idx) {
+  if (WDT == DSPARK_F32) return static_cast<const float*>(base)[idx];
+  const uint16_t bits = static_cast<const uint16_t*>(base)[idx];
+  return __uint_as_float(((uint32_t)bits) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// Tiling constants and the workspace layout (shared by host and device code).
+// ---------------------------------------------------------------------------
+constexpr int kDraftSlice = 1024;   // vocabulary columns per draft CTA (CUDA-core path)
+constexpr int kVerifySeg = 8192;    // vocabulary entries per verify task
+constexpr int kMaxGamma = 32;
+constexpr int kMaxCandidates = 8192;
+
+__host__ __device__ inline int div_up(int a, int b) { return (a + b - 1) / b; }
+
+__host__ __device__ inline int draft_num_slices(int V) { return div_up(V, kDraftSlice); }
+__host__ __device__ inline int verify_num_segs(int V) { return div_up(V, kVerifySeg); }
+
+struct WsLayout {
+  size_t status;      // int32 status word
+  size_t counters;    // int32 [8]: [0] verify row count
+  size_t draft_keys;  // u64 [gamma][B]
+  size_t draft_part;  // float2 [gamma][nslices][B]
+  size_t rows;        // int32 [B*(gamma+1)] row ids b*(gamma+1)+j of the verify rows
+  size_t row_part;    // float2 [B*(gamma+1)][nsegs]
+  size_t bonus_key;   // u64 [B]
+  size_t resid_key;   // u64 [2][B] residual key, fallback key
+  size_t resid_k;     // int32 [B] rejected position k* (0 = none)
+  size_t resid_lse;   // float [B] lse of the target row at k*
+  size_t total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
+  WsLayout L;
+  size_t off = 0;
+  const size_t rows = (size_t)B * (gamma + 1);
+  L.status = off;      off = align256(off + 4);
+  L.counters = off;    off = align256(off + 32);
+  L.draft_keys = off;  off = align256(off + 8ull * gamma * B);
+  L.draft_part = off;  off = align256(off + 8ull * gamma * draft_num_slices(V) * B);
+  L.rows = off;        off = align256(off + 4ull * rows);
+  L.row_part = off;    off = align256(off + 8ull * rows * verify_num_segs(V));
+  L.bonus_key = off;   off = align256(off + 8ull * B);
+  L.resid_key = off;   off = align256(off + 16ull * B);
+  L.resid_k = off;     off = align256(off + 4ull * B);
+  L.resid_lse = off;   off = align256(off + 4ull * B);
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+__host__ __device__ inline T* ws_ptr(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace dspark

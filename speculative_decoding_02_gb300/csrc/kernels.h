@@ -1,0 +1,60 @@
+// Internal launch functions of libdspark (host side).  Each enqueues its
+// kernels on `stream` and returns the cudaError_t of the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dspark {
+
+struct DraftArgs {
+  const float* U;
+  const void* W1;
+  const void* W2;
+  int wdtype;
+  const int32_t* anchor;
+  int B, gamma, V, r;
+  RngKey key;
+  int32_t* x_out;
+  float* p_out;
+  float* lse_out;
+  void* ws;
+};
+
+struct VerifyArgs {
+  const float* T;
+  const float* U;
+  const void* W1;
+  const void* W2;
+  int wdtype;
+  const int32_t* anchor;
+  const int32_t* x;
+  const float* p_d;
+  const float* lse_d;
+  const int32_t* ell;
+  int B, gamma, V, r;
+  RngKey key;
+  int32_t* n_out;
+  int32_t* tok_out;
+  void* ws;
+};
+
+cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream);
+
+cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdtype,
+                              const float* w, const float* sts_T, const int32_t* anchor,
+                              const int32_t* x, int B, int gamma, int H, int r, int V,
+                              float* c_out, int* status, cudaStream_t stream);
+
+size_t schedule_smem_bytes(int B, int gamma);
+
+cudaError_t launch_schedule(const float* c, int B, int gamma, const float* sps, int mode,
+                            uint32_t round_lo, int round_ge2, int32_t* khist, int32_t* ell_out,
+                            int32_t* nstar_out, double* theta_out, int* status,
+                            cudaStream_t stream);
+
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream);
+
+}  // namespace dspark

@@ -1,0 +1,205 @@
+// Confidence head (study report Eq.7) and the hardware-aware prefix scheduler
+// ("[DeepSeek-6] DSpark" blog, sections 6-7; study report Theta = tau * SPS(B)).
+#include "kernels.h"
+
+namespace dspark {
+namespace {
+
+// c_k = sigmoid((w[:H] . h_k + w[H:] . W1[x_{k-1}]) / T_k), one warp per (b, k).
+template <int HDT, int WDT>
+__global__ void confidence_kernel(const void* __restrict__ h, const void* __restrict__ W1,
+                                  const float* __restrict__ w, const float* __restrict__ sts_T,
+                                  const int32_t* __restrict__ anchor, const int32_t* __restrict__ x,
+                                  int B, int G, int H, int r, int V, float* __restrict__ c_out,
+                                  int* __restrict__ status) {
+  const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (item >= B * G) return;
+  const int b = item / G, k = item - (item / G) * G + 1;
+  const int prev = (k == 1) ? anchor[b] : x[(size_t)b * G + k - 2];
+  if (prev < 0 || prev >= V) {
+    if (lane == 0) {
+      if (status) record_status(status, DSPARK_ERR_INVALID);
+      c_out[item] = 0.f;
+    }
+    return;
+  }
+  const size_t hrow = (size_t)item * H;
+  float z = 0.f;
+  for (int i = lane; i < H; i += 32) z = fmaf(w[i], load_weight<HDT>(h, hrow + i), z);
+  for (int i = lane; i < r; i += 32) z = fmaf(w[H + i], load_weight<WDT>(W1, (size_t)prev * r + i), z);
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+  if (lane == 0) {
+    const float T = sts_T ? sts_T[k - 1] : 1.f;
+    c_out[item] = 1.f / (1.f + expf(-z / T));
+  }
+}
+
+constexpr int kSchedThreads = 1024;
+
+__device__ __forceinline__ bool cand_before(double a1, int i1, double a2, int i2) {
+  return a1 > a2 || (a1 == a2 && i1 < i2);
+}
+
+// One CTA.  a = prefix products in fp64; bitonic sort of the candidates by
+// (a desc, index asc) where index = b*gamma + j-1 gives (b asc, j asc); an
+// inclusive fp64 scan of the sorted a; Theta_n = (R + S_n) * SPS(R + n); the
+// greedy count n* is one less than the first n whose Theta does not exceed
+// Theta_{n-1}.
+__global__ void __launch_bounds__(kSchedThreads)
+schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restrict__ sps, int mode,
+                uint32_t round_lo, int round_ge2, int32_t* __restrict__ khist,
+                int32_t* __restrict__ ell_out, int32_t* __restrict__ nstar_out,
+                double* __restrict__ theta_out, int* __restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int N = R * G;
+  int NP = 1;
+  while (NP < N) NP <<= 1;
+  double* akey = reinterpret_cast<double*>(smem_raw);       // [NP]
+  int* aidx = reinterpret_cast<int*>(akey + NP);            // [NP]
+  int* ell_s = aidx + NP;                                    // [R]
+  __shared__ double warp_tot[32];
+  __shared__ int s_first_stop;
+  __shared__ int s_K;
+  const int tid = threadIdx.x;
+
+  if (mode == DSPARK_SCHED_FIXED) {
+    for (int b = tid; b < R; b += kSchedThreads) ell_out[b] = G;
+    if (tid == 0) {
+      *nstar_out = N;
+      *theta_out = 0.0;
+    }
+    return;
+  }
+
+  for (int b = tid; b < R; b += kSchedThreads) {
+    double a = 1.0;
+    bool bad = false;
+    for (int j = 0; j < G; ++j) {
+      const float cj = c[(size_t)b * G + j];
+      bad |= !(cj >= 0.f && cj <= 1.f);
+      a *= (double)cj;
+      akey[b * G + j] = a;
+      aidx[b * G + j] = b * G + j;
+    }
+    if (bad) record_status(status, DSPARK_ERR_NONFINITE);
+    ell_s[b] = 0;
+  }
+  for (int i = N + tid; i < NP; i += kSchedThreads) {
+    akey[i] = -1.0;
+    aidx[i] = 0x7fffffff;
+  }
+  if (tid == 0) {
+    s_first_stop = N + 1;
+    s_K = -1;
+    if (mode == DSPARK_SCHED_TOPK && round_ge2) s_K = khist[round_lo & 1u];
+  }
+  __syncthreads();
+
+  for (int size = 2; size <= NP; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = tid; t < (NP >> 1); t += kSchedThreads) {
+        const int i = (t / stride) * (stride << 1) + (t % stride);
+        const int j = i + stride;
+        const double ai = akey[i], aj = akey[j];
+        const int ii = aidx[i], ij = aidx[j];
+        const bool up = (i & size) == 0;
+        const bool swap = up ? cand_before(aj, ij, ai, ii) : cand_before(ai, ii, aj, ij);
+        if (swap) {
+          akey[i] = aj; akey[j] = ai;
+          aidx[i] = ij; aidx[j] = ii;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // inclusive scan of the sorted a in place: akey[i] = S_{i+1}
+  const int chunk = div_up(N, kSchedThreads);
+  const int lo = tid * chunk, hi = min(N, lo + chunk);
+  double run = 0.0;
+  for (int i = lo; i < hi; ++i) {
+    run += akey[i];
+    akey[i] = run;
+  }
+  double incl = run;
+  const int lane = tid & 31, wid = tid >> 5;
+  for (int off = 1; off < 32; off <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    double wt = warp_tot[lane];
+    for (int off = 1; off < 32; off <<= 1) {
+      const double o = __shfl_up_sync(0xffffffffu, wt, off);
+      if (lane >= off) wt += o;
+    }
+    warp_tot[lane] = wt;
+  }
+  __syncthreads();
+  const double base = (incl - run) + (wid > 0 ? warp_tot[wid - 1] : 0.0);
+  for (int i = lo; i < hi; ++i) akey[i] += base;
+  __syncthreads();
+
+  // Theta_n for n = 0..N; the first n >= 1 with Theta_n <= Theta_{n-1} stops
+  const double Rd = (double)R;
+  for (int n = tid + 1; n <= N; n += kSchedThreads) {
+    const double s_prev = n >= 2 ? akey[n - 2] : 0.0;
+    const double th_prev = (Rd + s_prev) * (double)sps[R + n - 1];
+    const double th = (Rd + akey[n - 1]) * (double)sps[R + n];
+    if (th <= th_prev) atomicMin(&s_first_stop, n);
+  }
+  __syncthreads();
+  const int nstar = (s_first_stop <= N) ? s_first_stop - 1 : N;
+  int admitted = nstar;
+  if (mode == DSPARK_SCHED_TOPK && round_ge2) admitted = min(max(s_K, 0), N);
+  for (int p = tid; p < admitted; p += kSchedThreads) atomicAdd(&ell_s[aidx[p] / G], 1);
+  __syncthreads();
+  for (int b = tid; b < R; b += kSchedThreads) ell_out[b] = ell_s[b];
+  if (tid == 0) {
+    *nstar_out = nstar;
+    const double S = admitted > 0 ? akey[admitted - 1] : 0.0;
+    *theta_out = (Rd + S) * (double)sps[R + admitted];
+    if (mode == DSPARK_SCHED_TOPK) khist[round_lo & 1u] = nstar;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdtype, const float* w,
+                              const float* sts_T, const int32_t* anchor, const int32_t* x, int B,
+                              int gamma, int H, int r, int V, float* c_out, int* status,
+                              cudaStream_t stream) {
+  const int items = B * gamma;
+  const dim3 grid(div_up(items * 32, 256));
+  if (hdtype == DSPARK_BF16 && wdtype == DSPARK_BF16)
+    confidence_kernel<DSPARK_BF16, DSPARK_BF16><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, c_out, status);
+  else if (hdtype == DSPARK_BF16)
+    confidence_kernel<DSPARK_BF16, DSPARK_F32><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, c_out, status);
+  else if (wdtype == DSPARK_BF16)
+    confidence_kernel<DSPARK_F32, DSPARK_BF16><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, c_out, status);
+  else
+    confidence_kernel<DSPARK_F32, DSPARK_F32><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, c_out, status);
+  return cudaGetLastError();
+}
+
+size_t schedule_smem_bytes(int B, int gamma) {
+  int NP = 1;
+  while (NP < B * gamma) NP <<= 1;
+  return (size_t)NP * (sizeof(double) + sizeof(int)) + sizeof(int) * (size_t)B;
+}
+
+cudaError_t launch_schedule(const float* c, int B, int gamma, const float* sps, int mode,
+                            uint32_t round_lo, int round_ge2, int32_t* khist, int32_t* ell_out,
+                            int32_t* nstar_out, double* theta_out, int* status, cudaStream_t stream) {
+  const size_t smem = schedule_smem_bytes(B, gamma);
+  cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  schedule_kernel<<<1, kSchedThreads, smem, stream>>>(c, B, gamma, sps, mode, round_lo, round_ge2, khist,
+                                                       ell_out, nstar_out, theta_out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

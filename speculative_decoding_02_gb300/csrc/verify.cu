@@ -1,0 +1,289 @@
+// Lossless rejection-sampling verification (the "10 key concepts" digest, item
+// 2: accept the longest valid prefix, resample at the first divergence; the
+// "[DeepSeek-6] DSpark" blog, section 1: plus one bonus token).
+//
+// 1. verify_prep      one CTA lists the target rows each request needs
+//                     (rows 0..ell_b of T[b]) so that the row pass sees a
+//                     flat, ragged-free task list.
+// 2. verify_rows      the streaming pass: every (row, segment) task reads one
+//                     kVerifySeg-long piece of a target row with 16-byte loads
+//                     and leaves an online-softmax partial; on the bonus row
+//                     (j = ell_b) it also races the Gumbel-perturbed logits.
+// 3. verify_decide    one warp per request, one lane per position: merge the
+//                     partials into lse_t, form p_t(x_k) / p_d(x_k), compare it
+//                     with the accept uniform; the first failing lane is the
+//                     rejection.
+// 4. verify_residual  only for rejecting requests: recompute the draft logits
+//                     of the rejected position (bias of x_{k-1} + U row) and
+//                     race Gumbel noise over log max(0, p_t - p_d).
+#include <algorithm>
+
+#include "kernels.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kRowThreads = 256;
+
+__global__ void __launch_bounds__(1024)
+verify_prep(const int32_t* __restrict__ ell, int B, int G, int32_t* __restrict__ rows,
+            int* __restrict__ counters, int* __restrict__ status) {
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int chunk = div_up(B, 1024);
+  const int lo = tid * chunk, hi = min(B, lo + chunk);
+  int run = 0;
+  for (int b = lo; b < hi; ++b) {
+    int L = ell[b];
+    if (L < 0 || L > G) {
+      record_status(status, DSPARK_ERR_INVALID);
+      L = L < 0 ? 0 : G;
+    }
+    run += L + 1;
+  }
+  int incl = run;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int wt = warp_tot[lane];
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, wt, off);
+      if (lane >= off) wt += o;
+    }
+    warp_tot[lane] = wt;
+  }
+  __syncthreads();
+  int pos = (incl - run) + (wid > 0 ? warp_tot[wid - 1] : 0);
+  for (int b = lo; b < hi; ++b) {
+    const int L = min(max(ell[b], 0), G);
+    for (int j = 0; j <= L; ++j) rows[pos++] = b * (G + 1) + j;
+  }
+  if (tid == 1023) counters[0] = pos;
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+verify_rows(const float* __restrict__ T, const int32_t* __restrict__ ell, int G, int V, int nsegs,
+            RngKey key, const int32_t* __restrict__ rows, const int* __restrict__ counters,
+            float2* __restrict__ row_part, unsigned long long* __restrict__ bonus_key,
+            int* __restrict__ status) {
+  __shared__ float s_m[kRowThreads / 32], s_s[kRowThreads / 32];
+  __shared__ unsigned long long s_k[kRowThreads / 32];
+  const int nrows = counters[0];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const long long ntasks = (long long)nrows * nsegs;
+  for (long long t = blockIdx.x; t < ntasks; t += gridDim.x) {
+    const int ri = (int)(t / nsegs), seg = (int)(t - (t / nsegs) * nsegs);
+    const int rowid = rows[ri];
+    const int b = rowid / (G + 1), j = rowid - (rowid / (G + 1)) * (G + 1);
+    const bool bonus = (j == min(max(ell[b], 0), G));
+    const float* Trow = T + (size_t)rowid * V;
+    const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
+    float m = -INFINITY, s = 0.f;
+    unsigned long long best = 0ull;
+    bool bad = false;
+    for (int v = v0 + 4 * tid; v < v1; v += 4 * kRowThreads) {
+      const float4 t4 = __ldcs(reinterpret_cast<const float4*>(Trow + v));
+      const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+      float mx = fmaxf(fmaxf(tv[0], tv[1]), fmaxf(tv[2], tv[3]));
+      bad |= !isfinite(tv[0]) | !isfinite(tv[1]) | !isfinite(tv[2]) | !isfinite(tv[3]);
+      if (mx > m) {
+        s *= expf(m - mx);
+        m = mx;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s += expf(tv[q] - m);
+      if (bonus) {
+        const uint4 rw = rng4(key, kStreamBonus, (uint32_t)b, (uint32_t)(j + 1), (uint32_t)(v >> 2));
+        const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const unsigned long long kz = argmax_key(tv[q] + gumbel_noise(words[q]), v + q);
+          best = kz > best ? kz : best;
+        }
+      }
+    }
+    warp_softmax_reduce(m, s, 0xffffffffu, 32);
+    best = warp_max_u64(best, 0xffffffffu, 32);
+    if (lane == 0) {
+      s_m[wid] = m;
+      s_s[wid] = s;
+      s_k[wid] = best;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float M = s_m[0], S = s_s[0];
+      unsigned long long K = s_k[0];
+      for (int w = 1; w < kRowThreads / 32; ++w) {
+        softmax_merge(M, S, s_m[w], s_s[w]);
+        K = s_k[w] > K ? s_k[w] : K;
+      }
+      row_part[(size_t)rowid * nsegs + seg] = make_float2(M, S);
+      if (bonus) atomicMax(&bonus_key[b], K);
+    }
+    __syncthreads();
+    if (bad) record_status(status, DSPARK_ERR_NONFINITE);
+  }
+}
+
+__global__ void verify_decide(const float* __restrict__ T, const int32_t* __restrict__ x,
+                              const float* __restrict__ p_d, const int32_t* __restrict__ ell, int B,
+                              int G, int V, int nsegs, RngKey key,
+                              const float2* __restrict__ row_part,
+                              const unsigned long long* __restrict__ bonus_key,
+                              int32_t* __restrict__ resid_k, float* __restrict__ resid_lse,
+                              int32_t* __restrict__ n_out, int32_t* __restrict__ tok_out,
+                              int* __restrict__ status) {
+  const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (b >= B) return;
+  const int L = min(max(ell[b], 0), G);
+  bool reject = false;
+  float lse_t = 0.f;
+  if (lane < L) {
+    const int rowid = b * (G + 1) + lane;
+    float m = -INFINITY, s = 0.f;
+    for (int i = 0; i < nsegs; ++i) {
+      const float2 pr = row_part[(size_t)rowid * nsegs + i];
+      softmax_merge(m, s, pr.x, pr.y);
+    }
+    lse_t = m + logf(s);
+    const int xk = checked_token(x[(size_t)b * G + lane], V, status);
+    const float q = expf(T[(size_t)rowid * V + xk] - lse_t);
+    const float ratio = q / p_d[(size_t)b * G + lane];
+    const uint4 rw = rng4(key, kStreamAccept, (uint32_t)b, (uint32_t)(lane + 1), 0u);
+    reject = !(uniform01(rw.x) < ratio);
+  }
+  const unsigned ballot = __ballot_sync(0xffffffffu, reject);
+  const int n = ballot ? (__ffs(ballot) - 1) : L;
+  const float lse_n = __shfl_sync(0xffffffffu, lse_t, n & 31);
+  if (lane == 0) {
+    n_out[b] = n;
+    if (n < L) {
+      resid_k[b] = n + 1;
+      resid_lse[b] = lse_n;
+    } else {
+      resid_k[b] = 0;
+      const unsigned long long kk = bonus_key[b];
+      if (kk == 0ull) record_status(status, DSPARK_ERR_NONFINITE);
+      tok_out[b] = kk ? argmax_key_index(kk) : 0;
+    }
+  }
+}
+
+template <int WDT>
+__global__ void __launch_bounds__(kRowThreads)
+verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__ U,
+                          const void* __restrict__ W1, const void* __restrict__ W2,
+                          const int32_t* __restrict__ anchor, const int32_t* __restrict__ x,
+                          const float* __restrict__ lse_d, int B, int G, int V, int r, RngKey key,
+                          const int32_t* __restrict__ resid_k, const float* __restrict__ resid_lse,
+                          unsigned long long* __restrict__ resid_key, int* __restrict__ status) {
+  extern __shared__ float Es[];   // [r]
+  __shared__ unsigned long long s_k1[kRowThreads / 32], s_k2[kRowThreads / 32];
+  const int b = blockIdx.y;
+  const int ks = resid_k[b];
+  if (ks <= 0) return;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int prev = checked_token((ks == 1) ? anchor[b] : x[(size_t)b * G + ks - 2], V, status);
+  for (int i = tid; i < r; i += kRowThreads) Es[i] = load_weight<WDT>(W1, (size_t)prev * r + i);
+  __syncthreads();
+  const float* Urow = U + ((size_t)b * G + (ks - 1)) * (size_t)V;
+  const float* Trow = T + ((size_t)b * (G + 1) + (ks - 1)) * (size_t)V;
+  const float ld = lse_d[(size_t)b * G + ks - 1];
+  const float lt = resid_lse[b];
+  const int v_begin = blockIdx.x * kDraftSlice, v_end = min(V, v_begin + kDraftSlice);
+  unsigned long long k1 = 0ull, k2 = 0ull;
+  for (int v4 = v_begin + 4 * tid; v4 < v_end; v4 += 4 * kRowThreads) {
+    const uint4 rw = rng4(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v4 >> 2));
+    const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int v = v4 + q;
+      float bias = 0.f;
+      for (int i = 0; i < r; ++i) bias = fmaf(Es[i], load_weight<WDT>(W2, (size_t)v * r + i), bias);
+      const float pd = expf(Urow[v] + bias - ld);
+      const float lt_v = Trow[v] - lt;
+      const float pt = expf(lt_v);
+      const float rho = pt - pd;
+      const float g = gumbel_noise(words[q]);
+      if (rho > 0.f) {
+        const unsigned long long kz = argmax_key(logf(rho) + g, v);
+        k1 = kz > k1 ? kz : k1;
+      }
+      const unsigned long long kf = argmax_key(lt_v + g, v);
+      k2 = kf > k2 ? kf : k2;
+    }
+  }
+  k1 = warp_max_u64(k1, 0xffffffffu, 32);
+  k2 = warp_max_u64(k2, 0xffffffffu, 32);
+  if (lane == 0) {
+    s_k1[wid] = k1;
+    s_k2[wid] = k2;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kRowThreads / 32; ++w) {
+      k1 = s_k1[w] > k1 ? s_k1[w] : k1;
+      k2 = s_k2[w] > k2 ? s_k2[w] : k2;
+    }
+    k1 = s_k1[0] > k1 ? s_k1[0] : k1;
+    k2 = s_k2[0] > k2 ? s_k2[0] : k2;
+    if (k1) atomicMax(&resid_key[b], k1);
+    atomicMax(&resid_key[B + b], k2);
+  }
+}
+
+__global__ void verify_residual_finalize(int B, const int32_t* __restrict__ resid_k,
+                                         const unsigned long long* __restrict__ resid_key,
+                                         int32_t* __restrict__ tok_out, int* __restrict__ status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B || resid_k[b] <= 0) return;
+  const unsigned long long k1 = resid_key[b], k2 = resid_key[B + b];
+  if (k1 == 0ull && k2 == 0ull) record_status(status, DSPARK_ERR_NONFINITE);
+  tok_out[b] = k1 ? argmax_key_index(k1) : (k2 ? argmax_key_index(k2) : 0);
+}
+
+template <int WDT>
+cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
+  const WsLayout L = ws_layout(a.B, a.gamma, a.V);
+  int* status = ws_ptr<int>(a.ws, L.status);
+  int* counters = ws_ptr<int>(a.ws, L.counters);
+  int32_t* rows = ws_ptr<int32_t>(a.ws, L.rows);
+  float2* row_part = ws_ptr<float2>(a.ws, L.row_part);
+  unsigned long long* bonus_key = ws_ptr<unsigned long long>(a.ws, L.bonus_key);
+  unsigned long long* resid_key = ws_ptr<unsigned long long>(a.ws, L.resid_key);
+  int32_t* resid_k = ws_ptr<int32_t>(a.ws, L.resid_k);
+  float* resid_lse = ws_ptr<float>(a.ws, L.resid_lse);
+  const int nsegs = verify_num_segs(a.V);
+  cudaError_t e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.total - L.bonus_key, stream);
+  if (e != cudaSuccess) return e;
+  verify_prep<<<1, 1024, 0, stream>>>(a.ell, a.B, a.gamma, rows, counters, status);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long max_tasks = (long long)a.B * (a.gamma + 1) * nsegs;
+  const int grid_rows = (int)std::min<long long>(max_tasks, (long long)sms * 8);
+  verify_rows<<<grid_rows, kRowThreads, 0, stream>>>(a.T, a.ell, a.gamma, a.V, nsegs, a.key, rows, counters,
+                                                      row_part, bonus_key, status);
+  verify_decide<<<div_up(a.B * 32, 256), 256, 0, stream>>>(a.T, a.x, a.p_d, a.ell, a.B, a.gamma, a.V, nsegs,
+                                                          a.key, row_part, bonus_key, resid_k, resid_lse,
+                                                          a.n_out, a.tok_out, status);
+  const dim3 grid_res(draft_num_slices(a.V), a.B);
+  verify_residual_cuda_core<WDT><<<grid_res, kRowThreads, sizeof(float) * a.r, stream>>>(
+      a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, a.B, a.gamma, a.V, a.r, a.key, resid_k, resid_lse,
+      resid_key, status);
+  verify_residual_finalize<<<div_up(a.B, 256), 256, 0, stream>>>(a.B, resid_k, resid_key, a.tok_out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
+  return a.wdtype == DSPARK_BF16 ? run_verify<DSPARK_BF16>(a, stream) : run_verify<DSPARK_F32>(a, stream);
+}
+
+}  // namespace dspark

@@ -46,6 +46,7 @@ class Workload:
     rounds: int = 1
     w_sigma: float = 0.1
     weight_sigma: float = 0.02
+    sps_kind: str = "saturating"  # "saturating": B/(1+B/b0); "steps": 1/(1+B/b0)
     extra: dict = field(default_factory=dict)
 
 
@@ -88,10 +89,14 @@ def custom(name="custom", **kw):
 
 
 def sps_table(wl: Workload) -> Optional[torch.Tensor]:
-    """SPS(B) = B / (1 + B / b0) tabulated at B = 0 .. sps_len-1 (float32)."""
+    """The SPS table at B = 0 .. sps_len-1 (float32): B / (1 + B / b0) as the
+    workloads state it, or 1 / (1 + B / b0), a steps-per-second curve that falls
+    with the batch size (used by tests to make the scheduler truncate)."""
     if wl.sps_b0 is None:
         return None
     b = torch.arange(wl.sps_len, dtype=torch.float64)
+    if wl.sps_kind == "steps":
+        return (1.0 / (1.0 + b / wl.sps_b0)).to(torch.float32)
     return (b / (1.0 + b / wl.sps_b0)).to(torch.float32)
 
 

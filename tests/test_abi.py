@@ -1,0 +1,88 @@
+"""The C-ABI library loads without a GPU, exports every symbol its header
+declares, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_02_gb300 as ds
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_02_gb300 import build
+
+    build.build()
+    return ds.library()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(dspark_[a-z_0-9]+)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"dspark_markov_draft", "dspark_confidence", "dspark_schedule", "dspark_verify",
+            "dspark_round", "dspark_workspace_size", "dspark_read_status", "dspark_strerror"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), f"{n} declared but not exported"
+
+
+def test_strerror_and_workspace_size(lib):
+    for code in range(7):
+        assert ds._strerror(code)
+    assert ds._strerror(99) == "unknown status"
+    assert lib.dspark_workspace_size(0, 4, 1024) == 0
+    a = lib.dspark_workspace_size(2, 4, 1024)
+    b = lib.dspark_workspace_size(128, 16, 151936)
+    assert a > 0 and b > a and b % 256 == 0
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_host_side_argument_errors(lib):
+    p = _fake()
+    ws = _fake(0x100000)
+    big = 1 << 30
+    # null pointers
+    assert lib.dspark_markov_draft(None, p, p, 1, p, 2, 4, 1024, 16, 0, 0, p, p, p, ws, big, None) == ds.ERR_INVALID
+    # unsupported sizes: gamma > 32, V % 8, r % 16, r > 256
+    assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 33, 1024, 16, 0, 0, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 4, 1020, 16, 0, 0, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 4, 1024, 24, 0, 0, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 4, 1024, 512, 0, 0, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
+    # bad dtype, workspace too small / misaligned, round out of range
+    assert lib.dspark_markov_draft(p, p, p, 7, p, 2, 4, 1024, 16, 0, 0, p, p, p, ws, big, None) == ds.ERR_INVALID
+    assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 4, 1024, 16, 0, 0, p, p, p, ws, 64, None) == ds.ERR_WORKSPACE
+    assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 4, 1024, 16, 0, 0, p, p, p, _fake(0x100010), big,
+                                   None) == ds.ERR_WORKSPACE
+    assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 4, 1024, 16, 0, 1 << 29, p, p, p, ws, big,
+                                   None) == ds.ERR_INVALID
+    # scheduler: SPS table too short, B*gamma above 8192, bad mode, top-K without history
+    assert lib.dspark_schedule(p, 2, 4, p, 10, 1, 0, None, p, p, p, ws, big, None) == ds.ERR_INVALID
+    assert lib.dspark_schedule(p, 512, 32, p, 99999, 1, 0, None, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_schedule(p, 2, 4, p, 11, 5, 0, None, p, p, p, ws, big, None) == ds.ERR_INVALID
+    assert lib.dspark_schedule(p, 2, 4, p, 11, 2, 0, None, p, p, p, ws, big, None) == ds.ERR_INVALID
+    # verify: null target logits
+    assert lib.dspark_verify(None, p, p, p, 1, p, p, p, p, p, 2, 4, 1024, 16, 0, 0, p, p, ws, big,
+                             None) == ds.ERR_INVALID
+    # confidence: bad dtype
+    assert lib.dspark_confidence(p, 3, p, 1, p, None, p, p, 2, 4, 64, 16, 1024, p, None) == ds.ERR_INVALID
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+    U = torch.zeros(2, 4, 1024)
+    with pytest.raises(ValueError):
+        ds.markov_draft(U, U, U, torch.zeros(2, dtype=torch.int32), 0)
