@@ -156,6 +156,31 @@ int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
                  int32_t* n_out, int32_t* tok_out,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The Markov draft without a caller workspace.  The paper has no counterpart:
+ * this entry exists for callers that cannot allocate device memory when they
+ * call us (an engine whose pool owns all of HBM, a plugin given no allocator,
+ * a decode loop that must not call cudaMalloc).  It computes exactly what
+ * dspark_markov_draft computes, with its scratch in a fixed array of
+ * DSPARK_NOALLOC_SCRATCH_BYTES inside the library's device memory, which every
+ * GPU that loads the library holds until the process exits.  Inputs and outputs
+ * are the caller's, as above.  It allocates nothing.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU race.
+ *    Each call clears what must start at zero.  Errors that the kernels detect
+ *    are not reported back by this entry.
+ *  - Sizes whose draft scratch (about 8 * gamma * B bytes per vocabulary slice
+ *    of the draft kernel) exceeds the array return DSPARK_ERR_WORKSPACE before
+ *    anything is enqueued.
+ */
+#define DSPARK_NOALLOC_SCRATCH_BYTES (4u << 20)
+int dspark_markov_draft_noalloc(const float* U, const void* W1, const void* W2, int wdtype,
+                                const int32_t* anchor, int B, int gamma, int V, int r,
+                                uint64_t seed, uint64_t round,
+                                int32_t* x_out, float* p_out, float* lse_out, void* stream);
+
 /* Waits for `stream`, then copies the workspace status word (a DSPARK_* code,
  * the first error any kernel recorded since the last clear) to *host_status and
  * clears it.  Returns DSPARK_OK or DSPARK_ERR_CUDA. */
