@@ -148,6 +148,12 @@ constexpr int kMaxCandidates = 8192;
 __host__ __device__ inline int div_up(int a, int b) { return (a + b - 1) / b; }
 
 __host__ __device__ inline int draft_num_slices(int V) { return div_up(V, kDraftSlice); }
+// Slices reserved per position in the draft partial buffer: enough for the
+// CUDA-core grid and for one tensor-core CTA per SM (up to 160 SMs).
+constexpr int kMaxDraftCtas = 160;
+__host__ __device__ inline int draft_part_slices(int V) {
+  return draft_num_slices(V) > kMaxDraftCtas ? draft_num_slices(V) : kMaxDraftCtas;
+}
 __host__ __device__ inline int verify_num_segs(int V) { return div_up(V, kVerifySeg); }
 
 struct WsLayout {
@@ -173,7 +179,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   L.status = off;      off = align256(off + 4);
   L.counters = off;    off = align256(off + 32);
   L.draft_keys = off;  off = align256(off + 8ull * gamma * B);
-  L.draft_part = off;  off = align256(off + 8ull * gamma * draft_num_slices(V) * B);
+  L.draft_part = off;  off = align256(off + 8ull * gamma * draft_part_slices(V) * B);
   L.rows = off;        off = align256(off + 4ull * rows);
   L.row_part = off;    off = align256(off + 8ull * rows * verify_num_segs(V));
   L.bonus_key = off;   off = align256(off + 8ull * B);

@@ -1,0 +1,693 @@
+// Markov draft step on the 5th-generation tensor cores ("[DeepSeek-6] DSpark"
+// blog, sections 3-4; study report Eq.4).
+//
+// One launch per position k.  A CTA owns one 128-request M tile and a
+// contiguous range of 64-column vocabulary tiles:
+//
+//   warp 0      producer: per tile, four 8 KB TMA loads of W2 (one 64-wide K
+//               atom each, 128-byte swizzled, kept in L2 with evict_last) and
+//               up to 128 row copies of U (cp.async.bulk, evict_first) into a
+//               padded shared-memory tile.
+//   warp 1      allocates 128 TMEM columns; one lane issues the bias GEMM
+//               bias[128 x 64] = E[128 x 256] * W2_tile^T with tcgen05.mma
+//               (bf16 in, fp32 accumulate) into one of two TMEM accumulators.
+//   warps 2-9   gather E = W1[x_{k-1}] (128 rows, 128-byte swizzled) once, then
+//               per tile read the accumulator (tcgen05.ld, thread = request
+//               row, 32 columns per warp), add U, and fold the 32 fused logits
+//               into the row's online softmax (m, s) and its Gumbel-max race.
+//
+// Per CTA and request it leaves (m, s) in the partial buffer and pushes its best
+// perturbed logit into the request's 64-bit argmax key (atomicMax; ties go to
+// the smaller index).  The next position's CTAs decode x_k from that key.
+// Every wait is bounded; on a timeout the CTA records DSPARK_ERR_TIMEOUT,
+// drains the copies and MMAs it issued, frees its TMEM and returns.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace dspark {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;             // requests per M tile (TMEM lanes)
+constexpr int BN = 64;              // vocabulary columns per tile
+constexpr int KR = 256;             // Markov rank handled by this kernel
+constexpr int kAtoms = KR / 64;     // 64-wide K atoms (128 bytes of bf16)
+constexpr int kWStages = 6;         // W2 atom ring
+constexpr int kUStages = 3;         // U tile ring
+constexpr int kUBox = 32;           // fp32 columns per U box (128 bytes, swizzled)
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kTmemCols = 128;  // two 64-column accumulators
+
+constexpr int kEBytes = kAtoms * BM * 128;       // 65536
+constexpr int kWStageBytes = BN * 128;           // 8192
+constexpr int kUStageBytes = BN * BM * 4;        // 32768: two [rows x 32] boxes
+constexpr int kSmemBytes = 1024 /*align*/ + kEBytes + kWStages * kWStageBytes + kUStages * kUStageBytes + 256;
+
+struct __align__(8) Barriers {
+  uint64_t full_w[kWStages], empty_w[kWStages];
+  uint64_t full_u[kUStages], empty_u[kUStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t e_full, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+enum Mode { kDraft = 0, kResidual = 1 };
+
+struct StepParams {
+  const float* U;
+  const __nv_bfloat16* W1;
+  const int32_t* anchor;
+  // residual mode: rejected position k* of each request (0 = none), the draft
+  // tokens, the draft lse of every position, the target lse of row k*-1
+  const float* T;
+  const int32_t* x;
+  const int32_t* resid_k;
+  const float* lse_d;
+  const float* resid_lse;
+  unsigned long long* resid_key;
+  const unsigned long long* keys_prev;  // argmax keys of position k-1 (k >= 2)
+  unsigned long long* keys_cur;         // argmax keys of position k
+  float2* part;                         // [nslices][B] partials of position k
+  int* status;
+  int B, G, V, k;
+  int ctas_per_mtile;
+  int ntiles;                           // vocabulary tiles of width BN
+  RngKey key;
+};
+
+__device__ __forceinline__ int tile_begin(int slice, int nslices, int ntiles) {
+  return (int)(((long long)ntiles * slice) / nslices);
+}
+
+// Gumbel-max race of one request row inside one thread's column range.
+//
+// The perturbed logit of entry v is z_v = l_v + G_v, G_v = -log E_v,
+// E_v = -log u_v.  Entry v can beat the thread's best zbest only if
+// E_v < exp(l_v - zbest); since E_v >= 1 - u_v this needs
+// 1 - u_v < exp(l_v - run_m) * exp(run_m - zbest).  The first factor is the
+// softmax term already computed for the normaliser, so the test costs one FMA
+// and one compare on the raw random bits; only entries that pass it (a few per
+// thousand once zbest has settled) get the two exact logarithms.
+struct RowRace {
+  float run_m, run_s;   // online softmax: running max and sum of exp(l - run_m)
+  float zbest;          // best perturbed logit so far
+  int best_v;           // its vocabulary index
+  float bound;          // exp(run_m - zbest) with a 2^-10 safety margin
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float race_bound(float run_m, float zbest) {
+  return exp2f((run_m - zbest) * kLog2e) * (1.0f + 0x1p-10f);
+}
+
+__device__ __forceinline__ uint32_t pick_word(const uint4& w, int j) {
+  return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
+}
+
+// Folds the fused logits l[0..nv) of columns v0.. into the race.  `spill` is
+// this thread's 128-byte swizzled shared-memory row (chunks j0.., xor `sw`)
+// where the logits are parked when a candidate needs its exact perturbed logit.
+template <int CPP>
+__device__ __forceinline__ void race_tile(RowRace& st, float (&l)[CPP], int nv, int v0, unsigned char* spill,
+                                          int j0, int sw, const RngKey& key, uint32_t req, uint32_t pos) {
+  float tm = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < CPP; ++c)
+    if (c < nv) tm = fmaxf(tm, l[c]);
+  if (tm > st.run_m) {
+    st.run_s = (st.run_m == -INFINITY) ? 0.f : st.run_s * exp2f((st.run_m - tm) * kLog2e);
+    st.run_m = tm;
+    if (st.zbest == -INFINITY) {
+      // seed the race with this tile's largest logit
+      int cs = 0;
+#pragma unroll
+      for (int c = CPP - 1; c >= 0; --c)
+        if (c < nv && l[c] == tm) cs = c;
+      const int v = v0 + cs;
+      const uint4 rw = rng4(key, kStreamDraft, req, pos, (uint32_t)(v >> 2));
+      st.zbest = tm + gumbel_noise(pick_word(rw, v & 3));
+      st.best_v = v;
+    }
+    st.bound = race_bound(st.run_m, st.zbest);
+  }
+  const float mb = st.run_m * kLog2e;
+  uint32_t cand = 0;
+#pragma unroll
+  for (int g = 0; g < CPP / 4; ++g) {
+    if (4 * g < nv) {
+      const uint4 rw = rng4(key, kStreamDraft, req, pos, (uint32_t)((v0 >> 2) + g));
+      const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = 4 * g + j;
+        const float e = exp2f(fmaf(l[c], kLog2e, -mb));
+        st.run_s += e;
+        // 1 + m 2^-23 with m the top 23 random bits: 2 - up = 1 - u + 2^-24
+        const float up = __uint_as_float((words[j] >> 9) | 0x3F800000u);
+        const float thr = fmaf(-e, st.bound, 0x1.fffffcp0f);
+        if (up > thr) cand |= 1u << c;
+      }
+    }
+  }
+  if (cand) {
+#pragma unroll
+    for (int c = 0; c < CPP; c += 4)
+      *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(l[c], l[c + 1], l[c + 2], l[c + 3]);
+    while (cand) {
+      const int c = __ffs(cand) - 1;
+      cand &= cand - 1;
+      const int v = v0 + c;
+      const uint4 rw = rng4(key, kStreamDraft, req, pos, (uint32_t)(v >> 2));
+      const float lc = reinterpret_cast<const float*>(spill + (((j0 + c / 4) ^ sw) << 4))[c & 3];
+      const float z = lc + gumbel_noise(pick_word(rw, v & 3));
+      if (z > st.zbest) {
+        st.zbest = z;
+        st.best_v = v;
+        st.bound = race_bound(st.run_m, st.zbest);
+      }
+    }
+  }
+}
+
+// Race of the residual resample: argmax_v log rho_v + G_v over rho_v > 0,
+// rho = max(0, p_t - p_d).  Entry v can beat zbest only if
+// E_v < rho_v exp(-zbest), so the same cheap test on the raw random bits
+// applies with rho_v in place of the softmax term.
+struct ResRace {
+  float zbest;
+  int best_v;
+  float bound;   // exp(-zbest) with a 2^-10 safety margin
+};
+
+template <int CPP>
+__device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP], int nv, int v0, float* spill,
+                                           const RngKey& key, uint32_t req, uint32_t pos) {
+  if (st.zbest == -INFINITY) {
+    float rmax = 0.f;
+    int cs = -1;
+#pragma unroll
+    for (int c = 0; c < CPP; ++c)
+      if (c < nv && rho[c] > rmax) { rmax = rho[c]; cs = c; }
+    if (cs < 0) return;   // no positive residual mass seen yet
+    const int v = v0 + cs;
+    const uint4 rw = rng4(key, kStreamResidual, req, pos, (uint32_t)(v >> 2));
+    st.zbest = logf(rmax) + gumbel_noise(pick_word(rw, v & 3));
+    st.best_v = v;
+    st.bound = expf(-st.zbest) * (1.0f + 0x1p-10f);
+  }
+  uint32_t cand = 0;
+#pragma unroll
+  for (int g = 0; g < CPP / 4; ++g) {
+    if (4 * g < nv) {
+      const uint4 rw = rng4(key, kStreamResidual, req, pos, (uint32_t)((v0 >> 2) + g));
+      const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = 4 * g + j;
+        const float up = __uint_as_float((words[j] >> 9) | 0x3F800000u);
+        const float thr = fmaf(-rho[c], st.bound, 0x1.fffffcp0f);
+        if (rho[c] > 0.f && up > thr) cand |= 1u << c;
+      }
+    }
+  }
+  if (cand) {
+#pragma unroll
+    for (int c = 0; c < CPP; c += 4) *reinterpret_cast<float4*>(spill + c) = make_float4(rho[c], rho[c + 1], rho[c + 2], rho[c + 3]);
+    while (cand) {
+      const int c = __ffs(cand) - 1;
+      cand &= cand - 1;
+      const int v = v0 + c;
+      const uint4 rw = rng4(key, kStreamResidual, req, pos, (uint32_t)(v >> 2));
+      const float z = logf(spill[c]) + gumbel_noise(pick_word(rw, v & 3));
+      if (z > st.zbest) {
+        st.zbest = z;
+        st.best_v = v;
+        st.bound = expf(-st.zbest) * (1.0f + 0x1p-10f);
+      }
+    }
+  }
+}
+
+// R = rows of one request replica (32, 64 or 128).  With B <= 64 the M tile
+// holds 128 / R copies of the requests so that every TMEM lane quarter -- and
+// so every epilogue warp -- has rows to work on; each copy takes its own share
+// of the tile's columns.
+// MODE kDraft: one draft position for every request (U rows by TMA).
+// MODE kResidual: for every request that rejected at position k*, the fused
+// draft logits of k* again, raced over log max(0, p_t - p_d) (U and T rows
+// read directly by the epilogue threads).
+template <int R, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
+              const StepParams p) {
+  constexpr int kRepl = BM / R;            // copies of each request row
+  constexpr int kParts = 2 * kRepl;        // column parts of a tile
+  constexpr int CPP = BN / kParts;         // columns per thread per tile
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* E_s = smem;
+  unsigned char* W_s = E_s + kEBytes;
+  unsigned char* U_s = W_s + kWStages * kWStageBytes;
+  Barriers* bars = reinterpret_cast<Barriers*>(U_s + kUStages * kUStageBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mtile = blockIdx.x / p.ctas_per_mtile;
+  const int slice = blockIdx.x - mtile * p.ctas_per_mtile;
+  const int m0 = mtile * R;
+  const int rows_valid = min(R, p.B - m0);
+  const int t0 = tile_begin(slice, p.ctas_per_mtile, p.ntiles);
+  const int t1 = tile_begin(slice + 1, p.ctas_per_mtile, p.ntiles);
+  const int ntl = t1 - t0;
+  volatile int* abort = &bars->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWStages; ++s) { mbar_init(&bars->full_w[s], 1); mbar_init(&bars->empty_w[s], 1); }
+    for (int s = 0; s < kUStages; ++s) { mbar_init(&bars->full_u[s], 1); mbar_init(&bars->empty_u[s], kEpiWarps); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&bars->acc_full[s], 1); mbar_init(&bars->acc_empty[s], kEpiWarps); }
+    mbar_init(&bars->e_full, kEpiWarps);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&w2_map);
+    prefetch_tensormap(&u_map);
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_w = policy_evict_last(), pol_u = policy_evict_first();
+    uint32_t wcount = 0, ucount = 0;
+    bool ok = true;
+    for (int i = 0; i < ntl && ok; ++i) {
+      const int v0 = (t0 + i) * BN;
+      const int ncols = min(BN, p.V - v0);
+      for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
+        const int s = wcount % kWStages;
+        ok = mbar_wait(&bars->empty_w[s], ((wcount / kWStages) & 1) ^ 1, abort, p.status);
+        if (ok && lane == 0) {
+          mbar_arrive_expect_tx(&bars->full_w[s], kWStageBytes);
+          tma_g2s_2d(W_s + s * kWStageBytes, &w2_map, a * 64, v0, &bars->full_w[s], pol_w);
+        }
+      }
+      if (!ok) break;
+      if constexpr (MODE == kResidual) continue;
+      const int su = ucount % kUStages;
+      ok = mbar_wait(&bars->empty_u[su], ((ucount / kUStages) & 1) ^ 1, abort, p.status);
+      if (!ok) break;
+      if (lane == 0) {
+        // two [R rows x 32 columns] boxes of U[m0.., k-1, v0..]; rows past B and
+        // columns past V are filled with zeros by the copy engine
+        mbar_arrive_expect_tx(&bars->full_u[su], (uint32_t)(2 * kUBox * R * 4));
+        unsigned char* dst = U_s + su * kUStageBytes;
+        tma_g2s_3d(dst, &u_map, v0, p.k - 1, m0, &bars->full_u[su], pol_u);
+        tma_g2s_3d(dst + R * 128, &u_map, v0 + kUBox, p.k - 1, m0, &bars->full_u[su], pol_u);
+      }
+      (void)ncols;
+      ++ucount;
+    }
+    // drain: every copy this warp issued has landed before the CTA exits
+    if (lane == 0 && *abort) {
+      for (uint32_t c = (wcount > kWStages ? wcount - kWStages : 0); c < wcount; ++c)
+        mbar_drain(&bars->full_w[c % kWStages], (c / kWStages) & 1);
+      for (uint32_t c = (ucount > kUStages ? ucount - kUStages : 0); c < ucount; ++c)
+        mbar_drain(&bars->full_u[c % kUStages], (c / kUStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      const uint32_t e_addr = smem_u32(E_s);
+      uint32_t wcount = 0;
+      bool ok = mbar_wait(&bars->e_full, 0, abort, p.status);
+      tc_fence_after();
+      for (int i = 0; i < ntl && ok; ++i) {
+        const int acc = i & 1;
+        ok = mbar_wait(&bars->acc_empty[acc], ((i >> 1) & 1) ^ 1, abort, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
+          const int s = wcount % kWStages;
+          ok = mbar_wait(&bars->full_w[s], (wcount / kWStages) & 1, abort, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t w_addr = smem_u32(W_s + s * kWStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sw128_kmajor_desc(e_addr + a * (BM * 128) + kk * 32);
+            const uint64_t bd = sw128_kmajor_desc(w_addr + kk * 32);
+            umma_bf16(d_tmem, ad, bd, idesc, (a | kk) != 0);
+          }
+          umma_commit(&bars->empty_w[s]);
+        }
+        if (ok) umma_commit(&bars->acc_full[acc]);
+      }
+      // all MMAs this thread issued are complete before TMEM is released
+      umma_commit(&bars->drain);
+      mbar_drain(&bars->drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;               // TMEM lane quarter of this warp
+    const int h = (warp - 2) >> 2;        // which of the two warps of the quarter
+    const int m = q * 32 + lane;          // TMEM lane = row of the M tile
+    const int rep = m / R, r = m - rep * R;
+    const int part = rep * 2 + h;         // column part of every tile
+    const int b = m0 + r;
+    bool active = r < rows_valid;
+    int ks = p.k;                         // position of this row
+    if constexpr (MODE == kResidual) {
+      ks = active ? p.resid_k[b] : 0;
+      active = ks > 0;
+    }
+
+    // gather E[m, :] = W1[x_{k-1}] for K atoms 2h, 2h+1 (16-byte chunks, swizzled)
+    int prev = 0;
+    if (active) {
+      int raw;
+      if constexpr (MODE == kDraft)
+        raw = (p.k == 1) ? p.anchor[b] : argmax_key_index(p.keys_prev[b]);
+      else
+        raw = (ks == 1) ? p.anchor[b] : p.x[(size_t)b * p.G + ks - 2];
+      prev = checked_token(raw, p.V, p.status);
+    }
+    const uint4* wrow = reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * KR);
+#pragma unroll
+    for (int a2 = 0; a2 < 2; ++a2) {
+      const int a = 2 * h + a2;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 val = active ? __ldg(wrow + a * 8 + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(E_s + a * (BM * 128) + m * 128 + ((c ^ (m & 7)) << 4)) = val;
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->e_full);
+
+    RowRace st{-INFINITY, 0.f, -INFINITY, -1, INFINITY};
+    ResRace rs{-INFINITY, -1, INFINITY};
+    float ld2 = 0.f, lt2 = 0.f;
+    const float* Urow = nullptr;
+    const float* Trow = nullptr;
+    float* spill = reinterpret_cast<float*>(U_s + ((warp - 2) * 32 + lane) * 144);
+    if constexpr (MODE == kResidual) {
+      if (active) {
+        ld2 = p.lse_d[(size_t)b * p.G + ks - 1] * kLog2e;
+        lt2 = p.resid_lse[b] * kLog2e;
+        Urow = p.U + ((size_t)b * p.G + (ks - 1)) * (size_t)p.V;
+        Trow = p.T + ((size_t)b * (p.G + 1) + (ks - 1)) * (size_t)p.V;
+      }
+    }
+    for (int i = 0; i < ntl; ++i) {
+      const int acc_i = i & 1;
+      const int v0 = (t0 + i) * BN + part * CPP;
+      const int nv = min(CPP, p.V - v0);
+      float uu[CPP], tt[CPP];
+      if constexpr (MODE == kResidual) {
+        // issue this tile's row loads before waiting for the accumulator
+        if (active && nv > 0) {
+#pragma unroll
+          for (int c = 0; c < CPP; c += 4) {
+            if (c < nv) {
+              const float4 u4 = __ldcs(reinterpret_cast<const float4*>(Urow + v0 + c));
+              const float4 t4 = __ldcs(reinterpret_cast<const float4*>(Trow + v0 + c));
+              uu[c] = u4.x; uu[c + 1] = u4.y; uu[c + 2] = u4.z; uu[c + 3] = u4.w;
+              tt[c] = t4.x; tt[c + 1] = t4.y; tt[c + 2] = t4.z; tt[c + 3] = t4.w;
+            }
+          }
+        }
+      }
+      if (!mbar_wait(&bars->acc_full[acc_i], (i >> 1) & 1, abort, p.status)) break;
+      tc_fence_after();
+      float v[CPP];
+      tmem_load_cols<CPP>(tmem + ((uint32_t)(q * 32) << 16) + acc_i * BN + part * CPP, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty[acc_i]);
+      if constexpr (MODE == kDraft) {
+        const int su = i % kUStages;
+        if (!mbar_wait(&bars->full_u[su], (i / kUStages) & 1, abort, p.status)) break;
+        // this thread's columns: box (part*CPP)/32, 16-byte chunks j0.. of row r,
+        // stored at chunk j ^ (r & 7) (128-byte swizzle)
+        unsigned char* urow = U_s + su * kUStageBytes + ((part * CPP) / kUBox) * (R * 128) + r * 128;
+        const int j0 = ((part * CPP) % kUBox) / 4;
+        if (active && nv > 0) {
+#pragma unroll
+          for (int c = 0; c < CPP; c += 4) {
+            const float4 u4 = *reinterpret_cast<const float4*>(urow + (((j0 + c / 4) ^ (r & 7)) << 4));
+            v[c + 0] += u4.x; v[c + 1] += u4.y; v[c + 2] += u4.z; v[c + 3] += u4.w;
+          }
+          race_tile<CPP>(st, v, nv, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)p.k);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->empty_u[su]);
+      } else {
+        if (active && nv > 0) {
+          // rho = max(0, p_t - p_d), kept in place of U (non-positive entries
+          // are outside the residual's support and never race)
+#pragma unroll
+          for (int c = 0; c < CPP; ++c) {
+            const float pd = exp2f(fmaf(v[c] + uu[c], kLog2e, -ld2));
+            const float pt = exp2f(fmaf(tt[c], kLog2e, -lt2));
+            uu[c] = pt - pd;
+          }
+          resid_tile<CPP>(rs, uu, nv, v0, spill, p.key, (uint32_t)b, (uint32_t)ks);
+        }
+      }
+    }
+    if (MODE == kDraft && (st.run_m != st.run_m || st.run_m == INFINITY))
+      record_status(p.status, DSPARK_ERR_NONFINITE);
+
+    // combine the parts of each request row, then publish one partial per row
+    float* xm = reinterpret_cast<float*>(U_s);   // the U ring is idle once every tile is read
+    float* xs = xm + 2 * BM;
+    unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 2 * BM);
+    unsigned long long key = 0ull;
+    if constexpr (MODE == kDraft) key = st.best_v >= 0 ? argmax_key(st.zbest, st.best_v) : 0ull;
+    else key = rs.best_v >= 0 ? argmax_key(rs.zbest, rs.best_v) : 0ull;
+    named_bar_sync(1, kEpiWarps * 32);
+    const int slot = part * R + r;               // parts of row r at r, R + r, ...
+    xm[slot] = st.run_m;
+    xs[slot] = st.run_s;
+    xk[slot] = key;
+    named_bar_sync(1, kEpiWarps * 32);
+    if (part == 0 && active) {
+      float M = -INFINITY, S = 0.f;
+      unsigned long long K = 0ull;
+#pragma unroll
+      for (int j = 0; j < kParts; ++j) {
+        softmax_merge(M, S, xm[j * R + r], xs[j * R + r]);
+        K = xk[j * R + r] > K ? xk[j * R + r] : K;
+      }
+      if constexpr (MODE == kDraft) {
+        p.part[(size_t)slice * p.B + b] = make_float2(M, S);
+        if (K) atomicMax(&p.keys_cur[b], K);
+      } else {
+        if (K) atomicMax(&p.resid_key[b], K);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// One warp per (request, position): merge the slice partials into lse_k,
+// decode x_k from its argmax key and recompute the fused logit of x_k.
+__global__ void draft_finalize_tc(const float* __restrict__ U, const __nv_bfloat16* __restrict__ W1,
+                                  const __nv_bfloat16* __restrict__ W2, const int32_t* __restrict__ anchor,
+                                  const unsigned long long* __restrict__ keys, const float2* __restrict__ part,
+                                  int B, int G, int V, int nslices, int part_slices, int32_t* __restrict__ x_out,
+                                  float* __restrict__ p_out, float* __restrict__ lse_out, int* __restrict__ status) {
+  const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (item >= B * G) return;
+  const int b = item / G, k = item - (item / G) * G + 1;
+  const float2* pp = part + (size_t)(k - 1) * part_slices * B;
+  float m = -INFINITY, s = 0.f;
+  for (int i = lane; i < nslices; i += 32) {
+    const float2 pr = pp[(size_t)i * B + b];
+    softmax_merge(m, s, pr.x, pr.y);
+  }
+  warp_softmax_reduce(m, s, 0xffffffffu, 32);
+  const float lse = m + logf(s);
+  const unsigned long long kk = keys[(size_t)(k - 1) * B + b];
+  int x = kk ? argmax_key_index(kk) : -1;
+  if (x < 0 || x >= V) {
+    if (lane == 0) record_status(status, DSPARK_ERR_NONFINITE);
+    x = 0;
+  }
+  int prev = (k == 1) ? anchor[b] : argmax_key_index(keys[(size_t)(k - 2) * B + b]);
+  prev = checked_token(prev, V, status);
+  float dot = 0.f;
+  for (int i = lane; i < KR; i += 32)
+    dot = fmaf(__bfloat162float(W1[(size_t)prev * KR + i]), __bfloat162float(W2[(size_t)x * KR + i]), dot);
+  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  if (lane == 0) {
+    const size_t o = (size_t)b * G + (k - 1);
+    x_out[o] = x;
+    p_out[o] = expf(U[o * (size_t)V + x] + dot - lse);
+    lse_out[o] = lse;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+// W2 [V, 256] bf16 viewed as a 2-D tensor (K innermost) with 64 x 64 boxes,
+// 128-byte swizzled: one box is one K atom of a 64-column vocabulary tile.
+cudaError_t make_w2_tensor_map(const void* W2, int V, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)KR, (cuuint64_t)V};
+  cuuint64_t strides[1] = {(cuuint64_t)KR * 2};
+  cuuint32_t box[2] = {64, BN};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// U [B, G, V] fp32 viewed as a 3-D tensor (V innermost) with [R x 1 x 32]
+// boxes, 128-byte swizzled: one box is 32 columns of R request rows at one
+// position.
+cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)G, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)V * 4, (cuuint64_t)G * V * 4};
+  cuuint32_t box[3] = {(cuuint32_t)kUBox, 1, (cuuint32_t)R};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(U), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+bool draft_tc_supported(int wdtype, int r) { return wdtype == DSPARK_BF16 && r == KR; }
+
+cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
+  const WsLayout L = ws_layout(a.B, a.gamma, a.V);
+  int* status = ws_ptr<int>(a.ws, L.status);
+  unsigned long long* keys = ws_ptr<unsigned long long>(a.ws, L.draft_keys);
+  float2* part = ws_ptr<float2>(a.ws, L.draft_part);
+  const int part_slices = draft_num_slices(a.V);
+
+  CUtensorMap map;
+  cudaError_t e = make_w2_tensor_map(a.W2, a.V, &map);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int R = a.B <= 32 ? 32 : (a.B <= 64 ? 64 : BM);
+  CUtensorMap umap;
+  if ((e = make_u_tensor_map(a.U, a.B, a.gamma, a.V, R, &umap)) != cudaSuccess) return e;
+  auto kern = R == 32 ? draft_step_tc<32, kDraft> : (R == 64 ? draft_step_tc<64, kDraft> : draft_step_tc<BM, kDraft>);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * (size_t)a.gamma * a.B, stream);
+  if (e != cudaSuccess) return e;
+
+  const int mtiles = div_up(a.B, R);
+  const int ntiles = div_up(a.V, BN);
+  int per = std::max(1, sms / mtiles);
+  per = std::min(per, std::min(ntiles, part_slices));
+  StepParams sp{};
+  sp.U = a.U;
+  sp.W1 = static_cast<const __nv_bfloat16*>(a.W1);
+  sp.anchor = a.anchor;
+  sp.status = status;
+  sp.B = a.B; sp.G = a.gamma; sp.V = a.V;
+  sp.ctas_per_mtile = per;
+  sp.ntiles = ntiles;
+  sp.key = a.key;
+  for (int k = 1; k <= a.gamma; ++k) {
+    sp.k = k;
+    sp.keys_prev = (k >= 2) ? keys + (size_t)(k - 2) * a.B : nullptr;
+    sp.keys_cur = keys + (size_t)(k - 1) * a.B;
+    sp.part = part + (size_t)(k - 1) * part_slices * a.B;
+    kern<<<mtiles * per, kThreads, kSmemBytes, stream>>>(map, umap, sp);
+  }
+  draft_finalize_tc<<<div_up(a.B * a.gamma * 32, 256), 256, 0, stream>>>(
+      a.U, static_cast<const __nv_bfloat16*>(a.W1), static_cast<const __nv_bfloat16*>(a.W2), a.anchor, keys,
+      part, a.B, a.gamma, a.V, per, part_slices, a.x_out, a.p_out, a.lse_out, status);
+  return cudaGetLastError();
+}
+
+// The residual resample of every rejecting request on the tensor cores: the
+// bias of W1[x_{k*-1}] against all of W2 again (one GEMM, as for a draft
+// position), p_d = exp(U + bias - lse_d), p_t = exp(T - lse_t), and a Gumbel
+// race over log max(0, p_t - p_d) into resid_key (atomicMax).
+cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
+                               const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* resid_k,
+                               const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
+                               RngKey key, int* status, cudaStream_t stream) {
+  CUtensorMap map;
+  cudaError_t e = make_w2_tensor_map(W2, V, &map);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int R = B <= 32 ? 32 : (B <= 64 ? 64 : BM);
+  auto kern = R == 32 ? draft_step_tc<32, kResidual>
+                      : (R == 64 ? draft_step_tc<64, kResidual> : draft_step_tc<BM, kResidual>);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int mtiles = div_up(B, R);
+  const int ntiles = div_up(V, BN);
+  int per = std::max(1, sms / mtiles);
+  per = std::min(per, ntiles);
+  StepParams sp{};
+  sp.U = U;
+  sp.W1 = static_cast<const __nv_bfloat16*>(W1);
+  sp.anchor = anchor;
+  sp.T = T;
+  sp.x = x;
+  sp.resid_k = resid_k;
+  sp.lse_d = lse_d;
+  sp.resid_lse = resid_lse;
+  sp.resid_key = resid_key;
+  sp.status = status;
+  sp.B = B; sp.G = G; sp.V = V; sp.k = 0;
+  sp.ctas_per_mtile = per;
+  sp.ntiles = ntiles;
+  sp.key = key;
+  // the U map is not read in this mode; any valid map will do
+  kern<<<mtiles * per, kThreads, kSmemBytes, stream>>>(map, map, sp);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

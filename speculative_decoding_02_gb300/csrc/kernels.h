@@ -43,6 +43,14 @@ struct VerifyArgs {
 
 cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream);
 
+// Tensor-core draft (bf16 weights, r = 256); the dispatcher above picks it.
+bool draft_tc_supported(int wdtype, int r);
+cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream);
+cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
+                               const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* resid_k,
+                               const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
+                               RngKey key, int* status, cudaStream_t stream);
+
 cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdtype,
                               const float* w, const float* sts_T, const int32_t* anchor,
                               const int32_t* x, int B, int gamma, int H, int r, int V,

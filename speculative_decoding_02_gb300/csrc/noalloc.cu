@@ -54,7 +54,7 @@ cudaError_t scratch_address(void** out) {
 // per-position argmax keys and the per-slice softmax partials.
 size_t draft_scratch_bytes(int B, int gamma, int V) {
   const WsLayout L = ws_layout(B, gamma, V);
-  return L.draft_part + 8ull * gamma * (size_t)draft_num_slices(V) * B;
+  return L.draft_part + 8ull * gamma * (size_t)draft_part_slices(V) * B;
 }
 
 }  // namespace

@@ -183,7 +183,7 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
                           const int32_t* __restrict__ resid_k, const float* __restrict__ resid_lse,
                           unsigned long long* __restrict__ resid_key, int* __restrict__ status) {
   extern __shared__ float Es[];   // [r]
-  __shared__ unsigned long long s_k1[kRowThreads / 32], s_k2[kRowThreads / 32];
+  __shared__ unsigned long long s_k1[kRowThreads / 32];
   const int b = blockIdx.y;
   const int ks = resid_k[b];
   if (ks <= 0) return;
@@ -196,7 +196,7 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
   const float ld = lse_d[(size_t)b * G + ks - 1];
   const float lt = resid_lse[b];
   const int v_begin = blockIdx.x * kDraftSlice, v_end = min(V, v_begin + kDraftSlice);
-  unsigned long long k1 = 0ull, k2 = 0ull;
+  unsigned long long k1 = 0ull;
   for (int v4 = v_begin + 4 * tid; v4 < v_end; v4 += 4 * kRowThreads) {
     const uint4 rw = rng4(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v4 >> 2));
     const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
@@ -206,45 +206,60 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
       float bias = 0.f;
       for (int i = 0; i < r; ++i) bias = fmaf(Es[i], load_weight<WDT>(W2, (size_t)v * r + i), bias);
       const float pd = expf(Urow[v] + bias - ld);
-      const float lt_v = Trow[v] - lt;
-      const float pt = expf(lt_v);
+      const float pt = expf(Trow[v] - lt);
       const float rho = pt - pd;
-      const float g = gumbel_noise(words[q]);
       if (rho > 0.f) {
-        const unsigned long long kz = argmax_key(logf(rho) + g, v);
+        const unsigned long long kz = argmax_key(logf(rho) + gumbel_noise(words[q]), v);
         k1 = kz > k1 ? kz : k1;
       }
-      const unsigned long long kf = argmax_key(lt_v + g, v);
-      k2 = kf > k2 ? kf : k2;
     }
   }
   k1 = warp_max_u64(k1, 0xffffffffu, 32);
-  k2 = warp_max_u64(k2, 0xffffffffu, 32);
-  if (lane == 0) {
-    s_k1[wid] = k1;
-    s_k2[wid] = k2;
-  }
+  if (lane == 0) s_k1[wid] = k1;
   __syncthreads();
   if (tid == 0) {
-    for (int w = 1; w < kRowThreads / 32; ++w) {
-      k1 = s_k1[w] > k1 ? s_k1[w] : k1;
-      k2 = s_k2[w] > k2 ? s_k2[w] : k2;
-    }
-    k1 = s_k1[0] > k1 ? s_k1[0] : k1;
-    k2 = s_k2[0] > k2 ? s_k2[0] : k2;
+    for (int w = 1; w < kRowThreads / 32; ++w) k1 = s_k1[w] > k1 ? s_k1[w] : k1;
     if (k1) atomicMax(&resid_key[b], k1);
-    atomicMax(&resid_key[B + b], k2);
   }
 }
 
-__global__ void verify_residual_finalize(int B, const int32_t* __restrict__ resid_k,
-                                         const unsigned long long* __restrict__ resid_key,
-                                         int32_t* __restrict__ tok_out, int* __restrict__ status) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B || resid_k[b] <= 0) return;
-  const unsigned long long k1 = resid_key[b], k2 = resid_key[B + b];
-  if (k1 == 0ull && k2 == 0ull) record_status(status, DSPARK_ERR_NONFINITE);
-  tok_out[b] = k1 ? argmax_key_index(k1) : (k2 ? argmax_key_index(k2) : 0);
+// One block per request.  A rejecting request takes the winner of the residual
+// race; if the residual had no positive entry in floating point (a measure-zero
+// event in exact arithmetic) it draws from p_t instead, with the same noise.
+__global__ void __launch_bounds__(kRowThreads)
+verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKey key,
+                         const int32_t* __restrict__ resid_k, const unsigned long long* __restrict__ resid_key,
+                         int32_t* __restrict__ tok_out, int* __restrict__ status) {
+  __shared__ unsigned long long s_k[kRowThreads / 32];
+  const int b = blockIdx.x;
+  const int ks = resid_k[b];
+  if (ks <= 0) return;
+  const unsigned long long k1 = resid_key[b];
+  if (k1) {
+    if (threadIdx.x == 0) tok_out[b] = argmax_key_index(k1);
+    return;
+  }
+  const float* Trow = T + ((size_t)b * (G + 1) + (ks - 1)) * (size_t)V;
+  unsigned long long best = 0ull;
+  for (int v = 4 * threadIdx.x; v < V; v += 4 * kRowThreads) {
+    const float4 t4 = *reinterpret_cast<const float4*>(Trow + v);
+    const uint4 rw = rng4(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v >> 2));
+    const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+    const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const unsigned long long kz = argmax_key(tv[q] + gumbel_noise(words[q]), v + q);
+      best = kz > best ? kz : best;
+    }
+  }
+  best = warp_max_u64(best, 0xffffffffu, 32);
+  if ((threadIdx.x & 31) == 0) s_k[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kRowThreads / 32; ++w) best = s_k[w] > best ? s_k[w] : best;
+    if (!best) record_status(status, DSPARK_ERR_NONFINITE);
+    tok_out[b] = best ? argmax_key_index(best) : 0;
+  }
 }
 
 template <int WDT>
@@ -272,11 +287,18 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   verify_decide<<<div_up(a.B * 32, 256), 256, 0, stream>>>(a.T, a.x, a.p_d, a.ell, a.B, a.gamma, a.V, nsegs,
                                                           a.key, row_part, bonus_key, resid_k, resid_lse,
                                                           a.n_out, a.tok_out, status);
-  const dim3 grid_res(draft_num_slices(a.V), a.B);
-  verify_residual_cuda_core<WDT><<<grid_res, kRowThreads, sizeof(float) * a.r, stream>>>(
-      a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, a.B, a.gamma, a.V, a.r, a.key, resid_k, resid_lse,
-      resid_key, status);
-  verify_residual_finalize<<<div_up(a.B, 256), 256, 0, stream>>>(a.B, resid_k, resid_key, a.tok_out, status);
+  if (draft_tc_supported(a.wdtype, a.r)) {
+    e = launch_residual_tc(a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, resid_k, resid_lse, resid_key, a.B,
+                           a.gamma, a.V, a.key, status, stream);
+    if (e != cudaSuccess) return e;
+  } else {
+    const dim3 grid_res(draft_num_slices(a.V), a.B);
+    verify_residual_cuda_core<WDT><<<grid_res, kRowThreads, sizeof(float) * a.r, stream>>>(
+        a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, a.B, a.gamma, a.V, a.r, a.key, resid_k, resid_lse,
+        resid_key, status);
+  }
+  verify_residual_finalize<<<a.B, kRowThreads, 0, stream>>>(a.T, a.B, a.gamma, a.V, a.key, resid_k, resid_key,
+                                                           a.tok_out, status);
   return cudaGetLastError();
 }
 

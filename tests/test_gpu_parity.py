@@ -63,6 +63,12 @@ SMALL = [
     (33, 3, 9216, 32, 64, torch.bfloat16, wl.MODE_FIXED),
     (7, 8, 2056, 16, 32, torch.float32, wl.MODE_GREEDY),
     (3, 32, 1032, 256, 256, torch.bfloat16, wl.MODE_FIXED),
+    # r = 256 with bf16 weights runs the tensor-core draft: ragged last vocab
+    # tile, two M tiles with a ragged second one, several tiles per CTA
+    (40, 5, 5000, 256, 128, torch.bfloat16, wl.MODE_GREEDY),
+    (130, 3, 2056, 256, 64, torch.bfloat16, wl.MODE_FIXED),
+    (33, 2, 16384, 256, 64, torch.bfloat16, wl.MODE_GREEDY),
+    (128, 4, 65536, 256, 64, torch.bfloat16, wl.MODE_FIXED),
 ]
 
 
