@@ -21,41 +21,47 @@ constexpr uint32_t kPhiloxMulB = 0xCD9E8D57u;
 constexpr uint32_t kPhiloxWeylA = 0x9E3779B9u;
 constexpr uint32_t kPhiloxWeylB = 0xBB67AE85u;
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int i = 0; i < 10; ++i) {
-    const uint32_t lo_a = kPhiloxMulA * c.x;
-    const uint32_t hi_a = __umulhi(kPhiloxMulA, c.x);
-    const uint32_t lo_b = kPhiloxMulB * c.z;
-    const uint32_t hi_b = __umulhi(kPhiloxMulB, c.z);
-    c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
-    k0 += kPhiloxWeylA;
-    k1 += kPhiloxWeylB;
-  }
-  return c;
-}
-
 // Random-number streams of one round (the fourth counter word is
 // (round << 3) | stream).
 enum Stream : uint32_t { kStreamDraft = 0, kStreamAccept = 1, kStreamResidual = 2, kStreamBonus = 3 };
 
+// The key of one round with its ten round keys precomputed on the host, so
+// that kernels read them as constant operands instead of recomputing the
+// Weyl sequence per call.
 struct RngKey {
-  uint32_t k0, k1;   // seed low / high word
-  uint32_t round3;   // round << 3
+  uint32_t rk0[10], rk1[10];   // round i uses (seed_lo + i A, seed_hi + i B)
+  uint32_t round3;             // round << 3
 };
 
 __host__ __device__ inline RngKey make_rng_key(uint64_t seed, uint64_t round) {
   RngKey k;
-  k.k0 = (uint32_t)(seed & 0xffffffffu);
-  k.k1 = (uint32_t)(seed >> 32);
+  uint32_t k0 = (uint32_t)(seed & 0xffffffffu), k1 = (uint32_t)(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    k.rk0[i] = k0;
+    k.rk1[i] = k1;
+    k0 += kPhiloxWeylA;
+    k1 += kPhiloxWeylB;
+  }
   k.round3 = (uint32_t)(round << 3);
   return k;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const RngKey& key) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    // one 32x32 -> 64-bit product gives both halves
+    const uint64_t pa = (uint64_t)kPhiloxMulA * c.x;
+    const uint64_t pb = (uint64_t)kPhiloxMulB * c.z;
+    c = make_uint4((uint32_t)(pb >> 32) ^ c.y ^ key.rk0[i], (uint32_t)pb, (uint32_t)(pa >> 32) ^ c.w ^ key.rk1[i],
+                   (uint32_t)pa);
+  }
+  return c;
 }
 
 // The four words for vocabulary entries 4q .. 4q+3 of (stream, request, position).
 __device__ __forceinline__ uint4 rng4(const RngKey& key, uint32_t stream, uint32_t req,
                                       uint32_t pos, uint32_t q) {
-  return philox4x32_10(make_uint4(q, pos, req, key.round3 | stream), key.k0, key.k1);
+  return philox4x32_10(make_uint4(q, pos, req, key.round3 | stream), key);
 }
 
 // Uniform (2m + 1) / 2^24 with m the top 23 bits of w: exact in float32.

@@ -41,14 +41,16 @@ constexpr int kAtoms = KR / 64;     // 64-wide K atoms (128 bytes of bf16)
 constexpr int kWStages = 6;         // W2 atom ring
 constexpr int kUStages = 3;         // U tile ring
 constexpr int kUBox = 32;           // fp32 columns per U box (128 bytes, swizzled)
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
+constexpr int kThreads = 576;
+constexpr int kEpiWarps = 16;       // four warps per TMEM lane quarter
 constexpr uint32_t kTmemCols = 128;  // two 64-column accumulators
 
 constexpr int kEBytes = kAtoms * BM * 128;       // 65536
 constexpr int kWStageBytes = BN * 128;           // 8192
 constexpr int kUStageBytes = BN * BM * 4;        // 32768: two [rows x 32] boxes
-constexpr int kSmemBytes = 1024 /*align*/ + kEBytes + kWStages * kWStageBytes + kUStages * kUStageBytes + 256;
+constexpr int kXBytes = 4 * BM * (4 + 4 + 8);     // combine scratch: 4 parts x 128 rows
+constexpr int kSmemBytes =
+    1024 /*align*/ + kEBytes + kWStages * kWStageBytes + kUStages * kUStageBytes + 256 + kXBytes;
 
 struct __align__(8) Barriers {
   uint64_t full_w[kWStages], empty_w[kWStages];
@@ -57,6 +59,7 @@ struct __align__(8) Barriers {
   uint64_t e_full, drain;
   uint32_t tmem_base;
   int abort;
+  int stop;   // epilogue-wide decision to leave the position loop
 };
 
 enum Mode { kDraft = 0, kResidual = 1 };
@@ -73,11 +76,14 @@ struct StepParams {
   const float* lse_d;
   const float* resid_lse;
   unsigned long long* resid_key;
-  const unsigned long long* keys_prev;  // argmax keys of position k-1 (k >= 2)
-  unsigned long long* keys_cur;         // argmax keys of position k
-  float2* part;                         // [nslices][B] partials of position k
+  unsigned long long* keys;             // [G][B] argmax keys of every position
+  float2* part;                         // [G][part_slices][B] softmax partials
+  unsigned int* gbar;                   // grid-barrier counter (zeroed before launch)
   int* status;
-  int B, G, V, k;
+  int B, G, V;
+  int k_first, k_last;                  // draft positions of this launch
+  int part_slices;
+  int nctas;                            // CTAs of the grid
   int ctas_per_mtile;
   int ntiles;                           // vocabulary tiles of width BN
   RngKey key;
@@ -98,9 +104,11 @@ __device__ __forceinline__ int tile_begin(int slice, int nslices, int ntiles) {
 // thousand once zbest has settled) get the two exact logarithms.
 struct RowRace {
   float run_m, run_s;   // online softmax: running max and sum of exp(l - run_m)
-  float zbest;          // best perturbed logit so far
+  float zbest;          // best perturbed logit of this thread's entries
   int best_v;           // its vocabulary index
-  float bound;          // exp(run_m - zbest) with a 2^-10 safety margin
+  float zthr;           // best perturbed logit known anywhere in the row (>= zbest)
+  float zpub;           // zbest as last published to the row's global key
+  float bound;          // exp(run_m - zthr) with a 2^-10 safety margin
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -113,16 +121,23 @@ __device__ __forceinline__ uint32_t pick_word(const uint4& w, int j) {
   return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
 }
 
-// Folds the fused logits l[0..nv) of columns v0.. into the race.  `spill` is
-// this thread's 128-byte swizzled shared-memory row (chunks j0.., xor `sw`)
-// where the logits are parked when a candidate needs its exact perturbed logit.
+// Folds the fused logits l[0..nv) of columns v0.. into the race.  Candidates
+// are resolved as they are met, with the random word and logit still in
+// registers, and each one that wins tightens the bound for the rest.  The
+// bound uses zthr, the best perturbed logit known for the whole row (this
+// thread's own or one published by any CTA): an entry below it cannot win.
 template <int CPP>
 __device__ __forceinline__ void race_tile(RowRace& st, float (&l)[CPP], int nv, int v0, unsigned char* spill,
                                           int j0, int sw, const RngKey& key, uint32_t req, uint32_t pos) {
   float tm = -INFINITY;
+  if (nv >= CPP) {
 #pragma unroll
-  for (int c = 0; c < CPP; ++c)
-    if (c < nv) tm = fmaxf(tm, l[c]);
+    for (int c = 0; c < CPP; ++c) tm = fmaxf(tm, l[c]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < CPP; ++c)
+      if (c < nv) tm = fmaxf(tm, l[c]);
+  }
   if (tm > st.run_m) {
     st.run_s = (st.run_m == -INFINITY) ? 0.f : st.run_s * exp2f((st.run_m - tm) * kLog2e);
     st.run_m = tm;
@@ -136,11 +151,11 @@ __device__ __forceinline__ void race_tile(RowRace& st, float (&l)[CPP], int nv, 
       const uint4 rw = rng4(key, kStreamDraft, req, pos, (uint32_t)(v >> 2));
       st.zbest = tm + gumbel_noise(pick_word(rw, v & 3));
       st.best_v = v;
+      st.zthr = fmaxf(st.zthr, st.zbest);
     }
-    st.bound = race_bound(st.run_m, st.zbest);
+    st.bound = race_bound(st.run_m, st.zthr);
   }
   const float mb = st.run_m * kLog2e;
-  uint32_t cand = 0;
 #pragma unroll
   for (int g = 0; g < CPP / 4; ++g) {
     if (4 * g < nv) {
@@ -149,33 +164,27 @@ __device__ __forceinline__ void race_tile(RowRace& st, float (&l)[CPP], int nv, 
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = 4 * g + j;
-        const float e = exp2f(fmaf(l[c], kLog2e, -mb));
+        const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
         st.run_s += e;
         // 1 + m 2^-23 with m the top 23 random bits: 2 - up = 1 - u + 2^-24
         const float up = __uint_as_float((words[j] >> 9) | 0x3F800000u);
         const float thr = fmaf(-e, st.bound, 0x1.fffffcp0f);
-        if (up > thr) cand |= 1u << c;
+        if (up > thr) {
+          // a candidate: its exact perturbed logit decides
+          const float z = l[c] + gumbel_noise(words[j]);
+          if (z > st.zbest) {
+            st.zbest = z;
+            st.best_v = v0 + c;
+            if (z > st.zthr) {
+              st.zthr = z;
+              st.bound = race_bound(st.run_m, st.zthr);
+            }
+          }
+        }
       }
     }
   }
-  if (cand) {
-#pragma unroll
-    for (int c = 0; c < CPP; c += 4)
-      *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(l[c], l[c + 1], l[c + 2], l[c + 3]);
-    while (cand) {
-      const int c = __ffs(cand) - 1;
-      cand &= cand - 1;
-      const int v = v0 + c;
-      const uint4 rw = rng4(key, kStreamDraft, req, pos, (uint32_t)(v >> 2));
-      const float lc = reinterpret_cast<const float*>(spill + (((j0 + c / 4) ^ sw) << 4))[c & 3];
-      const float z = lc + gumbel_noise(pick_word(rw, v & 3));
-      if (z > st.zbest) {
-        st.zbest = z;
-        st.best_v = v;
-        st.bound = race_bound(st.run_m, st.zbest);
-      }
-    }
-  }
+  (void)spill; (void)j0; (void)sw;
 }
 
 // Race of the residual resample: argmax_v log rho_v + G_v over rho_v > 0,
@@ -241,7 +250,38 @@ __device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP],
 // holds 128 / R copies of the requests so that every TMEM lane quarter -- and
 // so every epilogue warp -- has rows to work on; each copy takes its own share
 // of the tile's columns.
-// MODE kDraft: one draft position for every request (U rows by TMA).
+// Grid-wide barrier between draft positions.  Every CTA adds 1 to a counter in
+// global memory after publishing its position-k results; the CTA then waits,
+// bounded in time, until all `nctas` CTAs have arrived for this position.
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned int* counter, uint32_t target, volatile int* abort,
+                                             int* status) {
+  __threadfence();
+  atomicAdd(counter, 1u);
+  const uint64_t t0 = globaltimer();
+  while (ld_acquire_u32(counter) < target) {
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_status(status, DSPARK_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// MODE kDraft: draft positions k_first..k_last for every request (U rows by
+// TMA).  With more than one position the CTAs of the grid must be co-resident
+// (cooperative launch): after each position they meet at a grid barrier so
+// that the next position can read x_k from the argmax keys.  The producer and
+// the MMA pipelines run on across positions, so the U and W2 tiles of the next
+// position are already loading while the barrier resolves.
 // MODE kResidual: for every request that rejected at position k*, the fused
 // draft logits of k* again, raced over log max(0, p_t - p_d) (U and T rows
 // read directly by the epilogue threads).
@@ -250,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
               const StepParams p) {
   constexpr int kRepl = BM / R;            // copies of each request row
-  constexpr int kParts = 2 * kRepl;        // column parts of a tile
+  constexpr int kParts = 4 * kRepl;        // column parts of a tile
   constexpr int CPP = BN / kParts;         // columns per thread per tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -258,6 +298,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   unsigned char* W_s = E_s + kEBytes;
   unsigned char* U_s = W_s + kWStages * kWStageBytes;
   Barriers* bars = reinterpret_cast<Barriers*>(U_s + kUStages * kUStageBytes);
+  unsigned char* X_s = reinterpret_cast<unsigned char*>(bars) + 256;   // combine scratch
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mtile = blockIdx.x / p.ctas_per_mtile;
@@ -267,6 +308,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   const int t0 = tile_begin(slice, p.ctas_per_mtile, p.ntiles);
   const int t1 = tile_begin(slice + 1, p.ctas_per_mtile, p.ntiles);
   const int ntl = t1 - t0;
+  const int kf = p.k_first, kl = p.k_last;
   volatile int* abort = &bars->abort;
 
   if (threadIdx.x == 0) {
@@ -280,7 +322,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&w2_map);
-    prefetch_tensormap(&u_map);
+    if (MODE == kDraft) prefetch_tensormap(&u_map);
   }
   if (warp == 1) tmem_alloc(&bars->tmem_base, kTmemCols);
   tc_fence_before();
@@ -293,32 +335,32 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     const uint64_t pol_w = policy_evict_last(), pol_u = policy_evict_first();
     uint32_t wcount = 0, ucount = 0;
     bool ok = true;
-    for (int i = 0; i < ntl && ok; ++i) {
-      const int v0 = (t0 + i) * BN;
-      const int ncols = min(BN, p.V - v0);
-      for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
-        const int s = wcount % kWStages;
-        ok = mbar_wait(&bars->empty_w[s], ((wcount / kWStages) & 1) ^ 1, abort, p.status);
-        if (ok && lane == 0) {
-          mbar_arrive_expect_tx(&bars->full_w[s], kWStageBytes);
-          tma_g2s_2d(W_s + s * kWStageBytes, &w2_map, a * 64, v0, &bars->full_w[s], pol_w);
+    for (int k = kf; k <= kl && ok; ++k) {
+      for (int i = 0; i < ntl && ok; ++i) {
+        const int v0 = (t0 + i) * BN;
+        for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
+          const int s = wcount % kWStages;
+          ok = mbar_wait(&bars->empty_w[s], ((wcount / kWStages) & 1) ^ 1, abort, p.status);
+          if (ok && lane == 0) {
+            mbar_arrive_expect_tx(&bars->full_w[s], kWStageBytes);
+            tma_g2s_2d(W_s + s * kWStageBytes, &w2_map, a * 64, v0, &bars->full_w[s], pol_w);
+          }
         }
+        if (!ok) break;
+        if constexpr (MODE == kResidual) continue;
+        const int su = ucount % kUStages;
+        ok = mbar_wait(&bars->empty_u[su], ((ucount / kUStages) & 1) ^ 1, abort, p.status);
+        if (!ok) break;
+        if (lane == 0) {
+          // two [R rows x 32 columns] boxes of U[m0.., k-1, v0..]; rows past B and
+          // columns past V are filled with zeros by the copy engine
+          mbar_arrive_expect_tx(&bars->full_u[su], (uint32_t)(2 * kUBox * R * 4));
+          unsigned char* dst = U_s + su * kUStageBytes;
+          tma_g2s_3d(dst, &u_map, v0, k - 1, m0, &bars->full_u[su], pol_u);
+          tma_g2s_3d(dst + R * 128, &u_map, v0 + kUBox, k - 1, m0, &bars->full_u[su], pol_u);
+        }
+        ++ucount;
       }
-      if (!ok) break;
-      if constexpr (MODE == kResidual) continue;
-      const int su = ucount % kUStages;
-      ok = mbar_wait(&bars->empty_u[su], ((ucount / kUStages) & 1) ^ 1, abort, p.status);
-      if (!ok) break;
-      if (lane == 0) {
-        // two [R rows x 32 columns] boxes of U[m0.., k-1, v0..]; rows past B and
-        // columns past V are filled with zeros by the copy engine
-        mbar_arrive_expect_tx(&bars->full_u[su], (uint32_t)(2 * kUBox * R * 4));
-        unsigned char* dst = U_s + su * kUStageBytes;
-        tma_g2s_3d(dst, &u_map, v0, p.k - 1, m0, &bars->full_u[su], pol_u);
-        tma_g2s_3d(dst + R * 128, &u_map, v0 + kUBox, p.k - 1, m0, &bars->full_u[su], pol_u);
-      }
-      (void)ncols;
-      ++ucount;
     }
     // drain: every copy this warp issued has landed before the CTA exits
     if (lane == 0 && *abort) {
@@ -332,30 +374,33 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(BM, BN);
       const uint32_t e_addr = smem_u32(E_s);
-      uint32_t wcount = 0;
-      bool ok = mbar_wait(&bars->e_full, 0, abort, p.status);
-      tc_fence_after();
-      for (int i = 0; i < ntl && ok; ++i) {
-        const int acc = i & 1;
-        ok = mbar_wait(&bars->acc_empty[acc], ((i >> 1) & 1) ^ 1, abort, p.status);
-        if (!ok) break;
+      uint32_t wcount = 0, it = 0;
+      bool ok = true;
+      for (int k = kf; k <= kl && ok; ++k) {
+        ok = mbar_wait(&bars->e_full, (uint32_t)(k - kf) & 1, abort, p.status);
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * BN;
-        for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
-          const int s = wcount % kWStages;
-          ok = mbar_wait(&bars->full_w[s], (wcount / kWStages) & 1, abort, p.status);
+        for (int i = 0; i < ntl && ok; ++i, ++it) {
+          const int acc = it & 1;
+          ok = mbar_wait(&bars->acc_empty[acc], ((it >> 1) & 1) ^ 1, abort, p.status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t w_addr = smem_u32(W_s + s * kWStageBytes);
+          const uint32_t d_tmem = tmem + acc * BN;
+          for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
+            const int s = wcount % kWStages;
+            ok = mbar_wait(&bars->full_w[s], (wcount / kWStages) & 1, abort, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t w_addr = smem_u32(W_s + s * kWStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sw128_kmajor_desc(e_addr + a * (BM * 128) + kk * 32);
-            const uint64_t bd = sw128_kmajor_desc(w_addr + kk * 32);
-            umma_bf16(d_tmem, ad, bd, idesc, (a | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sw128_kmajor_desc(e_addr + a * (BM * 128) + kk * 32);
+              const uint64_t bd = sw128_kmajor_desc(w_addr + kk * 32);
+              umma_bf16(d_tmem, ad, bd, idesc, (a | kk) != 0);
+            }
+            umma_commit(&bars->empty_w[s]);
           }
-          umma_commit(&bars->empty_w[s]);
+          if (ok) umma_commit(&bars->acc_full[acc]);
         }
-        if (ok) umma_commit(&bars->acc_full[acc]);
       }
       // all MMAs this thread issued are complete before TMEM is released
       umma_commit(&bars->drain);
@@ -365,142 +410,175 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;               // TMEM lane quarter of this warp
-    const int h = (warp - 2) >> 2;        // which of the two warps of the quarter
+    const int h = (warp - 2) >> 2;        // which of the four warps of the quarter
     const int m = q * 32 + lane;          // TMEM lane = row of the M tile
     const int rep = m / R, r = m - rep * R;
-    const int part = rep * 2 + h;         // column part of every tile
+    const int part = rep * 4 + h;         // column part of every tile
     const int b = m0 + r;
-    bool active = r < rows_valid;
-    int ks = p.k;                         // position of this row
-    if constexpr (MODE == kResidual) {
-      ks = active ? p.resid_k[b] : 0;
-      active = ks > 0;
-    }
+    float* xm = reinterpret_cast<float*>(X_s);
+    float* xs = xm + 4 * BM;
+    unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 4 * BM);
+    float* spill = reinterpret_cast<float*>(U_s + ((warp - 2) * 32 + lane) * 144);
+    uint32_t it = 0;
+    for (int k = kf; k <= kl; ++k) {
+      bool active = r < rows_valid;
+      int ks = k;                           // position of this row
+      if constexpr (MODE == kResidual) {
+        ks = active ? p.resid_k[b] : 0;
+        active = ks > 0;
+      }
 
-    // gather E[m, :] = W1[x_{k-1}] for K atoms 2h, 2h+1 (16-byte chunks, swizzled)
-    int prev = 0;
-    if (active) {
-      int raw;
-      if constexpr (MODE == kDraft)
-        raw = (p.k == 1) ? p.anchor[b] : argmax_key_index(p.keys_prev[b]);
-      else
-        raw = (ks == 1) ? p.anchor[b] : p.x[(size_t)b * p.G + ks - 2];
-      prev = checked_token(raw, p.V, p.status);
-    }
-    const uint4* wrow = reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * KR);
-#pragma unroll
-    for (int a2 = 0; a2 < 2; ++a2) {
-      const int a = 2 * h + a2;
+      // gather E[m, :] = W1[x_{k-1}] for K atom h (16-byte chunks, swizzled)
+      int prev = 0;
+      if (active) {
+        int raw;
+        if constexpr (MODE == kDraft)
+          raw = (k == 1) ? p.anchor[b] : argmax_key_index(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+        else
+          raw = (ks == 1) ? p.anchor[b] : p.x[(size_t)b * p.G + ks - 2];
+        prev = checked_token(raw, p.V, p.status);
+      }
+      const uint4* wrow = reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * KR);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint4 val = active ? __ldg(wrow + a * 8 + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(E_s + a * (BM * 128) + m * 128 + ((c ^ (m & 7)) << 4)) = val;
+        const uint4 val = active ? __ldg(wrow + h * 8 + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(E_s + h * (BM * 128) + m * 128 + ((c ^ (m & 7)) << 4)) = val;
       }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->e_full);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->e_full);
 
-    RowRace st{-INFINITY, 0.f, -INFINITY, -1, INFINITY};
-    ResRace rs{-INFINITY, -1, INFINITY};
-    float ld2 = 0.f, lt2 = 0.f;
-    const float* Urow = nullptr;
-    const float* Trow = nullptr;
-    float* spill = reinterpret_cast<float*>(U_s + ((warp - 2) * 32 + lane) * 144);
-    if constexpr (MODE == kResidual) {
-      if (active) {
-        ld2 = p.lse_d[(size_t)b * p.G + ks - 1] * kLog2e;
-        lt2 = p.resid_lse[b] * kLog2e;
-        Urow = p.U + ((size_t)b * p.G + (ks - 1)) * (size_t)p.V;
-        Trow = p.T + ((size_t)b * (p.G + 1) + (ks - 1)) * (size_t)p.V;
-      }
-    }
-    for (int i = 0; i < ntl; ++i) {
-      const int acc_i = i & 1;
-      const int v0 = (t0 + i) * BN + part * CPP;
-      const int nv = min(CPP, p.V - v0);
-      float uu[CPP], tt[CPP];
+      RowRace st{-INFINITY, 0.f, -INFINITY, -1, -INFINITY, -INFINITY, INFINITY};
+      // rows shared by many threads (small batches replicated across the tile)
+      // would turn the exchange into a hot spot: only full 128-row tiles use it
+      constexpr bool kShare = (MODE == kDraft) && (R == BM);
+      unsigned long long* row_key = (kShare && active) ? p.keys + (size_t)(k - 1) * p.B + b : nullptr;
+      ResRace rs{-INFINITY, -1, INFINITY};
+      float ld2 = 0.f, lt2 = 0.f;
+      const float* Urow = nullptr;
+      const float* Trow = nullptr;
       if constexpr (MODE == kResidual) {
-        // issue this tile's row loads before waiting for the accumulator
-        if (active && nv > 0) {
+        if (active) {
+          ld2 = p.lse_d[(size_t)b * p.G + ks - 1] * kLog2e;
+          lt2 = p.resid_lse[b] * kLog2e;
+          Urow = p.U + ((size_t)b * p.G + (ks - 1)) * (size_t)p.V;
+          Trow = p.T + ((size_t)b * (p.G + 1) + (ks - 1)) * (size_t)p.V;
+        }
+      }
+      bool ok = true;
+      for (int i = 0; i < ntl; ++i, ++it) {
+        const int acc_i = it & 1;
+        const int v0 = (t0 + i) * BN + part * CPP;
+        const int nv = min(CPP, p.V - v0);
+        float uu[CPP], tt[CPP];
+        if constexpr (MODE == kResidual) {
+          // issue this tile's row loads before waiting for the accumulator
+          if (active && nv > 0) {
 #pragma unroll
-          for (int c = 0; c < CPP; c += 4) {
-            if (c < nv) {
-              const float4 u4 = __ldcs(reinterpret_cast<const float4*>(Urow + v0 + c));
-              const float4 t4 = __ldcs(reinterpret_cast<const float4*>(Trow + v0 + c));
-              uu[c] = u4.x; uu[c + 1] = u4.y; uu[c + 2] = u4.z; uu[c + 3] = u4.w;
-              tt[c] = t4.x; tt[c + 1] = t4.y; tt[c + 2] = t4.z; tt[c + 3] = t4.w;
+            for (int c = 0; c < CPP; c += 4) {
+              if (c < nv) {
+                const float4 u4 = __ldcs(reinterpret_cast<const float4*>(Urow + v0 + c));
+                const float4 t4 = __ldcs(reinterpret_cast<const float4*>(Trow + v0 + c));
+                uu[c] = u4.x; uu[c + 1] = u4.y; uu[c + 2] = u4.z; uu[c + 3] = u4.w;
+                tt[c] = t4.x; tt[c + 1] = t4.y; tt[c + 2] = t4.z; tt[c + 3] = t4.w;
+              }
             }
           }
         }
-      }
-      if (!mbar_wait(&bars->acc_full[acc_i], (i >> 1) & 1, abort, p.status)) break;
-      tc_fence_after();
-      float v[CPP];
-      tmem_load_cols<CPP>(tmem + ((uint32_t)(q * 32) << 16) + acc_i * BN + part * CPP, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->acc_empty[acc_i]);
-      if constexpr (MODE == kDraft) {
-        const int su = i % kUStages;
-        if (!mbar_wait(&bars->full_u[su], (i / kUStages) & 1, abort, p.status)) break;
-        // this thread's columns: box (part*CPP)/32, 16-byte chunks j0.. of row r,
-        // stored at chunk j ^ (r & 7) (128-byte swizzle)
-        unsigned char* urow = U_s + su * kUStageBytes + ((part * CPP) / kUBox) * (R * 128) + r * 128;
-        const int j0 = ((part * CPP) % kUBox) / 4;
-        if (active && nv > 0) {
-#pragma unroll
-          for (int c = 0; c < CPP; c += 4) {
-            const float4 u4 = *reinterpret_cast<const float4*>(urow + (((j0 + c / 4) ^ (r & 7)) << 4));
-            v[c + 0] += u4.x; v[c + 1] += u4.y; v[c + 2] += u4.z; v[c + 3] += u4.w;
-          }
-          race_tile<CPP>(st, v, nv, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)p.k);
-        }
+        if (!mbar_wait(&bars->acc_full[acc_i], (it >> 1) & 1, abort, p.status)) { ok = false; break; }
+        tc_fence_after();
+        float v[CPP];
+        tmem_load_cols<CPP>(tmem + ((uint32_t)(q * 32) << 16) + acc_i * BN + part * CPP, v);
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->empty_u[su]);
-      } else {
-        if (active && nv > 0) {
-          // rho = max(0, p_t - p_d), kept in place of U (non-positive entries
-          // are outside the residual's support and never race)
+        if (lane == 0) mbar_arrive(&bars->acc_empty[acc_i]);
+        if constexpr (MODE == kDraft) {
+          const int su = it % kUStages;
+          if (!mbar_wait(&bars->full_u[su], (it / kUStages) & 1, abort, p.status)) { ok = false; break; }
+          // this thread's columns: box (part*CPP)/32, 16-byte chunks j0.. of row r,
+          // stored at chunk j ^ (r & 7) (128-byte swizzle)
+          unsigned char* urow = U_s + su * kUStageBytes + ((part * CPP) / kUBox) * (R * 128) + r * 128;
+          const int j0 = ((part * CPP) % kUBox) / 4;
+          if (active && nv > 0) {
 #pragma unroll
-          for (int c = 0; c < CPP; ++c) {
-            const float pd = exp2f(fmaf(v[c] + uu[c], kLog2e, -ld2));
-            const float pt = exp2f(fmaf(tt[c], kLog2e, -lt2));
-            uu[c] = pt - pd;
+            for (int c = 0; c < CPP; c += 4) {
+              const float4 u4 = *reinterpret_cast<const float4*>(urow + (((j0 + c / 4) ^ (r & 7)) << 4));
+              v[c + 0] += u4.x; v[c + 1] += u4.y; v[c + 2] += u4.z; v[c + 3] += u4.w;
+            }
+            // the row's best perturbed logit published so far by any CTA; read
+            // before the tile so that its latency hides behind the arithmetic
+            const unsigned long long gk = kShare ? __ldcg(row_key) : 0ull;
+            race_tile<CPP>(st, v, nv, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k);
+            if (kShare && gk) {
+              const float zg = argmax_key_value(gk);
+              if (zg > st.zthr) {
+                st.zthr = zg;
+                st.bound = race_bound(st.run_m, st.zthr);
+              }
+            }
+            // share this thread's progress with the other CTAs of the row
+            if (kShare && st.best_v >= 0 && st.zbest > st.zpub && st.zbest >= st.zthr) {
+              atomicMax(row_key, argmax_key(st.zbest, st.best_v));
+              st.zpub = st.zbest;
+            }
           }
-          resid_tile<CPP>(rs, uu, nv, v0, spill, p.key, (uint32_t)b, (uint32_t)ks);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->empty_u[su]);
+        } else {
+          if (active && nv > 0) {
+            // rho = max(0, p_t - p_d), kept in place of U (non-positive entries
+            // are outside the residual's support and never race)
+#pragma unroll
+            for (int c = 0; c < CPP; ++c) {
+              const float pd = ex2_approx(fmaf(v[c] + uu[c], kLog2e, -ld2));
+              const float pt = ex2_approx(fmaf(tt[c], kLog2e, -lt2));
+              uu[c] = pt - pd;
+            }
+            resid_tile<CPP>(rs, uu, nv, v0, spill, p.key, (uint32_t)b, (uint32_t)ks);
+          }
         }
       }
-    }
-    if (MODE == kDraft && (st.run_m != st.run_m || st.run_m == INFINITY))
-      record_status(p.status, DSPARK_ERR_NONFINITE);
+      if (MODE == kDraft && (st.run_m != st.run_m || st.run_m == INFINITY))
+        record_status(p.status, DSPARK_ERR_NONFINITE);
 
-    // combine the parts of each request row, then publish one partial per row
-    float* xm = reinterpret_cast<float*>(U_s);   // the U ring is idle once every tile is read
-    float* xs = xm + 2 * BM;
-    unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 2 * BM);
-    unsigned long long key = 0ull;
-    if constexpr (MODE == kDraft) key = st.best_v >= 0 ? argmax_key(st.zbest, st.best_v) : 0ull;
-    else key = rs.best_v >= 0 ? argmax_key(rs.zbest, rs.best_v) : 0ull;
-    named_bar_sync(1, kEpiWarps * 32);
-    const int slot = part * R + r;               // parts of row r at r, R + r, ...
-    xm[slot] = st.run_m;
-    xs[slot] = st.run_s;
-    xk[slot] = key;
-    named_bar_sync(1, kEpiWarps * 32);
-    if (part == 0 && active) {
-      float M = -INFINITY, S = 0.f;
-      unsigned long long K = 0ull;
+      // combine the parts of each request row, then publish one partial per row
+      unsigned long long key = 0ull;
+      if constexpr (MODE == kDraft) key = st.best_v >= 0 ? argmax_key(st.zbest, st.best_v) : 0ull;
+      else key = rs.best_v >= 0 ? argmax_key(rs.zbest, rs.best_v) : 0ull;
+      named_bar_sync(1, kEpiWarps * 32);
+      const int slot = part * R + r;               // parts of row r at r, R + r, ...
+      xm[slot] = st.run_m;
+      xs[slot] = st.run_s;
+      xk[slot] = key;
+      named_bar_sync(1, kEpiWarps * 32);
+      if (part == 0 && active && ok) {
+        float M = -INFINITY, S = 0.f;
+        unsigned long long K = 0ull;
 #pragma unroll
-      for (int j = 0; j < kParts; ++j) {
-        softmax_merge(M, S, xm[j * R + r], xs[j * R + r]);
-        K = xk[j * R + r] > K ? xk[j * R + r] : K;
+        for (int j = 0; j < kParts; ++j) {
+          softmax_merge(M, S, xm[j * R + r], xs[j * R + r]);
+          K = xk[j * R + r] > K ? xk[j * R + r] : K;
+        }
+        if constexpr (MODE == kDraft) {
+          p.part[((size_t)(k - 1) * p.part_slices + slice) * p.B + b] = make_float2(M, S);
+          if (K) atomicMax(&p.keys[(size_t)(k - 1) * p.B + b], K);
+        } else {
+          if (K) atomicMax(&p.resid_key[b], K);
+        }
       }
-      if constexpr (MODE == kDraft) {
-        p.part[(size_t)slice * p.B + b] = make_float2(M, S);
-        if (K) atomicMax(&p.keys_cur[b], K);
-      } else {
-        if (K) atomicMax(&p.resid_key[b], K);
+      (void)ok;
+      if (k < kl) {
+        // every CTA's position-k keys are in place before anyone reads x_k;
+        // one thread takes the decision to go on, all epilogue warps read it
+        // after the same barrier, so they all leave the loop together
+        named_bar_sync(1, kEpiWarps * 32);
+        if (warp == 2 && lane == 0) {
+          bool go = !*abort;
+          if (go) go = grid_barrier(p.gbar, (uint32_t)(p.nctas * (k - kf + 1)), abort, p.status);
+          bars->stop = go ? 0 : 1;
+        }
+        named_bar_sync(1, kEpiWarps * 32);
+        if (bars->stop) break;
       }
     }
   }
@@ -602,16 +680,18 @@ bool draft_tc_supported(int wdtype, int r) { return wdtype == DSPARK_BF16 && r =
 cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   const WsLayout L = ws_layout(a.B, a.gamma, a.V);
   int* status = ws_ptr<int>(a.ws, L.status);
+  unsigned int* gbar = ws_ptr<unsigned int>(a.ws, L.counters) + 1;
   unsigned long long* keys = ws_ptr<unsigned long long>(a.ws, L.draft_keys);
   float2* part = ws_ptr<float2>(a.ws, L.draft_part);
-  const int part_slices = draft_num_slices(a.V);
+  const int part_slices = draft_part_slices(a.V);
 
   CUtensorMap map;
   cudaError_t e = make_w2_tensor_map(a.W2, a.V, &map);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
+  int dev = 0, sms = 0, coop = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return e;
   const int R = a.B <= 32 ? 32 : (a.B <= 64 ? 64 : BM);
   CUtensorMap umap;
   if ((e = make_u_tensor_map(a.U, a.B, a.gamma, a.V, R, &umap)) != cudaSuccess) return e;
@@ -620,26 +700,52 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * (size_t)a.gamma * a.B, stream);
   if (e != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(gbar, 0, sizeof(unsigned int), stream)) != cudaSuccess) return e;
 
   const int mtiles = div_up(a.B, R);
   const int ntiles = div_up(a.V, BN);
   int per = std::max(1, sms / mtiles);
   per = std::min(per, std::min(ntiles, part_slices));
+  const int nctas = mtiles * per;
   StepParams sp{};
   sp.U = a.U;
   sp.W1 = static_cast<const __nv_bfloat16*>(a.W1);
   sp.anchor = a.anchor;
+  sp.keys = keys;
+  sp.part = part;
+  sp.gbar = gbar;
   sp.status = status;
   sp.B = a.B; sp.G = a.gamma; sp.V = a.V;
+  sp.part_slices = part_slices;
+  sp.nctas = nctas;
   sp.ctas_per_mtile = per;
   sp.ntiles = ntiles;
   sp.key = a.key;
-  for (int k = 1; k <= a.gamma; ++k) {
-    sp.k = k;
-    sp.keys_prev = (k >= 2) ? keys + (size_t)(k - 2) * a.B : nullptr;
-    sp.keys_cur = keys + (size_t)(k - 1) * a.B;
-    sp.part = part + (size_t)(k - 1) * part_slices * a.B;
-    kern<<<mtiles * per, kThreads, kSmemBytes, stream>>>(map, umap, sp);
+
+  // One persistent launch over all positions when every CTA can be resident
+  // at once (one CTA per SM); otherwise one launch per position.
+  int resident = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, kThreads, kSmemBytes)) != cudaSuccess)
+    return e;
+  if (coop && nctas <= resident * sms) {
+    sp.k_first = 1;
+    sp.k_last = a.gamma;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(nctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, kern, map, umap, sp)) != cudaSuccess) return e;
+  } else {
+    for (int k = 1; k <= a.gamma; ++k) {
+      sp.k_first = sp.k_last = k;
+      kern<<<nctas, kThreads, kSmemBytes, stream>>>(map, umap, sp);
+    }
   }
   draft_finalize_tc<<<div_up(a.B * a.gamma * 32, 256), 256, 0, stream>>>(
       a.U, static_cast<const __nv_bfloat16*>(a.W1), static_cast<const __nv_bfloat16*>(a.W2), a.anchor, keys,
@@ -681,7 +787,9 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
   sp.resid_lse = resid_lse;
   sp.resid_key = resid_key;
   sp.status = status;
-  sp.B = B; sp.G = G; sp.V = V; sp.k = 0;
+  sp.B = B; sp.G = G; sp.V = V;
+  sp.k_first = sp.k_last = 0;
+  sp.nctas = mtiles * per;
   sp.ctas_per_mtile = per;
   sp.ntiles = ntiles;
   sp.key = key;

@@ -24,6 +24,13 @@ namespace dspark {
 namespace {
 
 constexpr int kRowThreads = 256;
+constexpr float kLog2eF = 1.4426950408889634f;
+
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __global__ void __launch_bounds__(1024)
 verify_prep(const int32_t* __restrict__ ell, int B, int G, int32_t* __restrict__ rows,
@@ -78,31 +85,47 @@ verify_rows(const float* __restrict__ T, const int32_t* __restrict__ ell, int G,
   for (long long t = blockIdx.x; t < ntasks; t += gridDim.x) {
     const int ri = (int)(t / nsegs), seg = (int)(t - (t / nsegs) * nsegs);
     const int rowid = rows[ri];
-    const int b = rowid / (G + 1), j = rowid - (rowid / (G + 1)) * (G + 1);
-    const bool bonus = (j == min(max(ell[b], 0), G));
+    const int b = rowid / (G + 1), jrow = rowid - (rowid / (G + 1)) * (G + 1);
+    const bool bonus = (jrow == min(max(ell[b], 0), G));
     const float* Trow = T + (size_t)rowid * V;
     const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
-    float m = -INFINITY, s = 0.f;
-    unsigned long long best = 0ull;
-    bool bad = false;
-    for (int v = v0 + 4 * tid; v < v1; v += 4 * kRowThreads) {
-      const float4 t4 = __ldcs(reinterpret_cast<const float4*>(Trow + v));
-      const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-      float mx = fmaxf(fmaxf(tv[0], tv[1]), fmaxf(tv[2], tv[3]));
-      bad |= !isfinite(tv[0]) | !isfinite(tv[1]) | !isfinite(tv[2]) | !isfinite(tv[3]);
-      if (mx > m) {
-        s *= expf(m - mx);
-        m = mx;
+    // all of this thread's loads are issued before any arithmetic: 8 x 16 bytes
+    // in flight per thread keeps the memory system busy
+    constexpr int kPer = kVerifySeg / (4 * kRowThreads);
+    float4 t4[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int v = v0 + 4 * tid + 4 * kRowThreads * j;
+      t4[j] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(Trow + v))
+                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) m = fmaxf(fmaxf(m, fmaxf(t4[j].x, t4[j].y)), fmaxf(t4[j].z, t4[j].w));
+    bool bad = !(m < INFINITY);
+    float s = 0.f;
+    if (m != -INFINITY) {
+      const float mb = m * kLog2eF;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        s += exp2_fast(fmaf(t4[j].x, kLog2eF, -mb)) + exp2_fast(fmaf(t4[j].y, kLog2eF, -mb));
+        s += exp2_fast(fmaf(t4[j].z, kLog2eF, -mb)) + exp2_fast(fmaf(t4[j].w, kLog2eF, -mb));
       }
+    }
+    unsigned long long best = 0ull;
+    if (bonus) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) s += expf(tv[q] - m);
-      if (bonus) {
-        const uint4 rw = rng4(key, kStreamBonus, (uint32_t)b, (uint32_t)(j + 1), (uint32_t)(v >> 2));
-        const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+      for (int j = 0; j < kPer; ++j) {
+        const int v = v0 + 4 * tid + 4 * kRowThreads * j;
+        if (v < v1) {
+          const uint4 rw = rng4(key, kStreamBonus, (uint32_t)b, (uint32_t)(jrow + 1), (uint32_t)(v >> 2));
+          const float tv[4] = {t4[j].x, t4[j].y, t4[j].z, t4[j].w};
+          const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const unsigned long long kz = argmax_key(tv[q] + gumbel_noise(words[q]), v + q);
-          best = kz > best ? kz : best;
+          for (int q = 0; q < 4; ++q) {
+            const unsigned long long kz = argmax_key(tv[q] + gumbel_noise(words[q]), v + q);
+            best = kz > best ? kz : best;
+          }
         }
       }
     }
@@ -281,7 +304,7 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long max_tasks = (long long)a.B * (a.gamma + 1) * nsegs;
-  const int grid_rows = (int)std::min<long long>(max_tasks, (long long)sms * 8);
+  const int grid_rows = (int)std::min<long long>(max_tasks, (long long)sms * 4);
   verify_rows<<<grid_rows, kRowThreads, 0, stream>>>(a.T, a.ell, a.gamma, a.V, nsegs, a.key, rows, counters,
                                                       row_part, bonus_key, status);
   verify_decide<<<div_up(a.B * 32, 256), 256, 0, stream>>>(a.T, a.x, a.p_d, a.ell, a.B, a.gamma, a.V, nsegs,
