@@ -36,8 +36,16 @@ def lib():
         L.oracle_rng_word.restype = c_u32
         L.oracle_u01.argtypes = [c_u32]
         L.oracle_u01.restype = c_dbl
-        L.oracle_gumbel.argtypes = [c_u32]
-        L.oracle_gumbel.restype = c_dbl
+        L.oracle_philox_word.argtypes = [c_u64, c_u64, c_u32, c_u32, c_u32, c_u32, c_u32]
+        L.oracle_philox_word.restype = c_u32
+        L.oracle_gumbel_bits.argtypes = [c_u64, c_u64, c_u32, c_u32, c_u32, c_u32]
+        L.oracle_gumbel_bits.restype = c_u32
+        L.oracle_u01_bits.argtypes = [c_u32]
+        L.oracle_u01_bits.restype = c_dbl
+        L.oracle_gumbel_from_bits.argtypes = [c_u32]
+        L.oracle_gumbel_from_bits.restype = c_dbl
+        L.oracle_gumbel_noise.argtypes = [c_u64, c_u64, c_u32, c_u32, c_u32, c_u32]
+        L.oracle_gumbel_noise.restype = c_dbl
         L.oracle_draft_logits.argtypes = [c_int, c_int, vp, vp, vp, c_int, c_int, vp]
         L.oracle_draft_logits.restype = None
         L.oracle_draft_probs.argtypes = [c_int, c_int, vp, vp, vp, c_int, c_int, vp]
@@ -109,12 +117,31 @@ def rng_word(seed, rnd, stream, req, k, v):
     return int(lib().oracle_rng_word(seed, rnd, stream, req, k, v))
 
 
+def philox_word(seed, rnd, stream, req, k, c0, word):
+    return int(lib().oracle_philox_word(seed, rnd, stream, req, k, c0, word))
+
+
 def u01(word):
+    """The accept uniform from a whole 32-bit word (its top 23 bits)."""
     return float(lib().oracle_u01(word))
 
 
-def gumbel(word):
-    return float(lib().oracle_gumbel(word))
+def gumbel_bits(seed, rnd, stream, req, k, v):
+    """The 23 random bits of the Gumbel noise of entry v."""
+    return int(lib().oracle_gumbel_bits(seed, rnd, stream, req, k, v))
+
+
+def u01_bits(m):
+    return float(lib().oracle_u01_bits(m))
+
+
+def gumbel_from_bits(m):
+    return float(lib().oracle_gumbel_from_bits(m))
+
+
+def gumbel_noise(seed, rnd, stream, req, k, v):
+    """The Gumbel noise of entry v of stream `stream`."""
+    return float(lib().oracle_gumbel_noise(seed, rnd, stream, req, k, v))
 
 
 # --------------------------------------------------------------------------

@@ -72,36 +72,67 @@ void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2],
   out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
 }
 
-/* The stream layout of this library's random numbers (a choice of this
- * implementation; the pages do not say how tokens are sampled):
- *   key     = (seed mod 2^32, seed div 2^32)
- *   counter = (v div 4, position k, request index, (round << 3) | stream)
- *   word    = v mod 4 of the Philox output
- * Streams: 0 draft Gumbel, 1 verify accept uniform (v = 0), 2 residual Gumbel,
- * 3 bonus Gumbel. */
-uint32_t oracle_rng_word(uint64_t seed, uint64_t round, uint32_t stream,
-                         uint32_t req, uint32_t k, uint32_t v) {
+/* One 32-bit word of Philox4x32-10 for key (seed mod 2^32, seed div 2^32) and
+ * counter (c0, position k, request index, (round << 3) | stream). */
+uint32_t oracle_philox_word(uint64_t seed, uint64_t round, uint32_t stream,
+                            uint32_t req, uint32_t k, uint32_t c0, uint32_t word) {
   uint32_t ctr[4], key[2], out[4];
-  ctr[0] = v >> 2;
+  ctr[0] = c0;
   ctr[1] = k;
   ctr[2] = req;
   ctr[3] = (uint32_t)((round << 3) | (uint64_t)(stream & 7u));
   key[0] = (uint32_t)(seed & 0xffffffffu);
   key[1] = (uint32_t)(seed >> 32);
   oracle_philox4x32_10(ctr, key, out);
-  return out[v & 3u];
+  return out[word & 3u];
 }
 
-/* Uniform in the open interval (0, 1): the top 23 bits, centred in their cell,
- * i.e. (2m + 1) / 2^24 for m = w >> 9.  Smallest 2^-24, largest 1 - 2^-24. */
-double oracle_u01(uint32_t w) {
-  return ((double)(w >> 9) + 0.5) * (1.0 / 8388608.0);
+/* The random numbers of this library (a choice of this implementation: the
+ * pages do not say how tokens are sampled).
+ *
+ * Word v of a stream: counter (v div 4, ...), word v mod 4.  The accept uniform
+ * of position k (stream 1) uses word 0: m = its top 23 bits.
+ *
+ * The Gumbel noise of entry v (streams 0 draft, 2 residual, 3 bonus) takes the
+ * 23 bits m of its uniform from two calls:
+ *   high 16 bits: half (v mod 2) (0 = low half) of word ((v div 2) mod 4) of
+ *                 the call with counter (v div 8, k, request, round<<3 | stream);
+ *   low 7 bits:   the top 7 bits of word (v mod 4) of the call with counter
+ *                 (v div 4, k, request, round<<3 | (stream + 4)).
+ * Every m is equally likely and the entries' m are independent, so u is the
+ * same uniform on the 2^23-point grid as from a single word. */
+uint32_t oracle_rng_word(uint64_t seed, uint64_t round, uint32_t stream,
+                         uint32_t req, uint32_t k, uint32_t v) {
+  return oracle_philox_word(seed, round, stream, req, k, v >> 2, v & 3u);
 }
+
+uint32_t oracle_gumbel_bits(uint64_t seed, uint64_t round, uint32_t stream,
+                            uint32_t req, uint32_t k, uint32_t v) {
+  uint32_t a = oracle_philox_word(seed, round, stream, req, k, v >> 3, (v >> 1) & 3u);
+  uint32_t hi16 = (v & 1u) ? (a >> 16) : (a & 0xffffu);
+  uint32_t b = oracle_philox_word(seed, round, stream + 4u, req, k, v >> 2, v & 3u);
+  return (hi16 << 7) | (b >> 25);
+}
+
+/* Uniform in the open interval (0, 1) from 23 bits m: (2m + 1) / 2^24.
+ * Smallest 2^-24, largest 1 - 2^-24. */
+double oracle_u01_bits(uint32_t m) {
+  return ((double)(m & 0x7fffffu) + 0.5) * (1.0 / 8388608.0);
+}
+
+/* The accept uniform from a whole word: its top 23 bits. */
+double oracle_u01(uint32_t w) { return oracle_u01_bits(w >> 9); }
 
 /* Standard Gumbel variate by inversion of its CDF exp(-exp(-g)). */
-double oracle_gumbel(uint32_t w) {
-  double u = oracle_u01(w);
+double oracle_gumbel_from_bits(uint32_t m) {
+  double u = oracle_u01_bits(m);
   return -log(-log(u));
+}
+
+/* The Gumbel noise of entry v of a Gumbel stream. */
+double oracle_gumbel_noise(uint64_t seed, uint64_t round, uint32_t stream,
+                           uint32_t req, uint32_t k, uint32_t v) {
+  return oracle_gumbel_from_bits(oracle_gumbel_bits(seed, round, stream, req, k, v));
 }
 
 /* ------------------------------------------------------------------------- */
@@ -163,7 +194,7 @@ int oracle_gumbel_argmax(int V, const double* score, uint64_t seed,
   for (int v = 0; v < V; ++v) {
     if (score[v] == -INFINITY) continue;
     double z = score[v] +
-               oracle_gumbel(oracle_rng_word(seed, round, stream, req, k, (uint32_t)v));
+               oracle_gumbel_noise(seed, round, stream, req, k, (uint32_t)v);
     if (z > best) {
       second = best;
       best = z;

@@ -58,22 +58,55 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const RngKey& key) {
   return c;
 }
 
+// One Philox call of (stream, request, position) with first counter word c0.
+__device__ __forceinline__ uint4 rng_call(const RngKey& key, uint32_t stream, uint32_t req, uint32_t pos,
+                                          uint32_t c0) {
+  return philox4x32_10(make_uint4(c0, pos, req, key.round3 | stream), key);
+}
+
 // The four words for vocabulary entries 4q .. 4q+3 of (stream, request, position).
 __device__ __forceinline__ uint4 rng4(const RngKey& key, uint32_t stream, uint32_t req,
                                       uint32_t pos, uint32_t q) {
-  return philox4x32_10(make_uint4(q, pos, req, key.round3 | stream), key);
+  return rng_call(key, stream, req, pos, q);
 }
 
-// Uniform (2m + 1) / 2^24 with m the top 23 bits of w: exact in float32.
-__device__ __forceinline__ float uniform01(uint32_t w) {
-  return __uint2float_rn(w >> 9) * 0x1p-23f + 0x1p-24f;
+__device__ __forceinline__ uint32_t word_of(const uint4& w, uint32_t j) {
+  return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
 }
+
+// Uniform (2m + 1) / 2^24 from 23 random bits m: exact in float32.
+__device__ __forceinline__ float uniform_bits(uint32_t m) {
+  return __uint2float_rn(m) * 0x1p-23f + 0x1p-24f;
+}
+
+// The accept uniform of a position: the top 23 bits of a word.
+__device__ __forceinline__ float uniform01(uint32_t w) { return uniform_bits(w >> 9); }
 
 // Standard Gumbel variate by inversion.  The inner logarithm uses the
 // full-accuracy logf: near u = 1 its result is tiny and a fast approximation
 // with absolute error would distort the largest noise values.
-__device__ __forceinline__ float gumbel_noise(uint32_t w) {
-  return -logf(-logf(uniform01(w)));
+__device__ __forceinline__ float gumbel_from_bits(uint32_t m) {
+  return -logf(-logf(uniform_bits(m)));
+}
+
+// Gumbel noise of entry v: its 23 uniform bits come from two calls.  The high
+// 16 are half (v mod 2) of word ((v div 2) mod 4) of the call with counter
+// (v div 8, position, request, round<<3 | stream), shared by 8 entries; the low
+// 7 are the top bits of word (v mod 4) of the call with counter (v div 4, ...,
+// round<<3 | (stream + 4)).  The high half alone usually shows that an entry
+// cannot win a race, so the second call is made only for the rare rest.
+__device__ __forceinline__ uint32_t gumbel_hi16(const uint4& a, uint32_t v) {
+  const uint32_t w = word_of(a, (v >> 1) & 3u);
+  return (v & 1u) ? (w >> 16) : (w & 0xffffu);
+}
+__device__ __forceinline__ uint32_t gumbel_lo7(const RngKey& key, uint32_t stream, uint32_t req, uint32_t pos,
+                                               uint32_t v) {
+  return word_of(rng_call(key, stream + 4u, req, pos, v >> 2), v & 3u) >> 25;
+}
+__device__ __forceinline__ float gumbel_noise_at(const RngKey& key, uint32_t stream, uint32_t req, uint32_t pos,
+                                                 uint32_t v) {
+  const uint32_t hi = gumbel_hi16(rng_call(key, stream, req, pos, v >> 3), v);
+  return gumbel_from_bits((hi << 7) | gumbel_lo7(key, stream, req, pos, v));
 }
 
 // ---------------------------------------------------------------------------
@@ -147,7 +180,7 @@ __device__ __forceinline__ float load_weight(const void* base, size_t idx) {
 // Tiling constants and the workspace layout (shared by host and device code).
 // ---------------------------------------------------------------------------
 constexpr int kDraftSlice = 1024;   // vocabulary columns per draft CTA (CUDA-core path)
-constexpr int kVerifySeg = 8192;    // vocabulary entries per verify task
+constexpr int kVerifySeg = 32768;   // vocabulary entries per verify task
 constexpr int kMaxGamma = 32;
 constexpr int kMaxCandidates = 8192;
 

@@ -78,8 +78,8 @@ draft_step_cuda_core(const float* __restrict__ U, const void* __restrict__ W1,
     for (int q = 0; q < 2; ++q) {
       const int v4 = vt + cg + 4 * q;   // groups of 4 never straddle v_end (V % 8 == 0)
       if (v4 >= v_end) continue;
-      const uint4 rw = rng4(key, kStreamDraft, (uint32_t)b, (uint32_t)k, (uint32_t)(v4 >> 2));
-      const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+      const uint4 ra = rng_call(key, kStreamDraft, (uint32_t)b, (uint32_t)k, (uint32_t)(v4 >> 3));
+      const uint4 rb = rng_call(key, kStreamDraft + 4u, (uint32_t)b, (uint32_t)k, (uint32_t)(v4 >> 2));
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int v = v4 + j;
@@ -91,7 +91,8 @@ draft_step_cuda_core(const float* __restrict__ U, const void* __restrict__ W1,
         } else {
           run_s += expf(l - run_m);
         }
-        const unsigned long long kz = argmax_key(l + gumbel_noise(words[j]), v);
+        const uint32_t m = (gumbel_hi16(ra, (uint32_t)v) << 7) | (word_of(rb, (uint32_t)j) >> 25);
+        const unsigned long long kz = argmax_key(l + gumbel_from_bits(m), v);
         best = kz > best ? kz : best;
       }
     }

@@ -117,10 +117,6 @@ __device__ __forceinline__ float race_bound(float run_m, float zbest) {
   return exp2f((run_m - zbest) * kLog2e) * (1.0f + 0x1p-10f);
 }
 
-__device__ __forceinline__ uint32_t pick_word(const uint4& w, int j) {
-  return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
-}
-
 // Folds the fused logits l[0..nv) of columns v0.. into the race.  Candidates
 // are resolved as they are met, with the random word and logit still in
 // registers, and each one that wins tightens the bound for the rest.  The
@@ -148,43 +144,57 @@ __device__ __forceinline__ void race_tile(RowRace& st, float (&l)[CPP], int nv, 
       for (int c = CPP - 1; c >= 0; --c)
         if (c < nv && l[c] == tm) cs = c;
       const int v = v0 + cs;
-      const uint4 rw = rng4(key, kStreamDraft, req, pos, (uint32_t)(v >> 2));
-      st.zbest = tm + gumbel_noise(pick_word(rw, v & 3));
+      st.zbest = tm + gumbel_noise_at(key, kStreamDraft, req, pos, (uint32_t)v);
       st.best_v = v;
       st.zthr = fmaxf(st.zthr, st.zbest);
     }
     st.bound = race_bound(st.run_m, st.zthr);
   }
   const float mb = st.run_m * kLog2e;
+  // Screen on the high 16 bits h of each uniform: since
+  // E_v >= 1 - u_v > (65535 - h) / 65536, entry v can only win when
+  // h > 65535 - 65536 exp(l_v - zthr), i.e. when 32768 + h/2 (built exactly as
+  // a float from the bits) exceeds 65535.5 - 32768 e bound; half a step of
+  // slack absorbs the rounding of the threshold.
+  const float b32 = st.bound * 32768.0f;
+  uint32_t cand = 0;
+  uint4 ra = make_uint4(0, 0, 0, 0);
 #pragma unroll
-  for (int g = 0; g < CPP / 4; ++g) {
-    if (4 * g < nv) {
-      const uint4 rw = rng4(key, kStreamDraft, req, pos, (uint32_t)((v0 >> 2) + g));
-      const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+  for (int c = 0; c < CPP; ++c) {
+    if (c % 8 == 0) ra = rng_call(key, kStreamDraft, req, pos, (uint32_t)(v0 + c) >> 3);
+    if (c < nv) {
+      const uint32_t v = (uint32_t)(v0 + c);
+      const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
+      st.run_s += e;
+      const uint32_t w = word_of(ra, (v >> 1) & 3u);
+      const uint32_t hb = (v & 1u) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);   // h << 7
+      const float hf = __uint_as_float(0x47000000u | hb);                                 // 32768 + h/2
+      if (hf > fmaf(-e, b32, 65535.0f)) cand |= 1u << c;
+    }
+  }
+  if (cand) {
+    // rare: park the logits, then let the full uniforms decide, one entry at a time
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = 4 * g + j;
-        const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
-        st.run_s += e;
-        // 1 + m 2^-23 with m the top 23 random bits: 2 - up = 1 - u + 2^-24
-        const float up = __uint_as_float((words[j] >> 9) | 0x3F800000u);
-        const float thr = fmaf(-e, st.bound, 0x1.fffffcp0f);
-        if (up > thr) {
-          // a candidate: its exact perturbed logit decides
-          const float z = l[c] + gumbel_noise(words[j]);
-          if (z > st.zbest) {
-            st.zbest = z;
-            st.best_v = v0 + c;
-            if (z > st.zthr) {
-              st.zthr = z;
-              st.bound = race_bound(st.run_m, st.zthr);
-            }
-          }
+    for (int c = 0; c < CPP; c += 4)
+      *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(l[c], l[c + 1], l[c + 2], l[c + 3]);
+#pragma unroll 1
+    while (cand) {
+      const int c = __ffs(cand) - 1;
+      cand &= cand - 1;
+      const uint32_t v = (uint32_t)(v0 + c);
+      const uint32_t hi = gumbel_hi16(rng_call(key, kStreamDraft, req, pos, v >> 3), v);
+      const float lc = reinterpret_cast<const float*>(spill + (((j0 + c / 4) ^ sw) << 4))[c & 3];
+      const float z = lc + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamDraft, req, pos, v));
+      if (z > st.zbest) {
+        st.zbest = z;
+        st.best_v = (int)v;
+        if (z > st.zthr) {
+          st.zthr = z;
+          st.bound = race_bound(st.run_m, st.zthr);
         }
       }
     }
   }
-  (void)spill; (void)j0; (void)sw;
 }
 
 // Race of the residual resample: argmax_v log rho_v + G_v over rho_v > 0,
@@ -208,38 +218,39 @@ __device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP],
       if (c < nv && rho[c] > rmax) { rmax = rho[c]; cs = c; }
     if (cs < 0) return;   // no positive residual mass seen yet
     const int v = v0 + cs;
-    const uint4 rw = rng4(key, kStreamResidual, req, pos, (uint32_t)(v >> 2));
-    st.zbest = logf(rmax) + gumbel_noise(pick_word(rw, v & 3));
+    st.zbest = logf(rmax) + gumbel_noise_at(key, kStreamResidual, req, pos, (uint32_t)v);
     st.best_v = v;
     st.bound = expf(-st.zbest) * (1.0f + 0x1p-10f);
   }
+  // the same screen on the high 16 random bits as the draft race, with rho_v
+  // in place of the softmax term
+  const float b32 = st.bound * 32768.0f;
   uint32_t cand = 0;
+  uint4 ra = make_uint4(0, 0, 0, 0);
 #pragma unroll
-  for (int g = 0; g < CPP / 4; ++g) {
-    if (4 * g < nv) {
-      const uint4 rw = rng4(key, kStreamResidual, req, pos, (uint32_t)((v0 >> 2) + g));
-      const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = 4 * g + j;
-        const float up = __uint_as_float((words[j] >> 9) | 0x3F800000u);
-        const float thr = fmaf(-rho[c], st.bound, 0x1.fffffcp0f);
-        if (rho[c] > 0.f && up > thr) cand |= 1u << c;
-      }
+  for (int c = 0; c < CPP; ++c) {
+    if (c % 8 == 0) ra = rng_call(key, kStreamResidual, req, pos, (uint32_t)(v0 + c) >> 3);
+    if (c < nv && rho[c] > 0.f) {
+      const uint32_t v = (uint32_t)(v0 + c);
+      const uint32_t w = word_of(ra, (v >> 1) & 3u);
+      const uint32_t hb = (v & 1u) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);
+      const float hf = __uint_as_float(0x47000000u | hb);
+      if (hf > fmaf(-rho[c], b32, 65535.0f)) cand |= 1u << c;
     }
   }
   if (cand) {
 #pragma unroll
     for (int c = 0; c < CPP; c += 4) *reinterpret_cast<float4*>(spill + c) = make_float4(rho[c], rho[c + 1], rho[c + 2], rho[c + 3]);
+#pragma unroll 1
     while (cand) {
       const int c = __ffs(cand) - 1;
       cand &= cand - 1;
-      const int v = v0 + c;
-      const uint4 rw = rng4(key, kStreamResidual, req, pos, (uint32_t)(v >> 2));
-      const float z = logf(spill[c]) + gumbel_noise(pick_word(rw, v & 3));
+      const uint32_t v = (uint32_t)(v0 + c);
+      const uint32_t hi = gumbel_hi16(rng_call(key, kStreamResidual, req, pos, v >> 3), v);
+      const float z = logf(spill[c]) + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamResidual, req, pos, v));
       if (z > st.zbest) {
         st.zbest = z;
-        st.best_v = v;
+        st.best_v = (int)v;
         st.bound = expf(-st.zbest) * (1.0f + 0x1p-10f);
       }
     }
@@ -418,7 +429,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     float* xm = reinterpret_cast<float*>(X_s);
     float* xs = xm + 4 * BM;
     unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 4 * BM);
-    float* spill = reinterpret_cast<float*>(U_s + ((warp - 2) * 32 + lane) * 144);
+    float* spill = reinterpret_cast<float*>(U_s + ((warp - 2) * 32 + lane) * 144);   // residual mode only
     uint32_t it = 0;
     for (int k = kf; k <= kl; ++k) {
       bool active = r < rows_valid;

@@ -37,15 +37,14 @@ __global__ void confidence_kernel(const void* __restrict__ h, const void* __rest
 
 constexpr int kSchedThreads = 1024;
 
-__device__ __forceinline__ bool cand_before(double a1, int i1, double a2, int i2) {
-  return a1 > a2 || (a1 == a2 && i1 < i2);
-}
-
-// One CTA.  a = prefix products in fp64; bitonic sort of the candidates by
-// (a desc, index asc) where index = b*gamma + j-1 gives (b asc, j asc); an
-// inclusive fp64 scan of the sorted a; Theta_n = (R + S_n) * SPS(R + n); the
-// greedy count n* is one less than the first n whose Theta does not exceed
-// Theta_{n-1}.
+// One CTA.  a = prefix products in fp64.  The candidates are sorted as 64-bit
+// integers: the bits of a (non-negative, so ordered like the values) with the
+// low 13 bits replaced by 8191 - index, index = b*gamma + j-1; a descending
+// integer sort then gives a desc, b asc, j asc (values closer than 2^-39
+// relative count as ties and fall back to the index order).  The exact a
+// values stay aside for an inclusive fp64 scan of the sorted list;
+// Theta_n = (R + S_n) * SPS(R + n), and the greedy count n* is one less than
+// the first n whose Theta does not exceed Theta_{n-1}.
 __global__ void __launch_bounds__(kSchedThreads)
 schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restrict__ sps, int mode,
                 uint32_t round_lo, int round_ge2, int32_t* __restrict__ khist,
@@ -55,9 +54,9 @@ schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restri
   const int N = R * G;
   int NP = 1;
   while (NP < N) NP <<= 1;
-  double* akey = reinterpret_cast<double*>(smem_raw);       // [NP]
-  int* aidx = reinterpret_cast<int*>(akey + NP);            // [NP]
-  int* ell_s = aidx + NP;                                    // [R]
+  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem_raw);   // [NP]
+  double* av = reinterpret_cast<double*>(key + NP);                              // [N]
+  int* ell_s = reinterpret_cast<int*>(av + N);                                   // [R]
   __shared__ double warp_tot[32];
   __shared__ int s_first_stop;
   __shared__ int s_K;
@@ -79,16 +78,14 @@ schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restri
       const float cj = c[(size_t)b * G + j];
       bad |= !(cj >= 0.f && cj <= 1.f);
       a *= (double)cj;
-      akey[b * G + j] = a;
-      aidx[b * G + j] = b * G + j;
+      const int i = b * G + j;
+      av[i] = a;
+      key[i] = ((unsigned long long)__double_as_longlong(a) & ~0x1FFFull) | (unsigned long long)(8191 - i);
     }
     if (bad) record_status(status, DSPARK_ERR_NONFINITE);
     ell_s[b] = 0;
   }
-  for (int i = N + tid; i < NP; i += kSchedThreads) {
-    akey[i] = -1.0;
-    aidx[i] = 0x7fffffff;
-  }
+  for (int i = N + tid; i < NP; i += kSchedThreads) key[i] = 0ull;
   if (tid == 0) {
     s_first_stop = N + 1;
     s_K = -1;
@@ -96,31 +93,34 @@ schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restri
   }
   __syncthreads();
 
+  // bitonic sort, descending
   for (int size = 2; size <= NP; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int t = tid; t < (NP >> 1); t += kSchedThreads) {
         const int i = (t / stride) * (stride << 1) + (t % stride);
         const int j = i + stride;
-        const double ai = akey[i], aj = akey[j];
-        const int ii = aidx[i], ij = aidx[j];
-        const bool up = (i & size) == 0;
-        const bool swap = up ? cand_before(aj, ij, ai, ii) : cand_before(ai, ii, aj, ij);
-        if (swap) {
-          akey[i] = aj; akey[j] = ai;
-          aidx[i] = ij; aidx[j] = ii;
+        const unsigned long long ki = key[i], kj = key[j];
+        const bool desc = (i & size) == 0;
+        if (desc ? (kj > ki) : (ki > kj)) {
+          key[i] = kj;
+          key[j] = ki;
         }
       }
       __syncthreads();
     }
   }
 
-  // inclusive scan of the sorted a in place: akey[i] = S_{i+1}
+  // the exact a of each sorted position, then an inclusive scan in place:
+  // av[p] = S_{p+1}
   const int chunk = div_up(N, kSchedThreads);
   const int lo = tid * chunk, hi = min(N, lo + chunk);
+  double loc[8];
+  for (int p = lo; p < hi; ++p) loc[p - lo] = av[8191 - (int)(key[p] & 0x1FFFull)];
+  __syncthreads();
   double run = 0.0;
-  for (int i = lo; i < hi; ++i) {
-    run += akey[i];
-    akey[i] = run;
+  for (int p = lo; p < hi; ++p) {
+    run += loc[p - lo];
+    av[p] = run;
   }
   double incl = run;
   const int lane = tid & 31, wid = tid >> 5;
@@ -140,27 +140,28 @@ schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restri
   }
   __syncthreads();
   const double base = (incl - run) + (wid > 0 ? warp_tot[wid - 1] : 0.0);
-  for (int i = lo; i < hi; ++i) akey[i] += base;
+  for (int p = lo; p < hi; ++p) av[p] += base;
   __syncthreads();
 
   // Theta_n for n = 0..N; the first n >= 1 with Theta_n <= Theta_{n-1} stops
   const double Rd = (double)R;
   for (int n = tid + 1; n <= N; n += kSchedThreads) {
-    const double s_prev = n >= 2 ? akey[n - 2] : 0.0;
+    const double s_prev = n >= 2 ? av[n - 2] : 0.0;
     const double th_prev = (Rd + s_prev) * (double)sps[R + n - 1];
-    const double th = (Rd + akey[n - 1]) * (double)sps[R + n];
+    const double th = (Rd + av[n - 1]) * (double)sps[R + n];
     if (th <= th_prev) atomicMin(&s_first_stop, n);
   }
   __syncthreads();
   const int nstar = (s_first_stop <= N) ? s_first_stop - 1 : N;
   int admitted = nstar;
   if (mode == DSPARK_SCHED_TOPK && round_ge2) admitted = min(max(s_K, 0), N);
-  for (int p = tid; p < admitted; p += kSchedThreads) atomicAdd(&ell_s[aidx[p] / G], 1);
+  for (int p = tid; p < admitted; p += kSchedThreads)
+    atomicAdd(&ell_s[(8191 - (int)(key[p] & 0x1FFFull)) / G], 1);
   __syncthreads();
   for (int b = tid; b < R; b += kSchedThreads) ell_out[b] = ell_s[b];
   if (tid == 0) {
     *nstar_out = nstar;
-    const double S = admitted > 0 ? akey[admitted - 1] : 0.0;
+    const double S = admitted > 0 ? av[admitted - 1] : 0.0;
     *theta_out = (Rd + S) * (double)sps[R + admitted];
     if (mode == DSPARK_SCHED_TOPK) khist[round_lo & 1u] = nstar;
   }
@@ -188,7 +189,7 @@ cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdt
 size_t schedule_smem_bytes(int B, int gamma) {
   int NP = 1;
   while (NP < B * gamma) NP <<= 1;
-  return (size_t)NP * (sizeof(double) + sizeof(int)) + sizeof(int) * (size_t)B;
+  return (size_t)NP * sizeof(unsigned long long) + (size_t)B * gamma * sizeof(double) + sizeof(int) * (size_t)B;
 }
 
 cudaError_t launch_schedule(const float* c, int B, int gamma, const float* sps, int mode,

@@ -72,13 +72,44 @@ verify_prep(const int32_t* __restrict__ ell, int B, int G, int32_t* __restrict__
   if (tid == 1023) counters[0] = pos;
 }
 
+// Block-wide (max, sum) of per-thread online-softmax states: the maximum
+// first, then every thread rescales its own sum once, then one sum.
+__device__ __forceinline__ float2 block_softmax(float m, float s, float* s_red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  float mx = m;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) s_red[wid] = mx;
+  __syncthreads();
+  mx = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kRowThreads / 32; ++w) mx = fmaxf(mx, s_red[w]);
+  float t = (m == -INFINITY) ? 0.f : s * exp2_fast((m - mx) * kLog2eF);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  __syncthreads();
+  if (lane == 0) s_red[wid] = t;
+  __syncthreads();
+  float S = 0.f;
+#pragma unroll
+  for (int w = 0; w < kRowThreads / 32; ++w) S += s_red[w];
+  return make_float2(mx, S);
+}
+
+// One (row, segment) task per iteration: kVerifySeg entries of a target row,
+// read as batches of eight 16-byte loads per thread (all issued before any
+// arithmetic), folded into an online softmax; on the bonus row also a
+// screened Gumbel race (as in the draft).
 __global__ void __launch_bounds__(kRowThreads)
 verify_rows(const float* __restrict__ T, const int32_t* __restrict__ ell, int G, int V, int nsegs,
             RngKey key, const int32_t* __restrict__ rows, const int* __restrict__ counters,
             float2* __restrict__ row_part, unsigned long long* __restrict__ bonus_key,
             int* __restrict__ status) {
-  __shared__ float s_m[kRowThreads / 32], s_s[kRowThreads / 32];
+  __shared__ float s_red[kRowThreads / 32];
   __shared__ unsigned long long s_k[kRowThreads / 32];
+  constexpr int kBatch = 8;                                     // float4 loads per batch
+  constexpr int kStride = 4 * kRowThreads;                      // entries between a thread's loads
+  constexpr int kBatches = kVerifySeg / (kBatch * kStride);
   const int nrows = counters[0];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const long long ntasks = (long long)nrows * nsegs;
@@ -87,66 +118,96 @@ verify_rows(const float* __restrict__ T, const int32_t* __restrict__ ell, int G,
     const int rowid = rows[ri];
     const int b = rowid / (G + 1), jrow = rowid - (rowid / (G + 1)) * (G + 1);
     const bool bonus = (jrow == min(max(ell[b], 0), G));
+    const uint32_t pos = (uint32_t)(jrow + 1);
     const float* Trow = T + (size_t)rowid * V;
     const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
-    // all of this thread's loads are issued before any arithmetic: 8 x 16 bytes
-    // in flight per thread keeps the memory system busy
-    constexpr int kPer = kVerifySeg / (4 * kRowThreads);
-    float4 t4[kPer];
+    float m = -INFINITY, s = 0.f;
+    float zbest = -INFINITY;
+    int bestv = -1;
+    bool bad = false;
+#pragma unroll 1
+    for (int bt = 0; bt < kBatches; ++bt) {
+      const int vb = v0 + bt * kBatch * kStride + 4 * tid;
+      if (vb >= v1) break;
+      float4 t4[kBatch];
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int v = v0 + 4 * tid + 4 * kRowThreads * j;
-      t4[j] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(Trow + v))
-                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
-    float m = -INFINITY;
+      for (int j = 0; j < kBatch; ++j) {
+        const int v = vb + kStride * j;
+        t4[j] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(Trow + v))
+                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      float bm = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) m = fmaxf(fmaxf(m, fmaxf(t4[j].x, t4[j].y)), fmaxf(t4[j].z, t4[j].w));
-    bool bad = !(m < INFINITY);
-    float s = 0.f;
-    if (m != -INFINITY) {
+      for (int j = 0; j < kBatch; ++j) bm = fmaxf(fmaxf(bm, fmaxf(t4[j].x, t4[j].y)), fmaxf(t4[j].z, t4[j].w));
+      bad |= !(bm < INFINITY);
+      if (bm > m) {
+        s = (m == -INFINITY) ? 0.f : s * exp2_fast((m - bm) * kLog2eF);
+        m = bm;
+      }
+      if (m == -INFINITY) continue;
       const float mb = m * kLog2eF;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        s += exp2_fast(fmaf(t4[j].x, kLog2eF, -mb)) + exp2_fast(fmaf(t4[j].y, kLog2eF, -mb));
-        s += exp2_fast(fmaf(t4[j].z, kLog2eF, -mb)) + exp2_fast(fmaf(t4[j].w, kLog2eF, -mb));
-      }
-    }
-    unsigned long long best = 0ull;
-    if (bonus) {
+      for (int j = 0; j < kBatch; ++j)
+        s += (exp2_fast(fmaf(t4[j].x, kLog2eF, -mb)) + exp2_fast(fmaf(t4[j].y, kLog2eF, -mb))) +
+             (exp2_fast(fmaf(t4[j].z, kLog2eF, -mb)) + exp2_fast(fmaf(t4[j].w, kLog2eF, -mb)));
+      if (bonus) {
+        if (zbest == -INFINITY) {
+          // seed the race with the largest logit of the batch
+          int cs = 0;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int v = v0 + 4 * tid + 4 * kRowThreads * j;
-        if (v < v1) {
-          const uint4 rw = rng4(key, kStreamBonus, (uint32_t)b, (uint32_t)(jrow + 1), (uint32_t)(v >> 2));
-          const float tv[4] = {t4[j].x, t4[j].y, t4[j].z, t4[j].w};
-          const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+          for (int j = kBatch - 1; j >= 0; --j) {
+            if (t4[j].w == bm) cs = 4 * j + 3;
+            if (t4[j].z == bm) cs = 4 * j + 2;
+            if (t4[j].y == bm) cs = 4 * j + 1;
+            if (t4[j].x == bm) cs = 4 * j;
+          }
+          bestv = vb + kStride * (cs >> 2) + (cs & 3);
+          zbest = bm + gumbel_noise_at(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)bestv);
+        }
+        // screen on the high 16 random bits (see the draft race)
+        const float b32 = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f) * 32768.0f;
+        uint32_t cand = 0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const unsigned long long kz = argmax_key(tv[q] + gumbel_noise(words[q]), v + q);
-            best = kz > best ? kz : best;
+        for (int j = 0; j < kBatch; ++j) {
+          const int v = vb + kStride * j;
+          if (v < v1) {
+            const uint4 ra = rng_call(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)(v >> 3));
+            const float tv[4] = {t4[j].x, t4[j].y, t4[j].z, t4[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t vq = (uint32_t)(v + q);
+              const uint32_t w = word_of(ra, (vq >> 1) & 3u);
+              const uint32_t hb = (vq & 1u) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);
+              const float e = exp2_fast(fmaf(tv[q], kLog2eF, -mb));
+              if (__uint_as_float(0x47000000u | hb) > fmaf(-e, b32, 65535.0f)) cand |= 1u << (4 * j + q);
+            }
+          }
+        }
+#pragma unroll 1
+        while (cand) {
+          const int c = __ffs(cand) - 1;
+          cand &= cand - 1;
+          const int v = vb + kStride * (c >> 2) + (c & 3);
+          const float z = __ldcs(Trow + v) + gumbel_noise_at(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)v);
+          if (z > zbest || (z == zbest && v < bestv)) {
+            zbest = z;
+            bestv = v;
           }
         }
       }
     }
-    warp_softmax_reduce(m, s, 0xffffffffu, 32);
-    best = warp_max_u64(best, 0xffffffffu, 32);
-    if (lane == 0) {
-      s_m[wid] = m;
-      s_s[wid] = s;
-      s_k[wid] = best;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float M = s_m[0], S = s_s[0];
-      unsigned long long K = s_k[0];
-      for (int w = 1; w < kRowThreads / 32; ++w) {
-        softmax_merge(M, S, s_m[w], s_s[w]);
-        K = s_k[w] > K ? s_k[w] : K;
+    const float2 ms = block_softmax(m, s, s_red);
+    unsigned long long best = (bonus && bestv >= 0) ? argmax_key(zbest, bestv) : 0ull;
+    if (bonus) {
+      best = warp_max_u64(best, 0xffffffffu, 32);
+      if (lane == 0) s_k[wid] = best;
+      __syncthreads();
+      if (tid == 0) {
+        for (int w = 1; w < kRowThreads / 32; ++w) best = s_k[w] > best ? s_k[w] : best;
+        if (best) atomicMax(&bonus_key[b], best);
       }
-      row_part[(size_t)rowid * nsegs + seg] = make_float2(M, S);
-      if (bonus) atomicMax(&bonus_key[b], K);
     }
+    if (tid == 0) row_part[(size_t)rowid * nsegs + seg] = ms;
     __syncthreads();
     if (bad) record_status(status, DSPARK_ERR_NONFINITE);
   }
@@ -221,8 +282,8 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
   const int v_begin = blockIdx.x * kDraftSlice, v_end = min(V, v_begin + kDraftSlice);
   unsigned long long k1 = 0ull;
   for (int v4 = v_begin + 4 * tid; v4 < v_end; v4 += 4 * kRowThreads) {
-    const uint4 rw = rng4(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v4 >> 2));
-    const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+    const uint4 ra = rng_call(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v4 >> 3));
+    const uint4 rb = rng_call(key, kStreamResidual + 4u, (uint32_t)b, (uint32_t)ks, (uint32_t)(v4 >> 2));
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int v = v4 + q;
@@ -232,7 +293,8 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
       const float pt = expf(Trow[v] - lt);
       const float rho = pt - pd;
       if (rho > 0.f) {
-        const unsigned long long kz = argmax_key(logf(rho) + gumbel_noise(words[q]), v);
+        const uint32_t m = (gumbel_hi16(ra, (uint32_t)v) << 7) | (word_of(rb, (uint32_t)q) >> 25);
+        const unsigned long long kz = argmax_key(logf(rho) + gumbel_from_bits(m), v);
         k1 = kz > k1 ? kz : k1;
       }
     }
@@ -266,12 +328,13 @@ verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKe
   unsigned long long best = 0ull;
   for (int v = 4 * threadIdx.x; v < V; v += 4 * kRowThreads) {
     const float4 t4 = *reinterpret_cast<const float4*>(Trow + v);
-    const uint4 rw = rng4(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v >> 2));
+    const uint4 ra = rng_call(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v >> 3));
+    const uint4 rb = rng_call(key, kStreamResidual + 4u, (uint32_t)b, (uint32_t)ks, (uint32_t)(v >> 2));
     const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-    const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const unsigned long long kz = argmax_key(tv[q] + gumbel_noise(words[q]), v + q);
+      const uint32_t m = (gumbel_hi16(ra, (uint32_t)(v + q)) << 7) | (word_of(rb, (uint32_t)q) >> 25);
+      const unsigned long long kz = argmax_key(tv[q] + gumbel_from_bits(m), v + q);
       best = kz > best ? kz : best;
     }
   }

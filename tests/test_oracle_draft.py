@@ -155,7 +155,7 @@ def test_draft_margin_is_top_two_gap():
     rng = np.random.default_rng(4)
     l = rng.normal(0, 2, V)
     v, m = oracle.gumbel_argmax(l, 5, 6, 0, 1, 2)
-    z = np.array([l[i] + oracle.gumbel(oracle.rng_word(5, 6, 0, 1, 2, i)) for i in range(V)])
+    z = np.array([l[i] + oracle.gumbel_noise(5, 6, 0, 1, 2, i) for i in range(V)])
     srt = np.sort(z)
     assert v == int(np.argmax(z))
     assert m == pytest.approx(srt[-1] - srt[-2], abs=1e-12)
@@ -239,6 +239,6 @@ def test_draft_uses_stream0_counter_layout():
         prev = anchor[b]
         for k in range(1, G + 1):
             l = oracle.draft_logits(U[b, k - 1], W1, W2, prev)
-            z = [l[v] + oracle.gumbel(oracle.rng_word(seed, rnd, 0, b, k, v)) for v in range(V)]
+            z = [l[v] + oracle.gumbel_noise(seed, rnd, 0, b, k, v) for v in range(V)]
             assert out["x"][b, k - 1] == int(np.argmax(z))
             prev = out["x"][b, k - 1]
