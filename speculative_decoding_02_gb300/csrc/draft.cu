@@ -178,7 +178,7 @@ cudaError_t run_draft(const DraftArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream) {
-  if (draft_tc_supported(a.wdtype, a.r)) return launch_markov_draft_tc(a, stream);
+  if (draft_tc_supported(a.wdtype, a.r, a.V)) return launch_markov_draft_tc(a, stream);
   return a.wdtype == DSPARK_BF16 ? run_draft<DSPARK_BF16>(a, stream) : run_draft<DSPARK_F32>(a, stream);
 }
 

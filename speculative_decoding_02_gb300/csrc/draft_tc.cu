@@ -35,22 +35,25 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128;             // requests per M tile (TMEM lanes)
-constexpr int BN = 64;              // vocabulary columns per tile
+constexpr int BN = 64;              // vocabulary columns per tile (epilogue and U unit)
+constexpr int kGroup = 3;           // tiles per MMA: N = 64 x (up to 3)
+constexpr int kAccCols = kGroup * BN;  // 192 TMEM columns per accumulator
 constexpr int KR = 256;             // Markov rank handled by this kernel
 constexpr int kAtoms = KR / 64;     // 64-wide K atoms (128 bytes of bf16)
-constexpr int kWStages = 6;         // W2 atom ring
+constexpr int kWStages = 4;         // W2 atom ring (one MMA's worth)
 constexpr int kUStages = 3;         // U tile ring
 constexpr int kUBox = 32;           // fp32 columns per U box (128 bytes, swizzled)
 constexpr int kThreads = 576;
 constexpr int kEpiWarps = 16;       // four warps per TMEM lane quarter
-constexpr uint32_t kTmemCols = 128;  // two 64-column accumulators
+constexpr uint32_t kTmemCols = 512;  // two accumulators, then E
+constexpr uint32_t kTmemE = 2 * kAccCols;   // first TMEM column of E (128 x 256 bf16)
 
-constexpr int kEBytes = kAtoms * BM * 128;       // 65536
-constexpr int kWStageBytes = BN * 128;           // 8192
+constexpr int kWStageBytes = kAccCols * 128;     // 24576: 192 W2 rows x 64 K (bf16), swizzled
 constexpr int kUStageBytes = BN * BM * 4;        // 32768: two [rows x 32] boxes
 constexpr int kXBytes = 4 * BM * (4 + 4 + 8);     // combine scratch: 4 parts x 128 rows
+constexpr int kBarBytes = 512;                   // mbarriers and flags
 constexpr int kSmemBytes =
-    1024 /*align*/ + kEBytes + kWStages * kWStageBytes + kUStages * kUStageBytes + 256 + kXBytes;
+    1024 /*align*/ + kWStages * kWStageBytes + kUStages * kUStageBytes + kBarBytes + kXBytes;
 
 struct __align__(8) Barriers {
   uint64_t full_w[kWStages], empty_w[kWStages];
@@ -61,6 +64,8 @@ struct __align__(8) Barriers {
   int abort;
   int stop;   // epilogue-wide decision to leave the position loop
 };
+static_assert(sizeof(Barriers) <= kBarBytes, "barrier block overflows its shared-memory slot");
+static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may use");
 
 enum Mode { kDraft = 0, kResidual = 1 };
 
@@ -117,84 +122,141 @@ __device__ __forceinline__ float race_bound(float run_m, float zbest) {
   return exp2f((run_m - zbest) * kLog2e) * (1.0f + 0x1p-10f);
 }
 
-// Folds the fused logits l[0..nv) of columns v0.. into the race.  Candidates
-// are resolved as they are met, with the random word and logit still in
-// registers, and each one that wins tightens the bound for the rest.  The
-// bound uses zthr, the best perturbed logit known for the whole row (this
-// thread's own or one published by any CTA): an entry below it cannot win.
+// The 16 high random bits of this thread's columns: 32-bit word j of `wv`
+// holds the bits of columns v0 + 2j (low half) and v0 + 2j + 1 (high half).
+// v0 is a multiple of min(CPP, 8), so every index below is known at compile
+// time except, for CPP = 4, which half of the call's four words is used.
 template <int CPP>
-__device__ __forceinline__ void race_tile(RowRace& st, float (&l)[CPP], int nv, int v0, unsigned char* spill,
-                                          int j0, int sw, const RngKey& key, uint32_t req, uint32_t pos) {
-  float tm = -INFINITY;
-  if (nv >= CPP) {
+__device__ __forceinline__ void race_words(uint32_t (&wv)[(CPP + 1) / 2], const RngKey& key, uint32_t stream,
+                                           uint32_t req, uint32_t pos, int v0) {
+  if constexpr (CPP >= 8) {
 #pragma unroll
-    for (int c = 0; c < CPP; ++c) tm = fmaxf(tm, l[c]);
+    for (int j = 0; j < CPP / 8; ++j) {
+      const uint4 ra = rng_call(key, stream, req, pos, ((uint32_t)v0 >> 3) + j);
+      wv[4 * j] = ra.x; wv[4 * j + 1] = ra.y; wv[4 * j + 2] = ra.z; wv[4 * j + 3] = ra.w;
+    }
   } else {
-#pragma unroll
-    for (int c = 0; c < CPP; ++c)
-      if (c < nv) tm = fmaxf(tm, l[c]);
+    static_assert(CPP == 4, "4, 8 or 16 columns per thread");
+    const uint4 ra = rng_call(key, stream, req, pos, (uint32_t)v0 >> 3);
+    const bool up = (v0 & 4) != 0;
+    wv[0] = up ? ra.z : ra.x;
+    wv[1] = up ? ra.w : ra.y;
   }
+}
+
+// 32768 + h/2 built exactly as a float from the high 16 bits h of column c
+// (c is a constant once the callers' loops are unrolled).
+template <int CPP>
+__device__ __forceinline__ float race_hf(const uint32_t (&wv)[(CPP + 1) / 2], int c) {
+  const uint32_t w = wv[c >> 1];
+  const uint32_t hb = (c & 1) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);   // h << 7
+  return __uint_as_float(0x47000000u | hb);
+}
+
+// Folds the new running maximum of this tile's fused logits into the online
+// softmax state.  Columns past the vocabulary hold -inf.
+template <int CPP>
+__device__ __forceinline__ void race_prep(RowRace& st, const float (&l)[CPP]) {
+  float tm = l[0];
+#pragma unroll
+  for (int c = 1; c < CPP; ++c) tm = fmaxf(tm, l[c]);
   if (tm > st.run_m) {
     st.run_s = (st.run_m == -INFINITY) ? 0.f : st.run_s * exp2f((st.run_m - tm) * kLog2e);
     st.run_m = tm;
-    if (st.zbest == -INFINITY) {
-      // seed the race with this tile's largest logit
-      int cs = 0;
-#pragma unroll
-      for (int c = CPP - 1; c >= 0; --c)
-        if (c < nv && l[c] == tm) cs = c;
-      const int v = v0 + cs;
-      st.zbest = tm + gumbel_noise_at(key, kStreamDraft, req, pos, (uint32_t)v);
-      st.best_v = v;
-      st.zthr = fmaxf(st.zthr, st.zbest);
-    }
     st.bound = race_bound(st.run_m, st.zthr);
   }
+}
+
+// Opens the race of a row part: of this tile's columns, the one most likely to
+// hold the largest perturbed logit -- largest e_v / (1 - u_v), with u_v from
+// the 16 high bits, a monotone stand-in for l_v + G_v -- is resolved exactly
+// and becomes the part's best.  Its softmax term is added here and its logit
+// set to -inf, so the screen that follows does not meet it again.
+template <int CPP>
+__device__ __forceinline__ void race_seed(RowRace& st, float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2], int v0,
+                                          const RngKey& key, uint32_t req, uint32_t pos) {
   const float mb = st.run_m * kLog2e;
-  // Screen on the high 16 bits h of each uniform: since
-  // E_v >= 1 - u_v > (65535 - h) / 65536, entry v can only win when
-  // h > 65535 - 65536 exp(l_v - zthr), i.e. when 32768 + h/2 (built exactly as
-  // a float from the bits) exceeds 65535.5 - 32768 e bound; half a step of
-  // slack absorbs the rounding of the threshold.
-  const float b32 = st.bound * 32768.0f;
-  uint32_t cand = 0;
-  uint4 ra = make_uint4(0, 0, 0, 0);
+  float be = 0.f, bd = 1.f, bl = -INFINITY, bh = 0.f;
+  int bc = -1;
 #pragma unroll
   for (int c = 0; c < CPP; ++c) {
-    if (c % 8 == 0) ra = rng_call(key, kStreamDraft, req, pos, (uint32_t)(v0 + c) >> 3);
-    if (c < nv) {
-      const uint32_t v = (uint32_t)(v0 + c);
-      const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
-      st.run_s += e;
-      const uint32_t w = word_of(ra, (v >> 1) & 3u);
-      const uint32_t hb = (v & 1u) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);   // h << 7
-      const float hf = __uint_as_float(0x47000000u | hb);                                 // 32768 + h/2
-      if (hf > fmaf(-e, b32, 65535.0f)) cand |= 1u << c;
-    }
+    const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
+    const float d = fmaf(-2.0f, race_hf<CPP>(wv, c), 131072.0f);   // 65536 - h, exactly
+    if (e * bd > be * d || bc < 0) { be = e; bd = d; bl = l[c]; bh = race_hf<CPP>(wv, c); bc = c; }
   }
-  if (cand) {
-    // rare: park the logits, then let the full uniforms decide, one entry at a time
+  const uint32_t v = (uint32_t)(v0 + bc);
+  const uint32_t hi = (uint32_t)(int)fmaf(2.0f, bh, -65536.0f);   // h, exactly
+  st.zbest = bl + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamDraft, req, pos, v));
+  st.best_v = (int)v;
+  st.zthr = fmaxf(st.zthr, st.zbest);
+  st.bound = race_bound(st.run_m, st.zthr);
+  st.run_s += be;
 #pragma unroll
-    for (int c = 0; c < CPP; c += 4)
-      *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(l[c], l[c + 1], l[c + 2], l[c + 3]);
+  for (int c = 0; c < CPP; ++c)
+    if (c == bc) l[c] = -INFINITY;
+}
+
+// Rare path of the screen: rebuilds the candidate mask, parks the logits in
+// `spill` and lets the full uniforms decide, one entry at a time; each winner
+// tightens the bound for the rest.
+template <int CPP>
+__device__ __forceinline__ void race_resolve(RowRace& st, const float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2], int v0,
+                                          unsigned char* spill, int j0, int sw, const RngKey& key, uint32_t req,
+                                          uint32_t pos) {
+  const float mb = st.run_m * kLog2e;
+  const float b32 = st.bound * 32768.0f;
+  uint32_t cand = 0;
+#pragma unroll
+  for (int c = 0; c < CPP; ++c) {
+    const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
+    if (fmaf(e, b32, race_hf<CPP>(wv, c)) > 65535.0f) cand |= 1u << c;
+  }
+#pragma unroll
+  for (int c = 0; c < CPP; c += 4)
+    *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(l[c], l[c + 1], l[c + 2], l[c + 3]);
 #pragma unroll 1
-    while (cand) {
-      const int c = __ffs(cand) - 1;
-      cand &= cand - 1;
-      const uint32_t v = (uint32_t)(v0 + c);
-      const uint32_t hi = gumbel_hi16(rng_call(key, kStreamDraft, req, pos, v >> 3), v);
-      const float lc = reinterpret_cast<const float*>(spill + (((j0 + c / 4) ^ sw) << 4))[c & 3];
-      const float z = lc + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamDraft, req, pos, v));
-      if (z > st.zbest) {
-        st.zbest = z;
-        st.best_v = (int)v;
-        if (z > st.zthr) {
-          st.zthr = z;
-          st.bound = race_bound(st.run_m, st.zthr);
-        }
+  while (cand) {
+    const int c = __ffs(cand) - 1;
+    cand &= cand - 1;
+    const uint32_t v = (uint32_t)(v0 + c);
+    const uint32_t hi = gumbel_hi16(rng_call(key, kStreamDraft, req, pos, v >> 3), v);
+    const float lc = reinterpret_cast<const float*>(spill + (((j0 + c / 4) ^ sw) << 4))[c & 3];
+    const float z = lc + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamDraft, req, pos, v));
+    if (z > st.zbest) {
+      st.zbest = z;
+      st.best_v = (int)v;
+      if (z > st.zthr) {
+        st.zthr = z;
+        st.bound = race_bound(st.run_m, st.zthr);
       }
     }
   }
+}
+
+// Screens this tile's columns against the best perturbed logit known for the
+// row (zthr) and adds their softmax terms.  On the high 16 bits h of each
+// uniform: E_v = -log u_v > (65535 - h) / 65536, so entry v can only win when
+// h > 65535 - 65536 exp(l_v - zthr), i.e. when 32768 + h/2 (built exactly as
+// a float from the bits) plus 32768 e_v bound exceeds 65535.5, where
+// e_v = exp(l_v - run_m) and bound = exp(run_m - zthr) (2^-10 over).  The test
+// uses 65535: half a step of slack absorbs the rounding of the fused product.
+// Only the largest left-hand side is kept; the rare tile that passes goes to
+// race_resolve.
+template <int CPP>
+__device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2], int v0,
+                                            unsigned char* spill, int j0, int sw, const RngKey& key, uint32_t req,
+                                            uint32_t pos) {
+  const float mb = st.run_m * kLog2e;
+  const float b32 = st.bound * 32768.0f;
+  float smax = 0.f, s = 0.f;
+#pragma unroll
+  for (int c = 0; c < CPP; ++c) {
+    const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
+    s += e;
+    smax = fmaxf(smax, fmaf(e, b32, race_hf<CPP>(wv, c)));
+  }
+  st.run_s += s;
+  if (smax > 65535.0f) race_resolve<CPP>(st, l, wv, v0, spill, j0, sw, key, req, pos);
 }
 
 // Race of the residual resample: argmax_v log rho_v + G_v over rho_v > 0,
@@ -305,11 +367,10 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   constexpr int CPP = BN / kParts;         // columns per thread per tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  unsigned char* E_s = smem;
-  unsigned char* W_s = E_s + kEBytes;
+  unsigned char* W_s = smem;
   unsigned char* U_s = W_s + kWStages * kWStageBytes;
   Barriers* bars = reinterpret_cast<Barriers*>(U_s + kUStages * kUStageBytes);
-  unsigned char* X_s = reinterpret_cast<unsigned char*>(bars) + 256;   // combine scratch
+  unsigned char* X_s = reinterpret_cast<unsigned char*>(bars) + kBarBytes;   // combine scratch
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mtile = blockIdx.x / p.ctas_per_mtile;
@@ -347,8 +408,10 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     uint32_t wcount = 0, ucount = 0;
     bool ok = true;
     for (int k = kf; k <= kl && ok; ++k) {
-      for (int i = 0; i < ntl && ok; ++i) {
-        const int v0 = (t0 + i) * BN;
+      for (int g = 0; g < ntl && ok; g += kGroup) {
+        // the W2 rows of up to kGroup tiles, one K atom at a time (rows past
+        // the CTA's range or past V are loaded or zero-filled but not used)
+        const int v0 = (t0 + g) * BN;
         for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
           const int s = wcount % kWStages;
           ok = mbar_wait(&bars->empty_w[s], ((wcount / kWStages) & 1) ^ 1, abort, p.status);
@@ -359,18 +422,22 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         }
         if (!ok) break;
         if constexpr (MODE == kResidual) continue;
-        const int su = ucount % kUStages;
-        ok = mbar_wait(&bars->empty_u[su], ((ucount / kUStages) & 1) ^ 1, abort, p.status);
-        if (!ok) break;
-        if (lane == 0) {
-          // two [R rows x 32 columns] boxes of U[m0.., k-1, v0..]; rows past B and
-          // columns past V are filled with zeros by the copy engine
-          mbar_arrive_expect_tx(&bars->full_u[su], (uint32_t)(2 * kUBox * R * 4));
-          unsigned char* dst = U_s + su * kUStageBytes;
-          tma_g2s_3d(dst, &u_map, v0, k - 1, m0, &bars->full_u[su], pol_u);
-          tma_g2s_3d(dst + R * 128, &u_map, v0 + kUBox, k - 1, m0, &bars->full_u[su], pol_u);
+        const int nsub = min(kGroup, ntl - g);
+        for (int j = 0; j < nsub && ok; ++j) {
+          const int su = ucount % kUStages;
+          ok = mbar_wait(&bars->empty_u[su], ((ucount / kUStages) & 1) ^ 1, abort, p.status);
+          if (!ok) break;
+          if (lane == 0) {
+            // two [R rows x 32 columns] boxes of U[m0.., k-1, v..]; rows past B and
+            // columns past V are filled with zeros by the copy engine
+            const int v = v0 + j * BN;
+            mbar_arrive_expect_tx(&bars->full_u[su], (uint32_t)(2 * kUBox * R * 4));
+            unsigned char* dst = U_s + su * kUStageBytes;
+            tma_g2s_3d(dst, &u_map, v, k - 1, m0, &bars->full_u[su], pol_u);
+            tma_g2s_3d(dst + R * 128, &u_map, v + kUBox, k - 1, m0, &bars->full_u[su], pol_u);
+          }
+          ++ucount;
         }
-        ++ucount;
       }
     }
     // drain: every copy this warp issued has landed before the CTA exits
@@ -383,31 +450,31 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN);
-      const uint32_t e_addr = smem_u32(E_s);
-      uint32_t wcount = 0, it = 0;
+      uint32_t wcount = 0, gcount = 0;
       bool ok = true;
       for (int k = kf; k <= kl && ok; ++k) {
         ok = mbar_wait(&bars->e_full, (uint32_t)(k - kf) & 1, abort, p.status);
         tc_fence_after();
-        for (int i = 0; i < ntl && ok; ++i, ++it) {
-          const int acc = it & 1;
-          ok = mbar_wait(&bars->acc_empty[acc], ((it >> 1) & 1) ^ 1, abort, p.status);
+        for (int g = 0; g < ntl && ok; g += kGroup, ++gcount) {
+          // one MMA tile: up to kGroup vocabulary tiles, N = 64 per tile
+          const int acc = gcount & 1;
+          ok = mbar_wait(&bars->acc_empty[acc], ((gcount >> 1) & 1) ^ 1, abort, p.status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d_tmem = tmem + acc * BN;
+          const uint32_t idesc = idesc_bf16_f32(BM, BN * min(kGroup, ntl - g));
+          const uint32_t d_tmem = tmem + acc * kAccCols;
           for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
             const int s = wcount % kWStages;
             ok = mbar_wait(&bars->full_w[s], (wcount / kWStages) & 1, abort, p.status);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t w_addr = smem_u32(W_s + s * kWStageBytes);
+            // A = E in TMEM: K elements 64a + 16kk .. are columns 32a + 8kk ..;
+            // B = the atom's W2 rows, advanced 32 bytes per K step of 16
+            const uint64_t bd0 = sw128_kmajor_desc(smem_u32(W_s + s * kWStageBytes));
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sw128_kmajor_desc(e_addr + a * (BM * 128) + kk * 32);
-              const uint64_t bd = sw128_kmajor_desc(w_addr + kk * 32);
-              umma_bf16(d_tmem, ad, bd, idesc, (a | kk) != 0);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_tmem_a(d_tmem, tmem + kTmemE + a * 32 + kk * 8, bd0 + (uint64_t)(kk * 2), idesc,
+                               (a | kk) != 0);
             umma_commit(&bars->empty_w[s]);
           }
           if (ok) umma_commit(&bars->acc_full[acc]);
@@ -430,7 +497,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     float* xs = xm + 4 * BM;
     unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 4 * BM);
     float* spill = reinterpret_cast<float*>(U_s + ((warp - 2) * 32 + lane) * 144);   // residual mode only
-    uint32_t it = 0;
+    uint32_t it = 0, gcount = 0;
     for (int k = kf; k <= kl; ++k) {
       bool active = r < rows_valid;
       int ks = k;                           // position of this row
@@ -439,7 +506,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         active = ks > 0;
       }
 
-      // gather E[m, :] = W1[x_{k-1}] for K atom h (16-byte chunks, swizzled)
+      // E[m, 64h .. 64h+63] = W1[x_{k-1}] (K atom h) into TMEM lane m,
+      // columns kTmemE + 32h .. (two bf16 per column, lower k in the low half)
       int prev = 0;
       if (active) {
         int raw;
@@ -450,12 +518,14 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         prev = checked_token(raw, p.V, p.status);
       }
       const uint4* wrow = reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * KR);
+      uint32_t ev[32];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint4 val = active ? __ldg(wrow + h * 8 + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(E_s + h * (BM * 128) + m * 128 + ((c ^ (m & 7)) << 4)) = val;
+        ev[4 * c] = val.x; ev[4 * c + 1] = val.y; ev[4 * c + 2] = val.z; ev[4 * c + 3] = val.w;
       }
-      fence_proxy_async_smem();
+      tmem_store_32cols(tmem + ((uint32_t)(q * 32) << 16) + kTmemE + h * 32, ev);
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->e_full);
 
@@ -477,8 +547,13 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         }
       }
       bool ok = true;
+      unsigned long long gk = 0ull;   // row key as last read (kShare)
       for (int i = 0; i < ntl; ++i, ++it) {
-        const int acc_i = it & 1;
+        // tiles i come kGroup to an accumulator: wait for it at the first,
+        // hand it back after reading the last
+        const int sub = i % kGroup;
+        const bool last_sub = sub == kGroup - 1 || i == ntl - 1;
+        const int acc_i = gcount & 1;
         const int v0 = (t0 + i) * BN + part * CPP;
         const int nv = min(CPP, p.V - v0);
         float uu[CPP], tt[CPP];
@@ -496,30 +571,61 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
             }
           }
         }
-        if (!mbar_wait(&bars->acc_full[acc_i], (it >> 1) & 1, abort, p.status)) { ok = false; break; }
-        tc_fence_after();
+        const bool got_acc = sub != 0 || mbar_wait(&bars->acc_full[acc_i], (gcount >> 1) & 1, abort, p.status);
+        if (MODE == kResidual && !got_acc) { ok = false; break; }
         float v[CPP];
-        tmem_load_cols<CPP>(tmem + ((uint32_t)(q * 32) << 16) + acc_i * BN + part * CPP, v);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->acc_empty[acc_i]);
+        if (got_acc) {
+          tc_fence_after();
+          tmem_load_cols<CPP>(tmem + ((uint32_t)(q * 32) << 16) + acc_i * kAccCols + sub * BN + part * CPP, v);
+          if (last_sub) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->acc_empty[acc_i]);
+            ++gcount;
+          }
+        }
         if constexpr (MODE == kDraft) {
           const int su = it % kUStages;
-          if (!mbar_wait(&bars->full_u[su], (it / kUStages) & 1, abort, p.status)) { ok = false; break; }
+          const bool got_u = got_acc && mbar_wait(&bars->full_u[su], (it / kUStages) & 1, abort, p.status);
           // this thread's columns: box (part*CPP)/32, 16-byte chunks j0.. of row r,
           // stored at chunk j ^ (r & 7) (128-byte swizzle)
           unsigned char* urow = U_s + su * kUStageBytes + ((part * CPP) / kUBox) * (R * 128) + r * 128;
           const int j0 = ((part * CPP) % kUBox) / 4;
-          if (active && nv > 0) {
+          const bool live = got_u && active && nv > 0;
+          uint32_t wv[(CPP + 1) / 2];
+          if (live) {
 #pragma unroll
             for (int c = 0; c < CPP; c += 4) {
               const float4 u4 = *reinterpret_cast<const float4*>(urow + (((j0 + c / 4) ^ (r & 7)) << 4));
               v[c + 0] += u4.x; v[c + 1] += u4.y; v[c + 2] += u4.z; v[c + 3] += u4.w;
             }
-            // the row's best perturbed logit published so far by any CTA; read
-            // before the tile so that its latency hides behind the arithmetic
-            const unsigned long long gk = kShare ? __ldcg(row_key) : 0ull;
-            race_tile<CPP>(st, v, nv, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k);
+            if (nv < CPP) {
+              // past the end of the vocabulary: out of the softmax and the race
+#pragma unroll
+              for (int c = 0; c < CPP; ++c)
+                if (c >= nv) v[c] = -INFINITY;
+            }
+            race_words<CPP>(wv, p.key, kStreamDraft, (uint32_t)b, (uint32_t)k, v0);
+            race_prep<CPP>(st, v);
+            if (st.zbest == -INFINITY) race_seed<CPP>(st, v, wv, v0, p.key, (uint32_t)b, (uint32_t)k);
+          }
+          if (i == 0) {
+            // the parts of a row pool their seeds before the first screen
+            xm[part * R + r] = live ? st.zthr : -INFINITY;
+            named_bar_sync(1, kEpiWarps * 32);
+            if (live) {
+              float zm = st.zthr;
+#pragma unroll
+              for (int j = 0; j < kParts; ++j) zm = fmaxf(zm, xm[j * R + r]);
+              if (zm > st.zthr) {
+                st.zthr = zm;
+                st.bound = race_bound(st.run_m, st.zthr);
+              }
+            }
+          }
+          if (live) {
+            // the row's best perturbed logit published by any CTA, as read at
+            // the end of the previous tile
             if (kShare && gk) {
               const float zg = argmax_key_value(gk);
               if (zg > st.zthr) {
@@ -527,13 +633,16 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                 st.bound = race_bound(st.run_m, st.zthr);
               }
             }
+            race_screen<CPP>(st, v, wv, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k);
             // share this thread's progress with the other CTAs of the row
             if (kShare && st.best_v >= 0 && st.zbest > st.zpub && st.zbest >= st.zthr) {
               atomicMax(row_key, argmax_key(st.zbest, st.best_v));
               st.zpub = st.zbest;
             }
+            if (kShare) gk = __ldcg(row_key);
           }
           __syncwarp();
+          if (!got_u) { ok = false; break; }
           if (lane == 0) mbar_arrive(&bars->empty_u[su]);
         } else {
           if (active && nv > 0) {
@@ -662,7 +771,7 @@ cudaError_t make_w2_tensor_map(const void* W2, int V, CUtensorMap* map) {
   if (!enc) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {(cuuint64_t)KR, (cuuint64_t)V};
   cuuint64_t strides[1] = {(cuuint64_t)KR * 2};
-  cuuint32_t box[2] = {64, BN};
+  cuuint32_t box[2] = {64, (cuuint32_t)kAccCols};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -686,7 +795,7 @@ cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtens
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-bool draft_tc_supported(int wdtype, int r) { return wdtype == DSPARK_BF16 && r == KR; }
+bool draft_tc_supported(int wdtype, int r, int V) { return wdtype == DSPARK_BF16 && r == KR && V >= kAccCols; }
 
 cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   const WsLayout L = ws_layout(a.B, a.gamma, a.V);

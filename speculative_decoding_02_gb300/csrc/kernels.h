@@ -43,8 +43,8 @@ struct VerifyArgs {
 
 cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream);
 
-// Tensor-core draft (bf16 weights, r = 256); the dispatcher above picks it.
-bool draft_tc_supported(int wdtype, int r);
+// Tensor-core draft (bf16 weights, r = 256, V >= 192); the dispatcher above picks it.
+bool draft_tc_supported(int wdtype, int r, int V);
 cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream);
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
                                const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* resid_k,

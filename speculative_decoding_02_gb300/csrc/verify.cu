@@ -373,7 +373,7 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   verify_decide<<<div_up(a.B * 32, 256), 256, 0, stream>>>(a.T, a.x, a.p_d, a.ell, a.B, a.gamma, a.V, nsegs,
                                                           a.key, row_part, bonus_key, resid_k, resid_lse,
                                                           a.n_out, a.tok_out, status);
-  if (draft_tc_supported(a.wdtype, a.r)) {
+  if (draft_tc_supported(a.wdtype, a.r, a.V)) {
     e = launch_residual_tc(a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, resid_k, resid_lse, resid_key, a.B,
                            a.gamma, a.V, a.key, status, stream);
     if (e != cudaSuccess) return e;
