@@ -144,27 +144,33 @@ __device__ __forceinline__ void race_words(uint32_t (&wv)[(CPP + 1) / 2], const 
   }
 }
 
-// 32768 + h/2 built exactly as a float from the high 16 bits h of column c
-// (c is a constant once the callers' loops are unrolled).
+// 2^23 + h built exactly as a float from the high 16 bits h of column c (c is
+// a constant once the callers' loops are unrolled): one mask or one byte
+// permutation.
 template <int CPP>
 __device__ __forceinline__ float race_hf(const uint32_t (&wv)[(CPP + 1) / 2], int c) {
   const uint32_t w = wv[c >> 1];
-  const uint32_t hb = (c & 1) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);   // h << 7
-  return __uint_as_float(0x47000000u | hb);
+  return __uint_as_float((c & 1) ? __byte_perm(w, 0x4B000000u, 0x7632) : ((w & 0xFFFFu) | 0x4B000000u));
 }
 
-// Folds the new running maximum of this tile's fused logits into the online
-// softmax state.  Columns past the vocabulary hold -inf.
+// Screen threshold on fmaf(e_v, 65536 bound, 2^23 + h): entry v can only win
+// when h > 65535 - 65536 exp(l_v - zthr), i.e. when the exact sum exceeds
+// 2^23 + 65535.  Floats there are integers; one unit of slack absorbs the
+// rounding of the fused product.
+constexpr float kScreenThr = 8454142.0f;   // 2^23 + 65534
+
+// Opens the online softmax state of a row part at its first tile: the running
+// maximum is this tile's largest fused logit.  Later tiles keep it unless the
+// rare path of the screen finds it exceeded.  Columns past the vocabulary hold
+// -inf.
 template <int CPP>
 __device__ __forceinline__ void race_prep(RowRace& st, const float (&l)[CPP]) {
   float tm = l[0];
 #pragma unroll
   for (int c = 1; c < CPP; ++c) tm = fmaxf(tm, l[c]);
-  if (tm > st.run_m) {
-    st.run_s = (st.run_m == -INFINITY) ? 0.f : st.run_s * exp2f((st.run_m - tm) * kLog2e);
-    st.run_m = tm;
-    st.bound = race_bound(st.run_m, st.zthr);
-  }
+  st.run_s = 0.f;
+  st.run_m = tm;
+  st.bound = race_bound(st.run_m, st.zthr);
 }
 
 // Opens the race of a row part: of this tile's columns, the one most likely to
@@ -181,11 +187,11 @@ __device__ __forceinline__ void race_seed(RowRace& st, float (&l)[CPP], const ui
 #pragma unroll
   for (int c = 0; c < CPP; ++c) {
     const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
-    const float d = fmaf(-2.0f, race_hf<CPP>(wv, c), 131072.0f);   // 65536 - h, exactly
+    const float d = 8454144.0f - race_hf<CPP>(wv, c);   // 65536 - h, exactly
     if (e * bd > be * d || bc < 0) { be = e; bd = d; bl = l[c]; bh = race_hf<CPP>(wv, c); bc = c; }
   }
   const uint32_t v = (uint32_t)(v0 + bc);
-  const uint32_t hi = (uint32_t)(int)fmaf(2.0f, bh, -65536.0f);   // h, exactly
+  const uint32_t hi = __float_as_uint(bh) & 0xFFFFu;   // h
   st.zbest = bl + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamDraft, req, pos, v));
   st.best_v = (int)v;
   st.zthr = fmaxf(st.zthr, st.zbest);
@@ -196,21 +202,34 @@ __device__ __forceinline__ void race_seed(RowRace& st, float (&l)[CPP], const ui
     if (c == bc) l[c] = -INFINITY;
 }
 
-// Rare path of the screen: rebuilds the candidate mask, parks the logits in
-// `spill` and lets the full uniforms decide, one entry at a time; each winner
-// tightens the bound for the rest.
+// Rare path of the screen.  Moves the running maximum up to this tile's if it
+// is exceeded, recomputes the tile's softmax terms against it, rebuilds the
+// candidate mask, parks the logits in `spill` and lets the full uniforms
+// decide, one entry at a time; each winner tightens the bound for the rest.
+// Returns the tile's softmax sum.
 template <int CPP>
-__device__ __forceinline__ void race_resolve(RowRace& st, const float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2], int v0,
-                                          unsigned char* spill, int j0, int sw, const RngKey& key, uint32_t req,
-                                          uint32_t pos) {
+__device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2],
+                                              int v0, unsigned char* spill, int j0, int sw, const RngKey& key,
+                                              uint32_t req, uint32_t pos, int* status) {
+  float tm = l[0];
+#pragma unroll
+  for (int c = 1; c < CPP; ++c) tm = fmaxf(tm, l[c]);
+  if (tm > st.run_m) {
+    st.run_s *= exp2f((st.run_m - tm) * kLog2e);
+    st.run_m = tm;
+    st.bound = race_bound(st.run_m, st.zthr);
+  }
   const float mb = st.run_m * kLog2e;
-  const float b32 = st.bound * 32768.0f;
+  const float b16 = st.bound * 65536.0f;
+  float s = 0.f;
   uint32_t cand = 0;
 #pragma unroll
   for (int c = 0; c < CPP; ++c) {
     const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
-    if (fmaf(e, b32, race_hf<CPP>(wv, c)) > 65535.0f) cand |= 1u << c;
+    s += e;
+    if (fmaf(e, b16, race_hf<CPP>(wv, c)) > kScreenThr) cand |= 1u << c;
   }
+  if (!(s <= 3.0e38f)) record_status(status, DSPARK_ERR_NONFINITE);   // a NaN or infinite logit
 #pragma unroll
   for (int c = 0; c < CPP; c += 4)
     *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(l[c], l[c + 1], l[c + 2], l[c + 3]);
@@ -231,32 +250,33 @@ __device__ __forceinline__ void race_resolve(RowRace& st, const float (&l)[CPP],
       }
     }
   }
+  return s;
 }
 
 // Screens this tile's columns against the best perturbed logit known for the
-// row (zthr) and adds their softmax terms.  On the high 16 bits h of each
-// uniform: E_v = -log u_v > (65535 - h) / 65536, so entry v can only win when
-// h > 65535 - 65536 exp(l_v - zthr), i.e. when 32768 + h/2 (built exactly as
-// a float from the bits) plus 32768 e_v bound exceeds 65535.5, where
-// e_v = exp(l_v - run_m) and bound = exp(run_m - zthr) (2^-10 over).  The test
-// uses 65535: half a step of slack absorbs the rounding of the fused product.
-// Only the largest left-hand side is kept; the rare tile that passes goes to
-// race_resolve.
+// row (zthr) and adds their softmax terms e_v = exp(l_v - run_m) (run_m may
+// lag the true maximum: the terms are then above 1, which the merge of the
+// partials allows).  On the high 16 bits h of each uniform:
+// E_v = -log u_v > (65535 - h) / 65536, so entry v can only win when
+// h + 65536 e_v bound > 65535, with bound = exp(run_m - zthr) (2^-10 over).
+// Only the largest left-hand side is kept; a tile that may hold a winner, or
+// whose sum is not finite (a logit far above run_m), goes to race_resolve.
 template <int CPP>
-__device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2], int v0,
-                                            unsigned char* spill, int j0, int sw, const RngKey& key, uint32_t req,
-                                            uint32_t pos) {
+__device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2],
+                                            int v0, unsigned char* spill, int j0, int sw, const RngKey& key,
+                                            uint32_t req, uint32_t pos, int* status) {
   const float mb = st.run_m * kLog2e;
-  const float b32 = st.bound * 32768.0f;
+  const float b16 = st.bound * 65536.0f;
   float smax = 0.f, s = 0.f;
 #pragma unroll
   for (int c = 0; c < CPP; ++c) {
     const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
     s += e;
-    smax = fmaxf(smax, fmaf(e, b32, race_hf<CPP>(wv, c)));
+    smax = fmaxf(smax, fmaf(e, b16, race_hf<CPP>(wv, c)));
   }
+  if (smax > kScreenThr || !(s <= 3.0e38f))
+    s = race_resolve<CPP>(st, l, wv, v0, spill, j0, sw, key, req, pos, status);
   st.run_s += s;
-  if (smax > 65535.0f) race_resolve<CPP>(st, l, wv, v0, spill, j0, sw, key, req, pos);
 }
 
 // Race of the residual resample: argmax_v log rho_v + G_v over rho_v > 0,
@@ -344,7 +364,6 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* counter, uint32_t tar
       record_status(status, DSPARK_ERR_TIMEOUT);
       return false;
     }
-    __nanosleep(64);
   }
   return true;
 }
@@ -606,7 +625,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                 if (c >= nv) v[c] = -INFINITY;
             }
             race_words<CPP>(wv, p.key, kStreamDraft, (uint32_t)b, (uint32_t)k, v0);
-            race_prep<CPP>(st, v);
+            if (st.run_m == -INFINITY) race_prep<CPP>(st, v);
             if (st.zbest == -INFINITY) race_seed<CPP>(st, v, wv, v0, p.key, (uint32_t)b, (uint32_t)k);
           }
           if (i == 0) {
@@ -625,15 +644,24 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           }
           if (live) {
             // the row's best perturbed logit published by any CTA, as read at
-            // the end of the previous tile
-            if (kShare && gk) {
+            // the end of the previous tile: the second tile waits for it
+            // (little is known yet), later tiles take it after their screen
+            // so that the load's latency stays hidden
+            if (kShare && gk && i == 1) {
               const float zg = argmax_key_value(gk);
               if (zg > st.zthr) {
                 st.zthr = zg;
                 st.bound = race_bound(st.run_m, st.zthr);
               }
             }
-            race_screen<CPP>(st, v, wv, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k);
+            race_screen<CPP>(st, v, wv, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k, p.status);
+            if (kShare && gk && i > 1) {
+              const float zg = argmax_key_value(gk);
+              if (zg > st.zthr) {
+                st.zthr = zg;
+                st.bound = race_bound(st.run_m, st.zthr);
+              }
+            }
             // share this thread's progress with the other CTAs of the row
             if (kShare && st.best_v >= 0 && st.zbest > st.zpub && st.zbest >= st.zthr) {
               atomicMax(row_key, argmax_key(st.zbest, st.best_v));
