@@ -8,13 +8,15 @@ requests of the scheduled verify lengths l_r, per round, divided by the round
 time.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                        [--impl gb300|reference]
+                        [--impl gb300|reference] [--no-cpu-baseline] [--no-e2e]
+        python bench.py --profile-draft [--workload NAME]   (the draft alone, for ncu)
 
 Prints one JSON line.  With N > 1 (torchrun) each rank runs an independent
 replica of the workload (the path shards over requests with no exchange), the
 timing is the max over ranks and `value` counts all ranks' tokens.
 """
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -39,6 +41,9 @@ def parse():
     ap.add_argument("--workload", default="batch128")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-draft", action="store_true",
+                    help="run only the Markov draft of the workload a few times (small ncu captures)")
     return ap.parse_args()
 
 
@@ -67,9 +72,51 @@ def round_bytes(w, ell_sum, n_reject):
             + 16 * B * G + 8 * B)         # outputs
 
 
-def draft_bytes_per_position(w):
+def draft_bytes_per_launch(w):
+    """Algorithmic bytes of one draft call (all gamma positions): U once, W2
+    once, the gamma W1 row gathers, x/p/lse out."""
     sw = 2 if w.wdtype == torch.bfloat16 else 4
-    return 4 * w.B * w.V + sw * w.r * w.V + sw * w.B * w.r + 12 * w.B
+    return 4 * w.B * w.gamma * w.V + sw * w.r * w.V + sw * w.B * w.gamma * w.r + 12 * w.B * w.gamma
+
+
+def kernels_per_round(w):
+    """Launches of this library's kernels in one round (cudaMemsetAsync not
+    counted): draft = the persistent tensor-core kernel and its finalize (bf16,
+    r = 256, V >= 192; else a CUDA-core step and finalize per position);
+    confidence; schedule; verify = prep, rows, decide, residual (the draft
+    kernel in residual mode, or its CUDA-core form), residual finalize."""
+    tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
+    return (2 if tc else 2 * w.gamma) + 1 + 1 + 5
+
+
+# Source files of the draft kernel: a committed ncu figure counts only while
+# they are unchanged since the capture.
+DRAFT_SOURCES = ["draft_tc.cu", "tc_common.cuh", "common.cuh"]
+DRAFT_PROFILE = os.path.join(ROOT, "profiles", "draft_step_tc_batch128.md")
+
+
+def draft_source_hash():
+    h = hashlib.sha256()
+    for name in DRAFT_SOURCES:
+        with open(os.path.join(ROOT, "speculative_decoding_02_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def draft_traffic(w):
+    """DRAM bytes (read + write) of one draft launch from the committed ncu
+    summary, or None if it is missing, for another workload, or stale."""
+    try:
+        kv = {}
+        for line in open(DRAFT_PROFILE):
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                kv[k.strip()] = v.strip().strip("`")
+        if kv.get("workload") != w.name or kv.get("source_sha256_16") != draft_source_hash():
+            return None
+        return int(float(kv["dram_bytes_per_launch"]))
+    except Exception:
+        return None
 
 
 class Clocks:
@@ -222,9 +269,21 @@ def run_gpu(args):
     ws = ds.workspace(w.B, w.gamma, w.V, dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
-        ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed,
-                 rnd=i, sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws)
+    dstart = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dend = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    def step(i, rec=None):
+        # the four entry points in the order dspark_round runs them (the same
+        # kernels), with events around the draft for its roofline figure
+        if rec is not None:
+            dstart[rec].record(stream)
+        x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, i, ws=ws)
+        if rec is not None:
+            dend[rec].record(stream)
+        c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
+        ell, _, _ = ds.schedule(c, inp["sps"], w.mode, i, khist, ws)
+        n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, i, ws)
+        return ell, n
 
     for i in range(args.warmup):
         step(i)
@@ -238,12 +297,13 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    outs = []
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         barrier()
         e0.record(stream)
         for i in range(args.steps):
-            step(args.warmup + i)
+            outs.append(step(args.warmup + i, rec=i))
         e1.record(stream)
         barrier()
     ms = e0.elapsed_time(e1)
@@ -251,34 +311,25 @@ def run_gpu(args):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+    st = ds.read_status(ws)
+    if st != ds.OK:
+        raise RuntimeError(f"device status {st} in the timed rounds")
 
-    # verified tokens of the timed rounds (deterministic per round index: replay)
-    ell_sum, n_acc, n_rej = 0, 0, 0
-    for i in range(args.steps):
-        step(args.warmup + i)
-        ell_sum += int(out.ell.sum())
-        n_acc += int(out.n.sum())
-        n_rej += int((out.n < out.ell).sum())
+    ell_sum = sum(int(e.sum()) for e, _ in outs)
+    n_acc = sum(int(n.sum()) for _, n in outs)
+    n_rej = sum(int((n < e).sum()) for e, n in outs)
     per_round = ell_sum / args.steps
     value = world * ell_sum / (ms / 1e3)
 
-    # dominant kernel: the draft (gamma positions) timed alone on the same stream
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = max(3, args.steps // 2)
-    d0.record(stream)
-    for i in range(reps):
-        ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, i, ws=ws)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    draft_ms = d0.elapsed_time(d1) / reps
-    per_pos_s = draft_ms / 1e3 / w.gamma
+    # dominant kernel: the Markov draft, timed inside the timed region
+    draft_ms = float(np.mean([dstart[i].elapsed_time(dend[i]) for i in range(args.steps)]))
     hbm, bf16, peak_kind = peaks()
-    dbytes = draft_bytes_per_position(w)
-    achieved = dbytes / per_pos_s / 1e9
+    dbytes = draft_bytes_per_launch(w)
+    achieved = dbytes / (draft_ms / 1e3) / 1e9
 
     # end to end through host buffers: per-round inputs copied in, results out
     e2e = None
-    if rank == 0:
+    if rank == 0 and not args.no_e2e:
         e2e = run_e2e(w, inp, ds, dev, args, khist)
 
     cpu = None
@@ -295,7 +346,7 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32+bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "gamma": w.gamma, "V": w.V, "r": w.r, "H": w.H,
                        "weights": "bf16" if w.wdtype == torch.bfloat16 else "f32",
                        "l2": "inputs larger than L2 (U+T %.2f GB)" % ((4 * w.B * (2 * w.gamma + 1) * w.V) / 1e9),
@@ -303,13 +354,13 @@ def run_gpu(args):
                        "round_GB": rbytes / 1e9,
                        "round_hbm_frac": rbytes / (ms / args.steps / 1e3) / 1e9 / hbm,
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"kernel": "markov draft, per position (draft step + finalize)", "bound": "hbm",
-                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": None, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": dbytes},
+            "roofline": {"kernel": "markov draft (dspark_markov_draft: draft_step_tc + draft_finalize_tc)",
+                         "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": draft_traffic(w), "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
             "clocks": clk.summary(),
             "e2e": e2e,
-            "gpu_launches": args.steps * (2 * w.gamma + 7),
+            "gpu_launches": args.steps * kernels_per_round(w),
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -359,9 +410,32 @@ def run_e2e(w, inp, ds, dev, args, khist):
             "steps": steps, "wall_s": time.perf_counter() - t0}
 
 
+def run_profile_draft(args):
+    """The Markov draft of the workload alone, 4 calls (for ncu: U, W1, W2 and
+    the anchors are all it holds on the device)."""
+    import speculative_decoding_02_gb300 as ds
+    from speculative_decoding_02_gb300 import build as lib_build
+    from speculative_decoding_02_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    lib_build.build()
+    w = wl.WORKLOADS[args.workload]
+    weights = wl.make_weights(w, dev)
+    U = wl.make_round_inputs(w, 0, dev)["U"]
+    ws = ds.workspace(w.B, w.gamma, w.V, dev)
+    for i in range(4):
+        ds.markov_draft(U, weights["W1"], weights["W2"], weights["anchor"], w.seed, i, ws=ws)
+    torch.cuda.synchronize()
+    st = ds.read_status(ws)
+    print(json.dumps({"profile_draft": w.name, "status": st, "source_sha256_16": draft_source_hash()}))
+    if st != ds.OK:
+        sys.exit(1)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.profile_draft:
+        run_profile_draft(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

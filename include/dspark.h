@@ -28,10 +28,16 @@
  *    is the weight of the bias-free linear layer r -> V as a linear layer stores
  *    it, so the Markov bias of entry v is sum_i W1[prev, i] * W2[v, i]
  *    ([blog] section 4).  wdtype is DSPARK_BF16 or DSPARK_F32 for both.
- *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by `seed`, with
- *    counter (v / 4, position k, request b, (round << 3) | stream), word v % 4;
- *    uniform u = ((w >> 9) + 1/2) / 2^23; Gumbel noise -log(-log u).  Streams:
- *    0 draft, 1 accept test (v = 0), 2 residual, 3 bonus.  `round` < 2^29.
+ *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by
+ *    (seed mod 2^32, seed / 2^32); a call at counter (c, position k, request b,
+ *    (round << 3) | stream) gives four 32-bit words.  Accept uniform (stream 1):
+ *    word 0 of call c = 0, u = ((w >> 9) + 1/2) / 2^23.  Gumbel noise of entry v
+ *    (streams 0 draft, 2 residual, 3 bonus): a 23-bit m = (h << 7) | g with
+ *    h = 16-bit half (v mod 2) (low half first) of word ((v / 2) mod 4) of call
+ *    c = v / 8 of the stream, and g = the top 7 bits of word (v mod 4) of call
+ *    c = v / 4 of stream + 4; u = (m + 1/2) / 2^23, noise -log(-log u).  The high
+ *    bits come first so that a kernel can rule an entry out of a race from h
+ *    alone.  `round` < 2^29.
  *  - Return value: a DSPARK_* status.  Argument errors are detected on the host
  *    before anything is enqueued.  Errors found by the kernels (a bounded wait
  *    that gave up, non-finite logits) are recorded in a status word inside the
