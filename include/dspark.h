@@ -187,6 +187,18 @@ int dspark_markov_draft_noalloc(const float* U, const void* W1, const void* W2, 
                                 uint64_t seed, uint64_t round,
                                 int32_t* x_out, float* p_out, float* lse_out, void* stream);
 
+/*
+ * Self-test of the device-side bounded waits (no counterpart on the pages).
+ * Enqueues one small kernel whose wait can never be satisfied -- mode 0 an
+ * mbarrier that no thread arrives on, mode 1 a grid barrier that expects two
+ * CTAs in a one-CTA grid.  The wait gives up after the library's limit (1 s),
+ * records DSPARK_ERR_TIMEOUT in the status word and the kernel returns; the
+ * CUDA context stays usable.  Read the result with dspark_read_status.
+ * Uses (and overwrites) the first 256 bytes of `workspace` (256-byte aligned,
+ * workspace_bytes >= 256).  Returns DSPARK_ERR_INVALID for another mode.
+ */
+int dspark_selftest_wait_timeout(int mode, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Waits for `stream`, then copies the workspace status word (a DSPARK_* code,
  * the first error any kernel recorded since the last clear) to *host_status and
  * clears it.  Returns DSPARK_OK or DSPARK_ERR_CUDA. */

@@ -57,6 +57,8 @@ def _load():
     L.dspark_round.restype = i32
     L.dspark_read_status.argtypes = [vp, ctypes.POINTER(i32), vp]
     L.dspark_read_status.restype = i32
+    L.dspark_selftest_wait_timeout.argtypes = [i32, vp, sz, vp]
+    L.dspark_selftest_wait_timeout.restype = i32
     L.dspark_strerror.argtypes = [i32]
     L.dspark_strerror.restype = ctypes.c_char_p
     _lib = L
@@ -251,6 +253,14 @@ def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, 
                           _ptr(out.x), _ptr(out.p), _ptr(out.lse), _ptr(out.c), _ptr(out.ell), _ptr(out.nstar),
                           _ptr(out.theta), _ptr(out.n), _ptr(out.tok), _ptr(ws), ws.numel(), _stream(dev)), "round")
     return out
+
+
+def selftest_wait_timeout(mode, ws):
+    """Enqueue the bounded-wait self-test (mode 0: mbarrier, 1: grid barrier);
+    its status word then reads ERR_TIMEOUT (see read_status)."""
+    L = _load()
+    _check(L.dspark_selftest_wait_timeout(int(mode), _ptr(ws), ws.numel(), _stream(ws.device)),
+           "selftest_wait_timeout")
 
 
 def read_status(ws, device=None):

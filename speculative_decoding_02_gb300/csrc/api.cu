@@ -163,6 +163,12 @@ int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
   return cuda_status(launch_verify(va, s));
 }
 
+int dspark_selftest_wait_timeout(int mode, void* workspace, size_t workspace_bytes, void* stream) {
+  if (mode != 0 && mode != 1) return DSPARK_ERR_INVALID;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_WORKSPACE;
+  return cuda_status(launch_selftest_wait(mode, workspace, (cudaStream_t)stream));
+}
+
 int dspark_read_status(void* workspace, int* host_status, void* stream) {
   if (!workspace || !host_status) return DSPARK_ERR_INVALID;
   cudaStream_t s = (cudaStream_t)stream;

@@ -823,6 +823,41 @@ cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtens
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+namespace {
+
+// Self-test of the bounded waits: mode 0 waits on an mbarrier that no thread
+// arrives on, mode 1 at a grid barrier that expects two CTAs in a one-CTA
+// grid.  Either wait gives up after kWaitLimitNs, records DSPARK_ERR_TIMEOUT in
+// `status` and the kernel returns.
+__global__ void selftest_wait_kernel(int mode, unsigned int* counter, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile int* abort = &abort_flag;
+    if (mode == 0)
+      mbar_wait(&bar, 0, abort, status);
+    else
+      grid_barrier(counter, 2u, abort, status);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_wait(int mode, void* ws, cudaStream_t stream) {
+  unsigned int* counter = ws_ptr<unsigned int>(ws, 64);
+  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned int), stream);
+  if (e != cudaSuccess) return e;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(mode, counter, ws_ptr<int>(ws, 0));
+  return cudaGetLastError();
+}
+
 bool draft_tc_supported(int wdtype, int r, int V) { return wdtype == DSPARK_BF16 && r == KR && V >= kAccCols; }
 
 cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {

@@ -45,6 +45,12 @@ cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream);
 
 // Tensor-core draft (bf16 weights, r = 256, V >= 192); the dispatcher above picks it.
 bool draft_tc_supported(int wdtype, int r, int V);
+
+// One small kernel whose wait never completes (mode 0: an mbarrier, mode 1: a
+// grid barrier); it gives up after the library's wait limit and records
+// DSPARK_ERR_TIMEOUT in the workspace status word.  Uses the workspace's first
+// 256 bytes.
+cudaError_t launch_selftest_wait(int mode, void* ws, cudaStream_t stream);
 cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream);
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
                                const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* resid_k,

@@ -79,6 +79,11 @@ def test_host_side_argument_errors(lib):
                              None) == ds.ERR_INVALID
     # confidence: bad dtype
     assert lib.dspark_confidence(p, 3, p, 1, p, None, p, p, 2, 4, 64, 16, 1024, p, None) == ds.ERR_INVALID
+    # bounded-wait self-test: unknown mode, missing / small / misaligned workspace
+    assert lib.dspark_selftest_wait_timeout(2, ws, big, None) == ds.ERR_INVALID
+    assert lib.dspark_selftest_wait_timeout(0, None, big, None) == ds.ERR_WORKSPACE
+    assert lib.dspark_selftest_wait_timeout(1, ws, 128, None) == ds.ERR_WORKSPACE
+    assert lib.dspark_selftest_wait_timeout(0, _fake(0x100010), big, None) == ds.ERR_WORKSPACE
 
 
 def test_binding_requires_cuda_tensors():
