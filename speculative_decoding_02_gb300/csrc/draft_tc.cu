@@ -52,8 +52,14 @@ constexpr int kWStageBytes = kAccCols * 128;     // 24576: 192 W2 rows x 64 K (b
 constexpr int kUStageBytes = BN * BM * 4;        // 32768: two [rows x 32] boxes
 constexpr int kXBytes = 4 * BM * (4 + 4 + 8);     // combine scratch: 4 parts x 128 rows
 constexpr int kBarBytes = 512;                   // mbarriers and flags
+// Residual mode: a shallower W2 ring, and two stages of the U and T row
+// segments of one tile (R rows x 64 columns each, 256-byte rows).
+constexpr int kWStagesRes = 2;
+constexpr int kResStageBytes = 2 * BM * 256;      // U then T
 constexpr int kSmemBytes =
     1024 /*align*/ + kWStages * kWStageBytes + kUStages * kUStageBytes + kBarBytes + kXBytes;
+static_assert(kWStagesRes * kWStageBytes + 2 * kResStageBytes <= kWStages * kWStageBytes + kUStages * kUStageBytes,
+              "residual layout must fit the draft layout");
 
 struct __align__(8) Barriers {
   uint64_t full_w[kWStages], empty_w[kWStages];
@@ -284,14 +290,23 @@ __device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], 
 // E_v < rho_v exp(-zbest), so the same cheap test on the raw random bits
 // applies with rho_v in place of the softmax term.
 struct ResRace {
-  float zbest;
+  float zbest;   // best perturbed value of this thread's entries
   int best_v;
-  float bound;   // exp(-zbest) with a 2^-10 safety margin
+  float zthr;    // best known anywhere in the row (>= zbest)
+  float zpub;    // zbest as last published to the row's key
+  float bound;   // exp(-zthr) with a 2^-10 safety margin
 };
 
+__device__ __forceinline__ void resid_raise(ResRace& st, float z) {
+  if (z > st.zthr) {
+    st.zthr = z;
+    st.bound = expf(-st.zthr) * (1.0f + 0x1p-10f);
+  }
+}
+
 template <int CPP>
-__device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP], int nv, int v0, float* spill,
-                                           const RngKey& key, uint32_t req, uint32_t pos) {
+__device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP], int nv, int v0, unsigned char* spill,
+                                           int j0, int sw, const RngKey& key, uint32_t req, uint32_t pos) {
   if (st.zbest == -INFINITY) {
     float rmax = 0.f;
     int cs = -1;
@@ -302,41 +317,64 @@ __device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP],
     const int v = v0 + cs;
     st.zbest = logf(rmax) + gumbel_noise_at(key, kStreamResidual, req, pos, (uint32_t)v);
     st.best_v = v;
-    st.bound = expf(-st.zbest) * (1.0f + 0x1p-10f);
+    resid_raise(st, st.zbest);
   }
   // the same screen on the high 16 random bits as the draft race, with rho_v
-  // in place of the softmax term
-  const float b32 = st.bound * 32768.0f;
-  uint32_t cand = 0;
-  uint4 ra = make_uint4(0, 0, 0, 0);
+  // in place of the softmax term (only the largest left-hand side is kept;
+  // a tile that may hold a winner rebuilds the candidate mask)
+  uint32_t wv[(CPP + 1) / 2];
+  race_words<CPP>(wv, key, kStreamResidual, req, pos, v0);
+  const float b16 = st.bound * 65536.0f;
+  float smax = 0.f;
 #pragma unroll
-  for (int c = 0; c < CPP; ++c) {
-    if (c % 8 == 0) ra = rng_call(key, kStreamResidual, req, pos, (uint32_t)(v0 + c) >> 3);
-    if (c < nv && rho[c] > 0.f) {
-      const uint32_t v = (uint32_t)(v0 + c);
-      const uint32_t w = word_of(ra, (v >> 1) & 3u);
-      const uint32_t hb = (v & 1u) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);
-      const float hf = __uint_as_float(0x47000000u | hb);
-      if (hf > fmaf(-rho[c], b32, 65535.0f)) cand |= 1u << c;
-    }
-  }
-  if (cand) {
+  for (int c = 0; c < CPP; ++c)
+    if (c < nv) smax = fmaxf(smax, fmaf(fmaxf(rho[c], 0.f), b16, race_hf<CPP>(wv, c)));
+  if (smax > kScreenThr) {
+    uint32_t cand = 0;
 #pragma unroll
-    for (int c = 0; c < CPP; c += 4) *reinterpret_cast<float4*>(spill + c) = make_float4(rho[c], rho[c + 1], rho[c + 2], rho[c + 3]);
+    for (int c = 0; c < CPP; ++c)
+      if (c < nv && rho[c] > 0.f && fmaf(rho[c], b16, race_hf<CPP>(wv, c)) > kScreenThr) cand |= 1u << c;
+#pragma unroll
+    for (int c = 0; c < CPP; c += 4)
+      *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(rho[c], rho[c + 1], rho[c + 2], rho[c + 3]);
 #pragma unroll 1
     while (cand) {
       const int c = __ffs(cand) - 1;
       cand &= cand - 1;
       const uint32_t v = (uint32_t)(v0 + c);
       const uint32_t hi = gumbel_hi16(rng_call(key, kStreamResidual, req, pos, v >> 3), v);
-      const float z = logf(spill[c]) + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamResidual, req, pos, v));
+      const float z = logf(reinterpret_cast<const float*>(spill + (((j0 + c / 4) ^ sw) << 4))[c & 3]) + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamResidual, req, pos, v));
       if (z > st.zbest) {
         st.zbest = z;
         st.best_v = (int)v;
-        st.bound = expf(-st.zbest) * (1.0f + 0x1p-10f);
+        resid_raise(st, z);
       }
     }
   }
+}
+
+// Residual mode: copies the U and T row segments of one 64-column tile
+// starting at column vt into a shared-memory stage, 16 threads to a 256-byte
+// segment (coalesced).  Chunk c of row rr lands at rr * 256 + ((c ^ (rr & 15))
+// << 4) (U), R * 256 further (T), so that row-per-lane reads spread over the
+// banks.  off[rr] / off[BM + rr] are the element offsets of row rr's U / T
+// rows, -1 for a request that did not reject.  Called by every epilogue thread.
+template <int R>
+__device__ __forceinline__ void resid_copy(unsigned char* stage, const long long* off, const float* U,
+                                           const float* T, int vt, int V) {
+  const int tid = threadIdx.x - 64;
+#pragma unroll 1
+  for (int j = 0; j < R / 16; ++j) {
+    const int id = j * (kEpiWarps * 32) + tid;
+    const int tensor = id / (R * 16);
+    const int rem = id - tensor * (R * 16);
+    const int rr = rem >> 4, c16 = rem & 15;
+    const long long o = off[tensor * BM + rr];
+    const int v = vt + c16 * 4;
+    if (o >= 0 && v < V)
+      cp_async16(stage + tensor * (R * 256) + rr * 256 + ((c16 ^ (rr & 15)) << 4), (tensor ? T : U) + o + v);
+  }
+  cp_async_commit();
 }
 
 // R = rows of one request replica (32, 64 or 128).  With B <= 64 the M tile
@@ -386,9 +424,10 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   constexpr int CPP = BN / kParts;         // columns per thread per tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  constexpr int kWSt = MODE == kDraft ? kWStages : kWStagesRes;   // W2 ring depth of this mode
   unsigned char* W_s = smem;
-  unsigned char* U_s = W_s + kWStages * kWStageBytes;
-  Barriers* bars = reinterpret_cast<Barriers*>(U_s + kUStages * kUStageBytes);
+  unsigned char* U_s = W_s + kWSt * kWStageBytes;      // draft: U ring; residual: U/T row stages
+  Barriers* bars = reinterpret_cast<Barriers*>(W_s + kWStages * kWStageBytes + kUStages * kUStageBytes);
   unsigned char* X_s = reinterpret_cast<unsigned char*>(bars) + kBarBytes;   // combine scratch
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -432,8 +471,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         // the CTA's range or past V are loaded or zero-filled but not used)
         const int v0 = (t0 + g) * BN;
         for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
-          const int s = wcount % kWStages;
-          ok = mbar_wait(&bars->empty_w[s], ((wcount / kWStages) & 1) ^ 1, abort, p.status);
+          const int s = wcount % kWSt;
+          ok = mbar_wait(&bars->empty_w[s], ((wcount / kWSt) & 1) ^ 1, abort, p.status);
           if (ok && lane == 0) {
             mbar_arrive_expect_tx(&bars->full_w[s], kWStageBytes);
             tma_g2s_2d(W_s + s * kWStageBytes, &w2_map, a * 64, v0, &bars->full_w[s], pol_w);
@@ -461,8 +500,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     }
     // drain: every copy this warp issued has landed before the CTA exits
     if (lane == 0 && *abort) {
-      for (uint32_t c = (wcount > kWStages ? wcount - kWStages : 0); c < wcount; ++c)
-        mbar_drain(&bars->full_w[c % kWStages], (c / kWStages) & 1);
+      for (uint32_t c = (wcount > (uint32_t)kWSt ? wcount - kWSt : 0); c < wcount; ++c)
+        mbar_drain(&bars->full_w[c % kWSt], (c / kWSt) & 1);
       for (uint32_t c = (ucount > kUStages ? ucount - kUStages : 0); c < ucount; ++c)
         mbar_drain(&bars->full_u[c % kUStages], (c / kUStages) & 1);
     }
@@ -483,8 +522,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           const uint32_t idesc = idesc_bf16_f32(BM, BN * min(kGroup, ntl - g));
           const uint32_t d_tmem = tmem + acc * kAccCols;
           for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
-            const int s = wcount % kWStages;
-            ok = mbar_wait(&bars->full_w[s], (wcount / kWStages) & 1, abort, p.status);
+            const int s = wcount % kWSt;
+            ok = mbar_wait(&bars->full_w[s], (wcount / kWSt) & 1, abort, p.status);
             if (!ok) break;
             tc_fence_after();
             // A = E in TMEM: K elements 64a + 16kk .. are columns 32a + 8kk ..;
@@ -515,7 +554,6 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     float* xm = reinterpret_cast<float*>(X_s);
     float* xs = xm + 4 * BM;
     unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 4 * BM);
-    float* spill = reinterpret_cast<float*>(U_s + ((warp - 2) * 32 + lane) * 144);   // residual mode only
     uint32_t it = 0, gcount = 0;
     for (int k = kf; k <= kl; ++k) {
       bool active = r < rows_valid;
@@ -553,20 +591,33 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       // would turn the exchange into a hot spot: only full 128-row tiles use it
       constexpr bool kShare = (MODE == kDraft) && (R == BM);
       unsigned long long* row_key = (kShare && active) ? p.keys + (size_t)(k - 1) * p.B + b : nullptr;
-      ResRace rs{-INFINITY, -1, INFINITY};
+      ResRace rs{-INFINITY, -1, -INFINITY, -INFINITY, INFINITY};
+      constexpr bool kShareRes = (MODE == kResidual) && (R == BM);
+      unsigned long long* res_key = (kShareRes && active) ? p.resid_key + b : nullptr;
       float ld2 = 0.f, lt2 = 0.f;
-      const float* Urow = nullptr;
-      const float* Trow = nullptr;
       if constexpr (MODE == kResidual) {
         if (active) {
           ld2 = p.lse_d[(size_t)b * p.G + ks - 1] * kLog2e;
           lt2 = p.resid_lse[b] * kLog2e;
-          Urow = p.U + ((size_t)b * p.G + (ks - 1)) * (size_t)p.V;
-          Trow = p.T + ((size_t)b * (p.G + 1) + (ks - 1)) * (size_t)p.V;
         }
       }
       bool ok = true;
       unsigned long long gk = 0ull;   // row key as last read (kShare)
+      // residual mode: the U and T row segments of each tile are copied into
+      // shared memory one tile ahead by all epilogue threads (resid_copy)
+      long long* off_u = reinterpret_cast<long long*>(X_s);   // element offset of row rr's U row, or -1
+      long long* off_t = off_u + BM;
+      if constexpr (MODE == kResidual) {
+        const int tid = threadIdx.x - 64;
+        if (tid < R) {
+          const int bb = m0 + tid;
+          const int kk = bb < p.B ? p.resid_k[bb] : 0;
+          off_u[tid] = kk > 0 ? ((long long)bb * p.G + (kk - 1)) * p.V : -1;
+          off_t[tid] = kk > 0 ? ((long long)bb * (p.G + 1) + (kk - 1)) * p.V : -1;
+        }
+        named_bar_sync(1, kEpiWarps * 32);
+        if (ntl > 0) resid_copy<R>(U_s, off_u, p.U, p.T, t0 * BN, p.V);
+      }
       for (int i = 0; i < ntl; ++i, ++it) {
         // tiles i come kGroup to an accumulator: wait for it at the first,
         // hand it back after reading the last
@@ -575,23 +626,16 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         const int acc_i = gcount & 1;
         const int v0 = (t0 + i) * BN + part * CPP;
         const int nv = min(CPP, p.V - v0);
-        float uu[CPP], tt[CPP];
         if constexpr (MODE == kResidual) {
-          // issue this tile's row loads before waiting for the accumulator
-          if (active && nv > 0) {
-#pragma unroll
-            for (int c = 0; c < CPP; c += 4) {
-              if (c < nv) {
-                const float4 u4 = __ldcs(reinterpret_cast<const float4*>(Urow + v0 + c));
-                const float4 t4 = __ldcs(reinterpret_cast<const float4*>(Trow + v0 + c));
-                uu[c] = u4.x; uu[c + 1] = u4.y; uu[c + 2] = u4.z; uu[c + 3] = u4.w;
-                tt[c] = t4.x; tt[c + 1] = t4.y; tt[c + 2] = t4.z; tt[c + 3] = t4.w;
-              }
-            }
-          }
+          // this tile's rows have landed (own copies, then everyone's); the
+          // barrier also frees the other stage for the next tile's copies.
+          // Every epilogue thread passes here each tile, failed or not.
+          cp_async_wait_all();
+          named_bar_sync(1, kEpiWarps * 32);
+          if (i + 1 < ntl) resid_copy<R>(U_s + ((i + 1) & 1) * kResStageBytes, off_u, p.U, p.T, (t0 + i + 1) * BN, p.V);
         }
         const bool got_acc = sub != 0 || mbar_wait(&bars->acc_full[acc_i], (gcount >> 1) & 1, abort, p.status);
-        if (MODE == kResidual && !got_acc) { ok = false; break; }
+        if (MODE == kResidual && !got_acc) ok = false;
         float v[CPP];
         if (got_acc) {
           tc_fence_after();
@@ -673,16 +717,37 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           if (!got_u) { ok = false; break; }
           if (lane == 0) mbar_arrive(&bars->empty_u[su]);
         } else {
-          if (active && nv > 0) {
-            // rho = max(0, p_t - p_d), kept in place of U (non-positive entries
-            // are outside the residual's support and never race)
+          if (ok && got_acc && active && nv > 0) {
+            // this thread's columns of its row: chunks j0.. of the staged U and
+            // T segments; rho = max(0, p_t - p_d) goes back into the U slots
+            // (non-positive entries are outside the residual's support and
+            // never race)
+            unsigned char* urow = U_s + (i & 1) * kResStageBytes + r * 256;
+            const unsigned char* trow = urow + R * 256;
+            const int j0 = (part * CPP) / 4, sw = r & 15;
+            float uu[CPP];
 #pragma unroll
-            for (int c = 0; c < CPP; ++c) {
-              const float pd = ex2_approx(fmaf(v[c] + uu[c], kLog2e, -ld2));
-              const float pt = ex2_approx(fmaf(tt[c], kLog2e, -lt2));
-              uu[c] = pt - pd;
+            for (int c = 0; c < CPP; c += 4) {
+              const float4 u4 = *reinterpret_cast<const float4*>(urow + (((j0 + c / 4) ^ sw) << 4));
+              const float4 t4 = *reinterpret_cast<const float4*>(trow + (((j0 + c / 4) ^ sw) << 4));
+              const float uv[4] = {u4.x, u4.y, u4.z, u4.w}, tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float pd = ex2_approx(fmaf(v[c + e] + uv[e], kLog2e, -ld2));
+                const float pt = ex2_approx(fmaf(tv[e], kLog2e, -lt2));
+                uu[c + e] = pt - pd;
+              }
             }
-            resid_tile<CPP>(rs, uu, nv, v0, spill, p.key, (uint32_t)b, (uint32_t)ks);
+            // the row's best from other CTAs, read at the end of the previous
+            // tile: waited for at the second tile, taken after the screen later
+            if (kShareRes && gk && i == 1) resid_raise(rs, argmax_key_value(gk));
+            resid_tile<CPP>(rs, uu, nv, v0, urow, j0, sw, p.key, (uint32_t)b, (uint32_t)ks);
+            if (kShareRes && gk && i > 1) resid_raise(rs, argmax_key_value(gk));
+            if (kShareRes && rs.best_v >= 0 && rs.zbest > rs.zpub && rs.zbest >= rs.zthr) {
+              atomicMax(res_key, argmax_key(rs.zbest, rs.best_v));
+              rs.zpub = rs.zbest;
+            }
+            if (kShareRes) gk = __ldcg(res_key);
           }
         }
       }
