@@ -56,6 +56,8 @@ def lib():
         L.oracle_softmax.restype = None
         L.oracle_gumbel_argmax.argtypes = [c_int, vp, c_u64, c_u64, c_u32, c_u32, c_u32, ctypes.POINTER(c_dbl)]
         L.oracle_gumbel_argmax.restype = c_int
+        L.oracle_block_sample.argtypes = [c_int, vp, c_u64, c_u64, c_u32, c_u32, ctypes.POINTER(c_dbl)]
+        L.oracle_block_sample.restype = c_int
         L.oracle_residual.argtypes = [c_int, vp, vp, vp]
         L.oracle_residual.restype = None
         L.oracle_acceptance_label.argtypes = [c_int, vp, vp]
@@ -129,6 +131,14 @@ def u01(word):
 def gumbel_bits(seed, rnd, stream, req, k, v):
     """The 23 random bits of the Gumbel noise of entry v."""
     return int(lib().oracle_gumbel_bits(seed, rnd, stream, req, k, v))
+
+
+def block_sample(l, seed, rnd, req, k):
+    """The draft sampler's draw from softmax(l): (token, margin)."""
+    l = _c(l, np.float64)
+    m = ctypes.c_double(0.0)
+    x = lib().oracle_block_sample(l.size, _ptr(l), seed, rnd, req, k, ctypes.byref(m))
+    return int(x), float(m.value)
 
 
 def u01_bits(m):

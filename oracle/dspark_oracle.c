@@ -207,6 +207,75 @@ int oracle_gumbel_argmax(int V, const double* score, uint64_t seed,
   return arg;
 }
 
+/* The draft sampler: an exact draw from softmax(l) in two levels.
+ *
+ * The vocabulary is cut into blocks of 4 consecutive entries, block j holding
+ * v = 4j .. 4j+3 (the last block may be shorter).  Block j's log-mass is
+ * L_j = log sum_{v in j} exp(l(v)).  A Gumbel-max over the blocks picks
+ * j* = argmax_j L_j + G_j (ties to the smallest j), where G_j = -log(-log u_j)
+ * and u_j = ((w >> 9) + 1/2) / 2^23 from the word w = word (j mod 4) of Philox
+ * call j / 4 of stream 0.  Inside j* the token is drawn by inverse CDF: with
+ * u' from word (j* mod 4) of call j* / 4 of stream 5 (same map to (0, 1)),
+ * x = the first v of j* whose cumulative mass exceeds u' times the block's
+ * mass.  The block wins with probability mass(j) / sum, the token then with
+ * p(v) / mass(j): x is distributed as softmax(l).
+ * *margin is the smaller of the top-two gap of L_j + G_j and the distance of
+ * u' from the nearest inner boundary of the block's CDF (as a fraction of the
+ * block's mass).  Returns -1 when every l(v) is -inf. */
+int oracle_block_sample(int V, const double* l, uint64_t seed, uint64_t round,
+                        uint32_t req, uint32_t k, double* margin) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v)
+    if (l[v] > m) m = l[v];
+  if (m == -INFINITY) {
+    if (margin) *margin = 0.0;
+    return -1;
+  }
+  double best = -INFINITY, second = -INFINITY;
+  int jb = -1;
+  for (int j = 0; 4 * j < V; ++j) {
+    double s = 0.0;
+    for (int v = 4 * j; v < V && v < 4 * j + 4; ++v) s += exp(l[v] - m);
+    if (s == 0.0) continue;
+    uint32_t w = oracle_philox_word(seed, round, 0u, req, k, (uint32_t)j >> 2,
+                                    (uint32_t)j & 3u);
+    double z = m + log(s) + oracle_gumbel_from_bits(w >> 9);
+    if (z > best) {
+      second = best;
+      best = z;
+      jb = j;
+    } else if (z > second) {
+      second = z;
+    }
+  }
+  uint32_t w5 = oracle_philox_word(seed, round, 5u, req, k, (uint32_t)jb >> 2,
+                                   (uint32_t)jb & 3u);
+  double u = oracle_u01(w5);
+  int v0 = 4 * jb, v1 = (4 * jb + 4 < V) ? 4 * jb + 4 : V;
+  double S = 0.0;
+  int last = -1;
+  for (int v = v0; v < v1; ++v) {
+    double e = exp(l[v] - m);
+    S += e;
+    if (e > 0.0) last = v;
+  }
+  double target = u * S, cum = 0.0, dmin = INFINITY;
+  int x = -1;
+  for (int v = v0; v < v1; ++v) {
+    double e = exp(l[v] - m);
+    if (e == 0.0) continue;
+    cum += e;
+    if (x < 0 && target < cum) x = v;
+    if (v != last) {
+      double d = fabs(u - cum / S);
+      if (d < dmin) dmin = d;
+    }
+  }
+  if (x < 0) x = last;
+  if (margin) *margin = fmin(best - second, dmin);
+  return x;
+}
+
 /* Residual of rejection sampling ([digest] item 2: resample at the first
  * divergence): rho(v) = max(0, p_t(v) - p_d(v)), unnormalised. */
 void oracle_residual(int V, const double* p_t, const double* p_d, double* rho) {
@@ -241,7 +310,7 @@ void oracle_draft_probs(int V, int r, const float* U_row, const void* W1,
  * with x0 the anchor token ([blog] section 3: the anchor is the first predicted
  * position's input).  For k = 1..gamma and every request b in [b0, b1):
  *   l = U[b, k-1, :] + B_k(x_{k-1});   lse = log sum exp l;
- *   x_k = argmax_v l(v) + G(seed, round, stream 0, b, k, v);
+ *   x_k = the two-level softmax draw of oracle_block_sample (streams 0 and 5);
  *   p_k(x_k) = exp(l(x_k) - lse).
  * When x_force is given, the previous token of step k >= 2 is taken from it
  * (teacher forcing: each step is checked on the other side's upstream token);
@@ -274,8 +343,8 @@ int oracle_draft(int B, int G, int V, int r, const float* U, const void* W1,
       oracle_draft_logits(V, r, U_row, W1, W2, wdt, prev, l);
       double lse = oracle_logsumexp(V, l);
       double margin = 0.0;
-      int xk = oracle_gumbel_argmax(V, l, seed, round, 0u, (uint32_t)b,
-                                    (uint32_t)k, &margin);
+      int xk = oracle_block_sample(V, l, seed, round, (uint32_t)b, (uint32_t)k,
+                                   &margin);
       size_t o = (size_t)b * G + (k - 1);
       x_out[o] = xk;
       if (p_out) p_out[o] = exp(l[xk] - lse);
