@@ -22,8 +22,12 @@ constexpr uint32_t kPhiloxWeylA = 0x9E3779B9u;
 constexpr uint32_t kPhiloxWeylB = 0xBB67AE85u;
 
 // Random-number streams of one round (the fourth counter word is
-// (round << 3) | stream).
-enum Stream : uint32_t { kStreamDraft = 0, kStreamAccept = 1, kStreamResidual = 2, kStreamBonus = 3 };
+// (round << 3) | stream).  The draft uses stream 0 for its block race and
+// stream 5 for the token inside the winning block; the bonus and residual
+// races take their low noise bits from stream + 4.
+enum Stream : uint32_t {
+  kStreamDraft = 0, kStreamAccept = 1, kStreamResidual = 2, kStreamBonus = 3, kStreamBlockPick = 5
+};
 
 // The key of one round with its ten round keys precomputed on the host, so
 // that kernels read them as constant operands instead of recomputing the
@@ -81,6 +85,33 @@ __device__ __forceinline__ float uniform_bits(uint32_t m) {
 
 // The accept uniform of a position: the top 23 bits of a word.
 __device__ __forceinline__ float uniform01(uint32_t w) { return uniform_bits(w >> 9); }
+
+// Draft sampler: blocks of 4 consecutive tokens race with their log-mass plus
+// Gumbel noise from one 32-bit word each (word j of the draft stream's call
+// sequence: word j mod 4 of call j / 4); the token inside the winning block is
+// drawn by inverse CDF with the uniform of word j of kStreamBlockPick.  Both
+// levels together draw exactly from the softmax.
+
+// Token of block j from the block's four softmax terms e0..e3 (any common
+// scale): the first whose cumulative mass exceeds u times the block's mass, or
+// the last with mass when rounding leaves none.
+__device__ __forceinline__ int block_pick(const RngKey& key, uint32_t req, uint32_t pos, uint32_t j, float e0,
+                                          float e1, float e2, float e3) {
+  const float u = uniform01(word_of(rng_call(key, kStreamBlockPick, req, pos, j >> 2), j & 3u));
+  const float t = u * (((e0 + e1) + e2) + e3);
+  float cum = e0;
+  int c;
+  if (t < cum) {
+    c = 0;
+  } else if (t < (cum += e1)) {
+    c = 1;
+  } else if (t < (cum += e2)) {
+    c = 2;
+  } else {
+    c = e3 > 0.f ? 3 : (e2 > 0.f ? 2 : (e1 > 0.f ? 1 : 0));
+  }
+  return (int)(4u * j) + c;
+}
 
 // Standard Gumbel variate by inversion.  The inner logarithm uses the
 // full-accuracy logf: near u = 1 its result is tiny and a fast approximation

@@ -1,14 +1,17 @@
 // Semi-autoregressive Markov draft ("[DeepSeek-6] DSpark" blog, sections 3-4;
 // study report Eq.4): for each position k the Markov bias of the previous token
-// is added to the backbone logits, and the token is drawn by Gumbel-max while an
-// online softmax accumulates the normaliser.
+// is added to the backbone logits, and the token is drawn from their softmax
+// (a Gumbel race over blocks of 4 tokens on their log-mass, then the inverse
+// CDF inside the winning block) while an online softmax accumulates the
+// normaliser.
 //
 // CUDA-core path: one launch per position.  A CTA owns 32 requests and one
 // kDraftSlice-wide slice of the vocabulary; it gathers the 32 embedding rows
 // W1[x_{k-1}] into shared memory once and walks its slice in 64-column tiles of
 // W2, computing the bias with fp32 FMAs.  Every (request, slice) pair leaves an
-// online-softmax partial (m, s) and pushes its best perturbed logit into a
-// per-request 64-bit argmax key (atomicMax).  A per-position finalize kernel
+// online-softmax partial (m, s) and pushes its best perturbed block log-mass
+// (with the token drawn inside that block) into a per-request 64-bit argmax
+// key (atomicMax).  A per-position finalize kernel
 // merges the partials into lse_k, decodes x_k and recomputes l_k(x_k) to give
 // p_k(x_k).
 #include "kernels.h"
@@ -76,23 +79,36 @@ draft_step_cuda_core(const float* __restrict__ U, const void* __restrict__ W1,
     if (!row_ok) continue;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const int v4 = vt + cg + 4 * q;   // groups of 4 never straddle v_end (V % 8 == 0)
+      // one block of 4 tokens (blocks never straddle v_end: V % 8 == 0)
+      const int v4 = vt + cg + 4 * q;
       if (v4 >= v_end) continue;
-      const uint4 ra = rng_call(key, kStreamDraft, (uint32_t)b, (uint32_t)k, (uint32_t)(v4 >> 3));
-      const uint4 rb = rng_call(key, kStreamDraft + 4u, (uint32_t)b, (uint32_t)k, (uint32_t)(v4 >> 2));
+      float l[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int v = v4 + j;
-        const float l = Urow[v] + acc[4 * q + j];
-        bad |= !isfinite(l);
-        if (l > run_m) {
-          run_s = run_s * expf(run_m - l) + 1.f;
-          run_m = l;
-        } else {
-          run_s += expf(l - run_m);
-        }
-        const uint32_t m = (gumbel_hi16(ra, (uint32_t)v) << 7) | (word_of(rb, (uint32_t)j) >> 25);
-        const unsigned long long kz = argmax_key(l + gumbel_from_bits(m), v);
+        l[j] = Urow[v4 + j] + acc[4 * q + j];
+        bad |= !isfinite(l[j]);
+      }
+      // online softmax over the block's terms, and the block's own log-mass
+      const float m4 = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+      if (m4 == -INFINITY) continue;   // no mass in this block
+      float e[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) e[j] = expf(l[j] - m4);
+      const float s4 = ((e[0] + e[1]) + e[2]) + e[3];
+      if (m4 > run_m) {
+        run_s = (run_m == -INFINITY ? 0.f : run_s * expf(run_m - m4)) + s4;
+        run_m = m4;
+      } else {
+        run_s += s4 * expf(m4 - run_m);
+      }
+      // the block's perturbed log-mass; the token inside it only when it
+      // could still win this thread's race
+      const uint32_t jb = (uint32_t)v4 >> 2;
+      const uint32_t w = word_of(rng_call(key, kStreamDraft, (uint32_t)b, (uint32_t)k, jb >> 2), jb & 3u);
+      const float z = m4 + logf(s4) + gumbel_from_bits(w >> 9);
+      if (argmax_key(z, v4) > best) {
+        const int v = block_pick(key, (uint32_t)b, (uint32_t)k, jb, e[0], e[1], e[2], e[3]);
+        const unsigned long long kz = argmax_key(z, v);
         best = kz > best ? kz : best;
       }
     }

@@ -128,13 +128,14 @@ __device__ __forceinline__ float race_bound(float run_m, float zbest) {
   return exp2f((run_m - zbest) * kLog2e) * (1.0f + 0x1p-10f);
 }
 
-// The 16 high random bits of this thread's columns: 32-bit word j of `wv`
-// holds the bits of columns v0 + 2j (low half) and v0 + 2j + 1 (high half).
-// v0 is a multiple of min(CPP, 8), so every index below is known at compile
-// time except, for CPP = 4, which half of the call's four words is used.
+// Per-token random words (the residual race): the 16 high random bits of this
+// thread's columns; 32-bit word j of `wv` holds the bits of columns v0 + 2j
+// (low half) and v0 + 2j + 1 (high half).  v0 is a multiple of min(CPP, 8), so
+// every index below is known at compile time except, for CPP = 4, which half
+// of the call's four words is used.
 template <int CPP>
-__device__ __forceinline__ void race_words(uint32_t (&wv)[(CPP + 1) / 2], const RngKey& key, uint32_t stream,
-                                           uint32_t req, uint32_t pos, int v0) {
+__device__ __forceinline__ void entry_words(uint32_t (&wv)[(CPP + 1) / 2], const RngKey& key, uint32_t stream,
+                                            uint32_t req, uint32_t pos, int v0) {
   if constexpr (CPP >= 8) {
 #pragma unroll
     for (int j = 0; j < CPP / 8; ++j) {
@@ -154,15 +155,49 @@ __device__ __forceinline__ void race_words(uint32_t (&wv)[(CPP + 1) / 2], const 
 // a constant once the callers' loops are unrolled): one mask or one byte
 // permutation.
 template <int CPP>
-__device__ __forceinline__ float race_hf(const uint32_t (&wv)[(CPP + 1) / 2], int c) {
+__device__ __forceinline__ float entry_hf(const uint32_t (&wv)[(CPP + 1) / 2], int c) {
   const uint32_t w = wv[c >> 1];
   return __uint_as_float((c & 1) ? __byte_perm(w, 0x4B000000u, 0x7632) : ((w & 0xFFFFu) | 0x4B000000u));
 }
 
-// Screen threshold on fmaf(e_v, 65536 bound, 2^23 + h): entry v can only win
-// when h > 65535 - 65536 exp(l_v - zthr), i.e. when the exact sum exceeds
-// 2^23 + 65535.  Floats there are integers; one unit of slack absorbs the
-// rounding of the fused product.
+// The draft's block race.  Block j (tokens 4j .. 4j+3) takes word j of the
+// draft stream's call sequence (word j mod 4 of call j / 4).  A thread's
+// CPP / 4 blocks start at block v0 / 4, a multiple of CPP / 4, so one call
+// covers them.
+template <int CPP>
+__device__ __forceinline__ void block_words(uint32_t (&wb)[CPP / 4], const RngKey& key, uint32_t req, uint32_t pos,
+                                            int v0) {
+  const uint32_t j0 = (uint32_t)v0 >> 2;
+  const uint4 ra = rng_call(key, kStreamDraft, req, pos, j0 >> 2);
+  if constexpr (CPP == 16) {
+    wb[0] = ra.x; wb[1] = ra.y; wb[2] = ra.z; wb[3] = ra.w;
+  } else if constexpr (CPP == 8) {
+    const bool up = (j0 & 2u) != 0;
+    wb[0] = up ? ra.z : ra.x;
+    wb[1] = up ? ra.w : ra.y;
+  } else {
+    static_assert(CPP == 4, "4, 8 or 16 columns per thread");
+    wb[0] = word_of(ra, j0 & 3u);
+  }
+}
+
+// 2^23 + h from a word's high 16 bits h, exactly, by one byte permutation.
+__device__ __forceinline__ float block_hf(uint32_t w) { return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632)); }
+
+// wb[q] for a run-time q by explicit selects (no indexed local array).
+template <int NB>
+__device__ __forceinline__ uint32_t pick_word(const uint32_t (&wb)[NB], int q) {
+  uint32_t w = wb[0];
+#pragma unroll
+  for (int i = 1; i < NB; ++i) w = (q == i) ? wb[i] : w;
+  return w;
+}
+
+// Screen threshold on fmaf(mass, 65536 bound, 2^23 + h): an entry (a block of
+// the draft, a token of the residual) can only win when h > 65535 - 65536 *
+// mass * exp(-zthr), i.e. when the exact sum exceeds 2^23 + 65535.  Floats
+// there are integers; one unit of slack absorbs the rounding of the fused
+// product.
 constexpr float kScreenThr = 8454142.0f;   // 2^23 + 65534
 
 // Opens the online softmax state of a row part at its first tile: the running
@@ -179,44 +214,56 @@ __device__ __forceinline__ void race_prep(RowRace& st, const float (&l)[CPP]) {
   st.bound = race_bound(st.run_m, st.zthr);
 }
 
-// Opens the race of a row part: of this tile's columns, the one most likely to
-// hold the largest perturbed logit -- largest e_v / (1 - u_v), with u_v from
-// the 16 high bits, a monotone stand-in for l_v + G_v -- is resolved exactly
-// and becomes the part's best.  Its softmax term is added here and its logit
-// set to -inf, so the screen that follows does not meet it again.
+// Opens the race of a row part: of this tile's blocks, the one most likely to
+// win -- largest s_q / (1 - u_q), with its mass s_q and u_q from the 16 high
+// bits, a monotone stand-in for L_q + G_q -- is resolved exactly (with its
+// token drawn inside it) and becomes the part's best.  Its softmax mass is
+// added here and its logits set to -inf, so the screen that follows does not
+// meet it again.
 template <int CPP>
-__device__ __forceinline__ void race_seed(RowRace& st, float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2], int v0,
+__device__ __forceinline__ void race_seed(RowRace& st, float (&l)[CPP], const uint32_t (&wb)[CPP / 4], int v0,
                                           const RngKey& key, uint32_t req, uint32_t pos) {
+  constexpr int NB = CPP / 4;
   const float mb = st.run_m * kLog2e;
-  float be = 0.f, bd = 1.f, bl = -INFINITY, bh = 0.f;
-  int bc = -1;
+  float bs = 0.f, bd = 1.f, e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+  uint32_t bw = 0u;
+  int bq = -1;
 #pragma unroll
-  for (int c = 0; c < CPP; ++c) {
-    const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
-    const float d = 8454144.0f - race_hf<CPP>(wv, c);   // 65536 - h, exactly
-    if (e * bd > be * d || bc < 0) { be = e; bd = d; bl = l[c]; bh = race_hf<CPP>(wv, c); bc = c; }
+  for (int q = 0; q < NB; ++q) {
+    float e[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) e[c] = ex2_approx(fmaf(l[4 * q + c], kLog2e, -mb));
+    const float sq = ((e[0] + e[1]) + e[2]) + e[3];
+    const float d = 8454144.0f - block_hf(wb[q]);   // 65536 - h, exactly
+    if (sq * bd > bs * d || bq < 0) {
+      bs = sq; bd = d; bw = wb[q]; bq = q;
+      e0 = e[0]; e1 = e[1]; e2 = e[2]; e3 = e[3];
+    }
   }
-  const uint32_t v = (uint32_t)(v0 + bc);
-  const uint32_t hi = __float_as_uint(bh) & 0xFFFFu;   // h
-  st.zbest = bl + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamDraft, req, pos, v));
-  st.best_v = (int)v;
+  const uint32_t j = ((uint32_t)v0 >> 2) + (uint32_t)bq;
+  st.zbest = st.run_m + logf(bs) + gumbel_from_bits(bw >> 9);
+  st.best_v = block_pick(key, req, pos, j, e0, e1, e2, e3);
   st.zthr = fmaxf(st.zthr, st.zbest);
   st.bound = race_bound(st.run_m, st.zthr);
-  st.run_s += be;
+  st.run_s += bs;
 #pragma unroll
-  for (int c = 0; c < CPP; ++c)
-    if (c == bc) l[c] = -INFINITY;
+  for (int q = 0; q < NB; ++q)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (q == bq) l[4 * q + c] = -INFINITY;
 }
 
 // Rare path of the screen.  Moves the running maximum up to this tile's if it
 // is exceeded, recomputes the tile's softmax terms against it, rebuilds the
-// candidate mask, parks the logits in `spill` and lets the full uniforms
-// decide, one entry at a time; each winner tightens the bound for the rest.
-// Returns the tile's softmax sum.
+// block candidate mask, parks the terms in `spill` (block q in 16-byte chunk
+// j0 + q, swizzled) and resolves the candidates one by one with the full
+// 23-bit uniforms; a block that wins draws its token and tightens the bound
+// for the rest.  Returns the tile's softmax sum.
 template <int CPP>
-__device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2],
+__device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP], const uint32_t (&wb)[CPP / 4],
                                               int v0, unsigned char* spill, int j0, int sw, const RngKey& key,
                                               uint32_t req, uint32_t pos, int* status) {
+  constexpr int NB = CPP / 4;
   float tm = l[0];
 #pragma unroll
   for (int c = 1; c < CPP; ++c) tm = fmaxf(tm, l[c]);
@@ -230,26 +277,26 @@ __device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP]
   float s = 0.f;
   uint32_t cand = 0;
 #pragma unroll
-  for (int c = 0; c < CPP; ++c) {
-    const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
-    s += e;
-    if (fmaf(e, b16, race_hf<CPP>(wv, c)) > kScreenThr) cand |= 1u << c;
+  for (int q = 0; q < NB; ++q) {
+    float e[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) e[c] = ex2_approx(fmaf(l[4 * q + c], kLog2e, -mb));
+    const float sq = ((e[0] + e[1]) + e[2]) + e[3];
+    s += sq;
+    if (fmaf(sq, b16, block_hf(wb[q])) > kScreenThr) cand |= 1u << q;
+    *reinterpret_cast<float4*>(spill + (((j0 + q) ^ sw) << 4)) = make_float4(e[0], e[1], e[2], e[3]);
   }
   if (!(s <= 3.0e38f)) record_status(status, DSPARK_ERR_NONFINITE);   // a NaN or infinite logit
-#pragma unroll
-  for (int c = 0; c < CPP; c += 4)
-    *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(l[c], l[c + 1], l[c + 2], l[c + 3]);
 #pragma unroll 1
   while (cand) {
-    const int c = __ffs(cand) - 1;
+    const int q = __ffs(cand) - 1;
     cand &= cand - 1;
-    const uint32_t v = (uint32_t)(v0 + c);
-    const uint32_t hi = gumbel_hi16(rng_call(key, kStreamDraft, req, pos, v >> 3), v);
-    const float lc = reinterpret_cast<const float*>(spill + (((j0 + c / 4) ^ sw) << 4))[c & 3];
-    const float z = lc + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamDraft, req, pos, v));
+    const float4 e = *reinterpret_cast<const float4*>(spill + (((j0 + q) ^ sw) << 4));
+    const float sq = ((e.x + e.y) + e.z) + e.w;
+    const float z = st.run_m + logf(sq) + gumbel_from_bits(pick_word<NB>(wb, q) >> 9);
     if (z > st.zbest) {
       st.zbest = z;
-      st.best_v = (int)v;
+      st.best_v = block_pick(key, req, pos, ((uint32_t)v0 >> 2) + (uint32_t)q, e.x, e.y, e.z, e.w);
       if (z > st.zthr) {
         st.zthr = z;
         st.bound = race_bound(st.run_m, st.zthr);
@@ -259,29 +306,34 @@ __device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP]
   return s;
 }
 
-// Screens this tile's columns against the best perturbed logit known for the
-// row (zthr) and adds their softmax terms e_v = exp(l_v - run_m) (run_m may
-// lag the true maximum: the terms are then above 1, which the merge of the
-// partials allows).  On the high 16 bits h of each uniform:
-// E_v = -log u_v > (65535 - h) / 65536, so entry v can only win when
-// h + 65536 e_v bound > 65535, with bound = exp(run_m - zthr) (2^-10 over).
-// Only the largest left-hand side is kept; a tile that may hold a winner, or
-// whose sum is not finite (a logit far above run_m), goes to race_resolve.
+// Screens this tile's blocks against the best perturbed log-mass known for the
+// row (zthr) and adds their softmax terms e_v = exp(l_v - run_m) (run_m may lag
+// the true maximum: the terms are then above 1, which the merge of the
+// partials allows).  With the block's mass s_q and the high 16 bits h of its
+// uniform: E_q = -log u_q > (65535 - h) / 65536, so the block can only win
+// when h + 65536 s_q bound > 65535, with bound = exp(run_m - zthr) (2^-10
+// over).  Only the largest left-hand side is kept; a tile that may hold a
+// winner, or whose sum is not finite (a logit far above run_m), goes to
+// race_resolve.
 template <int CPP>
-__device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], const uint32_t (&wv)[(CPP + 1) / 2],
+__device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], const uint32_t (&wb)[CPP / 4],
                                             int v0, unsigned char* spill, int j0, int sw, const RngKey& key,
                                             uint32_t req, uint32_t pos, int* status) {
+  constexpr int NB = CPP / 4;
   const float mb = st.run_m * kLog2e;
   const float b16 = st.bound * 65536.0f;
   float smax = 0.f, s = 0.f;
 #pragma unroll
-  for (int c = 0; c < CPP; ++c) {
-    const float e = ex2_approx(fmaf(l[c], kLog2e, -mb));
-    s += e;
-    smax = fmaxf(smax, fmaf(e, b16, race_hf<CPP>(wv, c)));
+  for (int q = 0; q < NB; ++q) {
+    float e[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) e[c] = ex2_approx(fmaf(l[4 * q + c], kLog2e, -mb));
+    const float sq = ((e[0] + e[1]) + e[2]) + e[3];
+    s += sq;
+    smax = fmaxf(smax, fmaf(sq, b16, block_hf(wb[q])));
   }
   if (smax > kScreenThr || !(s <= 3.0e38f))
-    s = race_resolve<CPP>(st, l, wv, v0, spill, j0, sw, key, req, pos, status);
+    s = race_resolve<CPP>(st, l, wb, v0, spill, j0, sw, key, req, pos, status);
   st.run_s += s;
 }
 
@@ -323,17 +375,17 @@ __device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP],
   // in place of the softmax term (only the largest left-hand side is kept;
   // a tile that may hold a winner rebuilds the candidate mask)
   uint32_t wv[(CPP + 1) / 2];
-  race_words<CPP>(wv, key, kStreamResidual, req, pos, v0);
+  entry_words<CPP>(wv, key, kStreamResidual, req, pos, v0);
   const float b16 = st.bound * 65536.0f;
   float smax = 0.f;
 #pragma unroll
   for (int c = 0; c < CPP; ++c)
-    if (c < nv) smax = fmaxf(smax, fmaf(fmaxf(rho[c], 0.f), b16, race_hf<CPP>(wv, c)));
+    if (c < nv) smax = fmaxf(smax, fmaf(fmaxf(rho[c], 0.f), b16, entry_hf<CPP>(wv, c)));
   if (smax > kScreenThr) {
     uint32_t cand = 0;
 #pragma unroll
     for (int c = 0; c < CPP; ++c)
-      if (c < nv && rho[c] > 0.f && fmaf(rho[c], b16, race_hf<CPP>(wv, c)) > kScreenThr) cand |= 1u << c;
+      if (c < nv && rho[c] > 0.f && fmaf(rho[c], b16, entry_hf<CPP>(wv, c)) > kScreenThr) cand |= 1u << c;
 #pragma unroll
     for (int c = 0; c < CPP; c += 4)
       *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(rho[c], rho[c + 1], rho[c + 2], rho[c + 3]);
@@ -655,7 +707,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           unsigned char* urow = U_s + su * kUStageBytes + ((part * CPP) / kUBox) * (R * 128) + r * 128;
           const int j0 = ((part * CPP) % kUBox) / 4;
           const bool live = got_u && active && nv > 0;
-          uint32_t wv[(CPP + 1) / 2];
+          uint32_t wb[CPP / 4];
           if (live) {
 #pragma unroll
             for (int c = 0; c < CPP; c += 4) {
@@ -668,9 +720,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
               for (int c = 0; c < CPP; ++c)
                 if (c >= nv) v[c] = -INFINITY;
             }
-            race_words<CPP>(wv, p.key, kStreamDraft, (uint32_t)b, (uint32_t)k, v0);
+            block_words<CPP>(wb, p.key, (uint32_t)b, (uint32_t)k, v0);
             if (st.run_m == -INFINITY) race_prep<CPP>(st, v);
-            if (st.zbest == -INFINITY) race_seed<CPP>(st, v, wv, v0, p.key, (uint32_t)b, (uint32_t)k);
+            if (st.zbest == -INFINITY) race_seed<CPP>(st, v, wb, v0, p.key, (uint32_t)b, (uint32_t)k);
           }
           if (i == 0) {
             // the parts of a row pool their seeds before the first screen
@@ -698,7 +750,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                 st.bound = race_bound(st.run_m, st.zthr);
               }
             }
-            race_screen<CPP>(st, v, wv, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k, p.status);
+            race_screen<CPP>(st, v, wb, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k, p.status);
             if (kShare && gk && i > 1) {
               const float zg = argmax_key_value(gk);
               if (zg > st.zthr) {
