@@ -226,15 +226,19 @@ __host__ __device__ inline int draft_part_slices(int V) {
 }
 __host__ __device__ inline int verify_num_segs(int V) { return div_up(V, kVerifySeg); }
 
+// Each argmax key that many CTAs read and raise during a pass sits in its own
+// 128-byte line, so that the traffic of different rows spreads over L2.
+constexpr int kKeyStride = 16;   // u64 slots per key
+
 struct WsLayout {
   size_t status;      // int32 status word
   size_t counters;    // int32 [8]: [0] verify row count
-  size_t draft_keys;  // u64 [gamma][B]
+  size_t draft_keys;  // u64 [gamma][B], kKeyStride apart
   size_t draft_part;  // float2 [gamma][nslices][B]
   size_t rows;        // int32 [B*(gamma+1)] row ids b*(gamma+1)+j of the verify rows
   size_t row_part;    // float2 [B*(gamma+1)][nsegs]
   size_t bonus_key;   // u64 [B]
-  size_t resid_key;   // u64 [2][B] residual key, fallback key
+  size_t resid_key;   // u64 [B] residual key, kKeyStride apart
   size_t resid_k;     // int32 [B] rejected position k* (0 = none)
   size_t resid_lse;   // float [B] lse of the target row at k*
   size_t total;
@@ -248,12 +252,12 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   const size_t rows = (size_t)B * (gamma + 1);
   L.status = off;      off = align256(off + 4);
   L.counters = off;    off = align256(off + 32);
-  L.draft_keys = off;  off = align256(off + 8ull * gamma * B);
+  L.draft_keys = off;  off = align256(off + 8ull * kKeyStride * gamma * B);
   L.draft_part = off;  off = align256(off + 8ull * gamma * draft_part_slices(V) * B);
   L.rows = off;        off = align256(off + 4ull * rows);
   L.row_part = off;    off = align256(off + 8ull * rows * verify_num_segs(V));
   L.bonus_key = off;   off = align256(off + 8ull * B);
-  L.resid_key = off;   off = align256(off + 16ull * B);
+  L.resid_key = off;   off = align256(off + 8ull * kKeyStride * B);
   L.resid_k = off;     off = align256(off + 4ull * B);
   L.resid_lse = off;   off = align256(off + 4ull * B);
   L.total = off;

@@ -118,7 +118,7 @@ draft_step_cuda_core(const float* __restrict__ U, const void* __restrict__ W1,
   best = warp_max_u64(best, 0xffffffffu, 8);
   if (row_ok && (tid & 7) == 0) {
     part[(size_t)slice * B + b] = make_float2(run_m, run_s);
-    atomicMax(&keys[b], best);
+    atomicMax(&keys[(size_t)b * kKeyStride], best);
   }
   if (bad) record_status(status, DSPARK_ERR_NONFINITE);
 }
@@ -144,7 +144,7 @@ __global__ void draft_finalize(const float* __restrict__ U, const void* __restri
   }
   warp_softmax_reduce(m, s, 0xffffffffu, 32);
   const float lse = m + logf(s);
-  const unsigned long long kk = keys[b];
+  const unsigned long long kk = keys[(size_t)b * kKeyStride];
   int x = argmax_key_index(kk);
   if (kk == 0ull || x < 0 || x >= V) {
     if (lane == 0) record_status(status, DSPARK_ERR_NONFINITE);
@@ -171,7 +171,7 @@ cudaError_t run_draft(const DraftArgs& a, cudaStream_t stream) {
   unsigned long long* keys = ws_ptr<unsigned long long>(a.ws, L.draft_keys);
   float2* part = ws_ptr<float2>(a.ws, L.draft_part);
   const int nslices = draft_num_slices(a.V);
-  cudaError_t e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * (size_t)a.gamma * a.B, stream);
+  cudaError_t e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * kKeyStride * (size_t)a.gamma * a.B, stream);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(float) * ((size_t)kRowsPerCta * a.r + (size_t)kColsPerTile * (a.r + 1));
   e = cudaFuncSetAttribute(draft_step_cuda_core<WDT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -180,7 +180,7 @@ cudaError_t run_draft(const DraftArgs& a, cudaStream_t stream) {
   for (int k = 1; k <= a.gamma; ++k) {
     const int32_t* prev = (k == 1) ? a.anchor : a.x_out + (k - 2);
     const int stride = (k == 1) ? 1 : a.gamma;
-    unsigned long long* kk = keys + (size_t)(k - 1) * a.B;
+    unsigned long long* kk = keys + (size_t)(k - 1) * a.B * kKeyStride;
     float2* pp = part + (size_t)(k - 1) * nslices * a.B;
     draft_step_cuda_core<WDT><<<grid, kThreads, smem, stream>>>(
         a.U, a.W1, a.W2, prev, stride, a.B, a.gamma, a.V, a.r, k, a.key, pp, kk, status);

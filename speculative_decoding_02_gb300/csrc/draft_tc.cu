@@ -87,7 +87,7 @@ struct StepParams {
   const float* lse_d;
   const float* resid_lse;
   unsigned long long* resid_key;
-  unsigned long long* keys;             // [G][B] argmax keys of every position
+  unsigned long long* keys;             // [G][B] argmax keys of every position, kKeyStride apart
   float2* part;                         // [G][part_slices][B] softmax partials
   unsigned int* gbar;                   // grid-barrier counter (zeroed before launch)
   int* status;
@@ -405,6 +405,20 @@ __device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP],
   }
 }
 
+// E[m, 64h .. 64h+63] = W1[tok] (K atom h of the token's embedding) into this
+// warp's TMEM lanes, columns kTmemE + 32h .. (two bf16 per column, lower k in
+// the low half); zeros for rows without a request.
+__device__ __forceinline__ void gather_e(const __nv_bfloat16* W1, int tok, bool active, int h, uint32_t taddr) {
+  const uint4* wrow = reinterpret_cast<const uint4*>(W1 + (size_t)tok * KR);
+  uint32_t ev[32];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 val = active ? __ldg(wrow + h * 8 + c) : make_uint4(0, 0, 0, 0);
+    ev[4 * c] = val.x; ev[4 * c + 1] = val.y; ev[4 * c + 2] = val.z; ev[4 * c + 3] = val.w;
+  }
+  tmem_store_32cols(taddr, ev);
+}
+
 // Residual mode: copies the U and T row segments of one 64-column tile
 // starting at column vt into a shared-memory stage, 16 threads to a 256-byte
 // segment (coalesced).  Chunk c of row rr lands at rr * 256 + ((c ^ (rr & 15))
@@ -442,10 +456,12 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
   return v;
 }
 
-__device__ __forceinline__ bool grid_barrier(unsigned int* counter, uint32_t target, volatile int* abort,
-                                             int* status) {
+__device__ __forceinline__ void grid_arrive(unsigned int* counter) {
   __threadfence();
   atomicAdd(counter, 1u);
+}
+
+__device__ __forceinline__ bool grid_wait(unsigned int* counter, uint32_t target, volatile int* abort, int* status) {
   const uint64_t t0 = globaltimer();
   while (ld_acquire_u32(counter) < target) {
     if (*abort) return false;
@@ -456,6 +472,12 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* counter, uint32_t tar
     }
   }
   return true;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned int* counter, uint32_t target, volatile int* abort,
+                                             int* status) {
+  grid_arrive(counter);
+  return grid_wait(counter, target, abort, status);
 }
 
 // MODE kDraft: draft positions k_first..k_last for every request (U rows by
@@ -607,6 +629,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     float* xs = xm + 4 * BM;
     unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 4 * BM);
     uint32_t it = 0, gcount = 0;
+    int spec_prev = -1;   // token whose W1 row is in TMEM E from the speculative gather
     for (int k = kf; k <= kl; ++k) {
       bool active = r < rows_valid;
       int ks = k;                           // position of this row
@@ -615,25 +638,39 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         active = ks > 0;
       }
 
-      // E[m, 64h .. 64h+63] = W1[x_{k-1}] (K atom h) into TMEM lane m,
-      // columns kTmemE + 32h .. (two bf16 per column, lower k in the low half)
+      // E = W1[x_{k-1}] into TMEM (gather_e).  From the second position on, E
+      // was already gathered speculatively from the row keys as they stood when
+      // this CTA reached the grid barrier; a warp reloads only if one of its
+      // rows' final x_{k-1} differs.
       int prev = 0;
       if (active) {
         int raw;
         if constexpr (MODE == kDraft)
-          raw = (k == 1) ? p.anchor[b] : argmax_key_index(__ldcg(p.keys + (size_t)(k - 2) * p.B + b));
+          raw = (k == 1) ? p.anchor[b] : argmax_key_index(__ldcg(p.keys + ((size_t)(k - 2) * p.B + b) * kKeyStride));
         else
           raw = (ks == 1) ? p.anchor[b] : p.x[(size_t)b * p.G + ks - 2];
         prev = checked_token(raw, p.V, p.status);
       }
-      const uint4* wrow = reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * KR);
-      uint32_t ev[32];
+      const uint32_t e_taddr = tmem + ((uint32_t)(q * 32) << 16) + kTmemE + h * 32;
+      if (MODE == kResidual || k == kf) {
+        gather_e(p.W1, prev, active, h, e_taddr);
+      } else if (__any_sync(0xffffffffu, prev != spec_prev)) {
+        // only the rows whose token changed are read again
+        float ef[32];
+        tmem_load_cols<32>(e_taddr, ef);
+        uint32_t ev[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 val = active ? __ldg(wrow + h * 8 + c) : make_uint4(0, 0, 0, 0);
-        ev[4 * c] = val.x; ev[4 * c + 1] = val.y; ev[4 * c + 2] = val.z; ev[4 * c + 3] = val.w;
+        for (int c = 0; c < 32; ++c) ev[c] = __float_as_uint(ef[c]);
+        if (prev != spec_prev) {
+          const uint4* wrow = reinterpret_cast<const uint4*>(p.W1 + (size_t)prev * KR);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 val = active ? __ldg(wrow + h * 8 + c) : make_uint4(0, 0, 0, 0);
+            ev[4 * c] = val.x; ev[4 * c + 1] = val.y; ev[4 * c + 2] = val.z; ev[4 * c + 3] = val.w;
+          }
+        }
+        tmem_store_32cols(e_taddr, ev);
       }
-      tmem_store_32cols(tmem + ((uint32_t)(q * 32) << 16) + kTmemE + h * 32, ev);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->e_full);
@@ -642,10 +679,10 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       // rows shared by many threads (small batches replicated across the tile)
       // would turn the exchange into a hot spot: only full 128-row tiles use it
       constexpr bool kShare = (MODE == kDraft) && (R == BM);
-      unsigned long long* row_key = (kShare && active) ? p.keys + (size_t)(k - 1) * p.B + b : nullptr;
+      unsigned long long* row_key = (kShare && active) ? p.keys + ((size_t)(k - 1) * p.B + b) * kKeyStride : nullptr;
       ResRace rs{-INFINITY, -1, -INFINITY, -INFINITY, INFINITY};
       constexpr bool kShareRes = (MODE == kResidual) && (R == BM);
-      unsigned long long* res_key = (kShareRes && active) ? p.resid_key + b : nullptr;
+      unsigned long long* res_key = (kShareRes && active) ? p.resid_key + (size_t)b * kKeyStride : nullptr;
       float ld2 = 0.f, lt2 = 0.f;
       if constexpr (MODE == kResidual) {
         if (active) {
@@ -826,20 +863,35 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         }
         if constexpr (MODE == kDraft) {
           p.part[((size_t)(k - 1) * p.part_slices + slice) * p.B + b] = make_float2(M, S);
-          if (K) atomicMax(&p.keys[(size_t)(k - 1) * p.B + b], K);
+          if (K) atomicMax(&p.keys[((size_t)(k - 1) * p.B + b) * kKeyStride], K);
         } else {
-          if (K) atomicMax(&p.resid_key[b], K);
+          if (K) atomicMax(&p.resid_key[(size_t)b * kKeyStride], K);
         }
       }
       (void)ok;
       if (k < kl) {
-        // every CTA's position-k keys are in place before anyone reads x_k;
+        // every CTA's position-k keys are in place before anyone reads x_k:
+        // one thread arrives at the grid barrier once this CTA's keys are out
+        named_bar_sync(1, kEpiWarps * 32);
+        if (warp == 2 && lane == 0 && !*abort) grid_arrive(p.gbar);
+        // Speculative gather while the barrier resolves: this CTA's MMAs of
+        // position k are complete (its last accumulator was read), so TMEM E
+        // is free; load W1[x_k] for the row keys as they stand now.  After the
+        // barrier the final keys are compared and only changed rows reload.
+        if constexpr (MODE == kDraft) {
+          int sp = 0;
+          if (active) {
+            const int t = argmax_key_index(__ldcg(p.keys + ((size_t)(k - 1) * p.B + b) * kKeyStride));
+            sp = (t >= 0 && t < p.V) ? t : 0;
+          }
+          gather_e(p.W1, sp, active, h, tmem + ((uint32_t)(q * 32) << 16) + kTmemE + h * 32);
+          spec_prev = active ? sp : 0;
+        }
         // one thread takes the decision to go on, all epilogue warps read it
         // after the same barrier, so they all leave the loop together
-        named_bar_sync(1, kEpiWarps * 32);
         if (warp == 2 && lane == 0) {
           bool go = !*abort;
-          if (go) go = grid_barrier(p.gbar, (uint32_t)(p.nctas * (k - kf + 1)), abort, p.status);
+          if (go) go = grid_wait(p.gbar, (uint32_t)(p.nctas * (k - kf + 1)), abort, p.status);
           bars->stop = go ? 0 : 1;
         }
         named_bar_sync(1, kEpiWarps * 32);
@@ -873,13 +925,13 @@ __global__ void draft_finalize_tc(const float* __restrict__ U, const __nv_bfloat
   }
   warp_softmax_reduce(m, s, 0xffffffffu, 32);
   const float lse = m + logf(s);
-  const unsigned long long kk = keys[(size_t)(k - 1) * B + b];
+  const unsigned long long kk = keys[((size_t)(k - 1) * B + b) * kKeyStride];
   int x = kk ? argmax_key_index(kk) : -1;
   if (x < 0 || x >= V) {
     if (lane == 0) record_status(status, DSPARK_ERR_NONFINITE);
     x = 0;
   }
-  int prev = (k == 1) ? anchor[b] : argmax_key_index(keys[(size_t)(k - 2) * B + b]);
+  int prev = (k == 1) ? anchor[b] : argmax_key_index(keys[((size_t)(k - 2) * B + b) * kKeyStride]);
   prev = checked_token(prev, V, status);
   float dot = 0.f;
   for (int i = lane; i < KR; i += 32)
@@ -998,7 +1050,7 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   auto kern = R == 32 ? draft_step_tc<32, kDraft> : (R == 64 ? draft_step_tc<64, kDraft> : draft_step_tc<BM, kDraft>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * (size_t)a.gamma * a.B, stream);
+  e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * kKeyStride * (size_t)a.gamma * a.B, stream);
   if (e != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(gbar, 0, sizeof(unsigned int), stream)) != cudaSuccess) return e;
 

@@ -304,7 +304,7 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
   __syncthreads();
   if (tid == 0) {
     for (int w = 1; w < kRowThreads / 32; ++w) k1 = s_k1[w] > k1 ? s_k1[w] : k1;
-    if (k1) atomicMax(&resid_key[b], k1);
+    if (k1) atomicMax(&resid_key[(size_t)b * kKeyStride], k1);
   }
 }
 
@@ -319,7 +319,7 @@ verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKe
   const int b = blockIdx.x;
   const int ks = resid_k[b];
   if (ks <= 0) return;
-  const unsigned long long k1 = resid_key[b];
+  const unsigned long long k1 = resid_key[(size_t)b * kKeyStride];
   if (k1) {
     if (threadIdx.x == 0) tok_out[b] = argmax_key_index(k1);
     return;
