@@ -83,10 +83,11 @@ def kernels_per_round(w):
     """Launches of this library's kernels in one round (cudaMemsetAsync not
     counted): draft = the persistent tensor-core kernel and its finalize (bf16,
     r = 256, V >= 192; else a CUDA-core step and finalize per position);
-    confidence; schedule; verify = prep, rows, decide, residual (the draft
-    kernel in residual mode, or its CUDA-core form), residual finalize."""
+    confidence; schedule; verify = prep, row statistics, bonus race, decide,
+    residual (the draft kernel in residual mode, or its CUDA-core form),
+    residual finalize."""
     tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
-    return (2 if tc else 2 * w.gamma) + 1 + 1 + 5
+    return (2 if tc else 2 * w.gamma) + 1 + 1 + 6
 
 
 # Source files of the draft kernel: a committed ncu figure counts only while

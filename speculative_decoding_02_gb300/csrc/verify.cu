@@ -2,20 +2,22 @@
 // 2: accept the longest valid prefix, resample at the first divergence; the
 // "[DeepSeek-6] DSpark" blog, section 1: plus one bonus token).
 //
-// 1. verify_prep      one CTA lists the target rows each request needs
-//                     (rows 0..ell_b of T[b]) so that the row pass sees a
-//                     flat, ragged-free task list.
-// 2. verify_rows      the streaming pass: every (row, segment) task reads one
-//                     kVerifySeg-long piece of a target row with 16-byte loads
-//                     and leaves an online-softmax partial; on the bonus row
-//                     (j = ell_b) it also races the Gumbel-perturbed logits.
-// 3. verify_decide    one warp per request, one lane per position: merge the
-//                     partials into lse_t, form p_t(x_k) / p_d(x_k), compare it
-//                     with the accept uniform; the first failing lane is the
-//                     rejection.
-// 4. verify_residual  only for rejecting requests: recompute the draft logits
-//                     of the rejected position (bias of x_{k-1} + U row) and
-//                     race Gumbel noise over log max(0, p_t - p_d).
+// 1. verify_prep       one CTA lists the target rows whose softmax statistics
+//                      the accept tests need (rows 0..ell_b - 1 of T[b]) as a
+//                      flat, ragged-free task list.
+// 2. verify_row_stats  the streaming pass: every (row, segment) task reads one
+//                      kVerifySeg-long piece of a listed row with 16-byte
+//                      loads and leaves an online-softmax partial.
+// 3. verify_bonus_race every request's row j = ell_b: the Gumbel race of the
+//                      bonus token (a separate kernel, so that the streaming
+//                      pass stays light enough for high occupancy).
+// 4. verify_decide     one warp per request, one lane per position: merge the
+//                      partials into lse_t, form p_t(x_k) / p_d(x_k), compare
+//                      it with the accept uniform; the first failing lane is
+//                      the rejection.
+// 5. residual          only for rejecting requests: recompute the draft logits
+//                      of the rejected position (bias of x_{k-1} + U row) and
+//                      race Gumbel noise over log max(0, p_t - p_d).
 #include <algorithm>
 
 #include "kernels.h"
@@ -46,7 +48,7 @@ verify_prep(const int32_t* __restrict__ ell, int B, int G, int32_t* __restrict__
       record_status(status, DSPARK_ERR_INVALID);
       L = L < 0 ? 0 : G;
     }
-    run += L + 1;
+    run += L;
   }
   int incl = run;
   for (int off = 1; off < 32; off <<= 1) {
@@ -67,7 +69,7 @@ verify_prep(const int32_t* __restrict__ ell, int B, int G, int32_t* __restrict__
   int pos = (incl - run) + (wid > 0 ? warp_tot[wid - 1] : 0);
   for (int b = lo; b < hi; ++b) {
     const int L = min(max(ell[b], 0), G);
-    for (int j = 0; j <= L; ++j) rows[pos++] = b * (G + 1) + j;
+    for (int j = 0; j < L; ++j) rows[pos++] = b * (G + 1) + j;
   }
   if (tid == 1023) counters[0] = pos;
 }
@@ -96,35 +98,29 @@ __device__ __forceinline__ float2 block_softmax(float m, float s, float* s_red) 
   return make_float2(mx, S);
 }
 
-// One (row, segment) task per iteration: kVerifySeg entries of a target row,
-// read as batches of eight 16-byte loads per thread (all issued before any
-// arithmetic), folded into an online softmax; on the bonus row also a
-// screened Gumbel race (as in the draft).
+// Softmax statistics of the target rows the accept tests need (rows j < ell[b]
+// of every request, listed by verify_prep).  One (row, segment) task per
+// iteration: kVerifySeg entries of a row, read as batches of eight 16-byte
+// loads per thread (all issued before any arithmetic), folded into an online
+// softmax.  Few registers, so that many CTAs per SM keep enough loads in
+// flight to stream T at the HBM rate.
 __global__ void __launch_bounds__(kRowThreads)
-verify_rows(const float* __restrict__ T, const int32_t* __restrict__ ell, int G, int V, int nsegs,
-            RngKey key, const int32_t* __restrict__ rows, const int* __restrict__ counters,
-            float2* __restrict__ row_part, unsigned long long* __restrict__ bonus_key,
-            int* __restrict__ status) {
+verify_row_stats(const float* __restrict__ T, int V, int nsegs, const int32_t* __restrict__ rows,
+                 const int* __restrict__ counters, float2* __restrict__ row_part, int* __restrict__ status) {
   __shared__ float s_red[kRowThreads / 32];
-  __shared__ unsigned long long s_k[kRowThreads / 32];
   constexpr int kBatch = 8;                                     // float4 loads per batch
   constexpr int kStride = 4 * kRowThreads;                      // entries between a thread's loads
   constexpr int kBatches = kVerifySeg / (kBatch * kStride);
   const int nrows = counters[0];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const long long ntasks = (long long)nrows * nsegs;
-  for (long long t = blockIdx.x; t < ntasks; t += gridDim.x) {
-    const int ri = (int)(t / nsegs), seg = (int)(t - (t / nsegs) * nsegs);
+  const int tid = threadIdx.x;
+  const int ntasks = nrows * nsegs;
+  bool bad = false;
+  for (int t = blockIdx.x; t < ntasks; t += gridDim.x) {
+    const int ri = t / nsegs, seg = t - ri * nsegs;
     const int rowid = rows[ri];
-    const int b = rowid / (G + 1), jrow = rowid - (rowid / (G + 1)) * (G + 1);
-    const bool bonus = (jrow == min(max(ell[b], 0), G));
-    const uint32_t pos = (uint32_t)(jrow + 1);
     const float* Trow = T + (size_t)rowid * V;
     const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
     float m = -INFINITY, s = 0.f;
-    float zbest = -INFINITY;
-    int bestv = -1;
-    bool bad = false;
 #pragma unroll 1
     for (int bt = 0; bt < kBatches; ++bt) {
       const int vb = v0 + bt * kBatch * kStride + 4 * tid;
@@ -150,67 +146,112 @@ verify_rows(const float* __restrict__ T, const int32_t* __restrict__ ell, int G,
       for (int j = 0; j < kBatch; ++j)
         s += (exp2_fast(fmaf(t4[j].x, kLog2eF, -mb)) + exp2_fast(fmaf(t4[j].y, kLog2eF, -mb))) +
              (exp2_fast(fmaf(t4[j].z, kLog2eF, -mb)) + exp2_fast(fmaf(t4[j].w, kLog2eF, -mb)));
-      if (bonus) {
-        if (zbest == -INFINITY) {
-          // seed the race with the largest logit of the batch
-          int cs = 0;
-#pragma unroll
-          for (int j = kBatch - 1; j >= 0; --j) {
-            if (t4[j].w == bm) cs = 4 * j + 3;
-            if (t4[j].z == bm) cs = 4 * j + 2;
-            if (t4[j].y == bm) cs = 4 * j + 1;
-            if (t4[j].x == bm) cs = 4 * j;
-          }
-          bestv = vb + kStride * (cs >> 2) + (cs & 3);
-          zbest = bm + gumbel_noise_at(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)bestv);
-        }
-        // screen on the high 16 random bits (see the draft race)
-        const float b32 = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f) * 32768.0f;
-        uint32_t cand = 0;
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-          const int v = vb + kStride * j;
-          if (v < v1) {
-            const uint4 ra = rng_call(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)(v >> 3));
-            const float tv[4] = {t4[j].x, t4[j].y, t4[j].z, t4[j].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t vq = (uint32_t)(v + q);
-              const uint32_t w = word_of(ra, (vq >> 1) & 3u);
-              const uint32_t hb = (vq & 1u) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);
-              const float e = exp2_fast(fmaf(tv[q], kLog2eF, -mb));
-              if (__uint_as_float(0x47000000u | hb) > fmaf(-e, b32, 65535.0f)) cand |= 1u << (4 * j + q);
-            }
-          }
-        }
-#pragma unroll 1
-        while (cand) {
-          const int c = __ffs(cand) - 1;
-          cand &= cand - 1;
-          const int v = vb + kStride * (c >> 2) + (c & 3);
-          const float z = __ldcs(Trow + v) + gumbel_noise_at(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)v);
-          if (z > zbest || (z == zbest && v < bestv)) {
-            zbest = z;
-            bestv = v;
-          }
-        }
-      }
     }
     const float2 ms = block_softmax(m, s, s_red);
-    unsigned long long best = (bonus && bestv >= 0) ? argmax_key(zbest, bestv) : 0ull;
-    if (bonus) {
-      best = warp_max_u64(best, 0xffffffffu, 32);
-      if (lane == 0) s_k[wid] = best;
-      __syncthreads();
-      if (tid == 0) {
-        for (int w = 1; w < kRowThreads / 32; ++w) best = s_k[w] > best ? s_k[w] : best;
-        if (best) atomicMax(&bonus_key[b], best);
-      }
-    }
     if (tid == 0) row_part[(size_t)rowid * nsegs + seg] = ms;
     __syncthreads();
-    if (bad) record_status(status, DSPARK_ERR_NONFINITE);
   }
+  if (bad) record_status(status, DSPARK_ERR_NONFINITE);
+}
+
+// The bonus race of every request over its row j = ell[b] (the bonus token if
+// the whole prefix survives, [blog] section 1): y = argmax_v T[b, j, v] +
+// G(stream 3, b, j + 1, v), one (request, segment) task per iteration.  The
+// race is screened on the high 16 random bits as in the draft: the running
+// maximum of the row part gives the bound; candidates are resolved exactly.
+__global__ void __launch_bounds__(kRowThreads)
+verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, int B, int G, int V, int nsegs,
+                  RngKey key, unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
+  __shared__ unsigned long long s_k[kRowThreads / 32];
+  constexpr int kBatch = 8;
+  constexpr int kStride = 4 * kRowThreads;
+  constexpr int kBatches = kVerifySeg / (kBatch * kStride);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int ntasks = B * nsegs;
+  bool bad = false;
+  for (int t = blockIdx.x; t < ntasks; t += gridDim.x) {
+    const int b = t / nsegs, seg = t - b * nsegs;
+    const int jrow = min(max(ell[b], 0), G);
+    const int rowid = b * (G + 1) + jrow;
+    const uint32_t pos = (uint32_t)(jrow + 1);
+    const float* Trow = T + (size_t)rowid * V;
+    const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
+    float m = -INFINITY;
+    float zbest = -INFINITY;
+    int bestv = -1;
+#pragma unroll 1
+    for (int bt = 0; bt < kBatches; ++bt) {
+      const int vb = v0 + bt * kBatch * kStride + 4 * tid;
+      if (vb >= v1) break;
+      float4 t4[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int v = vb + kStride * j;
+        t4[j] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(Trow + v))
+                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      float bm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) bm = fmaxf(fmaxf(bm, fmaxf(t4[j].x, t4[j].y)), fmaxf(t4[j].z, t4[j].w));
+      bad |= !(bm < INFINITY);
+      m = fmaxf(m, bm);
+      if (m == -INFINITY) continue;
+      const float mb = m * kLog2eF;
+      if (zbest == -INFINITY) {
+        // seed the race with the largest logit of the batch
+        int cs = 0;
+#pragma unroll
+        for (int j = kBatch - 1; j >= 0; --j) {
+          if (t4[j].w == bm) cs = 4 * j + 3;
+          if (t4[j].z == bm) cs = 4 * j + 2;
+          if (t4[j].y == bm) cs = 4 * j + 1;
+          if (t4[j].x == bm) cs = 4 * j;
+        }
+        bestv = vb + kStride * (cs >> 2) + (cs & 3);
+        zbest = bm + gumbel_noise_at(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)bestv);
+      }
+      // screen on the high 16 random bits (see the draft race)
+      const float b32 = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f) * 32768.0f;
+      uint32_t cand = 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int v = vb + kStride * j;
+        if (v < v1) {
+          const uint4 ra = rng_call(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)(v >> 3));
+          const float tv[4] = {t4[j].x, t4[j].y, t4[j].z, t4[j].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t vq = (uint32_t)(v + q);
+            const uint32_t w = word_of(ra, (vq >> 1) & 3u);
+            const uint32_t hb = (vq & 1u) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);
+            const float e = exp2_fast(fmaf(tv[q], kLog2eF, -mb));
+            if (__uint_as_float(0x47000000u | hb) > fmaf(-e, b32, 65535.0f)) cand |= 1u << (4 * j + q);
+          }
+        }
+      }
+#pragma unroll 1
+      while (cand) {
+        const int c = __ffs(cand) - 1;
+        cand &= cand - 1;
+        const int v = vb + kStride * (c >> 2) + (c & 3);
+        const float z = __ldcs(Trow + v) + gumbel_noise_at(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)v);
+        if (z > zbest || (z == zbest && v < bestv)) {
+          zbest = z;
+          bestv = v;
+        }
+      }
+    }
+    unsigned long long best = bestv >= 0 ? argmax_key(zbest, bestv) : 0ull;
+    best = warp_max_u64(best, 0xffffffffu, 32);
+    if (lane == 0) s_k[wid] = best;
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kRowThreads / 32; ++w) best = s_k[w] > best ? s_k[w] : best;
+      if (best) atomicMax(&bonus_key[b], best);
+    }
+    __syncthreads();
+  }
+  if (bad) record_status(status, DSPARK_ERR_NONFINITE);
 }
 
 __global__ void verify_decide(const float* __restrict__ T, const int32_t* __restrict__ x,
@@ -366,10 +407,15 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long max_tasks = (long long)a.B * (a.gamma + 1) * nsegs;
-  const int grid_rows = (int)std::min<long long>(max_tasks, (long long)sms * 4);
-  verify_rows<<<grid_rows, kRowThreads, 0, stream>>>(a.T, a.ell, a.gamma, a.V, nsegs, a.key, rows, counters,
-                                                      row_part, bonus_key, status);
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_row_stats, kRowThreads, 0)) != cudaSuccess)
+    return e;
+  const long long stat_tasks = (long long)a.B * a.gamma * nsegs;
+  const int grid_stats = (int)std::max<long long>(1, std::min<long long>(stat_tasks, (long long)sms * std::max(1, per_sm)));
+  verify_row_stats<<<grid_stats, kRowThreads, 0, stream>>>(a.T, a.V, nsegs, rows, counters, row_part, status);
+  const int grid_bonus = std::min(a.B * nsegs, sms * 2);
+  verify_bonus_race<<<grid_bonus, kRowThreads, 0, stream>>>(a.T, a.ell, a.B, a.gamma, a.V, nsegs, a.key, bonus_key,
+                                                            status);
   verify_decide<<<div_up(a.B * 32, 256), 256, 0, stream>>>(a.T, a.x, a.p_d, a.ell, a.B, a.gamma, a.V, nsegs,
                                                           a.key, row_part, bonus_key, resid_k, resid_lse,
                                                           a.n_out, a.tok_out, status);
