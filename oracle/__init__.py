@@ -38,14 +38,10 @@ def lib():
         L.oracle_u01.restype = c_dbl
         L.oracle_philox_word.argtypes = [c_u64, c_u64, c_u32, c_u32, c_u32, c_u32, c_u32]
         L.oracle_philox_word.restype = c_u32
-        L.oracle_gumbel_bits.argtypes = [c_u64, c_u64, c_u32, c_u32, c_u32, c_u32]
-        L.oracle_gumbel_bits.restype = c_u32
         L.oracle_u01_bits.argtypes = [c_u32]
         L.oracle_u01_bits.restype = c_dbl
         L.oracle_gumbel_from_bits.argtypes = [c_u32]
         L.oracle_gumbel_from_bits.restype = c_dbl
-        L.oracle_gumbel_noise.argtypes = [c_u64, c_u64, c_u32, c_u32, c_u32, c_u32]
-        L.oracle_gumbel_noise.restype = c_dbl
         L.oracle_draft_logits.argtypes = [c_int, c_int, vp, vp, vp, c_int, c_int, vp]
         L.oracle_draft_logits.restype = None
         L.oracle_draft_probs.argtypes = [c_int, c_int, vp, vp, vp, c_int, c_int, vp]
@@ -54,10 +50,12 @@ def lib():
         L.oracle_logsumexp.restype = c_dbl
         L.oracle_softmax.argtypes = [c_int, vp, vp]
         L.oracle_softmax.restype = None
-        L.oracle_gumbel_argmax.argtypes = [c_int, vp, c_u64, c_u64, c_u32, c_u32, c_u32, ctypes.POINTER(c_dbl)]
-        L.oracle_gumbel_argmax.restype = c_int
         L.oracle_block_sample.argtypes = [c_int, vp, c_u64, c_u64, c_u32, c_u32, ctypes.POINTER(c_dbl)]
         L.oracle_block_sample.restype = c_int
+        L.oracle_block_draw.argtypes = [c_int, vp, c_dbl, c_u64, c_u64, c_u32, c_u32, c_u32, ctypes.POINTER(c_dbl)]
+        L.oracle_block_draw.restype = c_int
+        L.oracle_softmax_draw.argtypes = [c_int, vp, c_u64, c_u64, c_u32, c_u32, c_u32, ctypes.POINTER(c_dbl)]
+        L.oracle_softmax_draw.restype = c_int
         L.oracle_residual.argtypes = [c_int, vp, vp, vp]
         L.oracle_residual.restype = None
         L.oracle_acceptance_label.argtypes = [c_int, vp, vp]
@@ -128,9 +126,20 @@ def u01(word):
     return float(lib().oracle_u01(word))
 
 
-def gumbel_bits(seed, rnd, stream, req, k, v):
-    """The 23 random bits of the Gumbel noise of entry v."""
-    return int(lib().oracle_gumbel_bits(seed, rnd, stream, req, k, v))
+def block_draw(w, seed, rnd, stream, req, k, logscale=0.0):
+    """Two-level draw from non-negative weights w: (entry, margin)."""
+    w = _c(w, np.float64)
+    m = ctypes.c_double(0.0)
+    x = lib().oracle_block_draw(w.size, _ptr(w), float(logscale), seed, rnd, stream, req, k, ctypes.byref(m))
+    return int(x), float(m.value)
+
+
+def softmax_draw(score, seed, rnd, stream, req, k):
+    """Two-level draw from softmax(score): (entry, margin)."""
+    score = _c(score, np.float64)
+    m = ctypes.c_double(0.0)
+    x = lib().oracle_softmax_draw(score.size, _ptr(score), seed, rnd, stream, req, k, ctypes.byref(m))
+    return int(x), float(m.value)
 
 
 def block_sample(l, seed, rnd, req, k):
@@ -148,15 +157,6 @@ def u01_bits(m):
 def gumbel_from_bits(m):
     return float(lib().oracle_gumbel_from_bits(m))
 
-
-def gumbel_noise(seed, rnd, stream, req, k, v):
-    """The Gumbel noise of entry v of stream `stream`."""
-    return float(lib().oracle_gumbel_noise(seed, rnd, stream, req, k, v))
-
-
-# --------------------------------------------------------------------------
-# building blocks
-# --------------------------------------------------------------------------
 
 def draft_logits(U_row, W1, W2, prev):
     U_row = _c(U_row, np.float32)
@@ -186,13 +186,6 @@ def softmax(l):
     out = np.empty_like(l)
     lib().oracle_softmax(l.size, _ptr(l), _ptr(out))
     return out
-
-
-def gumbel_argmax(score, seed, rnd, stream, req, k):
-    score = _c(score, np.float64)
-    m = ctypes.c_double()
-    v = lib().oracle_gumbel_argmax(score.size, _ptr(score), seed, rnd, stream, req, k, ctypes.byref(m))
-    return int(v), float(m.value)
 
 
 def residual(p_t, p_d):

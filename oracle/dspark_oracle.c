@@ -90,28 +90,14 @@ uint32_t oracle_philox_word(uint64_t seed, uint64_t round, uint32_t stream,
 /* The random numbers of this library (a choice of this implementation: the
  * pages do not say how tokens are sampled).
  *
- * Word v of a stream: counter (v div 4, ...), word v mod 4.  The accept uniform
- * of position k (stream 1) uses word 0: m = its top 23 bits.
- *
- * The Gumbel noise of entry v (streams 0 draft, 2 residual, 3 bonus) takes the
- * 23 bits m of its uniform from two calls:
- *   high 16 bits: half (v mod 2) (0 = low half) of word ((v div 2) mod 4) of
- *                 the call with counter (v div 8, k, request, round<<3 | stream);
- *   low 7 bits:   the top 7 bits of word (v mod 4) of the call with counter
- *                 (v div 4, k, request, round<<3 | (stream + 4)).
- * Every m is equally likely and the entries' m are independent, so u is the
- * same uniform on the 2^23-point grid as from a single word. */
+ * Word v of a stream: counter (v div 4, k, request, round<<3 | stream), word
+ * v mod 4.  The accept uniform of position k (stream 1) uses word 0.  The
+ * two-level draws (oracle_block_draw) use word j of stream s for block j's
+ * Gumbel noise and word j of stream s + 4 for the entry inside the winning
+ * block: s = 0 for the draft, 2 for the residual, 3 for the bonus token. */
 uint32_t oracle_rng_word(uint64_t seed, uint64_t round, uint32_t stream,
                          uint32_t req, uint32_t k, uint32_t v) {
   return oracle_philox_word(seed, round, stream, req, k, v >> 2, v & 3u);
-}
-
-uint32_t oracle_gumbel_bits(uint64_t seed, uint64_t round, uint32_t stream,
-                            uint32_t req, uint32_t k, uint32_t v) {
-  uint32_t a = oracle_philox_word(seed, round, stream, req, k, v >> 3, (v >> 1) & 3u);
-  uint32_t hi16 = (v & 1u) ? (a >> 16) : (a & 0xffffu);
-  uint32_t b = oracle_philox_word(seed, round, stream + 4u, req, k, v >> 2, v & 3u);
-  return (hi16 << 7) | (b >> 25);
 }
 
 /* Uniform in the open interval (0, 1) from 23 bits m: (2m + 1) / 2^24.
@@ -127,12 +113,6 @@ double oracle_u01(uint32_t w) { return oracle_u01_bits(w >> 9); }
 double oracle_gumbel_from_bits(uint32_t m) {
   double u = oracle_u01_bits(m);
   return -log(-log(u));
-}
-
-/* The Gumbel noise of entry v of a Gumbel stream. */
-double oracle_gumbel_noise(uint64_t seed, uint64_t round, uint32_t stream,
-                           uint32_t req, uint32_t k, uint32_t v) {
-  return oracle_gumbel_from_bits(oracle_gumbel_bits(seed, round, stream, req, k, v));
 }
 
 /* ------------------------------------------------------------------------- */
@@ -183,63 +163,36 @@ void oracle_softmax(int V, const double* l, double* p_out) {
   for (int v = 0; v < V; ++v) p_out[v] = exp(l[v] - lse);
 }
 
-/* Gumbel-max: argmax_v (score(v) + G(v)), skipping entries with score = -inf.
- * Ties go to the smallest v.  Returns -1 when every score is -inf.  The gap
- * between the best and second-best perturbed score is written to *margin. */
-int oracle_gumbel_argmax(int V, const double* score, uint64_t seed,
-                         uint64_t round, uint32_t stream, uint32_t req,
-                         uint32_t k, double* margin) {
-  double best = -INFINITY, second = -INFINITY;
-  int arg = -1;
-  for (int v = 0; v < V; ++v) {
-    if (score[v] == -INFINITY) continue;
-    double z = score[v] +
-               oracle_gumbel_noise(seed, round, stream, req, k, (uint32_t)v);
-    if (z > best) {
-      second = best;
-      best = z;
-      arg = v;
-    } else if (z > second) {
-      second = z;
-    }
-  }
-  if (margin) *margin = best - second;
-  return arg;
-}
-
-/* The draft sampler: an exact draw from softmax(l) in two levels.
+/* The sampler of every draw (draft, residual, bonus): an exact draw from
+ * non-negative weights w(v) in two levels.
  *
- * The vocabulary is cut into blocks of 4 consecutive entries, block j holding
- * v = 4j .. 4j+3 (the last block may be shorter).  Block j's log-mass is
- * L_j = log sum_{v in j} exp(l(v)).  A Gumbel-max over the blocks picks
- * j* = argmax_j L_j + G_j (ties to the smallest j), where G_j = -log(-log u_j)
- * and u_j = ((w >> 9) + 1/2) / 2^23 from the word w = word (j mod 4) of Philox
- * call j / 4 of stream 0.  Inside j* the token is drawn by inverse CDF: with
- * u' from word (j* mod 4) of call j* / 4 of stream 5 (same map to (0, 1)),
- * x = the first v of j* whose cumulative mass exceeds u' times the block's
- * mass.  The block wins with probability mass(j) / sum, the token then with
- * p(v) / mass(j): x is distributed as softmax(l).
- * *margin is the smaller of the top-two gap of L_j + G_j and the distance of
- * u' from the nearest inner boundary of the block's CDF (as a fraction of the
- * block's mass).  Returns -1 when every l(v) is -inf. */
-int oracle_block_sample(int V, const double* l, uint64_t seed, uint64_t round,
-                        uint32_t req, uint32_t k, double* margin) {
-  double m = -INFINITY;
-  for (int v = 0; v < V; ++v)
-    if (l[v] > m) m = l[v];
-  if (m == -INFINITY) {
-    if (margin) *margin = 0.0;
-    return -1;
-  }
+ * The entries are cut into blocks of 4 consecutive ones, block j holding
+ * v = 4j .. 4j+3 (the last block may be shorter), with weight W_j = the sum of
+ * its w(v).  A Gumbel-max over the blocks picks j* = argmax_j log W_j + G_j
+ * (ties to the smallest j; blocks with W_j = 0 never win), where
+ * G_j = -log(-log u_j) and u_j = ((w >> 9) + 1/2) / 2^23 from the word
+ * w = word (j mod 4) of Philox call j / 4 of `stream`.  Inside j* the entry is
+ * drawn by inverse CDF with u' from word (j* mod 4) of call j* / 4 of
+ * stream + 4 (same map to (0, 1)): the first v of j* whose cumulative weight
+ * exceeds u' times W_j*.  The block wins with probability W_j / sum W, the
+ * entry then with w(v) / W_j: v is drawn with probability w(v) / sum w.
+ * logscale is added to every log W_j (so that weights exp(l - m) race as
+ * log sum exp l); it changes no decision, only the reported scores.
+ * *margin is the smaller of the top-two gap of log W_j + G_j and the distance
+ * of u' from the nearest inner boundary of the block's CDF (as a fraction of
+ * W_j*).  Returns -1 when every weight is 0. */
+int oracle_block_draw(int V, const double* w, double logscale, uint64_t seed,
+                      uint64_t round, uint32_t stream, uint32_t req, uint32_t k,
+                      double* margin) {
   double best = -INFINITY, second = -INFINITY;
   int jb = -1;
   for (int j = 0; 4 * j < V; ++j) {
     double s = 0.0;
-    for (int v = 4 * j; v < V && v < 4 * j + 4; ++v) s += exp(l[v] - m);
-    if (s == 0.0) continue;
-    uint32_t w = oracle_philox_word(seed, round, 0u, req, k, (uint32_t)j >> 2,
-                                    (uint32_t)j & 3u);
-    double z = m + log(s) + oracle_gumbel_from_bits(w >> 9);
+    for (int v = 4 * j; v < V && v < 4 * j + 4; ++v) s += w[v];
+    if (s <= 0.0) continue;
+    uint32_t word = oracle_philox_word(seed, round, stream, req, k,
+                                       (uint32_t)j >> 2, (uint32_t)j & 3u);
+    double z = logscale + log(s) + oracle_gumbel_from_bits(word >> 9);
     if (z > best) {
       second = best;
       best = z;
@@ -248,23 +201,25 @@ int oracle_block_sample(int V, const double* l, uint64_t seed, uint64_t round,
       second = z;
     }
   }
-  uint32_t w5 = oracle_philox_word(seed, round, 5u, req, k, (uint32_t)jb >> 2,
-                                   (uint32_t)jb & 3u);
-  double u = oracle_u01(w5);
+  if (jb < 0) {
+    if (margin) *margin = 0.0;
+    return -1;
+  }
+  uint32_t wp = oracle_philox_word(seed, round, stream + 4u, req, k,
+                                   (uint32_t)jb >> 2, (uint32_t)jb & 3u);
+  double u = oracle_u01(wp);
   int v0 = 4 * jb, v1 = (4 * jb + 4 < V) ? 4 * jb + 4 : V;
   double S = 0.0;
   int last = -1;
   for (int v = v0; v < v1; ++v) {
-    double e = exp(l[v] - m);
-    S += e;
-    if (e > 0.0) last = v;
+    S += w[v];
+    if (w[v] > 0.0) last = v;
   }
   double target = u * S, cum = 0.0, dmin = INFINITY;
   int x = -1;
   for (int v = v0; v < v1; ++v) {
-    double e = exp(l[v] - m);
-    if (e == 0.0) continue;
-    cum += e;
+    if (!(w[v] > 0.0)) continue;
+    cum += w[v];
     if (x < 0 && target < cum) x = v;
     if (v != last) {
       double d = fabs(u - cum / S);
@@ -274,6 +229,33 @@ int oracle_block_sample(int V, const double* l, uint64_t seed, uint64_t round,
   if (x < 0) x = last;
   if (margin) *margin = fmin(best - second, dmin);
   return x;
+}
+
+/* A draw from softmax(score) (entries with score = -inf excluded) by
+ * oracle_block_draw on the weights exp(score - max).  Returns -1 when every
+ * score is -inf. */
+int oracle_softmax_draw(int V, const double* score, uint64_t seed,
+                        uint64_t round, uint32_t stream, uint32_t req,
+                        uint32_t k, double* margin) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v)
+    if (score[v] > m) m = score[v];
+  if (m == -INFINITY) {
+    if (margin) *margin = 0.0;
+    return -1;
+  }
+  double* w = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!w) return -1;
+  for (int v = 0; v < V; ++v) w[v] = exp(score[v] - m);
+  int x = oracle_block_draw(V, w, m, seed, round, stream, req, k, margin);
+  free(w);
+  return x;
+}
+
+/* The draft's draw of x_k from softmax(l): streams 0 (blocks) and 4 (entry). */
+int oracle_block_sample(int V, const double* l, uint64_t seed, uint64_t round,
+                        uint32_t req, uint32_t k, double* margin) {
+  return oracle_softmax_draw(V, l, seed, round, 0u, req, k, margin);
 }
 
 /* Residual of rejection sampling ([digest] item 2: resample at the first
@@ -496,16 +478,16 @@ int oracle_schedule(int R, int G, const double* c, const float* sps, int n_sps,
  *   p_d = the draft distribution of position k given x_{k-1} (step 1),
  *   accept x_k while u_k < p_t(x_k) / p_d(x_k),  u_k = U01(stream 1, b, k, 0);
  *   at the first rejection, n = k - 1 and the corrected token is drawn from
- *   normalize(max(0, p_t - p_d)) by Gumbel-max over log rho (stream 2, b, k);
+ *   normalize(max(0, p_t - p_d)) (oracle_block_draw, streams 2 and 6, b, k);
  *   if every rho is 0 in floating point (a measure-zero event in exact
- *   arithmetic) it is drawn from p_t instead, with the same noise.
+ *   arithmetic) it is drawn from p_t instead, with the same streams.
  * If all L tokens are accepted, n = L and the bonus token is drawn from
- * softmax(T[b, L, :]) by Gumbel-max (stream 3, b, k = L + 1).
+ * softmax(T[b, L, :]) (streams 3 and 7, b, k = L + 1).
  *
  * Outputs per request: n (accepted count), y (the corrected or bonus token),
  * flags (1 = bonus, 2 = residual, 4 = residual fell back to p_t); per verified
  * position the ratio p_t/p_d and |u - ratio| (NaN where not evaluated); per
- * request the Gumbel margin of y. */
+ * request the margin of the draw of y. */
 int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
                   const void* W1, const void* W2, int wdt,
                   const int32_t* anchor, const int32_t* x, const int32_t* ell,
@@ -554,29 +536,23 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
       if (u < ratio) continue;
       n = k - 1;
       flags = 2;
+      /* y ~ rho / sum rho, rho = max(0, p_t - p_d) (stream 2); an empty
+       * residual in floating point draws from p_t with the same streams */
       oracle_residual(V, p_t, p_d, score);
-      int any = 0;
-      for (int v = 0; v < V; ++v) {
-        if (score[v] > 0.0) {
-          score[v] = log(score[v]);
-          any = 1;
-        } else {
-          score[v] = -INFINITY;
-        }
-      }
-      if (!any) {
+      y = oracle_block_draw(V, score, 0.0, seed, round, 2u, (uint32_t)b,
+                            (uint32_t)k, &ymargin);
+      if (y < 0) {
         flags |= 4;
-        for (int v = 0; v < V; ++v) score[v] = log(p_t[v]);
+        y = oracle_block_draw(V, p_t, 0.0, seed, round, 2u, (uint32_t)b,
+                              (uint32_t)k, &ymargin);
       }
-      y = oracle_gumbel_argmax(V, score, seed, round, 2u, (uint32_t)b,
-                               (uint32_t)k, &ymargin);
       break;
     }
     if (n == L) {
       const float* T_row = T + ((size_t)b * (G + 1) + L) * (size_t)V;
       for (int v = 0; v < V; ++v) score[v] = (double)T_row[v];
-      y = oracle_gumbel_argmax(V, score, seed, round, 3u, (uint32_t)b,
-                               (uint32_t)(L + 1), &ymargin);
+      y = oracle_softmax_draw(V, score, seed, round, 3u, (uint32_t)b,
+                              (uint32_t)(L + 1), &ymargin);
       flags = 1;
     }
     n_out[b] = n;

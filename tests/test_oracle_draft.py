@@ -156,7 +156,7 @@ def test_draft_teacher_forcing_uses_forced_previous_token():
 def _block_sample_by_hand(l, seed, rnd, req, k):
     """The two-level draw restated from raw Philox words: Gumbel-max over
     blocks of 4 on their log-mass (stream 0, word j of the call sequence), then
-    the inverse CDF inside the winner (stream 5)."""
+    the inverse CDF inside the winner (stream 4)."""
     V = l.size
     m = np.max(l)
     best, second, jb = -np.inf, -np.inf, -1
@@ -171,12 +171,61 @@ def _block_sample_by_hand(l, seed, rnd, req, k):
             best, second, jb = z, best, j
         elif z > second:
             second = z
-    u2 = ((oracle.rng_word(seed, rnd, 5, req, k, jb) >> 9) + 0.5) / 2.0 ** 23
+    u2 = ((oracle.rng_word(seed, rnd, 4, req, k, jb) >> 9) + 0.5) / 2.0 ** 23
     e = np.exp(l[4 * jb:4 * jb + 4] - m)
     cum = np.cumsum(e) / e.sum()
     x = 4 * jb + int(np.argmax(cum > u2))
     inner = [abs(u2 - c) for i, c in enumerate(cum[:-1]) if e[i] > 0 and e[i + 1:].sum() > 0]
     return x, min([best - second] + inner)
+
+
+def _block_draw_by_hand(w, seed, rnd, stream, req, k):
+    """The generic two-level draw from weights w, restated from raw words."""
+    V = w.size
+    best, second, jb = -np.inf, -np.inf, -1
+    for j in range((V + 3) // 4):
+        s_ = w[4 * j:4 * j + 4].sum()
+        if s_ <= 0:
+            continue
+        u = ((oracle.rng_word(seed, rnd, stream, req, k, j) >> 9) + 0.5) / 2.0 ** 23
+        z = math.log(s_) - math.log(-math.log(u))
+        if z > best:
+            best, second, jb = z, best, j
+        elif z > second:
+            second = z
+    if jb < 0:
+        return -1
+    u2 = ((oracle.rng_word(seed, rnd, stream + 4, req, k, jb) >> 9) + 0.5) / 2.0 ** 23
+    e = w[4 * jb:4 * jb + 4]
+    cum = np.cumsum(e) / e.sum()
+    return 4 * jb + int(np.argmax(cum > u2))
+
+
+@pytest.mark.parametrize("stream", [2, 3])
+def test_block_draw_definition_and_law(stream):
+    rng = np.random.default_rng(stream)
+    # definition, with zero weights and a short last block
+    for t in range(30):
+        V = [9, 16, 30][t % 3]
+        w = rng.uniform(0, 1, V) * (rng.uniform(0, 1, V) > 0.3)
+        x, _ = oracle.block_draw(w, 7 + t, 3, stream, 2, 5)
+        assert x == _block_draw_by_hand(w, 7 + t, 3, stream, 2, 5)
+        assert x < 0 or w[x] > 0
+    assert oracle.block_draw(np.zeros(8), 1, 1, stream, 0, 1)[0] == -1
+    # law over seeds: w / sum w
+    w = np.array([0.5, 0.0, 2.0, 0.1, 0.0, 0.0, 1.4, 0.3, 0.9, 0.2])
+    n = 30000
+    counts = np.bincount([oracle.block_draw(w, s, 0, stream, 1, 2)[0] for s in range(n)], minlength=w.size)
+    p = w / w.sum()
+    assert np.all(counts[p == 0] == 0)
+    keep = p > 0
+    chi2 = ((counts[keep] - n * p[keep]) ** 2 / (n * p[keep])).sum()
+    assert stats.chi2.sf(chi2, keep.sum() - 1) > 1e-4
+    # a softmax draw is the block draw of exp(score - max)
+    sc = rng.normal(0, 2, 24)
+    sc[5] = -np.inf
+    assert oracle.softmax_draw(sc, 3, 1, stream, 4, 2)[0] == \
+        oracle.block_draw(np.exp(sc - sc.max()), 3, 1, stream, 4, 2)[0]
 
 
 def test_block_sample_definition_and_margin():

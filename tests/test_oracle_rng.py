@@ -61,42 +61,11 @@ def test_uniformity_ks_and_streams():
         assert not np.array_equal(u[:4000], u2)
 
 
-def test_gumbel_bits_layout():
-    # high 16 bits: half (v mod 2) of word ((v div 2) mod 4) of counter (v div 8, ...)
-    # of the stream; low 7 bits: top 7 bits of word (v mod 4) of counter
-    # (v div 4, ...) of stream + 4
-    seed, rnd, req, k = (5 << 33) + 77, 3, 9, 4
-    for stream in (0, 2, 3):
-        for v in list(range(0, 40)) + [151935, 262143]:
-            a = oracle.philox4x32_10([v >> 3, k, req, (rnd << 3) | stream], [seed & 0xffffffff, seed >> 32])
-            w = a[(v >> 1) & 3]
-            hi = (w >> 16) if (v & 1) else (w & 0xffff)
-            b = oracle.philox4x32_10([v >> 2, k, req, (rnd << 3) | (stream + 4)], [seed & 0xffffffff, seed >> 32])
-            m = (hi << 7) | (b[v & 3] >> 25)
-            assert oracle.gumbel_bits(seed, rnd, stream, req, k, v) == m
-            assert oracle.gumbel_noise(seed, rnd, stream, req, k, v) == oracle.gumbel_from_bits(m)
-
-
-def test_gumbel_bits_uniform_and_independent():
-    n = 60000
-    m = np.array([oracle.gumbel_bits(21, 1, 0, 5, 2, v) for v in range(n)])
-    assert m.min() >= 0 and m.max() < (1 << 23)
-    u = (m + 0.5) / 2.0 ** 23
-    assert stats.kstest(u, "uniform").pvalue > 1e-3
-    # the 16-bit and 7-bit parts are each uniform and unrelated to each other
-    hi, lo = m >> 7, m & 127
-    assert stats.chisquare(np.bincount(lo, minlength=128)).pvalue > 1e-4
-    assert stats.chisquare(np.bincount(hi >> 10, minlength=64)).pvalue > 1e-4
-    assert abs(np.corrcoef(hi, lo)[0, 1]) < 0.02
-    # neighbouring entries (sharing a call) are unrelated
-    assert abs(np.corrcoef(u[:-1], u[1:])[0, 1]) < 0.02
-    assert abs(np.corrcoef(u[:-8], u[8:])[0, 1]) < 0.02
-
-
 def test_gumbel_distribution():
+    # the block noise G = -log(-log u) with u from a word's top 23 bits:
+    # CDF exp(-exp(-g)), mean = Euler-Mascheroni, var = pi^2/6
     n = 40000
-    g = np.array([oracle.gumbel_noise(11, 2, 0, 0, 1, v) for v in range(n)])
-    # standard Gumbel: CDF exp(-exp(-g)), mean = Euler-Mascheroni, var = pi^2/6
+    g = np.array([oracle.gumbel_from_bits(oracle.rng_word(11, 2, 0, 0, 1, v) >> 9) for v in range(n)])
     assert stats.kstest(g, stats.gumbel_r.cdf).pvalue > 1e-3
     assert abs(g.mean() - 0.5772156649) < 0.03
     assert abs(g.var() - math.pi ** 2 / 6) < 0.06

@@ -271,7 +271,7 @@ def test_identical_distributions_always_accept_and_bonus_row():
     np.testing.assert_array_equal(out["n"], ell)
     assert np.all(out["flags"] == 1)
     for b in range(B):
-        want, _ = oracle.gumbel_argmax(T[b, ell[b]].astype(np.float64), 5, 0, 3, b, int(ell[b]) + 1)
+        want, _ = oracle.softmax_draw(T[b, ell[b]].astype(np.float64), 5, 0, 3, b, int(ell[b]) + 1)
         assert out["y"][b] == want
 
 
@@ -288,8 +288,7 @@ def test_residual_uses_stream2_at_rejected_position():
         pt = M.p_t(tuple(x[b, :n]))
         prev = M.anchor[0] if n == 0 else x[b, n - 1]
         rho = oracle.residual(pt, M.p_d(n, prev))
-        score = np.where(rho > 0, np.log(np.where(rho > 0, rho, 1.0)), -np.inf)
-        want, _ = oracle.gumbel_argmax(score, seed, rnd, 2, b, n + 1)
+        want, _ = oracle.block_draw(rho, seed, rnd, 2, b, n + 1)
         assert v["y"][b] == want
         checked += 1
     assert checked > 50
