@@ -30,14 +30,14 @@
  *    ([blog] section 4).  wdtype is DSPARK_BF16 or DSPARK_F32 for both.
  *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by
  *    (seed mod 2^32, seed / 2^32); a call at counter (c, position k, request b,
- *    (round << 3) | stream) gives four 32-bit words.  Accept uniform (stream 1):
- *    word 0 of call c = 0, u = ((w >> 9) + 1/2) / 2^23.  Gumbel noise of entry v
- *    (streams 0 draft, 2 residual, 3 bonus): a 23-bit m = (h << 7) | g with
- *    h = 16-bit half (v mod 2) (low half first) of word ((v / 2) mod 4) of call
- *    c = v / 8 of the stream, and g = the top 7 bits of word (v mod 4) of call
- *    c = v / 4 of stream + 4; u = (m + 1/2) / 2^23, noise -log(-log u).  The high
- *    bits come first so that a kernel can rule an entry out of a race from h
- *    alone.  `round` < 2^29.
+ *    (round << 3) | stream) gives four 32-bit words; word j of a stream is word
+ *    (j mod 4) of call j / 4.  Accept uniform (stream 1): word 0,
+ *    u = ((w >> 9) + 1/2) / 2^23.  Every categorical draw (draft x_k: stream 0;
+ *    corrected token: stream 2; bonus token: stream 3) is one exact two-level
+ *    draw from its weights: blocks of 4 consecutive entries race with the log
+ *    of their summed weight plus -log(-log u_j), u_j from word j of the stream;
+ *    inside the winning block the entry is drawn by inverse CDF with the
+ *    uniform of word j of stream + 4.  `round` < 2^29.
  *  - Return value: a DSPARK_* status.  Argument errors are detected on the host
  *    before anything is enqueued.  Errors found by the kernels (a bounded wait
  *    that gave up, non-finite logits) are recorded in a status word inside the
@@ -78,11 +78,11 @@ size_t dspark_workspace_size(int B, int gamma, int V);
  * Semi-autoregressive Markov draft ([report] Eq.4; [blog] sections 3-4).
  * For k = 1..gamma (x_0 = anchor, [blog] section 3):
  *   l_k(v) = U[b, k-1, v] + sum_i W1[x_{k-1}, i] * W2[v, i]
- *   x_k    = argmax_v l_k(v) + Gumbel(seed, round, stream 0, b, k, v)
+ *   x_k    ~ softmax(l_k), the two-level draw on streams 0 and 4 (b, k)
  *   lse_k  = log sum_v exp l_k(v);   p_k(x_k) = exp(l_k(x_k) - lse_k)
  * In:  U [B, gamma, V] f32, W1/W2 [V, r] (wdtype), anchor [B] i32 in [0, V).
  * Out: x_out [B, gamma] i32, p_out [B, gamma] f32, lse_out [B, gamma] f32.
- * Ties of the perturbed logit go to the smallest v.
+ * Ties of the perturbed block log-mass go to the smallest block.
  */
 int dspark_markov_draft(const float* U, const void* W1, const void* W2, int wdtype,
                         const int32_t* anchor, int B, int gamma, int V, int r,
@@ -130,11 +130,12 @@ int dspark_schedule(const float* c, int B, int gamma, const float* sps, int n_sp
  * Lossless rejection-sampling verification ([digest] item 2; [blog] section 1).
  * For request b and k = 1..ell[b]: p_t = softmax(T[b, k-1, :]); accept x_k
  * while u < p_t(x_k) / p_d(x_k), u = uniform(stream 1, b, k).  At the first
- * rejection the corrected token is drawn from normalize(max(0, p_t - p_d)) by
- * Gumbel-max over its logarithm (stream 2, b, k), p_d = softmax(U[b,k-1,:] +
+ * rejection the corrected token is drawn from normalize(max(0, p_t - p_d))
+ * (the two-level draw on streams 2 and 6, b, k), p_d = softmax(U[b,k-1,:] +
  * bias(x_{k-1})) recomputed from lse_d; if that residual is empty in floating
- * point, from p_t with the same noise.  If all ell[b] tokens are accepted, the
- * bonus token is drawn from softmax(T[b, ell[b], :]) (stream 3, k = ell[b]+1).
+ * point, from p_t with the same streams.  If all ell[b] tokens are accepted,
+ * the bonus token is drawn from softmax(T[b, ell[b], :]) (streams 3 and 7,
+ * k = ell[b]+1).
  * In:  T [B, gamma+1, V] f32 (row k-1 scores position k); U, W1, W2, anchor as
  *      for the draft; x, p_d, lse_d [B, gamma] from the draft; ell [B] i32 in
  *      [0, gamma].  Only rows 0..ell[b] of T are read.

@@ -22,12 +22,10 @@ constexpr uint32_t kPhiloxWeylA = 0x9E3779B9u;
 constexpr uint32_t kPhiloxWeylB = 0xBB67AE85u;
 
 // Random-number streams of one round (the fourth counter word is
-// (round << 3) | stream).  The draft uses stream 0 for its block race and
-// stream 5 for the token inside the winning block; the bonus and residual
-// races take their low noise bits from stream + 4.
-enum Stream : uint32_t {
-  kStreamDraft = 0, kStreamAccept = 1, kStreamResidual = 2, kStreamBonus = 3, kStreamBlockPick = 5
-};
+// (round << 3) | stream).  Every draw races blocks of 4 entries on stream s and
+// picks the entry inside the winning block from stream s + 4.
+enum Stream : uint32_t { kStreamDraft = 0, kStreamAccept = 1, kStreamResidual = 2, kStreamBonus = 3 };
+constexpr uint32_t kPickStreamOffset = 4;
 
 // The key of one round with its ten round keys precomputed on the host, so
 // that kernels read them as constant operands instead of recomputing the
@@ -86,18 +84,18 @@ __device__ __forceinline__ float uniform_bits(uint32_t m) {
 // The accept uniform of a position: the top 23 bits of a word.
 __device__ __forceinline__ float uniform01(uint32_t w) { return uniform_bits(w >> 9); }
 
-// Draft sampler: blocks of 4 consecutive tokens race with their log-mass plus
-// Gumbel noise from one 32-bit word each (word j of the draft stream's call
-// sequence: word j mod 4 of call j / 4); the token inside the winning block is
-// drawn by inverse CDF with the uniform of word j of kStreamBlockPick.  Both
-// levels together draw exactly from the softmax.
+// The sampler of every draw: blocks of 4 consecutive entries race with the log
+// of their summed weight plus Gumbel noise from one 32-bit word each (word j of
+// the stream's call sequence: word j mod 4 of call j / 4); the entry inside the
+// winning block is drawn by inverse CDF with the uniform of word j of stream +
+// kPickStreamOffset.  Both levels together draw exactly from the weights.
 
-// Token of block j from the block's four softmax terms e0..e3 (any common
-// scale): the first whose cumulative mass exceeds u times the block's mass, or
-// the last with mass when rounding leaves none.
-__device__ __forceinline__ int block_pick(const RngKey& key, uint32_t req, uint32_t pos, uint32_t j, float e0,
-                                          float e1, float e2, float e3) {
-  const float u = uniform01(word_of(rng_call(key, kStreamBlockPick, req, pos, j >> 2), j & 3u));
+// Entry of block j of `stream` from the block's four weights e0..e3 (any common
+// scale): the first whose cumulative weight exceeds u times the block's, or the
+// last with weight when rounding leaves none.
+__device__ __forceinline__ int block_pick(const RngKey& key, uint32_t stream, uint32_t req, uint32_t pos, uint32_t j,
+                                          float e0, float e1, float e2, float e3) {
+  const float u = uniform01(word_of(rng_call(key, stream + kPickStreamOffset, req, pos, j >> 2), j & 3u));
   const float t = u * (((e0 + e1) + e2) + e3);
   float cum = e0;
   int c;
@@ -118,26 +116,6 @@ __device__ __forceinline__ int block_pick(const RngKey& key, uint32_t req, uint3
 // with absolute error would distort the largest noise values.
 __device__ __forceinline__ float gumbel_from_bits(uint32_t m) {
   return -logf(-logf(uniform_bits(m)));
-}
-
-// Gumbel noise of entry v: its 23 uniform bits come from two calls.  The high
-// 16 are half (v mod 2) of word ((v div 2) mod 4) of the call with counter
-// (v div 8, position, request, round<<3 | stream), shared by 8 entries; the low
-// 7 are the top bits of word (v mod 4) of the call with counter (v div 4, ...,
-// round<<3 | (stream + 4)).  The high half alone usually shows that an entry
-// cannot win a race, so the second call is made only for the rare rest.
-__device__ __forceinline__ uint32_t gumbel_hi16(const uint4& a, uint32_t v) {
-  const uint32_t w = word_of(a, (v >> 1) & 3u);
-  return (v & 1u) ? (w >> 16) : (w & 0xffffu);
-}
-__device__ __forceinline__ uint32_t gumbel_lo7(const RngKey& key, uint32_t stream, uint32_t req, uint32_t pos,
-                                               uint32_t v) {
-  return word_of(rng_call(key, stream + 4u, req, pos, v >> 2), v & 3u) >> 25;
-}
-__device__ __forceinline__ float gumbel_noise_at(const RngKey& key, uint32_t stream, uint32_t req, uint32_t pos,
-                                                 uint32_t v) {
-  const uint32_t hi = gumbel_hi16(rng_call(key, stream, req, pos, v >> 3), v);
-  return gumbel_from_bits((hi << 7) | gumbel_lo7(key, stream, req, pos, v));
 }
 
 // ---------------------------------------------------------------------------

@@ -107,7 +107,7 @@ draft_step_cuda_core(const float* __restrict__ U, const void* __restrict__ W1,
       const uint32_t w = word_of(rng_call(key, kStreamDraft, (uint32_t)b, (uint32_t)k, jb >> 2), jb & 3u);
       const float z = m4 + logf(s4) + gumbel_from_bits(w >> 9);
       if (argmax_key(z, v4) > best) {
-        const int v = block_pick(key, (uint32_t)b, (uint32_t)k, jb, e[0], e[1], e[2], e[3]);
+        const int v = block_pick(key, kStreamDraft, (uint32_t)b, (uint32_t)k, jb, e[0], e[1], e[2], e[3]);
         const unsigned long long kz = argmax_key(z, v);
         best = kz > best ? kz : best;
       }

@@ -128,47 +128,15 @@ __device__ __forceinline__ float race_bound(float run_m, float zbest) {
   return exp2f((run_m - zbest) * kLog2e) * (1.0f + 0x1p-10f);
 }
 
-// Per-token random words (the residual race): the 16 high random bits of this
-// thread's columns; 32-bit word j of `wv` holds the bits of columns v0 + 2j
-// (low half) and v0 + 2j + 1 (high half).  v0 is a multiple of min(CPP, 8), so
-// every index below is known at compile time except, for CPP = 4, which half
-// of the call's four words is used.
+// The block race (draft: stream 0; residual: stream 2).  Block j (entries
+// 4j .. 4j+3) takes word j of the stream's call sequence (word j mod 4 of
+// call j / 4).  A thread's CPP / 4 blocks start at block v0 / 4, a multiple
+// of CPP / 4, so one call covers them.
 template <int CPP>
-__device__ __forceinline__ void entry_words(uint32_t (&wv)[(CPP + 1) / 2], const RngKey& key, uint32_t stream,
+__device__ __forceinline__ void block_words(uint32_t (&wb)[CPP / 4], const RngKey& key, uint32_t stream,
                                             uint32_t req, uint32_t pos, int v0) {
-  if constexpr (CPP >= 8) {
-#pragma unroll
-    for (int j = 0; j < CPP / 8; ++j) {
-      const uint4 ra = rng_call(key, stream, req, pos, ((uint32_t)v0 >> 3) + j);
-      wv[4 * j] = ra.x; wv[4 * j + 1] = ra.y; wv[4 * j + 2] = ra.z; wv[4 * j + 3] = ra.w;
-    }
-  } else {
-    static_assert(CPP == 4, "4, 8 or 16 columns per thread");
-    const uint4 ra = rng_call(key, stream, req, pos, (uint32_t)v0 >> 3);
-    const bool up = (v0 & 4) != 0;
-    wv[0] = up ? ra.z : ra.x;
-    wv[1] = up ? ra.w : ra.y;
-  }
-}
-
-// 2^23 + h built exactly as a float from the high 16 bits h of column c (c is
-// a constant once the callers' loops are unrolled): one mask or one byte
-// permutation.
-template <int CPP>
-__device__ __forceinline__ float entry_hf(const uint32_t (&wv)[(CPP + 1) / 2], int c) {
-  const uint32_t w = wv[c >> 1];
-  return __uint_as_float((c & 1) ? __byte_perm(w, 0x4B000000u, 0x7632) : ((w & 0xFFFFu) | 0x4B000000u));
-}
-
-// The draft's block race.  Block j (tokens 4j .. 4j+3) takes word j of the
-// draft stream's call sequence (word j mod 4 of call j / 4).  A thread's
-// CPP / 4 blocks start at block v0 / 4, a multiple of CPP / 4, so one call
-// covers them.
-template <int CPP>
-__device__ __forceinline__ void block_words(uint32_t (&wb)[CPP / 4], const RngKey& key, uint32_t req, uint32_t pos,
-                                            int v0) {
   const uint32_t j0 = (uint32_t)v0 >> 2;
-  const uint4 ra = rng_call(key, kStreamDraft, req, pos, j0 >> 2);
+  const uint4 ra = rng_call(key, stream, req, pos, j0 >> 2);
   if constexpr (CPP == 16) {
     wb[0] = ra.x; wb[1] = ra.y; wb[2] = ra.z; wb[3] = ra.w;
   } else if constexpr (CPP == 8) {
@@ -242,7 +210,7 @@ __device__ __forceinline__ void race_seed(RowRace& st, float (&l)[CPP], const ui
   }
   const uint32_t j = ((uint32_t)v0 >> 2) + (uint32_t)bq;
   st.zbest = st.run_m + logf(bs) + gumbel_from_bits(bw >> 9);
-  st.best_v = block_pick(key, req, pos, j, e0, e1, e2, e3);
+  st.best_v = block_pick(key, kStreamDraft, req, pos, j, e0, e1, e2, e3);
   st.zthr = fmaxf(st.zthr, st.zbest);
   st.bound = race_bound(st.run_m, st.zthr);
   st.run_s += bs;
@@ -296,7 +264,7 @@ __device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP]
     const float z = st.run_m + logf(sq) + gumbel_from_bits(pick_word<NB>(wb, q) >> 9);
     if (z > st.zbest) {
       st.zbest = z;
-      st.best_v = block_pick(key, req, pos, ((uint32_t)v0 >> 2) + (uint32_t)q, e.x, e.y, e.z, e.w);
+      st.best_v = block_pick(key, kStreamDraft, req, pos, ((uint32_t)v0 >> 2) + (uint32_t)q, e.x, e.y, e.z, e.w);
       if (z > st.zthr) {
         st.zthr = z;
         st.bound = race_bound(st.run_m, st.zthr);
@@ -337,13 +305,14 @@ __device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], 
   st.run_s += s;
 }
 
-// Race of the residual resample: argmax_v log rho_v + G_v over rho_v > 0,
-// rho = max(0, p_t - p_d).  Entry v can beat zbest only if
-// E_v < rho_v exp(-zbest), so the same cheap test on the raw random bits
-// applies with rho_v in place of the softmax term.
+// Race of the residual resample: the two-level draw from rho = max(0, p_t -
+// p_d) on streams 2 and 6.  Blocks of 4 race with log W_q + G_q, W_q the
+// block's summed rho.  A block can beat zthr only if E_q < W_q exp(-zthr), so
+// the draft's screen applies with W_q in place of the softmax mass and
+// bound = exp(-zthr).
 struct ResRace {
-  float zbest;   // best perturbed value of this thread's entries
-  int best_v;
+  float zbest;   // best perturbed log-weight of this thread's blocks
+  int best_v;    // the entry drawn inside that block
   float zthr;    // best known anywhere in the row (>= zbest)
   float zpub;    // zbest as last published to the row's key
   float bound;   // exp(-zthr) with a 2^-10 safety margin
@@ -356,49 +325,61 @@ __device__ __forceinline__ void resid_raise(ResRace& st, float z) {
   }
 }
 
+// One tile of the residual race.  rho[c] is this thread's entry v0 + c (any
+// value; non-positive ones and those past the vocabulary weigh nothing).
+// spill is the thread's row in shared memory (block q in 16-byte chunk
+// j0 + q, swizzled by sw).
 template <int CPP>
-__device__ __forceinline__ void resid_tile(ResRace& st, const float (&rho)[CPP], int nv, int v0, unsigned char* spill,
+__device__ __forceinline__ void resid_tile(ResRace& st, float (&rho)[CPP], int nv, int v0, unsigned char* spill,
                                            int j0, int sw, const RngKey& key, uint32_t req, uint32_t pos) {
-  if (st.zbest == -INFINITY) {
-    float rmax = 0.f;
-    int cs = -1;
+  constexpr int NB = CPP / 4;
 #pragma unroll
-    for (int c = 0; c < CPP; ++c)
-      if (c < nv && rho[c] > rmax) { rmax = rho[c]; cs = c; }
-    if (cs < 0) return;   // no positive residual mass seen yet
-    const int v = v0 + cs;
-    st.zbest = logf(rmax) + gumbel_noise_at(key, kStreamResidual, req, pos, (uint32_t)v);
-    st.best_v = v;
+  for (int c = 0; c < CPP; ++c) rho[c] = (c < nv) ? fmaxf(rho[c], 0.f) : 0.f;
+  uint32_t wb[NB];
+  block_words<CPP>(wb, key, kStreamResidual, req, pos, v0);
+  float W[NB];
+#pragma unroll
+  for (int q = 0; q < NB; ++q) W[q] = ((rho[4 * q] + rho[4 * q + 1]) + rho[4 * q + 2]) + rho[4 * q + 3];
+  if (st.zbest == -INFINITY) {
+    // open the race with the block most likely to win: largest W_q / (1 - u_q)
+    float bw = 0.f, bd = 1.f;
+    int bq = -1;
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      const float d = 8454144.0f - block_hf(wb[q]);   // 65536 - h
+      if (W[q] > 0.f && (bq < 0 || W[q] * bd > bw * d)) { bw = W[q]; bd = d; bq = q; }
+    }
+    if (bq < 0) return;   // no residual weight seen yet
+    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+    uint32_t wq = 0u;
+#pragma unroll
+    for (int q = 0; q < NB; ++q)
+      if (q == bq) { r0 = rho[4 * q]; r1 = rho[4 * q + 1]; r2 = rho[4 * q + 2]; r3 = rho[4 * q + 3]; wq = wb[q]; W[q] = 0.f; }
+    st.zbest = logf(bw) + gumbel_from_bits(wq >> 9);
+    st.best_v = block_pick(key, kStreamResidual, req, pos, ((uint32_t)v0 >> 2) + (uint32_t)bq, r0, r1, r2, r3);
     resid_raise(st, st.zbest);
   }
-  // the same screen on the high 16 random bits as the draft race, with rho_v
-  // in place of the softmax term (only the largest left-hand side is kept;
-  // a tile that may hold a winner rebuilds the candidate mask)
-  uint32_t wv[(CPP + 1) / 2];
-  entry_words<CPP>(wv, key, kStreamResidual, req, pos, v0);
   const float b16 = st.bound * 65536.0f;
   float smax = 0.f;
 #pragma unroll
-  for (int c = 0; c < CPP; ++c)
-    if (c < nv) smax = fmaxf(smax, fmaf(fmaxf(rho[c], 0.f), b16, entry_hf<CPP>(wv, c)));
+  for (int q = 0; q < NB; ++q) smax = fmaxf(smax, fmaf(W[q], b16, block_hf(wb[q])));
   if (smax > kScreenThr) {
     uint32_t cand = 0;
 #pragma unroll
-    for (int c = 0; c < CPP; ++c)
-      if (c < nv && rho[c] > 0.f && fmaf(rho[c], b16, entry_hf<CPP>(wv, c)) > kScreenThr) cand |= 1u << c;
-#pragma unroll
-    for (int c = 0; c < CPP; c += 4)
-      *reinterpret_cast<float4*>(spill + (((j0 + c / 4) ^ sw) << 4)) = make_float4(rho[c], rho[c + 1], rho[c + 2], rho[c + 3]);
+    for (int q = 0; q < NB; ++q) {
+      if (W[q] > 0.f && fmaf(W[q], b16, block_hf(wb[q])) > kScreenThr) cand |= 1u << q;
+      *reinterpret_cast<float4*>(spill + (((j0 + q) ^ sw) << 4)) =
+          make_float4(rho[4 * q], rho[4 * q + 1], rho[4 * q + 2], rho[4 * q + 3]);
+    }
 #pragma unroll 1
     while (cand) {
-      const int c = __ffs(cand) - 1;
+      const int q = __ffs(cand) - 1;
       cand &= cand - 1;
-      const uint32_t v = (uint32_t)(v0 + c);
-      const uint32_t hi = gumbel_hi16(rng_call(key, kStreamResidual, req, pos, v >> 3), v);
-      const float z = logf(reinterpret_cast<const float*>(spill + (((j0 + c / 4) ^ sw) << 4))[c & 3]) + gumbel_from_bits((hi << 7) | gumbel_lo7(key, kStreamResidual, req, pos, v));
+      const float4 e = *reinterpret_cast<const float4*>(spill + (((j0 + q) ^ sw) << 4));
+      const float z = logf(((e.x + e.y) + e.z) + e.w) + gumbel_from_bits(pick_word<NB>(wb, q) >> 9);
       if (z > st.zbest) {
         st.zbest = z;
-        st.best_v = (int)v;
+        st.best_v = block_pick(key, kStreamResidual, req, pos, ((uint32_t)v0 >> 2) + (uint32_t)q, e.x, e.y, e.z, e.w);
         resid_raise(st, z);
       }
     }
@@ -757,7 +738,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
               for (int c = 0; c < CPP; ++c)
                 if (c >= nv) v[c] = -INFINITY;
             }
-            block_words<CPP>(wb, p.key, (uint32_t)b, (uint32_t)k, v0);
+            block_words<CPP>(wb, p.key, kStreamDraft, (uint32_t)b, (uint32_t)k, v0);
             if (st.run_m == -INFINITY) race_prep<CPP>(st, v);
             if (st.zbest == -INFINITY) race_seed<CPP>(st, v, wb, v0, p.key, (uint32_t)b, (uint32_t)k);
           }

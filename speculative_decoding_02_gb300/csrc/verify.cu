@@ -154,18 +154,24 @@ verify_row_stats(const float* __restrict__ T, int V, int nsegs, const int32_t* _
   if (bad) record_status(status, DSPARK_ERR_NONFINITE);
 }
 
-// The bonus race of every request over its row j = ell[b] (the bonus token if
-// the whole prefix survives, [blog] section 1): y = argmax_v T[b, j, v] +
-// G(stream 3, b, j + 1, v), one (request, segment) task per iteration.  The
-// race is screened on the high 16 random bits as in the draft: the running
-// maximum of the row part gives the bound; candidates are resolved exactly.
+// Block screen value 2^23 + h from a word's high 16 bits h (one byte permutation).
+__device__ __forceinline__ float block_hf_v(uint32_t w) {
+  return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632));
+}
+constexpr float kScreenThrV = 8454142.0f;   // 2^23 + 65534 (see the draft race)
+
+// The bonus draw of every request from its row j = ell[b] (the bonus token if
+// the whole prefix survives, [blog] section 1): the two-level draw from
+// softmax(T[b, j, :]) on streams 3 and 7, one (request, segment) task per
+// iteration.  A thread takes 16 consecutive tokens at a time (four blocks, one
+// Philox call): the block weights exp(T - m) against the running maximum m,
+// a screen of each block on its 16 high random bits, exact values for the
+// rare candidates and the token inside a block that takes the lead.
 __global__ void __launch_bounds__(kRowThreads)
 verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, int B, int G, int V, int nsegs,
                   RngKey key, unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
   __shared__ unsigned long long s_k[kRowThreads / 32];
-  constexpr int kBatch = 8;
-  constexpr int kStride = 4 * kRowThreads;
-  constexpr int kBatches = kVerifySeg / (kBatch * kStride);
+  constexpr int kChunks = kVerifySeg / (16 * kRowThreads);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int ntasks = B * nsegs;
   bool bad = false;
@@ -176,68 +182,68 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, 
     const uint32_t pos = (uint32_t)(jrow + 1);
     const float* Trow = T + (size_t)rowid * V;
     const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
-    float m = -INFINITY;
-    float zbest = -INFINITY;
+    float m = -INFINITY, zbest = -INFINITY, bound = INFINITY;
     int bestv = -1;
 #pragma unroll 1
-    for (int bt = 0; bt < kBatches; ++bt) {
-      const int vb = v0 + bt * kBatch * kStride + 4 * tid;
-      if (vb >= v1) break;
-      float4 t4[kBatch];
+    for (int ch = 0; ch < kChunks; ++ch) {
+      const int vc = v0 + 16 * (ch * kRowThreads + tid);
+      if (vc >= v1) break;
+      float tv[16];
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int v = vb + kStride * j;
-        t4[j] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(Trow + v))
-                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      for (int i = 0; i < 4; ++i) {
+        const float4 t4 = (vc + 4 * i < v1) ? __ldcs(reinterpret_cast<const float4*>(Trow + vc + 4 * i))
+                                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        tv[4 * i] = t4.x; tv[4 * i + 1] = t4.y; tv[4 * i + 2] = t4.z; tv[4 * i + 3] = t4.w;
       }
-      float bm = -INFINITY;
+      float cm = tv[0];
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) bm = fmaxf(fmaxf(bm, fmaxf(t4[j].x, t4[j].y)), fmaxf(t4[j].z, t4[j].w));
-      bad |= !(bm < INFINITY);
-      m = fmaxf(m, bm);
+      for (int c = 1; c < 16; ++c) cm = fmaxf(cm, tv[c]);
+      bad |= !(cm < INFINITY);
+      if (cm > m) {
+        m = cm;
+        if (zbest > -INFINITY) bound = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f);
+      }
       if (m == -INFINITY) continue;
       const float mb = m * kLog2eF;
+      float e[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) e[c] = exp2_fast(fmaf(tv[c], kLog2eF, -mb));
+      float W[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) W[q] = ((e[4 * q] + e[4 * q + 1]) + e[4 * q + 2]) + e[4 * q + 3];
+      const uint4 ra = rng_call(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)vc >> 4);
+      const uint32_t wq[4] = {ra.x, ra.y, ra.z, ra.w};
       if (zbest == -INFINITY) {
-        // seed the race with the largest logit of the batch
-        int cs = 0;
+        // open the race with the block most likely to win
+        float bw = 0.f, bd = 1.f;
+        int bq = 0;
 #pragma unroll
-        for (int j = kBatch - 1; j >= 0; --j) {
-          if (t4[j].w == bm) cs = 4 * j + 3;
-          if (t4[j].z == bm) cs = 4 * j + 2;
-          if (t4[j].y == bm) cs = 4 * j + 1;
-          if (t4[j].x == bm) cs = 4 * j;
+        for (int q = 0; q < 4; ++q) {
+          const float d = 8454144.0f - block_hf_v(wq[q]);
+          if (W[q] * bd > bw * d) { bw = W[q]; bd = d; bq = q; }
         }
-        bestv = vb + kStride * (cs >> 2) + (cs & 3);
-        zbest = bm + gumbel_noise_at(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)bestv);
-      }
-      // screen on the high 16 random bits (see the draft race)
-      const float b32 = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f) * 32768.0f;
-      uint32_t cand = 0;
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int v = vb + kStride * j;
-        if (v < v1) {
-          const uint4 ra = rng_call(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)(v >> 3));
-          const float tv[4] = {t4[j].x, t4[j].y, t4[j].z, t4[j].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t vq = (uint32_t)(v + q);
-            const uint32_t w = word_of(ra, (vq >> 1) & 3u);
-            const uint32_t hb = (vq & 1u) ? ((w >> 9) & 0x7FFF80u) : ((w << 7) & 0x7FFF80u);
-            const float e = exp2_fast(fmaf(tv[q], kLog2eF, -mb));
-            if (__uint_as_float(0x47000000u | hb) > fmaf(-e, b32, 65535.0f)) cand |= 1u << (4 * j + q);
+        for (int q = 0; q < 4; ++q) {
+          if (q == bq) {
+            zbest = m + logf(W[q]) + gumbel_from_bits(wq[q] >> 9);
+            bestv = block_pick(key, kStreamBonus, (uint32_t)b, pos, ((uint32_t)vc >> 2) + q, e[4 * q],
+                               e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
+            W[q] = 0.f;
           }
         }
+        bound = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f);
       }
-#pragma unroll 1
-      while (cand) {
-        const int c = __ffs(cand) - 1;
-        cand &= cand - 1;
-        const int v = vb + kStride * (c >> 2) + (c & 3);
-        const float z = __ldcs(Trow + v) + gumbel_noise_at(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)v);
-        if (z > zbest || (z == zbest && v < bestv)) {
-          zbest = z;
-          bestv = v;
+      const float b16 = bound * 65536.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (W[q] > 0.f && fmaf(W[q], b16, block_hf_v(wq[q])) > kScreenThrV) {
+          const float z = m + logf(W[q]) + gumbel_from_bits(wq[q] >> 9);
+          if (z > zbest) {
+            zbest = z;
+            bestv = block_pick(key, kStreamBonus, (uint32_t)b, pos, ((uint32_t)vc >> 2) + q, e[4 * q],
+                               e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
+            bound = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f);
+          }
         }
       }
     }
@@ -323,8 +329,8 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
   const int v_begin = blockIdx.x * kDraftSlice, v_end = min(V, v_begin + kDraftSlice);
   unsigned long long k1 = 0ull;
   for (int v4 = v_begin + 4 * tid; v4 < v_end; v4 += 4 * kRowThreads) {
-    const uint4 ra = rng_call(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v4 >> 3));
-    const uint4 rb = rng_call(key, kStreamResidual + 4u, (uint32_t)b, (uint32_t)ks, (uint32_t)(v4 >> 2));
+    // one block of 4 entries of the residual draw (streams 2 and 6)
+    float rho[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int v = v4 + q;
@@ -332,10 +338,16 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
       for (int i = 0; i < r; ++i) bias = fmaf(Es[i], load_weight<WDT>(W2, (size_t)v * r + i), bias);
       const float pd = expf(Urow[v] + bias - ld);
       const float pt = expf(Trow[v] - lt);
-      const float rho = pt - pd;
-      if (rho > 0.f) {
-        const uint32_t m = (gumbel_hi16(ra, (uint32_t)v) << 7) | (word_of(rb, (uint32_t)q) >> 25);
-        const unsigned long long kz = argmax_key(logf(rho) + gumbel_from_bits(m), v);
+      rho[q] = fmaxf(pt - pd, 0.f);
+    }
+    const float W = ((rho[0] + rho[1]) + rho[2]) + rho[3];
+    if (W > 0.f) {
+      const uint32_t j = (uint32_t)v4 >> 2;
+      const uint32_t w = word_of(rng_call(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, j >> 2), j & 3u);
+      const float z = logf(W) + gumbel_from_bits(w >> 9);
+      if (argmax_key(z, v4) > k1) {
+        const int v = block_pick(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, j, rho[0], rho[1], rho[2], rho[3]);
+        const unsigned long long kz = argmax_key(z, v);
         k1 = kz > k1 ? kz : k1;
       }
     }
@@ -350,8 +362,8 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
 }
 
 // One block per request.  A rejecting request takes the winner of the residual
-// race; if the residual had no positive entry in floating point (a measure-zero
-// event in exact arithmetic) it draws from p_t instead, with the same noise.
+// draw; if the residual had no positive entry in floating point (a measure-zero
+// event in exact arithmetic) it draws from p_t instead, with the same streams.
 __global__ void __launch_bounds__(kRowThreads)
 verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKey key,
                          const int32_t* __restrict__ resid_k, const unsigned long long* __restrict__ resid_key,
@@ -366,16 +378,31 @@ verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKe
     return;
   }
   const float* Trow = T + ((size_t)b * (G + 1) + (ks - 1)) * (size_t)V;
+  // the row's maximum, then the two-level draw of softmax(T row) (streams 2
+  // and 6) with weights exp(T - max)
+  __shared__ float s_m[kRowThreads / 32];
+  float mx = -INFINITY;
+  for (int v = 4 * threadIdx.x; v < V; v += 4 * kRowThreads) {
+    const float4 t4 = *reinterpret_cast<const float4*>(Trow + v);
+    mx = fmaxf(mx, fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w)));
+  }
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = s_m[0];
+  for (int w = 1; w < kRowThreads / 32; ++w) mx = fmaxf(mx, s_m[w]);
   unsigned long long best = 0ull;
   for (int v = 4 * threadIdx.x; v < V; v += 4 * kRowThreads) {
     const float4 t4 = *reinterpret_cast<const float4*>(Trow + v);
-    const uint4 ra = rng_call(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, (uint32_t)(v >> 3));
-    const uint4 rb = rng_call(key, kStreamResidual + 4u, (uint32_t)b, (uint32_t)ks, (uint32_t)(v >> 2));
-    const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t m = (gumbel_hi16(ra, (uint32_t)(v + q)) << 7) | (word_of(rb, (uint32_t)q) >> 25);
-      const unsigned long long kz = argmax_key(tv[q] + gumbel_from_bits(m), v + q);
+    const float e0 = expf(t4.x - mx), e1 = expf(t4.y - mx), e2 = expf(t4.z - mx), e3 = expf(t4.w - mx);
+    const float W = ((e0 + e1) + e2) + e3;
+    if (!(W > 0.f)) continue;
+    const uint32_t j = (uint32_t)v >> 2;
+    const uint32_t w = word_of(rng_call(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, j >> 2), j & 3u);
+    const float z = mx + logf(W) + gumbel_from_bits(w >> 9);
+    if (argmax_key(z, v) > best) {
+      const int vv = block_pick(key, kStreamResidual, (uint32_t)b, (uint32_t)ks, j, e0, e1, e2, e3);
+      const unsigned long long kz = argmax_key(z, vv);
       best = kz > best ? kz : best;
     }
   }
