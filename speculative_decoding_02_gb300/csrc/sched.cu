@@ -40,8 +40,9 @@ constexpr int kSchedThreads = 1024;
 // One CTA.  a = prefix products in fp64.  The candidates are sorted as 64-bit
 // integers: the bits of a (non-negative, so ordered like the values) with the
 // low 13 bits replaced by 8191 - index, index = b*gamma + j-1; a descending
-// integer sort then gives a desc, b asc, j asc (values closer than 2^-39
-// relative count as ties and fall back to the index order).  The exact a
+// integer sort (merges of the per-request runs) then gives a desc, b asc,
+// j asc (values closer than 2^-39 relative count as ties and fall back to the
+// index order).  The exact a
 // values stay aside for an inclusive fp64 scan of the sorted list;
 // Theta_n = (R + S_n) * SPS(R + n), and the greedy count n* is one less than
 // the first n whose Theta does not exceed Theta_{n-1}.
@@ -54,8 +55,9 @@ schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restri
   const int N = R * G;
   int NP = 1;
   while (NP < N) NP <<= 1;
-  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem_raw);   // [NP]
-  double* av = reinterpret_cast<double*>(key + NP);                              // [N]
+  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem_raw);   // [NP]: sort buffer A
+  unsigned long long* key2 = key + NP;                                           // [NP]: sort buffer B
+  double* av = reinterpret_cast<double*>(key2 + NP);                             // [N]
   int* ell_s = reinterpret_cast<int*>(av + N);                                   // [R]
   __shared__ double warp_tot[32];
   __shared__ int s_first_stop;
@@ -85,7 +87,6 @@ schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restri
     if (bad) record_status(status, DSPARK_ERR_NONFINITE);
     ell_s[b] = 0;
   }
-  for (int i = N + tid; i < NP; i += kSchedThreads) key[i] = 0ull;
   if (tid == 0) {
     s_first_stop = N + 1;
     s_K = -1;
@@ -93,21 +94,40 @@ schedule_kernel(const float* __restrict__ c, int R, int G, const float* __restri
   }
   __syncthreads();
 
-  // bitonic sort, descending
-  for (int size = 2; size <= NP; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = tid; t < (NP >> 1); t += kSchedThreads) {
-        const int i = (t / stride) * (stride << 1) + (t % stride);
-        const int j = i + stride;
-        const unsigned long long ki = key[i], kj = key[j];
-        const bool desc = (i & size) == 0;
-        if (desc ? (kj > ki) : (ki > kj)) {
-          key[i] = kj;
-          key[j] = ki;
+  // Sort the keys descending by merging.  Each request's G keys are already in
+  // descending order (c <= 1 makes a non-increasing in j, and equal a break
+  // by the smaller j), so ceil(log2 R) rounds of pairwise merges of adjacent
+  // runs finish the sort.  In a round every key finds its place on its own:
+  // its index in its run plus the number of keys of the partner run that are
+  // larger (binary search; keys are distinct through their index bits).
+  unsigned long long* src = key;
+  unsigned long long* dst = key2;
+  for (int run = G; run < N; run <<= 1) {
+    for (int i = tid; i < N; i += kSchedThreads) {
+      const unsigned long long x = src[i];
+      const int r0 = (i / run) * run;             // start of this key's run
+      const bool left = ((i / run) & 1) == 0;
+      const int p0 = left ? r0 + run : r0 - run;  // start of the partner run
+      const int p1 = min(p0 + run, N);
+      int rank = 0;
+      if (p0 < N) {
+        // number of partner keys larger than x (partner run is descending)
+        int lo = p0, hi = p1;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (src[mid] > x) lo = mid + 1; else hi = mid;
         }
+        rank = lo - p0;
       }
-      __syncthreads();
+      const int base = left ? r0 : p0;            // start of the merged run
+      dst[base + (i - r0) + rank] = x;
     }
+    __syncthreads();
+    unsigned long long* t = src; src = dst; dst = t;
+  }
+  if (src != key) {
+    for (int i = tid; i < N; i += kSchedThreads) key[i] = src[i];
+    __syncthreads();
   }
 
   // the exact a of each sorted position, then an inclusive scan in place:
@@ -189,7 +209,7 @@ cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdt
 size_t schedule_smem_bytes(int B, int gamma) {
   int NP = 1;
   while (NP < B * gamma) NP <<= 1;
-  return (size_t)NP * sizeof(unsigned long long) + (size_t)B * gamma * sizeof(double) + sizeof(int) * (size_t)B;
+  return 2 * (size_t)NP * sizeof(unsigned long long) + (size_t)B * gamma * sizeof(double) + sizeof(int) * (size_t)B;
 }
 
 cudaError_t launch_schedule(const float* c, int B, int gamma, const float* sps, int mode,
