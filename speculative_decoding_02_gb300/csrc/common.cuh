@@ -212,7 +212,7 @@ struct WsLayout {
   size_t status;      // int32 status word
   size_t counters;    // int32 [8]: [0] verify row count
   size_t draft_keys;  // u64 [gamma][B], kKeyStride apart
-  size_t draft_part;  // float2 [gamma][nslices][B]
+  size_t draft_part;  // float2 [gamma][B][nslices]
   size_t rows;        // int32 [B*gamma] row ids b*(gamma+1)+j (j < ell_b) of the rows whose stats verify needs
   size_t row_part;    // float2 [B*(gamma+1)][nsegs]
   size_t bonus_key;   // u64 [B]

@@ -117,7 +117,7 @@ draft_step_cuda_core(const float* __restrict__ U, const void* __restrict__ W1,
   warp_softmax_reduce(run_m, run_s, 0xffffffffu, 8);
   best = warp_max_u64(best, 0xffffffffu, 8);
   if (row_ok && (tid & 7) == 0) {
-    part[(size_t)slice * B + b] = make_float2(run_m, run_s);
+    part[(size_t)b * gridDim.x + slice] = make_float2(run_m, run_s);
     atomicMax(&keys[(size_t)b * kKeyStride], best);
   }
   if (bad) record_status(status, DSPARK_ERR_NONFINITE);
@@ -139,7 +139,7 @@ __global__ void draft_finalize(const float* __restrict__ U, const void* __restri
   const int b = warp;
   float m = -INFINITY, s = 0.f;
   for (int i = lane; i < nslices; i += 32) {
-    const float2 pr = part[(size_t)i * B + b];
+    const float2 pr = part[(size_t)b * nslices + i];
     softmax_merge(m, s, pr.x, pr.y);
   }
   warp_softmax_reduce(m, s, 0xffffffffu, 32);

@@ -843,7 +843,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           K = xk[j * R + r] > K ? xk[j * R + r] : K;
         }
         if constexpr (MODE == kDraft) {
-          p.part[((size_t)(k - 1) * p.part_slices + slice) * p.B + b] = make_float2(M, S);
+          p.part[((size_t)(k - 1) * p.B + b) * p.part_slices + slice] = make_float2(M, S);
           if (K) atomicMax(&p.keys[((size_t)(k - 1) * p.B + b) * kKeyStride], K);
         } else {
           if (K) atomicMax(&p.resid_key[(size_t)b * kKeyStride], K);
@@ -901,7 +901,7 @@ __global__ void draft_finalize_tc(const float* __restrict__ U, const __nv_bfloat
   const float2* pp = part + (size_t)(k - 1) * part_slices * B;
   float m = -INFINITY, s = 0.f;
   for (int i = lane; i < nslices; i += 32) {
-    const float2 pr = pp[(size_t)i * B + b];
+    const float2 pr = pp[(size_t)b * part_slices + i];
     softmax_merge(m, s, pr.x, pr.y);
   }
   warp_softmax_reduce(m, s, 0xffffffffu, 32);

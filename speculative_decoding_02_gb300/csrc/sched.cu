@@ -6,11 +6,36 @@ namespace dspark {
 namespace {
 
 // c_k = sigmoid((w[:H] . h_k + w[H:] . W1[x_{k-1}]) / T_k), one warp per (b, k).
+// z + sum_{e < 8} wv[e] * x[i + e] for 8 consecutive elements of x (bf16 or f32
+// storage, element offset i a multiple of 8 from a 16-byte aligned base).
+template <int DT>
+__device__ __forceinline__ float dot8(const void* x, size_t i, const float* __restrict__ wv, float z) {
+  const float4 w0 = *reinterpret_cast<const float4*>(wv);
+  const float4 w1 = *reinterpret_cast<const float4*>(wv + 4);
+  float v[8];
+  if constexpr (DT == DSPARK_BF16) {
+    const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + i);
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = __uint_as_float(u[e] << 16);
+      v[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+    }
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + i);
+    const float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + i + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+  }
+  z = fmaf(w0.x, v[0], z); z = fmaf(w0.y, v[1], z); z = fmaf(w0.z, v[2], z); z = fmaf(w0.w, v[3], z);
+  z = fmaf(w1.x, v[4], z); z = fmaf(w1.y, v[5], z); z = fmaf(w1.z, v[6], z); z = fmaf(w1.w, v[7], z);
+  return z;
+}
+
 template <int HDT, int WDT>
 __global__ void confidence_kernel(const void* __restrict__ h, const void* __restrict__ W1,
                                   const float* __restrict__ w, const float* __restrict__ sts_T,
                                   const int32_t* __restrict__ anchor, const int32_t* __restrict__ x,
-                                  int B, int G, int H, int r, int V, float* __restrict__ c_out,
+                                  int B, int G, int H, int r, int V, bool vec, float* __restrict__ c_out,
                                   int* __restrict__ status) {
   const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -26,8 +51,16 @@ __global__ void confidence_kernel(const void* __restrict__ h, const void* __rest
   }
   const size_t hrow = (size_t)item * H;
   float z = 0.f;
-  for (int i = lane; i < H; i += 32) z = fmaf(w[i], load_weight<HDT>(h, hrow + i), z);
-  for (int i = lane; i < r; i += 32) z = fmaf(w[H + i], load_weight<WDT>(W1, (size_t)prev * r + i), z);
+  if (vec) {
+    // 8 elements per lane per step: 16-byte loads of bf16 (two 16-byte loads
+    // of f32), the weight as two float4 (16-byte aligned bases, H and r
+    // multiples of 8 keep every row aligned)
+    for (int i = 8 * lane; i < H; i += 256) z = dot8<HDT>(h, hrow + i, w + i, z);
+    for (int i = 8 * lane; i < r; i += 256) z = dot8<WDT>(W1, (size_t)prev * r + i, w + H + i, z);
+  } else {
+    for (int i = lane; i < H; i += 32) z = fmaf(w[i], load_weight<HDT>(h, hrow + i), z);
+    for (int i = lane; i < r; i += 32) z = fmaf(w[H + i], load_weight<WDT>(W1, (size_t)prev * r + i), z);
+  }
   for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
   if (lane == 0) {
     const float T = sts_T ? sts_T[k - 1] : 1.f;
@@ -195,14 +228,15 @@ cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdt
                               cudaStream_t stream) {
   const int items = B * gamma;
   const dim3 grid(div_up(items * 32, 256));
+  const bool vec = (H % 8 == 0) && (r % 8 == 0) && (((uintptr_t)h | (uintptr_t)W1 | (uintptr_t)w) % 16 == 0);
   if (hdtype == DSPARK_BF16 && wdtype == DSPARK_BF16)
-    confidence_kernel<DSPARK_BF16, DSPARK_BF16><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, c_out, status);
+    confidence_kernel<DSPARK_BF16, DSPARK_BF16><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, vec, c_out, status);
   else if (hdtype == DSPARK_BF16)
-    confidence_kernel<DSPARK_BF16, DSPARK_F32><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, c_out, status);
+    confidence_kernel<DSPARK_BF16, DSPARK_F32><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, vec, c_out, status);
   else if (wdtype == DSPARK_BF16)
-    confidence_kernel<DSPARK_F32, DSPARK_BF16><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, c_out, status);
+    confidence_kernel<DSPARK_F32, DSPARK_BF16><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, vec, c_out, status);
   else
-    confidence_kernel<DSPARK_F32, DSPARK_F32><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, c_out, status);
+    confidence_kernel<DSPARK_F32, DSPARK_F32><<<grid, 256, 0, stream>>>(h, W1, w, sts_T, anchor, x, B, gamma, H, r, V, vec, c_out, status);
   return cudaGetLastError();
 }
 
