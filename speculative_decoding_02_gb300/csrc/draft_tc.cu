@@ -1,24 +1,34 @@
-// Markov draft step on the 5th-generation tensor cores ("[DeepSeek-6] DSpark"
-// blog, sections 3-4; study report Eq.4).
+// Markov draft on the 5th-generation tensor cores ("[DeepSeek-6] DSpark" blog,
+// sections 3-4; study report Eq.4), and the residual resample of verification
+// (the "10 key concepts" digest, item 2), which needs the same fused logits.
 //
-// One launch per position k.  A CTA owns one 128-request M tile and a
-// contiguous range of 64-column vocabulary tiles:
+// Draft: one persistent, cooperative launch runs every position k; 152 CTAs,
+// each owning a 128-request M tile (128 / R replicas of R rows for small
+// batches) and a contiguous range of 64-column vocabulary tiles.  Per CTA:
 //
-//   warp 0      producer: per tile, four 8 KB TMA loads of W2 (one 64-wide K
-//               atom each, 128-byte swizzled, kept in L2 with evict_last) and
-//               up to 128 row copies of U (cp.async.bulk, evict_first) into a
-//               padded shared-memory tile.
-//   warp 1      allocates 128 TMEM columns; one lane issues the bias GEMM
-//               bias[128 x 64] = E[128 x 256] * W2_tile^T with tcgen05.mma
-//               (bf16 in, fp32 accumulate) into one of two TMEM accumulators.
-//   warps 2-9   gather E = W1[x_{k-1}] (128 rows, 128-byte swizzled) once, then
-//               per tile read the accumulator (tcgen05.ld, thread = request
-//               row, 32 columns per warp), add U, and fold the 32 fused logits
-//               into the row's online softmax (m, s) and its Gumbel-max race.
+//   warp 0      TMA producer: W2 in atoms of 192 rows x 64 K (bf16, 128-byte
+//               swizzled, evict_last so W2 stays in L2 across positions) and
+//               U in [R rows x 32 columns] fp32 boxes (evict_first); it runs
+//               ahead across positions, so the next position's first tiles
+//               load while the grid barrier resolves.
+//   warp 1      TMEM allocation (512 columns) and the single-thread MMA
+//               issuer: bias[128 x 64j] = E[128 x 256] * W2_rows^T, j <= 3
+//               tiles per tcgen05.mma (kind::f16, fp32 accumulate), A = E in
+//               TMEM columns 384-511, two accumulators of 192 columns.
+//   warps 2-17  epilogue, four per TMEM lane quarter (thread = request row,
+//               16 columns per tile): tcgen05.ld of the accumulator, + U, the
+//               online softmax and the block race of the sampler (blocks of
+//               4 tokens, screened on 16 random bits, exact only for the rare
+//               candidates).  At a position's end they merge their parts,
+//               publish one (m, s) partial per row and the row's argmax key
+//               (atomicMax), arrive at the grid barrier, gather
+//               E = W1[x_k] speculatively and, after the barrier, reload
+//               the rows whose final token differs.
 //
-// Per CTA and request it leaves (m, s) in the partial buffer and pushes its best
-// perturbed logit into the request's 64-bit argmax key (atomicMax; ties go to
-// the smaller index).  The next position's CTAs decode x_k from that key.
+// Residual (MODE kResidual): the same pipeline for one position per request
+// (the rejected k*), with U and T row segments staged by the epilogue's own
+// coalesced asynchronous copies, racing blocks of max(0, p_t - p_d).
+//
 // Every wait is bounded; on a timeout the CTA records DSPARK_ERR_TIMEOUT,
 // drains the copies and MMAs it issued, frees its TMEM and returns.
 #include <cuda_bf16.h>
@@ -104,20 +114,22 @@ __device__ __forceinline__ int tile_begin(int slice, int nslices, int ntiles) {
   return (int)(((long long)ntiles * slice) / nslices);
 }
 
-// Gumbel-max race of one request row inside one thread's column range.
+// Block race of one request row inside one thread's column range (the
+// two-level sampler: blocks of 4 tokens race with log of their softmax mass
+// plus Gumbel noise; the token inside a leading block is drawn by inverse CDF).
 //
-// The perturbed logit of entry v is z_v = l_v + G_v, G_v = -log E_v,
-// E_v = -log u_v.  Entry v can beat the thread's best zbest only if
-// E_v < exp(l_v - zbest); since E_v >= 1 - u_v this needs
-// 1 - u_v < exp(l_v - run_m) * exp(run_m - zbest).  The first factor is the
-// softmax term already computed for the normaliser, so the test costs one FMA
-// and one compare on the raw random bits; only entries that pass it (a few per
-// thousand once zbest has settled) get the two exact logarithms.
+// Block q's perturbed log-mass is z_q = run_m + log s_q + G_q, G_q = -log E_q,
+// E_q = -log u_q, s_q = sum of exp(l - run_m) over the block.  It can beat zthr
+// only if E_q < s_q exp(run_m - zthr); since E_q >= 1 - u_q this needs
+// 1 - u_q < s_q * bound.  s_q comes from the softmax terms already computed
+// for the normaliser, so the test costs one FMA and one max per block on the
+// word's 16 high bits; only blocks that pass it (a few per thousand once zthr
+// has settled) get the exact logarithms.
 struct RowRace {
   float run_m, run_s;   // online softmax: running max and sum of exp(l - run_m)
-  float zbest;          // best perturbed logit of this thread's entries
-  int best_v;           // its vocabulary index
-  float zthr;           // best perturbed logit known anywhere in the row (>= zbest)
+  float zbest;          // best perturbed block log-mass of this thread's blocks
+  int best_v;           // the token drawn inside that block
+  float zthr;           // best perturbed log-mass known anywhere in the row (>= zbest)
   float zpub;           // zbest as last published to the row's global key
   float bound;          // exp(run_m - zthr) with a 2^-10 safety margin
 };
