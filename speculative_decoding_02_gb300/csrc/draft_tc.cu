@@ -66,8 +66,10 @@ constexpr int kBarBytes = 512;                   // mbarriers and flags
 // segments of one tile (R rows x 64 columns each, 256-byte rows).
 constexpr int kWStagesRes = 2;
 constexpr int kResStageBytes = 2 * BM * 256;      // U then T
+constexpr int kEpiThreads = 32 * 16;       // epilogue threads
+constexpr int kGkBytes = 2 * 16 * kEpiThreads;   // two async copies of the row key per epilogue thread
 constexpr int kSmemBytes =
-    1024 /*align*/ + kWStages * kWStageBytes + kUStages * kUStageBytes + kBarBytes + kXBytes;
+    1024 /*align*/ + kWStages * kWStageBytes + kUStages * kUStageBytes + kBarBytes + kXBytes + kGkBytes;
 static_assert(kWStagesRes * kWStageBytes + 2 * kResStageBytes <= kWStages * kWStageBytes + kUStages * kUStageBytes,
               "residual layout must fit the draft layout");
 
@@ -621,6 +623,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     float* xm = reinterpret_cast<float*>(X_s);
     float* xs = xm + 4 * BM;
     unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 4 * BM);
+    // draft: this thread's two shared-memory slots for copies of its row key
+    ulonglong2* gk_slot = reinterpret_cast<ulonglong2*>(X_s + kXBytes) + (threadIdx.x - 64);
     uint32_t it = 0, gcount = 0;
     int spec_prev = -1;   // token whose W1 row is in TMEM E from the speculative gather
     for (int k = kf; k <= kl; ++k) {
@@ -684,7 +688,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         }
       }
       bool ok = true;
-      unsigned long long gk = 0ull;   // row key as last read (kShare)
+      unsigned long long gk = 0ull;   // residual: row key as last read (kShareRes)
       // residual mode: the U and T row segments of each tile are copied into
       // shared memory one tile ahead by all epilogue threads (resid_copy)
       long long* off_u = reinterpret_cast<long long*>(X_s);   // element offset of row rr's U row, or -1
@@ -769,23 +773,22 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
             }
           }
           if (live) {
-            // the row's best perturbed logit published by any CTA, as read at
-            // the end of the previous tile: the second tile waits for it
-            // (little is known yet), later tiles take it after their screen
-            // so that the load's latency stays hidden
-            if (kShare && gk && i == 1) {
-              const float zg = argmax_key_value(gk);
-              if (zg > st.zthr) {
-                st.zthr = zg;
-                st.bound = race_bound(st.run_m, st.zthr);
-              }
-            }
             race_screen<CPP>(st, v, wb, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k, p.status);
-            if (kShare && gk && i > 1) {
-              const float zg = argmax_key_value(gk);
-              if (zg > st.zthr) {
-                st.zthr = zg;
-                st.bound = race_bound(st.run_m, st.zthr);
+            // the row's best perturbed log-mass published by any CTA: each
+            // tile copies the row key into shared memory asynchronously (two
+            // slots per thread) and, after its screen, takes the copy made
+            // two tiles earlier (the second tile: the first tile's), so that
+            // the copy's latency stays hidden
+            if (kShare && i >= 1) {
+              if (i == 1) cp_async_wait_all();
+              else cp_async_wait_one();
+              const unsigned long long gkd = gk_slot[(i == 1 ? 0 : (i & 1)) * kEpiThreads].x;
+              if (gkd) {
+                const float zg = argmax_key_value(gkd);
+                if (zg > st.zthr) {
+                  st.zthr = zg;
+                  st.bound = race_bound(st.run_m, st.zthr);
+                }
               }
             }
             // share this thread's progress with the other CTAs of the row
@@ -793,7 +796,10 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
               atomicMax(row_key, argmax_key(st.zbest, st.best_v));
               st.zpub = st.zbest;
             }
-            if (kShare) gk = __ldcg(row_key);
+            if (kShare) {
+              cp_async16(gk_slot + (i & 1) * kEpiThreads, row_key);
+              cp_async_commit();
+            }
           }
           __syncwarp();
           if (!got_u) { ok = false; break; }
@@ -833,6 +839,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           }
         }
       }
+      if constexpr (kShare) cp_async_wait_all();   // no copy outlives its position
       if (MODE == kDraft && (st.run_m != st.run_m || st.run_m == INFINITY))
         record_status(p.status, DSPARK_ERR_NONFINITE);
 
