@@ -66,8 +66,7 @@ constexpr int kBarBytes = 512;                   // mbarriers and flags
 // segments of one tile (R rows x 64 columns each, 256-byte rows).
 constexpr int kWStagesRes = 2;
 constexpr int kResStageBytes = 2 * BM * 256;      // U then T
-constexpr int kEpiThreads = 32 * 16;       // epilogue threads
-constexpr int kGkBytes = 2 * 16 * kEpiThreads;   // two async copies of the row key per epilogue thread
+constexpr int kGkBytes = 2 * BM * 16;   // row-key copies: [position parity][row], 16 bytes each
 constexpr int kSmemBytes =
     1024 /*align*/ + kWStages * kWStageBytes + kUStages * kUStageBytes + kBarBytes + kXBytes + kGkBytes;
 static_assert(kWStagesRes * kWStageBytes + 2 * kResStageBytes <= kWStages * kWStageBytes + kUStages * kUStageBytes,
@@ -524,6 +523,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     if (MODE == kDraft) prefetch_tensormap(&u_map);
   }
   if (warp == 1) tmem_alloc(&bars->tmem_base, kTmemCols);
+  for (int idx = threadIdx.x; idx < kGkBytes / 16; idx += kThreads)
+    reinterpret_cast<uint4*>(X_s + kXBytes)[idx] = make_uint4(0u, 0u, 0u, 0u);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -623,8 +624,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     float* xm = reinterpret_cast<float*>(X_s);
     float* xs = xm + 4 * BM;
     unsigned long long* xk = reinterpret_cast<unsigned long long*>(xs + 4 * BM);
-    // draft: this thread's two shared-memory slots for copies of its row key
-    ulonglong2* gk_slot = reinterpret_cast<ulonglong2*>(X_s + kXBytes) + (threadIdx.x - 64);
+    // draft: shared-memory copies of the row keys, one region per position
+    // parity (filled by the first warp of each lane quarter, read by all)
+    ulonglong2* gk_rows = reinterpret_cast<ulonglong2*>(X_s + kXBytes);
     uint32_t it = 0, gcount = 0;
     int spec_prev = -1;   // token whose W1 row is in TMEM E from the speculative gather
     for (int k = kf; k <= kl; ++k) {
@@ -773,16 +775,12 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
             }
           }
           if (live) {
-            race_screen<CPP>(st, v, wb, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k, p.status);
-            // the row's best perturbed log-mass published by any CTA: each
-            // tile copies the row key into shared memory asynchronously (two
-            // slots per thread) and, after its screen, takes the copy made
-            // two tiles earlier (the second tile: the first tile's), so that
-            // the copy's latency stays hidden
+            // the row's best perturbed log-mass published by any CTA, from
+            // the latest copy of its key that has landed in shared memory (0
+            // while none has this position); nothing waits for the copies
             if (kShare && i >= 1) {
-              if (i == 1) cp_async_wait_all();
-              else cp_async_wait_one();
-              const unsigned long long gkd = gk_slot[(i == 1 ? 0 : (i & 1)) * kEpiThreads].x;
+              const unsigned long long gkd =
+                  *reinterpret_cast<volatile unsigned long long*>(&gk_rows[(k & 1) * BM + r].x);
               if (gkd) {
                 const float zg = argmax_key_value(gkd);
                 if (zg > st.zthr) {
@@ -791,13 +789,14 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                 }
               }
             }
+            race_screen<CPP>(st, v, wb, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k, p.status);
             // share this thread's progress with the other CTAs of the row
             if (kShare && st.best_v >= 0 && st.zbest > st.zpub && st.zbest >= st.zthr) {
               atomicMax(row_key, argmax_key(st.zbest, st.best_v));
               st.zpub = st.zbest;
             }
-            if (kShare) {
-              cp_async16(gk_slot + (i & 1) * kEpiThreads, row_key);
+            if (kShare && h == 0) {
+              cp_async16(gk_rows + (k & 1) * BM + r, row_key);
               cp_async_commit();
             }
           }
@@ -839,7 +838,16 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           }
         }
       }
-      if constexpr (kShare) cp_async_wait_all();   // no copy outlives its position
+      if constexpr (kShare) {
+        // this position's copies have landed; the region of the next
+        // position starts empty (its last copies, two positions back, have
+        // long landed, and every warp passes the combine barriers below
+        // before it reads the region again)
+        if (h == 0) {
+          cp_async_wait_all();
+          gk_rows[((k + 1) & 1) * BM + r] = make_ulonglong2(0ull, 0ull);
+        }
+      }
       if (MODE == kDraft && (st.run_m != st.run_m || st.run_m == INFINITY))
         record_status(p.status, DSPARK_ERR_NONFINITE);
 
