@@ -48,6 +48,10 @@ constexpr int BM = 128;             // requests per M tile (TMEM lanes)
 constexpr int BN = 64;              // vocabulary columns per tile (epilogue and U unit)
 constexpr int kGroup = 3;           // tiles per MMA: N = 64 x (up to 3)
 constexpr int kAccCols = kGroup * BN;  // 192 TMEM columns per accumulator
+// Tiles of the MMA group that starts at tile g of a position: the first group
+// is one tile, so that the epilogue starts after 16 narrow MMAs instead of 16
+// wide ones; the rest take kGroup tiles.
+__device__ __forceinline__ int group_tiles(int g) { return g == 0 ? 1 : kGroup; }
 constexpr int KR = 256;             // Markov rank handled by this kernel
 constexpr int kAtoms = KR / 64;     // 64-wide K atoms (128 bytes of bf16)
 constexpr int kWStages = 4;         // W2 atom ring (one MMA's worth)
@@ -80,6 +84,7 @@ struct __align__(8) Barriers {
   uint32_t tmem_base;
   int abort;
   int stop;   // epilogue-wide decision to leave the position loop
+  int last;   // this CTA's arrival completed the current grid barrier
 };
 static_assert(sizeof(Barriers) <= kBarBytes, "barrier block overflows its shared-memory slot");
 static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may use");
@@ -450,9 +455,14 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
   return v;
 }
 
-__device__ __forceinline__ void grid_arrive(unsigned int* counter) {
+// Returns the counter's value before this arrival.  The add also acquires, so
+// that the last CTA to arrive may read what the others published before their
+// arrivals without waiting in grid_wait.
+__device__ __forceinline__ unsigned int grid_arrive(unsigned int* counter) {
   __threadfence();
-  atomicAdd(counter, 1u);
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ bool grid_wait(unsigned int* counter, uint32_t target, volatile int* abort, int* status) {
@@ -516,6 +526,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     mbar_init(&bars->e_full, kEpiWarps);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
+    bars->last = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -536,8 +547,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     uint32_t wcount = 0, ucount = 0;
     bool ok = true;
     for (int k = kf; k <= kl && ok; ++k) {
-      for (int g = 0; g < ntl && ok; g += kGroup) {
-        // the W2 rows of up to kGroup tiles, one K atom at a time (rows past
+      for (int g = 0; g < ntl && ok; g += group_tiles(g)) {
+        // the W2 rows of an MMA group's tiles, one K atom at a time (rows past
         // the CTA's range or past V are loaded or zero-filled but not used)
         const int v0 = (t0 + g) * BN;
         for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
@@ -550,7 +561,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         }
         if (!ok) break;
         if constexpr (MODE == kResidual) continue;
-        const int nsub = min(kGroup, ntl - g);
+        const int nsub = min(group_tiles(g), ntl - g);
         for (int j = 0; j < nsub && ok; ++j) {
           const int su = ucount % kUStages;
           ok = mbar_wait(&bars->empty_u[su], ((ucount / kUStages) & 1) ^ 1, abort, p.status);
@@ -583,13 +594,13 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       for (int k = kf; k <= kl && ok; ++k) {
         ok = mbar_wait(&bars->e_full, (uint32_t)(k - kf) & 1, abort, p.status);
         tc_fence_after();
-        for (int g = 0; g < ntl && ok; g += kGroup, ++gcount) {
+        for (int g = 0; g < ntl && ok; g += group_tiles(g), ++gcount) {
           // one MMA tile: up to kGroup vocabulary tiles, N = 64 per tile
           const int acc = gcount & 1;
           ok = mbar_wait(&bars->acc_empty[acc], ((gcount >> 1) & 1) ^ 1, abort, p.status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t idesc = idesc_bf16_f32(BM, BN * min(kGroup, ntl - g));
+          const uint32_t idesc = idesc_bf16_f32(BM, BN * min(group_tiles(g), ntl - g));
           const uint32_t d_tmem = tmem + acc * kAccCols;
           for (int a = 0; a < kAtoms && ok; ++a, ++wcount) {
             const int s = wcount % kWSt;
@@ -629,6 +640,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     ulonglong2* gk_rows = reinterpret_cast<ulonglong2*>(X_s + kXBytes);
     uint32_t it = 0, gcount = 0;
     int spec_prev = -1;   // token whose W1 row is in TMEM E from the speculative gather
+    int spec_raw = 0;     // the key's token as read for that gather
+    bool spec_final = false;   // that read came after every CTA had arrived
     for (int k = kf; k <= kl; ++k) {
       bool active = r < rows_valid;
       int ks = k;                           // position of this row
@@ -645,7 +658,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       if (active) {
         int raw;
         if constexpr (MODE == kDraft)
-          raw = (k == 1) ? p.anchor[b] : argmax_key_index(__ldcg(p.keys + ((size_t)(k - 2) * p.B + b) * kKeyStride));
+          raw = (k == 1) ? p.anchor[b]
+                : spec_final ? spec_raw
+                             : argmax_key_index(__ldcg(p.keys + ((size_t)(k - 2) * p.B + b) * kKeyStride));
         else
           raw = (ks == 1) ? p.anchor[b] : p.x[(size_t)b * p.G + ks - 2];
         prev = checked_token(raw, p.V, p.status);
@@ -707,10 +722,10 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         if (ntl > 0) resid_copy<R>(U_s, off_u, p.U, p.T, t0 * BN, p.V);
       }
       for (int i = 0; i < ntl; ++i, ++it) {
-        // tiles i come kGroup to an accumulator: wait for it at the first,
-        // hand it back after reading the last
-        const int sub = i % kGroup;
-        const bool last_sub = sub == kGroup - 1 || i == ntl - 1;
+        // the tiles of an MMA group (group_tiles) share an accumulator: wait
+        // for it at the first, hand it back after reading the last
+        const int sub = i == 0 ? 0 : (i - 1) % kGroup;   // tile's place in its MMA group
+        const bool last_sub = i == 0 || sub == kGroup - 1 || i == ntl - 1;
         const int acc_i = gcount & 1;
         const int v0 = (t0 + i) * BN + part * CPP;
         const int nv = min(CPP, p.V - v0);
@@ -838,16 +853,6 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           }
         }
       }
-      if constexpr (kShare) {
-        // this position's copies have landed; the region of the next
-        // position starts empty (its last copies, two positions back, have
-        // long landed, and every warp passes the combine barriers below
-        // before it reads the region again)
-        if (h == 0) {
-          cp_async_wait_all();
-          gk_rows[((k + 1) & 1) * BM + r] = make_ulonglong2(0ull, 0ull);
-        }
-      }
       if (MODE == kDraft && (st.run_m != st.run_m || st.run_m == INFINITY))
         record_status(p.status, DSPARK_ERR_NONFINITE);
 
@@ -856,6 +861,14 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       if constexpr (MODE == kDraft) key = st.best_v >= 0 ? argmax_key(st.zbest, st.best_v) : 0ull;
       else key = rs.best_v >= 0 ? argmax_key(rs.zbest, rs.best_v) : 0ull;
       named_bar_sync(1, kEpiWarps * 32);
+      // Shared rows: every key publish of this position was issued before the
+      // barrier above, so the CTA arrives at the grid barrier now (the
+      // softmax partials below are read only after the kernel).
+      if (kShare && k < kl && warp == 2 && lane == 0) {
+        // the last CTA to arrive knows that every key is final already
+        const uint32_t target = (uint32_t)(p.nctas * (k - kf + 1));
+        bars->last = (!*abort && grid_arrive(p.gbar) + 1u == target) ? 1 : 0;
+      }
       const int slot = part * R + r;               // parts of row r at r, R + r, ...
       xm[slot] = st.run_m;
       xs[slot] = st.run_s;
@@ -871,29 +884,46 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         }
         if constexpr (MODE == kDraft) {
           p.part[((size_t)(k - 1) * p.B + b) * p.part_slices + slice] = make_float2(M, S);
-          if (K) atomicMax(&p.keys[((size_t)(k - 1) * p.B + b) * kKeyStride], K);
+          // With the row keys shared during the pass, the CTA's best is
+          // already in the key: each part published its best whenever it
+          // reached the part's threshold, and a threshold is always a value
+          // some part has published.  Only unshared rows publish here.
+          if (!kShare && K) atomicMax(&p.keys[((size_t)(k - 1) * p.B + b) * kKeyStride], K);
         } else {
           if (K) atomicMax(&p.resid_key[(size_t)b * kKeyStride], K);
         }
       }
       (void)ok;
       if (k < kl) {
-        // every CTA's position-k keys are in place before anyone reads x_k:
-        // one thread arrives at the grid barrier once this CTA's keys are out
-        named_bar_sync(1, kEpiWarps * 32);
-        if (warp == 2 && lane == 0 && !*abort) grid_arrive(p.gbar);
+        if constexpr (!kShare) {
+          // every CTA's position-k keys are in place before anyone reads x_k:
+          // one thread arrives once this CTA's keys are out
+          named_bar_sync(1, kEpiWarps * 32);
+          if (warp == 2 && lane == 0 && !*abort) grid_arrive(p.gbar);
+        }
         // Speculative gather while the barrier resolves: this CTA's MMAs of
         // position k are complete (its last accumulator was read), so TMEM E
         // is free; load W1[x_k] for the row keys as they stand now.  After the
         // barrier the final keys are compared and only changed rows reload.
         if constexpr (MODE == kDraft) {
           int sp = 0;
+          spec_final = kShare && bars->last;
           if (active) {
-            const int t = argmax_key_index(__ldcg(p.keys + ((size_t)(k - 1) * p.B + b) * kKeyStride));
-            sp = (t >= 0 && t < p.V) ? t : 0;
+            spec_raw = argmax_key_index(__ldcg(p.keys + ((size_t)(k - 1) * p.B + b) * kKeyStride));
+            sp = (spec_raw >= 0 && spec_raw < p.V) ? spec_raw : 0;
           }
           gather_e(p.W1, sp, active, h, tmem + ((uint32_t)(q * 32) << 16) + kTmemE + h * 32);
           spec_prev = active ? sp : 0;
+        }
+        if constexpr (kShare) {
+          // this position's key copies have landed; the next position's
+          // region starts empty (its copies, two positions back, have long
+          // landed, and every warp passes the barrier below before it reads
+          // the region again)
+          if (h == 0) {
+            cp_async_wait_all();
+            gk_rows[((k + 1) & 1) * BM + r] = make_ulonglong2(0ull, 0ull);
+          }
         }
         // one thread takes the decision to go on, all epilogue warps read it
         // after the same barrier, so they all leave the loop together
@@ -906,6 +936,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         if (bars->stop) break;
       }
     }
+    cp_async_wait_all();   // no copy outlives the CTA's shared memory
   }
 
   tc_fence_before();
