@@ -690,9 +690,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       if (lane == 0) mbar_arrive(&bars->e_full);
 
       RowRace st{-INFINITY, 0.f, -INFINITY, -1, -INFINITY, -INFINITY, INFINITY};
-      // rows shared by many threads (small batches replicated across the tile)
-      // would turn the exchange into a hot spot: only full 128-row tiles use it
-      constexpr bool kShare = (MODE == kDraft) && (R == BM);
+      // the draft shares every row's best across CTAs (residual: only full
+      // 128-row tiles)
+      constexpr bool kShare = (MODE == kDraft);
       unsigned long long* row_key = (kShare && active) ? p.keys + ((size_t)(k - 1) * p.B + b) * kKeyStride : nullptr;
       ResRace rs{-INFINITY, -1, -INFINITY, -INFINITY, INFINITY};
       constexpr bool kShareRes = (MODE == kResidual) && (R == BM);
@@ -705,7 +705,6 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         }
       }
       bool ok = true;
-      unsigned long long gk = 0ull;   // residual: row key as last read (kShareRes)
       // residual mode: the U and T row segments of each tile are copied into
       // shared memory one tile ahead by all epilogue threads (resid_copy)
       long long* off_u = reinterpret_cast<long long*>(X_s);   // element offset of row rr's U row, or -1
@@ -732,8 +731,11 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         if constexpr (MODE == kResidual) {
           // this tile's rows have landed (own copies, then everyone's); the
           // barrier also frees the other stage for the next tile's copies.
-          // Every epilogue thread passes here each tile, failed or not.
-          cp_async_wait_all();
+          // Every epilogue thread passes here each tile, failed or not.  The
+          // row-key copy of the previous tile (the newest group of the first
+          // warp of each quarter) may stay in flight.
+          if (kShareRes && h == 0 && i > 0) cp_async_wait_one();
+          else cp_async_wait_all();
           named_bar_sync(1, kEpiWarps * 32);
           if (i + 1 < ntl) resid_copy<R>(U_s + ((i + 1) & 1) * kResStageBytes, off_u, p.U, p.T, (t0 + i + 1) * BN, p.V);
         }
@@ -810,7 +812,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
               atomicMax(row_key, argmax_key(st.zbest, st.best_v));
               st.zpub = st.zbest;
             }
-            if (kShare && h == 0) {
+            if (kShare && h == 0 && rep == 0) {
               cp_async16(gk_rows + (k & 1) * BM + r, row_key);
               cp_async_commit();
             }
@@ -840,16 +842,23 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                 uu[c + e] = pt - pd;
               }
             }
-            // the row's best from other CTAs, read at the end of the previous
-            // tile: waited for at the second tile, taken after the screen later
-            if (kShareRes && gk && i == 1) resid_raise(rs, argmax_key_value(gk));
+            // the row's best from other CTAs: the latest copy of its key that
+            // has landed in shared memory (nothing waits for it)
+            if (kShareRes && i >= 1) {
+              const unsigned long long gkr = *reinterpret_cast<volatile unsigned long long*>(&gk_rows[r].x);
+              if (gkr) resid_raise(rs, argmax_key_value(gkr));
+            }
             resid_tile<CPP>(rs, uu, nv, v0, urow, j0, sw, p.key, (uint32_t)b, (uint32_t)ks);
-            if (kShareRes && gk && i > 1) resid_raise(rs, argmax_key_value(gk));
             if (kShareRes && rs.best_v >= 0 && rs.zbest > rs.zpub && rs.zbest >= rs.zthr) {
               atomicMax(res_key, argmax_key(rs.zbest, rs.best_v));
               rs.zpub = rs.zbest;
             }
-            if (kShareRes) gk = __ldcg(res_key);
+          }
+          if (kShareRes && h == 0) {
+            // one copy group per tile (empty when the row is idle), so that
+            // the wait above always leaves exactly this copy in flight
+            if (ok && active) cp_async16(gk_rows + r, res_key);
+            cp_async_commit();
           }
         }
       }
@@ -920,7 +929,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           // region starts empty (its copies, two positions back, have long
           // landed, and every warp passes the barrier below before it reads
           // the region again)
-          if (h == 0) {
+          if (h == 0 && rep == 0) {
             cp_async_wait_all();
             gk_rows[((k + 1) & 1) * BM + r] = make_ulonglong2(0ull, 0ull);
           }

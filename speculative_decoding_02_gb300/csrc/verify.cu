@@ -182,69 +182,89 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, 
     const uint32_t pos = (uint32_t)(jrow + 1);
     const float* Trow = T + (size_t)rowid * V;
     const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
-    float m = -INFINITY, zbest = -INFINITY, bound = INFINITY;
+    // zbest: this thread's best perturbed log-mass (bestv its token); zthr:
+    // the best known in the warp, a value some lane has reached, which the
+    // screen compares against (bound = exp(m - zthr), 2^-10 over)
+    float m = -INFINITY, zbest = -INFINITY, zthr = -INFINITY, bound = INFINITY;
     int bestv = -1;
 #pragma unroll 1
     for (int ch = 0; ch < kChunks; ++ch) {
       const int vc = v0 + 16 * (ch * kRowThreads + tid);
-      if (vc >= v1) break;
-      float tv[16];
+      if (vc < v1) {
+        float tv[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 t4 = (vc + 4 * i < v1) ? __ldcs(reinterpret_cast<const float4*>(Trow + vc + 4 * i))
-                                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        tv[4 * i] = t4.x; tv[4 * i + 1] = t4.y; tv[4 * i + 2] = t4.z; tv[4 * i + 3] = t4.w;
-      }
-      float cm = tv[0];
-#pragma unroll
-      for (int c = 1; c < 16; ++c) cm = fmaxf(cm, tv[c]);
-      bad |= !(cm < INFINITY);
-      if (cm > m) {
-        m = cm;
-        if (zbest > -INFINITY) bound = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f);
-      }
-      if (m == -INFINITY) continue;
-      const float mb = m * kLog2eF;
-      float e[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) e[c] = exp2_fast(fmaf(tv[c], kLog2eF, -mb));
-      float W[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) W[q] = ((e[4 * q] + e[4 * q + 1]) + e[4 * q + 2]) + e[4 * q + 3];
-      const uint4 ra = rng_call(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)vc >> 4);
-      const uint32_t wq[4] = {ra.x, ra.y, ra.z, ra.w};
-      if (zbest == -INFINITY) {
-        // open the race with the block most likely to win
-        float bw = 0.f, bd = 1.f;
-        int bq = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float d = 8454144.0f - block_hf_v(wq[q]);
-          if (W[q] * bd > bw * d) { bw = W[q]; bd = d; bq = q; }
+        for (int i = 0; i < 4; ++i) {
+          const float4 t4 = (vc + 4 * i < v1) ? __ldcs(reinterpret_cast<const float4*>(Trow + vc + 4 * i))
+                                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          tv[4 * i] = t4.x; tv[4 * i + 1] = t4.y; tv[4 * i + 2] = t4.z; tv[4 * i + 3] = t4.w;
         }
+        float cm = tv[0];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (q == bq) {
-            zbest = m + logf(W[q]) + gumbel_from_bits(wq[q] >> 9);
-            bestv = block_pick(key, kStreamBonus, (uint32_t)b, pos, ((uint32_t)vc >> 2) + q, e[4 * q],
-                               e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
-            W[q] = 0.f;
+        for (int c = 1; c < 16; ++c) cm = fmaxf(cm, tv[c]);
+        bad |= !(cm < INFINITY);
+        if (cm > m) {
+          m = cm;
+          if (zthr > -INFINITY) bound = exp2_fast((m - zthr) * kLog2eF) * (1.0f + 0x1p-10f);
+        }
+        if (m > -INFINITY) {
+          const float mb = m * kLog2eF;
+          float e[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) e[c] = exp2_fast(fmaf(tv[c], kLog2eF, -mb));
+          float W[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) W[q] = ((e[4 * q] + e[4 * q + 1]) + e[4 * q + 2]) + e[4 * q + 3];
+          const uint4 ra = rng_call(key, kStreamBonus, (uint32_t)b, pos, (uint32_t)vc >> 4);
+          const uint32_t wq[4] = {ra.x, ra.y, ra.z, ra.w};
+          if (zbest == -INFINITY) {
+            // open this thread's race with its block most likely to win
+            float bw = 0.f, bd = 1.f;
+            int bq = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float d = 8454144.0f - block_hf_v(wq[q]);
+              if (W[q] * bd > bw * d) { bw = W[q]; bd = d; bq = q; }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (q == bq) {
+                zbest = m + logf(W[q]) + gumbel_from_bits(wq[q] >> 9);
+                bestv = block_pick(key, kStreamBonus, (uint32_t)b, pos, ((uint32_t)vc >> 2) + q, e[4 * q],
+                                   e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
+                W[q] = 0.f;
+              }
+            }
+            if (zbest > zthr) {
+              zthr = zbest;
+              bound = exp2_fast((m - zthr) * kLog2eF) * (1.0f + 0x1p-10f);
+            }
+          }
+          const float b16 = bound * 65536.0f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (W[q] > 0.f && fmaf(W[q], b16, block_hf_v(wq[q])) > kScreenThrV) {
+              const float z = m + logf(W[q]) + gumbel_from_bits(wq[q] >> 9);
+              if (z > zbest) {
+                zbest = z;
+                bestv = block_pick(key, kStreamBonus, (uint32_t)b, pos, ((uint32_t)vc >> 2) + q, e[4 * q],
+                                   e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
+                if (z > zthr) {
+                  zthr = z;
+                  bound = exp2_fast((m - zthr) * kLog2eF) * (1.0f + 0x1p-10f);
+                }
+              }
+            }
           }
         }
-        bound = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f);
       }
-      const float b16 = bound * 65536.0f;
+      // the lanes pool their thresholds after every chunk, so that a block
+      // is screened against the warp's best, not only the thread's own
+      float zw = zthr;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (W[q] > 0.f && fmaf(W[q], b16, block_hf_v(wq[q])) > kScreenThrV) {
-          const float z = m + logf(W[q]) + gumbel_from_bits(wq[q] >> 9);
-          if (z > zbest) {
-            zbest = z;
-            bestv = block_pick(key, kStreamBonus, (uint32_t)b, pos, ((uint32_t)vc >> 2) + q, e[4 * q],
-                               e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
-            bound = exp2_fast((m - zbest) * kLog2eF) * (1.0f + 0x1p-10f);
-          }
-        }
+      for (int off = 16; off > 0; off >>= 1) zw = fmaxf(zw, __shfl_xor_sync(0xffffffffu, zw, off));
+      if (zw > zthr) {
+        zthr = zw;
+        bound = m > -INFINITY ? exp2_fast((m - zthr) * kLog2eF) * (1.0f + 0x1p-10f) : INFINITY;
       }
     }
     unsigned long long best = bestv >= 0 ? argmax_key(zbest, bestv) : 0ull;
