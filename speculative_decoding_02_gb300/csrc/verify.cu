@@ -167,6 +167,14 @@ constexpr float kScreenThrV = 8454142.0f;   // 2^23 + 65534 (see the draft race)
 // Philox call): the block weights exp(T - m) against the running maximum m,
 // a screen of each block on its 16 high random bits, exact values for the
 // rare candidates and the token inside a block that takes the lead.
+// Entries vc .. vc+15 of a row (-inf past v1), four 16-byte streaming loads.
+__device__ __forceinline__ void load_chunk16(const float* __restrict__ row, int vc, int v1, float4 (&t)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    t[i] = (vc + 4 * i < v1) ? __ldcs(reinterpret_cast<const float4*>(row + vc + 4 * i))
+                             : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+}
+
 __global__ void __launch_bounds__(kRowThreads)
 verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, int B, int G, int V, int nsegs,
                   RngKey key, unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
@@ -188,16 +196,18 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, 
     float m = -INFINITY, zbest = -INFINITY, zthr = -INFINITY, bound = INFINITY;
     int bestv = -1;
 #pragma unroll 1
+    // a thread's 16 entries of chunk ch+1 are loaded while chunk ch is raced
+    float4 nx[4];
+    load_chunk16(Trow, v0 + 16 * tid, v1, nx);
     for (int ch = 0; ch < kChunks; ++ch) {
       const int vc = v0 + 16 * (ch * kRowThreads + tid);
-      if (vc < v1) {
-        float tv[16];
+      float tv[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 t4 = (vc + 4 * i < v1) ? __ldcs(reinterpret_cast<const float4*>(Trow + vc + 4 * i))
-                                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-          tv[4 * i] = t4.x; tv[4 * i + 1] = t4.y; tv[4 * i + 2] = t4.z; tv[4 * i + 3] = t4.w;
-        }
+      for (int i = 0; i < 4; ++i) {
+        tv[4 * i] = nx[i].x; tv[4 * i + 1] = nx[i].y; tv[4 * i + 2] = nx[i].z; tv[4 * i + 3] = nx[i].w;
+      }
+      if (ch + 1 < kChunks) load_chunk16(Trow, vc + 16 * kRowThreads, v1, nx);
+      if (vc < v1) {
         float cm = tv[0];
 #pragma unroll
         for (int c = 1; c < 16; ++c) cm = fmaxf(cm, tv[c]);
