@@ -13,17 +13,22 @@
 //               load while the grid barrier resolves.
 //   warp 1      TMEM allocation (512 columns) and the single-thread MMA
 //               issuer: bias[128 x 64j] = E[128 x 256] * W2_rows^T, j <= 3
-//               tiles per tcgen05.mma (kind::f16, fp32 accumulate), A = E in
-//               TMEM columns 384-511, two accumulators of 192 columns.
+//               tiles per tcgen05.mma (kind::f16, fp32 accumulate; the first
+//               group of a position is one tile), A = E in TMEM columns
+//               384-511, two accumulators of 192 columns.
 //   warps 2-17  epilogue, four per TMEM lane quarter (thread = request row,
 //               16 columns per tile): tcgen05.ld of the accumulator, + U, the
 //               online softmax and the block race of the sampler (blocks of
 //               4 tokens, screened on 16 random bits, exact only for the rare
-//               candidates).  At a position's end they merge their parts,
-//               publish one (m, s) partial per row and the row's argmax key
-//               (atomicMax), arrive at the grid barrier, gather
-//               E = W1[x_k] speculatively and, after the barrier, reload
-//               the rows whose final token differs.
+//               candidates).  A row's parts pool their first seeds in shared
+//               memory; every part publishes its best to the row's argmax key
+//               (atomicMax) whenever it reaches the row's threshold, and each
+//               tile copies the key back asynchronously (one copy per row,
+//               read without waiting) to raise the threshold from the other
+//               CTAs' progress.  At a position's end the CTA arrives at the
+//               grid barrier, merges its parts into one (m, s) partial per
+//               row, gathers E = W1[x_k] speculatively and, after the
+//               barrier, reloads the rows whose final token differs.
 //
 // Residual (MODE kResidual): the same pipeline for one position per request
 // (the rejected k*), with U and T row segments staged by the epilogue's own
