@@ -81,13 +81,14 @@ def draft_bytes_per_launch(w):
 
 def kernels_per_round(w):
     """Launches of this library's kernels in one round (cudaMemsetAsync not
-    counted): draft = the persistent tensor-core kernel and its finalize (bf16,
-    r = 256, V >= 192; else a CUDA-core step and finalize per position);
+    counted): draft = the persistent tensor-core kernel, which also finishes
+    x, p and lse after a last grid barrier (bf16, r = 256, V >= 192; else a
+    CUDA-core step and finalize per position);
     confidence; schedule; verify = prep, row statistics, bonus race, decide,
     residual (the draft kernel in residual mode, or its CUDA-core form),
     residual finalize."""
     tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
-    return (2 if tc else 2 * w.gamma) + 1 + 1 + 6
+    return (1 if tc else 2 * w.gamma) + 1 + 1 + 6
 
 
 # Source files of the draft kernel: a committed ncu figure counts only while
@@ -355,7 +356,7 @@ def run_gpu(args):
                        "round_GB": rbytes / 1e9,
                        "round_hbm_frac": rbytes / (ms / args.steps / 1e3) / 1e9 / hbm,
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"kernel": "markov draft (dspark_markov_draft: draft_step_tc + draft_finalize_tc)",
+            "roofline": {"kernel": "markov draft (dspark_markov_draft: draft_step_tc with its fused finalize)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": draft_traffic(w), "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},

@@ -99,7 +99,12 @@ enum Mode { kDraft = 0, kResidual = 1 };
 struct StepParams {
   const float* U;
   const __nv_bfloat16* W1;
+  const __nv_bfloat16* W2;              // for the fused finalize
   const int32_t* anchor;
+  // draft outputs written by the fused finalize (null: a separate kernel does it)
+  int32_t* x_out;
+  float* p_out;
+  float* lse_out;
   // residual mode: rejected position k* of each request (0 = none), the draft
   // tokens, the draft lse of every position, the target lse of row k*-1
   const float* T;
@@ -487,6 +492,45 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* counter, uint32_t tar
                                              int* status) {
   grid_arrive(counter);
   return grid_wait(counter, target, abort, status);
+}
+
+// The draft outputs of one (request, position), by one warp: merge the slice
+// partials into lse_k, decode x_k from its argmax key and recompute the fused
+// logit of x_k for p_k(x_k).
+__device__ __forceinline__ void finalize_item(int item, int lane, const float* __restrict__ U,
+                                              const __nv_bfloat16* __restrict__ W1,
+                                              const __nv_bfloat16* __restrict__ W2, const int32_t* __restrict__ anchor,
+                                              const unsigned long long* __restrict__ keys,
+                                              const float2* __restrict__ part, int B, int G, int V, int nslices,
+                                              int part_slices, int32_t* __restrict__ x_out, float* __restrict__ p_out,
+                                              float* __restrict__ lse_out, int* __restrict__ status) {
+  const int b = item / G, k = item - (item / G) * G + 1;
+  const float2* pp = part + (size_t)(k - 1) * part_slices * B;
+  float m = -INFINITY, s = 0.f;
+  for (int i = lane; i < nslices; i += 32) {
+    const float2 pr = __ldcg(pp + (size_t)b * part_slices + i);   // written by other CTAs of this launch
+    softmax_merge(m, s, pr.x, pr.y);
+  }
+  warp_softmax_reduce(m, s, 0xffffffffu, 32);
+  const float lse = m + logf(s);
+  const unsigned long long kk = __ldcg(keys + ((size_t)(k - 1) * B + b) * kKeyStride);
+  int x = kk ? argmax_key_index(kk) : -1;
+  if (x < 0 || x >= V) {
+    if (lane == 0) record_status(status, DSPARK_ERR_NONFINITE);
+    x = 0;
+  }
+  int prev = (k == 1) ? anchor[b] : argmax_key_index(__ldcg(keys + ((size_t)(k - 2) * B + b) * kKeyStride));
+  prev = checked_token(prev, V, status);
+  float dot = 0.f;
+  for (int i = lane; i < KR; i += 32)
+    dot = fmaf(__bfloat162float(W1[(size_t)prev * KR + i]), __bfloat162float(W2[(size_t)x * KR + i]), dot);
+  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  if (lane == 0) {
+    const size_t o = (size_t)b * G + (k - 1);
+    x_out[o] = x;
+    p_out[o] = expf(U[o * (size_t)V + x] + dot - lse);
+    lse_out[o] = lse;
+  }
 }
 
 // MODE kDraft: draft positions k_first..k_last for every request (U rows by
@@ -951,6 +995,28 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       }
     }
     cp_async_wait_all();   // no copy outlives the CTA's shared memory
+    if constexpr (MODE == kDraft) {
+      if (p.x_out != nullptr) {
+        // Fused finalize (persistent launch over every position): once every
+        // CTA's partials of the last position are out, the epilogue warps of
+        // the grid finish the (request, position) items, one warp each.
+        named_bar_sync(1, kEpiWarps * 32);
+        if (warp == 2 && lane == 0) {
+          bool go = !*abort;
+          if (go) {
+            grid_arrive(p.gbar);
+            go = grid_wait(p.gbar, (uint32_t)(p.nctas * (kl - kf + 1)), abort, p.status);
+          }
+          bars->stop = go ? 0 : 1;
+        }
+        named_bar_sync(1, kEpiWarps * 32);
+        if (!bars->stop) {
+          for (int item = blockIdx.x * kEpiWarps + (warp - 2); item < p.B * p.G; item += p.nctas * kEpiWarps)
+            finalize_item(item, lane, p.U, p.W1, p.W2, p.anchor, p.keys, p.part, p.B, p.G, p.V, p.ctas_per_mtile,
+                          p.part_slices, p.x_out, p.p_out, p.lse_out, p.status);
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -967,35 +1033,9 @@ __global__ void draft_finalize_tc(const float* __restrict__ U, const __nv_bfloat
                                   int B, int G, int V, int nslices, int part_slices, int32_t* __restrict__ x_out,
                                   float* __restrict__ p_out, float* __restrict__ lse_out, int* __restrict__ status) {
   const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   if (item >= B * G) return;
-  const int b = item / G, k = item - (item / G) * G + 1;
-  const float2* pp = part + (size_t)(k - 1) * part_slices * B;
-  float m = -INFINITY, s = 0.f;
-  for (int i = lane; i < nslices; i += 32) {
-    const float2 pr = pp[(size_t)b * part_slices + i];
-    softmax_merge(m, s, pr.x, pr.y);
-  }
-  warp_softmax_reduce(m, s, 0xffffffffu, 32);
-  const float lse = m + logf(s);
-  const unsigned long long kk = keys[((size_t)(k - 1) * B + b) * kKeyStride];
-  int x = kk ? argmax_key_index(kk) : -1;
-  if (x < 0 || x >= V) {
-    if (lane == 0) record_status(status, DSPARK_ERR_NONFINITE);
-    x = 0;
-  }
-  int prev = (k == 1) ? anchor[b] : argmax_key_index(keys[((size_t)(k - 2) * B + b) * kKeyStride]);
-  prev = checked_token(prev, V, status);
-  float dot = 0.f;
-  for (int i = lane; i < KR; i += 32)
-    dot = fmaf(__bfloat162float(W1[(size_t)prev * KR + i]), __bfloat162float(W2[(size_t)x * KR + i]), dot);
-  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-  if (lane == 0) {
-    const size_t o = (size_t)b * G + (k - 1);
-    x_out[o] = x;
-    p_out[o] = expf(U[o * (size_t)V + x] + dot - lse);
-    lse_out[o] = lse;
-  }
+  finalize_item(item, threadIdx.x & 31, U, W1, W2, anchor, keys, part, B, G, V, nslices, part_slices, x_out, p_out,
+                lse_out, status);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1115,6 +1155,7 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   StepParams sp{};
   sp.U = a.U;
   sp.W1 = static_cast<const __nv_bfloat16*>(a.W1);
+  sp.W2 = static_cast<const __nv_bfloat16*>(a.W2);
   sp.anchor = a.anchor;
   sp.keys = keys;
   sp.part = part;
@@ -1145,16 +1186,20 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // the persistent launch also finishes the outputs (x, p, lse)
+    sp.x_out = a.x_out;
+    sp.p_out = a.p_out;
+    sp.lse_out = a.lse_out;
     if ((e = cudaLaunchKernelEx(&cfg, kern, map, umap, sp)) != cudaSuccess) return e;
   } else {
     for (int k = 1; k <= a.gamma; ++k) {
       sp.k_first = sp.k_last = k;
       kern<<<nctas, kThreads, kSmemBytes, stream>>>(map, umap, sp);
     }
+    draft_finalize_tc<<<div_up(a.B * a.gamma * 32, 256), 256, 0, stream>>>(
+        a.U, static_cast<const __nv_bfloat16*>(a.W1), static_cast<const __nv_bfloat16*>(a.W2), a.anchor, keys,
+        part, a.B, a.gamma, a.V, per, part_slices, a.x_out, a.p_out, a.lse_out, status);
   }
-  draft_finalize_tc<<<div_up(a.B * a.gamma * 32, 256), 256, 0, stream>>>(
-      a.U, static_cast<const __nv_bfloat16*>(a.W1), static_cast<const __nv_bfloat16*>(a.W2), a.anchor, keys,
-      part, a.B, a.gamma, a.V, per, part_slices, a.x_out, a.p_out, a.lse_out, status);
   return cudaGetLastError();
 }
 
