@@ -55,8 +55,19 @@ __global__ void confidence_kernel(const void* __restrict__ h, const void* __rest
     // 8 elements per lane per step: 16-byte loads of bf16 (two 16-byte loads
     // of f32), the weight as two float4 (16-byte aligned bases, H and r
     // multiples of 8 keep every row aligned)
-    for (int i = 8 * lane; i < H; i += 256) z = dot8<HDT>(h, hrow + i, w + i, z);
-    for (int i = 8 * lane; i < r; i += 256) z = dot8<WDT>(W1, (size_t)prev * r + i, w + H + i, z);
+    // four independent partial sums, so that four loads per lane are in
+    // flight at once
+    float z1 = 0.f, z2 = 0.f, z3 = 0.f;
+    int i = 8 * lane;
+    for (; i + 768 < H; i += 1024) {
+      z = dot8<HDT>(h, hrow + i, w + i, z);
+      z1 = dot8<HDT>(h, hrow + i + 256, w + i + 256, z1);
+      z2 = dot8<HDT>(h, hrow + i + 512, w + i + 512, z2);
+      z3 = dot8<HDT>(h, hrow + i + 768, w + i + 768, z3);
+    }
+    for (; i < H; i += 256) z = dot8<HDT>(h, hrow + i, w + i, z);
+    for (int j = 8 * lane; j < r; j += 256) z1 = dot8<WDT>(W1, (size_t)prev * r + j, w + H + j, z1);
+    z = (z + z1) + (z2 + z3);
   } else {
     for (int i = lane; i < H; i += 32) z = fmaf(w[i], load_weight<HDT>(h, hrow + i), z);
     for (int i = lane; i < r; i += 32) z = fmaf(w[H + i], load_weight<WDT>(W1, (size_t)prev * r + i), z);
