@@ -739,12 +739,11 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       if (lane == 0) mbar_arrive(&bars->e_full);
 
       RowRace st{-INFINITY, 0.f, -INFINITY, -1, -INFINITY, -INFINITY, INFINITY};
-      // the draft shares every row's best across CTAs (residual: only full
-      // 128-row tiles)
+      // every row's best is shared across CTAs (draft and residual)
       constexpr bool kShare = (MODE == kDraft);
       unsigned long long* row_key = (kShare && active) ? p.keys + ((size_t)(k - 1) * p.B + b) * kKeyStride : nullptr;
       ResRace rs{-INFINITY, -1, -INFINITY, -INFINITY, INFINITY};
-      constexpr bool kShareRes = (MODE == kResidual) && (R == BM);
+      constexpr bool kShareRes = (MODE == kResidual);
       unsigned long long* res_key = (kShareRes && active) ? p.resid_key + (size_t)b * kKeyStride : nullptr;
       float ld2 = 0.f, lt2 = 0.f;
       if constexpr (MODE == kResidual) {
@@ -904,9 +903,10 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
             }
           }
           if (kShareRes && h == 0) {
-            // one copy group per tile (empty when the row is idle), so that
-            // the wait above always leaves exactly this copy in flight
-            if (ok && active) cp_async16(gk_rows + r, res_key);
+            // one copy group per tile (empty when the row is idle or held by
+            // another replica), so that the wait above always leaves exactly
+            // this copy in flight
+            if (ok && active && rep == 0) cp_async16(gk_rows + r, res_key);
             cp_async_commit();
           }
         }
