@@ -919,9 +919,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       if constexpr (MODE == kDraft) key = st.best_v >= 0 ? argmax_key(st.zbest, st.best_v) : 0ull;
       else key = rs.best_v >= 0 ? argmax_key(rs.zbest, rs.best_v) : 0ull;
       named_bar_sync(1, kEpiWarps * 32);
-      // Shared rows: every key publish of this position was issued before the
-      // barrier above, so the CTA arrives at the grid barrier now (the
-      // softmax partials below are read only after the kernel).
+      // Every key publish of this position was issued before the barrier
+      // above, so the CTA arrives at the grid barrier now (the softmax
+      // partials below are read only after the last barrier).
       if (kShare && k < kl && warp == 2 && lane == 0) {
         // the last CTA to arrive knows that every key is final already
         const uint32_t target = (uint32_t)(p.nctas * (k - kf + 1));
@@ -941,24 +941,17 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           K = xk[j * R + r] > K ? xk[j * R + r] : K;
         }
         if constexpr (MODE == kDraft) {
+          // No key update here: the CTA's best is already in the row key.
+          // Each part published its best whenever it reached the part's
+          // threshold, and a threshold is always a value some part has
+          // published.
           p.part[((size_t)(k - 1) * p.B + b) * p.part_slices + slice] = make_float2(M, S);
-          // With the row keys shared during the pass, the CTA's best is
-          // already in the key: each part published its best whenever it
-          // reached the part's threshold, and a threshold is always a value
-          // some part has published.  Only unshared rows publish here.
-          if (!kShare && K) atomicMax(&p.keys[((size_t)(k - 1) * p.B + b) * kKeyStride], K);
         } else {
           if (K) atomicMax(&p.resid_key[(size_t)b * kKeyStride], K);
         }
       }
       (void)ok;
       if (k < kl) {
-        if constexpr (!kShare) {
-          // every CTA's position-k keys are in place before anyone reads x_k:
-          // one thread arrives once this CTA's keys are out
-          named_bar_sync(1, kEpiWarps * 32);
-          if (warp == 2 && lane == 0 && !*abort) grid_arrive(p.gbar);
-        }
         // Speculative gather while the barrier resolves: this CTA's MMAs of
         // position k are complete (its last accumulator was read), so TMEM E
         // is free; load W1[x_k] for the row keys as they stand now.  After the
