@@ -465,11 +465,12 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
   return v;
 }
 
-// Returns the counter's value before this arrival.  The add also acquires, so
-// that the last CTA to arrive may read what the others published before their
-// arrivals without waiting in grid_wait.
+// Returns the counter's value before this arrival.  The add is an
+// acquire-release atomic at GPU scope: its release covers this thread's
+// writes and, through the CTA barrier that precedes every arrival, the other
+// threads' writes and key atomics; its acquire lets the last CTA to arrive
+// read what the others published without waiting in grid_wait.
 __device__ __forceinline__ unsigned int grid_arrive(unsigned int* counter) {
-  __threadfence();
   unsigned int old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
   return old;
