@@ -329,6 +329,36 @@ def run_gpu(args):
     dbytes = draft_bytes_per_launch(w)
     achieved = dbytes / (draft_ms / 1e3) / 1e9
 
+    # the acceptance labels of one round's verified positions (a widening of
+    # the path: sum_v min(p_d, p_t) per position), timed on their own
+    label = None
+    if rank == 0 and w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192:
+        x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 7, ws=ws)
+        c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
+        ell, _, _ = ds.schedule(c, inp["sps"], w.mode, 7, khist, ws)
+
+        def lab():
+            return ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, lse, ell, ws=ws)
+
+        for _ in range(2):
+            lab()
+        torch.cuda.synchronize()
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        for _ in range(3):
+            lab()
+        l1.record(stream)
+        torch.cuda.synchronize()
+        if ds.read_status(ws) != ds.OK:
+            raise RuntimeError("device status after the acceptance labels")
+        lms = l0.elapsed_time(l1) / 3
+        npos = int(ell.sum())
+        lbytes = 8 * w.V * npos + (2 if w.wdtype == torch.bfloat16 else 4) * w.r * w.V
+        label = {"ms": lms, "positions": npos, "algorithmic_GB": lbytes / 1e9,
+                 "achieved_GBs": lbytes / (lms / 1e3) / 1e9, "frac": lbytes / (lms / 1e3) / 1e9 / hbm,
+                 "note": "U and T rows of the verified positions once, W2 once; the implementation reads the "
+                         "T rows twice (their softmax statistics first)"}
+
     # end to end through host buffers: per-round inputs copied in, results out
     e2e = None
     if rank == 0 and not args.no_e2e:
@@ -361,6 +391,7 @@ def run_gpu(args):
                          "frac": achieved / hbm, "traffic": draft_traffic(w), "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
             "clocks": clk.summary(),
+            "acceptance_label": label,
             "e2e": e2e,
             "gpu_launches": args.steps * kernels_per_round(w),
             "cpu_baseline": cpu,

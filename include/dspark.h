@@ -149,6 +149,24 @@ int dspark_verify(const float* T, const float* U, const void* W1, const void* W2
                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Acceptance labels of the verified positions (the study report's label for
+ * training the confidence head: the probability that rejection sampling
+ * accepts position k, Eq.8, the mass p_d and p_t share).  For request b and
+ * k = 1..ell[b]:  label[b, k-1] = sum_v min(p_d(v), p_t(v)), p_d =
+ * softmax(U[b,k-1,:] + bias(x_{k-1})) from lse_d, p_t = softmax(T[b, k-1, :]);
+ * positions k > ell[b] get 0.  Arguments as for dspark_verify (the same
+ * workspace layout: it overwrites the target-row statistics there).
+ * Tensor-core path only (bf16 W1/W2, r = 256, V >= 192); other weights
+ * return DSPARK_ERR_UNSUPPORTED.
+ * Out: label_out [B, gamma] f32, caller-owned.
+ */
+int dspark_acceptance_label(const float* T, const float* U, const void* W1, const void* W2,
+                            int wdtype, const int32_t* anchor, const int32_t* x,
+                            const float* lse_d, const int32_t* ell, int B, int gamma,
+                            int V, int r, float* label_out, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * One whole round: draft, confidence, schedule, verify, enqueued in that order
  * on one stream with no host synchronisation.  Arguments as above.
  */

@@ -52,6 +52,9 @@ def _load():
     L.dspark_verify.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp,
                                 vp, sz, vp]
     L.dspark_verify.restype = i32
+    L.dspark_acceptance_label.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp,
+                                          ctypes.c_size_t, vp]
+    L.dspark_acceptance_label.restype = i32
     L.dspark_round.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
                                vp, u64, u64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_round.restype = i32
@@ -203,6 +206,29 @@ def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None):
                            _ptr(lse_d), _ptr(ell), B, G, V, r, seed, rnd, _ptr(n), _ptr(tok), _ptr(ws), ws.numel(),
                            _stream(dev)), "verify")
     return n, tok
+
+
+def acceptance_label(T, U, W1, W2, anchor, x, lse_d, ell, ws=None):
+    """label [B, gamma] f32: sum_v min(p_d, p_t) for every verified position
+    k <= ell[b] (0 elsewhere).  Tensor-core path only (bf16, r = 256)."""
+    L = _load()
+    _need(T, "T", torch.float32)
+    dev = T.device
+    _need(U, "U", torch.float32, dev)
+    B, G, V = U.shape
+    if tuple(T.shape) != (B, G + 1, V):
+        raise ValueError(f"T must be [B, gamma+1, V] = {(B, G + 1, V)}, got {tuple(T.shape)}")
+    _need(W1, "W1", device=dev); _need(W2, "W2", W1.dtype, dev)
+    for t, n in [(anchor, "anchor"), (x, "x"), (ell, "ell")]:
+        _need(t, n, torch.int32, dev)
+    _need(lse_d, "lse_d", torch.float32, dev)
+    r = W1.shape[1]
+    label = torch.empty(B, G, dtype=torch.float32, device=dev)
+    ws = workspace(B, G, V, dev) if ws is None else ws
+    _check(L.dspark_acceptance_label(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x),
+                                     _ptr(lse_d), _ptr(ell), B, G, V, r, _ptr(label), _ptr(ws), ws.numel(),
+                                     _stream(dev)), "acceptance_label")
+    return label
 
 
 class RoundOutputs:

@@ -136,6 +136,25 @@ int dspark_verify(const float* T, const float* U, const void* W1, const void* W2
   return cuda_status(launch_verify(a, (cudaStream_t)stream));
 }
 
+int dspark_acceptance_label(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
+                            const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* ell, int B,
+                            int gamma, int V, int r, float* label_out, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  DSPARK_TRY(check_shapes(B, gamma, V, r));
+  DSPARK_TRY(check_dtype(wdtype));
+  if (!T || !U || !W1 || !W2 || !anchor || !x || !lse_d || !ell || !label_out) return DSPARK_ERR_INVALID;
+  if (!aligned(T, 16) || !aligned(U, 16)) return DSPARK_ERR_INVALID;
+  DSPARK_TRY(check_ws(workspace, workspace_bytes, B, gamma, V));
+  if (!draft_tc_supported(wdtype, r, V)) return DSPARK_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(B, gamma, V);
+  DSPARK_TRY(cuda_status(cudaMemsetAsync(label_out, 0, sizeof(float) * (size_t)B * gamma, s)));
+  DSPARK_TRY(cuda_status(launch_row_stats(T, ell, B, gamma, V, workspace, s)));
+  return cuda_status(launch_acceptance_label_tc(T, U, W1, W2, anchor, x, lse_d, ell,
+                                                ws_ptr<float2>(workspace, L.row_part), verify_num_segs(V), label_out,
+                                                B, gamma, V, ws_ptr<int>(workspace, L.status), s));
+}
+
 int dspark_round(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,
                  int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B, int gamma, int V,
                  int r, int H, const float* sps, int n_sps, int mode, int32_t* khist, uint64_t seed,

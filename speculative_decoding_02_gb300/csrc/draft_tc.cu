@@ -94,7 +94,7 @@ struct __align__(8) Barriers {
 static_assert(sizeof(Barriers) <= kBarBytes, "barrier block overflows its shared-memory slot");
 static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may use");
 
-enum Mode { kDraft = 0, kResidual = 1 };
+enum Mode { kDraft = 0, kResidual = 1, kLabel = 2 };
 
 struct StepParams {
   const float* U;
@@ -113,6 +113,12 @@ struct StepParams {
   const float* lse_d;
   const float* resid_lse;
   unsigned long long* resid_key;
+  // label mode: position k_fixed of every request with k_fixed <= ell_b, the
+  // target-row softmax partials [B*(G+1)][nsegs] and the label output [B][G]
+  const int32_t* ell;
+  const float2* row_part;
+  float* label;
+  int k_fixed, nsegs;
   unsigned long long* keys;             // [G][B] argmax keys of every position, kKeyStride apart
   float2* part;                         // [G][part_slices][B] softmax partials
   unsigned int* gbar;                   // grid-barrier counter (zeroed before launch)
@@ -610,7 +616,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           }
         }
         if (!ok) break;
-        if constexpr (MODE == kResidual) continue;
+        if constexpr (MODE != kDraft) continue;
         const int nsub = min(group_tiles(g), ntl - g);
         for (int j = 0; j < nsub && ok; ++j) {
           const int su = ucount % kUStages;
@@ -698,6 +704,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       if constexpr (MODE == kResidual) {
         ks = active ? p.resid_k[b] : 0;
         active = ks > 0;
+      } else if constexpr (MODE == kLabel) {
+        ks = (active && p.k_fixed <= min(max(p.ell[b], 0), p.G)) ? p.k_fixed : 0;
+        active = ks > 0;
       }
 
       // E = W1[x_{k-1}] into TMEM (gather_e).  From the second position on, E
@@ -716,7 +725,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         prev = checked_token(raw, p.V, p.status);
       }
       const uint32_t e_taddr = tmem + ((uint32_t)(q * 32) << 16) + kTmemE + h * 32;
-      if (MODE == kResidual || k == kf) {
+      if (MODE != kDraft || k == kf) {
         gather_e(p.W1, prev, active, h, e_taddr);
       } else if (__any_sync(0xffffffffu, prev != spec_prev)) {
         // only the rows whose token changed are read again
@@ -747,10 +756,22 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       constexpr bool kShareRes = (MODE == kResidual);
       unsigned long long* res_key = (kShareRes && active) ? p.resid_key + (size_t)b * kKeyStride : nullptr;
       float ld2 = 0.f, lt2 = 0.f;
-      if constexpr (MODE == kResidual) {
+      float lacc = 0.f;   // label mode: this thread's sum of min(p_d, p_t)
+      if constexpr (MODE != kDraft) {
         if (active) {
           ld2 = p.lse_d[(size_t)b * p.G + ks - 1] * kLog2e;
-          lt2 = p.resid_lse[b] * kLog2e;
+          if constexpr (MODE == kResidual) {
+            lt2 = p.resid_lse[b] * kLog2e;
+          } else {
+            // lse of the target row from its segment partials
+            const float2* rp = p.row_part + ((size_t)b * (p.G + 1) + ks - 1) * p.nsegs;
+            float mt = -INFINITY, st2 = 0.f;
+            for (int sg = 0; sg < p.nsegs; ++sg) {
+              const float2 pr = rp[sg];
+              softmax_merge(mt, st2, pr.x, pr.y);
+            }
+            lt2 = (mt + logf(st2)) * kLog2e;
+          }
         }
       }
       bool ok = true;
@@ -758,11 +779,15 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       // shared memory one tile ahead by all epilogue threads (resid_copy)
       long long* off_u = reinterpret_cast<long long*>(X_s);   // element offset of row rr's U row, or -1
       long long* off_t = off_u + BM;
-      if constexpr (MODE == kResidual) {
+      if constexpr (MODE != kDraft) {
         const int tid = threadIdx.x - 64;
         if (tid < R) {
           const int bb = m0 + tid;
-          const int kk = bb < p.B ? p.resid_k[bb] : 0;
+          int kk = 0;
+          if (bb < p.B) {
+            if constexpr (MODE == kResidual) kk = p.resid_k[bb];
+            else kk = p.k_fixed <= min(max(p.ell[bb], 0), p.G) ? p.k_fixed : 0;
+          }
           off_u[tid] = kk > 0 ? ((long long)bb * p.G + (kk - 1)) * p.V : -1;
           off_t[tid] = kk > 0 ? ((long long)bb * (p.G + 1) + (kk - 1)) * p.V : -1;
         }
@@ -777,7 +802,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         const int acc_i = gcount & 1;
         const int v0 = (t0 + i) * BN + part * CPP;
         const int nv = min(CPP, p.V - v0);
-        if constexpr (MODE == kResidual) {
+        if constexpr (MODE != kDraft) {
           // this tile's rows have landed (own copies, then everyone's); the
           // barrier also frees the other stage for the next tile's copies.
           // Every epilogue thread passes here each tile, failed or not.  The
@@ -789,7 +814,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           if (i + 1 < ntl) resid_copy<R>(U_s + ((i + 1) & 1) * kResStageBytes, off_u, p.U, p.T, (t0 + i + 1) * BN, p.V);
         }
         const bool got_acc = sub != 0 || mbar_wait(&bars->acc_full[acc_i], (gcount >> 1) & 1, abort, p.status);
-        if (MODE == kResidual && !got_acc) ok = false;
+        if (MODE != kDraft && !got_acc) ok = false;
         float v[CPP];
         if (got_acc) {
           tc_fence_after();
@@ -888,19 +913,25 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
               for (int e = 0; e < 4; ++e) {
                 const float pd = ex2_approx(fmaf(v[c + e] + uv[e], kLog2e, -ld2));
                 const float pt = ex2_approx(fmaf(tv[e], kLog2e, -lt2));
-                uu[c + e] = pt - pd;
+                if constexpr (MODE == kLabel) {
+                  if (c + e < nv) lacc += fminf(pd, pt);
+                } else {
+                  uu[c + e] = pt - pd;
+                }
               }
             }
-            // the row's best from other CTAs: the latest copy of its key that
-            // has landed in shared memory (nothing waits for it)
-            if (kShareRes && i >= 1) {
-              const unsigned long long gkr = *reinterpret_cast<volatile unsigned long long*>(&gk_rows[r].x);
-              if (gkr) resid_raise(rs, argmax_key_value(gkr));
-            }
-            resid_tile<CPP>(rs, uu, nv, v0, urow, j0, sw, p.key, (uint32_t)b, (uint32_t)ks);
-            if (kShareRes && rs.best_v >= 0 && rs.zbest > rs.zpub && rs.zbest >= rs.zthr) {
-              atomicMax(res_key, argmax_key(rs.zbest, rs.best_v));
-              rs.zpub = rs.zbest;
+            if constexpr (MODE == kResidual) {
+              // the row's best from other CTAs: the latest copy of its key that
+              // has landed in shared memory (nothing waits for it)
+              if (kShareRes && i >= 1) {
+                const unsigned long long gkr = *reinterpret_cast<volatile unsigned long long*>(&gk_rows[r].x);
+                if (gkr) resid_raise(rs, argmax_key_value(gkr));
+              }
+              resid_tile<CPP>(rs, uu, nv, v0, urow, j0, sw, p.key, (uint32_t)b, (uint32_t)ks);
+              if (kShareRes && rs.best_v >= 0 && rs.zbest > rs.zpub && rs.zbest >= rs.zthr) {
+                atomicMax(res_key, argmax_key(rs.zbest, rs.best_v));
+                rs.zpub = rs.zbest;
+              }
             }
           }
           if (kShareRes && h == 0) {
@@ -930,7 +961,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       }
       const int slot = part * R + r;               // parts of row r at r, R + r, ...
       xm[slot] = st.run_m;
-      xs[slot] = st.run_s;
+      xs[slot] = MODE == kLabel ? lacc : st.run_s;
       xk[slot] = key;
       named_bar_sync(1, kEpiWarps * 32);
       if (part == 0 && active && ok) {
@@ -947,8 +978,14 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           // threshold, and a threshold is always a value some part has
           // published.
           p.part[((size_t)(k - 1) * p.B + b) * p.part_slices + slice] = make_float2(M, S);
-        } else {
+        } else if constexpr (MODE == kResidual) {
           if (K) atomicMax(&p.resid_key[(size_t)b * kKeyStride], K);
+        } else {
+          // label: the CTA's sum of min(p_d, p_t) over its columns
+          float Ssum = 0.f;
+#pragma unroll
+          for (int j = 0; j < kParts; ++j) Ssum += xs[j * R + r];
+          atomicAdd(&p.label[(size_t)b * p.G + ks - 1], Ssum);
         }
       }
       (void)ok;
@@ -1239,6 +1276,52 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
   sp.key = key;
   // the U map is not read in this mode; any valid map will do
   kern<<<mtiles * per, kThreads, kSmemBytes, stream>>>(map, map, sp);
+  return cudaGetLastError();
+}
+
+// The acceptance label of every verified position on the tensor cores: for
+// k = 1..G, one launch of the residual pipeline in label mode over the
+// requests with k <= ell_b, adding sum_v min(p_d(v), p_t(v)) into label[b][k-1]
+// (label zeroed by the caller; row_part holds the target rows' partials).
+cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const void* W1, const void* W2,
+                                       const int32_t* anchor, const int32_t* x, const float* lse_d,
+                                       const int32_t* ell, const float2* row_part, int nsegs, float* label, int B,
+                                       int G, int V, int* status, cudaStream_t stream) {
+  CUtensorMap map;
+  cudaError_t e = make_w2_tensor_map(W2, V, &map);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int R = B <= 32 ? 32 : (B <= 64 ? 64 : BM);
+  auto kern = R == 32 ? draft_step_tc<32, kLabel> : (R == 64 ? draft_step_tc<64, kLabel> : draft_step_tc<BM, kLabel>);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int mtiles = div_up(B, R);
+  const int ntiles = div_up(V, BN);
+  int per = std::max(1, sms / mtiles);
+  per = std::min(per, ntiles);
+  StepParams sp{};
+  sp.U = U;
+  sp.W1 = static_cast<const __nv_bfloat16*>(W1);
+  sp.anchor = anchor;
+  sp.T = T;
+  sp.x = x;
+  sp.lse_d = lse_d;
+  sp.ell = ell;
+  sp.row_part = row_part;
+  sp.nsegs = nsegs;
+  sp.label = label;
+  sp.status = status;
+  sp.B = B; sp.G = G; sp.V = V;
+  sp.k_first = sp.k_last = 0;
+  sp.nctas = mtiles * per;
+  sp.ctas_per_mtile = per;
+  sp.ntiles = ntiles;
+  for (int k = 1; k <= G; ++k) {
+    sp.k_fixed = k;
+    kern<<<mtiles * per, kThreads, kSmemBytes, stream>>>(map, map, sp);
+  }
   return cudaGetLastError();
 }
 

@@ -57,6 +57,19 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
                                const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
                                RngKey key, int* status, cudaStream_t stream);
 
+// Acceptance labels (tensor-core path): sum_v min(p_d, p_t) per verified
+// position into label [B][G] (zeroed by the caller), from the target-row
+// partials of launch_row_stats.
+cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const void* W1, const void* W2,
+                                       const int32_t* anchor, const int32_t* x, const float* lse_d,
+                                       const int32_t* ell, const float2* row_part, int nsegs, float* label, int B,
+                                       int G, int V, int* status, cudaStream_t stream);
+
+// The softmax partials of the target rows j < ell_b of every request into the
+// workspace (verify's first two kernels).
+cudaError_t launch_row_stats(const float* T, const int32_t* ell, int B, int gamma, int V, void* ws,
+                             cudaStream_t stream);
+
 cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdtype,
                               const float* w, const float* sts_T, const int32_t* anchor,
                               const int32_t* x, int B, int gamma, int H, int r, int V,

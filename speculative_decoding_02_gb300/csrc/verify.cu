@@ -195,7 +195,6 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, 
     // screen compares against (bound = exp(m - zthr), 2^-10 over)
     float m = -INFINITY, zbest = -INFINITY, zthr = -INFINITY, bound = INFINITY;
     int bestv = -1;
-#pragma unroll 1
     // a thread's 16 entries of chunk ch+1 are loaded while chunk ch is raced
     float4 nx[4];
     load_chunk16(Trow, v0 + 16 * tid, v1, nx);
@@ -446,12 +445,31 @@ verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKe
   }
 }
 
+// verify_prep, then verify_row_stats on a grid sized by the occupancy query.
+cudaError_t row_stats(const float* T, const int32_t* ell, int B, int gamma, int V, void* ws, cudaStream_t stream) {
+  const WsLayout L = ws_layout(B, gamma, V);
+  int* status = ws_ptr<int>(ws, L.status);
+  int* counters = ws_ptr<int>(ws, L.counters);
+  int32_t* rows = ws_ptr<int32_t>(ws, L.rows);
+  float2* row_part = ws_ptr<float2>(ws, L.row_part);
+  const int nsegs = verify_num_segs(V);
+  verify_prep<<<1, 1024, 0, stream>>>(ell, B, gamma, rows, counters, status);
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_row_stats, kRowThreads, 0)) != cudaSuccess)
+    return e;
+  const long long stat_tasks = (long long)B * gamma * nsegs;
+  const int grid_stats = (int)std::max<long long>(1, std::min<long long>(stat_tasks, (long long)sms * std::max(1, per_sm)));
+  verify_row_stats<<<grid_stats, kRowThreads, 0, stream>>>(T, V, nsegs, rows, counters, row_part, status);
+  return cudaGetLastError();
+}
+
 template <int WDT>
 cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   const WsLayout L = ws_layout(a.B, a.gamma, a.V);
   int* status = ws_ptr<int>(a.ws, L.status);
-  int* counters = ws_ptr<int>(a.ws, L.counters);
-  int32_t* rows = ws_ptr<int32_t>(a.ws, L.rows);
   float2* row_part = ws_ptr<float2>(a.ws, L.row_part);
   unsigned long long* bonus_key = ws_ptr<unsigned long long>(a.ws, L.bonus_key);
   unsigned long long* resid_key = ws_ptr<unsigned long long>(a.ws, L.resid_key);
@@ -460,16 +478,10 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   const int nsegs = verify_num_segs(a.V);
   cudaError_t e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.total - L.bonus_key, stream);
   if (e != cudaSuccess) return e;
-  verify_prep<<<1, 1024, 0, stream>>>(a.ell, a.B, a.gamma, rows, counters, status);
+  if ((e = row_stats(a.T, a.ell, a.B, a.gamma, a.V, a.ws, stream)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int per_sm = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_row_stats, kRowThreads, 0)) != cudaSuccess)
-    return e;
-  const long long stat_tasks = (long long)a.B * a.gamma * nsegs;
-  const int grid_stats = (int)std::max<long long>(1, std::min<long long>(stat_tasks, (long long)sms * std::max(1, per_sm)));
-  verify_row_stats<<<grid_stats, kRowThreads, 0, stream>>>(a.T, a.V, nsegs, rows, counters, row_part, status);
   const int grid_bonus = std::min(a.B * nsegs, sms * 2);
   verify_bonus_race<<<grid_bonus, kRowThreads, 0, stream>>>(a.T, a.ell, a.B, a.gamma, a.V, nsegs, a.key, bonus_key,
                                                             status);
@@ -492,6 +504,11 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_row_stats(const float* T, const int32_t* ell, int B, int gamma, int V, void* ws,
+                             cudaStream_t stream) {
+  return row_stats(T, ell, B, gamma, V, ws, stream);
+}
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
   return a.wdtype == DSPARK_BF16 ? run_verify<DSPARK_BF16>(a, stream) : run_verify<DSPARK_F32>(a, stream);
