@@ -25,12 +25,6 @@ def _built():
     ds.library()
 
 
-def _softmax64(row):
-    z = row.astype(np.float64)
-    e = np.exp(z - z.max())
-    return e / e.sum()
-
-
 def _check(w, inp, out, label, reqs):
     h = host(inp)
     x, ell = out.x.cpu().numpy(), out.ell.cpu().numpy()
@@ -43,7 +37,7 @@ def _check(w, inp, out, label, reqs):
                 continue
             prev = int(h["anchor"][b]) if k == 1 else int(x[b, k - 2])
             pd = oracle.draft_probs(h["U"][b, k - 1], h["W1"], h["W2"], prev)
-            pt = _softmax64(h["T"][b, k - 1])
+            pt = oracle.softmax(h["T"][b, k - 1])
             want = oracle.acceptance_label(pd, pt)
             assert abs(lab[b, k - 1] - want) <= 2e-4 + 1e-3 * want, (b, k, lab[b, k - 1], want)
             checked += 1
