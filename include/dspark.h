@@ -167,6 +167,28 @@ int dspark_acceptance_label(const float* T, const float* U, const void* W1, cons
                             size_t workspace_bytes, void* stream);
 
 /*
+ * Sequential temperature scaling of the confidence head ([blog] section 5; the
+ * study report's answer on calibration), a post-hoc fit on held-out samples.
+ * Sample n: confidence logits z[n, :] (c = sigmoid(z / T_k)), verified length
+ * ell[n] in [0, gamma] and accepted count acc[n] <= ell[n].  Position k of
+ * sample n is observed when k <= ell[n], with outcome 1 if acc[n] >= k.  For
+ * k = 1..gamma in order, T_k is the grid value that minimises the expected
+ * calibration error (15 equal-width bins on [0, 1]: sum over bins of
+ * |sum(P - outcome)| / observed samples) of P = prod_{i<k} sigmoid(z_i / T_i)
+ * * sigmoid(z_k / T_k) over the observed samples; the first grid value wins
+ * ties; a position no sample observes gets T = 1 and ECE 0.  fp64 throughout.
+ * In:  z [N, gamma] f32, ell [N] i32, acc [N] i32, grid [ngrid] f32 (> 0), all
+ *      device; gamma <= 32, ngrid <= 256.
+ * Out: T_out [gamma] f32 (usable as sts_T of dspark_confidence), ece_out
+ *      [gamma] f32.  Workspace: dspark_sts_workspace_size bytes, 256-byte
+ *      aligned.
+ */
+size_t dspark_sts_workspace_size(int N, int gamma, int ngrid);
+int dspark_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N, int gamma,
+                   const float* grid, int ngrid, float* T_out, float* ece_out,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * One whole round: draft, confidence, schedule, verify, enqueued in that order
  * on one stream with no host synchronisation.  Arguments as above.
  */

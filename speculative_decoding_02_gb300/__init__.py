@@ -7,7 +7,8 @@ torch stream.  If the compiled library is missing, every call raises
 ``DSparkError`` -- there is no CPU fallback.
 
 Entry points (same names as the C ABI in include/dspark.h):
-  markov_draft, confidence, schedule, verify, round, read_status
+  markov_draft, confidence, schedule, verify, round, read_status,
+  acceptance_label, sts_fit
 """
 import ctypes
 import os
@@ -55,6 +56,10 @@ def _load():
     L.dspark_acceptance_label.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp,
                                           ctypes.c_size_t, vp]
     L.dspark_acceptance_label.restype = i32
+    L.dspark_sts_workspace_size.argtypes = [i32, i32, i32]
+    L.dspark_sts_workspace_size.restype = sz
+    L.dspark_sts_fit.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, vp, vp, sz, vp]
+    L.dspark_sts_fit.restype = i32
     L.dspark_round.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
                                vp, u64, u64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_round.restype = i32
@@ -229,6 +234,24 @@ def acceptance_label(T, U, W1, W2, anchor, x, lse_d, ell, ws=None):
                                      _ptr(lse_d), _ptr(ell), B, G, V, r, _ptr(label), _ptr(ws), ws.numel(),
                                      _stream(dev)), "acceptance_label")
     return label
+
+
+def sts_fit(z, ell, acc, grid):
+    """Sequential temperature scaling: (T [gamma] f32, ece [gamma] f32) fitted on
+    the samples (z [N, gamma] f32 logits, ell and acc [N] i32) over the grid of
+    temperatures (f32), all on one device."""
+    L = _load()
+    _need(z, "z", torch.float32)
+    dev = z.device
+    N, G = z.shape
+    _need(ell, "ell", torch.int32, dev); _need(acc, "acc", torch.int32, dev); _need(grid, "grid", torch.float32, dev)
+    T = torch.empty(G, dtype=torch.float32, device=dev)
+    e = torch.empty(G, dtype=torch.float32, device=dev)
+    nbytes = L.dspark_sts_workspace_size(N, G, grid.numel())
+    ws = torch.empty(max(256, nbytes), dtype=torch.uint8, device=dev)
+    _check(L.dspark_sts_fit(_ptr(z), _ptr(ell), _ptr(acc), N, G, _ptr(grid), grid.numel(), _ptr(T), _ptr(e), _ptr(ws),
+                            ws.numel(), _stream(dev)), "sts_fit")
+    return T, e
 
 
 class RoundOutputs:

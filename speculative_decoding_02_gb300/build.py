@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdspark.so")
-SOURCES = ["api.cu", "draft.cu", "draft_tc.cu", "sched.cu", "verify.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "draft.cu", "draft_tc.cu", "sched.cu", "verify.cu", "noalloc.cu", "sts.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

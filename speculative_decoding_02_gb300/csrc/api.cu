@@ -136,6 +136,22 @@ int dspark_verify(const float* T, const float* U, const void* W1, const void* W2
   return cuda_status(launch_verify(a, (cudaStream_t)stream));
 }
 
+size_t dspark_sts_workspace_size(int N, int gamma, int ngrid) {
+  if (N <= 0 || gamma <= 0 || ngrid <= 0) return 0;
+  return sts_workspace_bytes(N, ngrid);
+}
+
+int dspark_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N, int gamma, const float* grid,
+                   int ngrid, float* T_out, float* ece_out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!z || !ell || !acc || !grid || !T_out || !ece_out) return DSPARK_ERR_INVALID;
+  if (N <= 0 || gamma <= 0 || ngrid <= 0) return DSPARK_ERR_INVALID;
+  if (gamma > kMaxGamma || ngrid > kMaxStsGrid) return DSPARK_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < sts_workspace_bytes(N, ngrid))
+    return DSPARK_ERR_WORKSPACE;
+  return cuda_status(launch_sts_fit(z, ell, acc, N, gamma, grid, ngrid, T_out, ece_out, workspace,
+                                    (cudaStream_t)stream));
+}
+
 int dspark_acceptance_label(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
                             const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* ell, int B,
                             int gamma, int V, int r, float* label_out, void* workspace, size_t workspace_bytes,

@@ -70,6 +70,16 @@ cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const voi
 cudaError_t launch_row_stats(const float* T, const int32_t* ell, int B, int gamma, int V, void* ws,
                              cudaStream_t stream);
 
+// Sequential temperature scaling (per-position grid search on the prefix
+// product, fp64); the workspace holds per-block ECE bin sums.
+constexpr int kStsBins = 15;       // ECE bins
+constexpr int kStsChunk = 2048;    // samples per block
+constexpr int kMaxStsGrid = 256;   // grid values
+size_t sts_workspace_bytes(int N, int ngrid);
+cudaError_t launch_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N, int gamma,
+                           const float* grid, int ngrid, float* T_out, float* ece_out, void* ws,
+                           cudaStream_t stream);
+
 cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdtype,
                               const float* w, const float* sts_T, const int32_t* anchor,
                               const int32_t* x, int B, int gamma, int H, int r, int V,
