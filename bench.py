@@ -359,6 +359,33 @@ def run_gpu(args):
                  "note": "U and T rows of the verified positions once, W2 once; the implementation reads the "
                          "T rows twice (their softmax statistics first)"}
 
+    # sequential temperature scaling over held-out samples of this batch size
+    # (1024 rounds of the workload's requests), timed on its own
+    sts_fit = None
+    if rank == 0:
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        N = 1024 * w.B
+        zs = torch.randn((N, w.gamma), generator=g, device=dev) * 1.8 + 1.2
+        ells = torch.randint(0, w.gamma + 1, (N,), generator=g, device=dev, dtype=torch.int32)
+        accs = torch.minimum(torch.randint(0, w.gamma + 1, (N,), generator=g, device=dev, dtype=torch.int32), ells)
+        grid = torch.exp(torch.linspace(np.log(0.25), np.log(4.0), 49, device=dev)).float()
+        ds.sts_fit(zs, ells, accs, grid)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(3):
+            ds.sts_fit(zs, ells, accs, grid)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        sms = s0.elapsed_time(s1) / 3
+        # every observed (sample, position) evaluates one sigmoid per grid value
+        # plus its prefix product (fp64)
+        obs = int(sum(int((ells >= k).sum()) for k in range(1, w.gamma + 1)))
+        sts_fit = {"ms": sms, "samples": N, "grid": 49, "observed_positions": obs,
+                   "fp64_sigmoids_per_s": obs * (49 + (w.gamma - 1) / 2) / (sms / 1e3)}
+        del zs, ells, accs
+
     # end to end through host buffers: per-round inputs copied in, results out
     e2e = None
     if rank == 0 and not args.no_e2e:
@@ -392,6 +419,7 @@ def run_gpu(args):
                          "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
             "clocks": clk.summary(),
             "acceptance_label": label,
+            "sts_fit": sts_fit,
             "e2e": e2e,
             "gpu_launches": args.steps * kernels_per_round(w),
             "cpu_baseline": cpu,
