@@ -91,3 +91,26 @@ def test_binding_requires_cuda_tensors():
     U = torch.zeros(2, 4, 1024)
     with pytest.raises(ValueError):
         ds.markov_draft(U, U, U, torch.zeros(2, dtype=torch.int32), 0)
+
+
+def test_acceptance_label_and_sts_argument_errors(lib):
+    p = _fake()
+    ws = _fake(0x100000)
+    big = 1 << 30
+    # acceptance labels: a null output, fp32 weights (tensor-core path only),
+    # a workspace that is too small
+    assert lib.dspark_acceptance_label(p, p, p, p, 1, p, p, p, p, 2, 4, 1024, 256, None, ws, big,
+                                       None) == ds.ERR_INVALID
+    assert lib.dspark_acceptance_label(p, p, p, p, 0, p, p, p, p, 2, 4, 1024, 256, p, ws, big,
+                                       None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_acceptance_label(p, p, p, p, 1, p, p, p, p, 2, 4, 1024, 256, p, ws, 16,
+                                       None) == ds.ERR_WORKSPACE
+    # STS: workspace size grows with the samples and the grid; bad arguments
+    assert lib.dspark_sts_workspace_size(0, 4, 8) == 0
+    assert lib.dspark_sts_workspace_size(10000, 4, 49) > lib.dspark_sts_workspace_size(100, 4, 49) > 0
+    assert lib.dspark_sts_fit(None, p, p, 100, 4, p, 49, p, p, ws, big, None) == ds.ERR_INVALID
+    assert lib.dspark_sts_fit(p, p, p, 0, 4, p, 49, p, p, ws, big, None) == ds.ERR_INVALID
+    assert lib.dspark_sts_fit(p, p, p, 100, 33, p, 49, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_sts_fit(p, p, p, 100, 4, p, 257, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_sts_fit(p, p, p, 100, 4, p, 49, p, p, ws, 8, None) == ds.ERR_WORKSPACE
+    assert lib.dspark_sts_fit(p, p, p, 100, 4, p, 49, p, p, _fake(0x100010), big, None) == ds.ERR_WORKSPACE
