@@ -34,6 +34,10 @@
 // (the rejected k*), with U and T row segments staged by the epilogue's own
 // coalesced asynchronous copies, racing blocks of max(0, p_t - p_d).
 //
+// Label (MODE kLabel): the residual pipeline at one fixed position k for every
+// request with k <= ell_b, summing min(p_d, p_t) over the vocabulary (the
+// study report's Eq.8 acceptance) into the request's label.
+//
 // Every wait is bounded; on a timeout the CTA records DSPARK_ERR_TIMEOUT,
 // drains the copies and MMAs it issued, frees its TMEM and returns.
 #include <cuda_bf16.h>
@@ -549,6 +553,8 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
 // MODE kResidual: for every request that rejected at position k*, the fused
 // draft logits of k* again, raced over log max(0, p_t - p_d) (U and T rows
 // read directly by the epilogue threads).
+// MODE kLabel: the same at position k_fixed, adding sum_v min(p_d, p_t) of
+// each row into label[b][k_fixed - 1] (one atomicAdd per CTA and row).
 template <int R, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
