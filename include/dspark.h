@@ -190,7 +190,9 @@ int dspark_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N
 
 /*
  * One whole round: draft, confidence, schedule, verify, enqueued in that order
- * on one stream with no host synchronisation.  Arguments as above.
+ * on one stream with no host synchronisation.  Arguments as above.  A round
+ * can be captured into a CUDA graph (the draft's cooperative launch
+ * included); a replay repeats the captured seed and round.
  */
 int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
                  int wdtype, const void* h, int hdtype, const float* w,
