@@ -243,6 +243,29 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# Across ranks (one process per GPU; each rank runs its own replica)
+# ---------------------------------------------------------------------------
+def slowest_rank_ms(ms, device):
+    """The timed region's length on the slowest rank (the job's time)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_units(units, device):
+    """The units (verified draft tokens) that all ranks processed together."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return int(units)
+    t = torch.tensor([int(units)], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return int(t.item())
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def run_gpu(args):
@@ -308,11 +331,7 @@ def run_gpu(args):
             outs.append(step(args.warmup + i, rec=i))
         e1.record(stream)
         barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(e0.elapsed_time(e1), dev)
     st = ds.read_status(ws)
     if st != ds.OK:
         raise RuntimeError(f"device status {st} in the timed rounds")
@@ -321,7 +340,7 @@ def run_gpu(args):
     n_acc = sum(int(n.sum()) for _, n in outs)
     n_rej = sum(int((n < e).sum()) for e, n in outs)
     per_round = ell_sum / args.steps
-    value = world * ell_sum / (ms / 1e3)
+    value = job_units(ell_sum, dev) / (ms / 1e3)
 
     # dominant kernel: the Markov draft, timed inside the timed region
     draft_ms = float(np.mean([dstart[i].elapsed_time(dend[i]) for i in range(args.steps)]))
