@@ -212,6 +212,21 @@ def test_gpu_sampling_law_chi_square():
     lab = oracle.acceptance_label(pd, pt)
     rate = float((n >= 1).float().mean())
     assert abs(rate - lab) < 3.3 * np.sqrt(lab * (1 - lab) / B)
+    # the first two emitted tokens at ell = 2: a request that stops short is
+    # extended by sampling the target on the host, and since T does not depend
+    # on the prefix the pair follows softmax(T row 0) x softmax(T row 1)
+    ell2 = torch.full((B,), 2, dtype=torch.int32, device=DEV)
+    n2, tok2 = ds.verify(T, U, W1d, W2d, anchor, x, p, lse, ell2, 77, 5)
+    torch.cuda.synchronize()
+    n2, tok2, xh = n2.cpu().numpy(), tok2.cpu().numpy(), x.cpu().numpy()
+    pt1 = torch.softmax(T1[0, 1].double(), 0).numpy()
+    ext = np.random.default_rng(11).choice(V, size=B, p=pt1)
+    s1 = np.where(n2 >= 1, xh[:, 0], tok2)
+    s2 = np.where(n2 >= 2, xh[:, 1], np.where(n2 == 1, tok2, ext))
+    e = np.outer(pt, pt1).ravel() * B
+    cnt2 = np.bincount(s1 * V + s2, minlength=V * V)
+    assert e.min() > 5
+    assert stats.chi2.sf(((cnt2 - e) ** 2 / e).sum(), V * V - 1) > 1e-4
 
 
 FULL = ["qwen3_4b", "batch128", "large_vocab", "serving512"]
