@@ -211,6 +211,19 @@ def host_sample(w, nreq, device):
     return wsmall, d
 
 
+def single_thread_sample(w, hs):
+    """The oracle on one core: one round of the first request alone."""
+    import oracle
+    thr = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        tok, dt, _ = oracle_round_sample(w, hs, 1)
+    finally:
+        oracle.set_num_threads(thr)
+    return {"value": tok / dt, "unit": UNIT, "cores": 1,
+            "sample": f"one oracle round over 1 of {w.B} requests (full gamma, V), {dt:.1f} s wall"}
+
+
 def cpu_sample_size(w):
     import oracle
     return max(1, min(w.B, oracle.num_threads()))
@@ -417,7 +430,8 @@ def run_gpu(args):
         tok, dt, thr = oracle_round_sample(w, hs, nreq)
         cpu = {"value": tok / dt, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"one oracle round over {nreq} of {w.B} requests (full gamma, V), "
-                         f"{dt:.1f} s wall"}
+                         f"{dt:.1f} s wall",
+               "single_thread": single_thread_sample(w, hs)}
 
     if rank == 0:
         rbytes = round_bytes(w, per_round, n_rej / args.steps)

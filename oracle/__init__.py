@@ -73,6 +73,8 @@ def lib():
         L.oracle_verify.restype = c_int
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = c_int
+        L.oracle_set_num_threads.argtypes = [c_int]
+        L.oracle_set_num_threads.restype = None
         _lib = L
     return _lib
 
@@ -284,3 +286,8 @@ def verify(T, U, W1, W2, anchor, x, ell, seed, rnd, b0=0, b1=None):
 
 def num_threads():
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n):
+    """Threads of the parallel request loops from now on (n >= 1)."""
+    lib().oracle_set_num_threads(int(n))

@@ -572,3 +572,13 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Sets the number of threads of the parallel request loops (n >= 1; no effect
+ * without OpenMP).  Used to time the oracle on one core beside all of them. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

@@ -60,3 +60,19 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference"])
     assert bench.run_reference(bench.parse()) is None
     assert capsys.readouterr().out == ""
+
+
+def test_oracle_single_thread_leg():
+    # the CPU leg's one-core sample runs one request at one thread and leaves
+    # the oracle's thread count as it found it
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from speculative_decoding_02_gb300 import workloads as wl
+    w = wl.WORKLOADS["tiny"]
+    _, hs = bench.host_sample(w, 2, "cpu")
+    thr = oracle.num_threads()
+    st = bench.single_thread_sample(w, hs)
+    assert oracle.num_threads() == thr
+    assert st["cores"] == 1 and st["unit"] == bench.UNIT and st["value"] >= 0
+    assert "1 of 2 requests" in st["sample"]

@@ -336,3 +336,33 @@ def test_draft_uses_stream0_counter_layout():
             assert out["x"][b, k - 1] == x
             assert out["margin"][b, k - 1] == pytest.approx(mg, abs=1e-12)
             prev = out["x"][b, k - 1]
+
+
+def test_thread_count_leaves_results_unchanged():
+    # the request loops run in parallel; one thread must give the same rounds
+    rng = np.random.default_rng(17)
+    B, G, V, r = 6, 3, 96, 16
+    U = rng.normal(0, 2, (B, G, V)).astype(np.float32)
+    T = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.3, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.3, (V, r)).astype(np.float32)
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    ell = np.array([0, 1, 2, 3, 3, 2], np.int32)
+
+    def one_round():
+        d = oracle.draft(U, W1, W2, anchor, 9, 4)
+        v = oracle.verify(T, U, W1, W2, anchor, d["x"], ell, 9, 4)
+        return d, v
+
+    many = one_round()
+    thr = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        assert oracle.num_threads() == 1
+        single = one_round()
+    finally:
+        oracle.set_num_threads(thr)
+    assert oracle.num_threads() == thr
+    for a, b in zip(many, single):
+        for k in a:
+            assert np.array_equal(a[k], b[k], equal_nan=a[k].dtype.kind == "f"), k
