@@ -71,7 +71,8 @@ extern "C" {
 #define DSPARK_SCHED_GREEDY 1  /* greedy Theta maximisation with early stop */
 #define DSPARK_SCHED_TOPK 2    /* dynamic top-K, K = greedy count of round - 2 */
 
-/* Bytes of device scratch the entry points below need for these sizes. */
+/* Bytes of device scratch the entry points below need for these sizes; 0 when
+ * a size is not positive. */
 size_t dspark_workspace_size(int B, int gamma, int V);
 
 /*
@@ -181,7 +182,7 @@ int dspark_acceptance_label(const float* T, const float* U, const void* W1, cons
  *      device; gamma <= 32, ngrid <= 256.
  * Out: T_out [gamma] f32 (usable as sts_T of dspark_confidence), ece_out
  *      [gamma] f32.  Workspace: dspark_sts_workspace_size bytes, 256-byte
- *      aligned.
+ *      aligned (that size is 0 when a size is not positive).
  */
 size_t dspark_sts_workspace_size(int N, int gamma, int ngrid);
 int dspark_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N, int gamma,
@@ -206,9 +207,9 @@ int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * The Markov draft without a caller workspace.  The paper has no counterpart:
- * this entry exists for callers that cannot allocate device memory when they
- * call us (an engine whose pool owns all of HBM, a plugin given no allocator,
+ * The Markov draft without a caller workspace.  The method has no counterpart:
+ * this entry serves callers that cannot allocate device memory at the time of
+ * the call (an engine whose pool owns all of HBM, a plugin given no allocator,
  * a decode loop that must not call cudaMalloc).  It computes exactly what
  * dspark_markov_draft computes, with its scratch in a fixed array of
  * DSPARK_NOALLOC_SCRATCH_BYTES inside the library's device memory, which every
