@@ -21,7 +21,7 @@
  *    workspace must not be used by two calls that run concurrently.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only
  *    enqueue work and never synchronise, except dspark_read_status.
- *  - Shapes: B requests, gamma draft positions (1..32), V vocabulary entries
+ *  - Shapes: B requests (1..65535), gamma draft positions (1..32), V vocabulary entries
  *    (V % 8 == 0), r Markov rank (r % 16 == 0, 16..256), H hidden size.
  *    Position k = 1..gamma is row k-1 of the per-position tensors.
  *  - Weights: W1 [V, r] is the Markov embedding of the previous token; W2 [V, r]

@@ -53,7 +53,7 @@ int confidence_checks(const void* h, int hdtype, const void* W1, int wdtype, con
   DSPARK_TRY(check_dtype(hdtype));
   DSPARK_TRY(check_dtype(wdtype));
   if (B <= 0 || gamma <= 0 || H < 0 || r <= 0 || V <= 0) return DSPARK_ERR_INVALID;
-  if (gamma > kMaxGamma) return DSPARK_ERR_UNSUPPORTED;
+  if (gamma > kMaxGamma || B > 65535) return DSPARK_ERR_UNSUPPORTED;
   if ((H > 0 && !h) || !W1 || !w || !anchor || !x || !c_out) return DSPARK_ERR_INVALID;
   return DSPARK_OK;
 }
@@ -221,7 +221,7 @@ const char* dspark_strerror(int status) {
   switch (status) {
     case DSPARK_OK: return "ok";
     case DSPARK_ERR_INVALID: return "invalid argument (null pointer, size or table length)";
-    case DSPARK_ERR_UNSUPPORTED: return "unsupported size (gamma > 32, V % 8, r % 16 or r > 256, B*gamma > 8192)";
+    case DSPARK_ERR_UNSUPPORTED: return "unsupported size (B > 65535, gamma > 32, V % 8, r % 16 or r > 256, B*gamma > 8192)";
     case DSPARK_ERR_CUDA: return "a CUDA launch or runtime call failed";
     case DSPARK_ERR_TIMEOUT: return "a device-side bounded wait gave up";
     case DSPARK_ERR_WORKSPACE: return "workspace missing, misaligned (256 B) or smaller than dspark_workspace_size";

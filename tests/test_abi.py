@@ -57,7 +57,8 @@ def test_host_side_argument_errors(lib):
     big = 1 << 30
     # null pointers
     assert lib.dspark_markov_draft(None, p, p, 1, p, 2, 4, 1024, 16, 0, 0, p, p, p, ws, big, None) == ds.ERR_INVALID
-    # unsupported sizes: gamma > 32, V % 8, r % 16, r > 256
+    # unsupported sizes: B > 65535, gamma > 32, V % 8, r % 16, r > 256
+    assert lib.dspark_markov_draft(p, p, p, 1, p, 65536, 4, 1024, 16, 0, 0, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
     assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 33, 1024, 16, 0, 0, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
     assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 4, 1020, 16, 0, 0, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
     assert lib.dspark_markov_draft(p, p, p, 1, p, 2, 4, 1024, 24, 0, 0, p, p, p, ws, big, None) == ds.ERR_UNSUPPORTED
@@ -79,6 +80,9 @@ def test_host_side_argument_errors(lib):
                              None) == ds.ERR_INVALID
     # confidence: bad dtype
     assert lib.dspark_confidence(p, 3, p, 1, p, None, p, p, 2, 4, 64, 16, 1024, p, None) == ds.ERR_INVALID
+    # confidence: more requests than the grid arithmetic allows, gamma past 32
+    assert lib.dspark_confidence(p, 1, p, 1, p, None, p, p, 65536, 32, 64, 16, 1024, p, None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_confidence(p, 1, p, 1, p, None, p, p, 2, 33, 64, 16, 1024, p, None) == ds.ERR_UNSUPPORTED
     # bounded-wait self-test: unknown mode, missing / small / misaligned workspace
     assert lib.dspark_selftest_wait_timeout(2, ws, big, None) == ds.ERR_INVALID
     assert lib.dspark_selftest_wait_timeout(0, None, big, None) == ds.ERR_WORKSPACE
