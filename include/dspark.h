@@ -98,7 +98,9 @@ int dspark_markov_draft(const float* U, const void* W1, const void* W2, int wdty
  * [blog] section 5), or 1 when sts_T is NULL.  No bias term (Eq.7 has none).
  * In:  h [B, gamma, H] (hdtype), W1 [V, r] (wdtype), w [H + r] f32,
  *      sts_T [gamma] f32 or NULL, anchor [B], x [B, gamma] i32.
- * Out: c_out [B, gamma] f32.
+ * Out: c_out [B, gamma] f32.  A previous token outside [0, V) gives c = 0
+ * (this call has no workspace to report it in; dspark_round also records
+ * DSPARK_ERR_INVALID in its status word).
  */
 int dspark_confidence(const void* h, int hdtype, const void* W1, int wdtype,
                       const float* w, const float* sts_T, const int32_t* anchor,
