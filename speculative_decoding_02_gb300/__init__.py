@@ -117,6 +117,15 @@ def _need(t, what, dtype=None, device=None):
     return t
 
 
+def _sized(t, what, shape):
+    """Raise unless t has this shape.  The kernels index every tensor from the
+    sizes alone, so a tensor smaller than its sizes say would be read or
+    written past its end on the device."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must be {list(shape)}, got {list(t.shape)}")
+    return t
+
+
 _ws_cache = {}
 
 
@@ -143,7 +152,8 @@ def markov_draft(U, W1, W2, anchor, seed, rnd=0, ws=None):
     dev = U.device
     B, G, V = U.shape
     _need(W1, "W1", device=dev); _need(W2, "W2", W1.dtype, dev); _need(anchor, "anchor", torch.int32, dev)
-    r = W1.shape[1]
+    r = W1.shape[-1]
+    _sized(W1, "W1", (V, r)); _sized(W2, "W2", (V, r)); _sized(anchor, "anchor", (B,))
     x = torch.empty((B, G), dtype=torch.int32, device=dev)
     p = torch.empty((B, G), dtype=torch.float32, device=dev)
     lse = torch.empty((B, G), dtype=torch.float32, device=dev)
@@ -163,7 +173,10 @@ def confidence(h, W1, w, anchor, x, sts_T=None):
     _need(anchor, "anchor", torch.int32, dev); _need(x, "x", torch.int32, dev)
     if sts_T is not None:
         _need(sts_T, "sts_T", torch.float32, dev)
+    if W1.dim() != 2:
+        raise ValueError(f"W1 must be [V, r], got {list(W1.shape)}")
     V, r = W1.shape
+    _sized(w, "w", (H + r,)); _sized(anchor, "anchor", (B,)); _sized(x, "x", (B, G)); _sized(sts_T, "sts_T", (G,))
     c = torch.empty((B, G), dtype=torch.float32, device=dev)
     _check(L.dspark_confidence(_ptr(h), _dt(h, "h"), _ptr(W1), _dt(W1, "W1"), _ptr(w), _ptr(sts_T), _ptr(anchor),
                                _ptr(x), B, G, H, r, V, _ptr(c), _stream(dev)), "confidence")
@@ -180,6 +193,7 @@ def schedule(c, sps=None, mode=SCHED_GREEDY, rnd=0, khist=None, ws=None):
         _need(sps, "sps", torch.float32, dev)
     if khist is not None:
         _need(khist, "khist", torch.int32, dev)
+    _sized(khist, "khist", (2,))
     ell = torch.empty(B, dtype=torch.int32, device=dev)
     nstar = torch.empty(1, dtype=torch.int32, device=dev)
     theta = torch.empty(1, dtype=torch.float64, device=dev)
@@ -203,7 +217,10 @@ def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None):
     for t, n in [(anchor, "anchor"), (x, "x"), (ell, "ell")]:
         _need(t, n, torch.int32, dev)
     _need(p_d, "p_d", torch.float32, dev); _need(lse_d, "lse_d", torch.float32, dev)
-    r = W1.shape[1]
+    r = W1.shape[-1]
+    _sized(W1, "W1", (V, r)); _sized(W2, "W2", (V, r)); _sized(anchor, "anchor", (B,)); _sized(ell, "ell", (B,))
+    for t, n in [(x, "x"), (p_d, "p_d"), (lse_d, "lse_d")]:
+        _sized(t, n, (B, G))
     n = torch.empty(B, dtype=torch.int32, device=dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
@@ -227,7 +244,9 @@ def acceptance_label(T, U, W1, W2, anchor, x, lse_d, ell, ws=None):
     for t, n in [(anchor, "anchor"), (x, "x"), (ell, "ell")]:
         _need(t, n, torch.int32, dev)
     _need(lse_d, "lse_d", torch.float32, dev)
-    r = W1.shape[1]
+    r = W1.shape[-1]
+    _sized(W1, "W1", (V, r)); _sized(W2, "W2", (V, r)); _sized(anchor, "anchor", (B,)); _sized(ell, "ell", (B,))
+    _sized(x, "x", (B, G)); _sized(lse_d, "lse_d", (B, G))
     label = torch.empty(B, G, dtype=torch.float32, device=dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
     _check(L.dspark_acceptance_label(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x),
@@ -245,6 +264,7 @@ def sts_fit(z, ell, acc, grid):
     dev = z.device
     N, G = z.shape
     _need(ell, "ell", torch.int32, dev); _need(acc, "acc", torch.int32, dev); _need(grid, "grid", torch.float32, dev)
+    _sized(ell, "ell", (N,)); _sized(acc, "acc", (N,)); _sized(grid, "grid", (grid.numel(),))
     T = torch.empty(G, dtype=torch.float32, device=dev)
     e = torch.empty(G, dtype=torch.float32, device=dev)
     nbytes = L.dspark_sts_workspace_size(N, G, grid.numel())
@@ -273,6 +293,17 @@ class RoundOutputs:
         return dict(x=self.x, p=self.p, lse=self.lse, c=self.c, ell=self.ell, nstar=self.nstar,
                     theta=self.theta, n=self.n, tok=self.tok)
 
+    def check(self, B, G, device):
+        """Raise unless every buffer has the shape, dtype and device of a
+        round of B requests and G positions."""
+        i32, f32 = torch.int32, torch.float32
+        want = dict(x=((B, G), i32), p=((B, G), f32), lse=((B, G), f32), c=((B, G), f32), ell=((B,), i32),
+                    nstar=((1,), i32), theta=((1,), torch.float64), n=((B,), i32), tok=((B,), i32))
+        for name, (shape, dtype) in want.items():
+            t = getattr(self, name)
+            _need(t, f"out.{name}", dtype, device)
+            _sized(t, f"out.{name}", shape)
+
 
 def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
           out=None, ws=None):
@@ -293,8 +324,13 @@ def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, 
         _need(khist, "khist", torch.int32, dev)
     if sts_T is not None:
         _need(sts_T, "sts_T", torch.float32, dev)
-    r, H = W1.shape[1], h.shape[2]
+    if h.dim() != 3:
+        raise ValueError(f"h must be [B, gamma, H], got {list(h.shape)}")
+    r, H = W1.shape[-1], h.shape[2]
+    _sized(W1, "W1", (V, r)); _sized(W2, "W2", (V, r)); _sized(h, "h", (B, G, H)); _sized(w, "w", (H + r,))
+    _sized(anchor, "anchor", (B,)); _sized(khist, "khist", (2,)); _sized(sts_T, "sts_T", (G,))
     out = RoundOutputs(B, G, dev) if out is None else out
+    out.check(B, G, dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
     n_sps = 0 if sps is None else sps.numel()
     _check(L.dspark_round(_ptr(U), _ptr(T), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h), _dt(h, "h"), _ptr(w),

@@ -97,6 +97,22 @@ def test_binding_requires_cuda_tensors():
         ds.markov_draft(U, U, U, torch.zeros(2, dtype=torch.int32), 0)
 
 
+def test_binding_shape_checks():
+    # the kernels index every tensor from the sizes alone: a W1 with fewer rows
+    # than the vocabulary, or per-request tensors of the wrong length, must be
+    # refused before anything reaches the device
+    import torch
+    ds._sized(torch.zeros(8, 16), "W1", (8, 16))
+    ds._sized(None, "sts_T", (4,))
+    for t, shape in [(torch.zeros(7, 16), (8, 16)), (torch.zeros(8, 16), (16, 8)), (torch.zeros(2, 1), (2,)),
+                     (torch.zeros(3), (2,))]:
+        with pytest.raises(ValueError):
+            ds._sized(t, "t", shape)
+    out = ds.RoundOutputs(2, 3, "cpu")
+    with pytest.raises(ValueError):
+        out.check(2, 3, torch.device("cpu"))   # CPU buffers are refused first
+
+
 def test_acceptance_label_and_sts_argument_errors(lib):
     p = _fake()
     ws = _fake(0x100000)
