@@ -43,6 +43,14 @@
 #define ORACLE_ERR_INVALID 1
 #define ORACLE_ERR_NOMEM 2
 
+/* Records an error from inside a parallel request loop. */
+static void set_status(int* status, int value) {
+#ifdef _OPENMP
+#pragma omp critical(oracle_status)
+#endif
+  *status = value;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Counter-based generator: Philox4x32 with 10 rounds.                        */
 /* J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel Random       */
@@ -292,7 +300,7 @@ void oracle_draft_probs(int V, int r, const float* U_row, const void* W1,
  * with x0 the anchor token ([blog] section 3: the anchor is the first predicted
  * position's input).  For k = 1..gamma and every request b in [b0, b1):
  *   l = U[b, k-1, :] + B_k(x_{k-1});   lse = log sum exp l;
- *   x_k = the two-level softmax draw of oracle_block_sample (streams 0 and 5);
+ *   x_k = the two-level softmax draw of oracle_block_sample (streams 0 and 4);
  *   p_k(x_k) = exp(l(x_k) - lse).
  * When x_force is given, the previous token of step k >= 2 is taken from it
  * (teacher forcing: each step is checked on the other side's upstream token);
@@ -310,7 +318,7 @@ int oracle_draft(int B, int G, int V, int r, const float* U, const void* W1,
   for (int b = b0; b < b1; ++b) {
     double* l = (double*)malloc(sizeof(double) * (size_t)V);
     if (!l) {
-      status = ORACLE_ERR_NOMEM;
+      set_status(&status, ORACLE_ERR_NOMEM);
       continue;
     }
     int prev = anchor[b];
@@ -318,7 +326,7 @@ int oracle_draft(int B, int G, int V, int r, const float* U, const void* W1,
       if (k > 1) prev = x_force ? x_force[(size_t)b * G + k - 2]
                                 : x_out[(size_t)b * G + k - 2];
       if (prev < 0 || prev >= V) {
-        status = ORACLE_ERR_INVALID;
+        set_status(&status, ORACLE_ERR_INVALID);
         break;
       }
       const float* U_row = U + ((size_t)b * G + (k - 1)) * (size_t)V;
@@ -504,13 +512,13 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
     double* p_t = (double*)malloc(sizeof(double) * (size_t)V);
     double* score = (double*)malloc(sizeof(double) * (size_t)V);
     if (!p_d || !p_t || !score) {
-      status = ORACLE_ERR_NOMEM;
+      set_status(&status, ORACLE_ERR_NOMEM);
       free(p_d); free(p_t); free(score);
       continue;
     }
     int L = ell[b];
     if (L < 0 || L > G) {
-      status = ORACLE_ERR_INVALID;
+      set_status(&status, ORACLE_ERR_INVALID);
       free(p_d); free(p_t); free(score);
       continue;
     }
@@ -523,6 +531,11 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
     for (int k = 1; k <= L; ++k) {
       int prev = (k == 1) ? anchor[b] : x[(size_t)b * G + k - 2];
       int xk = x[(size_t)b * G + k - 1];
+      if (prev < 0 || prev >= V || xk < 0 || xk >= V) {
+        set_status(&status, ORACLE_ERR_INVALID);
+        n = -1;
+        break;
+      }
       const float* U_row = U + ((size_t)b * G + (k - 1)) * (size_t)V;
       const float* T_row = T + ((size_t)b * (G + 1) + (k - 1)) * (size_t)V;
       oracle_draft_probs(V, r, U_row, W1, W2, wdt, prev, p_d);
@@ -547,6 +560,12 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
                               (uint32_t)k, &ymargin);
       }
       break;
+    }
+    if (n < 0) {
+      n_out[b] = -1;
+      y_out[b] = -1;
+      free(p_d); free(p_t); free(score);
+      continue;
     }
     if (n == L) {
       const float* T_row = T + ((size_t)b * (G + 1) + L) * (size_t)V;

@@ -292,3 +292,22 @@ def test_residual_uses_stream2_at_rejected_position():
         assert v["y"][b] == want
         checked += 1
     assert checked > 50
+
+
+def test_out_of_range_tokens_are_refused():
+    # a drafted token outside the vocabulary is an error, not a read past W1
+    rng = np.random.default_rng(3)
+    B, G, V, r = 2, 2, 16, 4
+    U = rng.normal(0, 1, (B, G, V)).astype(np.float32)
+    T = rng.normal(0, 1, (B, G + 1, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.3, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.3, (V, r)).astype(np.float32)
+    anchor = np.array([1, 2], np.int32)
+    ell = np.array([2, 2], np.int32)
+    for bad in (V, -1):
+        x = np.array([[3, 4], [5, bad]], np.int32)
+        with pytest.raises(RuntimeError):
+            oracle.verify(T, U, W1, W2, anchor, x, ell, 1, 0)
+    bad_anchor = np.array([1, V + 3], np.int32)
+    with pytest.raises(RuntimeError):
+        oracle.verify(T, U, W1, W2, bad_anchor, np.array([[3, 4], [5, 6]], np.int32), ell, 1, 0)
