@@ -22,9 +22,10 @@
  *
  * Parity pins (all in tests/test_oracle_*.py, CPU only):
  *   philox      -- published known-answer vectors + uniformity tests
- *   draft       -- Markov-bias-free special case is an independent per-position
- *                  Gumbel-max (chi-square on V=8); uniform logits give p = 1/V;
- *                  lse against a direct log-sum-exp; bias against a matrix product
+ *   draft       -- the Markov-bias-free special case draws every position
+ *                  independently from softmax(U_k) (chi-square on V = 5); the law
+ *                  of a planted chain; uniform logits give p = 1/V; lse against a
+ *                  direct log-sum-exp; the two-level draw restated from raw words
  *   confidence  -- closed form on hand-made cases; w = 0 gives 1/2; T -> inf gives 1/2
  *   schedule    -- exhaustive search over all verify lengths on tiny batches;
  *                  closed-form SPS cases

@@ -92,7 +92,7 @@ def test_draft_probability_and_lse_by_construction():
 
 
 def test_draft_sequence_law_chi_square():
-    # Gumbel-max law (argmax of l + Gumbel noise is softmax(l)) over the whole
+    # the sampler's law (an exact draw from softmax(l)) over the whole
     # semi-autoregressive chain: P(x1,x2,x3) = prod_k q_k(x_k) A[x_{k-1},x_k] / Z_k
     V, G = 4, 3
     U, W1, W2, q, A = _constructed_case(V, G, seed=5)
@@ -121,8 +121,8 @@ def test_draft_sequence_law_chi_square():
 
 
 def test_markov_free_draft_is_parallel_drafter():
-    # With W2 = 0 the bias vanishes and each position is an independent
-    # Gumbel-max draw from softmax(U_k) (the parallel-drafter special case).
+    # With W2 = 0 the bias vanishes and each position is an independent draw
+    # from softmax(U_k) (the parallel-drafter special case).
     V, G, B = 5, 2, 40000
     rng = np.random.default_rng(2)
     Urow = rng.normal(0, 1, (G, V)).astype(np.float32)
