@@ -24,8 +24,10 @@
  *   philox      -- published known-answer vectors + uniformity tests
  *   draft       -- the Markov-bias-free special case draws every position
  *                  independently from softmax(U_k) (chi-square on V = 5); the law
- *                  of a planted chain; uniform logits give p = 1/V; lse against a
- *                  direct log-sum-exp; the two-level draw restated from raw words
+ *                  of a planted chain; p and lse of a one-hot construction
+ *                  (W1 = I, so the bias is log A[prev, v]: a transposed W2 fails
+ *                  it); uniform logits give p = 1/V; the two-level draw restated
+ *                  from raw words
  *   confidence  -- closed form on hand-made cases; w = 0 gives 1/2; T -> inf gives 1/2
  *   schedule    -- exhaustive search over all verify lengths on tiny batches;
  *                  closed-form SPS cases
