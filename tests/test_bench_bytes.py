@@ -1,0 +1,55 @@
+"""The bench's algorithmic byte counts and launch counts (CPU only): they follow
+the per-unit figures stated for the roofline, term by term, and agree with the
+committed profile of the draft kernel."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from speculative_decoding_02_gb300 import workloads as wl  # noqa: E402
+
+# round totals with ell = gamma and no residual, in MB, as tabulated by hand
+# from U + T rows + W2 + h (+ the small terms)
+ROUND_MB = {"qwen3_4b": 722.5, "batch128": 2656.4, "large_vocab": 1279.3, "serving512": 3000.9}
+
+
+@pytest.mark.parametrize("name", sorted(ROUND_MB))
+def test_round_bytes_match_the_tabulated_totals(name):
+    w = wl.WORKLOADS[name]
+    assert bench.round_bytes(w, w.B * w.gamma, 0) / 1e6 == pytest.approx(ROUND_MB[name], abs=0.1)
+
+
+def test_round_bytes_terms():
+    w = wl.WORKLOADS["batch128"]
+    base = bench.round_bytes(w, 1000, 0)
+    assert bench.round_bytes(w, 1001, 0) - base == 4 * w.V        # one more verified T row
+    assert bench.round_bytes(w, 1000, 1) - base == 8 * w.V        # a rejection re-reads a U and a T row
+    # every request reads at least its first T row (bonus or first verified)
+    assert bench.round_bytes(w, 0, 0) >= 4 * w.B * w.gamma * w.V + 4 * w.V * w.B
+
+
+def test_draft_bytes_match_the_profile():
+    w = wl.WORKLOADS["batch128"]
+    d = bench.draft_bytes_per_launch(w)
+    # U once (1244.7 MB), W2 once (77.8 MB), the W1 gathers and x/p/lse
+    assert d == 4 * 128 * 16 * 151936 + 2 * 256 * 151936 + 2 * 128 * 16 * 256 + 12 * 128 * 16
+    kv = {}
+    for line in open(bench.DRAFT_PROFILE):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            kv[k.strip()] = v.strip()
+    assert int(kv["algorithmic_bytes_per_launch"]) == d
+    # the profile's DRAM traffic is within a few per cent of the algorithmic bytes
+    assert 1.0 <= int(kv["dram_bytes_per_launch"]) / d < 1.05
+
+
+def test_kernels_per_round():
+    # tensor-core path: one persistent draft launch; CUDA-core path: a step and
+    # a finalize per position; then confidence, schedule and six verify kernels
+    assert bench.kernels_per_round(wl.WORKLOADS["batch128"]) == 9
+    t = wl.WORKLOADS["tiny"]
+    assert bench.kernels_per_round(t) == 2 * t.gamma + 8
