@@ -224,6 +224,27 @@ def single_thread_sample(w, hs):
             "sample": f"one oracle round over 1 of {w.B} requests (full gamma, V), {dt:.1f} s wall"}
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine
+    type); never raises."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
 def cpu_sample_size(w):
     import oracle
     return max(1, min(w.B, oracle.num_threads()))
@@ -250,7 +271,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": args.workload, "B": w.B, "gamma": w.gamma, "V": w.V},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -428,7 +450,7 @@ def run_gpu(args):
         nreq = cpu_sample_size(w)
         _, hs = host_sample(w, nreq, dev)
         tok, dt, thr = oracle_round_sample(w, hs, nreq)
-        cpu = {"value": tok / dt, "unit": UNIT, "cores": thr, "kind": "oracle",
+        cpu = {"value": tok / dt, "unit": UNIT, "cores": thr, "kind": "oracle", "cpu_model": cpu_model(),
                "sample": f"one oracle round over {nreq} of {w.B} requests (full gamma, V), "
                          f"{dt:.1f} s wall",
                "single_thread": single_thread_sample(w, hs)}

@@ -1,5 +1,6 @@
-"""The bench's clock record (CPU only): the summary of nvidia-smi samples that
-decides whether a timed run saw throttling."""
+"""The bench's host records (CPU only): the summary of nvidia-smi samples that
+decides whether a timed run saw throttling, and the CPU model beside the
+oracle's time."""
 import os
 import sys
 
@@ -42,3 +43,13 @@ def test_no_sampler_and_no_samples():
     c = bench.Clocks(0)
     assert c.summary()["reasons"] == ["nvidia-smi unavailable"]
     assert _summary(["garbage"])["reasons"] == ["no samples"]
+
+
+def test_cpu_model_never_raises(monkeypatch):
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+    def boom(*a, **k):
+        raise OSError("no lscpu")
+
+    monkeypatch.setattr(bench.subprocess, "run", boom)
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()   # /proc/cpuinfo or the machine type
