@@ -37,6 +37,30 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} declared but not exported"
 
 
+def _prototypes():
+    """name -> number of parameters, from every prototype in include/*.h."""
+    protos = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            for name, params in re.findall(r"\b(dspark_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", txt, flags=re.S):
+                params = params.strip()
+                protos[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return protos
+
+
+def test_binding_argument_counts_match_the_header(lib):
+    # ctypes cannot see the C signatures: a parameter added on one side only
+    # would shift every later argument, so the counts are compared here
+    protos = _prototypes()
+    assert set(protos) == _declared()
+    bound = [n for n in protos if getattr(lib, n).argtypes is not None]
+    assert {"dspark_markov_draft", "dspark_verify", "dspark_round", "dspark_sts_fit"} <= set(bound)
+    for n in bound:
+        assert len(getattr(lib, n).argtypes) == protos[n], n
+
+
 def test_strerror_and_workspace_size(lib):
     for code in range(7):
         assert ds._strerror(code)
