@@ -114,6 +114,29 @@ def test_host_side_argument_errors(lib):
     assert lib.dspark_selftest_wait_timeout(0, _fake(0x100010), big, None) == ds.ERR_WORKSPACE
 
 
+def test_product_path_never_loads_the_oracle():
+    # the package (binding, kernels, library build) imports, links and runs
+    # nothing under oracle/: a reference to it may only appear in prose
+    pkg = os.path.join(ROOT, "speculative_decoding_02_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", txt, flags=re.M), fn
+                assert "liboracle" not in txt and "dspark_oracle" not in txt, fn
+                assert not re.search(r"#include\s*[<\"][^>\"]*oracle", txt), fn
+
+
+def test_missing_library_raises(monkeypatch):
+    # no CPU fallback: without the built library every call fails loudly
+    monkeypatch.setattr(ds, "_lib", None)
+    monkeypatch.setattr(ds, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libdspark.so"))
+    with pytest.raises(ds.DSparkError):
+        ds.library()
+    with pytest.raises(ds.DSparkError):
+        ds.workspace_size(2, 4, 1024)
+
+
 def test_binding_requires_cuda_tensors():
     import torch
     U = torch.zeros(2, 4, 1024)
