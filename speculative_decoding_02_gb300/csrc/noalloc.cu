@@ -1,13 +1,14 @@
 // dspark_markov_draft_noalloc: the Markov draft for callers that cannot
-// allocate device memory at the time they call us.
+// allocate device memory at the time of the call.
 //
-// Some callers cannot hand us a workspace: an inference engine that gives all
-// of HBM to its own pool allocator at start-up and forbids other allocations,
-// a plugin loaded into a host process that passes it no allocator, or code that
-// would otherwise have to call cudaMalloc (which may synchronise the device)
-// in the middle of a latency-critical decode loop.  For them this entry point
-// runs the same draft kernels as dspark_markov_draft, but its scratch space is
-// a fixed array in the library's own device memory instead of a caller buffer.
+// Some callers cannot hand the library a workspace: an inference engine that
+// gives all of HBM to its own pool allocator at start-up and forbids other
+// allocations, a plugin loaded into a host process that passes it no
+// allocator, or code that would otherwise have to call cudaMalloc (which may
+// synchronise the device) in the middle of a latency-critical decode loop.
+// For them this entry point runs the same draft kernels as dspark_markov_draft,
+// but its scratch space is a fixed array in the library's own device memory
+// instead of a caller buffer.
 //
 // The array is a file-scope __device__ variable of DSPARK_NOALLOC_SCRATCH_BYTES
 // bytes.  Every GPU on which the library is loaded holds it until the process
@@ -69,6 +70,7 @@ extern "C" int dspark_markov_draft_noalloc(const float* U, const void* W1, const
   if (B <= 0 || gamma <= 0 || V <= 0 || r <= 0) return DSPARK_ERR_INVALID;
   if (gamma > kMaxGamma) return DSPARK_ERR_UNSUPPORTED;
   if (V % 8 != 0 || r % 16 != 0 || r > 256 || B > 65535) return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)B * (gamma + 1) * (long long)V >= (1ll << 40)) return DSPARK_ERR_UNSUPPORTED;
   if (wdtype != DSPARK_F32 && wdtype != DSPARK_BF16) return DSPARK_ERR_INVALID;
   if (!U || !W1 || !W2 || !anchor || !x_out || !p_out || !lse_out) return DSPARK_ERR_INVALID;
   if (((uintptr_t)U | (uintptr_t)W1 | (uintptr_t)W2) % 16 != 0) return DSPARK_ERR_INVALID;
