@@ -114,6 +114,21 @@ def test_host_side_argument_errors(lib):
     assert lib.dspark_selftest_wait_timeout(0, _fake(0x100010), big, None) == ds.ERR_WORKSPACE
 
 
+def test_noalloc_argument_errors(lib):
+    f = lib.dspark_markov_draft_noalloc
+    vp, i32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+    f.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp]
+    f.restype = i32
+    p = _fake(0x100000)
+    assert f(None, p, p, 1, p, 2, 4, 1024, 16, 0, 0, p, p, p, None) == ds.ERR_INVALID
+    assert f(p, p, p, 1, p, 2, 33, 1024, 16, 0, 0, p, p, p, None) == ds.ERR_UNSUPPORTED
+    assert f(p, p, p, 1, p, 65536, 4, 1024, 16, 0, 0, p, p, p, None) == ds.ERR_UNSUPPORTED
+    # more elements than the 2^40 the kernels' offsets are sized for
+    assert f(p, p, p, 1, p, 1000, 32, 1 << 30, 16, 0, 0, p, p, p, None) == ds.ERR_UNSUPPORTED
+    # scratch larger than the library's fixed array
+    assert f(p, p, p, 1, p, 4096, 32, 1024, 16, 0, 0, p, p, p, None) == ds.ERR_WORKSPACE
+
+
 def test_product_path_never_loads_the_oracle():
     # the package (binding, kernels, library build) imports, links and runs
     # nothing under oracle/: a reference to it may only appear in prose
