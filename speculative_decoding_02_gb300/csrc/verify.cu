@@ -17,7 +17,12 @@
 //                      the rejection.
 // 5. residual          only for rejecting requests: recompute the draft logits
 //                      of the rejected position (bias of x_{k-1} + U row) and
-//                      race Gumbel noise over log max(0, p_t - p_d).
+//                      run the two-level block race over max(0, p_t - p_d)
+//                      (the tensor-core draft kernel in residual mode, or its
+//                      CUDA-core form).
+// 6. verify_residual_finalize  one CTA per request: the corrected token from
+//                      the residual race's key, or, when the residual was
+//                      empty in floating point, a draw from p_t itself.
 #include <algorithm>
 
 #include "kernels.h"
