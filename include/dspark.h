@@ -71,6 +71,10 @@ extern "C" {
 #define DSPARK_SCHED_GREEDY 1  /* greedy Theta maximisation with early stop */
 #define DSPARK_SCHED_TOPK 2    /* dynamic top-K, K = greedy count of round - 2 */
 
+/* flags of dspark_verify_ex and dspark_round_ex */
+#define DSPARK_EARLY_TARGET_STATS 1u  /* the draft took the target rows' softmax statistics */
+#define DSPARK_ADVANCE_ROUND 2u       /* the call's last kernel adds 1 to *round_dev */
+
 /* Bytes of device scratch the entry points below need for these sizes; 0 when
  * a size is not positive. */
 size_t dspark_workspace_size(int B, int gamma, int V);
@@ -90,6 +94,31 @@ int dspark_markov_draft(const float* U, const void* W1, const void* W2, int wdty
                         uint64_t seed, uint64_t round,
                         int32_t* x_out, float* p_out, float* lse_out,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dspark_markov_draft with two additions (both may be NULL, which gives
+ * dspark_markov_draft exactly).
+ *  - T_early [B, gamma+1, V] f32, 16-byte aligned: target logits that the
+ *    caller already holds when the draft starts.  The softmax statistics of
+ *    its rows j < gamma of every request -- the rows verification tests when
+ *    every position is verified ([digest] item 2; [blog] section 1) -- are
+ *    taken while the draft runs, by warps that stream T in the memory time
+ *    the draft leaves idle, and left in the workspace for
+ *    dspark_verify_ex(..., DSPARK_EARLY_TARGET_STATS).  This reads 4 * V bytes
+ *    per row even for rows that the schedule later leaves unverified, so it
+ *    pays when the schedule verifies most positions.  In a serving engine
+ *    the target's logits of a round usually exist only after its draft; the
+ *    flag serves callers that hold them earlier (one micro-batch's verify
+ *    overlapping another's draft, or a replayed round).
+ *  - round_dev: device pointer to the round index (a uint64 < 2^29).  When
+ *    given, the kernels read the round from it when they start and `round` is
+ *    ignored, so that one captured CUDA graph serves consecutive rounds.
+ */
+int dspark_markov_draft_ex(const float* U, const float* T_early, const void* W1, const void* W2,
+                           int wdtype, const int32_t* anchor, int B, int gamma, int V, int r,
+                           uint64_t seed, uint64_t round, const uint64_t* round_dev,
+                           int32_t* x_out, float* p_out, float* lse_out,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Confidence head ([report] Eq.7; [blog] section 5):
@@ -120,7 +149,8 @@ int dspark_confidence(const void* h, int hdtype, const void* W1, int wdtype,
  *   khist[round % 2] after reading it (khist: device [2] i32, caller-owned).
  * FIXED:  l_b = gamma.
  * In:  c [B, gamma] f32 in [0, 1]; sps [n_sps] f32 indexed by batch size,
- *      n_sps > B * (gamma + 1) (not read in FIXED mode).  B * gamma <= 8192.
+ *      n_sps > B * (gamma + 1) (not read in FIXED mode).  B * gamma <= 8192
+ *      (GREEDY and TOPK; FIXED has no limit).
  * Out: ell_out [B] i32, nstar_out [1] i32 (greedy count), theta_out [1] f64
  *      (Theta of the admitted set; 0 in FIXED mode).
  */
@@ -128,6 +158,13 @@ int dspark_schedule(const float* c, int B, int gamma, const float* sps, int n_sp
                     int mode, uint64_t round, int32_t* khist,
                     int32_t* ell_out, int32_t* nstar_out, double* theta_out,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* dspark_schedule with the round index read from the device word *round_dev
+ * when round_dev is not NULL (see dspark_markov_draft_ex). */
+int dspark_schedule_ex(const float* c, int B, int gamma, const float* sps, int n_sps,
+                       int mode, uint64_t round, const uint64_t* round_dev, int32_t* khist,
+                       int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Lossless rejection-sampling verification ([digest] item 2; [blog] section 1).
@@ -150,6 +187,26 @@ int dspark_verify(const float* T, const float* U, const void* W1, const void* W2
                   int B, int gamma, int V, int r, uint64_t seed, uint64_t round,
                   int32_t* n_out, int32_t* tok_out,
                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dspark_verify with options (flags 0 and round_dev NULL give dspark_verify):
+ *  - DSPARK_EARLY_TARGET_STATS: the workspace already holds the softmax
+ *    statistics of the rows j < gamma of this T, left by
+ *    dspark_markov_draft_ex(T_early = T) on the same workspace earlier in
+ *    stream order; the call skips its own pass over those rows.  If no such
+ *    draft preceded it, the kernels record DSPARK_ERR_INVALID.
+ *  - round_dev: the round index as a device word (see dspark_markov_draft_ex).
+ *  - DSPARK_ADVANCE_ROUND (needs round_dev): the call's last kernel adds 1 to
+ *    *round_dev after every kernel of the call has read it.
+ * Other flag bits return DSPARK_ERR_INVALID.
+ */
+int dspark_verify_ex(const float* T, const float* U, const void* W1, const void* W2,
+                     int wdtype, const int32_t* anchor, const int32_t* x,
+                     const float* p_d, const float* lse_d, const int32_t* ell,
+                     int B, int gamma, int V, int r, uint64_t seed, uint64_t round,
+                     uint64_t* round_dev, unsigned flags,
+                     int32_t* n_out, int32_t* tok_out,
+                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Acceptance labels of the verified positions (the study report's label for
@@ -195,7 +252,8 @@ int dspark_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N
  * One whole round: draft, confidence, schedule, verify, enqueued in that order
  * on one stream with no host synchronisation.  Arguments as above.  A round
  * can be captured into a CUDA graph (the draft's cooperative launch
- * included); a replay repeats the captured seed and round.
+ * included); a replay repeats the captured seed and round (dspark_round_ex
+ * with a device round index advances it).
  */
 int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
                  int wdtype, const void* h, int hdtype, const float* w,
@@ -207,6 +265,27 @@ int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
                  int32_t* ell_out, int32_t* nstar_out, double* theta_out,
                  int32_t* n_out, int32_t* tok_out,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dspark_round with the options of the _ex calls: with
+ * DSPARK_EARLY_TARGET_STATS the draft takes the statistics of T's rows
+ * j < gamma while it runs (T is an input of the round) and verification
+ * skips its own pass over them; with round_dev the round index is the device
+ * word *round_dev (`round` ignored), and DSPARK_ADVANCE_ROUND makes the
+ * round's last kernel add 1 to it, so that replaying one captured graph runs
+ * consecutive rounds (the caller refreshes U, T, h and the anchors in place
+ * between replays).
+ */
+int dspark_round_ex(const float* U, const float* T, const void* W1, const void* W2,
+                    int wdtype, const void* h, int hdtype, const float* w,
+                    const float* sts_T, const int32_t* anchor,
+                    int B, int gamma, int V, int r, int H,
+                    const float* sps, int n_sps, int mode, int32_t* khist,
+                    uint64_t seed, uint64_t round, uint64_t* round_dev, unsigned flags,
+                    int32_t* x_out, float* p_out, float* lse_out, float* c_out,
+                    int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                    int32_t* n_out, int32_t* tok_out,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The Markov draft without a caller workspace.  The method has no counterpart:

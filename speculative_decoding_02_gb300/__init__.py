@@ -6,7 +6,9 @@ allocated with torch on that device and every call is enqueued on the current
 torch stream.  If the compiled library is missing, every call raises
 ``DSparkError`` -- there is no CPU fallback.
 
-Entry points (same names as the C ABI in include/dspark.h):
+Entry points (same names as the C ABI in include/dspark.h; the optional
+arguments of markov_draft, schedule, verify and round map to the C ABI's _ex
+forms):
   markov_draft, confidence, schedule, verify, round, read_status,
   acceptance_label, sts_fit
 """
@@ -21,6 +23,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libdspark.so")
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NONFINITE = range(7)
 F32, BF16 = 0, 1
 SCHED_FIXED, SCHED_GREEDY, SCHED_TOPK = 0, 1, 2
+EARLY_TARGET_STATS, ADVANCE_ROUND = 1, 2
 
 
 class DSparkError(RuntimeError):
@@ -46,13 +49,21 @@ def _load():
     L.dspark_workspace_size.restype = sz
     L.dspark_markov_draft.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, sz, vp]
     L.dspark_markov_draft.restype = i32
+    L.dspark_markov_draft_ex.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, vp,
+                                         sz, vp]
+    L.dspark_markov_draft_ex.restype = i32
     L.dspark_confidence.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
     L.dspark_confidence.restype = i32
     L.dspark_schedule.argtypes = [vp, i32, i32, vp, i32, i32, u64, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_schedule.restype = i32
+    L.dspark_schedule_ex.argtypes = [vp, i32, i32, vp, i32, i32, u64, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.dspark_schedule_ex.restype = i32
     L.dspark_verify.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp,
                                 vp, sz, vp]
     L.dspark_verify.restype = i32
+    L.dspark_verify_ex.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, u64, u64, vp,
+                                   ctypes.c_uint, vp, vp, vp, sz, vp]
+    L.dspark_verify_ex.restype = i32
     L.dspark_acceptance_label.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp,
                                           ctypes.c_size_t, vp]
     L.dspark_acceptance_label.restype = i32
@@ -63,6 +74,9 @@ def _load():
     L.dspark_round.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
                                vp, u64, u64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_round.restype = i32
+    L.dspark_round_ex.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
+                                  vp, u64, u64, vp, ctypes.c_uint, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.dspark_round_ex.restype = i32
     L.dspark_read_status.argtypes = [vp, ctypes.POINTER(i32), vp]
     L.dspark_read_status.restype = i32
     L.dspark_selftest_wait_timeout.argtypes = [i32, vp, sz, vp]
@@ -145,8 +159,18 @@ def workspace(B, gamma, V, device):
     return ws[off:off + n]
 
 
-def markov_draft(U, W1, W2, anchor, seed, rnd=0, ws=None):
-    """x [B,G] i32, p [B,G] f32, lse [B,G] f32 = the Markov draft of one round."""
+def _round_dev(round_dev, dev):
+    if round_dev is not None:
+        _need(round_dev, "round_dev", torch.int64, dev)
+        _sized(round_dev, "round_dev", (1,))
+    return _ptr(round_dev)
+
+
+def markov_draft(U, W1, W2, anchor, seed, rnd=0, ws=None, T_early=None, round_dev=None):
+    """x [B,G] i32, p [B,G] f32, lse [B,G] f32 = the Markov draft of one round.
+    T_early [B,G+1,V] f32: target logits whose rows j < G get their softmax
+    statistics into ws while the draft runs (for verify(early_stats=True)).
+    round_dev: int64 [1] device tensor holding the round index (rnd ignored)."""
     L = _load()
     _need(U, "U", torch.float32)
     dev = U.device
@@ -154,12 +178,17 @@ def markov_draft(U, W1, W2, anchor, seed, rnd=0, ws=None):
     _need(W1, "W1", device=dev); _need(W2, "W2", W1.dtype, dev); _need(anchor, "anchor", torch.int32, dev)
     r = W1.shape[-1]
     _sized(W1, "W1", (V, r)); _sized(W2, "W2", (V, r)); _sized(anchor, "anchor", (B,))
+    if T_early is not None:
+        _need(T_early, "T_early", torch.float32, dev)
+        _sized(T_early, "T_early", (B, G + 1, V))
+    rd = _round_dev(round_dev, dev)
     x = torch.empty((B, G), dtype=torch.int32, device=dev)
     p = torch.empty((B, G), dtype=torch.float32, device=dev)
     lse = torch.empty((B, G), dtype=torch.float32, device=dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
-    _check(L.dspark_markov_draft(_ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), B, G, V, r, seed, rnd,
-                                 _ptr(x), _ptr(p), _ptr(lse), _ptr(ws), ws.numel(), _stream(dev)), "markov_draft")
+    _check(L.dspark_markov_draft_ex(_ptr(U), _ptr(T_early), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), B, G,
+                                    V, r, seed, rnd, rd, _ptr(x), _ptr(p), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream(dev)), "markov_draft")
     return x, p, lse
 
 
@@ -183,7 +212,7 @@ def confidence(h, W1, w, anchor, x, sts_T=None):
     return c
 
 
-def schedule(c, sps=None, mode=SCHED_GREEDY, rnd=0, khist=None, ws=None):
+def schedule(c, sps=None, mode=SCHED_GREEDY, rnd=0, khist=None, ws=None, round_dev=None):
     """ell [B] i32, nstar [1] i32, theta [1] f64 from confidences c [B,G]."""
     L = _load()
     _need(c, "c", torch.float32)
@@ -199,13 +228,18 @@ def schedule(c, sps=None, mode=SCHED_GREEDY, rnd=0, khist=None, ws=None):
     theta = torch.empty(1, dtype=torch.float64, device=dev)
     ws = workspace(B, G, 8, dev) if ws is None else ws
     n_sps = 0 if sps is None else sps.numel()
-    _check(L.dspark_schedule(_ptr(c), B, G, _ptr(sps), n_sps, mode, rnd, _ptr(khist), _ptr(ell), _ptr(nstar),
-                             _ptr(theta), _ptr(ws), ws.numel(), _stream(dev)), "schedule")
+    rd = _round_dev(round_dev, dev)
+    _check(L.dspark_schedule_ex(_ptr(c), B, G, _ptr(sps), n_sps, mode, rnd, rd, _ptr(khist), _ptr(ell),
+                                _ptr(nstar), _ptr(theta), _ptr(ws), ws.numel(), _stream(dev)), "schedule")
     return ell, nstar, theta
 
 
-def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None):
-    """n [B] i32 accepted counts, tok [B] i32 corrected / bonus tokens."""
+def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None, early_stats=False, round_dev=None,
+           advance_round=False):
+    """n [B] i32 accepted counts, tok [B] i32 corrected / bonus tokens.
+    early_stats: ws already holds the target-row statistics from
+    markov_draft(T_early=T).  round_dev / advance_round: the round index as a
+    device int64 [1], advanced by the call's last kernel."""
     L = _load()
     _need(T, "T", torch.float32)
     dev = T.device
@@ -224,9 +258,11 @@ def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None):
     n = torch.empty(B, dtype=torch.int32, device=dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
-    _check(L.dspark_verify(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x), _ptr(p_d),
-                           _ptr(lse_d), _ptr(ell), B, G, V, r, seed, rnd, _ptr(n), _ptr(tok), _ptr(ws), ws.numel(),
-                           _stream(dev)), "verify")
+    rd = _round_dev(round_dev, dev)
+    flags = (EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0)
+    _check(L.dspark_verify_ex(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x),
+                              _ptr(p_d), _ptr(lse_d), _ptr(ell), B, G, V, r, seed, rnd, rd, flags, _ptr(n), _ptr(tok),
+                              _ptr(ws), ws.numel(), _stream(dev)), "verify")
     return n, tok
 
 
@@ -306,8 +342,11 @@ class RoundOutputs:
 
 
 def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
-          out=None, ws=None):
+          out=None, ws=None, early_stats=False, round_dev=None, advance_round=False):
     """One whole round (draft, confidence, schedule, verify) on U's device.
+    early_stats: the draft takes the target rows' statistics while it runs.
+    round_dev / advance_round: the round index as a device int64 [1] (rnd
+    ignored), advanced by the round's last kernel.
     Returns a RoundOutputs (device tensors)."""
     L = _load()
     _need(U, "U", torch.float32)
@@ -333,10 +372,13 @@ def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, 
     out.check(B, G, dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
     n_sps = 0 if sps is None else sps.numel()
-    _check(L.dspark_round(_ptr(U), _ptr(T), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h), _dt(h, "h"), _ptr(w),
-                          _ptr(sts_T), _ptr(anchor), B, G, V, r, H, _ptr(sps), n_sps, mode, _ptr(khist), seed, rnd,
-                          _ptr(out.x), _ptr(out.p), _ptr(out.lse), _ptr(out.c), _ptr(out.ell), _ptr(out.nstar),
-                          _ptr(out.theta), _ptr(out.n), _ptr(out.tok), _ptr(ws), ws.numel(), _stream(dev)), "round")
+    rd = _round_dev(round_dev, dev)
+    flags = (EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0)
+    _check(L.dspark_round_ex(_ptr(U), _ptr(T), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h), _dt(h, "h"), _ptr(w),
+                             _ptr(sts_T), _ptr(anchor), B, G, V, r, H, _ptr(sps), n_sps, mode, _ptr(khist), seed,
+                             rnd, rd, flags, _ptr(out.x), _ptr(out.p), _ptr(out.lse), _ptr(out.c), _ptr(out.ell),
+                             _ptr(out.nstar), _ptr(out.theta), _ptr(out.n), _ptr(out.tok), _ptr(ws), ws.numel(),
+                             _stream(dev)), "round")
     return out
 
 

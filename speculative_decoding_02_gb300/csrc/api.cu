@@ -62,8 +62,11 @@ int schedule_checks(const float* c, int B, int gamma, const float* sps, int n_sp
                     const int32_t* khist, const int32_t* ell_out, const int32_t* nstar_out,
                     const double* theta_out) {
   if (B <= 0 || gamma <= 0) return DSPARK_ERR_INVALID;
-  if (gamma > kMaxGamma || (long long)B * gamma > kMaxCandidates) return DSPARK_ERR_UNSUPPORTED;
   if (mode < DSPARK_SCHED_FIXED || mode > DSPARK_SCHED_TOPK) return DSPARK_ERR_INVALID;
+  // the candidate sort holds B * gamma keys in one CTA's shared memory; the
+  // fixed mode sorts nothing
+  if (gamma > kMaxGamma || (mode != DSPARK_SCHED_FIXED && (long long)B * gamma > kMaxCandidates))
+    return DSPARK_ERR_UNSUPPORTED;
   if (!c || !ell_out || !nstar_out || !theta_out) return DSPARK_ERR_INVALID;
   if (mode != DSPARK_SCHED_FIXED && (!sps || (long long)n_sps <= (long long)B * (gamma + 1)))
     return DSPARK_ERR_INVALID;
@@ -92,16 +95,26 @@ size_t dspark_workspace_size(int B, int gamma, int V) {
   return ws_layout(B, gamma, V).total;
 }
 
+int dspark_markov_draft_ex(const float* U, const float* T_early, const void* W1, const void* W2, int wdtype,
+                           const int32_t* anchor, int B, int gamma, int V, int r, uint64_t seed, uint64_t round,
+                           const uint64_t* round_dev, int32_t* x_out, float* p_out, float* lse_out,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
+                          workspace_bytes));
+  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
+  if (T_early && !aligned(T_early, 16)) return DSPARK_ERR_INVALID;
+  DraftArgs a{U, W1, W2, wdtype, anchor, B, gamma, V, r,
+              make_rng_key(seed, round, reinterpret_cast<const unsigned long long*>(round_dev)), x_out, p_out,
+              lse_out, workspace, T_early};
+  return cuda_status(launch_markov_draft(a, (cudaStream_t)stream));
+}
+
 int dspark_markov_draft(const float* U, const void* W1, const void* W2, int wdtype, const int32_t* anchor,
                         int B, int gamma, int V, int r, uint64_t seed, uint64_t round, int32_t* x_out,
                         float* p_out, float* lse_out, void* workspace, size_t workspace_bytes,
                         void* stream) {
-  DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
-                          workspace_bytes));
-  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
-  DraftArgs a{U, W1, W2, wdtype, anchor, B, gamma, V, r, make_rng_key(seed, round), x_out, p_out, lse_out,
-              workspace};
-  return cuda_status(launch_markov_draft(a, (cudaStream_t)stream));
+  return dspark_markov_draft_ex(U, nullptr, W1, W2, wdtype, anchor, B, gamma, V, r, seed, round, nullptr, x_out,
+                                p_out, lse_out, workspace, workspace_bytes, stream);
 }
 
 int dspark_confidence(const void* h, int hdtype, const void* W1, int wdtype, const float* w,
@@ -114,26 +127,47 @@ int dspark_confidence(const void* h, int hdtype, const void* W1, int wdtype, con
                                        nullptr, (cudaStream_t)stream));
 }
 
-int dspark_schedule(const float* c, int B, int gamma, const float* sps, int n_sps, int mode, uint64_t round,
-                    int32_t* khist, int32_t* ell_out, int32_t* nstar_out, double* theta_out, void* workspace,
-                    size_t workspace_bytes, void* stream) {
+int dspark_schedule_ex(const float* c, int B, int gamma, const float* sps, int n_sps, int mode, uint64_t round,
+                       const uint64_t* round_dev, int32_t* khist, int32_t* ell_out, int32_t* nstar_out,
+                       double* theta_out, void* workspace, size_t workspace_bytes, void* stream) {
   DSPARK_TRY(schedule_checks(c, B, gamma, sps, n_sps, mode, khist, ell_out, nstar_out, theta_out));
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return DSPARK_ERR_WORKSPACE;
   int* status = ws_ptr<int>(workspace, 0);
-  return cuda_status(launch_schedule(c, B, gamma, sps, mode, (uint32_t)(round & 0xffffffffu), round >= 2 ? 1 : 0,
-                                     khist, ell_out, nstar_out, theta_out, status, (cudaStream_t)stream));
+  return cuda_status(launch_schedule(c, B, gamma, sps, mode, round,
+                                     reinterpret_cast<const unsigned long long*>(round_dev), khist, ell_out,
+                                     nstar_out, theta_out, status, (cudaStream_t)stream));
+}
+
+int dspark_schedule(const float* c, int B, int gamma, const float* sps, int n_sps, int mode, uint64_t round,
+                    int32_t* khist, int32_t* ell_out, int32_t* nstar_out, double* theta_out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  return dspark_schedule_ex(c, B, gamma, sps, n_sps, mode, round, nullptr, khist, ell_out, nstar_out, theta_out,
+                            workspace, workspace_bytes, stream);
+}
+
+int dspark_verify_ex(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
+                     const int32_t* anchor, const int32_t* x, const float* p_d, const float* lse_d,
+                     const int32_t* ell, int B, int gamma, int V, int r, uint64_t seed, uint64_t round,
+                     uint64_t* round_dev, unsigned flags, int32_t* n_out, int32_t* tok_out, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, n_out, tok_out,
+                           workspace, workspace_bytes));
+  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
+  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND)) return DSPARK_ERR_INVALID;
+  if ((flags & DSPARK_ADVANCE_ROUND) && !round_dev) return DSPARK_ERR_INVALID;
+  unsigned long long* rd = reinterpret_cast<unsigned long long*>(round_dev);
+  VerifyArgs a{T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, make_rng_key(seed, round, rd),
+               n_out, tok_out, workspace, (flags & DSPARK_EARLY_TARGET_STATS) != 0,
+               (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr};
+  return cuda_status(launch_verify(a, (cudaStream_t)stream));
 }
 
 int dspark_verify(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
                   const int32_t* anchor, const int32_t* x, const float* p_d, const float* lse_d,
                   const int32_t* ell, int B, int gamma, int V, int r, uint64_t seed, uint64_t round,
                   int32_t* n_out, int32_t* tok_out, void* workspace, size_t workspace_bytes, void* stream) {
-  DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, n_out, tok_out,
-                           workspace, workspace_bytes));
-  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
-  VerifyArgs a{T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, make_rng_key(seed, round),
-               n_out, tok_out, workspace};
-  return cuda_status(launch_verify(a, (cudaStream_t)stream));
+  return dspark_verify_ex(T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, seed, round, nullptr,
+                          0u, n_out, tok_out, workspace, workspace_bytes, stream);
 }
 
 size_t dspark_sts_workspace_size(int N, int gamma, int ngrid) {
@@ -171,12 +205,12 @@ int dspark_acceptance_label(const float* T, const float* U, const void* W1, cons
                                                 B, gamma, V, ws_ptr<int>(workspace, L.status), s));
 }
 
-int dspark_round(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,
-                 int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B, int gamma, int V,
-                 int r, int H, const float* sps, int n_sps, int mode, int32_t* khist, uint64_t seed,
-                 uint64_t round, int32_t* x_out, float* p_out, float* lse_out, float* c_out, int32_t* ell_out,
-                 int32_t* nstar_out, double* theta_out, int32_t* n_out, int32_t* tok_out, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+int dspark_round_ex(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,
+                    int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B, int gamma, int V,
+                    int r, int H, const float* sps, int n_sps, int mode, int32_t* khist, uint64_t seed,
+                    uint64_t round, uint64_t* round_dev, unsigned flags, int32_t* x_out, float* p_out,
+                    float* lse_out, float* c_out, int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                    int32_t* n_out, int32_t* tok_out, void* workspace, size_t workspace_bytes, void* stream) {
   DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
                           workspace_bytes));
   DSPARK_TRY(confidence_checks(h, hdtype, W1, wdtype, w, anchor, x_out, B, gamma, H, r, V, c_out));
@@ -184,18 +218,34 @@ int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
   DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, n_out,
                            tok_out, workspace, workspace_bytes));
   if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
+  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND)) return DSPARK_ERR_INVALID;
+  if ((flags & DSPARK_ADVANCE_ROUND) && !round_dev) return DSPARK_ERR_INVALID;
   cudaStream_t s = (cudaStream_t)stream;
-  const RngKey key = make_rng_key(seed, round);
+  unsigned long long* rd = reinterpret_cast<unsigned long long*>(round_dev);
+  const RngKey key = make_rng_key(seed, round, rd);
+  const bool early = (flags & DSPARK_EARLY_TARGET_STATS) != 0;
   int* status = ws_ptr<int>(workspace, ws_layout(B, gamma, V).status);
-  DraftArgs da{U, W1, W2, wdtype, anchor, B, gamma, V, r, key, x_out, p_out, lse_out, workspace};
+  DraftArgs da{U, W1, W2, wdtype, anchor, B, gamma, V, r, key, x_out, p_out, lse_out, workspace,
+               early ? T : nullptr};
   DSPARK_TRY(cuda_status(launch_markov_draft(da, s)));
   DSPARK_TRY(cuda_status(launch_confidence(h, hdtype, W1, wdtype, w, sts_T, anchor, x_out, B, gamma, H, r, V,
                                            c_out, status, s)));
-  DSPARK_TRY(cuda_status(launch_schedule(c_out, B, gamma, sps, mode, (uint32_t)(round & 0xffffffffu),
-                                         round >= 2 ? 1 : 0, khist, ell_out, nstar_out, theta_out, status, s)));
+  DSPARK_TRY(cuda_status(launch_schedule(c_out, B, gamma, sps, mode, round, rd, khist, ell_out, nstar_out,
+                                         theta_out, status, s)));
   VerifyArgs va{T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, key, n_out,
-                tok_out, workspace};
+                tok_out, workspace, early, (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr};
   return cuda_status(launch_verify(va, s));
+}
+
+int dspark_round(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,
+                 int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B, int gamma, int V,
+                 int r, int H, const float* sps, int n_sps, int mode, int32_t* khist, uint64_t seed,
+                 uint64_t round, int32_t* x_out, float* p_out, float* lse_out, float* c_out, int32_t* ell_out,
+                 int32_t* nstar_out, double* theta_out, int32_t* n_out, int32_t* tok_out, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  return dspark_round_ex(U, T, W1, W2, wdtype, h, hdtype, w, sts_T, anchor, B, gamma, V, r, H, sps, n_sps, mode,
+                         khist, seed, round, nullptr, 0u, x_out, p_out, lse_out, c_out, ell_out, nstar_out,
+                         theta_out, n_out, tok_out, workspace, workspace_bytes, stream);
 }
 
 int dspark_selftest_wait_timeout(int mode, void* workspace, size_t workspace_bytes, void* stream) {
@@ -221,7 +271,7 @@ const char* dspark_strerror(int status) {
   switch (status) {
     case DSPARK_OK: return "ok";
     case DSPARK_ERR_INVALID: return "invalid argument (null pointer, size or table length)";
-    case DSPARK_ERR_UNSUPPORTED: return "unsupported size (B > 65535, gamma > 32, V % 8, r % 16 or r > 256, B*gamma > 8192)";
+    case DSPARK_ERR_UNSUPPORTED: return "unsupported size (B > 65535, gamma > 32, V % 8, r % 16 or r > 256, B*gamma > 8192 for a sorting schedule)";
     case DSPARK_ERR_CUDA: return "a CUDA launch or runtime call failed";
     case DSPARK_ERR_TIMEOUT: return "a device-side bounded wait gave up";
     case DSPARK_ERR_WORKSPACE: return "workspace missing, misaligned (256 B) or smaller than dspark_workspace_size";

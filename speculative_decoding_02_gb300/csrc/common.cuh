@@ -33,9 +33,14 @@ constexpr uint32_t kPickStreamOffset = 4;
 struct RngKey {
   uint32_t rk0[10], rk1[10];   // round i uses (seed_lo + i A, seed_hi + i B)
   uint32_t round3;             // round << 3
+  // when not null the round index is read from this device word when a kernel
+  // starts (round3 is then ignored), so that one captured CUDA graph can serve
+  // consecutive rounds
+  const unsigned long long* round_dev;
 };
 
-__host__ __device__ inline RngKey make_rng_key(uint64_t seed, uint64_t round) {
+__host__ __device__ inline RngKey make_rng_key(uint64_t seed, uint64_t round,
+                                               const unsigned long long* round_dev = nullptr) {
   RngKey k;
   uint32_t k0 = (uint32_t)(seed & 0xffffffffu), k1 = (uint32_t)(seed >> 32);
   for (int i = 0; i < 10; ++i) {
@@ -45,7 +50,21 @@ __host__ __device__ inline RngKey make_rng_key(uint64_t seed, uint64_t round) {
     k1 += kPhiloxWeylB;
   }
   k.round3 = (uint32_t)(round << 3);
+  k.round_dev = round_dev;
   return k;
+}
+
+// The key of the round that runs: round3 from the device word when the caller
+// keeps the round index in device memory.
+__device__ __forceinline__ RngKey live_key(const RngKey& k) {
+  RngKey r = k;
+  if (k.round_dev != nullptr) r.round3 = (uint32_t)(__ldcg(k.round_dev) << 3);
+  return r;
+}
+
+// The round index a kernel runs (device word or host argument).
+__device__ __forceinline__ unsigned long long live_round(const RngKey& k) {
+  return k.round_dev != nullptr ? __ldcg(k.round_dev) : (unsigned long long)(k.round3 >> 3);
 }
 
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const RngKey& key) {
@@ -203,6 +222,11 @@ __host__ __device__ inline int draft_part_slices(int V) {
   return draft_num_slices(V) > kMaxDraftCtas ? draft_num_slices(V) : kMaxDraftCtas;
 }
 __host__ __device__ inline int verify_num_segs(int V) { return div_up(V, kVerifySeg); }
+// The statistics a draft takes along (one warp per task) use shorter segments,
+// so that the last tasks finish soon after the draft; the partial buffer is
+// sized for the larger count.
+constexpr int kStatsSeg = 16384;
+__host__ __device__ inline int stats_num_segs(int V) { return div_up(V, kStatsSeg); }
 
 // Each argmax key that many CTAs read and raise during a pass sits in its own
 // 128-byte line, so that the traffic of different rows spreads over L2.
@@ -210,15 +234,18 @@ constexpr int kKeyStride = 16;   // u64 slots per key
 
 struct WsLayout {
   size_t status;      // int32 status word
-  size_t counters;    // int32 [8]: [0] verify row count
+  size_t counters;    // int32 [8]: [0] verify row count, [1] draft grid barrier, [2] target-row
+                      // statistics: tasks taken (>= B*gamma*nsegs once rows j < gamma are done)
   size_t draft_keys;  // u64 [gamma][B], kKeyStride apart
   size_t draft_part;  // float2 [gamma][B][nslices]
   size_t rows;        // int32 [B*gamma] row ids b*(gamma+1)+j (j < ell_b) of the rows whose stats verify needs
-  size_t row_part;    // float2 [B*(gamma+1)][nsegs]
+  size_t row_part;    // float2 [B*(gamma+1)][nsegs]: softmax partials of target-row segments
+                      // (kVerifySeg long after verify's own pass, kStatsSeg after a draft's)
   size_t bonus_key;   // u64 [B]
   size_t resid_key;   // u64 [B] residual key, kKeyStride apart
   size_t resid_k;     // int32 [B] rejected position k* (0 = none)
   size_t resid_lse;   // float [B] lse of the target row at k*
+  size_t bonus_rows;  // int32 [1 + B]: count, then the requests that accepted their whole prefix
   size_t total;
 };
 
@@ -233,11 +260,12 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   L.draft_keys = off;  off = align256(off + 8ull * kKeyStride * gamma * B);
   L.draft_part = off;  off = align256(off + 8ull * gamma * draft_part_slices(V) * B);
   L.rows = off;        off = align256(off + 4ull * rows);
-  L.row_part = off;    off = align256(off + 8ull * rows * verify_num_segs(V));
+  L.row_part = off;    off = align256(off + 8ull * rows * stats_num_segs(V));
   L.bonus_key = off;   off = align256(off + 8ull * B);
   L.resid_key = off;   off = align256(off + 8ull * kKeyStride * B);
   L.resid_k = off;     off = align256(off + 4ull * B);
   L.resid_lse = off;   off = align256(off + 4ull * B);
+  L.bonus_rows = off;  off = align256(off + 4ull * (B + 1));
   L.total = off;
   return L;
 }

@@ -27,9 +27,10 @@ template <int WDT>
 __global__ void __launch_bounds__(kThreads)
 draft_step_cuda_core(const float* __restrict__ U, const void* __restrict__ W1,
                      const void* __restrict__ W2, const int32_t* __restrict__ prev_tok,
-                     int prev_stride, int B, int G, int V, int r, int k, RngKey key,
+                     int prev_stride, int B, int G, int V, int r, int k, RngKey key_arg,
                      float2* __restrict__ part, unsigned long long* __restrict__ keys,
                      int* __restrict__ status) {
+  const RngKey key = live_key(key_arg);
   extern __shared__ float smem[];
   float* Es = smem;                          // [kRowsPerCta][r]
   float* Ws = Es + kRowsPerCta * r;          // [kColsPerTile][r + 1]
@@ -195,7 +196,14 @@ cudaError_t run_draft(const DraftArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream) {
   if (draft_tc_supported(a.wdtype, a.r, a.V)) return launch_markov_draft_tc(a, stream);
-  return a.wdtype == DSPARK_BF16 ? run_draft<DSPARK_BF16>(a, stream) : run_draft<DSPARK_F32>(a, stream);
+  // the target-statistics marker is cleared by every draft (set again below
+  // when this call takes the statistics)
+  const WsLayout L = ws_layout(a.B, a.gamma, a.V);
+  cudaError_t e = cudaMemsetAsync(ws_ptr<unsigned int>(a.ws, L.counters) + 2, 0, sizeof(unsigned int), stream);
+  if (e != cudaSuccess) return e;
+  e = a.wdtype == DSPARK_BF16 ? run_draft<DSPARK_BF16>(a, stream) : run_draft<DSPARK_F32>(a, stream);
+  if (e == cudaSuccess && a.T_stats != nullptr) e = launch_row_stats(a.T_stats, nullptr, a.B, a.gamma, a.V, a.ws, stream);
+  return e;
 }
 
 }  // namespace dspark

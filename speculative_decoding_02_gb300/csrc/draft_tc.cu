@@ -66,8 +66,10 @@ constexpr int kAtoms = KR / 64;     // 64-wide K atoms (128 bytes of bf16)
 constexpr int kWStages = 4;         // W2 atom ring (one MMA's worth)
 constexpr int kUStages = 3;         // U tile ring
 constexpr int kUBox = 32;           // fp32 columns per U box (128 bytes, swizzled)
-constexpr int kThreads = 576;
 constexpr int kEpiWarps = 16;       // four warps per TMEM lane quarter
+constexpr int kStatsWarps = 2;      // draft mode: warps that stream target-row statistics
+constexpr int kThreads = 64 + 32 * kEpiWarps;                 // residual and label modes
+constexpr int kDraftThreads = kThreads + 32 * kStatsWarps;    // draft mode (640 x 96 registers fit)
 constexpr uint32_t kTmemCols = 512;  // two accumulators, then E
 constexpr uint32_t kTmemE = 2 * kAccCols;   // first TMEM column of E (128 x 256 bf16)
 
@@ -80,10 +82,12 @@ constexpr int kBarBytes = 512;                   // mbarriers and flags
 constexpr int kWStagesRes = 2;
 constexpr int kResStageBytes = 2 * BM * 256;      // U then T
 constexpr int kGkBytes = 2 * BM * 16;   // row-key copies: [position parity][row], 16 bytes each
-constexpr int kSmemBytes =
-    1024 /*align*/ + kWStages * kWStageBytes + kUStages * kUStageBytes + kBarBytes + kXBytes + kGkBytes;
-static_assert(kWStagesRes * kWStageBytes + 2 * kResStageBytes <= kWStages * kWStageBytes + kUStages * kUStageBytes,
-              "residual layout must fit the draft layout");
+// the rings: draft mode W2 and U; residual and label modes W2 and the U/T row
+// stages, in the same space
+constexpr int kDraftRingBytes = kWStages * kWStageBytes + kUStages * kUStageBytes;
+constexpr int kResRingBytes = kWStagesRes * kWStageBytes + 2 * kResStageBytes;
+constexpr int kRingBytes = kDraftRingBytes > kResRingBytes ? kDraftRingBytes : kResRingBytes;
+constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + kBarBytes + kXBytes + kGkBytes;
 
 struct __align__(8) Barriers {
   uint64_t full_w[kWStages], empty_w[kWStages];
@@ -99,6 +103,9 @@ static_assert(sizeof(Barriers) <= kBarBytes, "barrier block overflows its shared
 static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may use");
 
 enum Mode { kDraft = 0, kResidual = 1, kLabel = 2 };
+
+template <int MODE>
+__host__ __device__ constexpr int threads_of() { return MODE == kDraft ? kDraftThreads : kThreads; }
 
 struct StepParams {
   const float* U;
@@ -123,6 +130,13 @@ struct StepParams {
   const float2* row_part;
   float* label;
   int k_fixed, nsegs;
+  // draft mode: softmax partials of the target rows j < G of every request,
+  // taken while the draft runs (T_stats null: none); stats_part is the
+  // [B*(G+1)][nsegs] partial buffer of verification, stats_next a task counter
+  // zeroed before the launch
+  const float* T_stats;
+  float2* stats_part;
+  unsigned int* stats_next;
   unsigned long long* keys;             // [G][B] argmax keys of every position, kKeyStride apart
   float2* part;                         // [G][part_slices][B] softmax partials
   unsigned int* gbar;                   // grid-barrier counter (zeroed before launch)
@@ -259,21 +273,24 @@ __device__ __forceinline__ void race_seed(RowRace& st, float (&l)[CPP], const ui
       if (q == bq) l[4 * q + c] = -INFINITY;
 }
 
-// Rare path of the screen.  Moves the running maximum up to this tile's if it
-// is exceeded, recomputes the tile's softmax terms against it, rebuilds the
-// block candidate mask, parks the terms in `spill` (block q in 16-byte chunk
-// j0 + q, swizzled) and resolves the candidates one by one with the full
-// 23-bit uniforms; a block that wins draws its token and tightens the bound
-// for the rest.  Returns the tile's softmax sum.
+// Rare path of the screen.  When the screen's sum of the tile's softmax terms
+// overflowed (`raise`), moves the running maximum up to this tile's and
+// recomputes the terms against it; otherwise the terms are the screen's own,
+// so that the softmax state depends on the logits alone and not on when
+// another CTA's threshold arrived.  Rebuilds the block candidate mask, parks
+// the terms in `spill` (block q in 16-byte chunk j0 + q, swizzled) and
+// resolves the candidates one by one with the full 23-bit uniforms; a block
+// that wins draws its token and tightens the bound for the rest.  Returns the
+// tile's softmax sum.
 template <int CPP>
 __device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP], const uint32_t (&wb)[CPP / 4],
                                               int v0, unsigned char* spill, int j0, int sw, const RngKey& key,
-                                              uint32_t req, uint32_t pos, int* status) {
+                                              uint32_t req, uint32_t pos, int* status, bool raise) {
   constexpr int NB = CPP / 4;
   float tm = l[0];
 #pragma unroll
   for (int c = 1; c < CPP; ++c) tm = fmaxf(tm, l[c]);
-  if (tm > st.run_m) {
+  if (raise && tm > st.run_m) {
     st.run_s *= exp2f((st.run_m - tm) * kLog2e);
     st.run_m = tm;
     st.bound = race_bound(st.run_m, st.zthr);
@@ -315,7 +332,7 @@ __device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP]
 // Screens this tile's blocks against the best perturbed log-mass known for the
 // row (zthr) and adds their softmax terms e_v = exp(l_v - run_m) (run_m may lag
 // the true maximum: the terms are then above 1, which the merge of the
-// partials allows).  With the block's mass s_q and the high 16 bits h of its
+// partials allows; it is raised only when they overflow).  With the block's mass s_q and the high 16 bits h of its
 // uniform: E_q = -log u_q > (65535 - h) / 65536, so the block can only win
 // when h + 65536 s_q bound > 65535, with bound = exp(run_m - zthr) (2^-10
 // over).  Only the largest left-hand side is kept; a tile that may hold a
@@ -338,8 +355,9 @@ __device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], 
     s += sq;
     smax = fmaxf(smax, fmaf(sq, b16, block_hf(wb[q])));
   }
-  if (smax > kScreenThr || !(s <= 3.0e38f))
-    s = race_resolve<CPP>(st, l, wb, v0, spill, j0, sw, key, req, pos, status);
+  const bool overflow = !(s <= 3.0e38f);
+  if (smax > kScreenThr || overflow)
+    s = race_resolve<CPP>(st, l, wb, v0, spill, j0, sw, key, req, pos, status, overflow);
   st.run_s += s;
 }
 
@@ -505,6 +523,88 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* counter, uint32_t tar
   return grid_wait(counter, target, abort, status);
 }
 
+// Target-row statistics riding along the draft.  Verification needs the
+// softmax normaliser of every target row it tests; those rows depend only on
+// T, so when the caller already holds T they can be streamed while the draft
+// runs, in the HBM time the draft leaves idle.  Each warp takes (row,
+// segment) tasks from a shared counter -- rows j < G of every request,
+// kStatsSeg entries per segment -- and leaves the segment's (max, sum of exp)
+// in part[row][seg].  A segment is read in pieces of 2048 entries (16 float4
+// per lane, all in flight before any arithmetic), with loads marked for early
+// eviction from L2: W2, which every draft position re-reads from L2, must not
+// be pushed out by a stream that is read once.
+constexpr int kStatsLoadsWarp = 16;   // float4 per lane per piece of a warp that loads for itself
+
+// The (max, sum of exp) of one piece of a row, folded into a lane's running
+// state (x: this lane's entries, -inf past the row's end).
+template <int N>
+__device__ __forceinline__ void stats_fold(float& m, float& s, const float4 (&x)[N], bool& bad) {
+  float bm = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < N; ++i) bm = fmaxf(fmaxf(bm, fmaxf(x[i].x, x[i].y)), fmaxf(x[i].z, x[i].w));
+  bad |= !(bm < INFINITY);
+  if (bm > m) {
+    s = (m == -INFINITY) ? 0.f : s * ex2_approx((m - bm) * kLog2e);
+    m = bm;
+  }
+  if (m == -INFINITY) return;
+  const float mb = m * kLog2e;
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    acc += (ex2_approx(fmaf(x[i].x, kLog2e, -mb)) + ex2_approx(fmaf(x[i].y, kLog2e, -mb))) +
+           (ex2_approx(fmaf(x[i].z, kLog2e, -mb)) + ex2_approx(fmaf(x[i].w, kLog2e, -mb)));
+  s += acc;
+}
+
+// Row and segment of statistics task t.
+__device__ __forceinline__ void stats_task_at(int t, int G, int nsegs, size_t& rowid, int& seg) {
+  const int ri = t / nsegs;
+  seg = t - ri * nsegs;
+  const int b = ri / G, j = ri - b * G;
+  rowid = (size_t)b * (G + 1) + j;
+}
+
+// One warp, whole tasks with its own loads: kStatsLoadsWarp float4 per lane
+// per piece, all in flight before any arithmetic, marked for early eviction
+// from L2 (W2, which every draft position re-reads from L2, must not be
+// pushed out by a stream read once).  The next task index is fetched while a
+// task runs.
+__device__ void stats_tasks(const float* __restrict__ T, int B, int G, int V, int nsegs,
+                            float2* __restrict__ part, unsigned int* next, volatile int* abort, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int ntasks = B * G * nsegs;
+  const uint64_t pol = policy_evict_first();
+  bool bad = false;
+  unsigned int t = 0;
+  if (lane == 0) t = atomicAdd(next, 1u);
+  t = __shfl_sync(0xffffffffu, t, 0);
+  while ((int)t < ntasks && !*abort) {
+    unsigned int t_next = 0;
+    if (lane == 0) t_next = atomicAdd(next, 1u);   // its reply is needed only at the next task
+    size_t rowid;
+    int seg;
+    stats_task_at((int)t, G, nsegs, rowid, seg);
+    const float* row = T + rowid * V;
+    const int v0 = seg * kStatsSeg, v1 = min(V, v0 + kStatsSeg);
+    float m = -INFINITY, s = 0.f;
+#pragma unroll 1
+    for (int vp = v0; vp < v1; vp += 32 * 4 * kStatsLoadsWarp) {
+      float4 x[kStatsLoadsWarp];
+#pragma unroll
+      for (int i = 0; i < kStatsLoadsWarp; ++i) {
+        const int v = vp + 4 * (lane + 32 * i);
+        x[i] = v < v1 ? ld_stream_f4(row + v, pol) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      stats_fold(m, s, x, bad);
+    }
+    warp_softmax_reduce(m, s, 0xffffffffu, 32);
+    if (lane == 0) part[rowid * nsegs + seg] = make_float2(m, s);
+    t = __shfl_sync(0xffffffffu, t_next, 0);
+  }
+  if (bad) record_status(status, DSPARK_ERR_NONFINITE);
+}
+
 // The draft outputs of one (request, position), by one warp: merge the slice
 // partials into lse_k, decode x_k from its argmax key and recompute the fused
 // logit of x_k for p_k(x_k).
@@ -556,7 +656,7 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
 // MODE kLabel: the same at position k_fixed, adding sum_v min(p_d, p_t) of
 // each row into label[b][k_fixed - 1] (one atomicAdd per CTA and row).
 template <int R, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<MODE>(), 1)
 draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
               const StepParams p) {
   constexpr int kRepl = BM / R;            // copies of each request row
@@ -567,7 +667,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   constexpr int kWSt = MODE == kDraft ? kWStages : kWStagesRes;   // W2 ring depth of this mode
   unsigned char* W_s = smem;
   unsigned char* U_s = W_s + kWSt * kWStageBytes;      // draft: U ring; residual: U/T row stages
-  Barriers* bars = reinterpret_cast<Barriers*>(W_s + kWStages * kWStageBytes + kUStages * kUStageBytes);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + kRingBytes);
   unsigned char* X_s = reinterpret_cast<unsigned char*>(bars) + kBarBytes;   // combine scratch
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -580,6 +680,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   const int ntl = t1 - t0;
   const int kf = p.k_first, kl = p.k_last;
   volatile int* abort = &bars->abort;
+  const RngKey key = live_key(p.key);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) { mbar_init(&bars->full_w[s], 1); mbar_init(&bars->empty_w[s], 1); }
@@ -596,7 +697,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     if (MODE == kDraft) prefetch_tensormap(&u_map);
   }
   if (warp == 1) tmem_alloc(&bars->tmem_base, kTmemCols);
-  for (int idx = threadIdx.x; idx < kGkBytes / 16; idx += kThreads)
+  for (int idx = threadIdx.x; idx < kGkBytes / 16; idx += threads_of<MODE>())
     reinterpret_cast<uint4*>(X_s + kXBytes)[idx] = make_uint4(0u, 0u, 0u, 0u);
   tc_fence_before();
   __syncthreads();
@@ -686,7 +787,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       mbar_drain(&bars->drain, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;               // TMEM lane quarter of this warp
     const int h = (warp - 2) >> 2;        // which of the four warps of the quarter
@@ -853,9 +954,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
               for (int c = 0; c < CPP; ++c)
                 if (c >= nv) v[c] = -INFINITY;
             }
-            block_words<CPP>(wb, p.key, kStreamDraft, (uint32_t)b, (uint32_t)k, v0);
+            block_words<CPP>(wb, key, kStreamDraft, (uint32_t)b, (uint32_t)k, v0);
             if (st.run_m == -INFINITY) race_prep<CPP>(st, v);
-            if (st.zbest == -INFINITY) race_seed<CPP>(st, v, wb, v0, p.key, (uint32_t)b, (uint32_t)k);
+            if (st.zbest == -INFINITY) race_seed<CPP>(st, v, wb, v0, key, (uint32_t)b, (uint32_t)k);
           }
           if (i == 0) {
             // the parts of a row pool their seeds before the first screen
@@ -886,7 +987,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                 }
               }
             }
-            race_screen<CPP>(st, v, wb, v0, urow, j0, r & 7, p.key, (uint32_t)b, (uint32_t)k, p.status);
+            race_screen<CPP>(st, v, wb, v0, urow, j0, r & 7, key, (uint32_t)b, (uint32_t)k, p.status);
             // share this thread's progress with the other CTAs of the row
             if (kShare && st.best_v >= 0 && st.zbest > st.zpub && st.zbest >= st.zthr) {
               atomicMax(row_key, argmax_key(st.zbest, st.best_v));
@@ -933,7 +1034,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                 const unsigned long long gkr = *reinterpret_cast<volatile unsigned long long*>(&gk_rows[r].x);
                 if (gkr) resid_raise(rs, argmax_key_value(gkr));
               }
-              resid_tile<CPP>(rs, uu, nv, v0, urow, j0, sw, p.key, (uint32_t)b, (uint32_t)ks);
+              resid_tile<CPP>(rs, uu, nv, v0, urow, j0, sw, key, (uint32_t)b, (uint32_t)ks);
               if (kShareRes && rs.best_v >= 0 && rs.zbest > rs.zpub && rs.zbest >= rs.zthr) {
                 atomicMax(res_key, argmax_key(rs.zbest, rs.best_v));
                 rs.zpub = rs.zbest;
@@ -1053,7 +1154,17 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                           p.part_slices, p.x_out, p.p_out, p.lse_out, p.status);
         }
       }
+      // the draft is done: the epilogue warps help with whatever target-row
+      // statistics are left
+      if (p.T_stats != nullptr)
+        stats_tasks(p.T_stats, p.B, p.G, p.V, p.nsegs, p.stats_part, p.stats_next, abort, p.status);
     }
+  } else {
+    // ------------------------------------------------------------ statistics
+    // (draft mode only: the warps past the epilogue).  Their loads bypass the
+    // SM's bulk-copy engine, which the draft's U and W2 tiles keep busy.
+    if (p.T_stats != nullptr)
+      stats_tasks(p.T_stats, p.B, p.G, p.V, p.nsegs, p.stats_part, p.stats_next, abort, p.status);
   }
 
   tc_fence_before();
@@ -1182,7 +1293,8 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * kKeyStride * (size_t)a.gamma * a.B, stream);
   if (e != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(gbar, 0, sizeof(unsigned int), stream)) != cudaSuccess) return e;
+  // the grid-barrier counter and the target-statistics task counter after it
+  if ((e = cudaMemsetAsync(gbar, 0, 2 * sizeof(unsigned int), stream)) != cudaSuccess) return e;
 
   const int mtiles = div_up(a.B, R);
   const int ntiles = div_up(a.V, BN);
@@ -1204,18 +1316,24 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   sp.ctas_per_mtile = per;
   sp.ntiles = ntiles;
   sp.key = a.key;
+  sp.nsegs = stats_num_segs(a.V);
+  sp.stats_part = ws_ptr<float2>(a.ws, L.row_part);
+  sp.stats_next = gbar + 1;
 
   // One persistent launch over all positions when every CTA can be resident
   // at once (one CTA per SM); otherwise one launch per position.
   int resident = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, kThreads, kSmemBytes)) != cudaSuccess)
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, kDraftThreads, kSmemBytes)) !=
+      cudaSuccess)
     return e;
   if (coop && nctas <= resident * sms) {
     sp.k_first = 1;
     sp.k_last = a.gamma;
+    // the target-row statistics ride along in the statistics warps
+    sp.T_stats = a.T_stats;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(nctas);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kDraftThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1231,11 +1349,15 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   } else {
     for (int k = 1; k <= a.gamma; ++k) {
       sp.k_first = sp.k_last = k;
-      kern<<<nctas, kThreads, kSmemBytes, stream>>>(map, umap, sp);
+      kern<<<nctas, kDraftThreads, kSmemBytes, stream>>>(map, umap, sp);
     }
     draft_finalize_tc<<<div_up(a.B * a.gamma * 32, 256), 256, 0, stream>>>(
         a.U, static_cast<const __nv_bfloat16*>(a.W1), static_cast<const __nv_bfloat16*>(a.W2), a.anchor, keys,
         part, a.B, a.gamma, a.V, per, part_slices, a.x_out, a.p_out, a.lse_out, status);
+    // one launch per position: the target-row statistics follow the draft
+    if (a.T_stats != nullptr && (e = cudaGetLastError()) == cudaSuccess)
+      e = launch_row_stats(a.T_stats, nullptr, a.B, a.gamma, a.V, a.ws, stream);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

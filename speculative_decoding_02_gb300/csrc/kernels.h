@@ -21,6 +21,9 @@ struct DraftArgs {
   float* p_out;
   float* lse_out;
   void* ws;
+  // optional: target logits [B, gamma+1, V] whose rows j < gamma get their
+  // softmax statistics into the workspace during (or right after) the draft
+  const float* T_stats;
 };
 
 struct VerifyArgs {
@@ -39,6 +42,11 @@ struct VerifyArgs {
   int32_t* n_out;
   int32_t* tok_out;
   void* ws;
+  // the draft already left the statistics of the target rows j < gamma in the
+  // workspace (DraftArgs::T_stats): skip the row pass
+  bool stats_ready;
+  // when not null, the round's last kernel adds 1 to this device round index
+  unsigned long long* advance_round;
 };
 
 cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream);
@@ -66,7 +74,8 @@ cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const voi
                                        int G, int V, int* status, cudaStream_t stream);
 
 // The softmax partials of the target rows j < ell_b of every request into the
-// workspace (verify's first two kernels).
+// workspace (verify's first two kernels); ell == nullptr takes every row
+// j < gamma and marks the statistics as complete for a later verify.
 cudaError_t launch_row_stats(const float* T, const int32_t* ell, int B, int gamma, int V, void* ws,
                              cudaStream_t stream);
 
@@ -87,9 +96,10 @@ cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdt
 
 size_t schedule_smem_bytes(int B, int gamma);
 
+// `round` is the round index unless round_dev (a device word) is given.
 cudaError_t launch_schedule(const float* c, int B, int gamma, const float* sps, int mode,
-                            uint32_t round_lo, int round_ge2, int32_t* khist, int32_t* ell_out,
-                            int32_t* nstar_out, double* theta_out, int* status,
+                            unsigned long long round, const unsigned long long* round_dev, int32_t* khist,
+                            int32_t* ell_out, int32_t* nstar_out, double* theta_out, int* status,
                             cudaStream_t stream);
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream);

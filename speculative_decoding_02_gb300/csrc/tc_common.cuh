@@ -119,6 +119,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) from global memory into L2 (16-byte
+// aligned address, size % 16 == 0); nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// 16-byte load that bypasses L1 and is marked for early eviction from L2
+// (`policy` from policy_evict_first), so that a stream read once does not push
+// longer-lived lines out of L2.
+__device__ __forceinline__ float4 ld_stream_f4(const float* p, uint64_t policy) {
+  float4 v;
+  asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
 // 2-D tiled tensor copy global -> shared; c0 is the innermost coordinate.
 __device__ __forceinline__ void tma_g2s_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
                                            uint64_t policy) {

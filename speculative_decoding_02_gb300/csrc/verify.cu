@@ -8,21 +8,24 @@
 // 2. verify_row_stats  the streaming pass: every (row, segment) task reads one
 //                      kVerifySeg-long piece of a listed row with 16-byte
 //                      loads and leaves an online-softmax partial.
-// 3. verify_bonus_race every request's row j = ell_b: the Gumbel race of the
-//                      bonus token (a separate kernel, so that the streaming
-//                      pass stays light enough for high occupancy).
-// 4. verify_decide     one warp per request, one lane per position: merge the
+// 3. verify_decide     one warp per request, one lane per position: merge the
 //                      partials into lse_t, form p_t(x_k) / p_d(x_k), compare
 //                      it with the accept uniform; the first failing lane is
 //                      the rejection.
+// 4. verify_bonus_race only for requests that accepted their whole prefix: the
+//                      race of the bonus token over row j = ell_b (the other
+//                      requests never need that row).
 // 5. residual          only for rejecting requests: recompute the draft logits
 //                      of the rejected position (bias of x_{k-1} + U row) and
 //                      run the two-level block race over max(0, p_t - p_d)
 //                      (the tensor-core draft kernel in residual mode, or its
 //                      CUDA-core form).
-// 6. verify_residual_finalize  one CTA per request: the corrected token from
-//                      the residual race's key, or, when the residual was
-//                      empty in floating point, a draw from p_t itself.
+// 6. verify_residual_finalize  one CTA per request: the bonus token, or the
+//                      corrected token from the residual race's key, or, when
+//                      the residual was empty in floating point, a draw from
+//                      p_t itself.
+// Steps 1-2 are skipped when the draft already took the statistics of every
+// row j < gamma (the caller held T when the draft started).
 #include <algorithm>
 
 #include "kernels.h"
@@ -39,8 +42,11 @@ __device__ __forceinline__ float exp2_fast(float x) {
   return y;
 }
 
+// ell == nullptr lists every row j < G and marks the statistics of those
+// rows as complete (counters[2] = the number of row segments), the state a
+// draft that took them along leaves behind.
 __global__ void __launch_bounds__(1024)
-verify_prep(const int32_t* __restrict__ ell, int B, int G, int32_t* __restrict__ rows,
+verify_prep(const int32_t* __restrict__ ell, int B, int G, int nsegs, int32_t* __restrict__ rows,
             int* __restrict__ counters, int* __restrict__ status) {
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -48,7 +54,7 @@ verify_prep(const int32_t* __restrict__ ell, int B, int G, int32_t* __restrict__
   const int lo = tid * chunk, hi = min(B, lo + chunk);
   int run = 0;
   for (int b = lo; b < hi; ++b) {
-    int L = ell[b];
+    int L = ell ? ell[b] : G;
     if (L < 0 || L > G) {
       record_status(status, DSPARK_ERR_INVALID);
       L = L < 0 ? 0 : G;
@@ -73,10 +79,13 @@ verify_prep(const int32_t* __restrict__ ell, int B, int G, int32_t* __restrict__
   __syncthreads();
   int pos = (incl - run) + (wid > 0 ? warp_tot[wid - 1] : 0);
   for (int b = lo; b < hi; ++b) {
-    const int L = min(max(ell[b], 0), G);
+    const int L = ell ? min(max(ell[b], 0), G) : G;
     for (int j = 0; j < L; ++j) rows[pos++] = b * (G + 1) + j;
   }
-  if (tid == 1023) counters[0] = pos;
+  if (tid == 1023) {
+    counters[0] = pos;
+    if (!ell) counters[2] = B * G * nsegs;
+  }
 }
 
 // Block-wide (max, sum) of per-thread online-softmax states: the maximum
@@ -105,17 +114,19 @@ __device__ __forceinline__ float2 block_softmax(float m, float s, float* s_red) 
 
 // Softmax statistics of the target rows the accept tests need (rows j < ell[b]
 // of every request, listed by verify_prep).  One (row, segment) task per
-// iteration: kVerifySeg entries of a row, read as batches of eight 16-byte
+// iteration: seg_len entries of a row (kVerifySeg, or kStatsSeg for the
+// layout a draft leaves when it takes the statistics along; a multiple of
+// 8 * 4 * kRowThreads), read as batches of eight 16-byte
 // loads per thread (all issued before any arithmetic), folded into an online
 // softmax.  Few registers, so that many CTAs per SM keep enough loads in
 // flight to stream T at the HBM rate.
 __global__ void __launch_bounds__(kRowThreads)
-verify_row_stats(const float* __restrict__ T, int V, int nsegs, const int32_t* __restrict__ rows,
+verify_row_stats(const float* __restrict__ T, int V, int nsegs, int seg_len, const int32_t* __restrict__ rows,
                  const int* __restrict__ counters, float2* __restrict__ row_part, int* __restrict__ status) {
   __shared__ float s_red[kRowThreads / 32];
   constexpr int kBatch = 8;                                     // float4 loads per batch
   constexpr int kStride = 4 * kRowThreads;                      // entries between a thread's loads
-  constexpr int kBatches = kVerifySeg / (kBatch * kStride);
+  const int nbatches = seg_len / (kBatch * kStride);
   const int nrows = counters[0];
   const int tid = threadIdx.x;
   const int ntasks = nrows * nsegs;
@@ -124,10 +135,10 @@ verify_row_stats(const float* __restrict__ T, int V, int nsegs, const int32_t* _
     const int ri = t / nsegs, seg = t - ri * nsegs;
     const int rowid = rows[ri];
     const float* Trow = T + (size_t)rowid * V;
-    const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
+    const int v0 = seg * seg_len, v1 = min(V, v0 + seg_len);
     float m = -INFINITY, s = 0.f;
 #pragma unroll 1
-    for (int bt = 0; bt < kBatches; ++bt) {
+    for (int bt = 0; bt < nbatches; ++bt) {
       const int vb = v0 + bt * kBatch * kStride + 4 * tid;
       if (vb >= v1) break;
       float4 t4[kBatch];
@@ -165,10 +176,10 @@ __device__ __forceinline__ float block_hf_v(uint32_t w) {
 }
 constexpr float kScreenThrV = 8454142.0f;   // 2^23 + 65534 (see the draft race)
 
-// The bonus draw of every request from its row j = ell[b] (the bonus token if
-// the whole prefix survives, [blog] section 1): the two-level draw from
-// softmax(T[b, j, :]) on streams 3 and 7, one (request, segment) task per
-// iteration.  A thread takes 16 consecutive tokens at a time (four blocks, one
+// The bonus draw of every request that accepted its whole prefix (listed by
+// verify_decide in bonus_rows), from its row j = ell[b] ([blog] section 1):
+// the two-level draw from softmax(T[b, j, :]) on streams 3 and 7, one
+// (listed request, kBonusSeg-long segment) task per iteration.  A thread takes 16 consecutive tokens at a time (four blocks, one
 // Philox call): the block weights exp(T - m) against the running maximum m,
 // a screen of each block on its 16 high random bits, exact values for the
 // rare candidates and the token inside a block that takes the lead.
@@ -180,21 +191,27 @@ __device__ __forceinline__ void load_chunk16(const float* __restrict__ row, int 
                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 }
 
+constexpr int kBonusSeg = 8192;   // vocabulary entries per bonus-race task
+
 __global__ void __launch_bounds__(kRowThreads)
-verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, int B, int G, int V, int nsegs,
-                  RngKey key, unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
+verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
+                  const int32_t* __restrict__ bonus_rows, int G, int V, int nsegs, RngKey key_arg,
+                  unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
+  const int nrows = bonus_rows[0];
+  if ((int)blockIdx.x >= nrows * nsegs) return;
+  const RngKey key = live_key(key_arg);
   __shared__ unsigned long long s_k[kRowThreads / 32];
-  constexpr int kChunks = kVerifySeg / (16 * kRowThreads);
+  constexpr int kChunks = kBonusSeg / (16 * kRowThreads);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int ntasks = B * nsegs;
+  const int ntasks = nrows * nsegs;
   bool bad = false;
   for (int t = blockIdx.x; t < ntasks; t += gridDim.x) {
-    const int b = t / nsegs, seg = t - b * nsegs;
+    const int b = bonus_rows[1 + t / nsegs], seg = t - (t / nsegs) * nsegs;
     const int jrow = min(max(ell[b], 0), G);
     const int rowid = b * (G + 1) + jrow;
     const uint32_t pos = (uint32_t)(jrow + 1);
     const float* Trow = T + (size_t)rowid * V;
-    const int v0 = seg * kVerifySeg, v1 = min(V, v0 + kVerifySeg);
+    const int v0 = seg * kBonusSeg, v1 = min(V, v0 + kBonusSeg);
     // zbest: this thread's best perturbed log-mass (bestv its token); zthr:
     // the best known in the warp, a value some lane has reached, which the
     // screen compares against (bound = exp(m - zthr), 2^-10 over)
@@ -296,14 +313,16 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell, 
 
 __global__ void verify_decide(const float* __restrict__ T, const int32_t* __restrict__ x,
                               const float* __restrict__ p_d, const int32_t* __restrict__ ell, int B,
-                              int G, int V, int nsegs, RngKey key,
+                              int G, int V, int nsegs, RngKey key_arg,
                               const float2* __restrict__ row_part,
-                              const unsigned long long* __restrict__ bonus_key,
                               int32_t* __restrict__ resid_k, float* __restrict__ resid_lse,
-                              int32_t* __restrict__ n_out, int32_t* __restrict__ tok_out,
-                              int* __restrict__ status) {
+                              int32_t* __restrict__ n_out, int32_t* __restrict__ bonus_rows,
+                              const int* __restrict__ stats_done, int* __restrict__ status) {
+  const RngKey key = live_key(key_arg);
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  // statistics taken by the draft: they must cover every row j < G
+  if (stats_done && b == 0 && lane == 0 && *stats_done < B * G * nsegs) record_status(status, DSPARK_ERR_INVALID);
   if (b >= B) return;
   const int L = min(max(ell[b], 0), G);
   bool reject = false;
@@ -327,15 +346,9 @@ __global__ void verify_decide(const float* __restrict__ T, const int32_t* __rest
   const float lse_n = __shfl_sync(0xffffffffu, lse_t, n & 31);
   if (lane == 0) {
     n_out[b] = n;
-    if (n < L) {
-      resid_k[b] = n + 1;
-      resid_lse[b] = lse_n;
-    } else {
-      resid_k[b] = 0;
-      const unsigned long long kk = bonus_key[b];
-      if (kk == 0ull) record_status(status, DSPARK_ERR_NONFINITE);
-      tok_out[b] = kk ? argmax_key_index(kk) : 0;
-    }
+    resid_k[b] = n < L ? n + 1 : 0;
+    if (n < L) resid_lse[b] = lse_n;
+    else bonus_rows[1 + atomicAdd(bonus_rows, 1)] = b;   // the bonus race takes it
   }
 }
 
@@ -344,7 +357,7 @@ __global__ void __launch_bounds__(kRowThreads)
 verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__ U,
                           const void* __restrict__ W1, const void* __restrict__ W2,
                           const int32_t* __restrict__ anchor, const int32_t* __restrict__ x,
-                          const float* __restrict__ lse_d, int B, int G, int V, int r, RngKey key,
+                          const float* __restrict__ lse_d, int B, int G, int V, int r, RngKey key_arg,
                           const int32_t* __restrict__ resid_k, const float* __restrict__ resid_lse,
                           unsigned long long* __restrict__ resid_key, int* __restrict__ status) {
   extern __shared__ float Es[];   // [r]
@@ -352,6 +365,7 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
   const int b = blockIdx.y;
   const int ks = resid_k[b];
   if (ks <= 0) return;
+  const RngKey key = live_key(key_arg);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int prev = checked_token((ks == 1) ? anchor[b] : x[(size_t)b * G + ks - 2], V, status);
   for (int i = tid; i < r; i += kRowThreads) Es[i] = load_weight<WDT>(W1, (size_t)prev * r + i);
@@ -395,22 +409,32 @@ verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__
   }
 }
 
-// One block per request.  A rejecting request takes the winner of the residual
+// One block per request.  A request that accepted its whole prefix takes the
+// bonus race's winner.  A rejecting request takes the winner of the residual
 // draw; if the residual had no positive entry in floating point (a measure-zero
 // event in exact arithmetic) it draws from p_t instead, with the same streams.
 __global__ void __launch_bounds__(kRowThreads)
-verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKey key,
+verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKey key_arg,
                          const int32_t* __restrict__ resid_k, const unsigned long long* __restrict__ resid_key,
-                         int32_t* __restrict__ tok_out, int* __restrict__ status) {
+                         const unsigned long long* __restrict__ bonus_key, int32_t* __restrict__ tok_out,
+                         int* __restrict__ status) {
   __shared__ unsigned long long s_k[kRowThreads / 32];
   const int b = blockIdx.x;
   const int ks = resid_k[b];
-  if (ks <= 0) return;
+  if (ks <= 0) {
+    if (threadIdx.x == 0) {
+      const unsigned long long kb = bonus_key[b];
+      if (kb == 0ull) record_status(status, DSPARK_ERR_NONFINITE);
+      tok_out[b] = kb ? argmax_key_index(kb) : 0;
+    }
+    return;
+  }
   const unsigned long long k1 = resid_key[(size_t)b * kKeyStride];
   if (k1) {
     if (threadIdx.x == 0) tok_out[b] = argmax_key_index(k1);
     return;
   }
+  const RngKey key = live_key(key_arg);
   const float* Trow = T + ((size_t)b * (G + 1) + (ks - 1)) * (size_t)V;
   // the row's maximum, then the two-level draw of softmax(T row) (streams 2
   // and 6) with weights exp(T - max)
@@ -450,6 +474,12 @@ verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKe
   }
 }
 
+// The last kernel of a round whose index lives in device memory: the next
+// round reads index + 1.
+__global__ void advance_round(unsigned long long* round_dev) {
+  if (threadIdx.x == 0) *round_dev += 1ull;
+}
+
 // verify_prep, then verify_row_stats on a grid sized by the occupancy query.
 cudaError_t row_stats(const float* T, const int32_t* ell, int B, int gamma, int V, void* ws, cudaStream_t stream) {
   const WsLayout L = ws_layout(B, gamma, V);
@@ -457,8 +487,10 @@ cudaError_t row_stats(const float* T, const int32_t* ell, int B, int gamma, int 
   int* counters = ws_ptr<int>(ws, L.counters);
   int32_t* rows = ws_ptr<int32_t>(ws, L.rows);
   float2* row_part = ws_ptr<float2>(ws, L.row_part);
-  const int nsegs = verify_num_segs(V);
-  verify_prep<<<1, 1024, 0, stream>>>(ell, B, gamma, rows, counters, status);
+  // every row j < gamma: the segment layout of the statistics a draft takes along
+  const int seg_len = ell ? kVerifySeg : kStatsSeg;
+  const int nsegs = div_up(V, seg_len);
+  verify_prep<<<1, 1024, 0, stream>>>(ell, B, gamma, nsegs, rows, counters, status);
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -467,7 +499,7 @@ cudaError_t row_stats(const float* T, const int32_t* ell, int B, int gamma, int 
     return e;
   const long long stat_tasks = (long long)B * gamma * nsegs;
   const int grid_stats = (int)std::max<long long>(1, std::min<long long>(stat_tasks, (long long)sms * std::max(1, per_sm)));
-  verify_row_stats<<<grid_stats, kRowThreads, 0, stream>>>(T, V, nsegs, rows, counters, row_part, status);
+  verify_row_stats<<<grid_stats, kRowThreads, 0, stream>>>(T, V, nsegs, seg_len, rows, counters, row_part, status);
   return cudaGetLastError();
 }
 
@@ -480,19 +512,23 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   unsigned long long* resid_key = ws_ptr<unsigned long long>(a.ws, L.resid_key);
   int32_t* resid_k = ws_ptr<int32_t>(a.ws, L.resid_k);
   float* resid_lse = ws_ptr<float>(a.ws, L.resid_lse);
-  const int nsegs = verify_num_segs(a.V);
+  int32_t* bonus_rows = ws_ptr<int32_t>(a.ws, L.bonus_rows);
+  const int nsegs = a.stats_ready ? stats_num_segs(a.V) : verify_num_segs(a.V);
   cudaError_t e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.total - L.bonus_key, stream);
   if (e != cudaSuccess) return e;
-  if ((e = row_stats(a.T, a.ell, a.B, a.gamma, a.V, a.ws, stream)) != cudaSuccess) return e;
+  if (!a.stats_ready && (e = row_stats(a.T, a.ell, a.B, a.gamma, a.V, a.ws, stream)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid_bonus = std::min(a.B * nsegs, sms * 2);
-  verify_bonus_race<<<grid_bonus, kRowThreads, 0, stream>>>(a.T, a.ell, a.B, a.gamma, a.V, nsegs, a.key, bonus_key,
-                                                            status);
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   verify_decide<<<div_up(a.B * 32, 256), 256, 0, stream>>>(a.T, a.x, a.p_d, a.ell, a.B, a.gamma, a.V, nsegs,
-                                                          a.key, row_part, bonus_key, resid_k, resid_lse,
-                                                          a.n_out, a.tok_out, status);
+                                                          a.key, row_part, resid_k, resid_lse, a.n_out,
+                                                          bonus_rows,
+                                                          a.stats_ready ? ws_ptr<int>(a.ws, L.counters) + 2 : nullptr,
+                                                          status);
+  const int bonus_segs = div_up(a.V, kBonusSeg);
+  const int grid_bonus = std::min(a.B * bonus_segs, sms * 2);
+  verify_bonus_race<<<grid_bonus, kRowThreads, 0, stream>>>(a.T, a.ell, bonus_rows, a.gamma, a.V, bonus_segs, a.key,
+                                                            bonus_key, status);
   if (draft_tc_supported(a.wdtype, a.r, a.V)) {
     e = launch_residual_tc(a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, resid_k, resid_lse, resid_key, a.B,
                            a.gamma, a.V, a.key, status, stream);
@@ -504,7 +540,8 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
         resid_key, status);
   }
   verify_residual_finalize<<<a.B, kRowThreads, 0, stream>>>(a.T, a.B, a.gamma, a.V, a.key, resid_k, resid_key,
-                                                           a.tok_out, status);
+                                                           bonus_key, a.tok_out, status);
+  if (a.advance_round != nullptr) advance_round<<<1, 32, 0, stream>>>(a.advance_round);
   return cudaGetLastError();
 }
 

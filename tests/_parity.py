@@ -6,7 +6,8 @@ and compare under the parity rules:
   the deciding margin exceeds 1e-4 (the top-two Gumbel-perturbed logit gap of
   an argmax, |u - p_t/p_d| of an accept test);
 * probabilities and confidences within 1e-5 relative with fp32 weights; with
-  bf16 weights the fused logits (and so lse and log p) within 2e-2 absolute;
+  bf16 weights the fused logits within 2e-2 absolute: lse_k and the drafted
+  token's own logit l_k(x_k) = log p_k(x_k) + lse_k;
 * verify lengths bit-exact unless two survival products near the cut lie
   within 1e-5 relative or Theta at the stop is within 1e-6 relative of the
   best; then the achieved Theta within 1e-5 relative.
@@ -29,24 +30,39 @@ def is_bf16(inp):
     return inp["W1"].dtype == torch.bfloat16
 
 
+def ranges(reqs, B):
+    """Contiguous [b0, b1) runs covering the requests (all when None), so that
+    the oracle handles each run in one call (in parallel over its requests)."""
+    reqs = sorted(set(range(B) if reqs is None else reqs))
+    out = []
+    for b in reqs:
+        if out and out[-1][1] == b:
+            out[-1][1] = b + 1
+        else:
+            out.append([b, b + 1])
+    return [tuple(r) for r in out]
+
+
 def check_draft(h, out_x, out_p, out_lse, seed, rnd, bf16, reqs=None):
     """Teacher-forced oracle draft on the requests `reqs` (all when None)."""
     B = h["U"].shape[0]
-    reqs = range(B) if reqs is None else reqs
     stats = dict(checked=0, low_margin=0)
-    for b in reqs:
-        d = oracle.draft(h["U"], h["W1"], h["W2"], h["anchor"], seed, rnd, x_force=out_x, b0=b, b1=b + 1)
-        sure = d["margin"][b] > MARGIN
-        stats["checked"] += int(sure.sum())
-        stats["low_margin"] += int((~sure).sum())
-        assert np.array_equal(d["x"][b][sure], out_x[b][sure]), \
-            f"request {b}: draft tokens {out_x[b].tolist()} vs oracle {d['x'][b].tolist()}"
-        if bf16:
-            np.testing.assert_allclose(out_lse[b], d["lse"][b], rtol=0, atol=2e-2)
-            np.testing.assert_allclose(np.log(out_p[b]), np.log(d["p"][b]), rtol=0, atol=4e-2)
-        else:
-            np.testing.assert_allclose(out_lse[b], d["lse"][b], rtol=1e-5)
-            np.testing.assert_allclose(out_p[b], d["p"][b], rtol=1e-5)
+    for b0, b1 in ranges(reqs, B):
+        d = oracle.draft(h["U"], h["W1"], h["W2"], h["anchor"], seed, rnd, x_force=out_x, b0=b0, b1=b1)
+        for b in range(b0, b1):
+            sure = d["margin"][b] > MARGIN
+            stats["checked"] += int(sure.sum())
+            stats["low_margin"] += int((~sure).sum())
+            assert np.array_equal(d["x"][b][sure], out_x[b][sure]), \
+                f"request {b}: draft tokens {out_x[b].tolist()} vs oracle {d['x'][b].tolist()}"
+            if bf16:
+                # lse_k and the drafted token's fused logit l_k(x_k) = log p + lse
+                np.testing.assert_allclose(out_lse[b], d["lse"][b], rtol=0, atol=2e-2)
+                np.testing.assert_allclose(np.log(out_p[b]) + out_lse[b], np.log(d["p"][b]) + d["lse"][b], rtol=0,
+                                           atol=2e-2)
+            else:
+                np.testing.assert_allclose(out_lse[b], d["lse"][b], rtol=1e-5)
+                np.testing.assert_allclose(out_p[b], d["p"][b], rtol=1e-5)
     return stats
 
 
@@ -76,29 +92,29 @@ def check_schedule(c_gpu, sps, mode, ell_gpu, nstar_gpu, theta_gpu, K=-1):
 def check_verify(h, x, ell, n_gpu, tok_gpu, seed, rnd, reqs=None):
     """Teacher-forced oracle verification (GPU draft tokens and lengths)."""
     B = h["U"].shape[0]
-    reqs = list(range(B)) if reqs is None else list(reqs)
     stats = dict(checked=0, low_margin=0, residual=0, bonus=0)
-    for b in reqs:
-        v = oracle.verify(h["T"], h["U"], h["W1"], h["W2"], h["anchor"], x, ell, seed, rnd, b0=b, b1=b + 1)
-        um = v["umargin"][b]
-        evaluated = um[~np.isnan(um)]
-        if evaluated.size and evaluated.min() <= MARGIN:
-            stats["low_margin"] += 1
-            continue
-        assert n_gpu[b] == v["n"][b], f"request {b}: accepted {n_gpu[b]} vs oracle {v['n'][b]}"
-        stats["checked"] += 1
-        stats["residual" if v["flags"][b] & 2 else "bonus"] += 1
-        if v["ymargin"][b] > MARGIN:
-            assert tok_gpu[b] == v["y"][b], f"request {b}: token {tok_gpu[b]} vs oracle {v['y'][b]}"
+    for b0, b1 in ranges(reqs, B):
+        v = oracle.verify(h["T"], h["U"], h["W1"], h["W2"], h["anchor"], x, ell, seed, rnd, b0=b0, b1=b1)
+        for b in range(b0, b1):
+            um = v["umargin"][b]
+            evaluated = um[~np.isnan(um)]
+            if evaluated.size and evaluated.min() <= MARGIN:
+                stats["low_margin"] += 1
+                continue
+            assert n_gpu[b] == v["n"][b], f"request {b}: accepted {n_gpu[b]} vs oracle {v['n'][b]}"
+            stats["checked"] += 1
+            stats["residual" if v["flags"][b] & 2 else "bonus"] += 1
+            if v["ymargin"][b] > MARGIN:
+                assert tok_gpu[b] == v["y"][b], f"request {b}: token {tok_gpu[b]} vs oracle {v['y'][b]}"
     return stats
 
 
-def run_round(inp, w, rnd=0, mode=None, khist=None):
+def run_round(inp, w, rnd=0, mode=None, khist=None, early_stats=False):
     mode = w.mode if mode is None else mode
     if mode == wl.MODE_TOPK and khist is None:
         khist = torch.zeros(2, dtype=torch.int32, device=inp["U"].device)
     out = ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed,
-                   rnd=rnd, sps=inp["sps"], mode=mode, khist=khist)
+                   rnd=rnd, sps=inp["sps"], mode=mode, khist=khist, early_stats=early_stats)
     torch.cuda.synchronize()
     return out
 

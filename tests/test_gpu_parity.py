@@ -10,7 +10,7 @@ import speculative_decoding_02_gb300 as ds
 from speculative_decoding_02_gb300 import workloads as wl
 
 from _parity import (MARGIN, check_confidence, check_draft, check_schedule, check_status, check_verify, host,
-                     is_bf16, run_round)
+                     is_bf16, ranges, run_round)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,15 +35,16 @@ def full_check(w, inp, out, rnd=0, reqs=None, chain=True):
                    float(o["theta"][0]))
     sv = check_verify(h, o["x"], o["ell"], o["n"], o["tok"], w.seed, rnd, reqs)
     if chain:
-        # the whole chain on the oracle alone, compared up to the first
-        # low-margin decision of each request
+        # the whole chain on the oracle alone (no teacher forcing), compared up
+        # to the first low-margin decision of each request
         B = h["U"].shape[0]
-        for b in (range(B) if reqs is None else reqs):
-            d = oracle.draft(h["U"], h["W1"], h["W2"], h["anchor"], w.seed, rnd, b0=b, b1=b + 1)
-            for k in range(w.gamma):
-                if d["margin"][b, k] <= MARGIN:
-                    break
-                assert d["x"][b, k] == o["x"][b, k]
+        for b0, b1 in ranges(reqs, B):
+            d = oracle.draft(h["U"], h["W1"], h["W2"], h["anchor"], w.seed, rnd, b0=b0, b1=b1)
+            for b in range(b0, b1):
+                for k in range(w.gamma):
+                    if d["margin"][b, k] <= MARGIN:
+                        break
+                    assert d["x"][b, k] == o["x"][b, k]
     return sd, sv, c
 
 
@@ -229,17 +230,148 @@ def test_gpu_sampling_law_chi_square():
     assert stats.chi2.sf(((cnt2 - e) ** 2 / e).sum(), V * V - 1) > 1e-4
 
 
+EARLY = [
+    # (B, gamma, V, r, dtype, mode): tensor-core draft (persistent launch, the
+    # statistics warps), CUDA-core draft (statistics after the draft), a
+    # truncating schedule (rows past ell read but not used)
+    (40, 5, 5000, 256, torch.bfloat16, wl.MODE_GREEDY),
+    (128, 4, 65536, 256, torch.bfloat16, wl.MODE_FIXED),
+    (130, 3, 2056, 256, torch.bfloat16, wl.MODE_FIXED),
+    (40, 5, 5000, 64, torch.float32, wl.MODE_GREEDY),
+]
+
+
+@pytest.mark.parametrize("B,G,V,r,dt,mode", EARLY)
+def test_early_target_stats_round(B, G, V, r, dt, mode):
+    w = wl.custom(B=B, gamma=G, V=V, r=r, H=64, wdtype=dt, mode=mode, seed=B + 3 * G, u_sigma=2.5,
+                  t_sigma=(0.4, 1.5), sps_b0=float(4 * B) if mode == wl.MODE_GREEDY else None,
+                  sps_kind="steps", w_sigma=0.05)
+    inp = wl.make_inputs(w, 0, DEV)
+    base = run_round(inp, w)
+    check_status(w, DEV)
+    early = run_round(inp, w, early_stats=True)
+    check_status(w, DEV)
+    # the draft, confidence and schedule do not change; verification reads
+    # statistics taken earlier by other warps
+    for name in ("x", "p", "lse", "c", "ell"):
+        assert torch.equal(base.as_dict()[name], early.as_dict()[name]), name
+    full_check(w, inp, early, chain=False)
+
+
+def test_early_target_stats_fallback_launch():
+    # 153 M tiles of 128 requests: more CTAs than SMs, so the tensor-core draft
+    # runs one launch per position and the statistics follow it
+    w = wl.custom(B=153 * 128, gamma=2, V=256, r=256, H=8, wdtype=torch.bfloat16, mode=wl.MODE_FIXED, seed=21,
+                  u_sigma=2.0, t_sigma=(0.5,), sps_b0=None)
+    inp = wl.make_inputs(w, 0, DEV)
+    out = run_round(inp, w, early_stats=True)
+    check_status(w, DEV)
+    reqs = list(range(16)) + list(range(w.B - 16, w.B))
+    full_check(w, inp, out, reqs=reqs, chain=False)
+
+
+def test_verify_with_missing_early_stats_is_reported():
+    # verify(early_stats=True) after a draft that did not take the statistics
+    w = wl.custom(B=8, gamma=3, V=1024, r=256, H=8, wdtype=torch.bfloat16, seed=2)
+    inp = wl.make_inputs(w, 0, DEV)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    ds.read_status(ws)
+    x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 0, ws=ws)
+    ell = torch.full((w.B,), w.gamma, dtype=torch.int32, device=DEV)
+    ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, 0, ws=ws,
+              early_stats=True)
+    assert ds.read_status(ws) == ds.ERR_INVALID
+    # with the statistics taken by the draft the same call is clean
+    x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 0, ws=ws, T_early=inp["T"])
+    ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, 0, ws=ws,
+              early_stats=True)
+    assert ds.read_status(ws) == ds.OK
+
+
+def test_gpu_sampling_law_chi_square_tensor_cores():
+    # The product path: bf16 W1/W2 of rank 256, V = 256 (four 64-column
+    # tiles), 152 M tiles of 128 requests (the persistent cooperative draft
+    # with its 16-bit block screen, the tensor-core residual).  The mass sits
+    # on eight tokens in different blocks; the first emitted token must follow
+    # softmax(T row 0) and the first two the product of rows 0 and 1.
+    from scipy import stats
+    B, G, V, r = 152 * 128, 2, 256, 256
+    heavy = np.array([3, 37, 70, 101, 130, 166, 200, 250])
+    gen = torch.Generator(device="cpu").manual_seed(8)
+
+    def rows(n, sd):
+        t = torch.full((n, V), -6.0) + torch.randn(n, V, generator=gen) * 0.5
+        t[:, heavy] = torch.randn(n, len(heavy), generator=gen) * sd
+        return t
+
+    U1, T1 = rows(G, 1.0), rows(G + 1, 0.7)
+    W1 = (torch.randn(V, r, generator=gen) * 0.25).to(torch.bfloat16)
+    W2 = (torch.randn(V, r, generator=gen) * 0.25).to(torch.bfloat16)
+    U = U1.unsqueeze(0).expand(B, G, V).contiguous().to(DEV)
+    T = T1.unsqueeze(0).expand(B, G + 1, V).contiguous().to(DEV)
+    anchor = torch.full((B,), 5, dtype=torch.int32, device=DEV)
+    W1d, W2d = W1.to(DEV), W2.to(DEV)
+
+    def cell(tok):
+        c = np.full(tok.shape, len(heavy))
+        for i, hv in enumerate(heavy):
+            c[tok == hv] = i
+        return c
+
+    def probs(row):
+        p = torch.softmax(row.double(), 0).numpy()
+        return np.append(p[heavy], 1.0 - p[heavy].sum())
+
+    pt0, pt1 = probs(T1[0]), probs(T1[1])
+    firsts, pairs, accepted = [], [], 0
+    ext_rng = np.random.default_rng(17)
+    for rnd in (5, 6):
+        x, p, lse = ds.markov_draft(U, W1d, W2d, anchor, 91, rnd)
+        ell = torch.full((B,), 2, dtype=torch.int32, device=DEV)
+        n, tok = ds.verify(T, U, W1d, W2d, anchor, x, p, lse, ell, 91, rnd)
+        torch.cuda.synchronize()
+        n, tok, xh = n.cpu().numpy(), tok.cpu().numpy(), x.cpu().numpy()
+        s1 = np.where(n >= 1, xh[:, 0], tok)
+        ext = ext_rng.choice(V, size=B, p=torch.softmax(T1[1].double(), 0).numpy())
+        s2 = np.where(n >= 2, xh[:, 1], np.where(n == 1, tok, ext))
+        firsts.append(cell(s1))
+        pairs.append(cell(s1) * (len(heavy) + 1) + cell(s2))
+        accepted += int((n >= 1).sum())
+    first, pair = np.concatenate(firsts), np.concatenate(pairs)
+    N = first.size
+    cnt = np.bincount(first, minlength=len(heavy) + 1)
+    e = pt0 * N
+    assert e.min() > 5
+    assert stats.chi2.sf(((cnt - e) ** 2 / e).sum(), len(heavy)) > 1e-4
+    e2 = np.outer(pt0, pt1).ravel() * N
+    cnt2 = np.bincount(pair, minlength=e2.size)
+    assert e2.min() > 5
+    assert stats.chi2.sf(((cnt2 - e2) ** 2 / e2).sum(), e2.size - 1) > 1e-4
+    # position 1 is accepted at the rate sum_v min(p_d, p_t) (Eq.8)
+    pd = oracle.draft_probs(U1[0].numpy(), wl.to_numpy(W1), wl.to_numpy(W2), 5)
+    lab = oracle.acceptance_label(pd, torch.softmax(T1[0].double(), 0).numpy())
+    rate = accepted / N
+    assert abs(rate - lab) < 3.3 * np.sqrt(lab * (1 - lab) / N)
+
+
 FULL = ["qwen3_4b", "batch128", "large_vocab", "serving512"]
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workload_sampled(name):
+    # the round as the benchmark runs it: the draft takes the target rows'
+    # statistics on the tensor-core path
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w, 0, DEV)
-    out = run_round(inp, w)
+    out = run_round(inp, w, early_stats=True)
     check_status(w, DEV)
-    reqs = sorted({0, 1, w.B // 2, w.B - 1})
-    sd, sv, _ = full_check(w, inp, out, reqs=reqs, chain=False)
+    # 16 requests (two runs of 8 at both ends of the batch), teacher-forced
+    # and as a whole chain
+    reqs = list(range(8)) + list(range(w.B - 8, w.B)) if w.B > 16 else list(range(w.B))
+    if name == "batch128":
+        sig = inp["target_sigma"].cpu().numpy().astype(np.float64)[reqs]
+        assert set(np.round(sig, 3).tolist()) == {0.3, 1.0, 2.0}, "every target-noise class among the checked requests"
+    sd, sv, _ = full_check(w, inp, out, reqs=reqs, chain=True)
     assert sd["checked"] > 0 and sv["checked"] + sv["low_margin"] == len(reqs)
     # properties over every request
     o = out.as_dict()
