@@ -5,10 +5,15 @@ prefix scheduler, rejection-sampling verification -- over one batch of the
 synthetic workload (default: batch-128 engine point, B=128, gamma=16,
 V=151936).  The metric is verified draft tokens per second: the sum over
 requests of the scheduled verify lengths l_r, per round, divided by the round
-time.
+time.  The round's target logits T are an input of the round, so the draft
+takes their rows' softmax statistics while it runs (DSPARK_EARLY_TARGET_STATS);
+the same round with verification streaming those rows itself is reported
+beside it ("classic_round"), with the other workloads, a truncating schedule
+and a CUDA-graph replay of the round.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                         [--impl gb300|reference] [--no-cpu-baseline] [--no-e2e]
+                        [--no-workloads]
         python bench.py --profile-draft [--workload NAME]   (the draft alone, for ncu)
 
 Prints one JSON line.  With N > 1 (torchrun) each rank runs an independent
@@ -43,8 +48,16 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the records of the other workloads")
+    ap.add_argument("--soak", type=float, default=0.5,
+                    help="seconds of untimed rounds just before the timed ones (clock samples under load)")
     ap.add_argument("--profile-draft", action="store_true",
                     help="run only the Markov draft of the workload a few times (small ncu captures)")
+    ap.add_argument("--plain-draft", action="store_true",
+                    help="with --profile-draft: the draft without the target-row statistics")
+    ap.add_argument("--profile-round", action="store_true",
+                    help="run a few whole rounds of the workload (ncu launch lists and kernel captures)")
     return ap.parse_args()
 
 
@@ -80,22 +93,32 @@ def draft_bytes_per_launch(w):
     return 4 * w.B * w.gamma * w.V + sw * w.r * w.V + sw * w.B * w.gamma * w.r + 12 * w.B * w.gamma
 
 
-def kernels_per_round(w):
+def fused_draft_bytes_per_launch(w):
+    """The draft call that also takes the statistics of the target rows
+    j < gamma along (T_early): the draft's bytes plus those rows once."""
+    return draft_bytes_per_launch(w) + 4 * w.B * w.gamma * w.V
+
+
+def kernels_per_round(w, early=False):
     """Launches of this library's kernels in one round (cudaMemsetAsync not
     counted): draft = the persistent tensor-core kernel, which also finishes
     x, p and lse after a last grid barrier (bf16, r = 256, V >= 192; else a
-    CUDA-core step and finalize per position);
-    confidence; schedule; verify = prep, row statistics, bonus race, decide,
-    residual (the draft kernel in residual mode, or its CUDA-core form),
-    residual finalize."""
+    CUDA-core step and finalize per position; with early statistics on that
+    path a prep and a row-statistics kernel follow);
+    confidence; schedule; verify = prep and row statistics (not with early
+    statistics), decide, bonus race, residual (the draft kernel in residual
+    mode, or its CUDA-core form), residual finalize."""
     tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
-    return (1 if tc else 2 * w.gamma) + 1 + 1 + 6
+    draft = 1 if tc else 2 * w.gamma + (2 if early else 0)
+    verify = 4 if early else 6
+    return draft + 1 + 1 + verify
 
 
 # Source files of the draft kernel: a committed ncu figure counts only while
-# they are unchanged since the capture.
+# they are unchanged since the capture.  The figure itself is a small JSON
+# record beside the prose summary in profiles/.
 DRAFT_SOURCES = ["draft_tc.cu", "tc_common.cuh", "common.cuh"]
-DRAFT_PROFILE = os.path.join(ROOT, "profiles", "draft_step_tc_batch128.md")
+DRAFT_PROFILE = os.path.join(ROOT, "profiles", "draft_step_tc_batch128.json")
 
 
 def draft_source_hash():
@@ -106,18 +129,16 @@ def draft_source_hash():
     return h.hexdigest()[:16]
 
 
-def draft_traffic(w):
+def draft_traffic(w, early=True):
     """DRAM bytes (read + write) of one draft launch from the committed ncu
-    summary, or None if it is missing, for another workload, or stale."""
+    record, or None if it is missing, for another workload or mode, or stale."""
     try:
-        kv = {}
-        for line in open(DRAFT_PROFILE):
-            if line.startswith("- ") and ":" in line:
-                k, v = line[2:].split(":", 1)
-                kv[k.strip()] = v.strip().strip("`")
-        if kv.get("workload") != w.name or kv.get("source_sha256_16") != draft_source_hash():
+        with open(DRAFT_PROFILE) as f:
+            rec = json.load(f)
+        if (rec.get("workload") != w.name or rec.get("source_sha256_16") != draft_source_hash()
+                or bool(rec.get("early_target_stats")) != bool(early)):
             return None
-        return int(float(kv["dram_bytes_per_launch"]))
+        return int(rec["dram_bytes_per_launch"])
     except Exception:
         return None
 
@@ -303,6 +324,146 @@ def job_units(units, device):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+class RoundTimer:
+    """Rounds of one workload through the public entry points, in the order
+    dspark_round runs them (draft, confidence, schedule, verify), on the
+    current stream; events around the draft call give its duration inside the
+    same timed rounds."""
+
+    def __init__(self, ds, w, inp, dev, early, sps=None, khist=None, ws=None):
+        self.ds, self.w, self.inp, self.dev, self.early = ds, w, inp, dev, early
+        self.sps = inp["sps"] if sps is None else sps
+        self.khist = khist
+        self.ws = ds.workspace(w.B, w.gamma, w.V, dev) if ws is None else ws
+        self.stream = torch.cuda.current_stream(dev)
+
+    def step(self, i, d0=None, d1=None):
+        ds, w, inp = self.ds, self.w, self.inp
+        if d0 is not None:
+            d0.record(self.stream)
+        x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, i, ws=self.ws,
+                                    T_early=inp["T"] if self.early else None)
+        if d1 is not None:
+            d1.record(self.stream)
+        c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
+        ell, _, _ = ds.schedule(c, self.sps, w.mode, i, self.khist, self.ws)
+        n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, i,
+                         self.ws, early_stats=self.early)
+        return ell, n
+
+    def run(self, steps, warmup, rnd0=0, barrier=None, soak_s=0.0):
+        """Warm-up rounds, an optional untimed soak, then `steps` timed rounds.
+        Returns dict(ms (total), draft_ms (mean per call), ell_sum, n_acc, n_rej)."""
+        for i in range(warmup):
+            self.step(rnd0 + i)
+        torch.cuda.synchronize()
+        st = self.ds.read_status(self.ws)
+        if st != self.ds.OK:
+            raise RuntimeError(f"{self.w.name}: device status {st} after warm-up")
+        if soak_s > 0:
+            # keeps the GPU under the same load for a few clock-sampling periods
+            t0 = time.perf_counter()
+            j = 0
+            while time.perf_counter() - t0 < soak_s:
+                self.step(rnd0 + warmup + (j % 64))
+                j += 1
+                if j % 32 == 0:
+                    torch.cuda.synchronize()
+        dstart = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        dend = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        (barrier or torch.cuda.synchronize)()
+        e0.record(self.stream)
+        outs = [self.step(rnd0 + warmup + i, dstart[i], dend[i]) for i in range(steps)]
+        e1.record(self.stream)
+        (barrier or torch.cuda.synchronize)()
+        st = self.ds.read_status(self.ws)
+        if st != self.ds.OK:
+            raise RuntimeError(f"{self.w.name}: device status {st} in the timed rounds")
+        return dict(ms=e0.elapsed_time(e1),
+                    draft_ms=float(np.mean([dstart[i].elapsed_time(dend[i]) for i in range(steps)])),
+                    ell_sum=sum(int(e.sum()) for e, _ in outs), n_acc=sum(int(n.sum()) for _, n in outs),
+                    n_rej=sum(int((n < e).sum()) for e, n in outs), steps=steps)
+
+
+def round_record(w, r, hbm, early):
+    """Per-round figures of a RoundTimer result."""
+    steps = r["steps"]
+    ms = r["ms"] / steps
+    per_round = r["ell_sum"] / steps
+    rb = round_bytes(w, per_round, r["n_rej"] / steps)
+    db = fused_draft_bytes_per_launch(w) if early else draft_bytes_per_launch(w)
+    return {"ms": ms, "verified_per_round": per_round, "accepted_per_round": r["n_acc"] / steps,
+            "verified_tokens_per_s": r["ell_sum"] / (r["ms"] / 1e3),
+            "accepted_tokens_per_s": r["n_acc"] / (r["ms"] / 1e3),
+            "round_GB": rb / 1e9, "round_hbm_frac": rb / (ms / 1e3) / 1e9 / hbm,
+            "draft_ms": r["draft_ms"], "draft_GB": db / 1e9,
+            "draft_hbm_frac": db / (r["draft_ms"] / 1e3) / 1e9 / hbm, "early_target_stats": early}
+
+
+def graph_round_ms(ds, w, inp, dev, steps):
+    """One round captured into a CUDA graph with the round index in device
+    memory (advanced by the round's last kernel), replayed `steps` times."""
+    khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == 2 else None
+    out = ds.RoundOutputs(w.B, w.gamma, dev)
+    n = ds.workspace_size(w.B, w.gamma, w.V)
+    buf = torch.zeros(n + 256, dtype=torch.uint8, device=dev)
+    ws = buf[(-buf.data_ptr()) % 256:][:n]
+    round_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def call():
+        ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed, rnd=0,
+                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, early_stats=True, round_dev=round_dev,
+                 advance_round=True)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if ds.read_status(ws) != ds.OK:
+        raise RuntimeError("device status after the graph replays")
+    ms = e0.elapsed_time(e1) / steps
+    ell = int(out.ell.sum())
+    del g, buf
+    return {"ms": ms, "verified_per_round": ell, "verified_tokens_per_s": ell / (ms / 1e3),
+            "rounds_replayed": steps + 4, "round_index_after": int(round_dev[0])}
+
+
+def other_workload(ds, wl, name, dev, steps, warmup, hbm):
+    """Early-statistics and classic rounds of another workload (serving512:
+    100 consecutive rounds with the top-K schedule taking K from two rounds
+    earlier); the inputs are freed afterwards."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, 0, dev)
+    rec = {"B": w.B, "gamma": w.gamma, "V": w.V}
+    for early in (True, False):
+        khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == wl.MODE_TOPK else None
+        rt = RoundTimer(ds, w, inp, dev, early, khist=khist)
+        k = 100 if name == "serving512" else steps
+        r = rt.run(k, warmup)
+        rec["early" if early else "classic"] = round_record(w, r, hbm, early)
+    if name == "serving512":
+        rec["note"] = "100 consecutive timed rounds; top-K with K from two rounds earlier; inputs fixed, the " \
+                      "round index advancing"
+    del inp
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_gpu(args):
     import speculative_decoding_02_gb300 as ds
     from speculative_decoding_02_gb300 import build as lib_build
@@ -321,72 +482,55 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     ds.library()
+    hbm, bf16, peak_kind = peaks()
 
     w = wl.WORKLOADS[args.workload]
     inp = wl.make_inputs(w, 0, dev)
     khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == wl.MODE_TOPK else None
-    out = ds.RoundOutputs(w.B, w.gamma, dev)
-    ws = ds.workspace(w.B, w.gamma, w.V, dev)
-    stream = torch.cuda.current_stream(dev)
-
-    dstart = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    dend = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-
-    def step(i, rec=None):
-        # the four entry points in the order dspark_round runs them (the same
-        # kernels), with events around the draft for its roofline figure
-        if rec is not None:
-            dstart[rec].record(stream)
-        x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, i, ws=ws)
-        if rec is not None:
-            dend[rec].record(stream)
-        c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
-        ell, _, _ = ds.schedule(c, inp["sps"], w.mode, i, khist, ws)
-        n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, i, ws)
-        return ell, n
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    st = ds.read_status(ws)
-    if st != ds.OK:
-        raise RuntimeError(f"device status {st} after warm-up")
+    early = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    outs = []
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the headline: rounds with the target-row statistics taken by the draft
+    timer = RoundTimer(ds, w, inp, dev, early, khist=khist)
     with Clocks(local) as clk:
-        barrier()
-        e0.record(stream)
-        for i in range(args.steps):
-            outs.append(step(args.warmup + i, rec=i))
-        e1.record(stream)
-        barrier()
-    ms = slowest_rank_ms(e0.elapsed_time(e1), dev)
-    st = ds.read_status(ws)
-    if st != ds.OK:
-        raise RuntimeError(f"device status {st} in the timed rounds")
-
-    ell_sum = sum(int(e.sum()) for e, _ in outs)
-    n_acc = sum(int(n.sum()) for _, n in outs)
-    n_rej = sum(int((n < e).sum()) for e, n in outs)
+        r = timer.run(args.steps, args.warmup, barrier=barrier, soak_s=args.soak)
+    ms = slowest_rank_ms(r["ms"], dev)
+    ell_sum, n_acc, n_rej = r["ell_sum"], r["n_acc"], r["n_rej"]
     per_round = ell_sum / args.steps
     value = job_units(ell_sum, dev) / (ms / 1e3)
 
-    # dominant kernel: the Markov draft, timed inside the timed region
-    draft_ms = float(np.mean([dstart[i].elapsed_time(dend[i]) for i in range(args.steps)]))
-    hbm, bf16, peak_kind = peaks()
-    dbytes = draft_bytes_per_launch(w)
+    # dominant kernel: the Markov draft (with the target-row statistics when
+    # early), timed inside the timed region
+    draft_ms = r["draft_ms"]
+    dbytes = fused_draft_bytes_per_launch(w) if early else draft_bytes_per_launch(w)
     achieved = dbytes / (draft_ms / 1e3) / 1e9
+
+    extra = {}
+    if rank == 0:
+        # the same workload with verification streaming the target rows itself
+        extra["classic_round"] = round_record(w, RoundTimer(ds, w, inp, dev, False, khist=khist).run(
+            args.steps, 3, rnd0=1000), hbm, False)
+        # a falling steps-per-second curve, so that the greedy truncates (the
+        # scheduler's sorting path; only the verified rows are read)
+        if w.mode == wl.MODE_GREEDY:
+            b = torch.arange(inp["sps"].numel(), dtype=torch.float64, device=dev)
+            sps_fall = (1.0 / (1.0 + b / 256.0)).float()
+            rt = RoundTimer(ds, w, inp, dev, False, sps=sps_fall)
+            rec = round_record(w, rt.run(args.steps, 3, rnd0=2000), hbm, False)
+            rec["sps"] = "1 / (1 + B / 256)"
+            extra["truncating_schedule"] = rec
+        if early:
+            extra["graph_replay"] = graph_round_ms(ds, w, inp, dev, args.steps)
 
     # the acceptance labels of one round's verified positions (a widening of
     # the path: sum_v min(p_d, p_t) per position), timed on their own
     label = None
-    if rank == 0 and w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192:
+    ws = timer.ws
+    if rank == 0 and early:
         x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 7, ws=ws)
         c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
         ell, _, _ = ds.schedule(c, inp["sps"], w.mode, 7, khist, ws)
@@ -398,10 +542,10 @@ def run_gpu(args):
             lab()
         torch.cuda.synchronize()
         l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        l0.record(stream)
+        l0.record()
         for _ in range(3):
             lab()
-        l1.record(stream)
+        l1.record()
         torch.cuda.synchronize()
         if ds.read_status(ws) != ds.OK:
             raise RuntimeError("device status after the acceptance labels")
@@ -409,9 +553,7 @@ def run_gpu(args):
         npos = int(ell.sum())
         lbytes = 8 * w.V * npos + (2 if w.wdtype == torch.bfloat16 else 4) * w.r * w.V
         label = {"ms": lms, "positions": npos, "algorithmic_GB": lbytes / 1e9,
-                 "achieved_GBs": lbytes / (lms / 1e3) / 1e9, "frac": lbytes / (lms / 1e3) / 1e9 / hbm,
-                 "note": "U and T rows of the verified positions once, W2 once; the implementation reads the "
-                         "T rows twice (their softmax statistics first)"}
+                 "achieved_GBs": lbytes / (lms / 1e3) / 1e9, "frac": lbytes / (lms / 1e3) / 1e9 / hbm}
 
     # sequential temperature scaling over held-out samples of this batch size
     # (1024 rounds of the workload's requests), timed on its own
@@ -427,10 +569,10 @@ def run_gpu(args):
         ds.sts_fit(zs, ells, accs, grid)
         torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
+        s0.record()
         for _ in range(3):
             ds.sts_fit(zs, ells, accs, grid)
-        s1.record(stream)
+        s1.record()
         torch.cuda.synchronize()
         sms = s0.elapsed_time(s1) / 3
         # every observed (sample, position) evaluates one sigmoid per grid value
@@ -443,7 +585,7 @@ def run_gpu(args):
     # end to end through host buffers: per-round inputs copied in, results out
     e2e = None
     if rank == 0 and not args.no_e2e:
-        e2e = run_e2e(w, inp, ds, dev, args, khist)
+        e2e = run_e2e(w, inp, ds, dev, args, khist, early)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -455,6 +597,13 @@ def run_gpu(args):
                          f"{dt:.1f} s wall",
                "single_thread": single_thread_sample(w, hs)}
 
+    # the other workloads (after the headline's inputs are freed)
+    if rank == 0 and args.workload == "batch128" and not args.no_workloads:
+        del inp
+        torch.cuda.empty_cache()
+        extra["workloads"] = {n: other_workload(ds, wl, n, dev, args.steps, 3, hbm)
+                              for n in ("qwen3_4b", "large_vocab", "serving512")}
+
     if rank == 0:
         rbytes = round_bytes(w, per_round, n_rej / args.steps)
         line = {
@@ -464,33 +613,39 @@ def run_gpu(args):
             "config": {"workload": w.name, "B": w.B, "gamma": w.gamma, "V": w.V, "r": w.r, "H": w.H,
                        "weights": "bf16" if w.wdtype == torch.bfloat16 else "f32",
                        "l2": "inputs larger than L2 (U+T %.2f GB)" % ((4 * w.B * (2 * w.gamma + 1) * w.V) / 1e9),
+                       "early_target_stats": early,
                        "verified_per_round": per_round, "accepted_per_round": n_acc / args.steps,
                        "round_GB": rbytes / 1e9,
                        "round_hbm_frac": rbytes / (ms / args.steps / 1e3) / 1e9 / hbm,
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"kernel": "markov draft (dspark_markov_draft: draft_step_tc with its fused finalize)",
+            "roofline": {"kernel": "markov draft taking the target rows' statistics along "
+                                   "(dspark_markov_draft_ex: draft_step_tc with its fused finalize)"
+                         if early else "markov draft (dspark_markov_draft: draft_step_tc with its fused finalize)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": draft_traffic(w), "peak_kind": peak_kind,
+                         "frac": achieved / hbm, "traffic": draft_traffic(w, early), "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
             "clocks": clk.summary(),
             "acceptance_label": label,
             "sts_fit": sts_fit,
             "e2e": e2e,
-            "gpu_launches": args.steps * kernels_per_round(w),
+            "gpu_launches": args.steps * kernels_per_round(w, early),
             "cpu_baseline": cpu,
         }
+        line.update(extra)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def run_e2e(w, inp, ds, dev, args, khist):
+def run_e2e(w, inp, ds, dev, args, khist, early):
     """Rounds through the public API with the per-round inputs in pinned host
     memory: H2D of U, T, h, anchor and D2H of tokens, counts and lengths are
-    inside the timed region."""
+    inside the timed region.  The inputs are double-buffered on the device and
+    the next round's upload runs on a copy stream while the current round
+    computes."""
     names = ["U", "T", "h", "anchor"]
     hostb = {k: inp[k].cpu().pin_memory() for k in names}
-    devb = {k: torch.empty_like(inp[k]) for k in names}
+    devb = [{k: torch.empty_like(inp[k]) for k in names} for _ in range(2)]
     outs = ["x", "ell", "n", "tok"]
     out = ds.RoundOutputs(w.B, w.gamma, dev)
     hosto = {k: torch.empty(getattr(out, k).shape, dtype=getattr(out, k).dtype).pin_memory() for k in outs}
@@ -498,24 +653,45 @@ def run_e2e(w, inp, ds, dev, args, khist):
     bi = sum(t.numel() * t.element_size() for t in hostb.values())
     bo = sum(t.numel() * t.element_size() for t in hosto.values())
     stream = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
     steps = max(3, min(args.steps, 10))
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
-    def one(i):
-        for k in names:
-            devb[k].copy_(hostb[k], non_blocking=True)
-        ds.round(devb["U"], devb["T"], inp["W1"], inp["W2"], devb["h"], inp["w"], devb["anchor"], seed=w.seed,
-                 rnd=i, sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws)
+    def upload(slot):
+        copy.wait_event(consumed[slot])
+        with torch.cuda.stream(copy):
+            for k in names:
+                devb[slot][k].copy_(hostb[k], non_blocking=True)
+            uploaded[slot].record(copy)
+
+    def compute(i, slot):
+        stream.wait_event(uploaded[slot])
+        b = devb[slot]
+        ds.round(b["U"], b["T"], inp["W1"], inp["W2"], b["h"], inp["w"], b["anchor"], seed=w.seed, rnd=i,
+                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, early_stats=early)
+        consumed[slot].record(stream)
         for k in outs:
             hosto[k].copy_(getattr(out, k), non_blocking=True)
 
-    one(0)
+    for slot in range(2):
+        consumed[slot].record(stream)
+    upload(0)
+    compute(0, 0)
+    torch.cuda.synchronize()
+    # steady state: each timed step uploads the next round's inputs while it
+    # computes this round's (round 0's inputs are uploaded before timing; the
+    # last step's upload is for a round outside the timed region)
+    upload(1)
     torch.cuda.synchronize()
     ell_sum = 0
     t0 = time.perf_counter()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(steps):
-        one(i)
+        slot = (i + 1) % 2
+        upload((i + 2) % 2)   # the next round's inputs while this one computes
+        compute(i + 1, slot)
         stream.synchronize()
         ell_sum += int(hosto["ell"].sum())
     e1.record(stream)
@@ -523,12 +699,13 @@ def run_e2e(w, inp, ds, dev, args, khist):
     ms = e0.elapsed_time(e1)
     del hostb, devb
     return {"value": ell_sum / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "steps": steps, "wall_s": time.perf_counter() - t0}
+            "steps": steps, "wall_s": time.perf_counter() - t0, "uploads": "double-buffered on a copy stream"}
 
 
 def run_profile_draft(args):
-    """The Markov draft of the workload alone, 4 calls (for ncu: U, W1, W2 and
-    the anchors are all it holds on the device)."""
+    """The Markov draft of the workload alone, 4 calls, taking the target
+    rows' statistics along unless --plain-draft (for ncu: U, T, W1, W2 and the
+    anchors are all it holds on the device)."""
     import speculative_decoding_02_gb300 as ds
     from speculative_decoding_02_gb300 import build as lib_build
     from speculative_decoding_02_gb300 import workloads as wl
@@ -536,21 +713,45 @@ def run_profile_draft(args):
     lib_build.build()
     w = wl.WORKLOADS[args.workload]
     weights = wl.make_weights(w, dev)
-    U = wl.make_round_inputs(w, 0, dev)["U"]
+    rin = wl.make_round_inputs(w, 0, dev)
+    U = rin["U"]
+    T = None if args.plain_draft else rin["T"]
+    del rin["h"]
     ws = ds.workspace(w.B, w.gamma, w.V, dev)
     for i in range(4):
-        ds.markov_draft(U, weights["W1"], weights["W2"], weights["anchor"], w.seed, i, ws=ws)
+        ds.markov_draft(U, weights["W1"], weights["W2"], weights["anchor"], w.seed, i, ws=ws, T_early=T)
     torch.cuda.synchronize()
     st = ds.read_status(ws)
-    print(json.dumps({"profile_draft": w.name, "status": st, "source_sha256_16": draft_source_hash()}))
+    print(json.dumps({"profile_draft": w.name, "early_target_stats": T is not None, "status": st,
+                      "source_sha256_16": draft_source_hash()}))
     if st != ds.OK:
         sys.exit(1)
+
+
+def run_profile_round(args):
+    """A few whole rounds of the workload through the entry points (early
+    statistics where the tensor-core path runs): two warm-up rounds, then
+    args.steps rounds, for ncu launch lists and captures of round kernels."""
+    import speculative_decoding_02_gb300 as ds
+    from speculative_decoding_02_gb300 import build as lib_build
+    from speculative_decoding_02_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    lib_build.build()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w, 0, dev)
+    khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == wl.MODE_TOPK else None
+    early = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192 and not args.plain_draft
+    r = RoundTimer(ds, w, inp, dev, early, khist=khist).run(args.steps, 2)
+    print(json.dumps({"profile_round": w.name, "early_target_stats": early, "steps": args.steps,
+                      "ms_per_round": r["ms"] / args.steps, "kernels_per_round": kernels_per_round(w, early)}))
 
 
 def main():
     args = parse()
     if args.profile_draft:
         run_profile_draft(args)
+    elif args.profile_round:
+        run_profile_round(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

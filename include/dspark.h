@@ -296,12 +296,16 @@ int dspark_round_ex(const float* U, const float* T, const void* W1, const void* 
  * DSPARK_NOALLOC_SCRATCH_BYTES inside the library's device memory, which every
  * GPU that loads the library holds until the process exits.  Inputs and outputs
  * are the caller's, as above.  It allocates nothing.
- *  - The first call on a device looks up the array's device address on that
- *    device (cudaGetSymbolAddress); make that first call before any stream
- *    capture.
+ *  - With CUDA's lazy module loading the array is loaded, and so takes device
+ *    memory, when its device address is first looked up on a device.  Call
+ *    dspark_noalloc_init once per device at start-up, with that device
+ *    current, before the caller's pool reserves HBM and before any stream
+ *    capture; otherwise the first draft call on the device does the lookup.
  *  - All calls share the one array: calls whose work overlaps on the GPU race.
- *    Each call clears what must start at zero.  Errors that the kernels detect
- *    are not reported back by this entry.
+ *    Each call clears what must start at zero, the status word included.
+ *    Errors that the kernels detect (a bounded wait that gave up, a
+ *    non-finite logit, an anchor outside [0, V)) are recorded in the array's
+ *    status word; dspark_noalloc_read_status returns and clears it.
  *  - Sizes whose draft scratch (about 8 * gamma * B bytes per vocabulary slice
  *    of the draft kernel) exceeds the array return DSPARK_ERR_WORKSPACE before
  *    anything is enqueued.
@@ -311,6 +315,18 @@ int dspark_markov_draft_noalloc(const float* U, const void* W1, const void* W2, 
                                 const int32_t* anchor, int B, int gamma, int V, int r,
                                 uint64_t seed, uint64_t round,
                                 int32_t* x_out, float* p_out, float* lse_out, void* stream);
+
+/* Looks up the no-allocation draft's scratch array on the current device (and
+ * so loads it there); DSPARK_OK or DSPARK_ERR_CUDA.  No counterpart on the
+ * pages: it lets a caller that cannot allocate later place this one-time cost
+ * at start-up. */
+int dspark_noalloc_init(void);
+
+/* Waits for `stream`, then copies the status word of the no-allocation draft's
+ * scratch array (what the kernels of the latest dspark_markov_draft_noalloc
+ * call recorded, a DSPARK_* code) to *host_status and clears it.  Returns
+ * DSPARK_OK, DSPARK_ERR_INVALID (null host_status) or DSPARK_ERR_CUDA. */
+int dspark_noalloc_read_status(int* host_status, void* stream);
 
 /*
  * Self-test of the device-side bounded waits (no counterpart on the pages).

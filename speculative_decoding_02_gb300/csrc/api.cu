@@ -11,18 +11,6 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-int check_dtype(int dt) { return (dt == DSPARK_F32 || dt == DSPARK_BF16) ? DSPARK_OK : DSPARK_ERR_INVALID; }
-
-// Shapes shared by the draft and verify calls.
-int check_shapes(int B, int gamma, int V, int r) {
-  if (B <= 0 || gamma <= 0 || V <= 0 || r <= 0) return DSPARK_ERR_INVALID;
-  if (gamma > kMaxGamma) return DSPARK_ERR_UNSUPPORTED;
-  if (V % 8 != 0 || r % 16 != 0 || r > 256) return DSPARK_ERR_UNSUPPORTED;
-  if (B > 65535) return DSPARK_ERR_UNSUPPORTED;
-  if ((long long)B * (gamma + 1) * (long long)V >= (1ll << 40)) return DSPARK_ERR_UNSUPPORTED;
-  return DSPARK_OK;
-}
-
 int check_ws(void* ws, size_t ws_bytes, int B, int gamma, int V) {
   if (!ws || !aligned(ws, 256)) return DSPARK_ERR_WORKSPACE;
   if (ws_bytes < ws_layout(B, gamma, V).total) return DSPARK_ERR_WORKSPACE;
@@ -40,10 +28,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK : DSPARK_ER
 int draft_checks(const float* U, const void* W1, const void* W2, int wdtype, const int32_t* anchor, int B,
                  int gamma, int V, int r, int32_t* x_out, float* p_out, float* lse_out, void* ws,
                  size_t ws_bytes) {
-  DSPARK_TRY(check_shapes(B, gamma, V, r));
-  DSPARK_TRY(check_dtype(wdtype));
-  if (!U || !W1 || !W2 || !anchor || !x_out || !p_out || !lse_out) return DSPARK_ERR_INVALID;
-  if (!aligned(U, 16) || !aligned(W1, 16) || !aligned(W2, 16)) return DSPARK_ERR_INVALID;
+  DSPARK_TRY(draft_arg_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out));
   return check_ws(ws, ws_bytes, B, gamma, V);
 }
 

@@ -49,6 +49,34 @@ struct VerifyArgs {
   unsigned long long* advance_round;
 };
 
+// Host-side argument checks shared by every entry point that takes these
+// sizes (api.cu and noalloc.cu), so that a limit changed in one place holds
+// for all of them.
+inline int check_dtype(int dt) { return (dt == DSPARK_F32 || dt == DSPARK_BF16) ? DSPARK_OK : DSPARK_ERR_INVALID; }
+
+// Shapes shared by the draft and verify calls.
+inline int check_shapes(int B, int gamma, int V, int r) {
+  if (B <= 0 || gamma <= 0 || V <= 0 || r <= 0) return DSPARK_ERR_INVALID;
+  if (gamma > kMaxGamma) return DSPARK_ERR_UNSUPPORTED;
+  if (V % 8 != 0 || r % 16 != 0 || r > 256) return DSPARK_ERR_UNSUPPORTED;
+  if (B > 65535) return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)B * (gamma + 1) * (long long)V >= (1ll << 40)) return DSPARK_ERR_UNSUPPORTED;
+  return DSPARK_OK;
+}
+
+// The pointer and alignment checks of a draft call (everything but the
+// workspace).
+inline int draft_arg_checks(const float* U, const void* W1, const void* W2, int wdtype, const int32_t* anchor,
+                            int B, int gamma, int V, int r, const int32_t* x_out, const float* p_out,
+                            const float* lse_out) {
+  int st = check_shapes(B, gamma, V, r);
+  if (st != DSPARK_OK) return st;
+  if ((st = check_dtype(wdtype)) != DSPARK_OK) return st;
+  if (!U || !W1 || !W2 || !anchor || !x_out || !p_out || !lse_out) return DSPARK_ERR_INVALID;
+  if (((uintptr_t)U | (uintptr_t)W1 | (uintptr_t)W2) % 16 != 0) return DSPARK_ERR_INVALID;
+  return DSPARK_OK;
+}
+
 cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream);
 
 // Tensor-core draft (bf16 weights, r = 256, V >= 192); the dispatcher above picks it.

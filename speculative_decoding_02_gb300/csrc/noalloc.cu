@@ -11,14 +11,19 @@
 // instead of a caller buffer.
 //
 // The array is a file-scope __device__ variable of DSPARK_NOALLOC_SCRATCH_BYTES
-// bytes.  Every GPU on which the library is loaded holds it until the process
-// exits.  In host code the array's name is only a host-side stand-in, so the
-// device address is looked up with cudaGetSymbolAddress once per device, with
-// that device current, on the first call made on it; that first call should
-// therefore come before any stream capture.  All calls share the one array:
-// two calls whose work overlaps on the GPU race on it and give undefined
-// results.  The parts that must start at zero (the argmax keys and the status
-// word) are cleared by every call.
+// bytes.  Once the library's code for it is loaded on a GPU, that GPU holds it
+// until the process exits.  With CUDA's lazy module loading that happens when
+// its device address is first looked up, so dspark_noalloc_init does the
+// lookup for the current device and should be called at start-up, before the
+// caller's pool takes the rest of HBM and before any stream capture; the
+// first draft call on a device does it otherwise.  In host code the array's
+// name is only a host-side stand-in, so the device address comes from
+// cudaGetSymbolAddress, with that device current.  All calls share the one
+// array: two calls whose work overlaps on the GPU race on it and give
+// undefined results.  The parts that must start at zero (the argmax keys, the
+// counters and the status word) are cleared by every call; the status word
+// then holds what the kernels of the latest call recorded, for
+// dspark_noalloc_read_status.
 #include <mutex>
 
 #include "kernels.h"
@@ -63,17 +68,31 @@ size_t draft_scratch_bytes(int B, int gamma, int V) {
 
 using namespace dspark;
 
+extern "C" int dspark_noalloc_init(void) {
+  void* ws = nullptr;
+  return scratch_address(&ws) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+extern "C" int dspark_noalloc_read_status(int* host_status, void* stream) {
+  if (!host_status) return DSPARK_ERR_INVALID;
+  void* ws = nullptr;
+  if (scratch_address(&ws) != cudaSuccess) return DSPARK_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  int value = 0;
+  if (cudaMemcpyAsync(&value, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  *host_status = value;
+  return DSPARK_OK;
+}
+
 extern "C" int dspark_markov_draft_noalloc(const float* U, const void* W1, const void* W2, int wdtype,
                                            const int32_t* anchor, int B, int gamma, int V, int r,
                                            uint64_t seed, uint64_t round, int32_t* x_out, float* p_out,
                                            float* lse_out, void* stream) {
-  if (B <= 0 || gamma <= 0 || V <= 0 || r <= 0) return DSPARK_ERR_INVALID;
-  if (gamma > kMaxGamma) return DSPARK_ERR_UNSUPPORTED;
-  if (V % 8 != 0 || r % 16 != 0 || r > 256 || B > 65535) return DSPARK_ERR_UNSUPPORTED;
-  if ((long long)B * (gamma + 1) * (long long)V >= (1ll << 40)) return DSPARK_ERR_UNSUPPORTED;
-  if (wdtype != DSPARK_F32 && wdtype != DSPARK_BF16) return DSPARK_ERR_INVALID;
-  if (!U || !W1 || !W2 || !anchor || !x_out || !p_out || !lse_out) return DSPARK_ERR_INVALID;
-  if (((uintptr_t)U | (uintptr_t)W1 | (uintptr_t)W2) % 16 != 0) return DSPARK_ERR_INVALID;
+  const int st = draft_arg_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out);
+  if (st != DSPARK_OK) return st;
   if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
   if (draft_scratch_bytes(B, gamma, V) > kNoAllocScratchBytes) return DSPARK_ERR_WORKSPACE;
   void* ws = nullptr;

@@ -129,6 +129,13 @@ def test_noalloc_argument_errors(lib):
     assert f(p, p, p, 1, p, 4096, 32, 1024, 16, 0, 0, p, p, p, None) == ds.ERR_WORKSPACE
 
 
+def test_noalloc_status_argument_error(lib):
+    f = lib.dspark_noalloc_read_status
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(None, None) == ds.ERR_INVALID
+
+
 def test_product_path_never_loads_the_oracle():
     # the package (binding, kernels, library build) imports, links and runs
     # nothing under oracle/: a reference to it may only appear in prose

@@ -1,6 +1,7 @@
 """The bench's algorithmic byte counts and launch counts (CPU only): they follow
 the per-unit figures stated for the roofline, term by term, and agree with the
 committed profile of the draft kernel."""
+import json
 import os
 import sys
 
@@ -37,19 +38,23 @@ def test_draft_bytes_match_the_profile():
     d = bench.draft_bytes_per_launch(w)
     # U once (1244.7 MB), W2 once (77.8 MB), the W1 gathers and x/p/lse
     assert d == 4 * 128 * 16 * 151936 + 2 * 256 * 151936 + 2 * 128 * 16 * 256 + 12 * 128 * 16
-    kv = {}
-    for line in open(bench.DRAFT_PROFILE):
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            kv[k.strip()] = v.strip()
-    assert int(kv["algorithmic_bytes_per_launch"]) == d
+    # with the target rows j < gamma taken along: those rows once more (1244.7 MB)
+    fd = bench.fused_draft_bytes_per_launch(w)
+    assert fd - d == 4 * 128 * 16 * 151936
+    with open(bench.DRAFT_PROFILE) as f:
+        rec = json.load(f)
+    assert rec["workload"] == "batch128"
+    alg = fd if rec["early_target_stats"] else d
+    assert int(rec["algorithmic_bytes_per_launch"]) == alg
     # the profile's DRAM traffic is within a few per cent of the algorithmic bytes
-    assert 1.0 <= int(kv["dram_bytes_per_launch"]) / d < 1.05
+    assert 1.0 <= int(rec["dram_bytes_per_launch"]) / alg < 1.05
 
 
 def test_kernels_per_round():
     # tensor-core path: one persistent draft launch; CUDA-core path: a step and
-    # a finalize per position; then confidence, schedule and six verify kernels
+    # a finalize per position; then confidence, schedule and six verify
+    # kernels (four when the draft took the target-row statistics along)
     assert bench.kernels_per_round(wl.WORKLOADS["batch128"]) == 9
+    assert bench.kernels_per_round(wl.WORKLOADS["batch128"], early=True) == 7
     t = wl.WORKLOADS["tiny"]
     assert bench.kernels_per_round(t) == 2 * t.gamma + 8

@@ -67,12 +67,33 @@ def test_noalloc_draft_matches_workspace_draft(name):
         torch.testing.assert_close(lse, rl, rtol=1e-5, atol=0)
 
 
-def test_noalloc_rejects_sizes_beyond_its_scratch():
+def _read_status():
+    L = ds.library()
+    L.dspark_noalloc_read_status.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_void_p]
+    L.dspark_noalloc_read_status.restype = ctypes.c_int
+    v = ctypes.c_int(-1)
+    assert L.dspark_noalloc_read_status(ctypes.byref(v), ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)) \
+        == ds.OK
+    return int(v.value)
+
+
+def test_noalloc_reports_kernel_errors():
+    # an anchor outside [0, V) is caught by the kernels and shows in the
+    # scratch array's status word; a clean call after it reads OK
     f = _entry()
+    L = ds.library()
+    L.dspark_noalloc_init.argtypes = []
+    L.dspark_noalloc_init.restype = ctypes.c_int
+    assert L.dspark_noalloc_init() == ds.OK
     w = wl.custom(B=40, gamma=5, V=5000, r=64, H=16, wdtype=torch.bfloat16, seed=3)
     weights = wl.make_weights(w, DEV)
     rin = wl.make_round_inputs(w, 0, DEV)
-    inp = dict(U=rin["U"], W1=weights["W1"], W2=weights["W2"], anchor=weights["anchor"])
-    # sizes checked on the host before anything is enqueued; nothing is read
-    st, _, _, _ = _call(f, inp, w, 0, B=4096, G=32, V=151936)
-    assert st == ds.ERR_WORKSPACE
+    inp = dict(U=rin["U"], W1=weights["W1"], W2=weights["W2"], anchor=weights["anchor"].clone())
+    inp["anchor"][7] = w.V + 3
+    st, _, _, _ = _call(f, inp, w, 0)
+    assert st == ds.OK
+    assert _read_status() == ds.ERR_INVALID
+    inp["anchor"] = weights["anchor"]
+    st, _, _, _ = _call(f, inp, w, 1)
+    assert st == ds.OK
+    assert _read_status() == ds.OK
