@@ -15,6 +15,8 @@ Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                         [--impl gb300|reference] [--no-cpu-baseline] [--no-e2e]
                         [--no-workloads]
         python bench.py --profile-draft [--workload NAME]   (the draft alone, for ncu)
+        python bench.py --profile-label [--workload NAME]   (the acceptance labels alone)
+        python bench.py --profile-round [--workload NAME]   (whole rounds, for launch lists)
 
 Prints one JSON line.  With N > 1 (torchrun) each rank runs an independent
 replica of the workload (the path shards over requests with no exchange), the
@@ -56,6 +58,8 @@ def parse():
                     help="run only the Markov draft of the workload a few times (small ncu captures)")
     ap.add_argument("--plain-draft", action="store_true",
                     help="with --profile-draft: the draft without the target-row statistics")
+    ap.add_argument("--profile-label", action="store_true",
+                    help="the acceptance labels alone, 4 calls on a draft's statistics (for ncu)")
     ap.add_argument("--profile-round", action="store_true",
                     help="run a few whole rounds of the workload (ncu launch lists and kernel captures)")
     return ap.parse_args()
@@ -114,33 +118,51 @@ def kernels_per_round(w, early=False):
     return draft + 1 + 1 + verify
 
 
-# Source files of the draft kernel: a committed ncu figure counts only while
+# Source files of a profiled kernel: a committed ncu figure counts only while
 # they are unchanged since the capture.  The figure itself is a small JSON
 # record beside the prose summary in profiles/.
 DRAFT_SOURCES = ["draft_tc.cu", "tc_common.cuh", "common.cuh"]
 DRAFT_PROFILE = os.path.join(ROOT, "profiles", "draft_step_tc_batch128.json")
+LABEL_SOURCES = ["label_tc.cu", "tc_common.cuh", "common.cuh"]
+LABEL_PROFILE = os.path.join(ROOT, "profiles", "label_tc_batch128.json")
 
 
-def draft_source_hash():
+def source_hash(names):
     h = hashlib.sha256()
-    for name in DRAFT_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "speculative_decoding_02_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def draft_traffic(w, early=True):
-    """DRAM bytes (read + write) of one draft launch from the committed ncu
-    record, or None if it is missing, for another workload or mode, or stale."""
+def draft_source_hash():
+    return source_hash(DRAFT_SOURCES)
+
+
+def profile_traffic(path, sources, w, **match):
+    """DRAM bytes (read + write) of one launch from a committed ncu record, or
+    None if it is missing, for another workload or mode, or stale."""
     try:
-        with open(DRAFT_PROFILE) as f:
+        with open(path) as f:
             rec = json.load(f)
-        if (rec.get("workload") != w.name or rec.get("source_sha256_16") != draft_source_hash()
-                or bool(rec.get("early_target_stats")) != bool(early)):
+        if rec.get("workload") != w.name or rec.get("source_sha256_16") != source_hash(sources):
+            return None
+        if any(rec.get(k) != v for k, v in match.items()):
             return None
         return int(rec["dram_bytes_per_launch"])
     except Exception:
         return None
+
+
+def draft_traffic(w, early=True):
+    """DRAM bytes of one draft launch from the committed ncu record (None if
+    missing, for another workload or mode, or stale)."""
+    return profile_traffic(DRAFT_PROFILE, DRAFT_SOURCES, w, early_target_stats=bool(early))
+
+
+def label_traffic(w):
+    """DRAM bytes of one acceptance-label launch from the committed ncu record."""
+    return profile_traffic(LABEL_PROFILE, LABEL_SOURCES, w)
 
 
 class Clocks:
@@ -527,33 +549,41 @@ def run_gpu(args):
             extra["graph_replay"] = graph_round_ms(ds, w, inp, dev, args.steps)
 
     # the acceptance labels of one round's verified positions (a widening of
-    # the path: sum_v min(p_d, p_t) per position), timed on their own
+    # the path: sum_v min(p_d, p_t) per position), timed on their own; the
+    # target rows' statistics are the ones the round's draft took along
     label = None
     ws = timer.ws
     if rank == 0 and early:
-        x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 7, ws=ws)
+        x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 7, ws=ws,
+                                    T_early=inp["T"])
         c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
         ell, _, _ = ds.schedule(c, inp["sps"], w.mode, 7, khist, ws)
 
         def lab():
-            return ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, lse, ell, ws=ws)
+            return ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, lse, ell, ws=ws,
+                                       stats="early")
 
-        for _ in range(2):
-            lab()
-        torch.cuda.synchronize()
-        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        l0.record()
         for _ in range(3):
             lab()
-        l1.record()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream(dev)
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_lab = 5
+        l0.record(stream)
+        for _ in range(n_lab):
+            lab()
+        l1.record(stream)
         torch.cuda.synchronize()
         if ds.read_status(ws) != ds.OK:
             raise RuntimeError("device status after the acceptance labels")
-        lms = l0.elapsed_time(l1) / 3
+        lms = l0.elapsed_time(l1) / n_lab
         npos = int(ell.sum())
-        lbytes = 8 * w.V * npos + (2 if w.wdtype == torch.bfloat16 else 4) * w.r * w.V
+        # every position's U and T rows (the kernel streams each once) and W2
+        lbytes = 8 * w.V * w.B * w.gamma + (2 if w.wdtype == torch.bfloat16 else 4) * w.r * w.V
         label = {"ms": lms, "positions": npos, "algorithmic_GB": lbytes / 1e9,
-                 "achieved_GBs": lbytes / (lms / 1e3) / 1e9, "frac": lbytes / (lms / 1e3) / 1e9 / hbm}
+                 "achieved_GBs": lbytes / (lms / 1e3) / 1e9, "frac": lbytes / (lms / 1e3) / 1e9 / hbm,
+                 "launches_per_call": 2, "target_stats": "taken by the round's draft",
+                 "traffic": label_traffic(w)}
 
     # sequential temperature scaling over held-out samples of this batch size
     # (1024 rounds of the workload's requests), timed on its own
@@ -728,6 +758,33 @@ def run_profile_draft(args):
         sys.exit(1)
 
 
+def run_profile_label(args):
+    """The acceptance labels of the workload, 4 calls, reading the target
+    rows' statistics a draft took along (for ncu: U, T, W1, W2, the anchors
+    and the draft's outputs are all it holds on the device)."""
+    import speculative_decoding_02_gb300 as ds
+    from speculative_decoding_02_gb300 import build as lib_build
+    from speculative_decoding_02_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    lib_build.build()
+    w = wl.WORKLOADS[args.workload]
+    weights = wl.make_weights(w, dev)
+    rin = wl.make_round_inputs(w, 0, dev)
+    del rin["h"]
+    ws = ds.workspace(w.B, w.gamma, w.V, dev)
+    x, _, lse = ds.markov_draft(rin["U"], weights["W1"], weights["W2"], weights["anchor"], w.seed, 0, ws=ws,
+                                T_early=rin["T"])
+    ell = torch.full((w.B,), w.gamma, dtype=torch.int32, device=dev)
+    for _ in range(4):
+        ds.acceptance_label(rin["T"], rin["U"], weights["W1"], weights["W2"], weights["anchor"], x, lse, ell, ws=ws,
+                            stats="early")
+    torch.cuda.synchronize()
+    st = ds.read_status(ws)
+    print(json.dumps({"profile_label": w.name, "status": st, "source_sha256_16": source_hash(LABEL_SOURCES)}))
+    if st != ds.OK:
+        sys.exit(1)
+
+
 def run_profile_round(args):
     """A few whole rounds of the workload through the entry points (early
     statistics where the tensor-core path runs): two warm-up rounds, then
@@ -752,6 +809,8 @@ def main():
         run_profile_draft(args)
     elif args.profile_round:
         run_profile_round(args)
+    elif args.profile_label:
+        run_profile_label(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

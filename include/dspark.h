@@ -74,6 +74,7 @@ extern "C" {
 /* flags of dspark_verify_ex and dspark_round_ex */
 #define DSPARK_EARLY_TARGET_STATS 1u  /* the draft took the target rows' softmax statistics */
 #define DSPARK_ADVANCE_ROUND 2u       /* the call's last kernel adds 1 to *round_dev */
+#define DSPARK_TARGET_STATS_FROM_VERIFY 4u  /* dspark_acceptance_label_ex: a verification left them */
 
 /* Bytes of device scratch the entry points below need for these sizes; 0 when
  * a size is not positive. */
@@ -215,7 +216,8 @@ int dspark_verify_ex(const float* T, const float* U, const void* W1, const void*
  * k = 1..ell[b]:  label[b, k-1] = sum_v min(p_d(v), p_t(v)), p_d =
  * softmax(U[b,k-1,:] + bias(x_{k-1})) from lse_d, p_t = softmax(T[b, k-1, :]);
  * positions k > ell[b] get 0.  Arguments as for dspark_verify (the same
- * workspace layout: it overwrites the target-row statistics there).
+ * workspace layout: it overwrites the target-row statistics there).  One
+ * persistent launch runs every position; U and T rows stream in by TMA.
  * Tensor-core path only (bf16 W1/W2, r = 256, V >= 192); other weights
  * return DSPARK_ERR_UNSUPPORTED.
  * Out: label_out [B, gamma] f32, caller-owned.
@@ -225,6 +227,24 @@ int dspark_acceptance_label(const float* T, const float* U, const void* W1, cons
                             const float* lse_d, const int32_t* ell, int B, int gamma,
                             int V, int r, float* label_out, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/*
+ * dspark_acceptance_label reading the target rows' softmax statistics that
+ * the round already took, so that each U and T row is read once (flags 0
+ * gives dspark_acceptance_label, which streams the rows for them first):
+ *  - DSPARK_EARLY_TARGET_STATS: left by dspark_markov_draft_ex(T_early = T)
+ *    on the same workspace (rows j < gamma), with or without the verification
+ *    that used them;
+ *  - DSPARK_TARGET_STATS_FROM_VERIFY: left by a dspark_verify(_ex) without
+ *    that flag on the same workspace and T (rows j < ell[b]);
+ * either earlier in stream order.  Both flags at once, or other bits, return
+ * DSPARK_ERR_INVALID.
+ */
+int dspark_acceptance_label_ex(const float* T, const float* U, const void* W1, const void* W2,
+                               int wdtype, const int32_t* anchor, const int32_t* x,
+                               const float* lse_d, const int32_t* ell, int B, int gamma,
+                               int V, int r, unsigned flags, float* label_out, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /*
  * Sequential temperature scaling of the confidence head ([blog] section 5; the

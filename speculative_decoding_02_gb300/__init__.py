@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libdspark.so")
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NONFINITE = range(7)
 F32, BF16 = 0, 1
 SCHED_FIXED, SCHED_GREEDY, SCHED_TOPK = 0, 1, 2
-EARLY_TARGET_STATS, ADVANCE_ROUND = 1, 2
+EARLY_TARGET_STATS, ADVANCE_ROUND, TARGET_STATS_FROM_VERIFY = 1, 2, 4
 
 
 class DSparkError(RuntimeError):
@@ -67,6 +67,9 @@ def _load():
     L.dspark_acceptance_label.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp,
                                           ctypes.c_size_t, vp]
     L.dspark_acceptance_label.restype = i32
+    L.dspark_acceptance_label_ex.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_uint,
+                                             vp, vp, ctypes.c_size_t, vp]
+    L.dspark_acceptance_label_ex.restype = i32
     L.dspark_sts_workspace_size.argtypes = [i32, i32, i32]
     L.dspark_sts_workspace_size.restype = sz
     L.dspark_sts_fit.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, vp, vp, sz, vp]
@@ -266,9 +269,12 @@ def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None, early
     return n, tok
 
 
-def acceptance_label(T, U, W1, W2, anchor, x, lse_d, ell, ws=None):
+def acceptance_label(T, U, W1, W2, anchor, x, lse_d, ell, ws=None, stats=None):
     """label [B, gamma] f32: sum_v min(p_d, p_t) for every verified position
-    k <= ell[b] (0 elsewhere).  Tensor-core path only (bf16, r = 256)."""
+    k <= ell[b] (0 elsewhere).  Tensor-core path only (bf16, r = 256).
+    stats: None (the call streams the target rows' statistics first),
+    "early" (ws holds them from markov_draft(T_early=T)) or "verify" (ws
+    holds them from a verify without early_stats)."""
     L = _load()
     _need(T, "T", torch.float32)
     dev = T.device
@@ -285,9 +291,10 @@ def acceptance_label(T, U, W1, W2, anchor, x, lse_d, ell, ws=None):
     _sized(x, "x", (B, G)); _sized(lse_d, "lse_d", (B, G))
     label = torch.empty(B, G, dtype=torch.float32, device=dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
-    _check(L.dspark_acceptance_label(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x),
-                                     _ptr(lse_d), _ptr(ell), B, G, V, r, _ptr(label), _ptr(ws), ws.numel(),
-                                     _stream(dev)), "acceptance_label")
+    flags = {None: 0, "early": EARLY_TARGET_STATS, "verify": TARGET_STATS_FROM_VERIFY}[stats]
+    _check(L.dspark_acceptance_label_ex(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x),
+                                        _ptr(lse_d), _ptr(ell), B, G, V, r, flags, _ptr(label), _ptr(ws), ws.numel(),
+                                        _stream(dev)), "acceptance_label")
     return label
 
 

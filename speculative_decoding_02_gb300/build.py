@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdspark.so")
-SOURCES = ["api.cu", "draft.cu", "draft_tc.cu", "sched.cu", "verify.cu", "noalloc.cu", "sts.cu"]
+SOURCES = ["api.cu", "draft.cu", "draft_tc.cu", "label_tc.cu", "sched.cu", "verify.cu", "noalloc.cu", "sts.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -45,9 +45,7 @@ def build(force=False, verbose=False, extra_flags=()):
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     cc = nvcc()
-    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                    "--use_fast_math=false"] + list(extra_flags)
-    flags = [f for f in flags if f != "--use_fast_math=false"]
+    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE] + list(extra_flags)
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")

@@ -171,23 +171,42 @@ int dspark_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N
                                     (cudaStream_t)stream));
 }
 
-int dspark_acceptance_label(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
-                            const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* ell, int B,
-                            int gamma, int V, int r, float* label_out, void* workspace, size_t workspace_bytes,
-                            void* stream) {
+int dspark_acceptance_label_ex(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
+                               const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* ell, int B,
+                               int gamma, int V, int r, unsigned flags, float* label_out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   DSPARK_TRY(check_shapes(B, gamma, V, r));
   DSPARK_TRY(check_dtype(wdtype));
   if (!T || !U || !W1 || !W2 || !anchor || !x || !lse_d || !ell || !label_out) return DSPARK_ERR_INVALID;
   if (!aligned(T, 16) || !aligned(U, 16)) return DSPARK_ERR_INVALID;
   DSPARK_TRY(check_ws(workspace, workspace_bytes, B, gamma, V));
+  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_TARGET_STATS_FROM_VERIFY)) return DSPARK_ERR_INVALID;
+  if ((flags & DSPARK_EARLY_TARGET_STATS) && (flags & DSPARK_TARGET_STATS_FROM_VERIFY)) return DSPARK_ERR_INVALID;
   if (!draft_tc_supported(wdtype, r, V)) return DSPARK_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   const WsLayout L = ws_layout(B, gamma, V);
   DSPARK_TRY(cuda_status(cudaMemsetAsync(label_out, 0, sizeof(float) * (size_t)B * gamma, s)));
-  DSPARK_TRY(cuda_status(launch_row_stats(T, ell, B, gamma, V, workspace, s)));
+  // the target rows' softmax partials: taken along by a draft (rows j < gamma,
+  // kStatsSeg segments), left by a verification (rows j < ell, kVerifySeg
+  // segments), or taken here
+  int nsegs = verify_num_segs(V);
+  if (flags & DSPARK_EARLY_TARGET_STATS) nsegs = stats_num_segs(V);
+  else if (!(flags & DSPARK_TARGET_STATS_FROM_VERIFY))
+    DSPARK_TRY(cuda_status(launch_row_stats(T, ell, B, gamma, V, workspace, s)));
   return cuda_status(launch_acceptance_label_tc(T, U, W1, W2, anchor, x, lse_d, ell,
-                                                ws_ptr<float2>(workspace, L.row_part), verify_num_segs(V), label_out,
-                                                B, gamma, V, ws_ptr<int>(workspace, L.status), s));
+                                                ws_ptr<float2>(workspace, L.row_part), nsegs,
+                                                (flags & DSPARK_EARLY_TARGET_STATS) ? ws_ptr<int>(workspace, L.counters) + 2
+                                                                                    : nullptr,
+                                                label_out, B, gamma,
+                                                V, ws_ptr<int>(workspace, L.status), s));
+}
+
+int dspark_acceptance_label(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
+                            const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* ell, int B,
+                            int gamma, int V, int r, float* label_out, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  return dspark_acceptance_label_ex(T, U, W1, W2, wdtype, anchor, x, lse_d, ell, B, gamma, V, r, 0u, label_out,
+                                    workspace, workspace_bytes, stream);
 }
 
 int dspark_round_ex(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,

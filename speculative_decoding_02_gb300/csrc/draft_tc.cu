@@ -34,10 +34,6 @@
 // (the rejected k*), with U and T row segments staged by the epilogue's own
 // coalesced asynchronous copies, racing blocks of max(0, p_t - p_d).
 //
-// Label (MODE kLabel): the residual pipeline at one fixed position k for every
-// request with k <= ell_b, summing min(p_d, p_t) over the vocabulary (the
-// study report's Eq.8 acceptance) into the request's label.
-//
 // Every wait is bounded; on a timeout the CTA records DSPARK_ERR_TIMEOUT,
 // drains the copies and MMAs it issued, frees its TMEM and returns.
 #include <cuda_bf16.h>
@@ -68,7 +64,7 @@ constexpr int kUStages = 3;         // U tile ring
 constexpr int kUBox = 32;           // fp32 columns per U box (128 bytes, swizzled)
 constexpr int kEpiWarps = 16;       // four warps per TMEM lane quarter
 constexpr int kStatsWarps = 2;      // draft mode: warps that stream target-row statistics
-constexpr int kThreads = 64 + 32 * kEpiWarps;                 // residual and label modes
+constexpr int kThreads = 64 + 32 * kEpiWarps;                 // residual mode
 constexpr int kDraftThreads = kThreads + 32 * kStatsWarps;    // draft mode (640 x 96 registers fit)
 constexpr uint32_t kTmemCols = 512;  // two accumulators, then E
 constexpr uint32_t kTmemE = 2 * kAccCols;   // first TMEM column of E (128 x 256 bf16)
@@ -82,8 +78,8 @@ constexpr int kBarBytes = 512;                   // mbarriers and flags
 constexpr int kWStagesRes = 2;
 constexpr int kResStageBytes = 2 * BM * 256;      // U then T
 constexpr int kGkBytes = 2 * BM * 16;   // row-key copies: [position parity][row], 16 bytes each
-// the rings: draft mode W2 and U; residual and label modes W2 and the U/T row
-// stages, in the same space
+// the rings: draft mode W2 and U; residual mode W2 and the U/T row stages, in
+// the same space
 constexpr int kDraftRingBytes = kWStages * kWStageBytes + kUStages * kUStageBytes;
 constexpr int kResRingBytes = kWStagesRes * kWStageBytes + 2 * kResStageBytes;
 constexpr int kRingBytes = kDraftRingBytes > kResRingBytes ? kDraftRingBytes : kResRingBytes;
@@ -102,7 +98,7 @@ struct __align__(8) Barriers {
 static_assert(sizeof(Barriers) <= kBarBytes, "barrier block overflows its shared-memory slot");
 static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may use");
 
-enum Mode { kDraft = 0, kResidual = 1, kLabel = 2 };
+enum Mode { kDraft = 0, kResidual = 1 };
 
 template <int MODE>
 __host__ __device__ constexpr int threads_of() { return MODE == kDraft ? kDraftThreads : kThreads; }
@@ -124,12 +120,7 @@ struct StepParams {
   const float* lse_d;
   const float* resid_lse;
   unsigned long long* resid_key;
-  // label mode: position k_fixed of every request with k_fixed <= ell_b, the
-  // target-row softmax partials [B*(G+1)][nsegs] and the label output [B][G]
-  const int32_t* ell;
-  const float2* row_part;
-  float* label;
-  int k_fixed, nsegs;
+  int nsegs;                            // draft mode: target-statistics segments per row
   // draft mode: softmax partials of the target rows j < G of every request,
   // taken while the draft runs (T_stats null: none); stats_part is the
   // [B*(G+1)][nsegs] partial buffer of verification, stats_next a task counter
@@ -465,17 +456,23 @@ __device__ __forceinline__ void gather_e(const __nv_bfloat16* W1, int tok, bool 
 template <int R>
 __device__ __forceinline__ void resid_copy(unsigned char* stage, const long long* off, const float* U,
                                            const float* T, int vt, int V) {
+  // 2 tensors x R rows x 16 chunks = R / 16 copies for each of the 512
+  // epilogue threads: copy j of thread tid is tensor j / (R / 32), row
+  // (j % (R / 32)) * 32 + tid / 16, chunk tid % 16.  The chunk, the row's low
+  // bits (and so the swizzle) are the thread's own; with the loop unrolled
+  // only the row offset lookup and the addresses remain per copy.
+  constexpr int kPer = R / 16, kHalf = kPer / 2;
   const int tid = threadIdx.x - 64;
-#pragma unroll 1
-  for (int j = 0; j < R / 16; ++j) {
-    const int id = j * (kEpiWarps * 32) + tid;
-    const int tensor = id / (R * 16);
-    const int rem = id - tensor * (R * 16);
-    const int rr = rem >> 4, c16 = rem & 15;
-    const long long o = off[tensor * BM + rr];
-    const int v = vt + c16 * 4;
-    if (o >= 0 && v < V)
-      cp_async16(stage + tensor * (R * 256) + rr * 256 + ((c16 ^ (rr & 15)) << 4), (tensor ? T : U) + o + v);
+  const int c16 = tid & 15, r16 = tid >> 4;
+  const int v = vt + c16 * 4;
+  if (v < V) {
+    unsigned char* dst0 = stage + r16 * 256 + ((c16 ^ (r16 & 15)) << 4);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int tensor = j / kHalf, rr = (j % kHalf) * 32 + r16;
+      const long long o = off[tensor * BM + rr];
+      if (o >= 0) cp_async16(dst0 + tensor * (R * 256) + (j % kHalf) * 32 * 256, (tensor ? T : U) + o + v);
+    }
   }
   cp_async_commit();
 }
@@ -653,8 +650,6 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
 // MODE kResidual: for every request that rejected at position k*, the fused
 // draft logits of k* again, raced over log max(0, p_t - p_d) (U and T rows
 // read directly by the epilogue threads).
-// MODE kLabel: the same at position k_fixed, adding sum_v min(p_d, p_t) of
-// each row into label[b][k_fixed - 1] (one atomicAdd per CTA and row).
 template <int R, int MODE>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1)
 draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
@@ -811,9 +806,6 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       if constexpr (MODE == kResidual) {
         ks = active ? p.resid_k[b] : 0;
         active = ks > 0;
-      } else if constexpr (MODE == kLabel) {
-        ks = (active && p.k_fixed <= min(max(p.ell[b], 0), p.G)) ? p.k_fixed : 0;
-        active = ks > 0;
       }
 
       // E = W1[x_{k-1}] into TMEM (gather_e).  From the second position on, E
@@ -863,22 +855,10 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       constexpr bool kShareRes = (MODE == kResidual);
       unsigned long long* res_key = (kShareRes && active) ? p.resid_key + (size_t)b * kKeyStride : nullptr;
       float ld2 = 0.f, lt2 = 0.f;
-      float lacc = 0.f;   // label mode: this thread's sum of min(p_d, p_t)
-      if constexpr (MODE != kDraft) {
+      if constexpr (MODE == kResidual) {
         if (active) {
           ld2 = p.lse_d[(size_t)b * p.G + ks - 1] * kLog2e;
-          if constexpr (MODE == kResidual) {
-            lt2 = p.resid_lse[b] * kLog2e;
-          } else {
-            // lse of the target row from its segment partials
-            const float2* rp = p.row_part + ((size_t)b * (p.G + 1) + ks - 1) * p.nsegs;
-            float mt = -INFINITY, st2 = 0.f;
-            for (int sg = 0; sg < p.nsegs; ++sg) {
-              const float2 pr = rp[sg];
-              softmax_merge(mt, st2, pr.x, pr.y);
-            }
-            lt2 = (mt + logf(st2)) * kLog2e;
-          }
+          lt2 = p.resid_lse[b] * kLog2e;
         }
       }
       bool ok = true;
@@ -891,10 +871,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         if (tid < R) {
           const int bb = m0 + tid;
           int kk = 0;
-          if (bb < p.B) {
-            if constexpr (MODE == kResidual) kk = p.resid_k[bb];
-            else kk = p.k_fixed <= min(max(p.ell[bb], 0), p.G) ? p.k_fixed : 0;
-          }
+          if (bb < p.B) kk = p.resid_k[bb];
           off_u[tid] = kk > 0 ? ((long long)bb * p.G + (kk - 1)) * p.V : -1;
           off_t[tid] = kk > 0 ? ((long long)bb * (p.G + 1) + (kk - 1)) * p.V : -1;
         }
@@ -920,7 +897,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           named_bar_sync(1, kEpiWarps * 32);
           if (i + 1 < ntl) resid_copy<R>(U_s + ((i + 1) & 1) * kResStageBytes, off_u, p.U, p.T, (t0 + i + 1) * BN, p.V);
         }
-        const bool got_acc = sub != 0 || mbar_wait(&bars->acc_full[acc_i], (gcount >> 1) & 1, abort, p.status);
+        // (warp-uniform: the TMEM load below is warp-wide)
+        const bool got_acc =
+            sub != 0 || __all_sync(0xffffffffu, mbar_wait(&bars->acc_full[acc_i], (gcount >> 1) & 1, abort, p.status));
         if (MODE != kDraft && !got_acc) ok = false;
         float v[CPP];
         if (got_acc) {
@@ -1020,25 +999,19 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
               for (int e = 0; e < 4; ++e) {
                 const float pd = ex2_approx(fmaf(v[c + e] + uv[e], kLog2e, -ld2));
                 const float pt = ex2_approx(fmaf(tv[e], kLog2e, -lt2));
-                if constexpr (MODE == kLabel) {
-                  if (c + e < nv) lacc += fminf(pd, pt);
-                } else {
-                  uu[c + e] = pt - pd;
-                }
+                uu[c + e] = pt - pd;
               }
             }
-            if constexpr (MODE == kResidual) {
-              // the row's best from other CTAs: the latest copy of its key that
-              // has landed in shared memory (nothing waits for it)
-              if (kShareRes && i >= 1) {
-                const unsigned long long gkr = *reinterpret_cast<volatile unsigned long long*>(&gk_rows[r].x);
-                if (gkr) resid_raise(rs, argmax_key_value(gkr));
-              }
-              resid_tile<CPP>(rs, uu, nv, v0, urow, j0, sw, key, (uint32_t)b, (uint32_t)ks);
-              if (kShareRes && rs.best_v >= 0 && rs.zbest > rs.zpub && rs.zbest >= rs.zthr) {
-                atomicMax(res_key, argmax_key(rs.zbest, rs.best_v));
-                rs.zpub = rs.zbest;
-              }
+            // the row's best from other CTAs: the latest copy of its key that
+            // has landed in shared memory (nothing waits for it)
+            if (kShareRes && i >= 1) {
+              const unsigned long long gkr = *reinterpret_cast<volatile unsigned long long*>(&gk_rows[r].x);
+              if (gkr) resid_raise(rs, argmax_key_value(gkr));
+            }
+            resid_tile<CPP>(rs, uu, nv, v0, urow, j0, sw, key, (uint32_t)b, (uint32_t)ks);
+            if (kShareRes && rs.best_v >= 0 && rs.zbest > rs.zpub && rs.zbest >= rs.zthr) {
+              atomicMax(res_key, argmax_key(rs.zbest, rs.best_v));
+              rs.zpub = rs.zbest;
             }
           }
           if (kShareRes && h == 0) {
@@ -1068,7 +1041,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       }
       const int slot = part * R + r;               // parts of row r at r, R + r, ...
       xm[slot] = st.run_m;
-      xs[slot] = MODE == kLabel ? lacc : st.run_s;
+      xs[slot] = st.run_s;
       xk[slot] = key;
       named_bar_sync(1, kEpiWarps * 32);
       if (part == 0 && active && ok) {
@@ -1085,14 +1058,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           // threshold, and a threshold is always a value some part has
           // published.
           p.part[((size_t)(k - 1) * p.B + b) * p.part_slices + slice] = make_float2(M, S);
-        } else if constexpr (MODE == kResidual) {
-          if (K) atomicMax(&p.resid_key[(size_t)b * kKeyStride], K);
         } else {
-          // label: the CTA's sum of min(p_d, p_t) over its columns
-          float Ssum = 0.f;
-#pragma unroll
-          for (int j = 0; j < kParts; ++j) Ssum += xs[j * R + r];
-          atomicAdd(&p.label[(size_t)b * p.G + ks - 1], Ssum);
+          if (K) atomicMax(&p.resid_key[(size_t)b * kKeyStride], K);
         }
       }
       (void)ok;
@@ -1404,52 +1371,6 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
   sp.key = key;
   // the U map is not read in this mode; any valid map will do
   kern<<<mtiles * per, kThreads, kSmemBytes, stream>>>(map, map, sp);
-  return cudaGetLastError();
-}
-
-// The acceptance label of every verified position on the tensor cores: for
-// k = 1..G, one launch of the residual pipeline in label mode over the
-// requests with k <= ell_b, adding sum_v min(p_d(v), p_t(v)) into label[b][k-1]
-// (label zeroed by the caller; row_part holds the target rows' partials).
-cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const void* W1, const void* W2,
-                                       const int32_t* anchor, const int32_t* x, const float* lse_d,
-                                       const int32_t* ell, const float2* row_part, int nsegs, float* label, int B,
-                                       int G, int V, int* status, cudaStream_t stream) {
-  CUtensorMap map;
-  cudaError_t e = make_w2_tensor_map(W2, V, &map);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int R = B <= 32 ? 32 : (B <= 64 ? 64 : BM);
-  auto kern = R == 32 ? draft_step_tc<32, kLabel> : (R == 64 ? draft_step_tc<64, kLabel> : draft_step_tc<BM, kLabel>);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const int mtiles = div_up(B, R);
-  const int ntiles = div_up(V, BN);
-  int per = std::max(1, sms / mtiles);
-  per = std::min(per, ntiles);
-  StepParams sp{};
-  sp.U = U;
-  sp.W1 = static_cast<const __nv_bfloat16*>(W1);
-  sp.anchor = anchor;
-  sp.T = T;
-  sp.x = x;
-  sp.lse_d = lse_d;
-  sp.ell = ell;
-  sp.row_part = row_part;
-  sp.nsegs = nsegs;
-  sp.label = label;
-  sp.status = status;
-  sp.B = B; sp.G = G; sp.V = V;
-  sp.k_first = sp.k_last = 0;
-  sp.nctas = mtiles * per;
-  sp.ctas_per_mtile = per;
-  sp.ntiles = ntiles;
-  for (int k = 1; k <= G; ++k) {
-    sp.k_fixed = k;
-    kern<<<mtiles * per, kThreads, kSmemBytes, stream>>>(map, map, sp);
-  }
   return cudaGetLastError();
 }
 

@@ -2,6 +2,7 @@
 // kernels on `stream` and returns the cudaError_t of the launch.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -88,18 +89,26 @@ bool draft_tc_supported(int wdtype, int r, int V);
 // 256 bytes.
 cudaError_t launch_selftest_wait(int mode, void* ws, cudaStream_t stream);
 cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream);
+
+// Tensor maps of the tensor-core kernels: W2 [V, 256] bf16 in 64 x 192 boxes
+// (128-byte swizzle); a [B, G, V] fp32 tensor in [R rows x 1 x 32 columns]
+// boxes (128-byte swizzle).
+cudaError_t make_w2_tensor_map(const void* W2, int V, CUtensorMap* map);
+cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtensorMap* map);
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
                                const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* resid_k,
                                const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
                                RngKey key, int* status, cudaStream_t stream);
 
-// Acceptance labels (tensor-core path): sum_v min(p_d, p_t) per verified
-// position into label [B][G] (zeroed by the caller), from the target-row
-// partials of launch_row_stats.
+// Acceptance labels (tensor-core path, one persistent launch over the
+// positions): sum_v min(p_d, p_t) per verified position into label [B][G]
+// (zeroed by the caller), from target-row partials already in the workspace
+// (row_part, nsegs per row).
 cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const void* W1, const void* W2,
                                        const int32_t* anchor, const int32_t* x, const float* lse_d,
-                                       const int32_t* ell, const float2* row_part, int nsegs, float* label, int B,
-                                       int G, int V, int* status, cudaStream_t stream);
+                                       const int32_t* ell, const float2* row_part, int nsegs,
+                                       const int* stats_done, float* label, int B, int G, int V, int* status,
+                                       cudaStream_t stream);
 
 // The softmax partials of the target rows j < ell_b of every request into the
 // workspace (verify's first two kernels); ell == nullptr takes every row

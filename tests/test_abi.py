@@ -194,6 +194,10 @@ def test_acceptance_label_and_sts_argument_errors(lib):
                                        None) == ds.ERR_UNSUPPORTED
     assert lib.dspark_acceptance_label(p, p, p, p, 1, p, p, p, p, 2, 4, 1024, 256, p, ws, 16,
                                        None) == ds.ERR_WORKSPACE
+    # the statistics-source flags: not both, no other bits
+    for flags in (ds.EARLY_TARGET_STATS | ds.TARGET_STATS_FROM_VERIFY, 8, ds.ADVANCE_ROUND):
+        assert lib.dspark_acceptance_label_ex(p, p, p, p, 1, p, p, p, p, 2, 4, 1024, 256, flags, p, ws, big,
+                                              None) == ds.ERR_INVALID
     # STS: workspace size grows with the samples and the grid; bad arguments
     assert lib.dspark_sts_workspace_size(0, 4, 8) == 0
     assert lib.dspark_sts_workspace_size(10000, 4, 49) > lib.dspark_sts_workspace_size(100, 4, 49) > 0

@@ -44,25 +44,34 @@ def _check(w, inp, out, label, reqs):
     return checked
 
 
-def _round(w, inp):
-    out = ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed, rnd=0,
-                   sps=inp["sps"], mode=w.mode)
-    return out
+def _round(w, inp, ws=None, early=False):
+    return ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed, rnd=0,
+                    sps=inp["sps"], mode=w.mode, ws=ws, early_stats=early)
 
 
-@pytest.mark.parametrize("B", [24, 130])
-def test_labels_match_the_oracle(B):
+def _labels(w, inp, stats):
+    # stats None: the label call streams the target rows' statistics itself;
+    # "early": the round's draft took them; "verify": the round's verification
+    # did (both on the workspace the label call is given)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    out = _round(w, inp, ws=ws if stats else None, early=stats == "early")
+    label = ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], out.x, out.lse, out.ell,
+                                ws=ws, stats=stats)
+    torch.cuda.synchronize()
+    assert ds.read_status(ws) == ds.OK
+    return out, label
+
+
+@pytest.mark.parametrize("stats", [None, "early", "verify"])
+@pytest.mark.parametrize("B", [24, 60, 130])
+def test_labels_match_the_oracle(B, stats):
     # a falling steps-per-second curve makes ell vary across requests; B = 130
-    # takes two 128-row tiles, B = 24 replicated rows
+    # takes two 128-row tiles, B = 24 and 60 replicated rows (32 and 64 per
+    # tile); V = 8200 ends in a ragged 8-column tile
     w = wl.custom(B=B, gamma=4, V=8200, r=256, H=64, wdtype=torch.bfloat16, u_sigma=2.5, t_sigma=(0.4, 1.5),
                   seed=17, sps_b0=float(2 * B), sps_kind="steps")
     inp = wl.make_inputs(w, 0, DEV)
-    out = _round(w, inp)
-    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
-    label = ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], out.x, out.lse, out.ell,
-                                ws=ws)
-    torch.cuda.synchronize()
-    assert ds.read_status(ws) == ds.OK
+    out, label = _labels(w, inp, stats)
     ell = out.ell.cpu().numpy()
     assert 0 < ell.sum() < w.B * w.gamma   # both verified and unverified positions
     assert _check(w, inp, out, label, range(w.B)) == int(ell.sum())
@@ -70,15 +79,34 @@ def test_labels_match_the_oracle(B):
     assert np.all((lab >= 0.0) & (lab <= 1.0 + 1e-5))
 
 
+def test_label_sources_agree():
+    # the three sources of the target rows' statistics give labels within
+    # float rounding of one another (the partials differ only in segment size)
+    w = wl.custom(B=40, gamma=3, V=40000, r=256, H=64, wdtype=torch.bfloat16, u_sigma=2.0, t_sigma=(0.5, 1.2),
+                  seed=5, sps_b0=1e6)
+    inp = wl.make_inputs(w, 0, DEV)
+    labs = [_labels(w, inp, s)[1] for s in (None, "early", "verify")]
+    for lab in labs[1:]:
+        torch.testing.assert_close(lab, labs[0], rtol=1e-4, atol=1e-6)
+
+
+def test_missing_early_statistics_are_reported():
+    # a round whose draft did not take the statistics leaves the draft's count
+    # of row segments at zero: the label call with stats="early" reports it
+    w = wl.custom(B=8, gamma=2, V=4096, r=256, H=64, wdtype=torch.bfloat16, seed=3, sps_b0=1e6)
+    inp = wl.make_inputs(w, 0, DEV)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    out = _round(w, inp, ws=ws, early=False)
+    ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], out.x, out.lse, out.ell, ws=ws,
+                        stats="early")
+    torch.cuda.synchronize()
+    assert ds.read_status(ws) == ds.ERR_INVALID
+
+
 def test_labels_full_vocabulary_sampled():
     w = wl.WORKLOADS["batch128"]
     inp = wl.make_inputs(w, 0, DEV)
-    out = _round(w, inp)
-    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
-    label = ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], out.x, out.lse, out.ell,
-                                ws=ws)
-    torch.cuda.synchronize()
-    assert ds.read_status(ws) == ds.OK
-    assert _check(w, inp, out, label, [0, w.B - 1]) > 0
+    out, label = _labels(w, inp, "early")
+    assert _check(w, inp, out, label, [0, 37, 64, 101, w.B - 1]) > 0
     del inp
     torch.cuda.empty_cache()
