@@ -103,25 +103,35 @@ def fused_draft_bytes_per_launch(w):
     return draft_bytes_per_launch(w) + 4 * w.B * w.gamma * w.V
 
 
+def stage_bytes_per_launch(w, early=True):
+    """The first stage of a round (dspark_draft_schedule: draft, confidences,
+    schedule): the draft's bytes, the target rows j < gamma once when taken
+    along, the hidden states h and the head's w once, and c and ell out."""
+    sw = 2 if w.wdtype == torch.bfloat16 else 4
+    b = draft_bytes_per_launch(w) + sw * w.B * w.gamma * w.H + 4 * (w.H + w.r) + 4 * w.B * w.gamma + 4 * w.B
+    return b + (4 * w.B * w.gamma * w.V if early else 0)
+
+
 def kernels_per_round(w, early=False):
     """Launches of this library's kernels in one round (cudaMemsetAsync not
-    counted): draft = the persistent tensor-core kernel, which also finishes
-    x, p and lse after a last grid barrier (bf16, r = 256, V >= 192; else a
-    CUDA-core step and finalize per position; with early statistics on that
-    path a prep and a row-statistics kernel follow);
-    confidence; schedule; verify = prep and row statistics (not with early
-    statistics), decide, bonus race, residual (the draft kernel in residual
-    mode, or its CUDA-core form), residual finalize."""
+    counted).  First stage: on the tensor-core path (bf16, r = 256,
+    V >= 192) one persistent kernel, which also finishes x, p, lse and the
+    confidences after a last grid barrier and runs the schedule in its last
+    CTA; else a CUDA-core step and finalize per position (with early
+    statistics a prep and a row-statistics kernel follow), the confidence
+    and the schedule kernels.  Verify: prep and row statistics (not with
+    early statistics), decide, bonus race, residual (the draft kernel in
+    residual mode, or its CUDA-core form), residual finalize."""
     tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
-    draft = 1 if tc else 2 * w.gamma + (2 if early else 0)
+    stage = 1 if tc else 2 * w.gamma + (2 if early else 0) + 2
     verify = 4 if early else 6
-    return draft + 1 + 1 + verify
+    return stage + verify
 
 
 # Source files of a profiled kernel: a committed ncu figure counts only while
 # they are unchanged since the capture.  The figure itself is a small JSON
 # record beside the prose summary in profiles/.
-DRAFT_SOURCES = ["draft_tc.cu", "tc_common.cuh", "common.cuh"]
+DRAFT_SOURCES = ["draft_tc.cu", "tc_common.cuh", "common.cuh", "conf.cuh", "sched.cuh"]
 DRAFT_PROFILE = os.path.join(ROOT, "profiles", "draft_step_tc_batch128.json")
 LABEL_SOURCES = ["label_tc.cu", "tc_common.cuh", "common.cuh"]
 LABEL_PROFILE = os.path.join(ROOT, "profiles", "label_tc_batch128.json")
@@ -347,31 +357,32 @@ def job_units(units, device):
 # GPU arm
 # ---------------------------------------------------------------------------
 class RoundTimer:
-    """Rounds of one workload through the public entry points, in the order
-    dspark_round runs them (draft, confidence, schedule, verify), on the
-    current stream; events around the draft call give its duration inside the
-    same timed rounds."""
+    """Rounds of one workload through the public entry points that
+    dspark_round runs (draft_schedule: draft, confidences and schedule; then
+    verify), on the current stream; events around the first stage give its
+    duration inside the same timed rounds."""
 
     def __init__(self, ds, w, inp, dev, early, sps=None, khist=None, ws=None):
         self.ds, self.w, self.inp, self.dev, self.early = ds, w, inp, dev, early
         self.sps = inp["sps"] if sps is None else sps
         self.khist = khist
         self.ws = ds.workspace(w.B, w.gamma, w.V, dev) if ws is None else ws
+        self.out = ds.RoundOutputs(w.B, w.gamma, dev)
         self.stream = torch.cuda.current_stream(dev)
 
-    def step(self, i, d0=None, d1=None):
+    def step(self, i, d0=None, d1=None, out=None):
         ds, w, inp = self.ds, self.w, self.inp
         if d0 is not None:
             d0.record(self.stream)
-        x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, i, ws=self.ws,
-                                    T_early=inp["T"] if self.early else None)
+        o = ds.draft_schedule(inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], w.seed, i,
+                              sps=self.sps, mode=w.mode, khist=self.khist, out=self.out if out is None else out,
+                              ws=self.ws,
+                              T_early=inp["T"] if self.early else None)
         if d1 is not None:
             d1.record(self.stream)
-        c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
-        ell, _, _ = ds.schedule(c, self.sps, w.mode, i, self.khist, self.ws)
-        n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, i,
-                         self.ws, early_stats=self.early)
-        return ell, n
+        n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], o.x, o.p, o.lse, o.ell, w.seed, i,
+                         self.ws, early_stats=self.early, scratch_from_draft=True)
+        return o.ell, n
 
     def run(self, steps, warmup, rnd0=0, barrier=None, soak_s=0.0):
         """Warm-up rounds, an optional untimed soak, then `steps` timed rounds.
@@ -391,12 +402,14 @@ class RoundTimer:
                 j += 1
                 if j % 32 == 0:
                     torch.cuda.synchronize()
+        # each timed round writes outputs of its own (no copies in the timed region)
+        bufs = [self.ds.RoundOutputs(self.w.B, self.w.gamma, self.dev) for _ in range(steps)]
         dstart = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         dend = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         (barrier or torch.cuda.synchronize)()
         e0.record(self.stream)
-        outs = [self.step(rnd0 + warmup + i, dstart[i], dend[i]) for i in range(steps)]
+        outs = [self.step(rnd0 + warmup + i, dstart[i], dend[i], bufs[i]) for i in range(steps)]
         e1.record(self.stream)
         (barrier or torch.cuda.synchronize)()
         st = self.ds.read_status(self.ws)
@@ -414,7 +427,7 @@ def round_record(w, r, hbm, early):
     ms = r["ms"] / steps
     per_round = r["ell_sum"] / steps
     rb = round_bytes(w, per_round, r["n_rej"] / steps)
-    db = fused_draft_bytes_per_launch(w) if early else draft_bytes_per_launch(w)
+    db = stage_bytes_per_launch(w, early)
     return {"ms": ms, "verified_per_round": per_round, "accepted_per_round": r["n_acc"] / steps,
             "verified_tokens_per_s": r["ell_sum"] / (r["ms"] / 1e3),
             "accepted_tokens_per_s": r["n_acc"] / (r["ms"] / 1e3),
@@ -525,10 +538,11 @@ def run_gpu(args):
     per_round = ell_sum / args.steps
     value = job_units(ell_sum, dev) / (ms / 1e3)
 
-    # dominant kernel: the Markov draft (with the target-row statistics when
-    # early), timed inside the timed region
+    # dominant kernel: the round's first stage (one persistent launch: the
+    # Markov draft with the target-row statistics when early, the confidences
+    # and the schedule), timed inside the timed region
     draft_ms = r["draft_ms"]
-    dbytes = fused_draft_bytes_per_launch(w) if early else draft_bytes_per_launch(w)
+    dbytes = stage_bytes_per_launch(w, early)
     achieved = dbytes / (draft_ms / 1e3) / 1e9
 
     extra = {}
@@ -648,9 +662,12 @@ def run_gpu(args):
                        "round_GB": rbytes / 1e9,
                        "round_hbm_frac": rbytes / (ms / args.steps / 1e3) / 1e9 / hbm,
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"kernel": "markov draft taking the target rows' statistics along "
-                                   "(dspark_markov_draft_ex: draft_step_tc with its fused finalize)"
-                         if early else "markov draft (dspark_markov_draft: draft_step_tc with its fused finalize)",
+            "roofline": {"kernel": "the round's first stage, one persistent launch (dspark_draft_schedule: "
+                                   "draft_step_tc drafting, taking the target rows' statistics along, then its "
+                                   "fused finalize with the confidences and the schedule)"
+                         if early else "the round's first stage, one persistent launch (dspark_draft_schedule: "
+                                       "draft_step_tc drafting, then its fused finalize with the confidences and "
+                                       "the schedule)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": draft_traffic(w, early), "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
@@ -733,9 +750,10 @@ def run_e2e(w, inp, ds, dev, args, khist, early):
 
 
 def run_profile_draft(args):
-    """The Markov draft of the workload alone, 4 calls, taking the target
-    rows' statistics along unless --plain-draft (for ncu: U, T, W1, W2 and the
-    anchors are all it holds on the device)."""
+    """The round's first stage of the workload alone (dspark_draft_schedule:
+    draft, confidences, schedule), 4 calls, taking the target rows'
+    statistics along unless --plain-draft (for ncu: U, T, h, the weights and
+    the anchors are all it holds on the device)."""
     import speculative_decoding_02_gb300 as ds
     from speculative_decoding_02_gb300 import build as lib_build
     from speculative_decoding_02_gb300 import workloads as wl
@@ -744,12 +762,14 @@ def run_profile_draft(args):
     w = wl.WORKLOADS[args.workload]
     weights = wl.make_weights(w, dev)
     rin = wl.make_round_inputs(w, 0, dev)
-    U = rin["U"]
+    sps = wl.sps_table(w)
+    sps = None if sps is None else sps.to(dev)
+    khist = torch.zeros(2, dtype=torch.int32, device=dev)
     T = None if args.plain_draft else rin["T"]
-    del rin["h"]
     ws = ds.workspace(w.B, w.gamma, w.V, dev)
     for i in range(4):
-        ds.markov_draft(U, weights["W1"], weights["W2"], weights["anchor"], w.seed, i, ws=ws, T_early=T)
+        ds.draft_schedule(rin["U"], weights["W1"], weights["W2"], rin["h"], weights["w"], weights["anchor"], w.seed,
+                          i, sps=sps, mode=w.mode, khist=khist, ws=ws, T_early=T)
     torch.cuda.synchronize()
     st = ds.read_status(ws)
     print(json.dumps({"profile_draft": w.name, "early_target_stats": T is not None, "status": st,

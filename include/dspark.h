@@ -75,6 +75,7 @@ extern "C" {
 #define DSPARK_EARLY_TARGET_STATS 1u  /* the draft took the target rows' softmax statistics */
 #define DSPARK_ADVANCE_ROUND 2u       /* the call's last kernel adds 1 to *round_dev */
 #define DSPARK_TARGET_STATS_FROM_VERIFY 4u  /* dspark_acceptance_label_ex: a verification left them */
+#define DSPARK_SCRATCH_FROM_DRAFT 8u  /* dspark_verify_ex: dspark_draft_schedule cleared the scratch */
 
 /* Bytes of device scratch the entry points below need for these sizes; 0 when
  * a size is not positive. */
@@ -199,6 +200,11 @@ int dspark_verify(const float* T, const float* U, const void* W1, const void* W2
  *  - round_dev: the round index as a device word (see dspark_markov_draft_ex).
  *  - DSPARK_ADVANCE_ROUND (needs round_dev): the call's last kernel adds 1 to
  *    *round_dev after every kernel of the call has read it.
+ *  - DSPARK_SCRATCH_FROM_DRAFT: a dspark_draft_schedule on the same workspace,
+ *    earlier in stream order, cleared this call's scratch (its argmax keys and
+ *    bonus list; the tensor-core path does, others ignore the flag), so the
+ *    call skips its memset and its kernels run as one chain of dependent
+ *    launches.
  * Other flag bits return DSPARK_ERR_INVALID.
  */
 int dspark_verify_ex(const float* T, const float* U, const void* W1, const void* W2,
@@ -269,8 +275,31 @@ int dspark_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * One whole round: draft, confidence, schedule, verify, enqueued in that order
- * on one stream with no host synchronisation.  Arguments as above.  A round
+ * The first stage of a round: the Markov draft, the confidence head of every
+ * drafted position and the schedule (blog sections 4-7; study report Eq.7),
+ * with the arguments of dspark_markov_draft_ex, dspark_confidence and
+ * dspark_schedule_ex.  T_early (may be NULL) is taken along as in
+ * dspark_markov_draft_ex.  On the tensor-core path (bf16, r = 256) this is
+ * one persistent launch: its finalize computes the confidences and the last
+ * CTA to finish it runs the schedule (up to 4096 candidates; beyond, a
+ * schedule kernel follows) while the others stream the target-row
+ * statistics; it also clears the verification's scratch
+ * (DSPARK_SCRATCH_FROM_DRAFT).  Other paths run the three kernels in turn.
+ * Errors as for those three calls.
+ */
+int dspark_draft_schedule(const float* U, const float* T_early, const void* W1, const void* W2,
+                          int wdtype, const void* h, int hdtype, const float* w,
+                          const float* sts_T, const int32_t* anchor,
+                          int B, int gamma, int V, int r, int H,
+                          const float* sps, int n_sps, int mode, int32_t* khist,
+                          uint64_t seed, uint64_t round, uint64_t* round_dev,
+                          int32_t* x_out, float* p_out, float* lse_out, float* c_out,
+                          int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One whole round: dspark_draft_schedule, then dspark_verify_ex, enqueued in
+ * that order on one stream with no host synchronisation.  Arguments as above.  A round
  * can be captured into a CUDA graph (the draft's cooperative launch
  * included); a replay repeats the captured seed and round (dspark_round_ex
  * with a device round index advances it).

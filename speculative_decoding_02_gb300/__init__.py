@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libdspark.so")
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NONFINITE = range(7)
 F32, BF16 = 0, 1
 SCHED_FIXED, SCHED_GREEDY, SCHED_TOPK = 0, 1, 2
-EARLY_TARGET_STATS, ADVANCE_ROUND, TARGET_STATS_FROM_VERIFY = 1, 2, 4
+EARLY_TARGET_STATS, ADVANCE_ROUND, TARGET_STATS_FROM_VERIFY, SCRATCH_FROM_DRAFT = 1, 2, 4, 8
 
 
 class DSparkError(RuntimeError):
@@ -80,6 +80,9 @@ def _load():
     L.dspark_round_ex.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
                                   vp, u64, u64, vp, ctypes.c_uint, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_round_ex.restype = i32
+    L.dspark_draft_schedule.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32,
+                                        i32, vp, u64, u64, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.dspark_draft_schedule.restype = i32
     L.dspark_read_status.argtypes = [vp, ctypes.POINTER(i32), vp]
     L.dspark_read_status.restype = i32
     L.dspark_selftest_wait_timeout.argtypes = [i32, vp, sz, vp]
@@ -238,11 +241,12 @@ def schedule(c, sps=None, mode=SCHED_GREEDY, rnd=0, khist=None, ws=None, round_d
 
 
 def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None, early_stats=False, round_dev=None,
-           advance_round=False):
+           advance_round=False, scratch_from_draft=False):
     """n [B] i32 accepted counts, tok [B] i32 corrected / bonus tokens.
     early_stats: ws already holds the target-row statistics from
     markov_draft(T_early=T).  round_dev / advance_round: the round index as a
-    device int64 [1], advanced by the call's last kernel."""
+    device int64 [1], advanced by the call's last kernel.
+    scratch_from_draft: a draft_schedule on ws cleared the call's scratch."""
     L = _load()
     _need(T, "T", torch.float32)
     dev = T.device
@@ -262,7 +266,8 @@ def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None, early
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
     rd = _round_dev(round_dev, dev)
-    flags = (EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0)
+    flags = ((EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0) |
+             (SCRATCH_FROM_DRAFT if scratch_from_draft else 0))
     _check(L.dspark_verify_ex(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x),
                               _ptr(p_d), _ptr(lse_d), _ptr(ell), B, G, V, r, seed, rnd, rd, flags, _ptr(n), _ptr(tok),
                               _ptr(ws), ws.numel(), _stream(dev)), "verify")
@@ -348,20 +353,15 @@ class RoundOutputs:
             _sized(t, f"out.{name}", shape)
 
 
-def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
-          out=None, ws=None, early_stats=False, round_dev=None, advance_round=False):
-    """One whole round (draft, confidence, schedule, verify) on U's device.
-    early_stats: the draft takes the target rows' statistics while it runs.
-    round_dev / advance_round: the round index as a device int64 [1] (rnd
-    ignored), advanced by the round's last kernel.
-    Returns a RoundOutputs (device tensors)."""
-    L = _load()
+def _round_args(U, T, W1, W2, h, w, anchor, sps, khist, sts_T):
+    # shared checks of round and draft_schedule (T may be None for the latter)
     _need(U, "U", torch.float32)
     dev = U.device
     B, G, V = U.shape
-    _need(T, "T", torch.float32, dev)
-    if tuple(T.shape) != (B, G + 1, V):
-        raise ValueError(f"T must be [B, gamma+1, V] = {(B, G + 1, V)}, got {tuple(T.shape)}")
+    if T is not None:
+        _need(T, "T", torch.float32, dev)
+        if tuple(T.shape) != (B, G + 1, V):
+            raise ValueError(f"T must be [B, gamma+1, V] = {(B, G + 1, V)}, got {tuple(T.shape)}")
     _need(W1, "W1", device=dev); _need(W2, "W2", W1.dtype, dev); _need(h, "h", device=dev)
     _need(w, "w", torch.float32, dev); _need(anchor, "anchor", torch.int32, dev)
     if sps is not None:
@@ -375,6 +375,40 @@ def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, 
     r, H = W1.shape[-1], h.shape[2]
     _sized(W1, "W1", (V, r)); _sized(W2, "W2", (V, r)); _sized(h, "h", (B, G, H)); _sized(w, "w", (H + r,))
     _sized(anchor, "anchor", (B,)); _sized(khist, "khist", (2,)); _sized(sts_T, "sts_T", (G,))
+    return dev, B, G, V, r, H
+
+
+def draft_schedule(U, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
+                   out=None, ws=None, T_early=None, round_dev=None):
+    """The first stage of a round (draft, confidence head, schedule; one
+    persistent launch on the tensor-core path) into out.x, p, lse, c, ell,
+    nstar, theta.  T_early: target logits whose statistics the draft takes
+    along.  Returns the RoundOutputs."""
+    L = _load()
+    dev, B, G, V, r, H = _round_args(U, T_early, W1, W2, h, w, anchor, sps, khist, sts_T)
+    out = RoundOutputs(B, G, dev) if out is None else out
+    out.check(B, G, dev)
+    ws = workspace(B, G, V, dev) if ws is None else ws
+    n_sps = 0 if sps is None else sps.numel()
+    rd = _round_dev(round_dev, dev)
+    _check(L.dspark_draft_schedule(_ptr(U), _ptr(T_early), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h), _dt(h, "h"),
+                                   _ptr(w), _ptr(sts_T), _ptr(anchor), B, G, V, r, H, _ptr(sps), n_sps, mode,
+                                   _ptr(khist), seed, rnd, rd, _ptr(out.x), _ptr(out.p), _ptr(out.lse), _ptr(out.c),
+                                   _ptr(out.ell), _ptr(out.nstar), _ptr(out.theta), _ptr(ws), ws.numel(),
+                                   _stream(dev)), "draft_schedule")
+    return out
+
+
+def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
+          out=None, ws=None, early_stats=False, round_dev=None, advance_round=False):
+    """One whole round (draft, confidence, schedule, verify) on U's device.
+    early_stats: the draft takes the target rows' statistics while it runs.
+    round_dev / advance_round: the round index as a device int64 [1] (rnd
+    ignored), advanced by the round's last kernel.
+    Returns a RoundOutputs (device tensors)."""
+    L = _load()
+    _need(T, "T", torch.float32)
+    dev, B, G, V, r, H = _round_args(U, T, W1, W2, h, w, anchor, sps, khist, sts_T)
     out = RoundOutputs(B, G, dev) if out is None else out
     out.check(B, G, dev)
     ws = workspace(B, G, V, dev) if ws is None else ws

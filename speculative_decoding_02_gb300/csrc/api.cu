@@ -138,12 +138,15 @@ int dspark_verify_ex(const float* T, const float* U, const void* W1, const void*
   DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, n_out, tok_out,
                            workspace, workspace_bytes));
   if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
-  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND)) return DSPARK_ERR_INVALID;
+  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND | DSPARK_SCRATCH_FROM_DRAFT))
+    return DSPARK_ERR_INVALID;
   if ((flags & DSPARK_ADVANCE_ROUND) && !round_dev) return DSPARK_ERR_INVALID;
   unsigned long long* rd = reinterpret_cast<unsigned long long*>(round_dev);
+  // only the tensor-core draft of dspark_draft_schedule clears the scratch
+  const bool zeroed = (flags & DSPARK_SCRATCH_FROM_DRAFT) && draft_tc_supported(wdtype, r, V);
   VerifyArgs a{T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, make_rng_key(seed, round, rd),
                n_out, tok_out, workspace, (flags & DSPARK_EARLY_TARGET_STATS) != 0,
-               (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr};
+               (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr, zeroed};
   return cuda_status(launch_verify(a, (cudaStream_t)stream));
 }
 
@@ -209,36 +212,56 @@ int dspark_acceptance_label(const float* T, const float* U, const void* W1, cons
                                     workspace, workspace_bytes, stream);
 }
 
+int dspark_draft_schedule(const float* U, const float* T_early, const void* W1, const void* W2, int wdtype,
+                          const void* h, int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B,
+                          int gamma, int V, int r, int H, const float* sps, int n_sps, int mode, int32_t* khist,
+                          uint64_t seed, uint64_t round, uint64_t* round_dev, int32_t* x_out, float* p_out,
+                          float* lse_out, float* c_out, int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
+                          workspace_bytes));
+  DSPARK_TRY(confidence_checks(h, hdtype, W1, wdtype, w, anchor, x_out, B, gamma, H, r, V, c_out));
+  DSPARK_TRY(schedule_checks(c_out, B, gamma, sps, n_sps, mode, khist, ell_out, nstar_out, theta_out));
+  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
+  if (T_early && !aligned(T_early, 16)) return DSPARK_ERR_INVALID;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned long long* rd = reinterpret_cast<unsigned long long*>(round_dev);
+  const RngKey key = make_rng_key(seed, round, rd);
+  int* status = ws_ptr<int>(workspace, ws_layout(B, gamma, V).status);
+  // The tensor-core draft computes the confidence head in its finalize, runs
+  // the schedule in its last CTA and clears the verification's scratch on its
+  // way; the CUDA-core draft is followed by the confidence and schedule kernels.
+  const bool tc = draft_tc_supported(wdtype, r, V);
+  DraftArgs da{U, W1, W2, wdtype, anchor, B, gamma, V, r, key, x_out, p_out, lse_out, workspace, T_early, tc,
+               h, hdtype, w, sts_T, H, tc ? c_out : nullptr, sps, mode, khist, tc ? ell_out : nullptr, nstar_out,
+               theta_out};
+  DSPARK_TRY(cuda_status(launch_markov_draft(da, s)));
+  if (!tc) {
+    DSPARK_TRY(cuda_status(launch_confidence(h, hdtype, W1, wdtype, w, sts_T, anchor, x_out, B, gamma, H, r, V,
+                                             c_out, status, s)));
+    DSPARK_TRY(cuda_status(launch_schedule(c_out, B, gamma, sps, mode, round, rd, khist, ell_out, nstar_out,
+                                           theta_out, status, s)));
+  }
+  return DSPARK_OK;
+}
+
 int dspark_round_ex(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,
                     int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B, int gamma, int V,
                     int r, int H, const float* sps, int n_sps, int mode, int32_t* khist, uint64_t seed,
                     uint64_t round, uint64_t* round_dev, unsigned flags, int32_t* x_out, float* p_out,
                     float* lse_out, float* c_out, int32_t* ell_out, int32_t* nstar_out, double* theta_out,
                     int32_t* n_out, int32_t* tok_out, void* workspace, size_t workspace_bytes, void* stream) {
-  DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
-                          workspace_bytes));
-  DSPARK_TRY(confidence_checks(h, hdtype, W1, wdtype, w, anchor, x_out, B, gamma, H, r, V, c_out));
-  DSPARK_TRY(schedule_checks(c_out, B, gamma, sps, n_sps, mode, khist, ell_out, nstar_out, theta_out));
   DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, n_out,
                            tok_out, workspace, workspace_bytes));
-  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
   if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND)) return DSPARK_ERR_INVALID;
   if ((flags & DSPARK_ADVANCE_ROUND) && !round_dev) return DSPARK_ERR_INVALID;
-  cudaStream_t s = (cudaStream_t)stream;
-  unsigned long long* rd = reinterpret_cast<unsigned long long*>(round_dev);
-  const RngKey key = make_rng_key(seed, round, rd);
   const bool early = (flags & DSPARK_EARLY_TARGET_STATS) != 0;
-  int* status = ws_ptr<int>(workspace, ws_layout(B, gamma, V).status);
-  DraftArgs da{U, W1, W2, wdtype, anchor, B, gamma, V, r, key, x_out, p_out, lse_out, workspace,
-               early ? T : nullptr};
-  DSPARK_TRY(cuda_status(launch_markov_draft(da, s)));
-  DSPARK_TRY(cuda_status(launch_confidence(h, hdtype, W1, wdtype, w, sts_T, anchor, x_out, B, gamma, H, r, V,
-                                           c_out, status, s)));
-  DSPARK_TRY(cuda_status(launch_schedule(c_out, B, gamma, sps, mode, round, rd, khist, ell_out, nstar_out,
-                                         theta_out, status, s)));
-  VerifyArgs va{T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, key, n_out,
-                tok_out, workspace, early, (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr};
-  return cuda_status(launch_verify(va, s));
+  DSPARK_TRY(dspark_draft_schedule(U, early ? T : nullptr, W1, W2, wdtype, h, hdtype, w, sts_T, anchor, B, gamma, V,
+                                   r, H, sps, n_sps, mode, khist, seed, round, round_dev, x_out, p_out, lse_out,
+                                   c_out, ell_out, nstar_out, theta_out, workspace, workspace_bytes, stream));
+  return dspark_verify_ex(T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, seed, round,
+                          round_dev, flags | DSPARK_SCRATCH_FROM_DRAFT, n_out, tok_out, workspace, workspace_bytes,
+                          stream);
 }
 
 int dspark_round(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,

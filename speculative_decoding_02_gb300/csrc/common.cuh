@@ -62,6 +62,18 @@ __device__ __forceinline__ RngKey live_key(const RngKey& k) {
   return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute (launch_pdl) may begin while the kernel before
+// it in the stream is still running.  pdl_wait() returns once that kernel has
+// completed and its memory writes are visible (at once for a kernel launched
+// without the attribute), so every read of an earlier kernel's output, and
+// every write that an earlier kernel might still read, comes after it.  A
+// kernel whose every thread waits this way completes after its predecessor,
+// so the guarantee carries down the chain.  pdl_trigger() lets the next kernel
+// in the stream start launching; it releases no data.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // The round index a kernel runs (device word or host argument).
 __device__ __forceinline__ unsigned long long live_round(const RngKey& k) {
   return k.round_dev != nullptr ? __ldcg(k.round_dev) : (unsigned long long)(k.round3 >> 3);
@@ -166,6 +178,18 @@ __device__ __forceinline__ void softmax_merge(float& m, float& s, float m2, floa
   else { s = s + s2 * expf(m2 - m); }
 }
 
+// Merges n softmax partials (max, sum) from p into (m, s), eight loads in
+// flight at a time (a row's segment partials, read before the merge starts).
+__device__ __forceinline__ void merge_partials(const float2* __restrict__ p, int n, float& m, float& s) {
+  for (int i0 = 0; i0 < n; i0 += 8) {
+    float2 q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = i0 + j < n ? __ldcg(p + i0 + j) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) softmax_merge(m, s, q[j].x, q[j].y);
+  }
+}
+
 __device__ __forceinline__ void warp_softmax_reduce(float& m, float& s, unsigned mask, int width) {
   for (int off = width / 2; off > 0; off >>= 1) {
     float m2 = __shfl_xor_sync(mask, m, off, width);
@@ -245,6 +269,8 @@ struct WsLayout {
   size_t resid_key;   // u64 [B] residual key, kKeyStride apart
   size_t resid_k;     // int32 [B] rejected position k* (0 = none)
   size_t resid_lse;   // float [B] lse of the target row at k*
+  size_t resid_prev;  // int32 [B] x_{k*-1} as stored (the anchor when k* = 1)
+  size_t tx;          // float [B*gamma] T[b, k-1, x_k], gathered by a draft that takes T along
   size_t bonus_rows;  // int32 [1 + B]: count, then the requests that accepted their whole prefix
   size_t total;
 };
@@ -265,6 +291,8 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   L.resid_key = off;   off = align256(off + 8ull * kKeyStride * B);
   L.resid_k = off;     off = align256(off + 4ull * B);
   L.resid_lse = off;   off = align256(off + 4ull * B);
+  L.resid_prev = off;  off = align256(off + 4ull * B);
+  L.tx = off;          off = align256(off + 4ull * B * gamma);
   L.bonus_rows = off;  off = align256(off + 4ull * (B + 1));
   L.total = off;
   return L;

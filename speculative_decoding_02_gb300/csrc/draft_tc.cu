@@ -41,7 +41,9 @@
 #include <algorithm>
 #include <mutex>
 
+#include "conf.cuh"
 #include "kernels.h"
+#include "sched.cuh"
 #include "tc_common.cuh"
 
 namespace dspark {
@@ -94,14 +96,40 @@ struct __align__(8) Barriers {
   int abort;
   int stop;   // epilogue-wide decision to leave the position loop
   int last;   // this CTA's arrival completed the current grid barrier
+  int sched;  // this CTA finished the finalize last: it runs the schedule
 };
 static_assert(sizeof(Barriers) <= kBarBytes, "barrier block overflows its shared-memory slot");
+static_assert(sizeof(SchedShared) <= kXBytes, "the schedule's scratch overflows the combine scratch");
 static_assert(kSmemBytes <= 232448, "more dynamic shared memory than one CTA may use");
 
 enum Mode { kDraft = 0, kResidual = 1 };
 
 template <int MODE>
 __host__ __device__ constexpr int threads_of() { return MODE == kDraft ? kDraftThreads : kThreads; }
+
+// The confidence head computed by the draft's finalize (c_out null: not).
+struct ConfArgs {
+  const void* h;
+  const float* w;
+  const float* sts_T;
+  float* c_out;
+  int hdtype;
+  int H;
+  bool vec;
+};
+
+// The round's schedule run by the draft's last CTA to finish the finalize
+// (ell_out null: not; the caller launches the schedule kernel instead).
+struct SchedArgs {
+  const float* c;                       // the confidences the finalize wrote
+  const float* sps;
+  int mode;
+  int32_t* khist;
+  int32_t* ell_out;
+  int32_t* nstar_out;
+  double* theta_out;
+  unsigned int* done;                   // CTAs past the finalize (zeroed before the launch)
+};
 
 struct StepParams {
   const float* U;
@@ -112,10 +140,11 @@ struct StepParams {
   int32_t* x_out;
   float* p_out;
   float* lse_out;
-  // residual mode: rejected position k* of each request (0 = none), the draft
-  // tokens, the draft lse of every position, the target lse of row k*-1
+  // residual mode: rejected position k* of each request (0 = none), the
+  // token before it, the draft lse of every position, the target lse of row
+  // k*-1
   const float* T;
-  const int32_t* x;
+  const int32_t* resid_prev;            // x_{k*-1} (the anchor when k* = 1)
   const int32_t* resid_k;
   const float* lse_d;
   const float* resid_lse;
@@ -126,6 +155,7 @@ struct StepParams {
   // [B*(G+1)][nsegs] partial buffer of verification, stats_next a task counter
   // zeroed before the launch
   const float* T_stats;
+  float* tx;                            // [B][G] T[b, k-1, x_k] from the finalize (with T_stats)
   float2* stats_part;
   unsigned int* stats_next;
   unsigned long long* keys;             // [G][B] argmax keys of every position, kKeyStride apart
@@ -139,6 +169,12 @@ struct StepParams {
   int ctas_per_mtile;
   int ntiles;                           // vocabulary tiles of width BN
   RngKey key;
+  ConfArgs conf;                        // draft mode: the confidence head in the finalize
+  SchedArgs sched;                      // draft mode: the schedule after the finalize
+  // draft mode: the verification's scratch to clear at the start (null: none)
+  unsigned long long* vz;               // the bonus and residual argmax keys
+  int vz_words;
+  int* vz_count;                        // the bonus list's count
 };
 
 __device__ __forceinline__ int tile_begin(int slice, int nslices, int ntiles) {
@@ -605,13 +641,27 @@ __device__ void stats_tasks(const float* __restrict__ T, int B, int G, int V, in
 // The draft outputs of one (request, position), by one warp: merge the slice
 // partials into lse_k, decode x_k from its argmax key and recompute the fused
 // logit of x_k for p_k(x_k).
+// The confidence head of one finalize item, kept out of line so that its
+// loads in flight do not raise the draft loop's register count.
+__device__ __noinline__ void finalize_conf(const ConfArgs& ca, const __nv_bfloat16* __restrict__ W1, int item,
+                                           int k, int prev_x, int V, int lane, int* __restrict__ status) {
+  if (ca.hdtype == DSPARK_BF16)
+    conf_item<DSPARK_BF16, DSPARK_BF16>(ca.h, W1, ca.w, ca.sts_T, item, k, prev_x, ca.H, KR, V, ca.vec, lane,
+                                        ca.c_out, status);
+  else
+    conf_item<DSPARK_F32, DSPARK_BF16>(ca.h, W1, ca.w, ca.sts_T, item, k, prev_x, ca.H, KR, V, ca.vec, lane,
+                                       ca.c_out, status);
+}
+
 __device__ __forceinline__ void finalize_item(int item, int lane, const float* __restrict__ U,
                                               const __nv_bfloat16* __restrict__ W1,
                                               const __nv_bfloat16* __restrict__ W2, const int32_t* __restrict__ anchor,
                                               const unsigned long long* __restrict__ keys,
                                               const float2* __restrict__ part, int B, int G, int V, int nslices,
                                               int part_slices, int32_t* __restrict__ x_out, float* __restrict__ p_out,
-                                              float* __restrict__ lse_out, int* __restrict__ status) {
+                                              float* __restrict__ lse_out, const ConfArgs& ca,
+                                              const float* __restrict__ T_early, float* __restrict__ tx,
+                                              int* __restrict__ status) {
   const int b = item / G, k = item - (item / G) * G + 1;
   const float2* pp = part + (size_t)(k - 1) * part_slices * B;
   float m = -INFINITY, s = 0.f;
@@ -627,8 +677,14 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
     if (lane == 0) record_status(status, DSPARK_ERR_NONFINITE);
     x = 0;
   }
-  int prev = (k == 1) ? anchor[b] : argmax_key_index(__ldcg(keys + ((size_t)(k - 2) * B + b) * kKeyStride));
-  prev = checked_token(prev, V, status);
+  // x_{k-1} as the output holds it (the anchor at k = 1)
+  int prev_x = anchor[b];
+  if (k > 1) {
+    const unsigned long long kp = __ldcg(keys + ((size_t)(k - 2) * B + b) * kKeyStride);
+    prev_x = kp ? argmax_key_index(kp) : -1;
+    if (prev_x < 0 || prev_x >= V) prev_x = 0;
+  }
+  const int prev = checked_token(prev_x, V, status);
   float dot = 0.f;
   for (int i = lane; i < KR; i += 32)
     dot = fmaf(__bfloat162float(W1[(size_t)prev * KR + i]), __bfloat162float(W2[(size_t)x * KR + i]), dot);
@@ -638,7 +694,10 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
     x_out[o] = x;
     p_out[o] = expf(U[o * (size_t)V + x] + dot - lse);
     lse_out[o] = lse;
+    // the target logit of the drafted token, for the accept test (T taken along)
+    if (T_early != nullptr) tx[o] = T_early[((size_t)b * (G + 1) + (k - 1)) * V + x];
   }
+  if (ca.c_out != nullptr) finalize_conf(ca, W1, item, k, prev_x, V, lane, status);
 }
 
 // MODE kDraft: draft positions k_first..k_last for every request (U rows by
@@ -676,6 +735,17 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   const int kf = p.k_first, kl = p.k_last;
   volatile int* abort = &bars->abort;
   const RngKey key = live_key(p.key);
+  if constexpr (MODE == kDraft) {
+    if (p.vz != nullptr) {
+      for (int i = blockIdx.x * threads_of<MODE>() + threadIdx.x; i < p.vz_words; i += gridDim.x * threads_of<MODE>())
+        p.vz[i] = 0ull;
+      if (blockIdx.x == 0 && threadIdx.x == 0) *p.vz_count = 0;
+    }
+  }
+  // draft mode: the next kernel in the stream may start launching (it waits
+  // for this one, on SMs this grid has left); residual mode: no early trigger,
+  // the next kernel's waiting CTAs would share the SMs of this one
+  if constexpr (MODE == kDraft) pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) { mbar_init(&bars->full_w[s], 1); mbar_init(&bars->empty_w[s], 1); }
@@ -698,6 +768,11 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // residual mode: the set-up above overlapped the kernel before this one; its
+  // outputs (the rejected positions, the keys to raise) are read by the
+  // epilogue warps from here on.  The producer (W2 only) and the MMA issuer
+  // read nothing an earlier kernel writes, so the W2 atoms start loading now.
+  if (warp >= 2) pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -803,8 +878,14 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     for (int k = kf; k <= kl; ++k) {
       bool active = r < rows_valid;
       int ks = k;                           // position of this row
+      int res_prev = 0;
       if constexpr (MODE == kResidual) {
-        ks = active ? p.resid_k[b] : 0;
+        if (active) {
+          ks = p.resid_k[b];
+          res_prev = p.resid_prev[b];       // (loaded with ks; read only if ks > 0)
+        } else {
+          ks = 0;
+        }
         active = ks > 0;
       }
 
@@ -820,7 +901,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
                 : spec_final ? spec_raw
                              : argmax_key_index(__ldcg(p.keys + ((size_t)(k - 2) * p.B + b) * kKeyStride));
         else
-          raw = (ks == 1) ? p.anchor[b] : p.x[(size_t)b * p.G + ks - 2];
+          raw = res_prev;
         prev = checked_token(raw, p.V, p.status);
       }
       const uint32_t e_taddr = tmem + ((uint32_t)(q * 32) << 16) + kTmemE + h * 32;
@@ -1089,10 +1170,13 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
           }
         }
         // one thread takes the decision to go on, all epilogue warps read it
-        // after the same barrier, so they all leave the loop together
+        // after the same barrier, so they all leave the loop together.  The
+        // last CTA to arrive saw the count complete in its own arrival (an
+        // acquire), so it does not wait.
         if (warp == 2 && lane == 0) {
           bool go = !*abort;
-          if (go) go = grid_wait(p.gbar, (uint32_t)(p.nctas * (k - kf + 1)), abort, p.status);
+          if (go && !(kShare && bars->last))
+            go = grid_wait(p.gbar, (uint32_t)(p.nctas * (k - kf + 1)), abort, p.status);
           bars->stop = go ? 0 : 1;
         }
         named_bar_sync(1, kEpiWarps * 32);
@@ -1118,7 +1202,27 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         if (!bars->stop) {
           for (int item = blockIdx.x * kEpiWarps + (warp - 2); item < p.B * p.G; item += p.nctas * kEpiWarps)
             finalize_item(item, lane, p.U, p.W1, p.W2, p.anchor, p.keys, p.part, p.B, p.G, p.V, p.ctas_per_mtile,
-                          p.part_slices, p.x_out, p.p_out, p.lse_out, p.status);
+                          p.part_slices, p.x_out, p.p_out, p.lse_out, p.conf, p.T_stats, p.tx, p.status);
+          if (p.sched.ell_out != nullptr) {
+            // The last CTA to finish its finalize items (every confidence is
+            // written then) runs the round's schedule in its shared memory
+            // (the rings are idle now) while the other CTAs go on to the
+            // target-row statistics.
+            named_bar_sync(1, kEpiWarps * 32);
+            if (warp == 2 && lane == 0) {
+              __threadfence();
+              bars->sched = atomicAdd(p.sched.done, 1u) == (unsigned int)p.nctas - 1u ? 1 : 0;
+            }
+            named_bar_sync(1, kEpiWarps * 32);
+            if (bars->sched) {
+              __threadfence();
+              SchedShared* sh = reinterpret_cast<SchedShared*>(X_s);
+              schedule_block<kEpiWarps * 32>(p.sched.c, p.B, p.G, p.sched.sps, p.sched.mode, live_round(p.key),
+                                             p.sched.khist, p.sched.ell_out, p.sched.nstar_out, p.sched.theta_out,
+                                             p.status, smem, *sh, (int)threadIdx.x - 64,
+                                             NamedSync<kEpiWarps * 32>{});
+            }
+          }
         }
       }
       // the draft is done: the epilogue warps help with whatever target-row
@@ -1146,11 +1250,12 @@ __global__ void draft_finalize_tc(const float* __restrict__ U, const __nv_bfloat
                                   const __nv_bfloat16* __restrict__ W2, const int32_t* __restrict__ anchor,
                                   const unsigned long long* __restrict__ keys, const float2* __restrict__ part,
                                   int B, int G, int V, int nslices, int part_slices, int32_t* __restrict__ x_out,
-                                  float* __restrict__ p_out, float* __restrict__ lse_out, int* __restrict__ status) {
+                                  float* __restrict__ p_out, float* __restrict__ lse_out, const ConfArgs ca,
+                                  const float* __restrict__ T_early, float* __restrict__ tx, int* __restrict__ status) {
   const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (item >= B * G) return;
   finalize_item(item, threadIdx.x & 31, U, W1, W2, anchor, keys, part, B, G, V, nslices, part_slices, x_out, p_out,
-                lse_out, status);
+                lse_out, ca, T_early, tx, status);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1260,8 +1365,9 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * kKeyStride * (size_t)a.gamma * a.B, stream);
   if (e != cudaSuccess) return e;
-  // the grid-barrier counter and the target-statistics task counter after it
-  if ((e = cudaMemsetAsync(gbar, 0, 2 * sizeof(unsigned int), stream)) != cudaSuccess) return e;
+  // the grid-barrier counter, the target-statistics task counter and the
+  // count of CTAs past the finalize after it
+  if ((e = cudaMemsetAsync(gbar, 0, 3 * sizeof(unsigned int), stream)) != cudaSuccess) return e;
 
   const int mtiles = div_up(a.B, R);
   const int ntiles = div_up(a.V, BN);
@@ -1286,6 +1392,14 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   sp.nsegs = stats_num_segs(a.V);
   sp.stats_part = ws_ptr<float2>(a.ws, L.row_part);
   sp.stats_next = gbar + 1;
+  sp.tx = ws_ptr<float>(a.ws, L.tx);
+  if (a.c_out != nullptr)
+    sp.conf = ConfArgs{a.h, a.w, a.sts_T, a.c_out, a.hdtype, a.H, conf_vec(a.h, a.W1, a.w, a.H, a.r)};
+  if (a.zero_verify_scratch) {
+    sp.vz = ws_ptr<unsigned long long>(a.ws, L.bonus_key);
+    sp.vz_words = (int)((L.resid_k - L.bonus_key) / sizeof(unsigned long long));
+    sp.vz_count = ws_ptr<int>(a.ws, L.bonus_rows);
+  }
 
   // One persistent launch over all positions when every CTA can be resident
   // at once (one CTA per SM); otherwise one launch per position.
@@ -1293,9 +1407,18 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, kDraftThreads, kSmemBytes)) !=
       cudaSuccess)
     return e;
+  const bool want_sched = a.ell_out != nullptr && a.c_out != nullptr;
+  bool sched_fused = false;
   if (coop && nctas <= resident * sms) {
     sp.k_first = 1;
     sp.k_last = a.gamma;
+    // the schedule in the last CTA when its scan fits 512 threads (8
+    // candidates each) and its keys and values fit the idle rings
+    if (want_sched && (long long)a.B * a.gamma <= 8 * kEpiWarps * 32 &&
+        schedule_smem_bytes(a.B, a.gamma) <= (size_t)kRingBytes) {
+      sp.sched = SchedArgs{a.c_out, a.sps, a.mode, a.khist, a.ell_out, a.nstar_out, a.theta_out, gbar + 2};
+      sched_fused = true;
+    }
     // the target-row statistics ride along in the statistics warps
     sp.T_stats = a.T_stats;
     cudaLaunchConfig_t cfg{};
@@ -1320,10 +1443,16 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
     }
     draft_finalize_tc<<<div_up(a.B * a.gamma * 32, 256), 256, 0, stream>>>(
         a.U, static_cast<const __nv_bfloat16*>(a.W1), static_cast<const __nv_bfloat16*>(a.W2), a.anchor, keys,
-        part, a.B, a.gamma, a.V, per, part_slices, a.x_out, a.p_out, a.lse_out, status);
+        part, a.B, a.gamma, a.V, per, part_slices, a.x_out, a.p_out, a.lse_out, sp.conf, a.T_stats, sp.tx, status);
     // one launch per position: the target-row statistics follow the draft
     if (a.T_stats != nullptr && (e = cudaGetLastError()) == cudaSuccess)
       e = launch_row_stats(a.T_stats, nullptr, a.B, a.gamma, a.V, a.ws, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (want_sched && !sched_fused) {
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_schedule(a.c_out, a.B, a.gamma, a.sps, a.mode, (unsigned long long)(a.key.round3 >> 3),
+                        a.key.round_dev, a.khist, a.ell_out, a.nstar_out, a.theta_out, status, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
@@ -1334,7 +1463,7 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
 // position), p_d = exp(U + bias - lse_d), p_t = exp(T - lse_t), and a Gumbel
 // race over log max(0, p_t - p_d) into resid_key (atomicMax).
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
-                               const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* resid_k,
+                               const int32_t* resid_prev, const float* lse_d, const int32_t* resid_k,
                                const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
                                RngKey key, int* status, cudaStream_t stream) {
   CUtensorMap map;
@@ -1355,9 +1484,8 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
   StepParams sp{};
   sp.U = U;
   sp.W1 = static_cast<const __nv_bfloat16*>(W1);
-  sp.anchor = anchor;
   sp.T = T;
-  sp.x = x;
+  sp.resid_prev = resid_prev;
   sp.resid_k = resid_k;
   sp.lse_d = lse_d;
   sp.resid_lse = resid_lse;
@@ -1370,7 +1498,8 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
   sp.ntiles = ntiles;
   sp.key = key;
   // the U map is not read in this mode; any valid map will do
-  kern<<<mtiles * per, kThreads, kSmemBytes, stream>>>(map, map, sp);
+  e = launch_pdl(kern, dim3(mtiles * per), dim3(kThreads), kSmemBytes, stream, map, map, sp);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -6,9 +6,30 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace dspark {
+
+// Launches kern with the programmatic stream-serialization attribute: it may
+// start while the previous kernel in the stream runs, and it calls pdl_wait()
+// before it touches anything an earlier kernel writes or reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct DraftArgs {
   const float* U;
@@ -25,6 +46,29 @@ struct DraftArgs {
   // optional: target logits [B, gamma+1, V] whose rows j < gamma get their
   // softmax statistics into the workspace during (or right after) the draft
   const float* T_stats;
+  // the tensor-core draft clears the verification's scratch (its argmax keys
+  // and bonus list) at its start, so that the verification that follows in
+  // the same round needs no memset of its own
+  bool zero_verify_scratch;
+  // optional (c_out not null): the confidence head of every position, computed
+  // by the tensor-core draft's finalize (draft_tc_supported); the CUDA-core
+  // draft ignores it and the caller runs launch_confidence instead
+  const void* h;
+  int hdtype;
+  const float* w;
+  const float* sts_T;
+  int H;
+  float* c_out;
+  // optional (ell_out not null, with c_out, tensor-core path): the round's
+  // schedule right after the finalize, run by the persistent draft's last CTA
+  // while the others stream statistics (up to 4096 candidates), else by the
+  // schedule kernel launched after the draft; the CUDA-core draft ignores it
+  const float* sps;
+  int mode;
+  int32_t* khist;
+  int32_t* ell_out;
+  int32_t* nstar_out;
+  double* theta_out;
 };
 
 struct VerifyArgs {
@@ -48,6 +92,8 @@ struct VerifyArgs {
   bool stats_ready;
   // when not null, the round's last kernel adds 1 to this device round index
   unsigned long long* advance_round;
+  // the draft of this round cleared the scratch (DraftArgs::zero_verify_scratch)
+  bool scratch_zeroed;
 };
 
 // Host-side argument checks shared by every entry point that takes these
@@ -96,7 +142,7 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream);
 cudaError_t make_w2_tensor_map(const void* W2, int V, CUtensorMap* map);
 cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtensorMap* map);
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
-                               const int32_t* anchor, const int32_t* x, const float* lse_d, const int32_t* resid_k,
+                               const int32_t* resid_prev, const float* lse_d, const int32_t* resid_k,
                                const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
                                RngKey key, int* status, cudaStream_t stream);
 
@@ -130,8 +176,6 @@ cudaError_t launch_confidence(const void* h, int hdtype, const void* W1, int wdt
                               const float* w, const float* sts_T, const int32_t* anchor,
                               const int32_t* x, int B, int gamma, int H, int r, int V,
                               float* c_out, int* status, cudaStream_t stream);
-
-size_t schedule_smem_bytes(int B, int gamma);
 
 // `round` is the round index unless round_dev (a device word) is given.
 cudaError_t launch_schedule(const float* c, int B, int gamma, const float* sps, int mode,

@@ -253,10 +253,7 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
         ld2 = p.lse_d[(size_t)b * p.G + k - 1] * kL2e;
         const float2* rp = p.row_part + ((size_t)b * (p.G + 1) + k - 1) * p.nsegs;
         float mt = -INFINITY, st = 0.f;
-        for (int sg = 0; sg < p.nsegs; ++sg) {
-          const float2 pr = rp[sg];
-          softmax_merge(mt, st, pr.x, pr.y);
-        }
+        merge_partials(rp, p.nsegs, mt, st);
         lt2 = (mt + logf(st)) * kL2e;
       }
       float lacc = 0.f;

@@ -197,6 +197,10 @@ __global__ void __launch_bounds__(kRowThreads)
 verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
                   const int32_t* __restrict__ bonus_rows, int G, int V, int nsegs, RngKey key_arg,
                   unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
+  // the residual kernel that follows may start its set-up now: its CTAs need
+  // a whole SM each and take the place of this kernel's CTAs as they leave
+  pdl_trigger();
+  pdl_wait();   // the bonus list from verify_decide
   const int nrows = bonus_rows[0];
   if ((int)blockIdx.x >= nrows * nsegs) return;
   const RngKey key = live_key(key_arg);
@@ -312,12 +316,14 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
 }
 
 __global__ void verify_decide(const float* __restrict__ T, const int32_t* __restrict__ x,
-                              const float* __restrict__ p_d, const int32_t* __restrict__ ell, int B,
-                              int G, int V, int nsegs, RngKey key_arg,
-                              const float2* __restrict__ row_part,
+                              const float* __restrict__ p_d, const int32_t* __restrict__ ell,
+                              const int32_t* __restrict__ anchor, int B, int G, int V, int nsegs, RngKey key_arg,
+                              const float2* __restrict__ row_part, const float* __restrict__ tx,
                               int32_t* __restrict__ resid_k, float* __restrict__ resid_lse,
+                              int32_t* __restrict__ resid_prev,
                               int32_t* __restrict__ n_out, int32_t* __restrict__ bonus_rows,
                               const int* __restrict__ stats_done, int* __restrict__ status) {
+  pdl_wait();   // ell from the schedule
   const RngKey key = live_key(key_arg);
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -327,28 +333,38 @@ __global__ void verify_decide(const float* __restrict__ T, const int32_t* __rest
   const int L = min(max(ell[b], 0), G);
   bool reject = false;
   float lse_t = 0.f;
+  int xraw = 0;
   if (lane < L) {
+    // every load that does not depend on another is issued first: the token,
+    // p_d, T at the token when the draft gathered it (tx) and the row's
+    // partials; else T at the token after them
     const int rowid = b * (G + 1) + lane;
+    xraw = x[(size_t)b * G + lane];
+    const float pd = p_d[(size_t)b * G + lane];
+    float t = tx ? __ldcg(tx + (size_t)b * G + lane) : 0.f;
     float m = -INFINITY, s = 0.f;
-    for (int i = 0; i < nsegs; ++i) {
-      const float2 pr = row_part[(size_t)rowid * nsegs + i];
-      softmax_merge(m, s, pr.x, pr.y);
-    }
+    merge_partials(row_part + (size_t)rowid * nsegs, nsegs, m, s);
+    const int xk = checked_token(xraw, V, status);
+    if (!tx) t = T[(size_t)rowid * V + xk];
     lse_t = m + logf(s);
-    const int xk = checked_token(x[(size_t)b * G + lane], V, status);
-    const float q = expf(T[(size_t)rowid * V + xk] - lse_t);
-    const float ratio = q / p_d[(size_t)b * G + lane];
+    const float q = expf(t - lse_t);
+    const float ratio = q / pd;
     const uint4 rw = rng4(key, kStreamAccept, (uint32_t)b, (uint32_t)(lane + 1), 0u);
     reject = !(uniform01(rw.x) < ratio);
   }
   const unsigned ballot = __ballot_sync(0xffffffffu, reject);
   const int n = ballot ? (__ffs(ballot) - 1) : L;
   const float lse_n = __shfl_sync(0xffffffffu, lse_t, n & 31);
+  const int x_prev = __shfl_sync(0xffffffffu, xraw, (n + 31) & 31);   // x_n (lane n - 1)
   if (lane == 0) {
     n_out[b] = n;
     resid_k[b] = n < L ? n + 1 : 0;
-    if (n < L) resid_lse[b] = lse_n;
-    else bonus_rows[1 + atomicAdd(bonus_rows, 1)] = b;   // the bonus race takes it
+    if (n < L) {
+      resid_lse[b] = lse_n;
+      resid_prev[b] = n == 0 ? anchor[b] : x_prev;
+    } else {
+      bonus_rows[1 + atomicAdd(bonus_rows, 1)] = b;   // the bonus race takes it
+    }
   }
 }
 
@@ -419,6 +435,7 @@ verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKe
                          const unsigned long long* __restrict__ bonus_key, int32_t* __restrict__ tok_out,
                          int* __restrict__ status) {
   __shared__ unsigned long long s_k[kRowThreads / 32];
+  pdl_wait();   // the residual and bonus keys
   const int b = blockIdx.x;
   const int ks = resid_k[b];
   if (ks <= 0) {
@@ -477,6 +494,7 @@ verify_residual_finalize(const float* __restrict__ T, int B, int G, int V, RngKe
 // The last kernel of a round whose index lives in device memory: the next
 // round reads index + 1.
 __global__ void advance_round(unsigned long long* round_dev) {
+  pdl_wait();   // every kernel of the round has read the index
   if (threadIdx.x == 0) *round_dev += 1ull;
 }
 
@@ -513,24 +531,33 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   int32_t* resid_k = ws_ptr<int32_t>(a.ws, L.resid_k);
   float* resid_lse = ws_ptr<float>(a.ws, L.resid_lse);
   int32_t* bonus_rows = ws_ptr<int32_t>(a.ws, L.bonus_rows);
+  int32_t* resid_prev = ws_ptr<int32_t>(a.ws, L.resid_prev);
   const int nsegs = a.stats_ready ? stats_num_segs(a.V) : verify_num_segs(a.V);
-  cudaError_t e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.total - L.bonus_key, stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!a.scratch_zeroed && (e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.total - L.bonus_key, stream)) !=
+                               cudaSuccess)
+    return e;
   if (!a.stats_ready && (e = row_stats(a.T, a.ell, a.B, a.gamma, a.V, a.ws, stream)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  verify_decide<<<div_up(a.B * 32, 256), 256, 0, stream>>>(a.T, a.x, a.p_d, a.ell, a.B, a.gamma, a.V, nsegs,
-                                                          a.key, row_part, resid_k, resid_lse, a.n_out,
-                                                          bonus_rows,
-                                                          a.stats_ready ? ws_ptr<int>(a.ws, L.counters) + 2 : nullptr,
-                                                          status);
+  // a tensor-core draft that took T along also gathered T at its tokens (tx)
+  const bool tc = draft_tc_supported(a.wdtype, a.r, a.V);
+  // the kernels from here on are chained by programmatic dependent launch
+  // (each starts while the one before it ends; see pdl_wait)
+  e = launch_pdl(verify_decide, dim3(div_up(a.B * 32, 256)), dim3(256), 0, stream, a.T, a.x, a.p_d, a.ell,
+                 a.anchor, a.B, a.gamma, a.V, nsegs, a.key, (const float2*)row_part,
+                 (const float*)(a.stats_ready && tc ? ws_ptr<float>(a.ws, L.tx) : nullptr), resid_k, resid_lse, resid_prev,
+                 a.n_out, bonus_rows,
+                 (const int*)(a.stats_ready ? ws_ptr<int>(a.ws, L.counters) + 2 : nullptr), status);
+  if (e != cudaSuccess) return e;
   const int bonus_segs = div_up(a.V, kBonusSeg);
   const int grid_bonus = std::min(a.B * bonus_segs, sms * 2);
-  verify_bonus_race<<<grid_bonus, kRowThreads, 0, stream>>>(a.T, a.ell, bonus_rows, a.gamma, a.V, bonus_segs, a.key,
-                                                            bonus_key, status);
+  e = launch_pdl(verify_bonus_race, dim3(grid_bonus), dim3(kRowThreads), 0, stream, a.T, a.ell,
+                 (const int32_t*)bonus_rows, a.gamma, a.V, bonus_segs, a.key, bonus_key, status);
+  if (e != cudaSuccess) return e;
   if (draft_tc_supported(a.wdtype, a.r, a.V)) {
-    e = launch_residual_tc(a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, resid_k, resid_lse, resid_key, a.B,
+    e = launch_residual_tc(a.T, a.U, a.W1, a.W2, resid_prev, a.lse_d, resid_k, resid_lse, resid_key, a.B,
                            a.gamma, a.V, a.key, status, stream);
     if (e != cudaSuccess) return e;
   } else {
@@ -539,9 +566,13 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
         a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, a.B, a.gamma, a.V, a.r, a.key, resid_k, resid_lse,
         resid_key, status);
   }
-  verify_residual_finalize<<<a.B, kRowThreads, 0, stream>>>(a.T, a.B, a.gamma, a.V, a.key, resid_k, resid_key,
-                                                           bonus_key, a.tok_out, status);
-  if (a.advance_round != nullptr) advance_round<<<1, 32, 0, stream>>>(a.advance_round);
+  e = launch_pdl(verify_residual_finalize, dim3(a.B), dim3(kRowThreads), 0, stream, a.T, a.B, a.gamma, a.V, a.key,
+                 (const int32_t*)resid_k, (const unsigned long long*)resid_key, (const unsigned long long*)bonus_key,
+                 a.tok_out, status);
+  if (e != cudaSuccess) return e;
+  if (a.advance_round != nullptr && (e = launch_pdl(advance_round, dim3(1), dim3(32), 0, stream, a.advance_round)) !=
+                                        cudaSuccess)
+    return e;
   return cudaGetLastError();
 }
 

@@ -41,20 +41,26 @@ def test_draft_bytes_match_the_profile():
     # with the target rows j < gamma taken along: those rows once more (1244.7 MB)
     fd = bench.fused_draft_bytes_per_launch(w)
     assert fd - d == 4 * 128 * 16 * 151936
+    # the round's first stage adds the hidden states h (bf16, 10.5 MB), the
+    # head's w, the confidences and the verified lengths
+    sd = bench.stage_bytes_per_launch(w, early=True)
+    assert sd - fd == 2 * 128 * 16 * 2560 + 4 * (2560 + 256) + 4 * 128 * 16 + 4 * 128
+    assert bench.stage_bytes_per_launch(w, early=False) == sd - 4 * 128 * 16 * 151936
     with open(bench.DRAFT_PROFILE) as f:
         rec = json.load(f)
     assert rec["workload"] == "batch128"
-    alg = fd if rec["early_target_stats"] else d
+    alg = bench.stage_bytes_per_launch(w, rec["early_target_stats"])
     assert int(rec["algorithmic_bytes_per_launch"]) == alg
     # the profile's DRAM traffic is within a few per cent of the algorithmic bytes
     assert 1.0 <= int(rec["dram_bytes_per_launch"]) / alg < 1.05
 
 
 def test_kernels_per_round():
-    # tensor-core path: one persistent draft launch; CUDA-core path: a step and
-    # a finalize per position; then confidence, schedule and six verify
+    # tensor-core path: one persistent launch drafts, computes the confidences
+    # and runs the schedule; CUDA-core path: a step and a finalize per
+    # position, then the confidence and schedule kernels; then six verify
     # kernels (four when the draft took the target-row statistics along)
-    assert bench.kernels_per_round(wl.WORKLOADS["batch128"]) == 9
-    assert bench.kernels_per_round(wl.WORKLOADS["batch128"], early=True) == 7
+    assert bench.kernels_per_round(wl.WORKLOADS["batch128"]) == 7
+    assert bench.kernels_per_round(wl.WORKLOADS["batch128"], early=True) == 5
     t = wl.WORKLOADS["tiny"]
     assert bench.kernels_per_round(t) == 2 * t.gamma + 8
