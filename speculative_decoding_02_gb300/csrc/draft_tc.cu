@@ -567,6 +567,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* counter, uint32_t tar
 // eviction from L2: W2, which every draft position re-reads from L2, must not
 // be pushed out by a stream that is read once.
 constexpr int kStatsLoadsWarp = 16;   // float4 per lane per piece of a warp that loads for itself
+constexpr int kStatsPiece = 32 * 4 * kStatsLoadsWarp;   // entries per piece (8 KB)
 
 // The (max, sum of exp) of one piece of a row, folded into a lane's running
 // state (x: this lane's entries, -inf past the row's end).
@@ -622,7 +623,7 @@ __device__ void stats_tasks(const float* __restrict__ T, int B, int G, int V, in
     const int v0 = seg * kStatsSeg, v1 = min(V, v0 + kStatsSeg);
     float m = -INFINITY, s = 0.f;
 #pragma unroll 1
-    for (int vp = v0; vp < v1; vp += 32 * 4 * kStatsLoadsWarp) {
+    for (int vp = v0; vp < v1; vp += kStatsPiece) {
       float4 x[kStatsLoadsWarp];
 #pragma unroll
       for (int i = 0; i < kStatsLoadsWarp; ++i) {
@@ -742,10 +743,9 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       if (blockIdx.x == 0 && threadIdx.x == 0) *p.vz_count = 0;
     }
   }
-  // draft mode: the next kernel in the stream may start launching (it waits
-  // for this one, on SMs this grid has left); residual mode: no early trigger,
-  // the next kernel's waiting CTAs would share the SMs of this one
-  if constexpr (MODE == kDraft) pdl_trigger();
+  // (no early trigger in either mode: the next kernel's CTAs, resident and
+  // waiting on the SMs this grid leaves, were measured to slow the kernels
+  // that follow)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) { mbar_init(&bars->full_w[s], 1); mbar_init(&bars->empty_w[s], 1); }

@@ -27,6 +27,7 @@
 // Steps 1-2 are skipped when the draft already took the statistics of every
 // row j < gamma (the caller held T when the draft started).
 #include <algorithm>
+#include <mutex>
 
 #include "kernels.h"
 
@@ -192,20 +193,20 @@ __device__ __forceinline__ void load_chunk16(const float* __restrict__ row, int 
 }
 
 constexpr int kBonusSeg = 8192;   // vocabulary entries per bonus-race task
+// Two warps per CTA: the race runs beside the residual resample (another
+// stream), whose CTAs leave about 10 K registers per SM free.
+constexpr int kBonusThreads = 64;
 
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kBonusThreads)
 verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
                   const int32_t* __restrict__ bonus_rows, int G, int V, int nsegs, RngKey key_arg,
                   unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
-  // the residual kernel that follows may start its set-up now: its CTAs need
-  // a whole SM each and take the place of this kernel's CTAs as they leave
-  pdl_trigger();
-  pdl_wait();   // the bonus list from verify_decide
+  pdl_wait();   // the bonus list from verify_decide (a no-op on the side stream)
   const int nrows = bonus_rows[0];
   if ((int)blockIdx.x >= nrows * nsegs) return;
   const RngKey key = live_key(key_arg);
-  __shared__ unsigned long long s_k[kRowThreads / 32];
-  constexpr int kChunks = kBonusSeg / (16 * kRowThreads);
+  __shared__ unsigned long long s_k[kBonusThreads / 32];
+  constexpr int kChunks = kBonusSeg / (16 * kBonusThreads);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int ntasks = nrows * nsegs;
   bool bad = false;
@@ -225,13 +226,13 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
     float4 nx[4];
     load_chunk16(Trow, v0 + 16 * tid, v1, nx);
     for (int ch = 0; ch < kChunks; ++ch) {
-      const int vc = v0 + 16 * (ch * kRowThreads + tid);
+      const int vc = v0 + 16 * (ch * kBonusThreads + tid);
       float tv[16];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         tv[4 * i] = nx[i].x; tv[4 * i + 1] = nx[i].y; tv[4 * i + 2] = nx[i].z; tv[4 * i + 3] = nx[i].w;
       }
-      if (ch + 1 < kChunks) load_chunk16(Trow, vc + 16 * kRowThreads, v1, nx);
+      if (ch + 1 < kChunks) load_chunk16(Trow, vc + 16 * kBonusThreads, v1, nx);
       if (vc < v1) {
         float cm = tv[0];
 #pragma unroll
@@ -307,7 +308,7 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
     if (lane == 0) s_k[wid] = best;
     __syncthreads();
     if (tid == 0) {
-      for (int w = 1; w < kRowThreads / 32; ++w) best = s_k[w] > best ? s_k[w] : best;
+      for (int w = 1; w < kBonusThreads / 32; ++w) best = s_k[w] > best ? s_k[w] : best;
       if (best) atomicMax(&bonus_key[b], best);
     }
     __syncthreads();
@@ -521,6 +522,36 @@ cudaError_t row_stats(const float* T, const int32_t* ell, int B, int gamma, int 
   return cudaGetLastError();
 }
 
+// A second stream per device on which the bonus race runs beside the
+// residual resample (the two read different rows and write different keys;
+// the residual finalize needs both).  Created on first use; one mutex per
+// device keeps each fork and join of its two events in one piece when host
+// threads share the device.
+struct SideStream {
+  std::mutex mu;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxSideDevices = 64;
+SideStream g_side[kMaxSideDevices];
+std::mutex g_side_init;
+
+cudaError_t side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxSideDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_side_init);
+  SideStream& ss = g_side[dev];
+  if (ss.s == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+
 template <int WDT>
 cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   const WsLayout L = ws_layout(a.B, a.gamma, a.V);
@@ -551,20 +582,31 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
                  a.n_out, bonus_rows,
                  (const int*)(a.stats_ready ? ws_ptr<int>(a.ws, L.counters) + 2 : nullptr), status);
   if (e != cudaSuccess) return e;
-  const int bonus_segs = div_up(a.V, kBonusSeg);
-  const int grid_bonus = std::min(a.B * bonus_segs, sms * 2);
-  e = launch_pdl(verify_bonus_race, dim3(grid_bonus), dim3(kRowThreads), 0, stream, a.T, a.ell,
-                 (const int32_t*)bonus_rows, a.gamma, a.V, bonus_segs, a.key, bonus_key, status);
-  if (e != cudaSuccess) return e;
-  if (draft_tc_supported(a.wdtype, a.r, a.V)) {
-    e = launch_residual_tc(a.T, a.U, a.W1, a.W2, resid_prev, a.lse_d, resid_k, resid_lse, resid_key, a.B,
-                           a.gamma, a.V, a.key, status, stream);
-    if (e != cudaSuccess) return e;
-  } else {
-    const dim3 grid_res(draft_num_slices(a.V), a.B);
-    verify_residual_cuda_core<WDT><<<grid_res, kRowThreads, sizeof(float) * a.r, stream>>>(
-        a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, a.B, a.gamma, a.V, a.r, a.key, resid_k, resid_lse,
-        resid_key, status);
+  // the bonus race on the side stream (forked after verify_decide), the
+  // residual on this one, joined before the finalize
+  SideStream* ss = nullptr;
+  if ((e = side_stream(&ss)) != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(ss->mu);
+    if ((e = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
+    const int bonus_segs = div_up(a.V, kBonusSeg);
+    const int grid_bonus = std::min(a.B * bonus_segs, sms * 4);
+    verify_bonus_race<<<grid_bonus, kBonusThreads, 0, ss->s>>>(a.T, a.ell, bonus_rows, a.gamma, a.V, bonus_segs, a.key,
+                                                              bonus_key, status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
+    if (tc) {
+      e = launch_residual_tc(a.T, a.U, a.W1, a.W2, resid_prev, a.lse_d, resid_k, resid_lse, resid_key, a.B,
+                             a.gamma, a.V, a.key, status, stream);
+      if (e != cudaSuccess) return e;
+    } else {
+      const dim3 grid_res(draft_num_slices(a.V), a.B);
+      verify_residual_cuda_core<WDT><<<grid_res, kRowThreads, sizeof(float) * a.r, stream>>>(
+          a.T, a.U, a.W1, a.W2, a.anchor, a.x, a.lse_d, a.B, a.gamma, a.V, a.r, a.key, resid_k, resid_lse,
+          resid_key, status);
+    }
+    if ((e = cudaStreamWaitEvent(stream, ss->join, 0)) != cudaSuccess) return e;
   }
   e = launch_pdl(verify_residual_finalize, dim3(a.B), dim3(kRowThreads), 0, stream, a.T, a.B, a.gamma, a.V, a.key,
                  (const int32_t*)resid_k, (const unsigned long long*)resid_key, (const unsigned long long*)bonus_key,
