@@ -296,6 +296,62 @@ void oracle_draft_probs(int V, int r, const float* U_row, const void* W1,
 }
 
 /* ------------------------------------------------------------------------- */
+/* The gated recurrent Markov head.  [blog] section 4 and [digest] item 8 name
+ * a gated Markov head and an RNN head that keeps a state through the draft
+ * block; neither page gives their equations.  This is the plainest head with
+ * that description, and it keeps the Markov head's projection:
+ *
+ *   e_k = W1[x_{k-1}],   a_k = sigmoid(g .* e_k + c)   (g, c in R^r),
+ *   s_0 = 0,             s_k = e_k + a_k .* s_{k-1},
+ *   B_k(v) = sum_i s_k[i] * W2[v, i],
+ *
+ * so p_k(v) ~ exp(U_k(v) + B_k(v)) depends on the whole prefix x_0..x_{k-1}
+ * ([report] Eq.4's B_k(x_0, x_<k, v)).  With a_k = 0 it is the Markov head.  */
+/* ------------------------------------------------------------------------- */
+
+/* s <- e + a .* s for the previous token prev (one step of the recurrence). */
+static void gated_step(int r, const void* W1, int wdt, const float* g,
+                       const float* c, int prev, double* s) {
+  for (int i = 0; i < r; ++i) {
+    const double e = load_elem(W1, wdt, (size_t)prev * r + i);
+    const double a = 1.0 / (1.0 + exp(-((double)g[i] * e + (double)c[i])));
+    s[i] = e + a * s[i];
+  }
+}
+
+/* l(v) = U_row(v) + sum_i s[i] * W2[v, i]. */
+static void state_logits(int V, int r, const float* U_row, const double* s,
+                         const void* W2, int wdt, double* l_out) {
+  for (int v = 0; v < V; ++v) {
+    double acc = 0.0;
+    for (int i = 0; i < r; ++i) acc += s[i] * load_elem(W2, wdt, (size_t)v * r + i);
+    l_out[v] = (double)U_row[v] + acc;
+  }
+}
+
+/* The states s_1..s_G of one request ([G][r]) for the prefix anchor, x[0..G-2]. */
+int oracle_gated_states(int G, int V, int r, const void* W1, int wdt,
+                        const float* g, const float* c, int anchor,
+                        const int32_t* x, double* s_out) {
+  if (G <= 0 || V <= 0 || r <= 0 || !W1 || !g || !c || !s_out || (G > 1 && !x))
+    return ORACLE_ERR_INVALID;
+  double* s = (double*)calloc((size_t)r, sizeof(double));
+  if (!s) return ORACLE_ERR_NOMEM;
+  int status = ORACLE_OK;
+  for (int k = 1; k <= G; ++k) {
+    const int prev = (k == 1) ? anchor : x[k - 2];
+    if (prev < 0 || prev >= V) {
+      status = ORACLE_ERR_INVALID;
+      break;
+    }
+    gated_step(r, W1, wdt, g, c, prev, s);
+    memcpy(s_out + (size_t)(k - 1) * r, s, sizeof(double) * (size_t)r);
+  }
+  free(s);
+  return status;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Step 1: semi-autoregressive Markov draft ([report] Eq.4; [blog] sections 3-4)
  *
  *   P(X | x0) = prod_k p_k(x_k | x0, x_<k),  p_k(v) ~ exp(U_k(v) + B_k(v)),
@@ -308,20 +364,27 @@ void oracle_draft_probs(int V, int r, const float* U_row, const void* W1,
  * When x_force is given, the previous token of step k >= 2 is taken from it
  * (teacher forcing: each step is checked on the other side's upstream token);
  * otherwise from this oracle's own sample. */
-int oracle_draft(int B, int G, int V, int r, const float* U, const void* W1,
-                 const void* W2, int wdt, const int32_t* anchor,
-                 const int32_t* x_force, uint64_t seed, uint64_t round, int b0,
-                 int b1, int32_t* x_out, double* p_out, double* lse_out,
-                 double* margin_out) {
+/* (gate_g, gate_c non-NULL: the gated recurrent head, its state carried
+ * along the prefix; NULL: the Markov head) */
+static int draft_impl(int B, int G, int V, int r, const float* U, const void* W1,
+                      const void* W2, int wdt, const float* gate_g,
+                      const float* gate_c, const int32_t* anchor,
+                      const int32_t* x_force, uint64_t seed, uint64_t round,
+                      int b0, int b1, int32_t* x_out, double* p_out,
+                      double* lse_out, double* margin_out) {
   if (B <= 0 || G <= 0 || V <= 0 || r <= 0 || !U || !W1 || !W2 || !anchor ||
-      !x_out || b0 < 0 || b1 > B || b0 > b1 || (wdt != 0 && wdt != 1))
+      !x_out || b0 < 0 || b1 > B || b0 > b1 || (wdt != 0 && wdt != 1) ||
+      (!gate_g) != (!gate_c))
     return ORACLE_ERR_INVALID;
   int status = ORACLE_OK;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int b = b0; b < b1; ++b) {
     double* l = (double*)malloc(sizeof(double) * (size_t)V);
-    if (!l) {
+    double* s = (double*)calloc((size_t)r, sizeof(double));
+    if (!l || !s) {
       set_status(&status, ORACLE_ERR_NOMEM);
+      free(l);
+      free(s);
       continue;
     }
     int prev = anchor[b];
@@ -333,7 +396,12 @@ int oracle_draft(int B, int G, int V, int r, const float* U, const void* W1,
         break;
       }
       const float* U_row = U + ((size_t)b * G + (k - 1)) * (size_t)V;
-      oracle_draft_logits(V, r, U_row, W1, W2, wdt, prev, l);
+      if (gate_g) {
+        gated_step(r, W1, wdt, gate_g, gate_c, prev, s);
+        state_logits(V, r, U_row, s, W2, wdt, l);
+      } else {
+        oracle_draft_logits(V, r, U_row, W1, W2, wdt, prev, l);
+      }
       double lse = oracle_logsumexp(V, l);
       double margin = 0.0;
       int xk = oracle_block_sample(V, l, seed, round, (uint32_t)b, (uint32_t)k,
@@ -345,8 +413,30 @@ int oracle_draft(int B, int G, int V, int r, const float* U, const void* W1,
       if (margin_out) margin_out[o] = margin;
     }
     free(l);
+    free(s);
   }
   return status;
+}
+
+int oracle_draft(int B, int G, int V, int r, const float* U, const void* W1,
+                 const void* W2, int wdt, const int32_t* anchor,
+                 const int32_t* x_force, uint64_t seed, uint64_t round, int b0,
+                 int b1, int32_t* x_out, double* p_out, double* lse_out,
+                 double* margin_out) {
+  return draft_impl(B, G, V, r, U, W1, W2, wdt, NULL, NULL, anchor, x_force, seed,
+                    round, b0, b1, x_out, p_out, lse_out, margin_out);
+}
+
+/* The draft with the gated recurrent head (gate_g, gate_c [r]). */
+int oracle_gated_draft(int B, int G, int V, int r, const float* U, const void* W1,
+                       const void* W2, int wdt, const float* gate_g,
+                       const float* gate_c, const int32_t* anchor,
+                       const int32_t* x_force, uint64_t seed, uint64_t round,
+                       int b0, int b1, int32_t* x_out, double* p_out,
+                       double* lse_out, double* margin_out) {
+  if (!gate_g || !gate_c) return ORACLE_ERR_INVALID;
+  return draft_impl(B, G, V, r, U, W1, W2, wdt, gate_g, gate_c, anchor, x_force,
+                    seed, round, b0, b1, x_out, p_out, lse_out, margin_out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -499,14 +589,16 @@ int oracle_schedule(int R, int G, const double* c, const float* sps, int n_sps,
  * flags (1 = bonus, 2 = residual, 4 = residual fell back to p_t); per verified
  * position the ratio p_t/p_d and |u - ratio| (NaN where not evaluated); per
  * request the margin of the draw of y. */
-int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
-                  const void* W1, const void* W2, int wdt,
-                  const int32_t* anchor, const int32_t* x, const int32_t* ell,
-                  uint64_t seed, uint64_t round, int b0, int b1,
-                  int32_t* n_out, int32_t* y_out, int32_t* flags_out,
-                  double* ratio_out, double* umargin_out, double* ymargin_out) {
+static int verify_impl(int B, int G, int V, int r, const float* T, const float* U,
+                       const void* W1, const void* W2, int wdt, const float* gate_g,
+                       const float* gate_c, const int32_t* anchor, const int32_t* x,
+                       const int32_t* ell, uint64_t seed, uint64_t round, int b0,
+                       int b1, int32_t* n_out, int32_t* y_out, int32_t* flags_out,
+                       double* ratio_out, double* umargin_out,
+                       double* ymargin_out) {
   if (B <= 0 || G <= 0 || V <= 0 || r <= 0 || !T || !U || !W1 || !W2 ||
-      !anchor || !x || !ell || !n_out || !y_out || b0 < 0 || b1 > B || b0 > b1)
+      !anchor || !x || !ell || !n_out || !y_out || b0 < 0 || b1 > B || b0 > b1 ||
+      (!gate_g) != (!gate_c))
     return ORACLE_ERR_INVALID;
   int status = ORACLE_OK;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -514,15 +606,16 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
     double* p_d = (double*)malloc(sizeof(double) * (size_t)V);
     double* p_t = (double*)malloc(sizeof(double) * (size_t)V);
     double* score = (double*)malloc(sizeof(double) * (size_t)V);
-    if (!p_d || !p_t || !score) {
+    double* s = (double*)calloc((size_t)r, sizeof(double));
+    if (!p_d || !p_t || !score || !s) {
       set_status(&status, ORACLE_ERR_NOMEM);
-      free(p_d); free(p_t); free(score);
+      free(p_d); free(p_t); free(score); free(s);
       continue;
     }
     int L = ell[b];
     if (L < 0 || L > G) {
       set_status(&status, ORACLE_ERR_INVALID);
-      free(p_d); free(p_t); free(score);
+      free(p_d); free(p_t); free(score); free(s);
       continue;
     }
     for (int k = 1; k <= G; ++k) {
@@ -541,7 +634,14 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
       }
       const float* U_row = U + ((size_t)b * G + (k - 1)) * (size_t)V;
       const float* T_row = T + ((size_t)b * (G + 1) + (k - 1)) * (size_t)V;
-      oracle_draft_probs(V, r, U_row, W1, W2, wdt, prev, p_d);
+      if (gate_g) {
+        gated_step(r, W1, wdt, gate_g, gate_c, prev, s);
+        state_logits(V, r, U_row, s, W2, wdt, p_d);
+        const double lse = oracle_logsumexp(V, p_d);
+        for (int v = 0; v < V; ++v) p_d[v] = exp(p_d[v] - lse);
+      } else {
+        oracle_draft_probs(V, r, U_row, W1, W2, wdt, prev, p_d);
+      }
       for (int v = 0; v < V; ++v) score[v] = (double)T_row[v];
       oracle_softmax(V, score, p_t);
       double ratio = p_t[xk] / p_d[xk];
@@ -567,7 +667,7 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
     if (n < 0) {
       n_out[b] = -1;
       y_out[b] = -1;
-      free(p_d); free(p_t); free(score);
+      free(p_d); free(p_t); free(score); free(s);
       continue;
     }
     if (n == L) {
@@ -581,9 +681,36 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
     y_out[b] = y;
     if (flags_out) flags_out[b] = flags;
     if (ymargin_out) ymargin_out[b] = ymargin;
-    free(p_d); free(p_t); free(score);
+    free(p_d); free(p_t); free(score); free(s);
   }
   return status;
+}
+
+int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
+                  const void* W1, const void* W2, int wdt,
+                  const int32_t* anchor, const int32_t* x, const int32_t* ell,
+                  uint64_t seed, uint64_t round, int b0, int b1,
+                  int32_t* n_out, int32_t* y_out, int32_t* flags_out,
+                  double* ratio_out, double* umargin_out, double* ymargin_out) {
+  return verify_impl(B, G, V, r, T, U, W1, W2, wdt, NULL, NULL, anchor, x, ell, seed,
+                     round, b0, b1, n_out, y_out, flags_out, ratio_out,
+                     umargin_out, ymargin_out);
+}
+
+/* Verification of a draft made with the gated recurrent head: p_d of
+ * position k from the state s_k of the prefix anchor, x_1..x_{k-1}. */
+int oracle_gated_verify(int B, int G, int V, int r, const float* T,
+                        const float* U, const void* W1, const void* W2, int wdt,
+                        const float* gate_g, const float* gate_c,
+                        const int32_t* anchor, const int32_t* x,
+                        const int32_t* ell, uint64_t seed, uint64_t round, int b0,
+                        int b1, int32_t* n_out, int32_t* y_out,
+                        int32_t* flags_out, double* ratio_out,
+                        double* umargin_out, double* ymargin_out) {
+  if (!gate_g || !gate_c) return ORACLE_ERR_INVALID;
+  return verify_impl(B, G, V, r, T, U, W1, W2, wdt, gate_g, gate_c, anchor, x, ell,
+                     seed, round, b0, b1, n_out, y_out, flags_out, ratio_out,
+                     umargin_out, ymargin_out);
 }
 
 /* Number of threads the parallel request loops use (1 without OpenMP). */
