@@ -76,6 +76,7 @@ extern "C" {
 #define DSPARK_ADVANCE_ROUND 2u       /* the call's last kernel adds 1 to *round_dev */
 #define DSPARK_TARGET_STATS_FROM_VERIFY 4u  /* dspark_acceptance_label_ex: a verification left them */
 #define DSPARK_SCRATCH_FROM_DRAFT 8u  /* dspark_verify_ex: dspark_draft_schedule cleared the scratch */
+#define DSPARK_GATED_STATES 16u       /* dspark_verify_ex: the draft used the gated recurrent head */
 
 /* Bytes of device scratch the entry points below need for these sizes; 0 when
  * a size is not positive. */
@@ -200,6 +201,10 @@ int dspark_verify(const float* T, const float* U, const void* W1, const void* W2
  *  - round_dev: the round index as a device word (see dspark_markov_draft_ex).
  *  - DSPARK_ADVANCE_ROUND (needs round_dev): the call's last kernel adds 1 to
  *    *round_dev after every kernel of the call has read it.
+ *  - DSPARK_GATED_STATES: x, p_d and lse_d come from dspark_gated_markov_draft
+ *    on the same workspace, earlier in stream order; the residual's bias
+ *    operand is the state it left there (tensor-core path only, else
+ *    DSPARK_ERR_UNSUPPORTED).
  *  - DSPARK_SCRATCH_FROM_DRAFT: a dspark_draft_schedule on the same workspace,
  *    earlier in stream order, cleared this call's scratch (its argmax keys and
  *    bonus list; the tensor-core path does, others ignore the flag), so the
@@ -273,6 +278,28 @@ size_t dspark_sts_workspace_size(int N, int gamma, int ngrid);
 int dspark_sts_fit(const float* z, const int32_t* ell, const int32_t* acc, int N, int gamma,
                    const float* grid, int ngrid, float* T_out, float* ece_out,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The Markov draft with a gated recurrent head.  [blog] section 4 and
+ * [digest] item 8 name a gated Markov head and an RNN head whose state runs
+ * through the draft block, without equations; this library's plain form
+ * keeps the Markov head's rank-r space and projection:
+ *   e_k = W1[x_{k-1}],  a_k = sigmoid(gate_g * e_k + gate_c)  (elementwise),
+ *   s_0 = 0,  s_k = e_k + a_k * s_{k-1}  (kept in bf16, as the tensor cores read it),
+ *   l_k(v) = U[b, k-1, v] + sum_i s_k[i] * W2[v, i],
+ * so the draft distribution depends on the whole prefix x_0 .. x_{k-1}; with
+ * a_k = 0 it is dspark_markov_draft.  Sampling, outputs, T_early and round_dev
+ * as for dspark_markov_draft_ex.  gate_g, gate_c: float32 [r], 16-byte
+ * aligned.  The states are left in the workspace for dspark_verify_ex
+ * (DSPARK_GATED_STATES).  Tensor-core path only (bf16, r = 256, V >= 192);
+ * otherwise DSPARK_ERR_UNSUPPORTED.
+ */
+int dspark_gated_markov_draft(const float* U, const float* T_early, const void* W1, const void* W2,
+                              int wdtype, const float* gate_g, const float* gate_c,
+                              const int32_t* anchor, int B, int gamma, int V, int r,
+                              uint64_t seed, uint64_t round, const uint64_t* round_dev,
+                              int32_t* x_out, float* p_out, float* lse_out,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The first stage of a round: the Markov draft, the confidence head of every

@@ -71,13 +71,13 @@ def lib():
         L.oracle_verify.argtypes = [c_int, c_int, c_int, c_int, vp, vp, vp, vp, c_int, vp, vp, vp,
                                     c_u64, c_u64, c_int, c_int, vp, vp, vp, vp, vp, vp]
         L.oracle_verify.restype = c_int
-        L.oracle_gated_states.argtypes = [c_int, c_int, c_int, vp, c_int, vp, vp, c_int, vp, vp]
+        L.oracle_gated_states.argtypes = [c_int, c_int, c_int, vp, c_int, vp, vp, c_int, vp, c_int, vp]
         L.oracle_gated_states.restype = c_int
-        L.oracle_gated_draft.argtypes = [c_int, c_int, c_int, c_int, vp, vp, vp, c_int, vp, vp, vp, vp,
+        L.oracle_gated_draft.argtypes = [c_int, c_int, c_int, c_int, vp, vp, vp, c_int, vp, vp, c_int, vp, vp,
                                          c_u64, c_u64, c_int, c_int, vp, vp, vp, vp]
         L.oracle_gated_draft.restype = c_int
-        L.oracle_gated_verify.argtypes = [c_int, c_int, c_int, c_int, vp, vp, vp, vp, c_int, vp, vp, vp, vp, vp,
-                                          c_u64, c_u64, c_int, c_int, vp, vp, vp, vp, vp, vp]
+        L.oracle_gated_verify.argtypes = [c_int, c_int, c_int, c_int, vp, vp, vp, vp, c_int, vp, vp, c_int, vp, vp,
+                                          vp, c_u64, c_u64, c_int, c_int, vp, vp, vp, vp, vp, vp]
         L.oracle_gated_verify.restype = c_int
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = c_int
@@ -297,20 +297,24 @@ def verify(T, U, W1, W2, anchor, x, ell, seed, rnd, b0=0, b1=None):
 # s_k = e_k + a_k * s_{k-1}, bias s_k . W2[v]; g, c float32 [r])
 # --------------------------------------------------------------------------
 
-def gated_states(W1, g, c, anchor, x_prefix, G):
-    """The states s_1..s_G [G, r] (f64) of one request: anchor, then x_prefix[0..G-2]."""
+def gated_states(W1, g, c, anchor, x_prefix, G, bf16_state=False):
+    """The states s_1..s_G [G, r] (f64) of one request: anchor, then x_prefix[0..G-2].
+    bf16_state: each state rounded to bf16 as it is formed (the precision a
+    tensor-core operand holds it in); False: the exact definition."""
     W1 = _c(W1)
     V, r = W1.shape
     g, c = _c(g, np.float32), _c(c, np.float32)
     xp = _c(np.asarray(x_prefix, np.int32).reshape(-1)[:max(G - 1, 0)], np.int32) if G > 1 else None
     out = np.empty((G, r), np.float64)
-    st = lib().oracle_gated_states(G, V, r, _ptr(W1), _wdt(W1), _ptr(g), _ptr(c), int(anchor), _ptr(xp), _ptr(out))
+    st = lib().oracle_gated_states(G, V, r, _ptr(W1), _wdt(W1), _ptr(g), _ptr(c), int(anchor), _ptr(xp),
+                                   int(bool(bf16_state)), _ptr(out))
     _check(st, "gated_states")
     return out
 
 
-def gated_draft(U, W1, W2, g, c, anchor, seed, rnd, x_force=None, b0=0, b1=None):
-    """The draft with the gated recurrent head; as draft()."""
+def gated_draft(U, W1, W2, g, c, anchor, seed, rnd, x_force=None, b0=0, b1=None, bf16_state=False):
+    """The draft with the gated recurrent head; as draft() (bf16_state as for
+    gated_states)."""
     U = _c(U, np.float32)
     B, G, V = U.shape
     W1, W2 = _c(W1), _c(W2)
@@ -324,13 +328,14 @@ def gated_draft(U, W1, W2, g, c, anchor, seed, rnd, x_force=None, b0=0, b1=None)
     lse = np.full((B, G), np.nan)
     mg = np.full((B, G), np.nan)
     st = lib().oracle_gated_draft(B, G, V, r, _ptr(U), _ptr(W1), _ptr(W2), _wdt(W1), _ptr(g), _ptr(c),
-                                  _ptr(anchor), _ptr(xf), seed, rnd, b0, b1, _ptr(x), _ptr(p), _ptr(lse), _ptr(mg))
+                                  int(bool(bf16_state)), _ptr(anchor), _ptr(xf), seed, rnd, b0, b1, _ptr(x), _ptr(p), _ptr(lse), _ptr(mg))
     _check(st, "gated_draft")
     return dict(x=x, p=p, lse=lse, margin=mg)
 
 
-def gated_verify(T, U, W1, W2, g, c, anchor, x, ell, seed, rnd, b0=0, b1=None):
-    """Verification of a gated-head draft; as verify()."""
+def gated_verify(T, U, W1, W2, g, c, anchor, x, ell, seed, rnd, b0=0, b1=None, bf16_state=False):
+    """Verification of a gated-head draft; as verify() (bf16_state as for
+    gated_states)."""
     T, U = _c(T, np.float32), _c(U, np.float32)
     B, G, V = U.shape
     assert T.shape == (B, G + 1, V)
@@ -346,7 +351,7 @@ def gated_verify(T, U, W1, W2, g, c, anchor, x, ell, seed, rnd, b0=0, b1=None):
     um = np.full((B, G), np.nan)
     ym = np.full(B, np.nan)
     st = lib().oracle_gated_verify(B, G, V, r, _ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _wdt(W1), _ptr(g), _ptr(c),
-                                   _ptr(anchor), _ptr(x), _ptr(ell), seed, rnd, b0, b1, _ptr(n), _ptr(y), _ptr(fl),
+                                   int(bool(bf16_state)), _ptr(anchor), _ptr(x), _ptr(ell), seed, rnd, b0, b1, _ptr(n), _ptr(y), _ptr(fl),
                                    _ptr(ratio), _ptr(um), _ptr(ym))
     _check(st, "gated_verify")
     return dict(n=n, y=y, flags=fl, ratio=ratio, umargin=um, ymargin=ym)

@@ -309,13 +309,26 @@ void oracle_draft_probs(int V, int r, const float* U_row, const void* W1,
  * ([report] Eq.4's B_k(x_0, x_<k, v)).  With a_k = 0 it is the Markov head.  */
 /* ------------------------------------------------------------------------- */
 
-/* s <- e + a .* s for the previous token prev (one step of the recurrence). */
+/* x rounded to the nearest bf16 value (ties to even), by its float's bits. */
+static double round_bf16(double x) {
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) != 0x7f800000u) u = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* s <- e + a .* s for the previous token prev (one step of the recurrence).
+ * bf16_state: the new state is rounded to bf16 (the precision a tensor-core
+ * operand holds it in); 0 keeps the exact definition. */
 static void gated_step(int r, const void* W1, int wdt, const float* g,
-                       const float* c, int prev, double* s) {
+                       const float* c, int prev, int bf16_state, double* s) {
   for (int i = 0; i < r; ++i) {
     const double e = load_elem(W1, wdt, (size_t)prev * r + i);
     const double a = 1.0 / (1.0 + exp(-((double)g[i] * e + (double)c[i])));
     s[i] = e + a * s[i];
+    if (bf16_state) s[i] = round_bf16(s[i]);
   }
 }
 
@@ -329,10 +342,11 @@ static void state_logits(int V, int r, const float* U_row, const double* s,
   }
 }
 
-/* The states s_1..s_G of one request ([G][r]) for the prefix anchor, x[0..G-2]. */
+/* The states s_1..s_G of one request ([G][r]) for the prefix anchor, x[0..G-2]
+ * (bf16_state: each rounded to bf16 as it is formed). */
 int oracle_gated_states(int G, int V, int r, const void* W1, int wdt,
                         const float* g, const float* c, int anchor,
-                        const int32_t* x, double* s_out) {
+                        const int32_t* x, int bf16_state, double* s_out) {
   if (G <= 0 || V <= 0 || r <= 0 || !W1 || !g || !c || !s_out || (G > 1 && !x))
     return ORACLE_ERR_INVALID;
   double* s = (double*)calloc((size_t)r, sizeof(double));
@@ -344,7 +358,7 @@ int oracle_gated_states(int G, int V, int r, const void* W1, int wdt,
       status = ORACLE_ERR_INVALID;
       break;
     }
-    gated_step(r, W1, wdt, g, c, prev, s);
+    gated_step(r, W1, wdt, g, c, prev, bf16_state, s);
     memcpy(s_out + (size_t)(k - 1) * r, s, sizeof(double) * (size_t)r);
   }
   free(s);
@@ -368,7 +382,7 @@ int oracle_gated_states(int G, int V, int r, const void* W1, int wdt,
  * along the prefix; NULL: the Markov head) */
 static int draft_impl(int B, int G, int V, int r, const float* U, const void* W1,
                       const void* W2, int wdt, const float* gate_g,
-                      const float* gate_c, const int32_t* anchor,
+                      const float* gate_c, int bf16_state, const int32_t* anchor,
                       const int32_t* x_force, uint64_t seed, uint64_t round,
                       int b0, int b1, int32_t* x_out, double* p_out,
                       double* lse_out, double* margin_out) {
@@ -397,7 +411,7 @@ static int draft_impl(int B, int G, int V, int r, const float* U, const void* W1
       }
       const float* U_row = U + ((size_t)b * G + (k - 1)) * (size_t)V;
       if (gate_g) {
-        gated_step(r, W1, wdt, gate_g, gate_c, prev, s);
+        gated_step(r, W1, wdt, gate_g, gate_c, prev, bf16_state, s);
         state_logits(V, r, U_row, s, W2, wdt, l);
       } else {
         oracle_draft_logits(V, r, U_row, W1, W2, wdt, prev, l);
@@ -423,20 +437,21 @@ int oracle_draft(int B, int G, int V, int r, const float* U, const void* W1,
                  const int32_t* x_force, uint64_t seed, uint64_t round, int b0,
                  int b1, int32_t* x_out, double* p_out, double* lse_out,
                  double* margin_out) {
-  return draft_impl(B, G, V, r, U, W1, W2, wdt, NULL, NULL, anchor, x_force, seed,
+  return draft_impl(B, G, V, r, U, W1, W2, wdt, NULL, NULL, 0, anchor, x_force, seed,
                     round, b0, b1, x_out, p_out, lse_out, margin_out);
 }
 
-/* The draft with the gated recurrent head (gate_g, gate_c [r]). */
+/* The draft with the gated recurrent head (gate_g, gate_c [r]; bf16_state as
+ * for oracle_gated_states). */
 int oracle_gated_draft(int B, int G, int V, int r, const float* U, const void* W1,
                        const void* W2, int wdt, const float* gate_g,
-                       const float* gate_c, const int32_t* anchor,
+                       const float* gate_c, int bf16_state, const int32_t* anchor,
                        const int32_t* x_force, uint64_t seed, uint64_t round,
                        int b0, int b1, int32_t* x_out, double* p_out,
                        double* lse_out, double* margin_out) {
   if (!gate_g || !gate_c) return ORACLE_ERR_INVALID;
-  return draft_impl(B, G, V, r, U, W1, W2, wdt, gate_g, gate_c, anchor, x_force,
-                    seed, round, b0, b1, x_out, p_out, lse_out, margin_out);
+  return draft_impl(B, G, V, r, U, W1, W2, wdt, gate_g, gate_c, bf16_state, anchor,
+                    x_force, seed, round, b0, b1, x_out, p_out, lse_out, margin_out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -591,7 +606,8 @@ int oracle_schedule(int R, int G, const double* c, const float* sps, int n_sps,
  * request the margin of the draw of y. */
 static int verify_impl(int B, int G, int V, int r, const float* T, const float* U,
                        const void* W1, const void* W2, int wdt, const float* gate_g,
-                       const float* gate_c, const int32_t* anchor, const int32_t* x,
+                       const float* gate_c, int bf16_state, const int32_t* anchor,
+                       const int32_t* x,
                        const int32_t* ell, uint64_t seed, uint64_t round, int b0,
                        int b1, int32_t* n_out, int32_t* y_out, int32_t* flags_out,
                        double* ratio_out, double* umargin_out,
@@ -635,7 +651,7 @@ static int verify_impl(int B, int G, int V, int r, const float* T, const float* 
       const float* U_row = U + ((size_t)b * G + (k - 1)) * (size_t)V;
       const float* T_row = T + ((size_t)b * (G + 1) + (k - 1)) * (size_t)V;
       if (gate_g) {
-        gated_step(r, W1, wdt, gate_g, gate_c, prev, s);
+        gated_step(r, W1, wdt, gate_g, gate_c, prev, bf16_state, s);
         state_logits(V, r, U_row, s, W2, wdt, p_d);
         const double lse = oracle_logsumexp(V, p_d);
         for (int v = 0; v < V; ++v) p_d[v] = exp(p_d[v] - lse);
@@ -692,7 +708,7 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
                   uint64_t seed, uint64_t round, int b0, int b1,
                   int32_t* n_out, int32_t* y_out, int32_t* flags_out,
                   double* ratio_out, double* umargin_out, double* ymargin_out) {
-  return verify_impl(B, G, V, r, T, U, W1, W2, wdt, NULL, NULL, anchor, x, ell, seed,
+  return verify_impl(B, G, V, r, T, U, W1, W2, wdt, NULL, NULL, 0, anchor, x, ell, seed,
                      round, b0, b1, n_out, y_out, flags_out, ratio_out,
                      umargin_out, ymargin_out);
 }
@@ -701,14 +717,14 @@ int oracle_verify(int B, int G, int V, int r, const float* T, const float* U,
  * position k from the state s_k of the prefix anchor, x_1..x_{k-1}. */
 int oracle_gated_verify(int B, int G, int V, int r, const float* T,
                         const float* U, const void* W1, const void* W2, int wdt,
-                        const float* gate_g, const float* gate_c,
+                        const float* gate_g, const float* gate_c, int bf16_state,
                         const int32_t* anchor, const int32_t* x,
                         const int32_t* ell, uint64_t seed, uint64_t round, int b0,
                         int b1, int32_t* n_out, int32_t* y_out,
                         int32_t* flags_out, double* ratio_out,
                         double* umargin_out, double* ymargin_out) {
   if (!gate_g || !gate_c) return ORACLE_ERR_INVALID;
-  return verify_impl(B, G, V, r, T, U, W1, W2, wdt, gate_g, gate_c, anchor, x, ell,
+  return verify_impl(B, G, V, r, T, U, W1, W2, wdt, gate_g, gate_c, bf16_state, anchor, x, ell,
                      seed, round, b0, b1, n_out, y_out, flags_out, ratio_out,
                      umargin_out, ymargin_out);
 }

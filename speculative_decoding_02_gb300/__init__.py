@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libdspark.so")
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NONFINITE = range(7)
 F32, BF16 = 0, 1
 SCHED_FIXED, SCHED_GREEDY, SCHED_TOPK = 0, 1, 2
-EARLY_TARGET_STATS, ADVANCE_ROUND, TARGET_STATS_FROM_VERIFY, SCRATCH_FROM_DRAFT = 1, 2, 4, 8
+EARLY_TARGET_STATS, ADVANCE_ROUND, TARGET_STATS_FROM_VERIFY, SCRATCH_FROM_DRAFT, GATED_STATES = 1, 2, 4, 8, 16
 
 
 class DSparkError(RuntimeError):
@@ -52,6 +52,9 @@ def _load():
     L.dspark_markov_draft_ex.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, vp,
                                          sz, vp]
     L.dspark_markov_draft_ex.restype = i32
+    L.dspark_gated_markov_draft.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp,
+                                            vp, vp, vp, sz, vp]
+    L.dspark_gated_markov_draft.restype = i32
     L.dspark_confidence.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
     L.dspark_confidence.restype = i32
     L.dspark_schedule.argtypes = [vp, i32, i32, vp, i32, i32, u64, vp, vp, vp, vp, vp, sz, vp]
@@ -198,6 +201,34 @@ def markov_draft(U, W1, W2, anchor, seed, rnd=0, ws=None, T_early=None, round_de
     return x, p, lse
 
 
+def gated_markov_draft(U, W1, W2, gate_g, gate_c, anchor, seed, rnd=0, ws=None, T_early=None, round_dev=None):
+    """x, p, lse of the draft with the gated recurrent head (s_k = e_k + a_k *
+    s_{k-1}, a_k = sigmoid(gate_g * e_k + gate_c), e_k = W1[x_{k-1}]; bias
+    s_k . W2).  gate_g, gate_c: float32 [r].  The states stay in ws for
+    verify(gated=True).  Tensor-core path only (bf16, r = 256)."""
+    L = _load()
+    _need(U, "U", torch.float32)
+    dev = U.device
+    B, G, V = U.shape
+    _need(W1, "W1", device=dev); _need(W2, "W2", W1.dtype, dev); _need(anchor, "anchor", torch.int32, dev)
+    r = W1.shape[-1]
+    _sized(W1, "W1", (V, r)); _sized(W2, "W2", (V, r)); _sized(anchor, "anchor", (B,))
+    _need(gate_g, "gate_g", torch.float32, dev); _need(gate_c, "gate_c", torch.float32, dev)
+    _sized(gate_g, "gate_g", (r,)); _sized(gate_c, "gate_c", (r,))
+    if T_early is not None:
+        _need(T_early, "T_early", torch.float32, dev)
+        _sized(T_early, "T_early", (B, G + 1, V))
+    rd = _round_dev(round_dev, dev)
+    x = torch.empty((B, G), dtype=torch.int32, device=dev)
+    p = torch.empty((B, G), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, G), dtype=torch.float32, device=dev)
+    ws = workspace(B, G, V, dev) if ws is None else ws
+    _check(L.dspark_gated_markov_draft(_ptr(U), _ptr(T_early), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(gate_g),
+                                       _ptr(gate_c), _ptr(anchor), B, G, V, r, seed, rnd, rd, _ptr(x), _ptr(p),
+                                       _ptr(lse), _ptr(ws), ws.numel(), _stream(dev)), "gated_markov_draft")
+    return x, p, lse
+
+
 def confidence(h, W1, w, anchor, x, sts_T=None):
     """c [B,G] f32 = sigmoid(w . [h_k ; W1[x_{k-1}]] / T_k)."""
     L = _load()
@@ -241,12 +272,14 @@ def schedule(c, sps=None, mode=SCHED_GREEDY, rnd=0, khist=None, ws=None, round_d
 
 
 def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None, early_stats=False, round_dev=None,
-           advance_round=False, scratch_from_draft=False):
+           advance_round=False, scratch_from_draft=False, gated=False):
     """n [B] i32 accepted counts, tok [B] i32 corrected / bonus tokens.
     early_stats: ws already holds the target-row statistics from
     markov_draft(T_early=T).  round_dev / advance_round: the round index as a
     device int64 [1], advanced by the call's last kernel.
-    scratch_from_draft: a draft_schedule on ws cleared the call's scratch."""
+    scratch_from_draft: a draft_schedule on ws cleared the call's scratch.
+    gated: the draft was gated_markov_draft on ws (its states are the
+    residual's bias operand)."""
     L = _load()
     _need(T, "T", torch.float32)
     dev = T.device
@@ -267,7 +300,7 @@ def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None, early
     ws = workspace(B, G, V, dev) if ws is None else ws
     rd = _round_dev(round_dev, dev)
     flags = ((EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0) |
-             (SCRATCH_FROM_DRAFT if scratch_from_draft else 0))
+             (SCRATCH_FROM_DRAFT if scratch_from_draft else 0) | (GATED_STATES if gated else 0))
     _check(L.dspark_verify_ex(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x),
                               _ptr(p_d), _ptr(lse_d), _ptr(ell), B, G, V, r, seed, rnd, rd, flags, _ptr(n), _ptr(tok),
                               _ptr(ws), ws.numel(), _stream(dev)), "verify")

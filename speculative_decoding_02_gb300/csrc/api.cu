@@ -94,6 +94,25 @@ int dspark_markov_draft_ex(const float* U, const float* T_early, const void* W1,
   return cuda_status(launch_markov_draft(a, (cudaStream_t)stream));
 }
 
+int dspark_gated_markov_draft(const float* U, const float* T_early, const void* W1, const void* W2, int wdtype,
+                              const float* gate_g, const float* gate_c, const int32_t* anchor, int B, int gamma,
+                              int V, int r, uint64_t seed, uint64_t round, const uint64_t* round_dev,
+                              int32_t* x_out, float* p_out, float* lse_out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
+                          workspace_bytes));
+  if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
+  if (T_early && !aligned(T_early, 16)) return DSPARK_ERR_INVALID;
+  if (!gate_g || !gate_c || !aligned(gate_g, 16) || !aligned(gate_c, 16)) return DSPARK_ERR_INVALID;
+  if (!draft_tc_supported(wdtype, r, V)) return DSPARK_ERR_UNSUPPORTED;
+  DraftArgs a{U, W1, W2, wdtype, anchor, B, gamma, V, r,
+              make_rng_key(seed, round, reinterpret_cast<const unsigned long long*>(round_dev)), x_out, p_out,
+              lse_out, workspace, T_early};
+  a.gate_g = gate_g;
+  a.gate_c = gate_c;
+  return cuda_status(launch_markov_draft(a, (cudaStream_t)stream));
+}
+
 int dspark_markov_draft(const float* U, const void* W1, const void* W2, int wdtype, const int32_t* anchor,
                         int B, int gamma, int V, int r, uint64_t seed, uint64_t round, int32_t* x_out,
                         float* p_out, float* lse_out, void* workspace, size_t workspace_bytes,
@@ -138,15 +157,17 @@ int dspark_verify_ex(const float* T, const float* U, const void* W1, const void*
   DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, n_out, tok_out,
                            workspace, workspace_bytes));
   if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
-  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND | DSPARK_SCRATCH_FROM_DRAFT))
+  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND | DSPARK_SCRATCH_FROM_DRAFT |
+                          DSPARK_GATED_STATES))
     return DSPARK_ERR_INVALID;
+  if ((flags & DSPARK_GATED_STATES) && !draft_tc_supported(wdtype, r, V)) return DSPARK_ERR_UNSUPPORTED;
   if ((flags & DSPARK_ADVANCE_ROUND) && !round_dev) return DSPARK_ERR_INVALID;
   unsigned long long* rd = reinterpret_cast<unsigned long long*>(round_dev);
   // only the tensor-core draft of dspark_draft_schedule clears the scratch
   const bool zeroed = (flags & DSPARK_SCRATCH_FROM_DRAFT) && draft_tc_supported(wdtype, r, V);
   VerifyArgs a{T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, make_rng_key(seed, round, rd),
                n_out, tok_out, workspace, (flags & DSPARK_EARLY_TARGET_STATS) != 0,
-               (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr, zeroed};
+               (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr, zeroed, (flags & DSPARK_GATED_STATES) != 0};
   return cuda_status(launch_verify(a, (cudaStream_t)stream));
 }
 

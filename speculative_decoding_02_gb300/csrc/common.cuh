@@ -271,6 +271,7 @@ struct WsLayout {
   size_t resid_lse;   // float [B] lse of the target row at k*
   size_t resid_prev;  // int32 [B] x_{k*-1} as stored (the anchor when k* = 1)
   size_t tx;          // float [B*gamma] T[b, k-1, x_k], gathered by a draft that takes T along
+  size_t gstate;      // bf16 [B][gamma][256] the gated head's states s_k (tensor-core path)
   size_t bonus_rows;  // int32 [1 + B]: count, then the requests that accepted their whole prefix
   size_t total;
 };
@@ -293,6 +294,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   L.resid_lse = off;   off = align256(off + 4ull * B);
   L.resid_prev = off;  off = align256(off + 4ull * B);
   L.tx = off;          off = align256(off + 4ull * B * gamma);
+  L.gstate = off;      off = align256(off + 2ull * 256 * B * gamma);
   L.bonus_rows = off;  off = align256(off + 4ull * (B + 1));
   L.total = off;
   return L;

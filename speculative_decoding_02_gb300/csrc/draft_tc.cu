@@ -170,6 +170,12 @@ struct StepParams {
   int ntiles;                           // vocabulary tiles of width BN
   RngKey key;
   ConfArgs conf;                        // draft mode: the confidence head in the finalize
+  // the gated recurrent head (gate_g null: the Markov head): its gates [KR]
+  // and the states S [B][G][KR] (bf16) the draft writes and the finalize and
+  // the residual read as their E rows
+  const float* gate_g;
+  const float* gate_c;
+  __nv_bfloat16* S;
   SchedArgs sched;                      // draft mode: the schedule after the finalize
   // draft mode: the verification's scratch to clear at the start (null: none)
   unsigned long long* vz;               // the bonus and residual argmax keys
@@ -483,6 +489,58 @@ __device__ __forceinline__ void gather_e(const __nv_bfloat16* W1, int tok, bool 
   tmem_store_32cols(taddr, ev);
 }
 
+// The gated recurrent head: this warp's part of E becomes the state of
+// position k, s_k = e_k + a_k * s_{k-1} with e_k = W1[tok] and a_k =
+// sigmoid(g * e_k + c) elementwise (K elements 64h .. 64h+63 of the row, two
+// bf16 per TMEM column, lower k in the low half), rounded to bf16 as the
+// tensor cores read it.  s_{k-1} is this E as it stands (prev_from_tmem), the
+// row of S written one position earlier (prev_row, when a launch starts at
+// k > 1), or zero.  The new state also goes to s_row (unless null).
+__device__ __forceinline__ void gated_update_e(const __nv_bfloat16* W1, int tok, bool active, int h, uint32_t taddr,
+                                               const float* __restrict__ gate_g, const float* __restrict__ gate_c,
+                                               bool prev_from_tmem, const __nv_bfloat16* prev_row,
+                                               __nv_bfloat16* s_row) {
+  const uint4* wrow = reinterpret_cast<const uint4*>(W1 + (size_t)tok * KR);
+#pragma unroll 1
+  for (int q8 = 0; q8 < 4; ++q8) {   // 8 columns (16 K elements) at a time
+    uint32_t sp[8], out[8];
+    if (prev_from_tmem) {
+      float f[8];
+      tmem_load_cols<8>(taddr + q8 * 8, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sp[i] = __float_as_uint(f[i]);
+    } else if (prev_row != nullptr && active) {
+      const uint4 a0 = __ldcg(reinterpret_cast<const uint4*>(prev_row + 64 * h + 16 * q8));
+      const uint4 a1 = __ldcg(reinterpret_cast<const uint4*>(prev_row + 64 * h + 16 * q8) + 1);
+      sp[0] = a0.x; sp[1] = a0.y; sp[2] = a0.z; sp[3] = a0.w; sp[4] = a1.x; sp[5] = a1.y; sp[6] = a1.z; sp[7] = a1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sp[i] = 0u;
+    }
+    const uint4 w0 = active ? __ldg(wrow + h * 8 + 2 * q8) : make_uint4(0, 0, 0, 0);
+    const uint4 w1 = active ? __ldg(wrow + h * 8 + 2 * q8 + 1) : make_uint4(0, 0, 0, 0);
+    const uint32_t ew[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int kk = 64 * h + 16 * q8 + 2 * i;   // K element of the low half
+      const float2 g2 = __ldg(reinterpret_cast<const float2*>(gate_g + kk));
+      const float2 c2 = __ldg(reinterpret_cast<const float2*>(gate_c + kk));
+      const float e0 = __uint_as_float(ew[i] << 16), e1 = __uint_as_float(ew[i] & 0xFFFF0000u);
+      const float s0 = __uint_as_float(sp[i] << 16), s1 = __uint_as_float(sp[i] & 0xFFFF0000u);
+      const float a0 = 1.f / (1.f + expf(-fmaf(g2.x, e0, c2.x)));
+      const float a1 = 1.f / (1.f + expf(-fmaf(g2.y, e1, c2.y)));
+      const __nv_bfloat162 n2 = __floats2bfloat162_rn(fmaf(a0, s0, e0), fmaf(a1, s1, e1));
+      out[i] = active ? *reinterpret_cast<const uint32_t*>(&n2) : 0u;
+    }
+    tmem_store_8cols(taddr + q8 * 8, out);
+    if (s_row != nullptr && active) {
+      uint4* dst = reinterpret_cast<uint4*>(s_row + 64 * h + 16 * q8);
+      dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+      dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+  }
+}
+
 // Residual mode: copies the U and T row segments of one 64-column tile
 // starting at column vt into a shared-memory stage, 16 threads to a 256-byte
 // segment (coalesced).  Chunk c of row rr lands at rr * 256 + ((c ^ (rr & 15))
@@ -662,7 +720,7 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
                                               int part_slices, int32_t* __restrict__ x_out, float* __restrict__ p_out,
                                               float* __restrict__ lse_out, const ConfArgs& ca,
                                               const float* __restrict__ T_early, float* __restrict__ tx,
-                                              int* __restrict__ status) {
+                                              const __nv_bfloat16* __restrict__ S, int* __restrict__ status) {
   const int b = item / G, k = item - (item / G) * G + 1;
   const float2* pp = part + (size_t)(k - 1) * part_slices * B;
   float m = -INFINITY, s = 0.f;
@@ -686,9 +744,11 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
     if (prev_x < 0 || prev_x >= V) prev_x = 0;
   }
   const int prev = checked_token(prev_x, V, status);
+  // the bias operand: W1[x_{k-1}], or the gated head's state s_k
+  const __nv_bfloat16* erow = S != nullptr ? S + ((size_t)b * G + (k - 1)) * KR : W1 + (size_t)prev * KR;
   float dot = 0.f;
   for (int i = lane; i < KR; i += 32)
-    dot = fmaf(__bfloat162float(W1[(size_t)prev * KR + i]), __bfloat162float(W2[(size_t)x * KR + i]), dot);
+    dot = fmaf(__bfloat162float(erow[i]), __bfloat162float(W2[(size_t)x * KR + i]), dot);
   for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
   if (lane == 0) {
     const size_t o = (size_t)b * G + (k - 1);
@@ -905,7 +965,18 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         prev = checked_token(raw, p.V, p.status);
       }
       const uint32_t e_taddr = tmem + ((uint32_t)(q * 32) << 16) + kTmemE + h * 32;
-      if (MODE != kDraft || k == kf) {
+      if (MODE == kDraft && p.gate_g != nullptr) {
+        // the gated head: E becomes s_k (from s_{k-1}, which is E as it stands
+        // within a launch); slice 0 of the M tile records it for the finalize
+        // and the residual
+        const size_t srow = (size_t)b * p.G;
+        gated_update_e(p.W1, prev, active, h, e_taddr, p.gate_g, p.gate_c, k > kf,
+                       (k == kf && k > 1) ? p.S + (srow + k - 2) * KR : nullptr,
+                       (slice == 0 && rep == 0) ? p.S + (srow + k - 1) * KR : nullptr);
+      } else if (MODE == kResidual && p.S != nullptr) {
+        // residual of a gated-head draft: E is the state of position k*
+        gather_e(p.S, active ? b * p.G + ks - 1 : 0, active, h, e_taddr);
+      } else if (MODE != kDraft || k == kf) {
         gather_e(p.W1, prev, active, h, e_taddr);
       } else if (__any_sync(0xffffffffu, prev != spec_prev)) {
         // only the rows whose token changed are read again
@@ -1149,7 +1220,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         // position k are complete (its last accumulator was read), so TMEM E
         // is free; load W1[x_k] for the row keys as they stand now.  After the
         // barrier the final keys are compared and only changed rows reload.
-        if constexpr (MODE == kDraft) {
+        if (MODE == kDraft && p.gate_g == nullptr) {
           int sp = 0;
           spec_final = kShare && bars->last;
           if (active) {
@@ -1202,7 +1273,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
         if (!bars->stop) {
           for (int item = blockIdx.x * kEpiWarps + (warp - 2); item < p.B * p.G; item += p.nctas * kEpiWarps)
             finalize_item(item, lane, p.U, p.W1, p.W2, p.anchor, p.keys, p.part, p.B, p.G, p.V, p.ctas_per_mtile,
-                          p.part_slices, p.x_out, p.p_out, p.lse_out, p.conf, p.T_stats, p.tx, p.status);
+                          p.part_slices, p.x_out, p.p_out, p.lse_out, p.conf, p.T_stats, p.tx,
+                          p.gate_g != nullptr ? p.S : nullptr, p.status);
           if (p.sched.ell_out != nullptr) {
             // The last CTA to finish its finalize items (every confidence is
             // written then) runs the round's schedule in its shared memory
@@ -1251,11 +1323,12 @@ __global__ void draft_finalize_tc(const float* __restrict__ U, const __nv_bfloat
                                   const unsigned long long* __restrict__ keys, const float2* __restrict__ part,
                                   int B, int G, int V, int nslices, int part_slices, int32_t* __restrict__ x_out,
                                   float* __restrict__ p_out, float* __restrict__ lse_out, const ConfArgs ca,
-                                  const float* __restrict__ T_early, float* __restrict__ tx, int* __restrict__ status) {
+                                  const float* __restrict__ T_early, float* __restrict__ tx,
+                                  const __nv_bfloat16* __restrict__ S, int* __restrict__ status) {
   const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (item >= B * G) return;
   finalize_item(item, threadIdx.x & 31, U, W1, W2, anchor, keys, part, B, G, V, nslices, part_slices, x_out, p_out,
-                lse_out, ca, T_early, tx, status);
+                lse_out, ca, T_early, tx, S, status);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1393,6 +1466,11 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   sp.stats_part = ws_ptr<float2>(a.ws, L.row_part);
   sp.stats_next = gbar + 1;
   sp.tx = ws_ptr<float>(a.ws, L.tx);
+  if (a.gate_g != nullptr) {
+    sp.gate_g = a.gate_g;
+    sp.gate_c = a.gate_c;
+    sp.S = ws_ptr<__nv_bfloat16>(a.ws, L.gstate);
+  }
   if (a.c_out != nullptr)
     sp.conf = ConfArgs{a.h, a.w, a.sts_T, a.c_out, a.hdtype, a.H, conf_vec(a.h, a.W1, a.w, a.H, a.r)};
   if (a.zero_verify_scratch) {
@@ -1443,7 +1521,8 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
     }
     draft_finalize_tc<<<div_up(a.B * a.gamma * 32, 256), 256, 0, stream>>>(
         a.U, static_cast<const __nv_bfloat16*>(a.W1), static_cast<const __nv_bfloat16*>(a.W2), a.anchor, keys,
-        part, a.B, a.gamma, a.V, per, part_slices, a.x_out, a.p_out, a.lse_out, sp.conf, a.T_stats, sp.tx, status);
+        part, a.B, a.gamma, a.V, per, part_slices, a.x_out, a.p_out, a.lse_out, sp.conf, a.T_stats, sp.tx,
+        sp.gate_g != nullptr ? sp.S : nullptr, status);
     // one launch per position: the target-row statistics follow the draft
     if (a.T_stats != nullptr && (e = cudaGetLastError()) == cudaSuccess)
       e = launch_row_stats(a.T_stats, nullptr, a.B, a.gamma, a.V, a.ws, stream);
@@ -1465,7 +1544,7 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
                                const int32_t* resid_prev, const float* lse_d, const int32_t* resid_k,
                                const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
-                               RngKey key, int* status, cudaStream_t stream) {
+                               RngKey key, const void* gstate, int* status, cudaStream_t stream) {
   CUtensorMap map;
   cudaError_t e = make_w2_tensor_map(W2, V, &map);
   if (e != cudaSuccess) return e;
@@ -1486,6 +1565,8 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
   sp.W1 = static_cast<const __nv_bfloat16*>(W1);
   sp.T = T;
   sp.resid_prev = resid_prev;
+  // a gated-head draft's states: the residual's E rows (null: W1 rows)
+  sp.S = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(gstate));
   sp.resid_k = resid_k;
   sp.lse_d = lse_d;
   sp.resid_lse = resid_lse;

@@ -69,6 +69,10 @@ struct DraftArgs {
   int32_t* ell_out;
   int32_t* nstar_out;
   double* theta_out;
+  // optional: the gated recurrent head's gates g, c [r] (null: the Markov
+  // head); tensor-core path only, its states go to the workspace
+  const float* gate_g;
+  const float* gate_c;
 };
 
 struct VerifyArgs {
@@ -94,6 +98,9 @@ struct VerifyArgs {
   unsigned long long* advance_round;
   // the draft of this round cleared the scratch (DraftArgs::zero_verify_scratch)
   bool scratch_zeroed;
+  // the draft used the gated recurrent head: its states in the workspace are
+  // the residual's bias operand (tensor-core path)
+  bool gated_states;
 };
 
 // Host-side argument checks shared by every entry point that takes these
@@ -144,7 +151,7 @@ cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtens
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
                                const int32_t* resid_prev, const float* lse_d, const int32_t* resid_k,
                                const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
-                               RngKey key, int* status, cudaStream_t stream);
+                               RngKey key, const void* gstate, int* status, cudaStream_t stream);
 
 // Acceptance labels (tensor-core path, one persistent launch over the
 // positions): sum_v min(p_d, p_t) per verified position into label [B][G]

@@ -253,6 +253,14 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// 8 consecutive 32-bit columns of this warp's 32 TMEM lanes, one lane per thread.
+__device__ __forceinline__ void tmem_store_8cols(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // N consecutive fp32 columns (N = 4, 8, 16 or 32) of this warp's 32 TMEM lanes,
 // one lane per thread.
 template <int N>

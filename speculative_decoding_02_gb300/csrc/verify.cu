@@ -564,9 +564,12 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   int32_t* bonus_rows = ws_ptr<int32_t>(a.ws, L.bonus_rows);
   int32_t* resid_prev = ws_ptr<int32_t>(a.ws, L.resid_prev);
   const int nsegs = a.stats_ready ? stats_num_segs(a.V) : verify_num_segs(a.V);
+  // the scratch that must start at zero (the bonus and residual keys and the
+  // bonus list; resid_k and resid_lse lie between them and are rewritten):
+  // not what a draft left after it (resid_prev, tx, the gated states)
   cudaError_t e = cudaSuccess;
-  if (!a.scratch_zeroed && (e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.total - L.bonus_key, stream)) !=
-                               cudaSuccess)
+  if (!a.scratch_zeroed &&
+      (e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.resid_prev - L.bonus_key, stream)) != cudaSuccess)
     return e;
   if (!a.stats_ready && (e = row_stats(a.T, a.ell, a.B, a.gamma, a.V, a.ws, stream)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -598,7 +601,8 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
     if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
     if (tc) {
       e = launch_residual_tc(a.T, a.U, a.W1, a.W2, resid_prev, a.lse_d, resid_k, resid_lse, resid_key, a.B,
-                             a.gamma, a.V, a.key, status, stream);
+                             a.gamma, a.V, a.key, a.gated_states ? ws_ptr<void>(a.ws, L.gstate) : nullptr, status,
+                             stream);
       if (e != cudaSuccess) return e;
     } else {
       const dim3 grid_res(draft_num_slices(a.V), a.B);

@@ -132,6 +132,13 @@ def make_weights(wl: Workload, device="cpu"):
     return dict(W1=W1, W2=W2, w=w, anchor=anchor)
 
 
+def make_gates(wl: Workload, device="cpu"):
+    """The gated recurrent head's gates g, c [r] float32 (seeded; both N(0, 1),
+    so that the gates sigmoid(g * e + c) spread over (0, 1))."""
+    g = _gen(device, 1000003 * wl.seed + 29)
+    return dict(gate_g=_normal((wl.r,), 1.0, g, device), gate_c=_normal((wl.r,), 1.0, g, device))
+
+
 def make_round_inputs(wl: Workload, rnd: int = 0, device="cpu"):
     """U [B,gamma,V], T [B,gamma+1,V], h [B,gamma,H] for round `rnd` (seeded)."""
     g = _gen(device, 1000003 * wl.seed + 7919 * (rnd + 1))

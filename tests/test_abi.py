@@ -182,6 +182,24 @@ def test_binding_shape_checks():
         out.check(2, 3, torch.device("cpu"))   # CPU buffers are refused first
 
 
+def test_gated_draft_argument_errors(lib):
+    p = _fake()
+    ws = _fake(0x100000)
+    big = 1 << 30
+    # missing or misaligned gates; fp32 weights (tensor-core path only)
+    assert lib.dspark_gated_markov_draft(p, None, p, p, 1, None, p, p, 2, 4, 1024, 256, 0, 0, None, p, p, p, ws,
+                                         big, None) == ds.ERR_INVALID
+    assert lib.dspark_gated_markov_draft(p, None, p, p, 1, _fake(0x10004), p, p, 2, 4, 1024, 256, 0, 0, None, p, p,
+                                         p, ws, big, None) == ds.ERR_INVALID
+    assert lib.dspark_gated_markov_draft(p, None, p, p, 0, p, p, p, 2, 4, 1024, 256, 0, 0, None, p, p, p, ws, big,
+                                         None) == ds.ERR_UNSUPPORTED
+    assert lib.dspark_gated_markov_draft(p, None, p, p, 1, p, p, p, 2, 4, 1024, 64, 0, 0, None, p, p, p, ws, big,
+                                         None) == ds.ERR_UNSUPPORTED
+    # verification of a gated draft on the CUDA-core path
+    assert lib.dspark_verify_ex(p, p, p, p, 0, p, p, p, p, p, 2, 4, 1024, 64, 0, 0, None, ds.GATED_STATES, p, p,
+                                ws, big, None) == ds.ERR_UNSUPPORTED
+
+
 def test_acceptance_label_and_sts_argument_errors(lib):
     p = _fake()
     ws = _fake(0x100000)

@@ -242,6 +242,28 @@ EARLY = [
 
 
 @pytest.mark.parametrize("B,G,V,r,dt,mode", EARLY)
+def test_stages_called_one_by_one_equal_the_round(B, G, V, r, dt, mode):
+    # markov_draft(T_early) + confidence + schedule + verify(early_stats) on
+    # one workspace, each call separate (verification clears its own scratch):
+    # the same bits as the round, whose first stage clears that scratch and
+    # leaves T at the drafted tokens and the row statistics for verification
+    w = wl.custom(B=B, gamma=G, V=V, r=r, H=64, wdtype=dt, mode=mode, u_sigma=2.0, seed=71, sps_b0=float(B))
+    inp = wl.make_inputs(w, 0, DEV)
+    ref = run_round(inp, w, rnd=4, early_stats=True)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 4, ws=ws, T_early=inp["T"])
+    c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
+    khist = torch.zeros(2, dtype=torch.int32, device=DEV) if mode == wl.MODE_TOPK else None
+    ell, _, _ = ds.schedule(c, inp["sps"], mode, 4, khist, ws)
+    n, tok = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, 4, ws,
+                       early_stats=True)
+    torch.cuda.synchronize()
+    assert ds.read_status(ws) == ds.OK
+    for name, got in (("x", x), ("p", p), ("lse", lse), ("c", c), ("ell", ell), ("n", n), ("tok", tok)):
+        assert torch.equal(ref.as_dict()[name], got), name
+
+
+@pytest.mark.parametrize("B,G,V,r,dt,mode", EARLY)
 def test_early_target_stats_round(B, G, V, r, dt, mode):
     w = wl.custom(B=B, gamma=G, V=V, r=r, H=64, wdtype=dt, mode=mode, seed=B + 3 * G, u_sigma=2.5,
                   t_sigma=(0.4, 1.5), sps_b0=float(4 * B) if mode == wl.MODE_GREEDY else None,

@@ -101,3 +101,33 @@ def test_gated_draft_scores_each_position_with_its_state():
     m = oracle.draft(U, W1, W2, anchor, 9, 0, x_force=d["x"])
     assert np.array_equal(m["lse"][:, 0], d["lse"][:, 0])
     assert np.all(np.abs(m["lse"][:, 1:] - d["lse"][:, 1:]) > 1e-9)
+
+
+def _bf16_rne(x):
+    # nearest bf16 (ties to even) of float64 values, through their float32 bits
+    u = np.asarray(x, np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return u.view(np.float32).astype(np.float64)
+
+
+def test_bf16_state_rounds_each_step():
+    # the tensor-core precision option: every state rounded to bf16 as it is
+    # formed, then carried; checked against an independent rounding
+    V, r, G = 60, 16, 6
+    rng, W1, _ = _weights(V, r, 5)
+    W1b = (W1.view(np.uint32) >> 16).astype(np.uint16)           # bf16 bits
+    e_all = (W1b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    g = rng.standard_normal(r).astype(np.float32)
+    c = rng.standard_normal(r).astype(np.float32)
+    toks = rng.integers(0, V, G)
+    s = oracle.gated_states(W1b, g, c, int(toks[0]), toks[1:], G, bf16_state=True)
+    want = np.zeros(r)
+    for k in range(G):
+        e = e_all[toks[k]]
+        a = 1.0 / (1.0 + np.exp(-(g.astype(np.float64) * e + c.astype(np.float64))))
+        want = _bf16_rne(e + a * want)
+        assert np.array_equal(s[k], want), k
+    exact = oracle.gated_states(W1b, g, c, int(toks[0]), toks[1:], G)
+    # each step rounds to 2^-9 relative; the gate (below 1) carries the error on
+    np.testing.assert_allclose(s, exact, rtol=0, atol=G * 2.0 ** -9 * np.abs(exact).max())
+    assert not np.array_equal(s, exact)
