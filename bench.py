@@ -436,6 +436,50 @@ def round_record(w, r, hbm, early):
             "draft_hbm_frac": db / (r["draft_ms"] / 1e3) / 1e9 / hbm, "early_target_stats": early}
 
 
+def gated_round_ms(ds, w, inp, dev, steps):
+    """Rounds with the gated recurrent head instead of the Markov head: its
+    draft (target-row statistics taken along), the confidences, the schedule
+    and verification of the gated draft, K rounds timed with CUDA events."""
+    from speculative_decoding_02_gb300 import workloads as wl
+    gates = wl.make_gates(w, dev)
+    khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == 2 else None
+    ws = ds.workspace(w.B, w.gamma, w.V, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, d0=None, d1=None):
+        if d0 is not None:
+            d0.record(stream)
+        x, p, lse = ds.gated_markov_draft(inp["U"], inp["W1"], inp["W2"], gates["gate_g"], gates["gate_c"],
+                                          inp["anchor"], w.seed, i, ws=ws, T_early=inp["T"])
+        if d1 is not None:
+            d1.record(stream)
+        c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
+        ell, _, _ = ds.schedule(c, inp["sps"], w.mode, i, khist, ws)
+        n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, i, ws,
+                         early_stats=True, gated=True)
+        return ell, n
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    if ds.read_status(ws) != ds.OK:
+        raise RuntimeError("device status after the gated-head rounds")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    outs = [step(3 + i, *ev[i]) for i in range(steps)]
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if ds.read_status(ws) != ds.OK:
+        raise RuntimeError("device status in the gated-head rounds")
+    ms = e0.elapsed_time(e1) / steps
+    ell_sum = sum(int(e.sum()) for e, _ in outs)
+    return {"ms": ms, "draft_ms": float(np.mean([a.elapsed_time(b) for a, b in ev])),
+            "verified_tokens_per_s": ell_sum / (ms * steps / 1e3),
+            "accepted_per_round": sum(int(n.sum()) for _, n in outs) / steps,
+            "note": "gated recurrent head (gates N(0, 1)); draft, confidence, schedule and verify as separate calls"}
+
+
 def graph_round_ms(ds, w, inp, dev, steps):
     """One round captured into a CUDA graph with the round index in device
     memory (advanced by the round's last kernel), replayed `steps` times."""
@@ -561,6 +605,7 @@ def run_gpu(args):
             extra["truncating_schedule"] = rec
         if early:
             extra["graph_replay"] = graph_round_ms(ds, w, inp, dev, args.steps)
+            extra["gated_head"] = gated_round_ms(ds, w, inp, dev, args.steps)
 
     # the acceptance labels of one round's verified positions (a widening of
     # the path: sum_v min(p_d, p_t) per position), timed on their own; the
