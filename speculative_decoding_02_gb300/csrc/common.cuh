@@ -273,6 +273,7 @@ struct WsLayout {
   size_t tx;          // float [B*gamma] T[b, k-1, x_k], gathered by a draft that takes T along
   size_t gstate;      // bf16 [B][gamma][256] the gated head's states s_k (tensor-core path)
   size_t bonus_rows;  // int32 [1 + B]: count, then the requests that accepted their whole prefix
+  size_t fin_count;   // u32 [2]: CTAs of the bonus race and of the residual that are done
   size_t total;
 };
 
@@ -288,14 +289,17 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   L.draft_part = off;  off = align256(off + 8ull * gamma * draft_part_slices(V) * B);
   L.rows = off;        off = align256(off + 4ull * rows);
   L.row_part = off;    off = align256(off + 8ull * rows * stats_num_segs(V));
+  // [bonus_key, resid_k): the verification scratch that must start at zero
   L.bonus_key = off;   off = align256(off + 8ull * B);
   L.resid_key = off;   off = align256(off + 8ull * kKeyStride * B);
+  L.bonus_rows = off;  off = align256(off + 4ull * (B + 1));
+  L.fin_count = off;   off = align256(off + 8);
+  // then what verification writes before it reads, and what a draft leaves
   L.resid_k = off;     off = align256(off + 4ull * B);
   L.resid_lse = off;   off = align256(off + 4ull * B);
   L.resid_prev = off;  off = align256(off + 4ull * B);
   L.tx = off;          off = align256(off + 4ull * B * gamma);
   L.gstate = off;      off = align256(off + 2ull * 256 * B * gamma);
-  L.bonus_rows = off;  off = align256(off + 4ull * (B + 1));
   L.total = off;
   return L;
 }
@@ -303,6 +307,39 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
 template <typename T>
 __host__ __device__ inline T* ws_ptr(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// One warp's draw from softmax(Trow) on the residual's streams (2 and 6) for
+// request b at position ks: the fallback of a residual that had no positive
+// entry in floating point (a measure-zero event).  Two passes over the row,
+// the maximum and then the two-level race of blocks of 4 with weights
+// exp(T - max), as verify_residual_finalize draws it with a whole CTA.
+// Returns the token on every lane, -1 if no block had weight.
+static __device__ __noinline__ int warp_softmax_draw(const float* __restrict__ Trow, int V, uint32_t b, uint32_t ks,
+                                                     const RngKey& key, int lane) {
+  float mx = -INFINITY;
+  for (int v = 4 * lane; v < V; v += 128) {
+    const float4 t4 = *reinterpret_cast<const float4*>(Trow + v);
+    mx = fmaxf(mx, fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w)));
+  }
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  unsigned long long best = 0ull;
+  for (int v = 4 * lane; v < V; v += 128) {
+    const float4 t4 = *reinterpret_cast<const float4*>(Trow + v);
+    const float e0 = expf(t4.x - mx), e1 = expf(t4.y - mx), e2 = expf(t4.z - mx), e3 = expf(t4.w - mx);
+    const float W = ((e0 + e1) + e2) + e3;
+    if (!(W > 0.f)) continue;
+    const uint32_t j = (uint32_t)v >> 2;
+    const uint32_t w = word_of(rng_call(key, kStreamResidual, b, ks, j >> 2), j & 3u);
+    const float z = mx + logf(W) + gumbel_from_bits(w >> 9);
+    if (argmax_key(z, v) > best) {
+      const int vv = block_pick(key, kStreamResidual, b, ks, j, e0, e1, e2, e3);
+      const unsigned long long kz = argmax_key(z, vv);
+      best = kz > best ? kz : best;
+    }
+  }
+  best = warp_max_u64(best, 0xffffffffu, 32);
+  return best ? argmax_key_index(best) : -1;
 }
 
 }  // namespace dspark

@@ -178,9 +178,8 @@ struct StepParams {
   __nv_bfloat16* S;
   SchedArgs sched;                      // draft mode: the schedule after the finalize
   // draft mode: the verification's scratch to clear at the start (null: none)
-  unsigned long long* vz;               // the bonus and residual argmax keys
+  unsigned long long* vz;               // [bonus_key, resid_k): keys, bonus list, finish counters
   int vz_words;
-  int* vz_count;                        // the bonus list's count
 };
 
 __device__ __forceinline__ int tile_begin(int slice, int nslices, int ntiles) {
@@ -800,7 +799,6 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
     if (p.vz != nullptr) {
       for (int i = blockIdx.x * threads_of<MODE>() + threadIdx.x; i < p.vz_words; i += gridDim.x * threads_of<MODE>())
         p.vz[i] = 0ull;
-      if (blockIdx.x == 0 && threadIdx.x == 0) *p.vz_count = 0;
     }
   }
   // (no early trigger in either mode: the next kernel's CTAs, resident and
@@ -1476,7 +1474,6 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   if (a.zero_verify_scratch) {
     sp.vz = ws_ptr<unsigned long long>(a.ws, L.bonus_key);
     sp.vz_words = (int)((L.resid_k - L.bonus_key) / sizeof(unsigned long long));
-    sp.vz_count = ws_ptr<int>(a.ws, L.bonus_rows);
   }
 
   // One persistent launch over all positions when every CTA can be resident

@@ -199,10 +199,10 @@ constexpr int kBonusThreads = 64;
 
 __global__ void __launch_bounds__(kBonusThreads)
 verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
-                  const int32_t* __restrict__ bonus_rows, int G, int V, int nsegs, RngKey key_arg,
+                  const int32_t* __restrict__ bonus_rows, int B, int G, int V, int nsegs, RngKey key_arg,
                   unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
   pdl_wait();   // the bonus list from verify_decide (a no-op on the side stream)
-  const int nrows = bonus_rows[0];
+  const int nrows = min(bonus_rows[0], B);
   if ((int)blockIdx.x >= nrows * nsegs) return;
   const RngKey key = live_key(key_arg);
   __shared__ unsigned long long s_k[kBonusThreads / 32];
@@ -364,7 +364,11 @@ __global__ void verify_decide(const float* __restrict__ T, const int32_t* __rest
       resid_lse[b] = lse_n;
       resid_prev[b] = n == 0 ? anchor[b] : x_prev;
     } else {
-      bonus_rows[1 + atomicAdd(bonus_rows, 1)] = b;   // the bonus race takes it
+      // the bonus race takes it (a list of at most B: a count past it means
+      // the list did not start empty)
+      const int slot = atomicAdd(bonus_rows, 1);
+      if (slot < B) bonus_rows[1 + slot] = b;
+      else record_status(status, DSPARK_ERR_INVALID);
     }
   }
 }
@@ -564,12 +568,12 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   int32_t* bonus_rows = ws_ptr<int32_t>(a.ws, L.bonus_rows);
   int32_t* resid_prev = ws_ptr<int32_t>(a.ws, L.resid_prev);
   const int nsegs = a.stats_ready ? stats_num_segs(a.V) : verify_num_segs(a.V);
-  // the scratch that must start at zero (the bonus and residual keys and the
-  // bonus list; resid_k and resid_lse lie between them and are rewritten):
-  // not what a draft left after it (resid_prev, tx, the gated states)
+  // the scratch that must start at zero: the bonus and residual keys, the
+  // bonus list and the finish counters (not what a draft left after them:
+  // resid_prev, tx, the gated states)
   cudaError_t e = cudaSuccess;
   if (!a.scratch_zeroed &&
-      (e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.resid_prev - L.bonus_key, stream)) != cudaSuccess)
+      (e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.resid_k - L.bonus_key, stream)) != cudaSuccess)
     return e;
   if (!a.stats_ready && (e = row_stats(a.T, a.ell, a.B, a.gamma, a.V, a.ws, stream)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -595,8 +599,8 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
     if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
     const int bonus_segs = div_up(a.V, kBonusSeg);
     const int grid_bonus = std::min(a.B * bonus_segs, sms * 4);
-    verify_bonus_race<<<grid_bonus, kBonusThreads, 0, ss->s>>>(a.T, a.ell, bonus_rows, a.gamma, a.V, bonus_segs, a.key,
-                                                              bonus_key, status);
+    verify_bonus_race<<<grid_bonus, kBonusThreads, 0, ss->s>>>(a.T, a.ell, bonus_rows, a.B, a.gamma, a.V, bonus_segs,
+                                                              a.key, bonus_key, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
     if (tc) {

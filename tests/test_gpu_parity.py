@@ -255,12 +255,15 @@ def test_stages_called_one_by_one_equal_the_round(B, G, V, r, dt, mode):
     c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
     khist = torch.zeros(2, dtype=torch.int32, device=DEV) if mode == wl.MODE_TOPK else None
     ell, _, _ = ds.schedule(c, inp["sps"], mode, 4, khist, ws)
-    n, tok = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, 4, ws,
-                       early_stats=True)
-    torch.cuda.synchronize()
-    assert ds.read_status(ws) == ds.OK
-    for name, got in (("x", x), ("p", p), ("lse", lse), ("c", c), ("ell", ell), ("n", n), ("tok", tok)):
-        assert torch.equal(ref.as_dict()[name], got), name
+    # twice on the same workspace: each call starts its scratch (the bonus
+    # list, the keys) afresh
+    for _ in range(2):
+        n, tok = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, 4, ws,
+                           early_stats=True)
+        torch.cuda.synchronize()
+        assert ds.read_status(ws) == ds.OK
+        for name, got in (("x", x), ("p", p), ("lse", lse), ("c", c), ("ell", ell), ("n", n), ("tok", tok)):
+            assert torch.equal(ref.as_dict()[name], got), name
 
 
 @pytest.mark.parametrize("B,G,V,r,dt,mode", EARLY)
