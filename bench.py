@@ -121,10 +121,11 @@ def kernels_per_round(w, early=False):
     statistics a prep and a row-statistics kernel follow), the confidence
     and the schedule kernels.  Verify: prep and row statistics (not with
     early statistics), decide, bonus race, residual (the draft kernel in
-    residual mode, or its CUDA-core form), residual finalize."""
+    residual mode, whose last CTA and the bonus race's write the tokens; or
+    its CUDA-core form and then the residual finalize)."""
     tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
     stage = 1 if tc else 2 * w.gamma + (2 if early else 0) + 2
-    verify = 4 if early else 6
+    verify = (3 if tc else 4) + (0 if early else 2)
     return stage + verify
 
 

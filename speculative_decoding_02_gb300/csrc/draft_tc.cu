@@ -149,6 +149,10 @@ struct StepParams {
   const float* lse_d;
   const float* resid_lse;
   unsigned long long* resid_key;
+  // residual mode (fin not null): the last CTA to finish writes the tokens of
+  // the rejecting requests (fin counts finished CTAs, zeroed before)
+  unsigned int* fin;
+  int32_t* tok_out;
   int nsegs;                            // draft mode: target-statistics segments per row
   // draft mode: softmax partials of the target rows j < G of every request,
   // taken while the draft runs (T_stats null: none); stats_part is the
@@ -1253,6 +1257,47 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       }
     }
     cp_async_wait_all();   // no copy outlives the CTA's shared memory
+    if constexpr (MODE == kResidual) {
+      if (p.fin != nullptr) {
+        // every residual key this CTA raises was raised before this barrier;
+        // the CTA whose count completes the grid's writes the tokens: the
+        // winner of each rejecting request's race, or (a residual with no
+        // positive entry in floating point) a draw from its T row
+        named_bar_sync(1, kEpiWarps * 32);
+        if (warp == 2 && lane == 0) {
+          __threadfence();
+          bars->sched = atomicAdd(p.fin, 1u) == (unsigned int)p.nctas - 1u ? 1 : 0;
+        }
+        named_bar_sync(1, kEpiWarps * 32);
+        if (bars->sched) {
+          __threadfence();
+          // one request per thread; the rare draws from a T row by the warp
+          for (int base = 0; base < p.B; base += kEpiWarps * 32) {
+            const int bb = base + (int)threadIdx.x - 64;
+            int ks = 0;
+            unsigned long long k1 = 0ull;
+            if (bb < p.B) {
+              ks = p.resid_k[bb];
+              k1 = __ldcg(p.resid_key + (size_t)bb * kKeyStride);
+            }
+            if (bb < p.B && ks > 0 && k1) p.tok_out[bb] = argmax_key_index(k1);
+            unsigned int fb = __ballot_sync(0xffffffffu, bb < p.B && ks > 0 && !k1);
+            while (fb) {
+              const int src = __ffs(fb) - 1;
+              fb &= fb - 1;
+              const int b2 = __shfl_sync(0xffffffffu, bb, src), k2 = __shfl_sync(0xffffffffu, ks, src);
+              int tok = warp_softmax_draw(p.T + ((size_t)b2 * (p.G + 1) + (k2 - 1)) * p.V, p.V, (uint32_t)b2,
+                                          (uint32_t)k2, key, lane);
+              if (tok < 0) {
+                if (lane == 0) record_status(p.status, DSPARK_ERR_NONFINITE);
+                tok = 0;
+              }
+              if (lane == 0) p.tok_out[b2] = tok;
+            }
+          }
+        }
+      }
+    }
     if constexpr (MODE == kDraft) {
       if (p.x_out != nullptr) {
         // Fused finalize (persistent launch over every position): once every
@@ -1541,7 +1586,8 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
                                const int32_t* resid_prev, const float* lse_d, const int32_t* resid_k,
                                const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
-                               RngKey key, const void* gstate, int* status, cudaStream_t stream) {
+                               RngKey key, const void* gstate, unsigned int* fin, int32_t* tok_out, int* status,
+                               cudaStream_t stream) {
   CUtensorMap map;
   cudaError_t e = make_w2_tensor_map(W2, V, &map);
   if (e != cudaSuccess) return e;
@@ -1568,6 +1614,8 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
   sp.lse_d = lse_d;
   sp.resid_lse = resid_lse;
   sp.resid_key = resid_key;
+  sp.fin = fin;
+  sp.tok_out = tok_out;
   sp.status = status;
   sp.B = B; sp.G = G; sp.V = V;
   sp.k_first = sp.k_last = 0;

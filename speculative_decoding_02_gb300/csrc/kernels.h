@@ -151,7 +151,8 @@ cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtens
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,
                                const int32_t* resid_prev, const float* lse_d, const int32_t* resid_k,
                                const float* resid_lse, unsigned long long* resid_key, int B, int G, int V,
-                               RngKey key, const void* gstate, int* status, cudaStream_t stream);
+                               RngKey key, const void* gstate, unsigned int* fin, int32_t* tok_out, int* status,
+                               cudaStream_t stream);
 
 // Acceptance labels (tensor-core path, one persistent launch over the
 // positions): sum_v min(p_d, p_t) per verified position into label [B][G]

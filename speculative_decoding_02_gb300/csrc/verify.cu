@@ -200,10 +200,10 @@ constexpr int kBonusThreads = 64;
 __global__ void __launch_bounds__(kBonusThreads)
 verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
                   const int32_t* __restrict__ bonus_rows, int B, int G, int V, int nsegs, RngKey key_arg,
-                  unsigned long long* __restrict__ bonus_key, int* __restrict__ status) {
+                  unsigned long long* __restrict__ bonus_key, unsigned int* __restrict__ fin,
+                  int32_t* __restrict__ tok_out, int* __restrict__ status) {
   pdl_wait();   // the bonus list from verify_decide (a no-op on the side stream)
   const int nrows = min(bonus_rows[0], B);
-  if ((int)blockIdx.x >= nrows * nsegs) return;
   const RngKey key = live_key(key_arg);
   __shared__ unsigned long long s_k[kBonusThreads / 32];
   constexpr int kChunks = kBonusSeg / (16 * kBonusThreads);
@@ -314,6 +314,26 @@ verify_bonus_race(const float* __restrict__ T, const int32_t* __restrict__ ell,
     __syncthreads();
   }
   if (bad) record_status(status, DSPARK_ERR_NONFINITE);
+  // fin given: the last CTA to finish writes the bonus tokens (every task's
+  // key is final then)
+  if (fin != nullptr) {
+    __shared__ int s_last;
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      s_last = atomicAdd(fin, 1u) == gridDim.x - 1u;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      for (int i = tid; i < nrows; i += kBonusThreads) {
+        const int b = bonus_rows[1 + i];
+        const unsigned long long kb = __ldcg(bonus_key + b);
+        if (kb == 0ull) record_status(status, DSPARK_ERR_NONFINITE);
+        tok_out[b] = kb ? argmax_key_index(kb) : 0;
+      }
+    }
+  }
 }
 
 __global__ void verify_decide(const float* __restrict__ T, const int32_t* __restrict__ x,
@@ -599,14 +619,18 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
     if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
     const int bonus_segs = div_up(a.V, kBonusSeg);
     const int grid_bonus = std::min(a.B * bonus_segs, sms * 4);
+    // the tensor-core path writes every token from the two kernels' last
+    // CTAs; the CUDA-core path leaves them to verify_residual_finalize
+    unsigned int* fin = ws_ptr<unsigned int>(a.ws, L.fin_count);
     verify_bonus_race<<<grid_bonus, kBonusThreads, 0, ss->s>>>(a.T, a.ell, bonus_rows, a.B, a.gamma, a.V, bonus_segs,
-                                                              a.key, bonus_key, status);
+                                                              a.key, bonus_key, tc ? fin : nullptr, a.tok_out,
+                                                              status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
     if (tc) {
       e = launch_residual_tc(a.T, a.U, a.W1, a.W2, resid_prev, a.lse_d, resid_k, resid_lse, resid_key, a.B,
-                             a.gamma, a.V, a.key, a.gated_states ? ws_ptr<void>(a.ws, L.gstate) : nullptr, status,
-                             stream);
+                             a.gamma, a.V, a.key, a.gated_states ? ws_ptr<void>(a.ws, L.gstate) : nullptr, fin + 1,
+                             a.tok_out, status, stream);
       if (e != cudaSuccess) return e;
     } else {
       const dim3 grid_res(draft_num_slices(a.V), a.B);
@@ -616,10 +640,12 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
     }
     if ((e = cudaStreamWaitEvent(stream, ss->join, 0)) != cudaSuccess) return e;
   }
-  e = launch_pdl(verify_residual_finalize, dim3(a.B), dim3(kRowThreads), 0, stream, a.T, a.B, a.gamma, a.V, a.key,
-                 (const int32_t*)resid_k, (const unsigned long long*)resid_key, (const unsigned long long*)bonus_key,
-                 a.tok_out, status);
-  if (e != cudaSuccess) return e;
+  if (!tc) {
+    e = launch_pdl(verify_residual_finalize, dim3(a.B), dim3(kRowThreads), 0, stream, a.T, a.B, a.gamma, a.V, a.key,
+                   (const int32_t*)resid_k, (const unsigned long long*)resid_key, (const unsigned long long*)bonus_key,
+                   a.tok_out, status);
+    if (e != cudaSuccess) return e;
+  }
   if (a.advance_round != nullptr && (e = launch_pdl(advance_round, dim3(1), dim3(32), 0, stream, a.advance_round)) !=
                                         cudaSuccess)
     return e;
