@@ -5,18 +5,20 @@ prefix scheduler, rejection-sampling verification -- over one batch of the
 synthetic workload (default: batch-128 engine point, B=128, gamma=16,
 V=151936).  The metric is verified draft tokens per second: the sum over
 requests of the scheduled verify lengths l_r, per round, divided by the round
-time.  The round's target logits T are an input of the round, so the draft
-takes their rows' softmax statistics while it runs (DSPARK_EARLY_TARGET_STATS);
-the same round with verification streaming those rows itself is reported
-beside it ("classic_round"), with the other workloads, a truncating schedule
-and a CUDA-graph replay of the round.
+time.  The headline round verifies along each request's accept chain, reading
+the target rows its accept tests reach (the default of dspark_round).  The
+same round with the draft taking the statistics of every target row j < gamma
+while it runs (DSPARK_EARLY_TARGET_STATS: T given at draft time) and with
+verification taking those of every row j < l_r first (DSPARK_ALL_ROW_STATS)
+are reported beside it, with the other workloads, a truncating schedule and a
+CUDA-graph replay of the round.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                         [--impl gb300|reference] [--no-cpu-baseline] [--no-e2e]
-                        [--no-workloads]
+                        [--no-workloads] [--form chain|early|all]
         python bench.py --profile-draft [--workload NAME]   (the draft alone, for ncu)
         python bench.py --profile-label [--workload NAME]   (the acceptance labels alone)
-        python bench.py --profile-round [--workload NAME]   (whole rounds, for launch lists)
+        python bench.py --profile-round [--workload NAME] [--form F]   (whole rounds, for launch lists)
 
 Prints one JSON line.  With N > 1 (torchrun) each rank runs an independent
 replica of the workload (the path shards over requests with no exchange), the
@@ -40,6 +42,17 @@ sys.path.insert(0, ROOT)
 METRIC = "verified draft tokens/s (B=128,γ=16,V=151936) on 1 GB300; % HBM roofline"
 UNIT = "tokens/s"
 
+# Forms of a round, by where verification gets the softmax statistics of the
+# target rows its accept tests use:
+#   chain  verification reads only the rows the accept tests reach (row j of a
+#          request once its positions 1..j were accepted): dspark_round's default
+#   early  the draft takes the rows j < gamma while it runs (T given at draft
+#          time; DSPARK_EARLY_TARGET_STATS)
+#   all    verification takes every row j < l_r first (DSPARK_ALL_ROW_STATS)
+FORMS = {"chain": "verification along the accept chains",
+         "early": "target-row statistics taken by the draft",
+         "all": "verification's pass over every row j < l_r"}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -62,6 +75,9 @@ def parse():
                     help="the acceptance labels alone, 4 calls on a draft's statistics (for ncu)")
     ap.add_argument("--profile-round", action="store_true",
                     help="run a few whole rounds of the workload (ncu launch lists and kernel captures)")
+    ap.add_argument("--form", default="chain", choices=list(FORMS),
+                    help="the headline round's form (and --profile-round's): where the target rows' "
+                         "statistics come from")
     return ap.parse_args()
 
 
@@ -77,11 +93,27 @@ def peaks():
 # ---------------------------------------------------------------------------
 # algorithmic bytes of one round (each input byte counted once)
 # ---------------------------------------------------------------------------
-def round_bytes(w, ell_sum, n_reject):
+def t_rows(form, B, G, ell_sum, n_acc, n_full):
+    """Target rows one round reads once (a rejecting request's row k* - 1 is
+    counted here; the residual's second read of it is in round_bytes):
+    chain -- rows 0..n_r of every request, n_r + 1 each (the row of the
+    rejected position, or the bonus row after a whole accept); early -- every
+    row j < gamma, and the bonus rows; all -- every row j < l_r, and the bonus
+    rows."""
+    if form == "chain":
+        return n_acc + B
+    if form == "early":
+        return B * G + n_full
+    return ell_sum + n_full
+
+
+def round_bytes(w, rows, n_reject):
+    """Algorithmic bytes of one round that reads `rows` target rows once and
+    has n_reject rejecting requests (each re-reads its U and T rows at k*)."""
     sw = 2 if w.wdtype == torch.bfloat16 else 4
     B, G, V, r, H = w.B, w.gamma, w.V, w.r, w.H
     return (4 * B * G * V                 # U
-            + 4 * V * (ell_sum + B)       # target rows actually needed
+            + 4 * V * rows                # target rows read once
             + sw * r * V                  # W2 once
             + sw * B * G * r              # W1 gathers
             + sw * B * G * H              # h
@@ -112,20 +144,21 @@ def stage_bytes_per_launch(w, early=True):
     return b + (4 * w.B * w.gamma * w.V if early else 0)
 
 
-def kernels_per_round(w, early=False):
+def kernels_per_round(w, form="chain"):
     """Launches of this library's kernels in one round (cudaMemsetAsync not
     counted).  First stage: on the tensor-core path (bf16, r = 256,
     V >= 192) one persistent kernel, which also finishes x, p, lse and the
     confidences after a last grid barrier and runs the schedule in its last
     CTA; else a CUDA-core step and finalize per position (with early
     statistics a prep and a row-statistics kernel follow), the confidence
-    and the schedule kernels.  Verify: prep and row statistics (not with
-    early statistics), decide, bonus race, residual (the draft kernel in
-    residual mode, whose last CTA and the bonus race's write the tokens; or
-    its CUDA-core form and then the residual finalize)."""
+    and the schedule kernels.  Verify: the accept tests (verify_chain; or
+    verify_decide, after prep and row statistics for the full row pass),
+    bonus race, residual (the draft kernel in residual mode, whose last CTA
+    and the bonus race's write the tokens; or its CUDA-core form and then the
+    residual finalize)."""
     tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
-    stage = 1 if tc else 2 * w.gamma + (2 if early else 0) + 2
-    verify = (3 if tc else 4) + (0 if early else 2)
+    stage = 1 if tc else 2 * w.gamma + (2 if form == "early" else 0) + 2
+    verify = (3 if tc else 4) + (2 if form == "all" else 0)
     return stage + verify
 
 
@@ -150,19 +183,26 @@ def draft_source_hash():
     return source_hash(DRAFT_SOURCES)
 
 
+def profile_records(path):
+    """The committed ncu records of a file (one record or a list of them)."""
+    with open(path) as f:
+        recs = json.load(f)
+    return recs if isinstance(recs, list) else [recs]
+
+
 def profile_traffic(path, sources, w, **match):
     """DRAM bytes (read + write) of one launch from a committed ncu record, or
     None if it is missing, for another workload or mode, or stale."""
     try:
-        with open(path) as f:
-            rec = json.load(f)
-        if rec.get("workload") != w.name or rec.get("source_sha256_16") != source_hash(sources):
-            return None
-        if any(rec.get(k) != v for k, v in match.items()):
-            return None
-        return int(rec["dram_bytes_per_launch"])
+        for rec in profile_records(path):
+            if rec.get("workload") != w.name or rec.get("source_sha256_16") != source_hash(sources):
+                continue
+            if any(rec.get(k) != v for k, v in match.items()):
+                continue
+            return int(rec["dram_bytes_per_launch"])
     except Exception:
-        return None
+        pass
+    return None
 
 
 def draft_traffic(w, early=True):
@@ -363,8 +403,10 @@ class RoundTimer:
     verify), on the current stream; events around the first stage give its
     duration inside the same timed rounds."""
 
-    def __init__(self, ds, w, inp, dev, early, sps=None, khist=None, ws=None):
-        self.ds, self.w, self.inp, self.dev, self.early = ds, w, inp, dev, early
+    def __init__(self, ds, w, inp, dev, form, sps=None, khist=None, ws=None):
+        assert form in FORMS, form
+        self.ds, self.w, self.inp, self.dev, self.form = ds, w, inp, dev, form
+        self.early = form == "early"
         self.sps = inp["sps"] if sps is None else sps
         self.khist = khist
         self.ws = ds.workspace(w.B, w.gamma, w.V, dev) if ws is None else ws
@@ -382,12 +424,13 @@ class RoundTimer:
         if d1 is not None:
             d1.record(self.stream)
         n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], o.x, o.p, o.lse, o.ell, w.seed, i,
-                         self.ws, early_stats=self.early, scratch_from_draft=True)
+                         self.ws, early_stats=self.early, scratch_from_draft=True, all_row_stats=self.form == "all")
         return o.ell, n
 
     def run(self, steps, warmup, rnd0=0, barrier=None, soak_s=0.0):
         """Warm-up rounds, an optional untimed soak, then `steps` timed rounds.
-        Returns dict(ms (total), draft_ms (mean per call), ell_sum, n_acc, n_rej)."""
+        Returns dict(ms (total), draft_ms (mean per call), ell_sum, n_acc, n_rej,
+        n_full (requests that accepted every verified position))."""
         for i in range(warmup):
             self.step(rnd0 + i)
         torch.cuda.synchronize()
@@ -419,28 +462,38 @@ class RoundTimer:
         return dict(ms=e0.elapsed_time(e1),
                     draft_ms=float(np.mean([dstart[i].elapsed_time(dend[i]) for i in range(steps)])),
                     ell_sum=sum(int(e.sum()) for e, _ in outs), n_acc=sum(int(n.sum()) for _, n in outs),
-                    n_rej=sum(int((n < e).sum()) for e, n in outs), steps=steps)
+                    n_rej=sum(int((n < e).sum()) for e, n in outs), n_full=sum(int((n == e).sum()) for e, n in outs),
+                    steps=steps)
 
 
-def round_record(w, r, hbm, early):
+def round_rows(w, r, form):
+    """Target rows per round that a RoundTimer result's form reads once."""
+    steps = r["steps"]
+    return t_rows(form, w.B, w.gamma, r["ell_sum"] / steps, r["n_acc"] / steps, r["n_full"] / steps)
+
+
+def round_record(w, r, hbm, form):
     """Per-round figures of a RoundTimer result."""
     steps = r["steps"]
     ms = r["ms"] / steps
     per_round = r["ell_sum"] / steps
-    rb = round_bytes(w, per_round, r["n_rej"] / steps)
-    db = stage_bytes_per_launch(w, early)
-    return {"ms": ms, "verified_per_round": per_round, "accepted_per_round": r["n_acc"] / steps,
+    rows = round_rows(w, r, form)
+    rb = round_bytes(w, rows, r["n_rej"] / steps)
+    db = stage_bytes_per_launch(w, form == "early")
+    return {"form": FORMS[form], "ms": ms, "verified_per_round": per_round,
+            "accepted_per_round": r["n_acc"] / steps,
             "verified_tokens_per_s": r["ell_sum"] / (r["ms"] / 1e3),
             "accepted_tokens_per_s": r["n_acc"] / (r["ms"] / 1e3),
+            "target_rows_per_round": rows,
             "round_GB": rb / 1e9, "round_hbm_frac": rb / (ms / 1e3) / 1e9 / hbm,
             "draft_ms": r["draft_ms"], "draft_GB": db / 1e9,
-            "draft_hbm_frac": db / (r["draft_ms"] / 1e3) / 1e9 / hbm, "early_target_stats": early}
+            "draft_hbm_frac": db / (r["draft_ms"] / 1e3) / 1e9 / hbm, "early_target_stats": form == "early"}
 
 
 def gated_round_ms(ds, w, inp, dev, steps):
     """Rounds with the gated recurrent head instead of the Markov head: its
-    draft (target-row statistics taken along), the confidences, the schedule
-    and verification of the gated draft, K rounds timed with CUDA events."""
+    draft, the confidences, the schedule and verification of the gated draft
+    (along the accept chains), K rounds timed with CUDA events."""
     from speculative_decoding_02_gb300 import workloads as wl
     gates = wl.make_gates(w, dev)
     khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == 2 else None
@@ -451,13 +504,13 @@ def gated_round_ms(ds, w, inp, dev, steps):
         if d0 is not None:
             d0.record(stream)
         x, p, lse = ds.gated_markov_draft(inp["U"], inp["W1"], inp["W2"], gates["gate_g"], gates["gate_c"],
-                                          inp["anchor"], w.seed, i, ws=ws, T_early=inp["T"])
+                                          inp["anchor"], w.seed, i, ws=ws)
         if d1 is not None:
             d1.record(stream)
         c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
         ell, _, _ = ds.schedule(c, inp["sps"], w.mode, i, khist, ws)
         n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, i, ws,
-                         early_stats=True, gated=True)
+                         gated=True)
         return ell, n
 
     for i in range(3):
@@ -481,9 +534,10 @@ def gated_round_ms(ds, w, inp, dev, steps):
             "note": "gated recurrent head (gates N(0, 1)); draft, confidence, schedule and verify as separate calls"}
 
 
-def graph_round_ms(ds, w, inp, dev, steps):
-    """One round captured into a CUDA graph with the round index in device
-    memory (advanced by the round's last kernel), replayed `steps` times."""
+def graph_round_ms(ds, w, inp, dev, steps, form):
+    """One round of the given form captured into a CUDA graph with the round
+    index in device memory (advanced by the round's last kernel), replayed
+    `steps` times."""
     khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == 2 else None
     out = ds.RoundOutputs(w.B, w.gamma, dev)
     n = ds.workspace_size(w.B, w.gamma, w.V)
@@ -493,8 +547,8 @@ def graph_round_ms(ds, w, inp, dev, steps):
 
     def call():
         ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed, rnd=0,
-                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, early_stats=True, round_dev=round_dev,
-                 advance_round=True)
+                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, early_stats=form == "early",
+                 all_row_stats=form == "all", round_dev=round_dev, advance_round=True)
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
@@ -524,18 +578,18 @@ def graph_round_ms(ds, w, inp, dev, steps):
 
 
 def other_workload(ds, wl, name, dev, steps, warmup, hbm):
-    """Early-statistics and classic rounds of another workload (serving512:
-    100 consecutive rounds with the top-K schedule taking K from two rounds
-    earlier); the inputs are freed afterwards."""
+    """Rounds of every form of another workload (serving512: 100 consecutive
+    rounds with the top-K schedule taking K from two rounds earlier); the
+    inputs are freed afterwards."""
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w, 0, dev)
     rec = {"B": w.B, "gamma": w.gamma, "V": w.V}
-    for early in (True, False):
+    for form in FORMS:
         khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == wl.MODE_TOPK else None
-        rt = RoundTimer(ds, w, inp, dev, early, khist=khist)
+        rt = RoundTimer(ds, w, inp, dev, form, khist=khist)
         k = 100 if name == "serving512" else steps
         r = rt.run(k, warmup)
-        rec["early" if early else "classic"] = round_record(w, r, hbm, early)
+        rec[form] = round_record(w, r, hbm, form)
     if name == "serving512":
         rec["note"] = "100 consecutive timed rounds; top-K with K from two rounds earlier; inputs fixed, the " \
                       "round index advancing"
@@ -567,45 +621,49 @@ def run_gpu(args):
     w = wl.WORKLOADS[args.workload]
     inp = wl.make_inputs(w, 0, dev)
     khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == wl.MODE_TOPK else None
-    early = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
+    tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
+    form = args.form
+    early = form == "early"
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    # the headline: rounds with the target-row statistics taken by the draft
-    timer = RoundTimer(ds, w, inp, dev, early, khist=khist)
+    # the headline: rounds of the chosen form (default: verification along
+    # the accept chains)
+    timer = RoundTimer(ds, w, inp, dev, form, khist=khist)
     with Clocks(local) as clk:
         r = timer.run(args.steps, args.warmup, barrier=barrier, soak_s=args.soak)
     ms = slowest_rank_ms(r["ms"], dev)
     ell_sum, n_acc, n_rej = r["ell_sum"], r["n_acc"], r["n_rej"]
     per_round = ell_sum / args.steps
+    rows = round_rows(w, r, form)
     value = job_units(ell_sum, dev) / (ms / 1e3)
 
     # dominant kernel: the round's first stage (one persistent launch: the
-    # Markov draft with the target-row statistics when early, the confidences
-    # and the schedule), timed inside the timed region
+    # Markov draft, with the target-row statistics in the early form, the
+    # confidences and the schedule), timed inside the timed region
     draft_ms = r["draft_ms"]
     dbytes = stage_bytes_per_launch(w, early)
     achieved = dbytes / (draft_ms / 1e3) / 1e9
 
     extra = {}
     if rank == 0:
-        # the same workload with verification streaming the target rows itself
-        extra["classic_round"] = round_record(w, RoundTimer(ds, w, inp, dev, False, khist=khist).run(
-            args.steps, 3, rnd0=1000), hbm, False)
+        # the same workload in the other forms (same round indices)
+        extra["other_forms"] = {f: round_record(w, RoundTimer(ds, w, inp, dev, f, khist=khist).run(
+            args.steps, 3), hbm, f) for f in FORMS if f != form and (tc or f != "early")}
         # a falling steps-per-second curve, so that the greedy truncates (the
         # scheduler's sorting path; only the verified rows are read)
         if w.mode == wl.MODE_GREEDY:
             b = torch.arange(inp["sps"].numel(), dtype=torch.float64, device=dev)
             sps_fall = (1.0 / (1.0 + b / 256.0)).float()
-            rt = RoundTimer(ds, w, inp, dev, False, sps=sps_fall)
-            rec = round_record(w, rt.run(args.steps, 3, rnd0=2000), hbm, False)
+            rt = RoundTimer(ds, w, inp, dev, form, sps=sps_fall)
+            rec = round_record(w, rt.run(args.steps, 3, rnd0=2000), hbm, form)
             rec["sps"] = "1 / (1 + B / 256)"
             extra["truncating_schedule"] = rec
-        if early:
-            extra["graph_replay"] = graph_round_ms(ds, w, inp, dev, args.steps)
+        if tc:
+            extra["graph_replay"] = graph_round_ms(ds, w, inp, dev, args.steps, form)
             extra["gated_head"] = gated_round_ms(ds, w, inp, dev, args.steps)
 
     # the acceptance labels of one round's verified positions (a widening of
@@ -613,7 +671,7 @@ def run_gpu(args):
     # target rows' statistics are the ones the round's draft took along
     label = None
     ws = timer.ws
-    if rank == 0 and early:
+    if rank == 0 and tc:
         x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 7, ws=ws,
                                     T_early=inp["T"])
         c = ds.confidence(inp["h"], inp["W1"], inp["w"], inp["anchor"], x)
@@ -675,7 +733,7 @@ def run_gpu(args):
     # end to end through host buffers: per-round inputs copied in, results out
     e2e = None
     if rank == 0 and not args.no_e2e:
-        e2e = run_e2e(w, inp, ds, dev, args, khist, early)
+        e2e = run_e2e(w, inp, ds, dev, args, khist, form)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -695,7 +753,7 @@ def run_gpu(args):
                               for n in ("qwen3_4b", "large_vocab", "serving512")}
 
     if rank == 0:
-        rbytes = round_bytes(w, per_round, n_rej / args.steps)
+        rbytes = round_bytes(w, rows, n_rej / args.steps)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -703,8 +761,9 @@ def run_gpu(args):
             "config": {"workload": w.name, "B": w.B, "gamma": w.gamma, "V": w.V, "r": w.r, "H": w.H,
                        "weights": "bf16" if w.wdtype == torch.bfloat16 else "f32",
                        "l2": "inputs larger than L2 (U+T %.2f GB)" % ((4 * w.B * (2 * w.gamma + 1) * w.V) / 1e9),
-                       "early_target_stats": early,
+                       "form": FORMS[form], "early_target_stats": early,
                        "verified_per_round": per_round, "accepted_per_round": n_acc / args.steps,
+                       "target_rows_per_round": rows,
                        "round_GB": rbytes / 1e9,
                        "round_hbm_frac": rbytes / (ms / args.steps / 1e3) / 1e9 / hbm,
                        "parallelism": f"replicas x{world}"},
@@ -721,7 +780,7 @@ def run_gpu(args):
             "acceptance_label": label,
             "sts_fit": sts_fit,
             "e2e": e2e,
-            "gpu_launches": args.steps * kernels_per_round(w, early),
+            "gpu_launches": args.steps * kernels_per_round(w, form),
             "cpu_baseline": cpu,
         }
         line.update(extra)
@@ -730,7 +789,7 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_e2e(w, inp, ds, dev, args, khist, early):
+def run_e2e(w, inp, ds, dev, args, khist, form):
     """Rounds through the public API with the per-round inputs in pinned host
     memory: H2D of U, T, h, anchor and D2H of tokens, counts and lengths are
     inside the timed region.  The inputs are double-buffered on the device and
@@ -762,7 +821,8 @@ def run_e2e(w, inp, ds, dev, args, khist, early):
         stream.wait_event(uploaded[slot])
         b = devb[slot]
         ds.round(b["U"], b["T"], inp["W1"], inp["W2"], b["h"], inp["w"], b["anchor"], seed=w.seed, rnd=i,
-                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, early_stats=early)
+                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, early_stats=form == "early",
+                 all_row_stats=form == "all")
         consumed[slot].record(stream)
         for k in outs:
             hosto[k].copy_(getattr(out, k), non_blocking=True)
@@ -852,9 +912,9 @@ def run_profile_label(args):
 
 
 def run_profile_round(args):
-    """A few whole rounds of the workload through the entry points (early
-    statistics where the tensor-core path runs): two warm-up rounds, then
-    args.steps rounds, for ncu launch lists and captures of round kernels."""
+    """A few whole rounds of the workload through the entry points (the form
+    of --form): two warm-up rounds, then args.steps rounds, for ncu launch
+    lists and captures of round kernels."""
     import speculative_decoding_02_gb300 as ds
     from speculative_decoding_02_gb300 import build as lib_build
     from speculative_decoding_02_gb300 import workloads as wl
@@ -863,10 +923,9 @@ def run_profile_round(args):
     w = wl.WORKLOADS[args.workload]
     inp = wl.make_inputs(w, 0, dev)
     khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == wl.MODE_TOPK else None
-    early = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192 and not args.plain_draft
-    r = RoundTimer(ds, w, inp, dev, early, khist=khist).run(args.steps, 2)
-    print(json.dumps({"profile_round": w.name, "early_target_stats": early, "steps": args.steps,
-                      "ms_per_round": r["ms"] / args.steps, "kernels_per_round": kernels_per_round(w, early)}))
+    r = RoundTimer(ds, w, inp, dev, args.form, khist=khist).run(args.steps, 2)
+    print(json.dumps({"profile_round": w.name, "form": args.form, "steps": args.steps,
+                      "ms_per_round": r["ms"] / args.steps, "kernels_per_round": kernels_per_round(w, args.form)}))
 
 
 def main():

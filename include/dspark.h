@@ -77,6 +77,7 @@ extern "C" {
 #define DSPARK_TARGET_STATS_FROM_VERIFY 4u  /* dspark_acceptance_label_ex: a verification left them */
 #define DSPARK_SCRATCH_FROM_DRAFT 8u  /* dspark_verify_ex: dspark_draft_schedule cleared the scratch */
 #define DSPARK_GATED_STATES 16u       /* dspark_verify_ex: the draft used the gated recurrent head */
+#define DSPARK_ALL_ROW_STATS 32u      /* verification takes the statistics of every row j < ell */
 
 /* Bytes of device scratch the entry points below need for these sizes; 0 when
  * a size is not positive. */
@@ -181,8 +182,13 @@ int dspark_schedule_ex(const float* c, int B, int gamma, const float* sps, int n
  * k = ell[b]+1).
  * In:  T [B, gamma+1, V] f32 (row k-1 scores position k); U, W1, W2, anchor as
  *      for the draft; x, p_d, lse_d [B, gamma] from the draft; ell [B] i32 in
- *      [0, gamma].  Only rows 0..ell[b] of T are read.
+ *      [0, gamma].
  * Out: n_out [B] i32 accepted count; tok_out [B] i32 corrected or bonus token.
+ * Rows read: the accept tests run along each request's prefix and stop at its
+ * first rejection, so row k-1 is read only once positions 1..k-1 were
+ * accepted (every row 0), plus row ell[b] of a request that accepted all of
+ * its positions (the bonus draw).  The result is the same as reading every
+ * row j < ell[b]; DSPARK_ALL_ROW_STATS (dspark_verify_ex) reads them all.
  */
 int dspark_verify(const float* T, const float* U, const void* W1, const void* W2,
                   int wdtype, const int32_t* anchor, const int32_t* x,
@@ -210,6 +216,11 @@ int dspark_verify(const float* T, const float* U, const void* W1, const void* W2
  *    bonus list; the tensor-core path does, others ignore the flag), so the
  *    call skips its memset and its kernels run as one chain of dependent
  *    launches.
+ *  - DSPARK_ALL_ROW_STATS: take the softmax statistics of every row j < ell[b]
+ *    before the accept tests, as dspark_acceptance_label_ex with
+ *    DSPARK_TARGET_STATS_FROM_VERIFY needs them; without it (and without
+ *    DSPARK_EARLY_TARGET_STATS) only the rows the accept tests reach are
+ *    read.  Together with DSPARK_EARLY_TARGET_STATS: DSPARK_ERR_INVALID.
  * Other flag bits return DSPARK_ERR_INVALID.
  */
 int dspark_verify_ex(const float* T, const float* U, const void* W1, const void* W2,
@@ -246,8 +257,10 @@ int dspark_acceptance_label(const float* T, const float* U, const void* W1, cons
  *  - DSPARK_EARLY_TARGET_STATS: left by dspark_markov_draft_ex(T_early = T)
  *    on the same workspace (rows j < gamma), with or without the verification
  *    that used them;
- *  - DSPARK_TARGET_STATS_FROM_VERIFY: left by a dspark_verify(_ex) without
- *    that flag on the same workspace and T (rows j < ell[b]);
+ *  - DSPARK_TARGET_STATS_FROM_VERIFY: left by a dspark_verify_ex with
+ *    DSPARK_ALL_ROW_STATS on the same workspace and T (rows j < ell[b]), with
+ *    no draft on the workspace since; otherwise the kernel records
+ *    DSPARK_ERR_INVALID;
  * either earlier in stream order.  Both flags at once, or other bits, return
  * DSPARK_ERR_INVALID.
  */
@@ -346,7 +359,8 @@ int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
  * dspark_round with the options of the _ex calls: with
  * DSPARK_EARLY_TARGET_STATS the draft takes the statistics of T's rows
  * j < gamma while it runs (T is an input of the round) and verification
- * skips its own pass over them; with round_dev the round index is the device
+ * skips its own pass over them; with DSPARK_ALL_ROW_STATS verification takes
+ * the statistics of every row j < ell[b] (see dspark_verify_ex); with round_dev the round index is the device
  * word *round_dev (`round` ignored), and DSPARK_ADVANCE_ROUND makes the
  * round's last kernel add 1 to it, so that replaying one captured graph runs
  * consecutive rounds (the caller refreshes U, T, h and the anchors in place

@@ -24,6 +24,7 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NONF
 F32, BF16 = 0, 1
 SCHED_FIXED, SCHED_GREEDY, SCHED_TOPK = 0, 1, 2
 EARLY_TARGET_STATS, ADVANCE_ROUND, TARGET_STATS_FROM_VERIFY, SCRATCH_FROM_DRAFT, GATED_STATES = 1, 2, 4, 8, 16
+ALL_ROW_STATS = 32
 
 
 class DSparkError(RuntimeError):
@@ -272,14 +273,16 @@ def schedule(c, sps=None, mode=SCHED_GREEDY, rnd=0, khist=None, ws=None, round_d
 
 
 def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None, early_stats=False, round_dev=None,
-           advance_round=False, scratch_from_draft=False, gated=False):
+           advance_round=False, scratch_from_draft=False, gated=False, all_row_stats=False):
     """n [B] i32 accepted counts, tok [B] i32 corrected / bonus tokens.
     early_stats: ws already holds the target-row statistics from
     markov_draft(T_early=T).  round_dev / advance_round: the round index as a
     device int64 [1], advanced by the call's last kernel.
     scratch_from_draft: a draft_schedule on ws cleared the call's scratch.
     gated: the draft was gated_markov_draft on ws (its states are the
-    residual's bias operand)."""
+    residual's bias operand).  all_row_stats: take the statistics of every
+    row j < ell (for acceptance_label(stats="verify")) instead of only the
+    rows the accept tests reach."""
     L = _load()
     _need(T, "T", torch.float32)
     dev = T.device
@@ -300,7 +303,8 @@ def verify(T, U, W1, W2, anchor, x, p_d, lse_d, ell, seed, rnd=0, ws=None, early
     ws = workspace(B, G, V, dev) if ws is None else ws
     rd = _round_dev(round_dev, dev)
     flags = ((EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0) |
-             (SCRATCH_FROM_DRAFT if scratch_from_draft else 0) | (GATED_STATES if gated else 0))
+             (SCRATCH_FROM_DRAFT if scratch_from_draft else 0) | (GATED_STATES if gated else 0) |
+             (ALL_ROW_STATS if all_row_stats else 0))
     _check(L.dspark_verify_ex(_ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(anchor), _ptr(x),
                               _ptr(p_d), _ptr(lse_d), _ptr(ell), B, G, V, r, seed, rnd, rd, flags, _ptr(n), _ptr(tok),
                               _ptr(ws), ws.numel(), _stream(dev)), "verify")
@@ -312,7 +316,7 @@ def acceptance_label(T, U, W1, W2, anchor, x, lse_d, ell, ws=None, stats=None):
     k <= ell[b] (0 elsewhere).  Tensor-core path only (bf16, r = 256).
     stats: None (the call streams the target rows' statistics first),
     "early" (ws holds them from markov_draft(T_early=T)) or "verify" (ws
-    holds them from a verify without early_stats)."""
+    holds them from a verify or round with all_row_stats=True)."""
     L = _load()
     _need(T, "T", torch.float32)
     dev = T.device
@@ -433,9 +437,11 @@ def draft_schedule(U, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GR
 
 
 def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
-          out=None, ws=None, early_stats=False, round_dev=None, advance_round=False):
+          out=None, ws=None, early_stats=False, round_dev=None, advance_round=False, all_row_stats=False):
     """One whole round (draft, confidence, schedule, verify) on U's device.
     early_stats: the draft takes the target rows' statistics while it runs.
+    all_row_stats: verification takes the statistics of every row j < ell
+    (otherwise only the rows the accept tests reach).
     round_dev / advance_round: the round index as a device int64 [1] (rnd
     ignored), advanced by the round's last kernel.
     Returns a RoundOutputs (device tensors)."""
@@ -447,7 +453,8 @@ def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, 
     ws = workspace(B, G, V, dev) if ws is None else ws
     n_sps = 0 if sps is None else sps.numel()
     rd = _round_dev(round_dev, dev)
-    flags = (EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0)
+    flags = ((EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0) |
+             (ALL_ROW_STATS if all_row_stats else 0))
     _check(L.dspark_round_ex(_ptr(U), _ptr(T), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h), _dt(h, "h"), _ptr(w),
                              _ptr(sts_T), _ptr(anchor), B, G, V, r, H, _ptr(sps), n_sps, mode, _ptr(khist), seed,
                              rnd, rd, flags, _ptr(out.x), _ptr(out.p), _ptr(out.lse), _ptr(out.c), _ptr(out.ell),

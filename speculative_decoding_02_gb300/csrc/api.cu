@@ -158,8 +158,9 @@ int dspark_verify_ex(const float* T, const float* U, const void* W1, const void*
                            workspace, workspace_bytes));
   if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
   if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND | DSPARK_SCRATCH_FROM_DRAFT |
-                          DSPARK_GATED_STATES))
+                          DSPARK_GATED_STATES | DSPARK_ALL_ROW_STATS))
     return DSPARK_ERR_INVALID;
+  if ((flags & DSPARK_EARLY_TARGET_STATS) && (flags & DSPARK_ALL_ROW_STATS)) return DSPARK_ERR_INVALID;
   if ((flags & DSPARK_GATED_STATES) && !draft_tc_supported(wdtype, r, V)) return DSPARK_ERR_UNSUPPORTED;
   if ((flags & DSPARK_ADVANCE_ROUND) && !round_dev) return DSPARK_ERR_INVALID;
   unsigned long long* rd = reinterpret_cast<unsigned long long*>(round_dev);
@@ -167,7 +168,8 @@ int dspark_verify_ex(const float* T, const float* U, const void* W1, const void*
   const bool zeroed = (flags & DSPARK_SCRATCH_FROM_DRAFT) && draft_tc_supported(wdtype, r, V);
   VerifyArgs a{T, U, W1, W2, wdtype, anchor, x, p_d, lse_d, ell, B, gamma, V, r, make_rng_key(seed, round, rd),
                n_out, tok_out, workspace, (flags & DSPARK_EARLY_TARGET_STATS) != 0,
-               (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr, zeroed, (flags & DSPARK_GATED_STATES) != 0};
+               (flags & DSPARK_ADVANCE_ROUND) ? rd : nullptr, zeroed, (flags & DSPARK_GATED_STATES) != 0,
+               (flags & DSPARK_ALL_ROW_STATS) != 0};
   return cuda_status(launch_verify(a, (cudaStream_t)stream));
 }
 
@@ -217,12 +219,12 @@ int dspark_acceptance_label_ex(const float* T, const float* U, const void* W1, c
   if (flags & DSPARK_EARLY_TARGET_STATS) nsegs = stats_num_segs(V);
   else if (!(flags & DSPARK_TARGET_STATS_FROM_VERIFY))
     DSPARK_TRY(cuda_status(launch_row_stats(T, ell, B, gamma, V, workspace, s)));
+  int* counters = ws_ptr<int>(workspace, L.counters);
   return cuda_status(launch_acceptance_label_tc(T, U, W1, W2, anchor, x, lse_d, ell,
                                                 ws_ptr<float2>(workspace, L.row_part), nsegs,
-                                                (flags & DSPARK_EARLY_TARGET_STATS) ? ws_ptr<int>(workspace, L.counters) + 2
-                                                                                    : nullptr,
-                                                label_out, B, gamma,
-                                                V, ws_ptr<int>(workspace, L.status), s));
+                                                (flags & DSPARK_EARLY_TARGET_STATS) ? counters + 2 : nullptr,
+                                                (flags & DSPARK_TARGET_STATS_FROM_VERIFY) ? counters + 4 : nullptr,
+                                                label_out, B, gamma, V, ws_ptr<int>(workspace, L.status), s));
 }
 
 int dspark_acceptance_label(const float* T, const float* U, const void* W1, const void* W2, int wdtype,
@@ -274,7 +276,9 @@ int dspark_round_ex(const float* U, const float* T, const void* W1, const void* 
                     int32_t* n_out, int32_t* tok_out, void* workspace, size_t workspace_bytes, void* stream) {
   DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, n_out,
                            tok_out, workspace, workspace_bytes));
-  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND)) return DSPARK_ERR_INVALID;
+  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND | DSPARK_ALL_ROW_STATS))
+    return DSPARK_ERR_INVALID;
+  if ((flags & DSPARK_EARLY_TARGET_STATS) && (flags & DSPARK_ALL_ROW_STATS)) return DSPARK_ERR_INVALID;
   if ((flags & DSPARK_ADVANCE_ROUND) && !round_dev) return DSPARK_ERR_INVALID;
   const bool early = (flags & DSPARK_EARLY_TARGET_STATS) != 0;
   DSPARK_TRY(dspark_draft_schedule(U, early ? T : nullptr, W1, W2, wdtype, h, hdtype, w, sts_T, anchor, B, gamma, V,

@@ -246,6 +246,7 @@ __host__ __device__ inline int draft_part_slices(int V) {
   return draft_num_slices(V) > kMaxDraftCtas ? draft_num_slices(V) : kMaxDraftCtas;
 }
 __host__ __device__ inline int verify_num_segs(int V) { return div_up(V, kVerifySeg); }
+
 // The statistics a draft takes along (one warp per task) use shorter segments,
 // so that the last tasks finish soon after the draft; the partial buffer is
 // sized for the larger count.
@@ -259,7 +260,9 @@ constexpr int kKeyStride = 16;   // u64 slots per key
 struct WsLayout {
   size_t status;      // int32 status word
   size_t counters;    // int32 [8]: [0] verify row count, [1] draft grid barrier, [2] target-row
-                      // statistics: tasks taken (>= B*gamma*nsegs once rows j < gamma are done)
+                      // statistics: tasks taken (>= B*gamma*nsegs once rows j < gamma are done),
+                      // [3] draft CTAs past the finalize, [4] 1 while the row partials hold
+                      // verification's statistics of every row j < ell (cleared by every draft)
   size_t draft_keys;  // u64 [gamma][B], kKeyStride apart
   size_t draft_part;  // float2 [gamma][B][nslices]
   size_t rows;        // int32 [B*gamma] row ids b*(gamma+1)+j (j < ell_b) of the rows whose stats verify needs
@@ -274,6 +277,7 @@ struct WsLayout {
   size_t gstate;      // bf16 [B][gamma][256] the gated head's states s_k (tensor-core path)
   size_t bonus_rows;  // int32 [1 + B]: count, then the requests that accepted their whole prefix
   size_t fin_count;   // u32 [2]: CTAs of the bonus race and of the residual that are done
+  size_t chain_next;  // u32: requests verify_chain's clusters have taken
   size_t total;
 };
 
@@ -294,6 +298,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   L.resid_key = off;   off = align256(off + 8ull * kKeyStride * B);
   L.bonus_rows = off;  off = align256(off + 4ull * (B + 1));
   L.fin_count = off;   off = align256(off + 8);
+  L.chain_next = off;  off = align256(off + 4);
   // then what verification writes before it reads, and what a draft leaves
   L.resid_k = off;     off = align256(off + 4ull * B);
   L.resid_lse = off;   off = align256(off + 4ull * B);

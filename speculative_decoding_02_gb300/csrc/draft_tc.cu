@@ -1481,9 +1481,9 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * kKeyStride * (size_t)a.gamma * a.B, stream);
   if (e != cudaSuccess) return e;
-  // the grid-barrier counter, the target-statistics task counter and the
-  // count of CTAs past the finalize after it
-  if ((e = cudaMemsetAsync(gbar, 0, 3 * sizeof(unsigned int), stream)) != cudaSuccess) return e;
+  // the grid-barrier counter, the target-statistics task counter, the count
+  // of CTAs past the finalize and the marker of verification's full row pass
+  if ((e = cudaMemsetAsync(gbar, 0, 4 * sizeof(unsigned int), stream)) != cudaSuccess) return e;
 
   const int mtiles = div_up(a.B, R);
   const int ntiles = div_up(a.V, BN);

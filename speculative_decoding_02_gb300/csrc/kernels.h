@@ -101,6 +101,10 @@ struct VerifyArgs {
   // the draft used the gated recurrent head: its states in the workspace are
   // the residual's bias operand (tensor-core path)
   bool gated_states;
+  // without stats_ready: take the statistics of every row j < ell (the classic
+  // pass, reusable by the acceptance labels) instead of only the rows each
+  // request's accept chain reaches
+  bool all_row_stats;
 };
 
 // Host-side argument checks shared by every entry point that takes these
@@ -161,7 +165,8 @@ cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, c
 cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const void* W1, const void* W2,
                                        const int32_t* anchor, const int32_t* x, const float* lse_d,
                                        const int32_t* ell, const float2* row_part, int nsegs,
-                                       const int* stats_done, float* label, int B, int G, int V, int* status,
+                                       const int* stats_done, const int* full_rows, float* label, int B, int G,
+                                       int V, int* status,
                                        cudaStream_t stream);
 
 // The softmax partials of the target rows j < ell_b of every request into the

@@ -80,6 +80,7 @@ struct LabelParams {
   const float2* row_part;    // [B*(G+1)][nsegs] target-row partials
   int nsegs;
   const int* stats_done;     // row segments a draft took (nullptr: not checked)
+  const int* full_rows;      // 1 while verification's statistics cover every row j < ell (nullptr: not checked)
   float* label;              // [B][G], zeroed by the caller
   int* status;
   int B, G, V;
@@ -140,6 +141,8 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
     fence_mbar_init();
   }
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.stats_done && *p.stats_done < p.B * p.G * p.nsegs)
+    record_status(p.status, DSPARK_ERR_INVALID);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.full_rows && *p.full_rows != 1)
     record_status(p.status, DSPARK_ERR_INVALID);
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&w2_map);
@@ -326,12 +329,14 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
 // The acceptance label of every verified position in one persistent launch
 // (label zeroed by the caller; row_part holds the target rows' partials, nsegs
 // per row; stats_done, when given, is the draft's count of row segments taken,
-// and a short count is reported as DSPARK_ERR_INVALID).
+// and a short count is reported as DSPARK_ERR_INVALID; full_rows, when given,
+// is the marker of verification's pass over every row j < ell, and a marker
+// other than 1 is reported the same way).
 cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const void* W1, const void* W2,
                                        const int32_t* anchor, const int32_t* x, const float* lse_d,
                                        const int32_t* ell, const float2* row_part, int nsegs,
-                                       const int* stats_done, float* label, int B, int G, int V, int* status,
-                                       cudaStream_t stream) {
+                                       const int* stats_done, const int* full_rows, float* label, int B, int G,
+                                       int V, int* status, cudaStream_t stream) {
   CUtensorMap wmap, umap, tmap;
   cudaError_t e = make_w2_tensor_map(W2, V, &wmap);
   if (e != cudaSuccess) return e;
@@ -357,6 +362,7 @@ cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const voi
   lp.row_part = row_part;
   lp.nsegs = nsegs;
   lp.stats_done = stats_done;
+  lp.full_rows = full_rows;
   lp.label = label;
   lp.status = status;
   lp.B = B; lp.G = G; lp.V = V;

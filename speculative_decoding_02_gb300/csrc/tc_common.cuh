@@ -90,6 +90,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// A wait with no shared abort flag: gives up after kWaitLimitNs, records a
+// timeout and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait_sleep(bar, parity, 1000)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      record_status(status, DSPARK_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
 // Like mbar_wait but ignores `abort`: used to drain work already issued.
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();

@@ -25,11 +25,20 @@
 //                      the residual was empty in floating point, a draw from
 //                      p_t itself.
 // Steps 1-2 are skipped when the draft already took the statistics of every
-// row j < gamma (the caller held T when the draft started).
+// row j < gamma (the caller held T when the draft started).  Otherwise, unless
+// the caller asks for the statistics of every row j < ell (to reuse them for
+// the acceptance labels), steps 1-3 are one kernel, verify_chain, that reads
+// only the rows the accept tests reach: row j of a request once its positions
+// 1..j were accepted.
 #include <algorithm>
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "kernels.h"
+#include "tc_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dspark {
 namespace {
@@ -86,6 +95,7 @@ verify_prep(const int32_t* __restrict__ ell, int B, int G, int nsegs, int32_t* _
   if (tid == 1023) {
     counters[0] = pos;
     if (!ell) counters[2] = B * G * nsegs;
+    else counters[4] = 1;   // the row pass that follows takes every row j < ell
   }
 }
 
@@ -393,6 +403,236 @@ __global__ void verify_decide(const float* __restrict__ T, const int32_t* __rest
   }
 }
 
+// ---------------------------------------------------------------------------
+// Verification along each request's accept chain.  The accept test of
+// position k needs the softmax normaliser of target row k - 1, and once a
+// position is rejected no later row can change the round's result.  So the
+// rows are read in the order of the chains: row j of request b only once
+// positions 1..j of b were accepted.  At the engine point about 2.9 of 16
+// positions are accepted, so about 4 of the 16 rows a request submits are
+// read.
+//
+// A cluster of kChainCluster CTAs owns one request at a time.  Each CTA copies
+// its eighth of row j into shared memory (1-D bulk copies, two stages of
+// kChainChunk floats), folds it into a (max, sum of exp) partial and leaves it
+// in its shared memory; after a cluster barrier every CTA reads the eight
+// partials (distributed shared memory) and reduces them by the same tree, so
+// all of them take the same decision and go on to row j + 1 or to the next
+// request together.  Requests come from a counter, one atomic per request,
+// taken by rank 0 when the cluster is free: a cluster busy with a long chain
+// holds no other request, and one that starts late (not resident at first)
+// takes only what is left.  Nothing else is shared between clusters.
+// ---------------------------------------------------------------------------
+constexpr int kChainCluster = 8;            // CTAs reading one row together
+constexpr int kChainThreads = 512;
+constexpr int kChainChunk = 12288;          // floats per bulk copy (48 KB)
+constexpr int kChainStages = 2;
+constexpr int kChainSmemBytes = kChainStages * kChainChunk * 4;
+constexpr int kChainVec = kChainChunk / 4 / kChainThreads;   // float4 per thread per chunk
+constexpr int kChainWarps = kChainThreads / 32;
+static_assert(kChainVec * 4 * kChainThreads == kChainChunk, "a chunk is whole float4 per thread");
+
+struct ChainShared {
+  uint64_t full[kChainStages];   // bulk copy of a chunk landed
+  float2 part[2];                // this CTA's partial of the row, by level-barrier parity
+  float2 red[kChainWarps];
+  int req[2];                    // rank 0: the request the cluster takes next, by hand-off parity
+  float tx, pd;                  // T at the drafted token and p_d(x_k), this CTA's loads
+  float lse;
+  int accept;
+  int bnext;
+};
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`
+// (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void chain_copy(float* dst, const float* src, uint32_t bytes, uint64_t* bar) {
+  tc::mbar_arrive_expect_tx(bar, bytes);
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
+
+// (max, sum of exp) reduction over a warp: the maximum first, then each lane
+// rescales its sum once to it, then one sum.  A fixed shuffle tree with the
+// fast base-2 exponential: every CTA of a cluster runs the same sequence on
+// the same values, so all of them get the same bits.
+__device__ __forceinline__ void chain_warp_reduce(float& m, float& s, int width) {
+  float M = m;
+  for (int off = width / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float t = m == -INFINITY ? 0.f : s * exp2_fast((m - M) * kLog2eF);
+  for (int off = width / 2; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  m = M;
+  s = t;
+}
+
+__global__ void __cluster_dims__(kChainCluster, 1, 1) __launch_bounds__(kChainThreads, 2)
+verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const float* __restrict__ p_d,
+             const int32_t* __restrict__ ell, const int32_t* __restrict__ anchor, int B, int G, int V,
+             RngKey key_arg, unsigned int* __restrict__ req_next, int32_t* __restrict__ resid_k,
+             float* __restrict__ resid_lse, int32_t* __restrict__ resid_prev, int32_t* __restrict__ n_out,
+             int32_t* __restrict__ bonus_rows, int* __restrict__ full_stats, int* __restrict__ status) {
+  extern __shared__ __align__(128) float buf[];   // kChainStages x kChainChunk
+  __shared__ ChainShared sh;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kChainStages; ++s) tc::mbar_init(&sh.full[s], 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();   // ell from the schedule, x and p_d from the draft, the request counter cleared
+  const RngKey key = live_key(key_arg);
+  if (blockIdx.x == 0 && tid == 0) *full_stats = 0;   // the row partials no longer cover every row j < ell
+  // this CTA's share of a row: floats [c0, c1), in chunks of kChainChunk
+  const int share = div_up(div_up(V, kChainCluster), 4) * 4;
+  const int c0 = min(V, rank * share), c1 = min(V, c0 + share);
+  const int nch = div_up(c1 - c0, kChainChunk);
+  static_assert(kChainStages == 2, "two copy stages (scalars below)");
+  uint32_t issued0 = 0, issued1 = 0, waited0 = 0, waited1 = 0;   // copies per stage
+  bool dead = false;   // a copy wait gave up: this CTA copies nothing more
+  bool bad = false;
+  uint32_t nb = 0;     // level barriers passed (parity of the partial slots)
+  uint32_t hand = 0;   // hand-offs (parity of the request slots)
+  if (rank == 0 && tid == 0) sh.req[0] = (int)atomicAdd(req_next, 1u);
+  cl.sync();
+  if (tid == 0) sh.bnext = *cl.map_shared_rank(&sh.req[0], 0);
+  __syncthreads();
+  int b = sh.bnext;
+  while (b < B) {
+    const int Lraw = ell[b];
+    const int L = min(max(Lraw, 0), G);
+    if (rank == 0 && tid == 0 && (Lraw < 0 || Lraw > G)) record_status(status, DSPARK_ERR_INVALID);
+    int j = 0;
+    for (;;) {
+      const size_t item = (size_t)b * G + j;
+      const float* row = T + ((size_t)b * (G + 1) + j) * V;
+      float m = -INFINITY, s = 0.f;
+      float u = 0.f;   // the accept uniform (thread 0), drawn while the copies fly
+      if (L > 0) {
+        if (tid == 0) {
+          if (!dead)
+            for (int c = 0; c < min(nch, kChainStages); ++c) {
+              const int a = c0 + c * kChainChunk;
+              chain_copy(buf + c * kChainChunk, row + a, 4u * (uint32_t)(min(c1, a + kChainChunk) - a), &sh.full[c]);
+              if (c) ++issued1; else ++issued0;
+            }
+          // the drafted token's target logit and draft probability, while the copies fly
+          const int xk = checked_token(x[item], V, status);
+          sh.pd = p_d[item];
+          sh.tx = row[xk];
+          u = uniform01(rng4(key, kStreamAccept, (uint32_t)b, (uint32_t)(j + 1), 0u).x);
+        }
+        for (int c = 0; c < nch; ++c) {
+          const int st = c % kChainStages;
+          if (!dead) {
+            if (!tc::mbar_wait_bounded(&sh.full[st], (st ? waited1 : waited0) & 1u, status)) dead = true;
+            if (st) ++waited1; else ++waited0;
+          }
+          const int n4 = (min(c1, c0 + (c + 1) * kChainChunk) - (c0 + c * kChainChunk)) >> 2;
+          const float4* b4 = reinterpret_cast<const float4*>(buf + st * kChainChunk);
+          float4 q[kChainVec];
+#pragma unroll
+          for (int k = 0; k < kChainVec; ++k) {
+            const int i = tid + k * kChainThreads;
+            q[k] = i < n4 ? b4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          }
+          float bm = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < kChainVec; ++k) bm = fmaxf(fmaxf(bm, fmaxf(q[k].x, q[k].y)), fmaxf(q[k].z, q[k].w));
+          bad |= !(bm < INFINITY);
+          if (bm > m) {
+            s = (m == -INFINITY) ? 0.f : s * exp2_fast((m - bm) * kLog2eF);
+            m = bm;
+          }
+          if (m > -INFINITY) {
+            const float mb = m * kLog2eF;
+#pragma unroll
+            for (int k = 0; k < kChainVec; ++k)
+              s += (exp2_fast(fmaf(q[k].x, kLog2eF, -mb)) + exp2_fast(fmaf(q[k].y, kLog2eF, -mb))) +
+                   (exp2_fast(fmaf(q[k].z, kLog2eF, -mb)) + exp2_fast(fmaf(q[k].w, kLog2eF, -mb)));
+          }
+          // every thread is done with this stage before it is refilled
+          dead = __syncthreads_or(dead) != 0;
+          if (tid == 0 && !dead && c + kChainStages < nch) {
+            const int a = c0 + (c + kChainStages) * kChainChunk;
+            chain_copy(buf + st * kChainChunk, row + a, 4u * (uint32_t)(min(c1, a + kChainChunk) - a), &sh.full[st]);
+            if (st) ++issued1; else ++issued0;
+          }
+        }
+        chain_warp_reduce(m, s, 32);
+        if (lane == 0) sh.red[wid] = make_float2(m, s);
+        __syncthreads();
+        if (wid == 0) {
+          float2 pr = lane < kChainWarps ? sh.red[lane] : make_float2(-INFINITY, 0.f);
+          chain_warp_reduce(pr.x, pr.y, kChainWarps);
+          if (lane == 0) sh.part[nb & 1] = pr;
+        }
+      } else if (tid == 0) {
+        sh.part[nb & 1] = make_float2(-INFINITY, 0.f);
+      }
+      cl.sync();
+      // the decision, by each CTA from the cluster's partials (one lane per
+      // rank, the same reduction tree in every CTA)
+      if (wid == 0) {
+        float2 pr = lane < kChainCluster ? *cl.map_shared_rank(&sh.part[nb & 1], lane) : make_float2(-INFINITY, 0.f);
+        chain_warp_reduce(pr.x, pr.y, kChainCluster);
+        if (lane == 0) {
+          int acc = 0;
+          float lse_t = 0.f;
+          if (L > 0) {
+            lse_t = pr.x + logf(pr.y);
+            acc = u < expf(sh.tx - lse_t) / sh.pd;
+          }
+          sh.accept = acc;
+          sh.lse = lse_t;
+        }
+      }
+      ++nb;
+      __syncthreads();
+      const bool acc = sh.accept != 0;
+      if (L > 0 && acc && j + 1 < L) {
+        ++j;
+        continue;
+      }
+      // the chain ends here: rank 0 writes the request's results
+      if (rank == 0 && tid == 0) {
+        if (L > 0 && !acc) {
+          n_out[b] = j;
+          resid_k[b] = j + 1;
+          resid_lse[b] = sh.lse;
+          resid_prev[b] = j == 0 ? anchor[b] : x[item - 1];
+        } else {
+          // every verified position accepted (or none to verify): the bonus race
+          n_out[b] = L;
+          resid_k[b] = 0;
+          const int slot = atomicAdd(bonus_rows, 1);
+          if (slot < B) bonus_rows[1 + slot] = b;
+          else record_status(status, DSPARK_ERR_INVALID);
+        }
+      }
+      break;
+    }
+    // the next request (two hand-off slots: rank 0 rewrites one only after a
+    // cluster barrier that every peer reached after reading it)
+    ++hand;
+    if (rank == 0 && tid == 0) sh.req[hand & 1] = (int)atomicAdd(req_next, 1u);
+    cl.sync();
+    if (tid == 0) sh.bnext = *cl.map_shared_rank(&sh.req[hand & 1], 0);
+    __syncthreads();
+    b = sh.bnext;
+  }
+  if (bad) record_status(status, DSPARK_ERR_NONFINITE);
+  // no CTA leaves while a peer may still read its shared memory, nor while a
+  // copy it issued may still land
+  cl.sync();
+  if (tid == 0) {
+    if (issued0 > waited0) tc::mbar_drain(&sh.full[0], (issued0 - 1u) & 1u);
+    if (issued1 > waited1) tc::mbar_drain(&sh.full[1], (issued1 - 1u) & 1u);
+  }
+}
+
 template <int WDT>
 __global__ void __launch_bounds__(kRowThreads)
 verify_residual_cuda_core(const float* __restrict__ T, const float* __restrict__ U,
@@ -595,7 +835,11 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   if (!a.scratch_zeroed &&
       (e = cudaMemsetAsync(ws_ptr<char>(a.ws, L.bonus_key), 0, L.resid_k - L.bonus_key, stream)) != cudaSuccess)
     return e;
-  if (!a.stats_ready && (e = row_stats(a.T, a.ell, a.B, a.gamma, a.V, a.ws, stream)) != cudaSuccess) return e;
+  // statistics of every row j < ell first (the classic pass), or none: the
+  // chain reads the rows its accept tests reach
+  const bool chain = !a.stats_ready && !a.all_row_stats;
+  if (!a.stats_ready && !chain && (e = row_stats(a.T, a.ell, a.B, a.gamma, a.V, a.ws, stream)) != cudaSuccess)
+    return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -603,11 +847,34 @@ cudaError_t run_verify(const VerifyArgs& a, cudaStream_t stream) {
   const bool tc = draft_tc_supported(a.wdtype, a.r, a.V);
   // the kernels from here on are chained by programmatic dependent launch
   // (each starts while the one before it ends; see pdl_wait)
-  e = launch_pdl(verify_decide, dim3(div_up(a.B * 32, 256)), dim3(256), 0, stream, a.T, a.x, a.p_d, a.ell,
-                 a.anchor, a.B, a.gamma, a.V, nsegs, a.key, (const float2*)row_part,
-                 (const float*)(a.stats_ready && tc ? ws_ptr<float>(a.ws, L.tx) : nullptr), resid_k, resid_lse, resid_prev,
-                 a.n_out, bonus_rows,
-                 (const int*)(a.stats_ready ? ws_ptr<int>(a.ws, L.counters) + 2 : nullptr), status);
+  if (chain) {
+    if ((e = cudaFuncSetAttribute(verify_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmemBytes)) !=
+        cudaSuccess)
+      return e;
+    // as many clusters as can be resident at once, no more than requests
+    int resident = 0;
+    {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(sms * 2);
+      cfg.blockDim = dim3(kChainThreads);
+      cfg.dynamicSmemBytes = kChainSmemBytes;
+      cfg.stream = stream;
+      if (cudaOccupancyMaxActiveClusters(&resident, verify_chain, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        resident = sms * 2 / kChainCluster;
+      }
+    }
+    const int clusters = std::max(1, std::min(a.B, resident));
+    e = launch_pdl(verify_chain, dim3(clusters * kChainCluster), dim3(kChainThreads), kChainSmemBytes, stream, a.T,
+                   a.x, a.p_d, a.ell, a.anchor, a.B, a.gamma, a.V, a.key, ws_ptr<unsigned int>(a.ws, L.chain_next),
+                   resid_k, resid_lse, resid_prev, a.n_out, bonus_rows, ws_ptr<int>(a.ws, L.counters) + 4, status);
+  } else {
+    e = launch_pdl(verify_decide, dim3(div_up(a.B * 32, 256)), dim3(256), 0, stream, a.T, a.x, a.p_d, a.ell,
+                   a.anchor, a.B, a.gamma, a.V, nsegs, a.key, (const float2*)row_part,
+                   (const float*)(a.stats_ready && tc ? ws_ptr<float>(a.ws, L.tx) : nullptr), resid_k, resid_lse,
+                   resid_prev, a.n_out, bonus_rows,
+                   (const int*)(a.stats_ready ? ws_ptr<int>(a.ws, L.counters) + 2 : nullptr), status);
+  }
   if (e != cudaSuccess) return e;
   // the bonus race on the side stream (forked after verify_decide), the
   // residual on this one, joined before the finalize

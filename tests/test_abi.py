@@ -200,6 +200,21 @@ def test_gated_draft_argument_errors(lib):
                                 ws, big, None) == ds.ERR_UNSUPPORTED
 
 
+def test_row_statistics_flags(lib):
+    p = _fake()
+    ws = _fake(0x100000)
+    big = 1 << 30
+    # statistics taken by the draft and a full row pass by verification
+    # exclude one another, in verify_ex and in round_ex; an unknown bit is
+    # refused
+    both = ds.EARLY_TARGET_STATS | ds.ALL_ROW_STATS
+    for flags in (both, 64):
+        assert lib.dspark_verify_ex(p, p, p, p, 1, p, p, p, p, p, 2, 4, 1024, 256, 0, 0, None, flags, p, p, ws, big,
+                                    None) == ds.ERR_INVALID
+        assert lib.dspark_round_ex(p, p, p, p, 1, p, 1, p, None, p, 2, 4, 1024, 256, 64, p, 11, 1, None, 0, 0, None,
+                                   flags, p, p, p, p, p, p, p, p, p, ws, big, None) == ds.ERR_INVALID
+
+
 def test_acceptance_label_and_sts_argument_errors(lib):
     p = _fake()
     ws = _fake(0x100000)

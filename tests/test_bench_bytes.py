@@ -13,24 +13,41 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 from speculative_decoding_02_gb300 import workloads as wl  # noqa: E402
 
-# round totals with ell = gamma and no residual, in MB, as tabulated by hand
-# from U + T rows + W2 + h (+ the small terms)
+# round totals with ell = gamma, every position accepted (gamma verified rows
+# and the bonus row of each request) and no residual, in MB, as tabulated by
+# hand from U + T rows + W2 + h (+ the small terms)
 ROUND_MB = {"qwen3_4b": 722.5, "batch128": 2656.4, "large_vocab": 1279.3, "serving512": 3000.9}
 
 
 @pytest.mark.parametrize("name", sorted(ROUND_MB))
 def test_round_bytes_match_the_tabulated_totals(name):
     w = wl.WORKLOADS[name]
-    assert bench.round_bytes(w, w.B * w.gamma, 0) / 1e6 == pytest.approx(ROUND_MB[name], abs=0.1)
+    assert bench.round_bytes(w, w.B * (w.gamma + 1), 0) / 1e6 == pytest.approx(ROUND_MB[name], abs=0.1)
 
 
 def test_round_bytes_terms():
     w = wl.WORKLOADS["batch128"]
     base = bench.round_bytes(w, 1000, 0)
-    assert bench.round_bytes(w, 1001, 0) - base == 4 * w.V        # one more verified T row
+    assert bench.round_bytes(w, 1001, 0) - base == 4 * w.V        # one more T row
     assert bench.round_bytes(w, 1000, 1) - base == 8 * w.V        # a rejection re-reads a U and a T row
-    # every request reads at least its first T row (bonus or first verified)
-    assert bench.round_bytes(w, 0, 0) >= 4 * w.B * w.gamma * w.V + 4 * w.V * w.B
+
+
+def test_target_rows_per_form():
+    # 3 requests, gamma 4, every l_r = 4: n = (1, 4, 0) accepted, so request 1
+    # accepted everything (its bonus row is read) and 0 and 2 rejected
+    B, G, ell_sum, n_acc, n_full = 3, 4, 12, 5, 1
+    # along the accept chains: rows 0..n_r of each request (2 + 5 + 1)
+    assert bench.t_rows("chain", B, G, ell_sum, n_acc, n_full) == 8
+    # the draft took every row j < gamma; plus the bonus row
+    assert bench.t_rows("early", B, G, ell_sum, n_acc, n_full) == 13
+    # verification's pass over every row j < l_r; plus the bonus row
+    assert bench.t_rows("all", B, G, ell_sum, n_acc, n_full) == 13
+    # a truncating schedule: l = (2, 1, 0), n = (1, 1, 0): the chain reads
+    # rows 0-1, 0-1 (bonus row 1) and 0 (bonus row 0); the pass over j < l_r
+    # reads 3 rows and the two bonus rows; the early draft all 12 and the bonus rows
+    assert bench.t_rows("chain", 3, 4, 3, 2, 2) == 5
+    assert bench.t_rows("all", 3, 4, 3, 2, 2) == 5
+    assert bench.t_rows("early", 3, 4, 3, 2, 2) == 14
 
 
 def test_draft_bytes_match_the_profile():
@@ -46,23 +63,27 @@ def test_draft_bytes_match_the_profile():
     sd = bench.stage_bytes_per_launch(w, early=True)
     assert sd - fd == 2 * 128 * 16 * 2560 + 4 * (2560 + 256) + 4 * 128 * 16 + 4 * 128
     assert bench.stage_bytes_per_launch(w, early=False) == sd - 4 * 128 * 16 * 151936
-    with open(bench.DRAFT_PROFILE) as f:
-        rec = json.load(f)
-    assert rec["workload"] == "batch128"
-    alg = bench.stage_bytes_per_launch(w, rec["early_target_stats"])
-    assert int(rec["algorithmic_bytes_per_launch"]) == alg
-    # the profile's DRAM traffic is within a few per cent of the algorithmic bytes
-    assert 1.0 <= int(rec["dram_bytes_per_launch"]) / alg < 1.05
+    recs = bench.profile_records(bench.DRAFT_PROFILE)
+    assert {r["early_target_stats"] for r in recs} == {True, False}
+    for rec in recs:
+        assert rec["workload"] == "batch128"
+        alg = bench.stage_bytes_per_launch(w, rec["early_target_stats"])
+        assert int(rec["algorithmic_bytes_per_launch"]) == alg
+        # the profile's DRAM traffic is within a few per cent of the algorithmic bytes
+        assert 1.0 <= int(rec["dram_bytes_per_launch"]) / alg < 1.05
 
 
 def test_kernels_per_round():
     # tensor-core path: one persistent launch drafts, computes the confidences
-    # and runs the schedule; verification is decide, bonus race and residual
-    # (their last CTAs write the tokens), after prep and row statistics
-    # unless the draft took the target-row statistics along.  CUDA-core
-    # path: a step and a finalize per position, the confidence and schedule
-    # kernels, and a residual finalize as well
-    assert bench.kernels_per_round(wl.WORKLOADS["batch128"]) == 6
-    assert bench.kernels_per_round(wl.WORKLOADS["batch128"], early=True) == 4
+    # and runs the schedule; verification is the accept tests (verify_chain,
+    # or verify_decide after the draft's statistics, or after prep and row
+    # statistics), bonus race and residual (their last CTAs write the
+    # tokens).  CUDA-core path: a step and a finalize per position, the
+    # confidence and schedule kernels, and a residual finalize as well
+    b = wl.WORKLOADS["batch128"]
+    assert bench.kernels_per_round(b) == 4
+    assert bench.kernels_per_round(b, "early") == 4
+    assert bench.kernels_per_round(b, "all") == 6
     t = wl.WORKLOADS["tiny"]
-    assert bench.kernels_per_round(t) == 2 * t.gamma + 8
+    assert bench.kernels_per_round(t) == 2 * t.gamma + 6
+    assert bench.kernels_per_round(t, "all") == 2 * t.gamma + 8

@@ -44,17 +44,18 @@ def _check(w, inp, out, label, reqs):
     return checked
 
 
-def _round(w, inp, ws=None, early=False):
+def _round(w, inp, ws=None, early=False, all_rows=False):
     return ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed, rnd=0,
-                    sps=inp["sps"], mode=w.mode, ws=ws, early_stats=early)
+                    sps=inp["sps"], mode=w.mode, ws=ws, early_stats=early, all_row_stats=all_rows)
 
 
 def _labels(w, inp, stats):
     # stats None: the label call streams the target rows' statistics itself;
     # "early": the round's draft took them; "verify": the round's verification
-    # did (both on the workspace the label call is given)
+    # did, over every row j < ell (both on the workspace the label call is
+    # given)
     ws = ds.workspace(w.B, w.gamma, w.V, DEV)
-    out = _round(w, inp, ws=ws if stats else None, early=stats == "early")
+    out = _round(w, inp, ws=ws if stats else None, early=stats == "early", all_rows=stats == "verify")
     label = ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], out.x, out.lse, out.ell,
                                 ws=ws, stats=stats)
     torch.cuda.synchronize()
@@ -99,6 +100,19 @@ def test_missing_early_statistics_are_reported():
     out = _round(w, inp, ws=ws, early=False)
     ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], out.x, out.lse, out.ell, ws=ws,
                         stats="early")
+    torch.cuda.synchronize()
+    assert ds.read_status(ws) == ds.ERR_INVALID
+
+
+def test_statistics_of_a_chain_verification_are_refused():
+    # a verification along the accept chains reads only the rows its tests
+    # reach: the label call that would reuse its statistics reports it
+    w = wl.custom(B=8, gamma=3, V=4096, r=256, H=64, wdtype=torch.bfloat16, seed=3, sps_b0=1e6)
+    inp = wl.make_inputs(w, 0, DEV)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    out = _round(w, inp, ws=ws)
+    ds.acceptance_label(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], out.x, out.lse, out.ell, ws=ws,
+                        stats="verify")
     torch.cuda.synchronize()
     assert ds.read_status(ws) == ds.ERR_INVALID
 

@@ -122,6 +122,67 @@ def test_identical_distributions_accept_everything():
     assert torch.equal(n, ell)
 
 
+CHAIN = [
+    # (B, gamma, V, r, dtype): tensor-core and CUDA-core drafts, a ragged last
+    # segment (V % 2048), several lists deep, gamma = 1
+    (40, 5, 5000, 256, torch.bfloat16),
+    (130, 8, 9000, 256, torch.bfloat16),
+    (33, 6, 4104, 64, torch.float32),
+    (9, 1, 2056, 16, torch.float32),
+]
+
+
+@pytest.mark.parametrize("B,G,V,r,dt", CHAIN)
+def test_chain_verification_equals_the_full_row_pass(B, G, V, r, dt):
+    # verification along the accept chains reads only the rows its tests
+    # reach; the full row pass reads every row j < ell first.  The accept
+    # tests, the residual and the bonus draws are the same, and so are the
+    # results (the two passes sum a row's softmax in different segments, so
+    # they agree to float rounding, far inside every decision's margin here)
+    w = wl.custom(B=B, gamma=G, V=V, r=r, H=64, wdtype=dt, mode=wl.MODE_GREEDY, seed=B + 5 * G, u_sigma=2.5,
+                  t_sigma=(0.4, 1.5), sps_b0=float(4 * B), sps_kind="steps", w_sigma=0.05)
+    inp = wl.make_inputs(w, 0, DEV)
+    chain = run_round(inp, w)
+    check_status(w, DEV)
+    full = run_round(inp, w, all_row_stats=True)
+    check_status(w, DEV)
+    for name in ("x", "p", "lse", "c", "ell", "n", "tok"):
+        assert torch.equal(chain.as_dict()[name], full.as_dict()[name]), name
+    n, ell = chain.n.cpu().numpy(), chain.ell.cpu().numpy()
+    assert (n < ell).any() and (n == ell).any()   # rejections and whole accepts
+    full_check(w, inp, chain, chain=False)
+
+
+def test_chain_verification_reads_no_row_past_a_rejection():
+    # every target row past each request's rejected position is set to +inf:
+    # verification along the accept chains never reads one, so it returns the
+    # same results with no error; the full row pass reads them and reports a
+    # non-finite logit
+    w = wl.custom(B=48, gamma=6, V=6000, r=256, H=64, wdtype=torch.bfloat16, mode=wl.MODE_FIXED, seed=29,
+                  u_sigma=2.5, t_sigma=(0.4, 1.5), sps_b0=None)
+    inp = wl.make_inputs(w, 0, DEV)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    x, p, lse = ds.markov_draft(inp["U"], inp["W1"], inp["W2"], inp["anchor"], w.seed, 0, ws=ws)
+    ell = torch.full((w.B,), w.gamma, dtype=torch.int32, device=DEV)
+    args = (inp["U"], inp["W1"], inp["W2"], inp["anchor"], x, p, lse, ell, w.seed, 0, ws)
+    n0, tok0 = ds.verify(inp["T"], *args)
+    torch.cuda.synchronize()
+    assert ds.read_status(ws) == ds.OK
+    n_host = n0.cpu().numpy()
+    assert (n_host < w.gamma - 1).sum() >= w.B // 4   # most requests leave rows unread
+    T = inp["T"].clone()
+    for b in range(w.B):
+        if n_host[b] < w.gamma:
+            T[b, n_host[b] + 1:w.gamma] = float("inf")
+    n1, tok1 = ds.verify(T, *args)
+    torch.cuda.synchronize()
+    assert ds.read_status(ws) == ds.OK
+    assert torch.equal(n0, n1) and torch.equal(tok0, tok1)
+    ds.verify(T, *args, all_row_stats=True)
+    torch.cuda.synchronize()
+    assert ds.read_status(ws) == ds.ERR_NONFINITE
+
+
 def test_bad_anchor_and_nonfinite_logits_set_status():
     w = wl.custom(B=2, gamma=2, V=1024, r=16, H=8, seed=1)
     inp = wl.make_inputs(w, 0, DEV)
