@@ -434,10 +434,14 @@ static_assert(kChainVec * 4 * kChainThreads == kChainChunk, "a chunk is whole fl
 
 struct ChainShared {
   uint64_t full[kChainStages];   // bulk copy of a chunk landed
-  float2 part[2];                // this CTA's partial of the row, by level-barrier parity
+  // this CTA's partial of the row, by level-barrier parity: (max, sum of exp,
+  // T at the drafted token when this CTA's share holds it)
+  float4 part[2];
   float2 red[kChainWarps];
+  float txv;                     // T at the drafted token (the thread holding it)
+  int sx[32];                    // the request's drafted tokens (checked), ...
+  float spd[32], su[32];         // ... their draft probabilities and accept uniforms
   int req[2];                    // rank 0: the request the cluster takes next, by hand-off parity
-  float tx, pd;                  // T at the drafted token and p_d(x_k), this CTA's loads
   float lse;
   int accept;
   int bnext;
@@ -477,6 +481,7 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
   cg::cluster_group cl = cg::this_cluster();
   const int rank = (int)cl.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int ncl = gridDim.x / kChainCluster;
   if (tid == 0) {
     for (int s = 0; s < kChainStages; ++s) tc::mbar_init(&sh.full[s], 1);
     tc::fence_mbar_init();
@@ -500,30 +505,40 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
   if (tid == 0) sh.bnext = *cl.map_shared_rank(&sh.req[0], 0);
   __syncthreads();
   int b = sh.bnext;
+  // issues the first min(nch, kChainStages) chunks of a row (thread 0)
+  auto issue_row = [&](const float* r) {
+    for (int c = 0; c < min(nch, kChainStages); ++c) {
+      const int a = c0 + c * kChainChunk;
+      chain_copy(buf + c * kChainChunk, r + a, 4u * (uint32_t)(min(c1, a + kChainChunk) - a), &sh.full[c]);
+      if (c) ++issued1; else ++issued0;
+    }
+  };
   while (b < B) {
     const int Lraw = ell[b];
     const int L = min(max(Lraw, 0), G);
     if (rank == 0 && tid == 0 && (Lraw < 0 || Lraw > G)) record_status(status, DSPARK_ERR_INVALID);
+    // Near the end of the requests (fewer than one per cluster left to hand
+    // out) HBM has room: the next row's copies start before the decision that
+    // says whether it is needed, and a rejected chain drops one row.
+    const bool tail = b >= B - ncl;
+    bool ahead = false;   // the first chunks of the next level's row are in flight
+    if (L > 0 && tid == 0 && !dead) issue_row(T + (size_t)b * (G + 1) * V);
+    // the drafted tokens, their draft probabilities and the accept uniforms
+    // of every position, one load each while row 0's copies fly
+    if (wid == 0 && lane < L) {
+      const size_t it = (size_t)b * G + lane;
+      sh.sx[lane] = checked_token(x[it], V, status);
+      sh.spd[lane] = p_d[it];
+      sh.su[lane] = uniform01(rng4(key, kStreamAccept, (uint32_t)b, (uint32_t)(lane + 1), 0u).x);
+    }
+    __syncthreads();
     int j = 0;
     for (;;) {
-      const size_t item = (size_t)b * G + j;
       const float* row = T + ((size_t)b * (G + 1) + j) * V;
       float m = -INFINITY, s = 0.f;
-      float u = 0.f;   // the accept uniform (thread 0), drawn while the copies fly
       if (L > 0) {
-        if (tid == 0) {
-          if (!dead)
-            for (int c = 0; c < min(nch, kChainStages); ++c) {
-              const int a = c0 + c * kChainChunk;
-              chain_copy(buf + c * kChainChunk, row + a, 4u * (uint32_t)(min(c1, a + kChainChunk) - a), &sh.full[c]);
-              if (c) ++issued1; else ++issued0;
-            }
-          // the drafted token's target logit and draft probability, while the copies fly
-          const int xk = checked_token(x[item], V, status);
-          sh.pd = p_d[item];
-          sh.tx = row[xk];
-          u = uniform01(rng4(key, kStreamAccept, (uint32_t)b, (uint32_t)(j + 1), 0u).x);
-        }
+        if (j > 0 && tid == 0 && !dead && !ahead) issue_row(row);
+        const int xj = sh.sx[j];
         for (int c = 0; c < nch; ++c) {
           const int st = c % kChainStages;
           if (!dead) {
@@ -537,6 +552,12 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
           for (int k = 0; k < kChainVec; ++k) {
             const int i = tid + k * kChainThreads;
             q[k] = i < n4 ? b4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          }
+          // T at the drafted token, by the thread that holds it
+          const int e = xj - (c0 + c * kChainChunk);
+          if (e >= 0 && e < 4 * n4 && ((e >> 2) % kChainThreads) == tid) {
+            const float4 qe = b4[e >> 2];
+            sh.txv = (e & 3) == 0 ? qe.x : ((e & 3) == 1 ? qe.y : ((e & 3) == 2 ? qe.z : qe.w));
           }
           float bm = -INFINITY;
 #pragma unroll
@@ -561,29 +582,36 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
             if (st) ++issued1; else ++issued0;
           }
         }
+        // the next row's copies, in the tail (the stages are free now)
+        ahead = tail && !dead && j + 1 < L;
+        if (tid == 0 && ahead) issue_row(row + V);
         chain_warp_reduce(m, s, 32);
         if (lane == 0) sh.red[wid] = make_float2(m, s);
         __syncthreads();
         if (wid == 0) {
           float2 pr = lane < kChainWarps ? sh.red[lane] : make_float2(-INFINITY, 0.f);
           chain_warp_reduce(pr.x, pr.y, kChainWarps);
-          if (lane == 0) sh.part[nb & 1] = pr;
+          if (lane == 0) sh.part[nb & 1] = make_float4(pr.x, pr.y, (xj >= c0 && xj < c1) ? sh.txv : 0.f, 0.f);
         }
       } else if (tid == 0) {
-        sh.part[nb & 1] = make_float2(-INFINITY, 0.f);
+        sh.part[nb & 1] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
       }
       cl.sync();
       // the decision, by each CTA from the cluster's partials (one lane per
-      // rank, the same reduction tree in every CTA)
+      // rank, the same reduction tree in every CTA; T at the token from the
+      // rank whose share holds it)
       if (wid == 0) {
-        float2 pr = lane < kChainCluster ? *cl.map_shared_rank(&sh.part[nb & 1], lane) : make_float2(-INFINITY, 0.f);
-        chain_warp_reduce(pr.x, pr.y, kChainCluster);
+        const float4 pr = lane < kChainCluster ? *cl.map_shared_rank(&sh.part[nb & 1], lane)
+                                               : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        float pm = pr.x, ps = pr.y;
+        chain_warp_reduce(pm, ps, kChainCluster);
+        const float t = __shfl_sync(0xffffffffu, pr.z, L > 0 ? min(sh.sx[j] / share, kChainCluster - 1) : 0);
         if (lane == 0) {
           int acc = 0;
           float lse_t = 0.f;
           if (L > 0) {
-            lse_t = pr.x + logf(pr.y);
-            acc = u < expf(sh.tx - lse_t) / sh.pd;
+            lse_t = pm + logf(ps);
+            acc = sh.su[j] < expf(t - lse_t) / sh.spd[j];
           }
           sh.accept = acc;
           sh.lse = lse_t;
@@ -596,13 +624,23 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
         ++j;
         continue;
       }
-      // the chain ends here: rank 0 writes the request's results
+      // the chain ends here.  A row copied ahead is not needed: its copies
+      // land before the stages take the next request's rows.
+      if (ahead) {
+        for (int c = 0; c < min(nch, kChainStages); ++c) {
+          if (!tc::mbar_wait_bounded(&sh.full[c], (c ? waited1 : waited0) & 1u, status)) dead = true;
+          if (c) ++waited1; else ++waited0;
+        }
+        ahead = false;
+        dead = __syncthreads_or(dead) != 0;
+      }
+      // rank 0 writes the request's results
       if (rank == 0 && tid == 0) {
         if (L > 0 && !acc) {
           n_out[b] = j;
           resid_k[b] = j + 1;
           resid_lse[b] = sh.lse;
-          resid_prev[b] = j == 0 ? anchor[b] : x[item - 1];
+          resid_prev[b] = j == 0 ? anchor[b] : sh.sx[j - 1];
         } else {
           // every verified position accepted (or none to verify): the bonus race
           n_out[b] = L;
