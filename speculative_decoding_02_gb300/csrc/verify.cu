@@ -418,32 +418,42 @@ __global__ void verify_decide(const float* __restrict__ T, const int32_t* __rest
 // in its shared memory; after a cluster barrier every CTA reads the eight
 // partials (distributed shared memory) and reduces them by the same tree, so
 // all of them take the same decision and go on to row j + 1 or to the next
-// request together.  Requests come from a counter, one atomic per request,
-// taken by rank 0 when the cluster is free: a cluster busy with a long chain
-// holds no other request, and one that starts late (not resident at first)
-// takes only what is left.  Nothing else is shared between clusters.
+// request together.  T at the drafted token comes with the partial of the CTA
+// whose eighth holds it.  Requests come from a counter, one atomic per
+// request, taken by rank 0 when the cluster is free: a cluster busy with a
+// long chain holds no other request, and one that starts late (not resident
+// at first) takes only what is left.  Once every request has been handed out
+// HBM has room, and a step folds the next kChainTailRows rows of the chain
+// at once, ahead of their decisions (taken in order after one barrier; rows
+// past a rejection are read for nothing): the long chains left at the end
+// then move several positions per barrier.  Nothing else is shared between
+// clusters.
 // ---------------------------------------------------------------------------
 constexpr int kChainCluster = 8;            // CTAs reading one row together
 constexpr int kChainThreads = 512;
 constexpr int kChainChunk = 12288;          // floats per bulk copy (48 KB)
 constexpr int kChainStages = 2;
+constexpr int kChainTailRows = 4;           // rows per step once every request is handed out
 constexpr int kChainSmemBytes = kChainStages * kChainChunk * 4;
 constexpr int kChainVec = kChainChunk / 4 / kChainThreads;   // float4 per thread per chunk
 constexpr int kChainWarps = kChainThreads / 32;
 static_assert(kChainVec * 4 * kChainThreads == kChainChunk, "a chunk is whole float4 per thread");
+static_assert(kChainTailRows <= kChainWarps, "one warp per row decides");
 
 struct ChainShared {
   uint64_t full[kChainStages];   // bulk copy of a chunk landed
-  // this CTA's partial of the row, by level-barrier parity: (max, sum of exp,
-  // T at the drafted token when this CTA's share holds it)
-  float4 part[2];
-  float2 red[kChainWarps];
-  float txv;                     // T at the drafted token (the thread holding it)
+  // this CTA's partial of each row of the step, by step parity: (max, sum of
+  // exp, T at the drafted token when this CTA's share holds it, rank 0: every
+  // request handed out)
+  float4 part[2][kChainTailRows];
+  float2 red[kChainTailRows][kChainWarps];
+  float txv[kChainTailRows];     // T at the drafted token (the thread holding it)
   int sx[32];                    // the request's drafted tokens (checked), ...
   float spd[32], su[32];         // ... their draft probabilities and accept uniforms
   int req[2];                    // rank 0: the request the cluster takes next, by hand-off parity
-  float lse;
-  int accept;
+  float lse[kChainTailRows];
+  int acc[kChainTailRows];
+  int out;                       // every request handed out (rank 0's word at the last barrier)
   int bnext;
 };
 
@@ -481,70 +491,74 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
   cg::cluster_group cl = cg::this_cluster();
   const int rank = (int)cl.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int ncl = gridDim.x / kChainCluster;
   if (tid == 0) {
     for (int s = 0; s < kChainStages; ++s) tc::mbar_init(&sh.full[s], 1);
     tc::fence_mbar_init();
   }
   __syncthreads();
   pdl_wait();   // ell from the schedule, x and p_d from the draft, the request counter cleared
-  const RngKey key = live_key(key_arg);
   if (blockIdx.x == 0 && tid == 0) *full_stats = 0;   // the row partials no longer cover every row j < ell
   // this CTA's share of a row: floats [c0, c1), in chunks of kChainChunk
   const int share = div_up(div_up(V, kChainCluster), 4) * 4;
   const int c0 = min(V, rank * share), c1 = min(V, c0 + share);
   const int nch = div_up(c1 - c0, kChainChunk);
-  static_assert(kChainStages == 2, "two copy stages (scalars below)");
-  uint32_t issued0 = 0, issued1 = 0, waited0 = 0, waited1 = 0;   // copies per stage
+  // The chunk stream: chunk g of the kernel goes to stage g % kChainStages
+  // and completes phase (g / kChainStages) & 1 of its barrier.  Thread 0
+  // counts the chunks it issued (n_iss); every thread counts those used
+  // (n_use), in step.
+  uint32_t n_iss = 0, n_use = 0;
   bool dead = false;   // a copy wait gave up: this CTA copies nothing more
   bool bad = false;
-  uint32_t nb = 0;     // level barriers passed (parity of the partial slots)
+  bool all_out = false;   // every request handed out (the same in every CTA of the cluster)
+  uint32_t nb = 0;     // steps (parity of the partial slots)
   uint32_t hand = 0;   // hand-offs (parity of the request slots)
   if (rank == 0 && tid == 0) sh.req[0] = (int)atomicAdd(req_next, 1u);
   cl.sync();
   if (tid == 0) sh.bnext = *cl.map_shared_rank(&sh.req[0], 0);
   __syncthreads();
   int b = sh.bnext;
-  // issues the first min(nch, kChainStages) chunks of a row (thread 0)
-  auto issue_row = [&](const float* r) {
-    for (int c = 0; c < min(nch, kChainStages); ++c) {
-      const int a = c0 + c * kChainChunk;
-      chain_copy(buf + c * kChainChunk, r + a, 4u * (uint32_t)(min(c1, a + kChainChunk) - a), &sh.full[c]);
-      if (c) ++issued1; else ++issued0;
-    }
-  };
   while (b < B) {
     const int Lraw = ell[b];
     const int L = min(max(Lraw, 0), G);
     if (rank == 0 && tid == 0 && (Lraw < 0 || Lraw > G)) record_status(status, DSPARK_ERR_INVALID);
-    // Near the end of the requests (fewer than one per cluster left to hand
-    // out) HBM has room: the next row's copies start before the decision that
-    // says whether it is needed, and a rejected chain drops one row.
-    const bool tail = b >= B - ncl;
-    bool ahead = false;   // the first chunks of the next level's row are in flight
-    if (L > 0 && tid == 0 && !dead) issue_row(T + (size_t)b * (G + 1) * V);
+    const float* rows = T + (size_t)b * (G + 1) * V;   // row j at rows + j * V
     // the drafted tokens, their draft probabilities and the accept uniforms
-    // of every position, one load each while row 0's copies fly
+    // of every position, one load each
     if (wid == 0 && lane < L) {
       const size_t it = (size_t)b * G + lane;
       sh.sx[lane] = checked_token(x[it], V, status);
       sh.spd[lane] = p_d[it];
-      sh.su[lane] = uniform01(rng4(key, kStreamAccept, (uint32_t)b, (uint32_t)(lane + 1), 0u).x);
+      sh.su[lane] = uniform01(rng4(live_key(key_arg), kStreamAccept, (uint32_t)b, (uint32_t)(lane + 1), 0u).x);
     }
     __syncthreads();
-    int j = 0;
+    int j = 0;       // next undecided position - 1 (= next row)
+    int n = L;       // accepted positions (L: all of them)
+    float lse_rej = 0.f;
     for (;;) {
-      const float* row = T + ((size_t)b * (G + 1) + j) * V;
-      float m = -INFINITY, s = 0.f;
-      if (L > 0) {
-        if (j > 0 && tid == 0 && !dead && !ahead) issue_row(row);
-        const int xj = sh.sx[j];
+      // ---- the step's rows: j, and once every request is out, the rows after it
+      const int nr = L > 0 ? (all_out ? min(kChainTailRows, L - j) : 1) : 0;
+      const uint32_t total = (uint32_t)(nr * nch);   // chunks of this step
+      uint32_t s_iss = 0;                            // issued of them (thread 0)
+      auto top_up = [&]() {
+        while (!dead && s_iss < total && n_iss - n_use < (uint32_t)kChainStages) {
+          const int r = (int)(s_iss / (uint32_t)nch), c = (int)(s_iss % (uint32_t)nch);
+          const int a = c0 + c * kChainChunk;
+          const int st = (int)(n_iss % kChainStages);
+          chain_copy(buf + st * kChainChunk, rows + (size_t)(j + r) * V + a,
+                     4u * (uint32_t)(min(c1, a + kChainChunk) - a), &sh.full[st]);
+          ++n_iss;
+          ++s_iss;
+        }
+      };
+      if (tid == 0) top_up();
+      int bad_rows = 0;
+      for (int r = 0; r < nr; ++r) {
+        const int xj = sh.sx[j + r];
+        float m = -INFINITY, s = 0.f;
+        bool br = false;
         for (int c = 0; c < nch; ++c) {
-          const int st = c % kChainStages;
-          if (!dead) {
-            if (!tc::mbar_wait_bounded(&sh.full[st], (st ? waited1 : waited0) & 1u, status)) dead = true;
-            if (st) ++waited1; else ++waited0;
-          }
+          const int st = (int)(n_use % kChainStages);
+          if (!dead && !tc::mbar_wait_bounded(&sh.full[st], (n_use / kChainStages) & 1u, status)) dead = true;
           const int n4 = (min(c1, c0 + (c + 1) * kChainChunk) - (c0 + c * kChainChunk)) >> 2;
           const float4* b4 = reinterpret_cast<const float4*>(buf + st * kChainChunk);
           float4 q[kChainVec];
@@ -557,12 +571,12 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
           const int e = xj - (c0 + c * kChainChunk);
           if (e >= 0 && e < 4 * n4 && ((e >> 2) % kChainThreads) == tid) {
             const float4 qe = b4[e >> 2];
-            sh.txv = (e & 3) == 0 ? qe.x : ((e & 3) == 1 ? qe.y : ((e & 3) == 2 ? qe.z : qe.w));
+            sh.txv[r] = (e & 3) == 0 ? qe.x : ((e & 3) == 1 ? qe.y : ((e & 3) == 2 ? qe.z : qe.w));
           }
           float bm = -INFINITY;
 #pragma unroll
           for (int k = 0; k < kChainVec; ++k) bm = fmaxf(fmaxf(bm, fmaxf(q[k].x, q[k].y)), fmaxf(q[k].z, q[k].w));
-          bad |= !(bm < INFINITY);
+          br |= !(bm < INFINITY);
           if (bm > m) {
             s = (m == -INFINITY) ? 0.f : s * exp2_fast((m - bm) * kLog2eF);
             m = bm;
@@ -576,81 +590,87 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
           }
           // every thread is done with this stage before it is refilled
           dead = __syncthreads_or(dead) != 0;
-          if (tid == 0 && !dead && c + kChainStages < nch) {
-            const int a = c0 + (c + kChainStages) * kChainChunk;
-            chain_copy(buf + st * kChainChunk, row + a, 4u * (uint32_t)(min(c1, a + kChainChunk) - a), &sh.full[st]);
-            if (st) ++issued1; else ++issued0;
-          }
+          ++n_use;
+          if (tid == 0) top_up();
         }
-        // the next row's copies, in the tail (the stages are free now)
-        ahead = tail && !dead && j + 1 < L;
-        if (tid == 0 && ahead) issue_row(row + V);
+        bad_rows |= (int)br << r;
+        // the row's partial over this warp's lanes
         chain_warp_reduce(m, s, 32);
-        if (lane == 0) sh.red[wid] = make_float2(m, s);
-        __syncthreads();
-        if (wid == 0) {
-          float2 pr = lane < kChainWarps ? sh.red[lane] : make_float2(-INFINITY, 0.f);
-          chain_warp_reduce(pr.x, pr.y, kChainWarps);
-          if (lane == 0) sh.part[nb & 1] = make_float4(pr.x, pr.y, (xj >= c0 && xj < c1) ? sh.txv : 0.f, 0.f);
-        }
-      } else if (tid == 0) {
-        sh.part[nb & 1] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        if (lane == 0) sh.red[r][wid] = make_float2(m, s);
       }
+      // ---- one partial per row of the step: warp r reduces row r over the warps
+      __syncthreads();
+      if (wid < nr) {
+        const int r = wid;
+        float2 pr = lane < kChainWarps ? sh.red[r][lane] : make_float2(-INFINITY, 0.f);
+        chain_warp_reduce(pr.x, pr.y, kChainWarps);
+        const int xj = sh.sx[j + r];
+        if (lane == 0)
+          sh.part[nb & 1][r] =
+              make_float4(pr.x, pr.y, (xj >= c0 && xj < c1) ? sh.txv[r] : 0.f,
+                          rank == 0 && *reinterpret_cast<volatile unsigned int*>(req_next) >= (unsigned int)B ? 1.f
+                                                                                                             : 0.f);
+      } else if (nr == 0 && tid == 0) {
+        sh.part[nb & 1][0] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      }
+      // every peer has read the slots of step nb - 2 (it arrived at the
+      // barrier of step nb - 1 after reading them)
       cl.sync();
-      // the decision, by each CTA from the cluster's partials (one lane per
-      // rank, the same reduction tree in every CTA; T at the token from the
-      // rank whose share holds it)
-      if (wid == 0) {
-        const float4 pr = lane < kChainCluster ? *cl.map_shared_rank(&sh.part[nb & 1], lane)
+      // ---- the decisions, warp r for row r, from the cluster's partials
+      // (one lane per rank, the same reduction tree in every CTA; T at the
+      // token from the rank whose share holds it)
+      if (wid < nr) {
+        const int r = wid;
+        const float4 pr = lane < kChainCluster ? *cl.map_shared_rank(&sh.part[nb & 1][r], lane)
                                                : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-        float pm = pr.x, ps = pr.y;
-        chain_warp_reduce(pm, ps, kChainCluster);
-        const float t = __shfl_sync(0xffffffffu, pr.z, L > 0 ? min(sh.sx[j] / share, kChainCluster - 1) : 0);
+        float pm2 = pr.x, ps2 = pr.y;
+        chain_warp_reduce(pm2, ps2, kChainCluster);
+        const int pos = j + r;
+        const float t = __shfl_sync(0xffffffffu, pr.z, min(sh.sx[pos] / share, kChainCluster - 1));
+        const float out = __shfl_sync(0xffffffffu, pr.w, 0);   // rank 0's word
         if (lane == 0) {
-          int acc = 0;
-          float lse_t = 0.f;
-          if (L > 0) {
-            lse_t = pm + logf(ps);
-            acc = sh.su[j] < expf(t - lse_t) / sh.spd[j];
-          }
-          sh.accept = acc;
-          sh.lse = lse_t;
+          const float lse_t = pm2 + logf(ps2);
+          sh.acc[r] = sh.su[pos] < expf(t - lse_t) / sh.spd[pos];
+          sh.lse[r] = lse_t;
+          if (r == 0) sh.out = out != 0.f;
         }
       }
       ++nb;
       __syncthreads();
-      const bool acc = sh.accept != 0;
-      if (L > 0 && acc && j + 1 < L) {
-        ++j;
-        continue;
-      }
-      // the chain ends here.  A row copied ahead is not needed: its copies
-      // land before the stages take the next request's rows.
-      if (ahead) {
-        for (int c = 0; c < min(nch, kChainStages); ++c) {
-          if (!tc::mbar_wait_bounded(&sh.full[c], (c ? waited1 : waited0) & 1u, status)) dead = true;
-          if (c) ++waited1; else ++waited0;
-        }
-        ahead = false;
-        dead = __syncthreads_or(dead) != 0;
-      }
-      // rank 0 writes the request's results
-      if (rank == 0 && tid == 0) {
-        if (L > 0 && !acc) {
-          n_out[b] = j;
-          resid_k[b] = j + 1;
-          resid_lse[b] = sh.lse;
-          resid_prev[b] = j == 0 ? anchor[b] : sh.sx[j - 1];
-        } else {
-          // every verified position accepted (or none to verify): the bonus race
-          n_out[b] = L;
-          resid_k[b] = 0;
-          const int slot = atomicAdd(bonus_rows, 1);
-          if (slot < B) bonus_rows[1 + slot] = b;
-          else record_status(status, DSPARK_ERR_INVALID);
+      if (nr > 0) all_out = all_out || sh.out != 0;
+      // ---- the chain goes on past every accepted row of the step, up to the
+      // first rejection (rows after it count for nothing, their values too)
+      bool ended = nr == 0;
+      for (int r = 0; r < nr; ++r) {
+        bad |= (bad_rows >> r) & 1;
+        if (!sh.acc[r]) {
+          n = j + r;
+          lse_rej = sh.lse[r];
+          ended = true;
+          break;
         }
       }
-      break;
+      if (!ended) {
+        j += nr;
+        ended = j == L;
+      }
+      if (ended) break;
+    }
+    // rank 0 writes the request's results
+    if (rank == 0 && tid == 0) {
+      if (n < L) {
+        n_out[b] = n;
+        resid_k[b] = n + 1;
+        resid_lse[b] = lse_rej;
+        resid_prev[b] = n == 0 ? anchor[b] : sh.sx[n - 1];
+      } else {
+        // every verified position accepted (or none to verify): the bonus race
+        n_out[b] = L;
+        resid_k[b] = 0;
+        const int slot = atomicAdd(bonus_rows, 1);
+        if (slot < B) bonus_rows[1 + slot] = b;
+        else record_status(status, DSPARK_ERR_INVALID);
+      }
     }
     // the next request (two hand-off slots: rank 0 rewrites one only after a
     // cluster barrier that every peer reached after reading it)
@@ -662,13 +682,12 @@ verify_chain(const float* __restrict__ T, const int32_t* __restrict__ x, const f
     b = sh.bnext;
   }
   if (bad) record_status(status, DSPARK_ERR_NONFINITE);
-  // no CTA leaves while a peer may still read its shared memory, nor while a
-  // copy it issued may still land
+  // no CTA leaves while a peer may still read its shared memory; every chunk
+  // this CTA issued was used (or given up on) in its step
   cl.sync();
-  if (tid == 0) {
-    if (issued0 > waited0) tc::mbar_drain(&sh.full[0], (issued0 - 1u) & 1u);
-    if (issued1 > waited1) tc::mbar_drain(&sh.full[1], (issued1 - 1u) & 1u);
-  }
+  if (tid == 0 && dead)
+    for (uint32_t g = n_iss > (uint32_t)kChainStages ? n_iss - kChainStages : 0u; g < n_iss; ++g)
+      tc::mbar_drain(&sh.full[g % kChainStages], (g / kChainStages) & 1u);
 }
 
 template <int WDT>
