@@ -212,6 +212,49 @@ struct RowRace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Two fp32 values in one 64-bit register, and the two-wide fp32 add and fma
+// of sm_100 and later (each lane rounded as the scalar operation rounds).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2split(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// A block's softmax mass from its four terms: (e0 + e2) + (e1 + e3), the same
+// sum wherever a block's mass is formed.
+__device__ __forceinline__ float block_sum(float e0, float e1, float e2, float e3) {
+  float a, b;
+  f2split(f2add(f2(e0, e1), f2(e2, e3)), a, b);
+  return a + b;
+}
+
+// The four softmax terms e_c = 2^(l_c log2 e - mb) of a block (l2e2 = (log2 e,
+// log2 e), nmb2 = (-mb, -mb)) and their sum.
+__device__ __forceinline__ float block_terms(float l0, float l1, float l2, float l3, uint64_t l2e2, uint64_t nmb2,
+                                             float (&e)[4]) {
+  float t0, t1, t2, t3;
+  f2split(f2fma(f2(l0, l1), l2e2, nmb2), t0, t1);
+  f2split(f2fma(f2(l2, l3), l2e2, nmb2), t2, t3);
+  e[0] = ex2_approx(t0);
+  e[1] = ex2_approx(t1);
+  e[2] = ex2_approx(t2);
+  e[3] = ex2_approx(t3);
+  return block_sum(e[0], e[1], e[2], e[3]);
+}
+
 __device__ __forceinline__ float race_bound(float run_m, float zbest) {
   return exp2f((run_m - zbest) * kLog2e) * (1.0f + 0x1p-10f);
 }
@@ -281,15 +324,14 @@ __device__ __forceinline__ void race_seed(RowRace& st, float (&l)[CPP], const ui
                                           const RngKey& key, uint32_t req, uint32_t pos) {
   constexpr int NB = CPP / 4;
   const float mb = st.run_m * kLog2e;
+  const uint64_t l2e2 = f2(kLog2e, kLog2e), nmb2 = f2(-mb, -mb);
   float bs = 0.f, bd = 1.f, e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
   uint32_t bw = 0u;
   int bq = -1;
 #pragma unroll
   for (int q = 0; q < NB; ++q) {
     float e[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) e[c] = ex2_approx(fmaf(l[4 * q + c], kLog2e, -mb));
-    const float sq = ((e[0] + e[1]) + e[2]) + e[3];
+    const float sq = block_terms(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3], l2e2, nmb2, e);
     const float d = 8454144.0f - block_hf(wb[q]);   // 65536 - h, exactly
     if (sq * bd > bs * d || bq < 0) {
       bs = sq; bd = d; bw = wb[q]; bq = q;
@@ -332,15 +374,14 @@ __device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP]
     st.bound = race_bound(st.run_m, st.zthr);
   }
   const float mb = st.run_m * kLog2e;
+  const uint64_t l2e2 = f2(kLog2e, kLog2e), nmb2 = f2(-mb, -mb);
   const float b16 = st.bound * 65536.0f;
   float s = 0.f;
   uint32_t cand = 0;
 #pragma unroll
   for (int q = 0; q < NB; ++q) {
     float e[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) e[c] = ex2_approx(fmaf(l[4 * q + c], kLog2e, -mb));
-    const float sq = ((e[0] + e[1]) + e[2]) + e[3];
+    const float sq = block_terms(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3], l2e2, nmb2, e);
     s += sq;
     if (fmaf(sq, b16, block_hf(wb[q])) > kScreenThr) cand |= 1u << q;
     *reinterpret_cast<float4*>(spill + (((j0 + q) ^ sw) << 4)) = make_float4(e[0], e[1], e[2], e[3]);
@@ -351,7 +392,7 @@ __device__ __forceinline__ float race_resolve(RowRace& st, const float (&l)[CPP]
     const int q = __ffs(cand) - 1;
     cand &= cand - 1;
     const float4 e = *reinterpret_cast<const float4*>(spill + (((j0 + q) ^ sw) << 4));
-    const float sq = ((e.x + e.y) + e.z) + e.w;
+    const float sq = block_sum(e.x, e.y, e.z, e.w);
     const float z = st.run_m + logf(sq) + gumbel_from_bits(pick_word<NB>(wb, q) >> 9);
     if (z > st.zbest) {
       st.zbest = z;
@@ -380,14 +421,13 @@ __device__ __forceinline__ void race_screen(RowRace& st, const float (&l)[CPP], 
                                             uint32_t req, uint32_t pos, int* status) {
   constexpr int NB = CPP / 4;
   const float mb = st.run_m * kLog2e;
+  const uint64_t l2e2 = f2(kLog2e, kLog2e), nmb2 = f2(-mb, -mb);
   const float b16 = st.bound * 65536.0f;
   float smax = 0.f, s = 0.f;
 #pragma unroll
   for (int q = 0; q < NB; ++q) {
     float e[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) e[c] = ex2_approx(fmaf(l[4 * q + c], kLog2e, -mb));
-    const float sq = ((e[0] + e[1]) + e[2]) + e[3];
+    const float sq = block_terms(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3], l2e2, nmb2, e);
     s += sq;
     smax = fmaxf(smax, fmaf(sq, b16, block_hf(wb[q])));
   }
@@ -431,7 +471,7 @@ __device__ __forceinline__ void resid_tile(ResRace& st, float (&rho)[CPP], int n
   block_words<CPP>(wb, key, kStreamResidual, req, pos, v0);
   float W[NB];
 #pragma unroll
-  for (int q = 0; q < NB; ++q) W[q] = ((rho[4 * q] + rho[4 * q + 1]) + rho[4 * q + 2]) + rho[4 * q + 3];
+  for (int q = 0; q < NB; ++q) W[q] = block_sum(rho[4 * q], rho[4 * q + 1], rho[4 * q + 2], rho[4 * q + 3]);
   if (st.zbest == -INFINITY) {
     // open the race with the block most likely to win: largest W_q / (1 - u_q)
     float bw = 0.f, bd = 1.f;
@@ -468,7 +508,7 @@ __device__ __forceinline__ void resid_tile(ResRace& st, float (&rho)[CPP], int n
       const int q = __ffs(cand) - 1;
       cand &= cand - 1;
       const float4 e = *reinterpret_cast<const float4*>(spill + (((j0 + q) ^ sw) << 4));
-      const float z = logf(((e.x + e.y) + e.z) + e.w) + gumbel_from_bits(pick_word<NB>(wb, q) >> 9);
+      const float z = logf(block_sum(e.x, e.y, e.z, e.w)) + gumbel_from_bits(pick_word<NB>(wb, q) >> 9);
       if (z > st.zbest) {
         st.zbest = z;
         st.best_v = block_pick(key, kStreamResidual, req, pos, ((uint32_t)v0 >> 2) + (uint32_t)q, e.x, e.y, e.z, e.w);
@@ -1079,7 +1119,8 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
 #pragma unroll
             for (int c = 0; c < CPP; c += 4) {
               const float4 u4 = *reinterpret_cast<const float4*>(urow + (((j0 + c / 4) ^ (r & 7)) << 4));
-              v[c + 0] += u4.x; v[c + 1] += u4.y; v[c + 2] += u4.z; v[c + 3] += u4.w;
+              f2split(f2add(f2(v[c + 0], v[c + 1]), f2(u4.x, u4.y)), v[c + 0], v[c + 1]);
+              f2split(f2add(f2(v[c + 2], v[c + 3]), f2(u4.z, u4.w)), v[c + 2], v[c + 3]);
             }
             if (nv < CPP) {
               // past the end of the vocabulary: out of the softmax and the race
@@ -1144,17 +1185,19 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
             const unsigned char* trow = urow + R * 256;
             const int j0 = (part * CPP) / 4, sw = r & 15;
             float uu[CPP];
+            const uint64_t l2e2 = f2(kLog2e, kLog2e), nld2 = f2(-ld2, -ld2), nlt2 = f2(-lt2, -lt2);
 #pragma unroll
             for (int c = 0; c < CPP; c += 4) {
               const float4 u4 = *reinterpret_cast<const float4*>(urow + (((j0 + c / 4) ^ sw) << 4));
               const float4 t4 = *reinterpret_cast<const float4*>(trow + (((j0 + c / 4) ^ sw) << 4));
-              const float uv[4] = {u4.x, u4.y, u4.z, u4.w}, tv[4] = {t4.x, t4.y, t4.z, t4.w};
+              // exponents of p_d (fused logit) and p_t, two lanes at a time
+              float ad[4], at[4];
+              f2split(f2fma(f2add(f2(v[c], v[c + 1]), f2(u4.x, u4.y)), l2e2, nld2), ad[0], ad[1]);
+              f2split(f2fma(f2add(f2(v[c + 2], v[c + 3]), f2(u4.z, u4.w)), l2e2, nld2), ad[2], ad[3]);
+              f2split(f2fma(f2(t4.x, t4.y), l2e2, nlt2), at[0], at[1]);
+              f2split(f2fma(f2(t4.z, t4.w), l2e2, nlt2), at[2], at[3]);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float pd = ex2_approx(fmaf(v[c + e] + uv[e], kLog2e, -ld2));
-                const float pt = ex2_approx(fmaf(tv[e], kLog2e, -lt2));
-                uu[c + e] = pt - pd;
-              }
+              for (int e = 0; e < 4; ++e) uu[c + e] = ex2_approx(at[e]) - ex2_approx(ad[e]);
             }
             // the row's best from other CTAs: the latest copy of its key that
             // has landed in shared memory (nothing waits for it)
