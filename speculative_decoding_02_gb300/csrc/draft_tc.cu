@@ -1464,6 +1464,29 @@ cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtens
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// U [B, G, V] fp32 viewed as a 4-D tensor {32 columns, V / 32 column blocks,
+// G, B} with {32, 2, 1, R} boxes, 128-byte swizzled: one box is the 64
+// columns of one vocabulary tile for R request rows at one position, fetched
+// as 256 contiguous bytes per row (a [R x 1 x 32] box fetches 128 bytes per
+// row, and a stream of those runs reaches about two thirds of the copy rate
+// of 256-byte runs on GB300).  In shared memory row r's half h is the
+// 128-byte line 2r + h.  Only whole 32-column blocks are in the view: with V
+// % 32 != 0 the vocabulary's last tile must come from make_u_tensor_map's
+// boxes; blocks past the view (and rows past B) are zero-filled.
+cudaError_t make_u_tile_map(const float* U, int B, int G, int V, int R, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  if (V < 32) return cudaErrorInvalidValue;
+  cuuint64_t dims[4] = {32, (cuuint64_t)(V / 32), (cuuint64_t)G, (cuuint64_t)B};
+  cuuint64_t strides[3] = {128, (cuuint64_t)V * 4, (cuuint64_t)G * V * 4};
+  cuuint32_t box[4] = {32, 2, 1, (cuuint32_t)R};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(U), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 namespace {
 
 // Self-test of the bounded waits: mode 0 waits on an mbarrier that no thread

@@ -10,9 +10,11 @@
 // and [V, G + 1, B] tensors, so both stream in by TMA like the draft's U:
 //
 //   warp 0      TMA producer: W2 atoms of 192 rows x 64 K (bf16, 128-byte
-//               swizzled, evict_last) and, per 64-column tile, two [R x 32]
-//               boxes of U[., k-1, .] and two of T[., k-1, .] (evict_first)
-//               into a ring of two stages; it runs ahead across positions.
+//               swizzled, evict_last) and, per 64-column tile, one box of
+//               U[., k-1, .] and one of T[., k-1, .] (R rows x 64 columns,
+//               256 contiguous bytes per row, evict_first) into a ring of two
+//               stages; it runs ahead across positions.  With V % 32 != 0 the
+//               vocabulary's last tile comes as two [R x 32] boxes per tensor.
 //   warp 1      TMEM allocation and the single-thread MMA issuer: the bias
 //               E * W2_rows^T of up to three tiles per tcgen05.mma (fp32 in
 //               TMEM), E = W1[x_{k-1}] in TMEM columns 384-511.
@@ -79,6 +81,7 @@ struct LabelParams {
   const int32_t* ell;        // [B]
   const float2* row_part;    // [B*(G+1)][nsegs] target-row partials
   int nsegs;
+  int tail_tile;             // tile staged as [R x 32] boxes (V % 32 != 0), else -1
   const int* stats_done;     // row segments a draft took (nullptr: not checked)
   const int* full_rows;      // 1 while verification's statistics cover every row j < ell (nullptr: not checked)
   float* label;              // [B][G], zeroed by the caller
@@ -111,7 +114,8 @@ constexpr float kL2e = 1.4426950408889634f;
 template <int R>
 __global__ void __launch_bounds__(LThreads, 1)
 label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
-         const __grid_constant__ CUtensorMap t_map, const LabelParams p) {
+         const __grid_constant__ CUtensorMap t_map, const __grid_constant__ CUtensorMap u4_map,
+         const __grid_constant__ CUtensorMap t4_map, const LabelParams p) {
   constexpr int kRepl = LBM / R;
   constexpr int kParts = 4 * kRepl;
   constexpr int CPP = LBN / kParts;
@@ -148,6 +152,8 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
     prefetch_tensormap(&w2_map);
     prefetch_tensormap(&u_map);
     prefetch_tensormap(&t_map);
+    prefetch_tensormap(&u4_map);
+    prefetch_tensormap(&t4_map);
   }
   if (warp == 1) tmem_alloc(&bars->tmem_base, LTmemCols);
   tc_fence_before();
@@ -176,15 +182,20 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
           const int su = ucount % LUTStages;
           ok = mbar_wait(&bars->empty_ut[su], ((ucount / LUTStages) & 1) ^ 1, abort, p.status);
           if (ok && lane == 0) {
-            // U and T boxes of position k: [R rows x 32 columns] each, two per
-            // tensor (rows past B and columns past V are zero-filled)
+            // the U and T tiles of position k, R rows x 64 columns each (rows
+            // past B and columns past V are zero-filled)
             const int v = v0 + j * LBN;
             unsigned char* dst = UT_s + su * LUTStageBytes;
             mbar_arrive_expect_tx(&bars->full_ut[su], (uint32_t)(4 * LUBox * R * 4));
-            tma_g2s_3d(dst, &u_map, v, k - 1, m0, &bars->full_ut[su], pol_u);
-            tma_g2s_3d(dst + R * 128, &u_map, v + LUBox, k - 1, m0, &bars->full_ut[su], pol_u);
-            tma_g2s_3d(dst + 2 * R * 128, &t_map, v, k - 1, m0, &bars->full_ut[su], pol_u);
-            tma_g2s_3d(dst + 3 * R * 128, &t_map, v + LUBox, k - 1, m0, &bars->full_ut[su], pol_u);
+            if (t0 + g + j != p.tail_tile) {
+              tma_g2s_4d(dst, &u4_map, 0, v / LUBox, k - 1, m0, &bars->full_ut[su], pol_u);
+              tma_g2s_4d(dst + R * 256, &t4_map, 0, v / LUBox, k - 1, m0, &bars->full_ut[su], pol_u);
+            } else {
+              tma_g2s_3d(dst, &u_map, v, k - 1, m0, &bars->full_ut[su], pol_u);
+              tma_g2s_3d(dst + R * 128, &u_map, v + LUBox, k - 1, m0, &bars->full_ut[su], pol_u);
+              tma_g2s_3d(dst + 2 * R * 128, &t_map, v, k - 1, m0, &bars->full_ut[su], pol_u);
+              tma_g2s_3d(dst + 3 * R * 128, &t_map, v + LUBox, k - 1, m0, &bars->full_ut[su], pol_u);
+            }
           }
         }
       }
@@ -282,22 +293,33 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->full_ut[su], (it / LUTStages) & 1, abort, p.status));
         if (!ok) break;
         if (active && nv > 0) {
-          // this thread's columns: box (part * CPP) / 32, 16-byte chunks j0.. of
-          // row r at chunk j ^ (r & 7) (128-byte swizzle); T two boxes further
-          const unsigned char* urow = UT_s + su * LUTStageBytes + ((part * CPP) / LUBox) * (R * 128) + r * 128;
-          const unsigned char* trow = urow + 2 * R * 128;
-          const int j0 = ((part * CPP) % LUBox) / 4;
+          // this thread's columns: half hf = (part * CPP) / 32 of row r, the
+          // 128-byte line 2r + hf of a tile box (hf * R + r of the [R x 32]
+          // boxes of a tail tile), 16-byte chunks j0.. stored at chunk
+          // j ^ (line & 7) (128-byte swizzle); T R * 256 bytes further
+          const int hf = (part * CPP) / LUBox;
+          const int line = t0 + i == p.tail_tile ? hf * R + r : 2 * r + hf;
+          const unsigned char* urow = UT_s + su * LUTStageBytes + line * 128;
+          const unsigned char* trow = urow + R * 256;
+          const int j0 = ((part * CPP) % LUBox) / 4, sw = line & 7;
+          // lanes with bit 2 set take each pair of chunks in swapped order
+          // (rows r and r + 4 share a swizzle phase in a tile box: they then
+          // hit different banks); the sum does not depend on the order
+          constexpr int NB = CPP / 4;
+          const int ps = NB >= 2 ? (lane >> 2) & 1 : 0;
 #pragma unroll
-          for (int c = 0; c < CPP; c += 4) {
-            const int off = ((j0 + c / 4) ^ (r & 7)) << 4;
+          for (int c4 = 0; c4 < NB; ++c4) {
+            const int cc = c4 ^ ps;
+            const int off = ((j0 + cc) ^ sw) << 4;
             const float4 u4 = *reinterpret_cast<const float4*>(urow + off);
             const float4 t4 = *reinterpret_cast<const float4*>(trow + off);
             const float uv[4] = {u4.x, u4.y, u4.z, u4.w}, tv[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float pd = ex2_approx(fmaf(v[c + e] + uv[e], kL2e, -ld2));
+              const float ve = (NB >= 2 && ps) ? v[4 * (c4 ^ (NB >= 2 ? 1 : 0)) + e] : v[4 * c4 + e];
+              const float pd = ex2_approx(fmaf(ve + uv[e], kL2e, -ld2));
               const float pt = ex2_approx(fmaf(tv[e], kL2e, -lt2));
-              if (c + e < nv) lacc += fminf(pd, pt);
+              if (4 * cc + e < nv) lacc += fminf(pd, pt);
             }
           }
         }
@@ -337,7 +359,7 @@ cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const voi
                                        const int32_t* ell, const float2* row_part, int nsegs,
                                        const int* stats_done, const int* full_rows, float* label, int B, int G,
                                        int V, int* status, cudaStream_t stream) {
-  CUtensorMap wmap, umap, tmap;
+  CUtensorMap wmap, umap, tmap, u4map, t4map;
   cudaError_t e = make_w2_tensor_map(W2, V, &wmap);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -346,6 +368,13 @@ cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const voi
   const int R = B <= 32 ? 32 : (B <= 64 ? 64 : LBM);
   if ((e = make_u_tensor_map(U, B, G, V, R, &umap)) != cudaSuccess) return e;
   if ((e = make_u_tensor_map(T, B, G + 1, V, R, &tmap)) != cudaSuccess) return e;
+  // whole tiles by the 4-D view (V >= 32); below that every tile is the tail
+  u4map = umap;
+  t4map = tmap;
+  if (V >= 32) {
+    if ((e = make_u_tile_map(U, B, G, V, R, &u4map)) != cudaSuccess) return e;
+    if ((e = make_u_tile_map(T, B, G + 1, V, R, &t4map)) != cudaSuccess) return e;
+  }
   auto kern = R == 32 ? label_tc<32> : (R == 64 ? label_tc<64> : label_tc<LBM>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LSmemBytes);
   if (e != cudaSuccess) return e;
@@ -361,6 +390,7 @@ cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const voi
   lp.ell = ell;
   lp.row_part = row_part;
   lp.nsegs = nsegs;
+  lp.tail_tile = V % 32 != 0 ? ntiles - 1 : -1;
   lp.stats_done = stats_done;
   lp.full_rows = full_rows;
   lp.label = label;
@@ -368,7 +398,7 @@ cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const voi
   lp.B = B; lp.G = G; lp.V = V;
   lp.ctas_per_mtile = per;
   lp.ntiles = ntiles;
-  kern<<<mtiles * per, LThreads, LSmemBytes, stream>>>(wmap, umap, tmap, lp);
+  kern<<<mtiles * per, LThreads, LSmemBytes, stream>>>(wmap, umap, tmap, u4map, t4map, lp);
   return cudaGetLastError();
 }
 

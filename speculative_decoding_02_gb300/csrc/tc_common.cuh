@@ -170,6 +170,16 @@ __device__ __forceinline__ void tma_g2s_3d(void* dst, const CUtensorMap* map, in
       : "memory");
 }
 
+// 4-D tiled tensor copy global -> shared; c0 is the innermost coordinate.
+__device__ __forceinline__ void tma_g2s_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                           uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // 16-byte asynchronous global -> shared copies (L2 only), grouped and waited
 // for by the issuing thread; other threads see the data after a barrier.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
