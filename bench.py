@@ -5,18 +5,20 @@ prefix scheduler, rejection-sampling verification -- over one batch of the
 synthetic workload (default: batch-128 engine point, B=128, gamma=16,
 V=151936).  The metric is verified draft tokens per second: the sum over
 requests of the scheduled verify lengths l_r, per round, divided by the round
-time.  The headline round verifies along each request's accept chain, reading
-the target rows its accept tests reach (the default of dspark_round).  The
-same round with the draft taking the statistics of every target row j < gamma
-while it runs (DSPARK_EARLY_TARGET_STATS: T given at draft time) and with
-verification taking those of every row j < l_r first (DSPARK_ALL_ROW_STATS)
-are reported beside it, with the other workloads, a truncating schedule and a
-CUDA-graph replay of the round.
+time.  T is an input of the round, so in the headline round the draft takes
+the softmax statistics of the target rows the accept chains reach while it
+runs, testing each position as its inputs come out and skipping the rows past
+a known rejection (DSPARK_CHAIN_TARGET_STATS), and verification decides on
+them.  The same round verifying along each request's accept chain after the
+draft (dspark_round's default), with the draft taking every row j < gamma
+(DSPARK_EARLY_TARGET_STATS) and with verification taking every row j < l_r
+first (DSPARK_ALL_ROW_STATS) are reported beside it, with the other
+workloads, a truncating schedule and a CUDA-graph replay of the round.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                         [--impl gb300|reference] [--no-cpu-baseline] [--no-e2e]
-                        [--no-workloads] [--form chain|early|all]
-        python bench.py --profile-draft [--workload NAME]   (the draft alone, for ncu)
+                        [--no-workloads] [--form chain|early|all|lazy]
+        python bench.py --profile-draft [--workload NAME] [--form lazy] [--plain-draft]   (the first stage alone)
         python bench.py --profile-label [--workload NAME]   (the acceptance labels alone)
         python bench.py --profile-round [--workload NAME] [--form F]   (whole rounds, for launch lists)
 
@@ -49,9 +51,19 @@ UNIT = "tokens/s"
 #   early  the draft takes the rows j < gamma while it runs (T given at draft
 #          time; DSPARK_EARLY_TARGET_STATS)
 #   all    verification takes every row j < l_r first (DSPARK_ALL_ROW_STATS)
+#   lazy   the draft takes only the rows the accept chains reach, running the
+#          accept tests itself as their inputs come out (T given at draft
+#          time; DSPARK_CHAIN_TARGET_STATS)
 FORMS = {"chain": "verification along the accept chains",
          "early": "target-row statistics taken by the draft",
-         "all": "verification's pass over every row j < l_r"}
+         "all": "verification's pass over every row j < l_r",
+         "lazy": "target-row statistics of the rows the accept chains reach, taken by the draft"}
+DRAFT_T_FORMS = ("early", "lazy")   # forms whose draft takes T along
+
+
+def form_flags(form):
+    """Keyword arguments of ds.round for a form."""
+    return dict(early_stats=form == "early", all_row_stats=form == "all", chain_stats=form == "lazy")
 
 
 def parse():
@@ -75,7 +87,7 @@ def parse():
                     help="the acceptance labels alone, 4 calls on a draft's statistics (for ncu)")
     ap.add_argument("--profile-round", action="store_true",
                     help="run a few whole rounds of the workload (ncu launch lists and kernel captures)")
-    ap.add_argument("--form", default="chain", choices=list(FORMS),
+    ap.add_argument("--form", default="lazy", choices=list(FORMS),
                     help="the headline round's form (and --profile-round's): where the target rows' "
                          "statistics come from")
     return ap.parse_args()
@@ -96,11 +108,11 @@ def peaks():
 def t_rows(form, B, G, ell_sum, n_acc, n_full):
     """Target rows one round reads once (a rejecting request's row k* - 1 is
     counted here; the residual's second read of it is in round_bytes):
-    chain -- rows 0..n_r of every request, n_r + 1 each (the row of the
+    chain, lazy -- rows 0..n_r of every request, n_r + 1 each (the row of the
     rejected position, or the bonus row after a whole accept); early -- every
     row j < gamma, and the bonus rows; all -- every row j < l_r, and the bonus
     rows."""
-    if form == "chain":
+    if form in ("chain", "lazy"):
         return n_acc + B
     if form == "early":
         return B * G + n_full
@@ -135,13 +147,26 @@ def fused_draft_bytes_per_launch(w):
     return draft_bytes_per_launch(w) + 4 * w.B * w.gamma * w.V
 
 
-def stage_bytes_per_launch(w, early=True):
+def stage_bytes_per_launch(w, early=True, rows=None):
     """The first stage of a round (dspark_draft_schedule: draft, confidences,
-    schedule): the draft's bytes, the target rows j < gamma once when taken
-    along, the hidden states h and the head's w once, and c and ell out."""
+    schedule): the draft's bytes, the target rows it takes along once (every
+    row j < gamma when early; `rows` of them when given, the rows j < gamma
+    the accept chains reach), the hidden states h and the head's w once, and
+    c and ell out."""
     sw = 2 if w.wdtype == torch.bfloat16 else 4
     b = draft_bytes_per_launch(w) + sw * w.B * w.gamma * w.H + 4 * (w.H + w.r) + 4 * w.B * w.gamma + 4 * w.B
+    if rows is not None:
+        return b + 4 * w.V * rows
     return b + (4 * w.B * w.gamma * w.V if early else 0)
+
+
+def stage_bytes_of(w, r, form):
+    """The first stage's algorithmic bytes in a RoundTimer result's form
+    (lazy: the rows j < gamma of the chains, n_r + 1 per rejecting request
+    and gamma per whole accept)."""
+    if form == "lazy":
+        return stage_bytes_per_launch(w, rows=(r["n_acc"] + r["n_rej"]) / r["steps"])
+    return stage_bytes_per_launch(w, form == "early")
 
 
 def kernels_per_round(w, form="chain"):
@@ -157,7 +182,7 @@ def kernels_per_round(w, form="chain"):
     and the bonus race's write the tokens; or its CUDA-core form and then the
     residual finalize)."""
     tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
-    stage = 1 if tc else 2 * w.gamma + (2 if form == "early" else 0) + 2
+    stage = 1 if tc else 2 * w.gamma + (2 if form in DRAFT_T_FORMS else 0) + 2
     verify = (3 if tc else 4) + (2 if form == "all" else 0)
     return stage + verify
 
@@ -205,10 +230,13 @@ def profile_traffic(path, sources, w, **match):
     return None
 
 
-def draft_traffic(w, early=True):
-    """DRAM bytes of one draft launch from the committed ncu record (None if
-    missing, for another workload or mode, or stale)."""
-    return profile_traffic(DRAFT_PROFILE, DRAFT_SOURCES, w, early_target_stats=bool(early))
+def draft_traffic(w, form="early"):
+    """DRAM bytes of one first-stage launch of a form from the committed ncu
+    record (None if missing, for another workload or mode, or stale): the
+    draft alone (chain, all), with every row j < gamma (early), with the rows
+    the accept chains reach (lazy)."""
+    return profile_traffic(DRAFT_PROFILE, DRAFT_SOURCES, w, early_target_stats=form in DRAFT_T_FORMS,
+                           chain_target_stats=True if form == "lazy" else None)
 
 
 def label_traffic(w):
@@ -406,7 +434,7 @@ class RoundTimer:
     def __init__(self, ds, w, inp, dev, form, sps=None, khist=None, ws=None):
         assert form in FORMS, form
         self.ds, self.w, self.inp, self.dev, self.form = ds, w, inp, dev, form
-        self.early = form == "early"
+        self.early = form in DRAFT_T_FORMS
         self.sps = inp["sps"] if sps is None else sps
         self.khist = khist
         self.ws = ds.workspace(w.B, w.gamma, w.V, dev) if ws is None else ws
@@ -420,7 +448,7 @@ class RoundTimer:
         o = ds.draft_schedule(inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], w.seed, i,
                               sps=self.sps, mode=w.mode, khist=self.khist, out=self.out if out is None else out,
                               ws=self.ws,
-                              T_early=inp["T"] if self.early else None)
+                              T_early=inp["T"] if self.early else None, chain_stats=self.form == "lazy")
         if d1 is not None:
             d1.record(self.stream)
         n, _ = ds.verify(inp["T"], inp["U"], inp["W1"], inp["W2"], inp["anchor"], o.x, o.p, o.lse, o.ell, w.seed, i,
@@ -479,7 +507,7 @@ def round_record(w, r, hbm, form):
     per_round = r["ell_sum"] / steps
     rows = round_rows(w, r, form)
     rb = round_bytes(w, rows, r["n_rej"] / steps)
-    db = stage_bytes_per_launch(w, form == "early")
+    db = stage_bytes_of(w, r, form)
     return {"form": FORMS[form], "ms": ms, "verified_per_round": per_round,
             "accepted_per_round": r["n_acc"] / steps,
             "verified_tokens_per_s": r["ell_sum"] / (r["ms"] / 1e3),
@@ -487,7 +515,7 @@ def round_record(w, r, hbm, form):
             "target_rows_per_round": rows,
             "round_GB": rb / 1e9, "round_hbm_frac": rb / (ms / 1e3) / 1e9 / hbm,
             "draft_ms": r["draft_ms"], "draft_GB": db / 1e9,
-            "draft_hbm_frac": db / (r["draft_ms"] / 1e3) / 1e9 / hbm, "early_target_stats": form == "early"}
+            "draft_hbm_frac": db / (r["draft_ms"] / 1e3) / 1e9 / hbm, "early_target_stats": form in DRAFT_T_FORMS}
 
 
 def gated_round_ms(ds, w, inp, dev, steps):
@@ -547,8 +575,8 @@ def graph_round_ms(ds, w, inp, dev, steps, form):
 
     def call():
         ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed, rnd=0,
-                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, early_stats=form == "early",
-                 all_row_stats=form == "all", round_dev=round_dev, advance_round=True)
+                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, round_dev=round_dev,
+                 advance_round=True, **form_flags(form))
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
@@ -623,7 +651,7 @@ def run_gpu(args):
     khist = torch.zeros(2, dtype=torch.int32, device=dev) if w.mode == wl.MODE_TOPK else None
     tc = w.wdtype == torch.bfloat16 and w.r == 256 and w.V >= 192
     form = args.form
-    early = form == "early"
+    early = form in DRAFT_T_FORMS
 
     def barrier():
         if world > 1:
@@ -645,14 +673,14 @@ def run_gpu(args):
     # Markov draft, with the target-row statistics in the early form, the
     # confidences and the schedule), timed inside the timed region
     draft_ms = r["draft_ms"]
-    dbytes = stage_bytes_per_launch(w, early)
+    dbytes = stage_bytes_of(w, r, form)
     achieved = dbytes / (draft_ms / 1e3) / 1e9
 
     extra = {}
     if rank == 0:
         # the same workload in the other forms (same round indices)
         extra["other_forms"] = {f: round_record(w, RoundTimer(ds, w, inp, dev, f, khist=khist).run(
-            args.steps, 3), hbm, f) for f in FORMS if f != form and (tc or f != "early")}
+            args.steps, 3), hbm, f) for f in FORMS if f != form and (tc or f not in DRAFT_T_FORMS)}
         # a falling steps-per-second curve, so that the greedy truncates (the
         # scheduler's sorting path; only the verified rows are read)
         if w.mode == wl.MODE_GREEDY:
@@ -768,13 +796,19 @@ def run_gpu(args):
                        "round_hbm_frac": rbytes / (ms / args.steps / 1e3) / 1e9 / hbm,
                        "parallelism": f"replicas x{world}"},
             "roofline": {"kernel": "the round's first stage, one persistent launch (dspark_draft_schedule: "
+                                   "draft_step_tc drafting, taking the statistics of the target rows the accept "
+                                   "chains reach along, then its fused finalize with the confidences and the "
+                                   "schedule)"
+                         if form == "lazy" else
+                         "the round's first stage, one persistent launch (dspark_draft_schedule: "
                                    "draft_step_tc drafting, taking the target rows' statistics along, then its "
                                    "fused finalize with the confidences and the schedule)"
                          if early else "the round's first stage, one persistent launch (dspark_draft_schedule: "
                                        "draft_step_tc drafting, then its fused finalize with the confidences and "
                                        "the schedule)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": draft_traffic(w, early), "peak_kind": peak_kind,
+                         "frac": achieved / hbm, "traffic": draft_traffic(w, form),
+                         "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": dbytes, "ms_per_launch": draft_ms},
             "clocks": clk.summary(),
             "acceptance_label": label,
@@ -821,8 +855,7 @@ def run_e2e(w, inp, ds, dev, args, khist, form):
         stream.wait_event(uploaded[slot])
         b = devb[slot]
         ds.round(b["U"], b["T"], inp["W1"], inp["W2"], b["h"], inp["w"], b["anchor"], seed=w.seed, rnd=i,
-                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, early_stats=form == "early",
-                 all_row_stats=form == "all")
+                 sps=inp["sps"], mode=w.mode, khist=khist, out=out, ws=ws, **form_flags(form))
         consumed[slot].record(stream)
         for k in outs:
             hosto[k].copy_(getattr(out, k), non_blocking=True)
@@ -872,14 +905,30 @@ def run_profile_draft(args):
     sps = None if sps is None else sps.to(dev)
     khist = torch.zeros(2, dtype=torch.int32, device=dev)
     T = None if args.plain_draft else rin["T"]
+    chain = T is not None and args.form == "lazy"
     ws = ds.workspace(w.B, w.gamma, w.V, dev)
     for i in range(4):
         ds.draft_schedule(rin["U"], weights["W1"], weights["W2"], rin["h"], weights["w"], weights["anchor"], w.seed,
-                          i, sps=sps, mode=w.mode, khist=khist, ws=ws, T_early=T)
+                          i, sps=sps, mode=w.mode, khist=khist, ws=ws, T_early=T, chain_stats=chain)
     torch.cuda.synchronize()
     st = ds.read_status(ws)
-    print(json.dumps({"profile_draft": w.name, "early_target_stats": T is not None, "status": st,
-                      "source_sha256_16": draft_source_hash()}))
+    rec = {"profile_draft": w.name, "early_target_stats": T is not None, "chain_target_stats": chain, "status": st,
+           "source_sha256_16": draft_source_hash()}
+    if chain and st == ds.OK:
+        # the rows j < gamma the accept chains of the third call (the one a
+        # capture with -s 2 -c 1 takes) reach: n_r + 1 per rejecting request,
+        # n_r per whole accept (the same round again, then its verification)
+        o = ds.draft_schedule(rin["U"], weights["W1"], weights["W2"], rin["h"], weights["w"], weights["anchor"],
+                              w.seed, 2, sps=sps, mode=w.mode, khist=torch.zeros(2, dtype=torch.int32, device=dev),
+                              ws=ws, T_early=T, chain_stats=True)
+        n, _ = ds.verify(rin["T"], rin["U"], weights["W1"], weights["W2"], weights["anchor"], o.x, o.p, o.lse, o.ell,
+                         w.seed, 2, ws, early_stats=True, scratch_from_draft=True)
+        n, ell = n.cpu(), o.ell.cpu()
+        rec["chain_rows"] = int(n.sum()) + int((n < ell).sum())
+        rec["algorithmic_bytes_per_launch"] = stage_bytes_per_launch(w, rows=rec["chain_rows"])
+        st = ds.read_status(ws)
+        rec["status"] = st
+    print(json.dumps(rec))
     if st != ds.OK:
         sys.exit(1)
 

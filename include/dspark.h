@@ -71,13 +71,15 @@ extern "C" {
 #define DSPARK_SCHED_GREEDY 1  /* greedy Theta maximisation with early stop */
 #define DSPARK_SCHED_TOPK 2    /* dynamic top-K, K = greedy count of round - 2 */
 
-/* flags of dspark_verify_ex and dspark_round_ex */
+/* flags of dspark_verify_ex, dspark_round_ex, dspark_draft_schedule_ex and
+ * dspark_acceptance_label_ex */
 #define DSPARK_EARLY_TARGET_STATS 1u  /* the draft took the target rows' softmax statistics */
 #define DSPARK_ADVANCE_ROUND 2u       /* the call's last kernel adds 1 to *round_dev */
 #define DSPARK_TARGET_STATS_FROM_VERIFY 4u  /* dspark_acceptance_label_ex: a verification left them */
 #define DSPARK_SCRATCH_FROM_DRAFT 8u  /* dspark_verify_ex: dspark_draft_schedule cleared the scratch */
 #define DSPARK_GATED_STATES 16u       /* dspark_verify_ex: the draft used the gated recurrent head */
 #define DSPARK_ALL_ROW_STATS 32u      /* verification takes the statistics of every row j < ell */
+#define DSPARK_CHAIN_TARGET_STATS 64u /* the draft takes the statistics of the rows the accept chains reach */
 
 /* Bytes of device scratch the entry points below need for these sizes; 0 when
  * a size is not positive. */
@@ -202,8 +204,11 @@ int dspark_verify(const float* T, const float* U, const void* W1, const void* W2
  *  - DSPARK_EARLY_TARGET_STATS: the workspace already holds the softmax
  *    statistics of the rows j < gamma of this T, left by
  *    dspark_markov_draft_ex(T_early = T) on the same workspace earlier in
- *    stream order; the call skips its own pass over those rows.  If no such
- *    draft preceded it, the kernels record DSPARK_ERR_INVALID.
+ *    stream order (or those of the rows the accept tests reach, left by
+ *    dspark_draft_schedule_ex with DSPARK_CHAIN_TARGET_STATS); the call skips
+ *    its own pass over those rows.  If no such draft preceded it, the kernels
+ *    record DSPARK_ERR_INVALID.  A row the tests use that holds a NaN or +inf
+ *    is reported as DSPARK_ERR_NONFINITE.
  *  - round_dev: the round index as a device word (see dspark_markov_draft_ex).
  *  - DSPARK_ADVANCE_ROUND (needs round_dev): the call's last kernel adds 1 to
  *    *round_dev after every kernel of the call has read it.
@@ -256,7 +261,8 @@ int dspark_acceptance_label(const float* T, const float* U, const void* W1, cons
  * gives dspark_acceptance_label, which streams the rows for them first):
  *  - DSPARK_EARLY_TARGET_STATS: left by dspark_markov_draft_ex(T_early = T)
  *    on the same workspace (rows j < gamma), with or without the verification
- *    that used them;
+ *    that used them; after a draft with DSPARK_CHAIN_TARGET_STATS, which
+ *    leaves only some rows, the kernel records DSPARK_ERR_INVALID;
  *  - DSPARK_TARGET_STATS_FROM_VERIFY: left by a dspark_verify_ex with
  *    DSPARK_ALL_ROW_STATS on the same workspace and T (rows j < ell[b]), with
  *    no draft on the workspace since; otherwise the kernel records
@@ -338,6 +344,34 @@ int dspark_draft_schedule(const float* U, const float* T_early, const void* W1, 
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dspark_draft_schedule with flags (0 gives it exactly):
+ *  - DSPARK_CHAIN_TARGET_STATS (needs T_early): take the statistics only of
+ *    the target rows the accept tests can reach ([blog] section 1: the tests
+ *    run along the prefix and stop at the first rejection).  The warps that
+ *    stream T go position by position; before row j of request b they run
+ *    the accept tests of b's positions 1..j that are decidable from what the
+ *    draft has published (x_k once every CTA is past position k, lse_t of row
+ *    k-1 once all its segments are out), and skip the row once a test fails
+ *    by a margin of 2^-8 relative.  A position not yet decidable counts as
+ *    accepted, so a row is skipped only when verification is certain to stop
+ *    before it; some rows past a rejection may still be read.  At the engine
+ *    point about a quarter of the rows j < gamma are read.  Verification then
+ *    takes DSPARK_EARLY_TARGET_STATS; dspark_acceptance_label_ex refuses
+ *    these statistics.  Other paths than the tensor-core persistent draft
+ *    take every row j < gamma.
+ * Other bits return DSPARK_ERR_INVALID.
+ */
+int dspark_draft_schedule_ex(const float* U, const float* T_early, const void* W1, const void* W2,
+                             int wdtype, const void* h, int hdtype, const float* w,
+                             const float* sts_T, const int32_t* anchor,
+                             int B, int gamma, int V, int r, int H,
+                             const float* sps, int n_sps, int mode, int32_t* khist,
+                             uint64_t seed, uint64_t round, uint64_t* round_dev, unsigned flags,
+                             int32_t* x_out, float* p_out, float* lse_out, float* c_out,
+                             int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * One whole round: dspark_draft_schedule, then dspark_verify_ex, enqueued in
  * that order on one stream with no host synchronisation.  Arguments as above.  A round
  * can be captured into a CUDA graph (the draft's cooperative launch
@@ -359,8 +393,11 @@ int dspark_round(const float* U, const float* T, const void* W1, const void* W2,
  * dspark_round with the options of the _ex calls: with
  * DSPARK_EARLY_TARGET_STATS the draft takes the statistics of T's rows
  * j < gamma while it runs (T is an input of the round) and verification
- * skips its own pass over them; with DSPARK_ALL_ROW_STATS verification takes
- * the statistics of every row j < ell[b] (see dspark_verify_ex); with round_dev the round index is the device
+ * skips its own pass over them; with DSPARK_CHAIN_TARGET_STATS the draft
+ * takes only the rows the accept tests reach (see dspark_draft_schedule_ex)
+ * and verification decides on them; with DSPARK_ALL_ROW_STATS verification
+ * takes the statistics of every row j < ell[b] (see dspark_verify_ex); at
+ * most one of the three (else DSPARK_ERR_INVALID); with round_dev the round index is the device
  * word *round_dev (`round` ignored), and DSPARK_ADVANCE_ROUND makes the
  * round's last kernel add 1 to it, so that replaying one captured graph runs
  * consecutive rounds (the caller refreshes U, T, h and the anchors in place

@@ -25,6 +25,7 @@ F32, BF16 = 0, 1
 SCHED_FIXED, SCHED_GREEDY, SCHED_TOPK = 0, 1, 2
 EARLY_TARGET_STATS, ADVANCE_ROUND, TARGET_STATS_FROM_VERIFY, SCRATCH_FROM_DRAFT, GATED_STATES = 1, 2, 4, 8, 16
 ALL_ROW_STATS = 32
+CHAIN_TARGET_STATS = 64
 
 
 class DSparkError(RuntimeError):
@@ -87,6 +88,10 @@ def _load():
     L.dspark_draft_schedule.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32,
                                         i32, vp, u64, u64, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_draft_schedule.restype = i32
+    L.dspark_draft_schedule_ex.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                           i32, i32, vp, u64, u64, vp, ctypes.c_uint, vp, vp, vp, vp, vp, vp, vp,
+                                           vp, sz, vp]
+    L.dspark_draft_schedule_ex.restype = i32
     L.dspark_read_status.argtypes = [vp, ctypes.POINTER(i32), vp]
     L.dspark_read_status.restype = i32
     L.dspark_selftest_wait_timeout.argtypes = [i32, vp, sz, vp]
@@ -416,30 +421,36 @@ def _round_args(U, T, W1, W2, h, w, anchor, sps, khist, sts_T):
 
 
 def draft_schedule(U, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
-                   out=None, ws=None, T_early=None, round_dev=None):
+                   out=None, ws=None, T_early=None, round_dev=None, chain_stats=False):
     """The first stage of a round (draft, confidence head, schedule; one
     persistent launch on the tensor-core path) into out.x, p, lse, c, ell,
     nstar, theta.  T_early: target logits whose statistics the draft takes
-    along.  Returns the RoundOutputs."""
+    along (chain_stats: only of the rows the accept tests can reach; verify
+    with early_stats=True either way).  Returns the RoundOutputs."""
     L = _load()
+    if chain_stats and T_early is None:
+        raise ValueError("chain_stats needs T_early")
     dev, B, G, V, r, H = _round_args(U, T_early, W1, W2, h, w, anchor, sps, khist, sts_T)
     out = RoundOutputs(B, G, dev) if out is None else out
     out.check(B, G, dev)
     ws = workspace(B, G, V, dev) if ws is None else ws
     n_sps = 0 if sps is None else sps.numel()
     rd = _round_dev(round_dev, dev)
-    _check(L.dspark_draft_schedule(_ptr(U), _ptr(T_early), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h), _dt(h, "h"),
-                                   _ptr(w), _ptr(sts_T), _ptr(anchor), B, G, V, r, H, _ptr(sps), n_sps, mode,
-                                   _ptr(khist), seed, rnd, rd, _ptr(out.x), _ptr(out.p), _ptr(out.lse), _ptr(out.c),
-                                   _ptr(out.ell), _ptr(out.nstar), _ptr(out.theta), _ptr(ws), ws.numel(),
-                                   _stream(dev)), "draft_schedule")
+    _check(L.dspark_draft_schedule_ex(_ptr(U), _ptr(T_early), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h),
+                                      _dt(h, "h"), _ptr(w), _ptr(sts_T), _ptr(anchor), B, G, V, r, H, _ptr(sps),
+                                      n_sps, mode, _ptr(khist), seed, rnd, rd,
+                                      CHAIN_TARGET_STATS if chain_stats else 0, _ptr(out.x), _ptr(out.p),
+                                      _ptr(out.lse), _ptr(out.c), _ptr(out.ell), _ptr(out.nstar), _ptr(out.theta),
+                                      _ptr(ws), ws.numel(), _stream(dev)), "draft_schedule")
     return out
 
 
 def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, khist=None, sts_T=None,
-          out=None, ws=None, early_stats=False, round_dev=None, advance_round=False, all_row_stats=False):
+          out=None, ws=None, early_stats=False, round_dev=None, advance_round=False, all_row_stats=False,
+          chain_stats=False):
     """One whole round (draft, confidence, schedule, verify) on U's device.
     early_stats: the draft takes the target rows' statistics while it runs.
+    chain_stats: the draft takes those of the rows the accept tests reach.
     all_row_stats: verification takes the statistics of every row j < ell
     (otherwise only the rows the accept tests reach).
     round_dev / advance_round: the round index as a device int64 [1] (rnd
@@ -454,7 +465,7 @@ def round(U, T, W1, W2, h, w, anchor, seed, rnd=0, sps=None, mode=SCHED_GREEDY, 
     n_sps = 0 if sps is None else sps.numel()
     rd = _round_dev(round_dev, dev)
     flags = ((EARLY_TARGET_STATS if early_stats else 0) | (ADVANCE_ROUND if advance_round else 0) |
-             (ALL_ROW_STATS if all_row_stats else 0))
+             (ALL_ROW_STATS if all_row_stats else 0) | (CHAIN_TARGET_STATS if chain_stats else 0))
     _check(L.dspark_round_ex(_ptr(U), _ptr(T), _ptr(W1), _ptr(W2), _dt(W1, "W1"), _ptr(h), _dt(h, "h"), _ptr(w),
                              _ptr(sts_T), _ptr(anchor), B, G, V, r, H, _ptr(sps), n_sps, mode, _ptr(khist), seed,
                              rnd, rd, flags, _ptr(out.x), _ptr(out.p), _ptr(out.lse), _ptr(out.c), _ptr(out.ell),

@@ -235,14 +235,17 @@ int dspark_acceptance_label(const float* T, const float* U, const void* W1, cons
                                     workspace, workspace_bytes, stream);
 }
 
-int dspark_draft_schedule(const float* U, const float* T_early, const void* W1, const void* W2, int wdtype,
-                          const void* h, int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B,
-                          int gamma, int V, int r, int H, const float* sps, int n_sps, int mode, int32_t* khist,
-                          uint64_t seed, uint64_t round, uint64_t* round_dev, int32_t* x_out, float* p_out,
-                          float* lse_out, float* c_out, int32_t* ell_out, int32_t* nstar_out, double* theta_out,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+int dspark_draft_schedule_ex(const float* U, const float* T_early, const void* W1, const void* W2, int wdtype,
+                             const void* h, int hdtype, const float* w, const float* sts_T, const int32_t* anchor,
+                             int B, int gamma, int V, int r, int H, const float* sps, int n_sps, int mode,
+                             int32_t* khist, uint64_t seed, uint64_t round, uint64_t* round_dev, unsigned flags,
+                             int32_t* x_out, float* p_out, float* lse_out, float* c_out, int32_t* ell_out,
+                             int32_t* nstar_out, double* theta_out, void* workspace, size_t workspace_bytes,
+                             void* stream) {
   DSPARK_TRY(draft_checks(U, W1, W2, wdtype, anchor, B, gamma, V, r, x_out, p_out, lse_out, workspace,
                           workspace_bytes));
+  if (flags & ~(unsigned)DSPARK_CHAIN_TARGET_STATS) return DSPARK_ERR_INVALID;
+  if ((flags & DSPARK_CHAIN_TARGET_STATS) && !T_early) return DSPARK_ERR_INVALID;
   DSPARK_TRY(confidence_checks(h, hdtype, W1, wdtype, w, anchor, x_out, B, gamma, H, r, V, c_out));
   DSPARK_TRY(schedule_checks(c_out, B, gamma, sps, n_sps, mode, khist, ell_out, nstar_out, theta_out));
   if (round >= (1ull << 29)) return DSPARK_ERR_INVALID;
@@ -258,6 +261,7 @@ int dspark_draft_schedule(const float* U, const float* T_early, const void* W1, 
   DraftArgs da{U, W1, W2, wdtype, anchor, B, gamma, V, r, key, x_out, p_out, lse_out, workspace, T_early, tc,
                h, hdtype, w, sts_T, H, tc ? c_out : nullptr, sps, mode, khist, tc ? ell_out : nullptr, nstar_out,
                theta_out};
+  da.chain_stats = (flags & DSPARK_CHAIN_TARGET_STATS) != 0;
   DSPARK_TRY(cuda_status(launch_markov_draft(da, s)));
   if (!tc) {
     DSPARK_TRY(cuda_status(launch_confidence(h, hdtype, W1, wdtype, w, sts_T, anchor, x_out, B, gamma, H, r, V,
@@ -268,6 +272,17 @@ int dspark_draft_schedule(const float* U, const float* T_early, const void* W1, 
   return DSPARK_OK;
 }
 
+int dspark_draft_schedule(const float* U, const float* T_early, const void* W1, const void* W2, int wdtype,
+                          const void* h, int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B,
+                          int gamma, int V, int r, int H, const float* sps, int n_sps, int mode, int32_t* khist,
+                          uint64_t seed, uint64_t round, uint64_t* round_dev, int32_t* x_out, float* p_out,
+                          float* lse_out, float* c_out, int32_t* ell_out, int32_t* nstar_out, double* theta_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return dspark_draft_schedule_ex(U, T_early, W1, W2, wdtype, h, hdtype, w, sts_T, anchor, B, gamma, V, r, H, sps,
+                                  n_sps, mode, khist, seed, round, round_dev, 0u, x_out, p_out, lse_out, c_out, ell_out,
+                                  nstar_out, theta_out, workspace, workspace_bytes, stream);
+}
+
 int dspark_round_ex(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,
                     int hdtype, const float* w, const float* sts_T, const int32_t* anchor, int B, int gamma, int V,
                     int r, int H, const float* sps, int n_sps, int mode, int32_t* khist, uint64_t seed,
@@ -276,17 +291,23 @@ int dspark_round_ex(const float* U, const float* T, const void* W1, const void* 
                     int32_t* n_out, int32_t* tok_out, void* workspace, size_t workspace_bytes, void* stream) {
   DSPARK_TRY(verify_checks(T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, n_out,
                            tok_out, workspace, workspace_bytes));
-  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND | DSPARK_ALL_ROW_STATS))
+  if (flags & ~(unsigned)(DSPARK_EARLY_TARGET_STATS | DSPARK_ADVANCE_ROUND | DSPARK_ALL_ROW_STATS |
+                          DSPARK_CHAIN_TARGET_STATS))
     return DSPARK_ERR_INVALID;
-  if ((flags & DSPARK_EARLY_TARGET_STATS) && (flags & DSPARK_ALL_ROW_STATS)) return DSPARK_ERR_INVALID;
+  const unsigned forms = flags & (DSPARK_EARLY_TARGET_STATS | DSPARK_ALL_ROW_STATS | DSPARK_CHAIN_TARGET_STATS);
+  if (forms & (forms - 1)) return DSPARK_ERR_INVALID;   // at most one of the three
   if ((flags & DSPARK_ADVANCE_ROUND) && !round_dev) return DSPARK_ERR_INVALID;
-  const bool early = (flags & DSPARK_EARLY_TARGET_STATS) != 0;
-  DSPARK_TRY(dspark_draft_schedule(U, early ? T : nullptr, W1, W2, wdtype, h, hdtype, w, sts_T, anchor, B, gamma, V,
-                                   r, H, sps, n_sps, mode, khist, seed, round, round_dev, x_out, p_out, lse_out,
-                                   c_out, ell_out, nstar_out, theta_out, workspace, workspace_bytes, stream));
+  // the draft takes the target rows' statistics (every row j < gamma, or the
+  // rows the accept chains reach) and verification decides on them
+  const bool early = (flags & (DSPARK_EARLY_TARGET_STATS | DSPARK_CHAIN_TARGET_STATS)) != 0;
+  DSPARK_TRY(dspark_draft_schedule_ex(U, early ? T : nullptr, W1, W2, wdtype, h, hdtype, w, sts_T, anchor, B, gamma,
+                                      V, r, H, sps, n_sps, mode, khist, seed, round, round_dev,
+                                      flags & DSPARK_CHAIN_TARGET_STATS, x_out, p_out, lse_out, c_out, ell_out,
+                                      nstar_out, theta_out, workspace, workspace_bytes, stream));
+  unsigned vflags = (flags & ~(unsigned)DSPARK_CHAIN_TARGET_STATS) | DSPARK_SCRATCH_FROM_DRAFT;
+  if (early) vflags |= DSPARK_EARLY_TARGET_STATS;
   return dspark_verify_ex(T, U, W1, W2, wdtype, anchor, x_out, p_out, lse_out, ell_out, B, gamma, V, r, seed, round,
-                          round_dev, flags | DSPARK_SCRATCH_FROM_DRAFT, n_out, tok_out, workspace, workspace_bytes,
-                          stream);
+                          round_dev, vflags, n_out, tok_out, workspace, workspace_bytes, stream);
 }
 
 int dspark_round(const float* U, const float* T, const void* W1, const void* W2, int wdtype, const void* h,

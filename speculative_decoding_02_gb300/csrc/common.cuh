@@ -259,10 +259,13 @@ constexpr int kKeyStride = 16;   // u64 slots per key
 
 struct WsLayout {
   size_t status;      // int32 status word
-  size_t counters;    // int32 [8]: [0] verify row count, [1] draft grid barrier, [2] target-row
+  size_t counters;    // int32 [8]: [0] verify row count, [1] unused, [2] target-row
                       // statistics: tasks taken (>= B*gamma*nsegs once rows j < gamma are done),
                       // [3] draft CTAs past the finalize, [4] 1 while the row partials hold
-                      // verification's statistics of every row j < ell (cleared by every draft)
+                      // verification's statistics of every row j < ell (cleared by every draft),
+                      // [5] 1 when a draft took only the rows the accept chains can reach; word
+                      // 32 (its own 128-byte line, away from the task counter's atomics): the
+                      // draft's grid-barrier counter
   size_t draft_keys;  // u64 [gamma][B], kKeyStride apart
   size_t draft_part;  // float2 [gamma][B][nslices]
   size_t rows;        // int32 [B*gamma] row ids b*(gamma+1)+j (j < ell_b) of the rows whose stats verify needs
@@ -275,6 +278,9 @@ struct WsLayout {
   size_t resid_prev;  // int32 [B] x_{k*-1} as stored (the anchor when k* = 1)
   size_t tx;          // float [B*gamma] T[b, k-1, x_k], gathered by a draft that takes T along
   size_t gstate;      // bf16 [B][gamma][256] the gated head's states s_k (tensor-core path)
+  size_t chain_stats; // int32 [B] first position known to reject (0: none), int32 [B] positions
+                      // known not to reject, u32 [B*(gamma+1)] segments of each row written: a
+                      // draft that takes the statistics of the rows the accept chains reach
   size_t bonus_rows;  // int32 [1 + B]: count, then the requests that accepted their whole prefix
   size_t fin_count;   // u32 [2]: CTAs of the bonus race and of the residual that are done
   size_t chain_next;  // u32: requests verify_chain's clusters have taken
@@ -288,7 +294,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   size_t off = 0;
   const size_t rows = (size_t)B * (gamma + 1);
   L.status = off;      off = align256(off + 4);
-  L.counters = off;    off = align256(off + 32);
+  L.counters = off;    off = align256(off + 4 * 33);
   L.draft_keys = off;  off = align256(off + 8ull * kKeyStride * gamma * B);
   L.draft_part = off;  off = align256(off + 8ull * gamma * draft_part_slices(V) * B);
   L.rows = off;        off = align256(off + 4ull * rows);
@@ -305,6 +311,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int gamma, int V) {
   L.resid_prev = off;  off = align256(off + 4ull * B);
   L.tx = off;          off = align256(off + 4ull * B * gamma);
   L.gstate = off;      off = align256(off + 2ull * 256 * B * gamma);
+  L.chain_stats = off; off = align256(off + 4ull * (2 * B + rows));
   L.total = off;
   return L;
 }

@@ -197,10 +197,11 @@ cudaError_t run_draft(const DraftArgs& a, cudaStream_t stream) {
 cudaError_t launch_markov_draft(const DraftArgs& a, cudaStream_t stream) {
   if (draft_tc_supported(a.wdtype, a.r, a.V)) return launch_markov_draft_tc(a, stream);
   // the target-statistics marker (set again below when this call takes the
-  // statistics) and the marker of verification's full row pass are cleared
-  // by every draft
+  // statistics), the marker of verification's full row pass and the marker of
+  // statistics taken along the accept chains only (this path takes every row)
+  // are cleared by every draft
   const WsLayout L = ws_layout(a.B, a.gamma, a.V);
-  cudaError_t e = cudaMemsetAsync(ws_ptr<unsigned int>(a.ws, L.counters) + 2, 0, 3 * sizeof(unsigned int), stream);
+  cudaError_t e = cudaMemsetAsync(ws_ptr<unsigned int>(a.ws, L.counters) + 2, 0, 4 * sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;
   e = a.wdtype == DSPARK_BF16 ? run_draft<DSPARK_BF16>(a, stream) : run_draft<DSPARK_F32>(a, stream);
   if (e == cudaSuccess && a.T_stats != nullptr) e = launch_row_stats(a.T_stats, nullptr, a.B, a.gamma, a.V, a.ws, stream);

@@ -162,6 +162,12 @@ struct StepParams {
   float* tx;                            // [B][G] T[b, k-1, x_k] from the finalize (with T_stats)
   float2* stats_part;
   unsigned int* stats_next;
+  // with T_stats: only the rows the accept chains can reach (chain_rej null:
+  // every row j < G); chain_mark is set to 1 when so
+  int* chain_rej;                       // [B] first position known to reject (0: none yet)
+  int* chain_pass;                      // [B] positions 1..chain_pass[b] known not to reject
+  unsigned int* rows_done;              // [B*(G+1)] segments of each row's partials written
+  int* chain_mark;
   unsigned long long* keys;             // [G][B] argmax keys of every position, kKeyStride apart
   float2* part;                         // [G][part_slices][B] softmax partials
   unsigned int* gbar;                   // grid-barrier counter (zeroed before launch)
@@ -700,15 +706,158 @@ __device__ __forceinline__ void stats_task_at(int t, int G, int nsegs, size_t& r
   rowid = (size_t)b * (G + 1) + j;
 }
 
+// (max, sum of exp) partial merge with one 2^x on the special-function unit,
+// kept small: the accept tests below run beside the draft's epilogue warps,
+// and every instruction they bring in competes with the epilogue's own for
+// the SM's instruction cache.
+__device__ __forceinline__ void chain_merge(float& m, float& s, float m2, float s2) {
+  if (m2 > m) {
+    const float tm = m, ts = s;
+    m = m2; s = s2; m2 = tm; s2 = ts;
+  }
+  if (m2 > -INFINITY) s += s2 * ex2_approx((m2 - m) * kLog2e);
+}
+
+// The accept test of position m of request b, run by one warp on what the
+// draft has published so far ([blog] section 1: accept x_m when u < p_t(x_m)
+// / p_d(x_m), u the verification's uniform of stream 1 at (b, m)).  Returns
+// -1 while an input is not out yet (lse_d of position m needs every CTA's
+// softmax partial of m, which a CTA writes after its arrival at the grid
+// barrier of m and before its next arrival -- at the barrier of m + 1, or
+// the finalize's after the last position; lse_t of row m-1 needs every
+// segment of that row), -2 when the
+// test cannot be run (a non-finite ratio or a bad token: verification sees
+// to it), 1 when the test fails with a margin of 2^-8 relative, 0 otherwise.
+// p_d comes from the draft's partials and the fused logit of x_m as the
+// finalize forms them, p_t from the row's partials as verify_decide merges
+// them; the margin covers the rounding of the two and of the special-function
+// unit's 2^x and log2, so that a position called rejected here is rejected
+// there too.  Lane 0 reads the readiness with plain loads, acquires once it
+// sees it, and takes the decision for the warp (the lanes' reductions may
+// differ in their last bit).
+__device__ __forceinline__ int chain_test(const StepParams* __restrict__ p, const RngKey& key, int b, int m,
+                                          int lane) {
+  const int B = p->B, G = p->G, V = p->V, nsegs = p->nsegs;
+  const size_t rowid = (size_t)b * (G + 1) + (m - 1);
+  int ready = 0;
+  if (lane == 0) {
+    ready = *reinterpret_cast<const volatile unsigned int*>(p->gbar) >=
+                (uint32_t)p->nctas * (uint32_t)min(m + 1, G) &&
+            *reinterpret_cast<const volatile unsigned int*>(p->rows_done + rowid) >= (uint32_t)nsegs;
+    if (ready) {
+      // acquire what the arrivals and the segment counts released
+      (void)ld_acquire_u32(p->gbar);
+      (void)ld_acquire_u32(p->rows_done + rowid);
+    }
+  }
+  ready = __shfl_sync(0xffffffffu, ready, 0);
+  __syncwarp();
+  if (!ready) return -1;
+  const float2* pp = p->part + (size_t)(m - 1) * p->part_slices * B + (size_t)b * p->part_slices;
+  float md = -INFINITY, sd = 0.f;
+#pragma unroll 1
+  for (int i = lane; i < p->ctas_per_mtile; i += 32) {
+    const float2 pr = __ldcg(pp + i);
+    chain_merge(md, sd, pr.x, pr.y);
+  }
+#pragma unroll 1
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, md, off), s2 = __shfl_xor_sync(0xffffffffu, sd, off);
+    chain_merge(md, sd, m2, s2);
+  }
+  const unsigned long long kk = __ldcg(p->keys + ((size_t)(m - 1) * B + b) * kKeyStride);
+  const int x = kk ? argmax_key_index(kk) : -1;
+  int prev = p->anchor[b];
+  if (m > 1) {
+    const unsigned long long kp = __ldcg(p->keys + ((size_t)(m - 2) * B + b) * kKeyStride);
+    prev = kp ? argmax_key_index(kp) : -1;
+  }
+  if (x < 0 || x >= V || prev < 0 || prev >= V) return -2;   // (the same on every lane)
+  const __nv_bfloat16* erow =
+      p->gate_g != nullptr ? p->S + ((size_t)b * G + (m - 1)) * KR : p->W1 + (size_t)prev * KR;
+  // this lane's 8 of the 256 products (one 16-byte load per row)
+  const uint4 e8 = __ldcg(reinterpret_cast<const uint4*>(erow) + lane);
+  const uint4 w8 = __ldg(reinterpret_cast<const uint4*>(p->W2 + (size_t)x * KR) + lane);
+  const __nv_bfloat162* ea = reinterpret_cast<const __nv_bfloat162*>(&e8);
+  const __nv_bfloat162* wa = reinterpret_cast<const __nv_bfloat162*>(&w8);
+  float dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 ef = __bfloat1622float2(ea[i]), wf = __bfloat1622float2(wa[i]);
+    dot = fmaf(ef.x, wf.x, fmaf(ef.y, wf.y, dot));
+  }
+#pragma unroll 1
+  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  int res = -2;
+  if (lane == 0) {
+    float mt = -INFINITY, st = 0.f;
+#pragma unroll 1
+    for (int i = 0; i < nsegs; ++i) {
+      const float2 q2 = __ldcg(p->stats_part + rowid * nsegs + i);
+      chain_merge(mt, st, q2.x, q2.y);
+    }
+    // p_t / p_d in base 2 on the special-function unit (within the margin)
+    const float l2d = (p->U[((size_t)b * G + (m - 1)) * V + x] + dot - md) * kLog2e - lg2_approx(sd);
+    const float l2t = (p->T_stats[rowid * V + x] - mt) * kLog2e - lg2_approx(st);
+    const float ratio = ex2_approx(l2t - l2d);
+    if (sd > 0.f && st > 0.f && ratio >= 0.f) {   // (sums that a row can have; not NaN)
+      const uint4 rw = rng4(key, kStreamAccept, (uint32_t)b, (uint32_t)m, 0u);
+      res = uniform01(rw.x) >= ratio * (1.0f + 0x1p-8f) ? 1 : 0;
+    }
+  }
+  return __shfl_sync(0xffffffffu, res, 0);
+}
+
+// Whether row j of request b can be reached by the accept tests: no position
+// 1..j is known to reject.  Positions are tested in order and the outcome is
+// kept per request.  A test whose inputs are not out yet, or that cannot be
+// run, counts as reachable: the row is taken ahead of its decision (waiting
+// for the draft's barriers instead left the rows of the long chains for
+// after the draft), so a row is skipped only once verification is certain to
+// stop before it.  Out of line and small, as chain_merge.  Warp-uniform.
+__device__ __noinline__ bool chain_row_needed(const StepParams* __restrict__ p, const RngKey key, int b, int j,
+                                              int lane) {
+#pragma unroll 1
+  for (int guard = 0; guard <= j; ++guard) {
+    int rej = 0, pass = 0;
+    if (lane == 0) {
+      rej = *reinterpret_cast<volatile int*>(p->chain_rej + b);
+      pass = *reinterpret_cast<volatile int*>(p->chain_pass + b);
+    }
+    rej = __shfl_sync(0xffffffffu, rej, 0);
+    pass = __shfl_sync(0xffffffffu, pass, 0);
+    if (rej != 0 && rej <= j) return false;
+    if (pass >= j) return true;
+    const int m = pass + 1;
+    const int res = chain_test(p, key, b, m, lane);
+    if (res < 0) return true;
+    if (res == 1) {
+      if (lane == 0) atomicCAS(p->chain_rej + b, 0, m);
+      return false;
+    }
+    if (lane == 0) atomicMax(p->chain_pass + b, m);
+  }
+  return true;
+}
+
 // One warp, whole tasks with its own loads: kStatsLoadsWarp float4 per lane
 // per piece, all in flight before any arithmetic, marked for early eviction
 // from L2 (W2, which every draft position re-reads from L2, must not be
 // pushed out by a stream read once).  The next task index is fetched while a
-// task runs.
-__device__ void stats_tasks(const float* __restrict__ T, int B, int G, int V, int nsegs,
-                            float2* __restrict__ part, unsigned int* next, volatile int* abort, int* status) {
+// task runs.  With chain_rej the tasks go position by position (every
+// request's row 0, then row 1, ...), rows no accept test will reach are
+// skipped, each finished segment is counted in rows_done, and non-finite
+// entries are left to verification, which checks the rows its tests use (a
+// row read here ahead of its request's rejection is not one of them).
+__device__ __forceinline__ void stats_tasks(const StepParams* __restrict__ p, const RngKey& key,
+                                            volatile int* abort) {
+  const float* __restrict__ T = p->T_stats;
+  const int B = p->B, G = p->G, V = p->V, nsegs = p->nsegs;
+  float2* __restrict__ part = p->stats_part;
+  unsigned int* next = p->stats_next;
   const int lane = threadIdx.x & 31;
   const int ntasks = B * G * nsegs;
+  const bool chain = p->chain_rej != nullptr;
   const uint64_t pol = policy_evict_first();
   bool bad = false;
   unsigned int t = 0;
@@ -719,7 +868,18 @@ __device__ void stats_tasks(const float* __restrict__ T, int B, int G, int V, in
     if (lane == 0) t_next = atomicAdd(next, 1u);   // its reply is needed only at the next task
     size_t rowid;
     int seg;
-    stats_task_at((int)t, G, nsegs, rowid, seg);
+    if (chain) {
+      const int ri = (int)t / nsegs;
+      seg = (int)t - ri * nsegs;
+      const int j = ri / B, b = ri - j * B;
+      rowid = (size_t)b * (G + 1) + j;
+      if (j > 0 && !chain_row_needed(p, key, b, j, lane)) {
+        t = __shfl_sync(0xffffffffu, t_next, 0);
+        continue;
+      }
+    } else {
+      stats_task_at((int)t, G, nsegs, rowid, seg);
+    }
     const float* row = T + rowid * V;
     const int v0 = seg * kStatsSeg, v1 = min(V, v0 + kStatsSeg);
     float m = -INFINITY, s = 0.f;
@@ -734,10 +894,15 @@ __device__ void stats_tasks(const float* __restrict__ T, int B, int G, int V, in
       stats_fold(m, s, x, bad);
     }
     warp_softmax_reduce(m, s, 0xffffffffu, 32);
-    if (lane == 0) part[rowid * nsegs + seg] = make_float2(m, s);
+    if (lane == 0) {
+      part[rowid * nsegs + seg] = make_float2(m, s);
+      // the segment count is a release add: the partial above is visible to
+      // whoever acquires the count
+      if (chain) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p->rows_done + rowid) : "memory");
+    }
     t = __shfl_sync(0xffffffffu, t_next, 0);
   }
-  if (bad) record_status(status, DSPARK_ERR_NONFINITE);
+  if (bad && !chain) record_status(p->status, DSPARK_ERR_NONFINITE);
 }
 
 // The draft outputs of one (request, position), by one warp: merge the slice
@@ -816,7 +981,7 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
 template <int R, int MODE>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1)
 draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
-              const StepParams p) {
+              const __grid_constant__ StepParams p) {
   constexpr int kRepl = BM / R;            // copies of each request row
   constexpr int kParts = 4 * kRepl;        // column parts of a tile
   constexpr int CPP = BN / kParts;         // columns per thread per tile
@@ -840,6 +1005,7 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
   volatile int* abort = &bars->abort;
   const RngKey key = live_key(p.key);
   if constexpr (MODE == kDraft) {
+    if (p.chain_mark != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *p.chain_mark = 1;
     if (p.vz != nullptr) {
       for (int i = blockIdx.x * threads_of<MODE>() + threadIdx.x; i < p.vz_words; i += gridDim.x * threads_of<MODE>())
         p.vz[i] = 0ull;
@@ -1386,14 +1552,14 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       // the draft is done: the epilogue warps help with whatever target-row
       // statistics are left
       if (p.T_stats != nullptr)
-        stats_tasks(p.T_stats, p.B, p.G, p.V, p.nsegs, p.stats_part, p.stats_next, abort, p.status);
+        stats_tasks(&p, key, abort);
     }
   } else {
     // ------------------------------------------------------------ statistics
     // (draft mode only: the warps past the epilogue).  Their loads bypass the
     // SM's bulk-copy engine, which the draft's U and W2 tiles keep busy.
     if (p.T_stats != nullptr)
-      stats_tasks(p.T_stats, p.B, p.G, p.V, p.nsegs, p.stats_part, p.stats_next, abort, p.status);
+      stats_tasks(&p, key, abort);
   }
 
   tc_fence_before();
@@ -1527,7 +1693,8 @@ bool draft_tc_supported(int wdtype, int r, int V) { return wdtype == DSPARK_BF16
 cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   const WsLayout L = ws_layout(a.B, a.gamma, a.V);
   int* status = ws_ptr<int>(a.ws, L.status);
-  unsigned int* gbar = ws_ptr<unsigned int>(a.ws, L.counters) + 1;
+  unsigned int* ctr = ws_ptr<unsigned int>(a.ws, L.counters);
+  unsigned int* gbar = ctr + 32;   // the grid-barrier counter, on a line of its own
   unsigned long long* keys = ws_ptr<unsigned long long>(a.ws, L.draft_keys);
   float2* part = ws_ptr<float2>(a.ws, L.draft_part);
   const int part_slices = draft_part_slices(a.V);
@@ -1547,9 +1714,11 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * kKeyStride * (size_t)a.gamma * a.B, stream);
   if (e != cudaSuccess) return e;
-  // the grid-barrier counter, the target-statistics task counter, the count
-  // of CTAs past the finalize and the marker of verification's full row pass
-  if ((e = cudaMemsetAsync(gbar, 0, 4 * sizeof(unsigned int), stream)) != cudaSuccess) return e;
+  // the target-statistics task counter, the count of CTAs past the
+  // finalize, the marker of verification's full row pass, the marker of
+  // statistics taken along the accept chains only and the grid-barrier
+  // counter (words 1..32)
+  if ((e = cudaMemsetAsync(ctr + 1, 0, 32 * sizeof(unsigned int), stream)) != cudaSuccess) return e;
 
   const int mtiles = div_up(a.B, R);
   const int ntiles = div_up(a.V, BN);
@@ -1573,7 +1742,7 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   sp.key = a.key;
   sp.nsegs = stats_num_segs(a.V);
   sp.stats_part = ws_ptr<float2>(a.ws, L.row_part);
-  sp.stats_next = gbar + 1;
+  sp.stats_next = ctr + 2;
   sp.tx = ws_ptr<float>(a.ws, L.tx);
   if (a.gate_g != nullptr) {
     sp.gate_g = a.gate_g;
@@ -1602,11 +1771,22 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
     // candidates each) and its keys and values fit the idle rings
     if (want_sched && (long long)a.B * a.gamma <= 8 * kEpiWarps * 32 &&
         schedule_smem_bytes(a.B, a.gamma) <= (size_t)kRingBytes) {
-      sp.sched = SchedArgs{a.c_out, a.sps, a.mode, a.khist, a.ell_out, a.nstar_out, a.theta_out, gbar + 2};
+      sp.sched = SchedArgs{a.c_out, a.sps, a.mode, a.khist, a.ell_out, a.nstar_out, a.theta_out, ctr + 3};
       sched_fused = true;
     }
-    // the target-row statistics ride along in the statistics warps
+    // the target-row statistics ride along in the statistics warps, of every
+    // row j < gamma or of the rows the accept chains can reach
     sp.T_stats = a.T_stats;
+    if (a.T_stats != nullptr && a.chain_stats) {
+      int* cst = ws_ptr<int>(a.ws, L.chain_stats);
+      if ((e = cudaMemsetAsync(cst, 0, sizeof(int) * (2 * (size_t)a.B + (size_t)a.B * (a.gamma + 1)), stream)) !=
+          cudaSuccess)
+        return e;
+      sp.chain_rej = cst;
+      sp.chain_pass = cst + a.B;
+      sp.rows_done = reinterpret_cast<unsigned int*>(cst + 2 * a.B);
+      sp.chain_mark = reinterpret_cast<int*>(ctr) + 5;
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(nctas);
     cfg.blockDim = dim3(kDraftThreads);

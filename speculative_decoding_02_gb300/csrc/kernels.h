@@ -73,6 +73,10 @@ struct DraftArgs {
   // head); tensor-core path only, its states go to the workspace
   const float* gate_g;
   const float* gate_c;
+  // with T_stats, tensor-core persistent path: only the rows the accept
+  // chains can reach (a row is skipped once its request is known to reject
+  // at an earlier position); workspace counter [5] then reads 1
+  bool chain_stats;
 };
 
 struct VerifyArgs {

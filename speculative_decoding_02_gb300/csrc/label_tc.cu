@@ -82,7 +82,8 @@ struct LabelParams {
   const float2* row_part;    // [B*(G+1)][nsegs] target-row partials
   int nsegs;
   int tail_tile;             // tile staged as [R x 32] boxes (V % 32 != 0), else -1
-  const int* stats_done;     // row segments a draft took (nullptr: not checked)
+  const int* stats_done;     // row segments a draft took (nullptr: not checked); the word after the
+                             // next is 1 when that draft took only the rows the accept chains reach
   const int* full_rows;      // 1 while verification's statistics cover every row j < ell (nullptr: not checked)
   float* label;              // [B][G], zeroed by the caller
   int* status;
@@ -144,7 +145,8 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0 && p.stats_done && *p.stats_done < p.B * p.G * p.nsegs)
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.stats_done &&
+      (*p.stats_done < p.B * p.G * p.nsegs || p.stats_done[3] != 0))
     record_status(p.status, DSPARK_ERR_INVALID);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.full_rows && *p.full_rows != 1)
     record_status(p.status, DSPARK_ERR_INVALID);
@@ -351,9 +353,10 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
 // The acceptance label of every verified position in one persistent launch
 // (label zeroed by the caller; row_part holds the target rows' partials, nsegs
 // per row; stats_done, when given, is the draft's count of row segments taken,
-// and a short count is reported as DSPARK_ERR_INVALID; full_rows, when given,
-// is the marker of verification's pass over every row j < ell, and a marker
-// other than 1 is reported the same way).
+// and a short count, or the marker three words further of a draft that took
+// only the rows the accept chains reach, is reported as DSPARK_ERR_INVALID;
+// full_rows, when given, is the marker of verification's pass over every row
+// j < ell, and a marker other than 1 is reported the same way).
 cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const void* W1, const void* W2,
                                        const int32_t* anchor, const int32_t* x, const float* lse_d,
                                        const int32_t* ell, const float2* row_part, int nsegs,

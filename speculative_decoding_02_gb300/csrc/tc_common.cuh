@@ -335,6 +335,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// log2(x) on the special-function unit (absolute error about 2^-22 near 1).
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -385,6 +385,12 @@ __global__ void verify_decide(const float* __restrict__ T, const int32_t* __rest
   }
   const unsigned ballot = __ballot_sync(0xffffffffu, reject);
   const int n = ballot ? (__ffs(ballot) - 1) : L;
+  // the rows the tests used (rows 0..n, row n only when position n + 1 was
+  // tested) must be finite; rows past them may never have been read (a draft
+  // that took only the rows the accept chains reach)
+  const unsigned used = n < L ? (n >= 31 ? 0xffffffffu : (2u << n) - 1u) : (L >= 32 ? 0xffffffffu : (1u << L) - 1u);
+  if ((__ballot_sync(0xffffffffu, lane < L && !(lse_t < INFINITY)) & used) && lane == 0)
+    record_status(status, DSPARK_ERR_NONFINITE);
   const float lse_n = __shfl_sync(0xffffffffu, lse_t, n & 31);
   const int x_prev = __shfl_sync(0xffffffffu, xraw, (n + 31) & 31);   // x_n (lane n - 1)
   if (lane == 0) {

@@ -109,13 +109,14 @@ def check_verify(h, x, ell, n_gpu, tok_gpu, seed, rnd, reqs=None):
     return stats
 
 
-def run_round(inp, w, rnd=0, mode=None, khist=None, early_stats=False, all_row_stats=False):
+def run_round(inp, w, rnd=0, mode=None, khist=None, early_stats=False, all_row_stats=False, chain_stats=False,
+              T=None, ws=None):
     mode = w.mode if mode is None else mode
     if mode == wl.MODE_TOPK and khist is None:
         khist = torch.zeros(2, dtype=torch.int32, device=inp["U"].device)
-    out = ds.round(inp["U"], inp["T"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], seed=w.seed,
-                   rnd=rnd, sps=inp["sps"], mode=mode, khist=khist, early_stats=early_stats,
-                   all_row_stats=all_row_stats)
+    out = ds.round(inp["U"], inp["T"] if T is None else T, inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"],
+                   seed=w.seed, rnd=rnd, sps=inp["sps"], mode=mode, khist=khist, early_stats=early_stats,
+                   all_row_stats=all_row_stats, chain_stats=chain_stats, ws=ws)
     torch.cuda.synchronize()
     return out
 

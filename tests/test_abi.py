@@ -204,15 +204,23 @@ def test_row_statistics_flags(lib):
     p = _fake()
     ws = _fake(0x100000)
     big = 1 << 30
-    # statistics taken by the draft and a full row pass by verification
-    # exclude one another, in verify_ex and in round_ex; an unknown bit is
-    # refused
+    # statistics taken by the draft (of every row or along the accept
+    # chains) and a full row pass by verification exclude one another, in
+    # verify_ex and in round_ex; an unknown bit is refused; verify_ex takes
+    # the draft's chain statistics as early ones, not by the chain flag
     both = ds.EARLY_TARGET_STATS | ds.ALL_ROW_STATS
-    for flags in (both, 64):
+    for flags in (both, 128, ds.CHAIN_TARGET_STATS):
         assert lib.dspark_verify_ex(p, p, p, p, 1, p, p, p, p, p, 2, 4, 1024, 256, 0, 0, None, flags, p, p, ws, big,
                                     None) == ds.ERR_INVALID
+    for flags in (both, 128, ds.CHAIN_TARGET_STATS | ds.EARLY_TARGET_STATS,
+                  ds.CHAIN_TARGET_STATS | ds.ALL_ROW_STATS):
         assert lib.dspark_round_ex(p, p, p, p, 1, p, 1, p, None, p, 2, 4, 1024, 256, 64, p, 11, 1, None, 0, 0, None,
                                    flags, p, p, p, p, p, p, p, p, p, ws, big, None) == ds.ERR_INVALID
+    # draft_schedule_ex: the chain flag needs T_early; other bits are refused
+    for t_early, flags in ((None, ds.CHAIN_TARGET_STATS), (p, ds.EARLY_TARGET_STATS), (p, 128)):
+        assert lib.dspark_draft_schedule_ex(p, t_early, p, p, 1, p, 1, p, None, p, 2, 4, 1024, 256, 64, p, 11, 1,
+                                            None, 0, 0, None, flags, p, p, p, p, p, p, p, ws, big,
+                                            None) == ds.ERR_INVALID
 
 
 def test_acceptance_label_and_sts_argument_errors(lib):

@@ -38,6 +38,8 @@ def test_target_rows_per_form():
     B, G, ell_sum, n_acc, n_full = 3, 4, 12, 5, 1
     # along the accept chains: rows 0..n_r of each request (2 + 5 + 1)
     assert bench.t_rows("chain", B, G, ell_sum, n_acc, n_full) == 8
+    # the draft took the rows the accept chains reach: the same rows
+    assert bench.t_rows("lazy", B, G, ell_sum, n_acc, n_full) == 8
     # the draft took every row j < gamma; plus the bonus row
     assert bench.t_rows("early", B, G, ell_sum, n_acc, n_full) == 13
     # verification's pass over every row j < l_r; plus the bonus row
@@ -63,13 +65,20 @@ def test_draft_bytes_match_the_profile():
     sd = bench.stage_bytes_per_launch(w, early=True)
     assert sd - fd == 2 * 128 * 16 * 2560 + 4 * (2560 + 256) + 4 * 128 * 16 + 4 * 128
     assert bench.stage_bytes_per_launch(w, early=False) == sd - 4 * 128 * 16 * 151936
+    # the rows the accept chains reach, taken along instead: those rows once
+    assert bench.stage_bytes_per_launch(w, rows=517) - bench.stage_bytes_per_launch(w, early=False) == 517 * 4 * w.V
     recs = bench.profile_records(bench.DRAFT_PROFILE)
-    assert {r["early_target_stats"] for r in recs} == {True, False}
+    assert {(r["early_target_stats"], bool(r.get("chain_target_stats"))) for r in recs} == \
+        {(True, False), (False, False), (True, True)}
     for rec in recs:
         assert rec["workload"] == "batch128"
-        alg = bench.stage_bytes_per_launch(w, rec["early_target_stats"])
+        if rec.get("chain_target_stats"):
+            alg = bench.stage_bytes_per_launch(w, rows=rec["chain_rows"])
+        else:
+            alg = bench.stage_bytes_per_launch(w, rec["early_target_stats"])
         assert int(rec["algorithmic_bytes_per_launch"]) == alg
-        # the profile's DRAM traffic is within a few per cent of the algorithmic bytes
+        # the profile's DRAM traffic is within a few per cent of the algorithmic
+        # bytes (the chains' draft also reads a few rows ahead of their tests)
         assert 1.0 <= int(rec["dram_bytes_per_launch"]) / alg < 1.05
 
 
@@ -83,6 +92,7 @@ def test_kernels_per_round():
     b = wl.WORKLOADS["batch128"]
     assert bench.kernels_per_round(b) == 4
     assert bench.kernels_per_round(b, "early") == 4
+    assert bench.kernels_per_round(b, "lazy") == 4
     assert bench.kernels_per_round(b, "all") == 6
     t = wl.WORKLOADS["tiny"]
     assert bench.kernels_per_round(t) == 2 * t.gamma + 6

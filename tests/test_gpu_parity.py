@@ -183,6 +183,71 @@ def test_chain_verification_reads_no_row_past_a_rejection():
     assert ds.read_status(ws) == ds.ERR_NONFINITE
 
 
+CHAIN_STATS = [
+    # (B, gamma, V): replicated 64- and 32-row tiles, two 128-row tiles,
+    # one and several statistics segments per row with a ragged last one,
+    # gamma = 16
+    (40, 5, 5000),
+    (24, 6, 40000),
+    (130, 8, 9000),
+    (128, 16, 33000),
+]
+
+
+@pytest.mark.parametrize("B,G,V", CHAIN_STATS)
+def test_chain_statistics_round_equals_the_early_round(B, G, V):
+    # the draft takes the statistics only of the rows the accept tests can
+    # reach (it runs those tests itself as their inputs come out and skips a
+    # row once its request is certain to stop before it); the rows it takes
+    # get the same partials as when it takes every row j < gamma, so the
+    # round's results are the early round's bit for bit
+    w = wl.custom(B=B, gamma=G, V=V, r=256, H=64, wdtype=torch.bfloat16, mode=wl.MODE_GREEDY, seed=B + 7 * G,
+                  u_sigma=2.5, t_sigma=(0.4, 1.5), sps_b0=float(4 * B), sps_kind="steps", w_sigma=0.05)
+    inp = wl.make_inputs(w, 0, DEV)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    early = run_round(inp, w, early_stats=True, ws=ws)
+    assert ds.read_status(ws) == ds.OK
+    # another round on the same workspace first, so that every partial the
+    # round under test reads too early would be a different round's
+    run_round(inp, w, rnd=3, chain_stats=True, ws=ws)
+    lazy = run_round(inp, w, chain_stats=True, ws=ws)
+    assert ds.read_status(ws) == ds.OK
+    for name in ("x", "p", "lse", "c", "ell", "n", "tok"):
+        assert torch.equal(lazy.as_dict()[name], early.as_dict()[name]), name
+    n, ell = lazy.n.cpu().numpy(), lazy.ell.cpu().numpy()
+    assert (n < ell).any() and (n == ell).any()   # rejections and whole accepts
+
+
+def test_chain_statistics_round_skips_rows_past_a_rejection():
+    # every target row past each request's rejected position is set to +inf.
+    # The draft that takes the chains' rows reads few of them (any it reads
+    # ahead of a decision are not used) and verification checks only the rows
+    # its tests use, so the round returns the same results with no error; the
+    # draft that takes every row reports the non-finite logits; the label call
+    # refuses the chains' statistics, which do not cover every row
+    w = wl.custom(B=48, gamma=6, V=6000, r=256, H=64, wdtype=torch.bfloat16, mode=wl.MODE_FIXED, seed=29,
+                  u_sigma=2.5, t_sigma=(0.4, 1.5), sps_b0=None)
+    inp = wl.make_inputs(w, 0, DEV)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    ref = run_round(inp, w, chain_stats=True, ws=ws)
+    assert ds.read_status(ws) == ds.OK
+    n_host = ref.n.cpu().numpy()
+    assert (n_host < w.gamma - 1).sum() >= w.B // 4   # most requests leave rows unread
+    T = inp["T"].clone()
+    for b in range(w.B):
+        if n_host[b] < w.gamma:
+            T[b, n_host[b] + 1:w.gamma] = float("inf")
+    lazy = run_round(inp, w, chain_stats=True, T=T, ws=ws)
+    assert ds.read_status(ws) == ds.OK
+    for name in ("x", "p", "lse", "c", "ell", "n", "tok"):
+        assert torch.equal(lazy.as_dict()[name], ref.as_dict()[name]), name
+    ds.acceptance_label(T, inp["U"], inp["W1"], inp["W2"], inp["anchor"], lazy.x, lazy.lse, lazy.ell, ws=ws,
+                        stats="early")
+    assert ds.read_status(ws) == ds.ERR_INVALID
+    run_round(inp, w, early_stats=True, T=T, ws=ws)
+    assert ds.read_status(ws) == ds.ERR_NONFINITE
+
+
 def test_bad_anchor_and_nonfinite_logits_set_status():
     w = wl.custom(B=2, gamma=2, V=1024, r=16, H=8, seed=1)
     inp = wl.make_inputs(w, 0, DEV)
