@@ -873,9 +873,20 @@ __device__ __forceinline__ void stats_tasks(const StepParams* __restrict__ p, co
       seg = (int)t - ri * nsegs;
       const int j = ri / B, b = ri - j * B;
       rowid = (size_t)b * (G + 1) + j;
-      if (j > 0 && !chain_row_needed(p, key, b, j, lane)) {
-        t = __shfl_sync(0xffffffffu, t_next, 0);
-        continue;
+      if (j > 0) {
+        // the request's known outcome first, here in the loop's own code; the
+        // out-of-line tests only when a position must be tested
+        int known = 0;   // 1: needed, -1: not needed, 0: test
+        if (lane == 0) {
+          const int rej = *reinterpret_cast<volatile int*>(p->chain_rej + b);
+          const int pass = *reinterpret_cast<volatile int*>(p->chain_pass + b);
+          known = (rej != 0 && rej <= j) ? -1 : (pass >= j ? 1 : 0);
+        }
+        known = __shfl_sync(0xffffffffu, known, 0);
+        if (known < 0 || (known == 0 && !chain_row_needed(p, key, b, j, lane))) {
+          t = __shfl_sync(0xffffffffu, t_next, 0);
+          continue;
+        }
       }
     } else {
       stats_task_at((int)t, G, nsegs, rowid, seg);
