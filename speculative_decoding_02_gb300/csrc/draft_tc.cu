@@ -1612,12 +1612,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // W2 [V, 256] bf16 viewed as a 2-D tensor (K innermost) with 64 x 64 boxes,
 // 128-byte swizzled: one box is one K atom of a 64-column vocabulary tile.
-cudaError_t make_w2_tensor_map(const void* W2, int V, CUtensorMap* map) {
+cudaError_t make_w2_tensor_map(const void* W2, int V, CUtensorMap* map, int rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
+  if (rows <= 0 || rows > 256) return cudaErrorInvalidValue;
   cuuint64_t dims[2] = {(cuuint64_t)KR, (cuuint64_t)V};
   cuuint64_t strides[1] = {(cuuint64_t)KR * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kAccCols};
+  cuuint32_t box[2] = {64, (cuuint32_t)rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

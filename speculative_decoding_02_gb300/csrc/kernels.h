@@ -151,12 +151,12 @@ bool draft_tc_supported(int wdtype, int r, int V);
 cudaError_t launch_selftest_wait(int mode, void* ws, cudaStream_t stream);
 cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream);
 
-// Tensor maps of the tensor-core kernels: W2 [V, 256] bf16 in 64 x 192 boxes
-// (128-byte swizzle); a [B, G, V] fp32 tensor in [R rows x 1 x 32 columns]
+// Tensor maps of the tensor-core kernels: W2 [V, 256] bf16 in 64 x `rows` boxes
+// (128-byte swizzle, rows <= 256); a [B, G, V] fp32 tensor in [R rows x 1 x 32 columns]
 // boxes (128-byte swizzle); the same tensor as [B, G, V / 32, 32] in boxes of
 // R rows x 64 columns (make_u_tile_map, 128-byte swizzle, V >= 32), which land
 // in shared memory as [row][half][32 columns].
-cudaError_t make_w2_tensor_map(const void* W2, int V, CUtensorMap* map);
+cudaError_t make_w2_tensor_map(const void* W2, int V, CUtensorMap* map, int rows = 192);
 cudaError_t make_u_tensor_map(const float* U, int B, int G, int V, int R, CUtensorMap* map);
 cudaError_t make_u_tile_map(const float* U, int B, int G, int V, int R, CUtensorMap* map);
 cudaError_t launch_residual_tc(const float* T, const float* U, const void* W1, const void* W2,

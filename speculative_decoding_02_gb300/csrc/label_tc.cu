@@ -16,15 +16,22 @@
 //               stages; it runs ahead across positions.  With V % 32 != 0 the
 //               vocabulary's last tile comes as two [R x 32] boxes per tensor.
 //   warp 1      TMEM allocation and the single-thread MMA issuer: the bias
-//               E * W2_rows^T of up to three tiles per tcgen05.mma (fp32 in
-//               TMEM), E = W1[x_{k-1}] in TMEM columns 384-511.
+//               E * W2_rows^T of up to two tiles per tcgen05.mma (fp32 in
+//               TMEM columns 0-255, two accumulators), E = W1[x_{k-1}] in
+//               TMEM columns 256-383 or 384-511 by the parity of k, so that
+//               the E of position k + 2 is gathered while position k + 1's
+//               MMAs run and the issuer never waits for a gather at a
+//               position boundary.
 //   warps 2-17  epilogue (thread = request row, 16 columns per tile):
 //               p_d = exp(acc + U - lse_d), p_t = exp(T - lse_t), sum of
 //               min(p_d, p_t) over the row's columns; at a position's end the
 //               parts of a row are added and each CTA adds its share into
-//               label[b][k-1] (one atomicAdd per CTA and row).  E for the next
-//               position is gathered once the position's last accumulator is
-//               read (its MMAs are then complete).
+//               label[b][k-1] (one atomicAdd per CTA and row).  When a
+//               position's last accumulator is read (its MMAs are then
+//               complete) the epilogue gathers E of position k + 2 into the
+//               buffer position k used; the loads of position k + 1's lse_d and
+//               target-row partials go out first, so that their latency
+//               overlaps the row sums' barriers.
 //
 // lse_d comes from the draft; lse_t from target-row partials already in the
 // workspace, so that each U and T row is read once.  Rows of positions past a
@@ -45,8 +52,8 @@ using namespace tc;
 
 constexpr int LBM = 128;                 // requests per M tile (TMEM lanes)
 constexpr int LBN = 64;                  // vocabulary columns per tile
-constexpr int LGroup = 3;                // tiles per MMA: N = 64 x (up to 3)
-constexpr int LAccCols = LGroup * LBN;   // 192 TMEM columns per accumulator
+constexpr int LGroup = 2;                // tiles per MMA: N = 64 x (up to 2)
+constexpr int LAccCols = LGroup * LBN;   // 128 TMEM columns per accumulator (and per E buffer)
 constexpr int LKR = 256;                 // Markov rank
 constexpr int LAtoms = LKR / 64;         // 64-wide K atoms
 constexpr int LWStages = 3;              // W2 atom ring
@@ -55,8 +62,8 @@ constexpr int LUBox = 32;                // fp32 columns per box (128 bytes, swi
 constexpr int LEpiWarps = 16;
 constexpr int LThreads = 64 + 32 * LEpiWarps;
 constexpr uint32_t LTmemCols = 512;
-constexpr uint32_t LTmemE = 2 * LAccCols;
-constexpr int LWStageBytes = LAccCols * 128;       // 24576
+constexpr uint32_t LTmemE = 2 * LAccCols;          // E of odd positions at LTmemE + 128, of even at LTmemE
+constexpr int LWStageBytes = LAccCols * 128;       // 16384
 constexpr int LUTStageBytes = 2 * LBN * LBM * 4;   // U then T: 65536
 constexpr int LBarBytes = 512;
 constexpr int LXBytes = 4 * LBM * 4;               // the parts' sums of a position
@@ -67,7 +74,7 @@ struct __align__(8) LBars {
   uint64_t full_w[LWStages], empty_w[LWStages];
   uint64_t full_ut[LUTStages], empty_ut[LUTStages];
   uint64_t acc_full[2], acc_empty[2];
-  uint64_t e_full, drain;
+  uint64_t e_full[2], drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -140,7 +147,7 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
     for (int s = 0; s < LWStages; ++s) { mbar_init(&bars->full_w[s], 1); mbar_init(&bars->empty_w[s], 1); }
     for (int s = 0; s < LUTStages; ++s) { mbar_init(&bars->full_ut[s], 1); mbar_init(&bars->empty_ut[s], LEpiWarps); }
     for (int s = 0; s < 2; ++s) { mbar_init(&bars->acc_full[s], 1); mbar_init(&bars->acc_empty[s], LEpiWarps); }
-    mbar_init(&bars->e_full, LEpiWarps);
+    for (int s = 0; s < 2; ++s) mbar_init(&bars->e_full[s], LEpiWarps);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -214,7 +221,9 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
       uint32_t wcount = 0, gcount = 0;
       bool ok = true;
       for (int k = 1; k <= p.G && ok; ++k) {
-        ok = mbar_wait(&bars->e_full, (uint32_t)(k - 1) & 1, abort, p.status);
+        // E of position k: buffer k & 1, its ((k - 1) / 2)-th gather
+        const int eb = k & 1;
+        ok = mbar_wait(&bars->e_full[eb], (uint32_t)((k - 1) >> 1) & 1, abort, p.status);
         tc_fence_after();
         for (int g = 0; g < ntl && ok; g += l_group_tiles(g), ++gcount) {
           const int acc = gcount & 1;
@@ -231,8 +240,8 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
             const uint64_t bd0 = sw128_kmajor_desc(smem_u32(W_s + s * LWStageBytes));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_tmem_a(d_tmem, tmem + LTmemE + a * 32 + kk * 8, bd0 + (uint64_t)(kk * 2), idesc,
-                               (a | kk) != 0);
+              umma_bf16_tmem_a(d_tmem, tmem + LTmemE + eb * LAccCols + a * 32 + kk * 8, bd0 + (uint64_t)(kk * 2),
+                               idesc, (a | kk) != 0);
             umma_commit(&bars->empty_w[s]);
           }
           if (ok) umma_commit(&bars->acc_full[acc]);
@@ -252,26 +261,28 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
     const int b = m0 + r;
     uint32_t it = 0, gcount = 0;
     bool ok = true;
-    for (int k = 1; k <= p.G && ok; ++k) {
-      const bool in_batch = r < rows_valid;
-      const bool active = in_batch && k <= min(max(p.ell[b], 0), p.G);
-      int prev = 0;
-      if (active) prev = checked_token(k == 1 ? p.anchor[b] : p.x[(size_t)b * p.G + k - 2], p.V, p.status);
-      // this position's E (the MMAs of the previous position are complete:
-      // its last accumulator has been read)
-      l_gather_e(p.W1, prev, active, h, tmem + ((uint32_t)(q * 32) << 16) + LTmemE + h * 32);
+    // positions 1..ellb of this row are labelled
+    const int ellb = r < rows_valid ? min(max(p.ell[b], 0), p.G) : 0;
+    const uint32_t e_lanes = tmem + ((uint32_t)(q * 32) << 16) + LTmemE + h * 32;
+    // E of positions 1 and 2 (buffers 1 and 0)
+    for (int k = 1; k <= min(2, p.G); ++k) {
+      const bool act = k <= ellb;
+      const int prev = act ? checked_token(k == 1 ? p.anchor[b] : p.x[(size_t)b * p.G + k - 2], p.V, p.status) : 0;
+      l_gather_e(p.W1, prev, act, h, e_lanes + (uint32_t)((k & 1) * LAccCols));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->e_full);
-
-      float ld2 = 0.f, lt2 = 0.f;
-      if (active) {
-        ld2 = p.lse_d[(size_t)b * p.G + k - 1] * kL2e;
-        const float2* rp = p.row_part + ((size_t)b * (p.G + 1) + k - 1) * p.nsegs;
-        float mt = -INFINITY, st = 0.f;
-        merge_partials(rp, p.nsegs, mt, st);
-        lt2 = (mt + logf(st)) * kL2e;
-      }
+      if (lane == 0) mbar_arrive(&bars->e_full[k & 1]);
+    }
+    // lse_d and lse_t of position 1, in base 2
+    float ld2 = 0.f, lt2 = 0.f;
+    if (1 <= ellb) {
+      ld2 = p.lse_d[(size_t)b * p.G] * kL2e;
+      float mt = -INFINITY, st = 0.f;
+      merge_partials(p.row_part + (size_t)b * (p.G + 1) * p.nsegs, p.nsegs, mt, st);
+      lt2 = (mt + logf(st)) * kL2e;
+    }
+    for (int k = 1; k <= p.G && ok; ++k) {
+      const bool active = k <= ellb;
       float lacc = 0.f;
       for (int i = 0; i < ntl; ++i, ++it) {
         const int sub = i == 0 ? 0 : (i - 1) % LGroup;
@@ -328,9 +339,34 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->empty_ut[su]);
       }
+      // What position k + 1 needs goes out first: its lse_d, the first
+      // eight partials of its target row and the token whose W1 row is E of
+      // position k + 2; their latency overlaps the row sums below.
+      const bool act1 = k + 1 <= ellb, act2 = k + 2 <= ellb;
+      float ldn = 0.f;
+      float2 pq[8];
+      const float2* rpn = p.row_part + ((size_t)b * (p.G + 1) + k) * p.nsegs;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pq[j] = make_float2(-INFINITY, 0.f);
+      if (act1) {
+        ldn = p.lse_d[(size_t)b * p.G + k];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < p.nsegs) pq[j] = __ldcg(rpn + j);
+      }
+      const int tok2 = act2 ? p.x[(size_t)b * p.G + k] : 0;
       // the parts of each row, then one atomicAdd per CTA and row
       xs[part * R + r] = lacc;
       named_bar_sync(1, LEpiWarps * 32);
+      if (ok && k + 2 <= p.G) {
+        // E of position k + 2 into the buffer position k used: every MMA of
+        // position k is complete, its last accumulator having been read
+        l_gather_e(p.W1, act2 ? checked_token(tok2, p.V, p.status) : 0, act2, h,
+                   e_lanes + (uint32_t)((k & 1) * LAccCols));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->e_full[k & 1]);
+      }
       if (part == 0 && active && ok) {
         float S = 0.f;
 #pragma unroll
@@ -339,6 +375,16 @@ label_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUt
       }
       named_bar_sync(1, LEpiWarps * 32);
       if (*abort) ok = false;
+      // lse_d and lse_t of position k + 1, in base 2
+      ld2 = lt2 = 0.f;
+      if (act1) {
+        ld2 = ldn * kL2e;
+        float mt = -INFINITY, st = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) softmax_merge(mt, st, pq[j].x, pq[j].y);
+        if (p.nsegs > 8) merge_partials(rpn + 8, p.nsegs - 8, mt, st);
+        lt2 = (mt + logf(st)) * kL2e;
+      }
     }
   }
 
@@ -363,7 +409,7 @@ cudaError_t launch_acceptance_label_tc(const float* T, const float* U, const voi
                                        const int* stats_done, const int* full_rows, float* label, int B, int G,
                                        int V, int* status, cudaStream_t stream) {
   CUtensorMap wmap, umap, tmap, u4map, t4map;
-  cudaError_t e = make_w2_tensor_map(W2, V, &wmap);
+  cudaError_t e = make_w2_tensor_map(W2, V, &wmap, LAccCols);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
