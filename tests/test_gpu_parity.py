@@ -508,6 +508,26 @@ def test_gpu_sampling_law_chi_square_tensor_cores():
 FULL = ["qwen3_4b", "batch128", "large_vocab", "serving512"]
 
 
+@pytest.mark.parametrize("name", ["batch128", "serving512"])
+def test_full_size_chain_statistics_round(name):
+    # the benchmark's headline form at full size: the draft taking the rows
+    # the accept chains reach gives the early round's results bit for bit
+    # (after a different round on the same workspace), which the test below
+    # holds against the oracle on sampled requests
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, 0, DEV)
+    ws = ds.workspace(w.B, w.gamma, w.V, DEV)
+    early = run_round(inp, w, early_stats=True, ws=ws)
+    assert ds.read_status(ws) == ds.OK
+    run_round(inp, w, rnd=5, chain_stats=True, ws=ws)
+    lazy = run_round(inp, w, chain_stats=True, ws=ws)
+    assert ds.read_status(ws) == ds.OK
+    for name_ in ("x", "p", "lse", "c", "ell", "n", "tok"):
+        assert torch.equal(lazy.as_dict()[name_], early.as_dict()[name_]), name_
+    del inp, ws
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workload_sampled(name):
     # the round as the benchmark runs it: the draft takes the target rows'
