@@ -725,9 +725,9 @@ __device__ __forceinline__ void chain_merge(float& m, float& s, float m2, float 
 // softmax partial of m, which a CTA writes after its arrival at the grid
 // barrier of m and before its next arrival -- at the barrier of m + 1, or
 // the finalize's after the last position; lse_t of row m-1 needs every
-// segment of that row), -2 when the
-// test cannot be run (a non-finite ratio or a bad token: verification sees
-// to it), 1 when the test fails with a margin of 2^-8 relative, 0 otherwise.
+// segment of that row), -2 when the test cannot be run (a non-finite ratio
+// or a bad token: verification sees to it), 1 when the test fails with a
+// margin of 2^-8 relative, 0 otherwise.
 // p_d comes from the draft's partials and the fused logit of x_m as the
 // finalize forms them, p_t from the row's partials as verify_decide merges
 // them; the margin covers the rounding of the two and of the special-function
