@@ -814,9 +814,11 @@ __device__ __forceinline__ int chain_test(const StepParams* __restrict__ p, cons
 // run, counts as reachable: the row is taken ahead of its decision (waiting
 // for the draft's barriers instead left the rows of the long chains for
 // after the draft), so a row is skipped only once verification is certain to
-// stop before it.  Out of line and small, as chain_merge.  Warp-uniform.
-__device__ __noinline__ bool chain_row_needed(const StepParams* __restrict__ p, const RngKey key, int b, int j,
-                                              int lane) {
+// stop before it.  Inline: an out-of-line call here cost the draft ~10 us per
+// launch in every form, lazy or not (the calling convention's hold on the
+// kernel's registers).  Warp-uniform.
+__device__ __forceinline__ bool chain_row_needed(const StepParams* __restrict__ p, const RngKey& key, int b, int j,
+                                                 int lane) {
 #pragma unroll 1
   for (int guard = 0; guard <= j; ++guard) {
     int rej = 0, pass = 0;
