@@ -327,8 +327,8 @@ __host__ __device__ inline T* ws_ptr(void* ws, size_t off) {
 // the maximum and then the two-level race of blocks of 4 with weights
 // exp(T - max), as verify_residual_finalize draws it with a whole CTA.
 // Returns the token on every lane, -1 if no block had weight.
-static __device__ __noinline__ int warp_softmax_draw(const float* __restrict__ Trow, int V, uint32_t b, uint32_t ks,
-                                                     const RngKey& key, int lane) {
+static __device__ __forceinline__ int warp_softmax_draw(const float* __restrict__ Trow, int V, uint32_t b, uint32_t ks,
+                                                        const RngKey& key, int lane) {
   float mx = -INFINITY;
   for (int v = 4 * lane; v < V; v += 128) {
     const float4 t4 = *reinterpret_cast<const float4*>(Trow + v);
