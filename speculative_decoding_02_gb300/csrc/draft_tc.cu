@@ -851,6 +851,7 @@ __device__ __forceinline__ bool chain_row_needed(const StepParams* __restrict__ 
 // skipped, each finished segment is counted in rows_done, and non-finite
 // entries are left to verification, which checks the rows its tests use (a
 // row read here ahead of its request's rejection is not one of them).
+template <bool kChain>
 __device__ __forceinline__ void stats_tasks(const StepParams* __restrict__ p, const RngKey& key,
                                             volatile int* abort) {
   const float* __restrict__ T = p->T_stats;
@@ -859,7 +860,11 @@ __device__ __forceinline__ void stats_tasks(const StepParams* __restrict__ p, co
   unsigned int* next = p->stats_next;
   const int lane = threadIdx.x & 31;
   const int ntasks = B * G * nsegs;
-  const bool chain = p->chain_rej != nullptr;
+  // kChain false: the chain code is compiled out (its mere presence in the
+  // loop cost the drafts that take every row, or none, ~5 us per launch);
+  // kChain true keeps both paths behind the run-time test, which measured
+  // ~6 us faster for the chains' draft than a loop with the chain path alone
+  const bool chain = kChain && p->chain_rej != nullptr;
   const uint64_t pol = policy_evict_first();
   bool bad = false;
   unsigned int t = 0;
@@ -991,7 +996,7 @@ __device__ __forceinline__ void finalize_item(int item, int lane, const float* _
 // MODE kResidual: for every request that rejected at position k*, the fused
 // draft logits of k* again, raced over log max(0, p_t - p_d) (U and T rows
 // read directly by the epilogue threads).
-template <int R, int MODE>
+template <int R, int MODE, bool kChain = false>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1)
 draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant__ CUtensorMap u_map,
               const __grid_constant__ StepParams p) {
@@ -1565,14 +1570,14 @@ draft_step_tc(const __grid_constant__ CUtensorMap w2_map, const __grid_constant_
       // the draft is done: the epilogue warps help with whatever target-row
       // statistics are left
       if (p.T_stats != nullptr)
-        stats_tasks(&p, key, abort);
+        stats_tasks<kChain>(&p, key, abort);
     }
   } else {
     // ------------------------------------------------------------ statistics
     // (draft mode only: the warps past the epilogue).  Their loads bypass the
     // SM's bulk-copy engine, which the draft's U and W2 tiles keep busy.
     if (p.T_stats != nullptr)
-      stats_tasks(&p, key, abort);
+      stats_tasks<kChain>(&p, key, abort);
   }
 
   tc_fence_before();
@@ -1724,8 +1729,14 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
   CUtensorMap umap;
   if ((e = make_u_tensor_map(a.U, a.B, a.gamma, a.V, R, &umap)) != cudaSuccess) return e;
   auto kern = R == 32 ? draft_step_tc<32, kDraft> : (R == 64 ? draft_step_tc<64, kDraft> : draft_step_tc<BM, kDraft>);
+  // the persistent launch taking the chains' target rows runs a kernel of its own
+  auto kern_chain = R == 32 ? draft_step_tc<32, kDraft, true>
+                            : (R == 64 ? draft_step_tc<64, kDraft, true> : draft_step_tc<BM, kDraft, true>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  if (a.T_stats != nullptr && a.chain_stats &&
+      (e = cudaFuncSetAttribute(kern_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) != cudaSuccess)
+    return e;
   e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * kKeyStride * (size_t)a.gamma * a.B, stream);
   if (e != cudaSuccess) return e;
   // the target-statistics task counter, the count of CTAs past the
@@ -1815,7 +1826,8 @@ cudaError_t launch_markov_draft_tc(const DraftArgs& a, cudaStream_t stream) {
     sp.x_out = a.x_out;
     sp.p_out = a.p_out;
     sp.lse_out = a.lse_out;
-    if ((e = cudaLaunchKernelEx(&cfg, kern, map, umap, sp)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&cfg, sp.chain_rej != nullptr ? kern_chain : kern, map, umap, sp)) != cudaSuccess)
+      return e;
   } else {
     for (int k = 1; k <= a.gamma; ++k) {
       sp.k_first = sp.k_last = k;
